@@ -1,0 +1,155 @@
+"""The five synthetic workloads: shapes, value distributions and structure.
+
+  tiny             B=2, H=4, L=256, int4, K/V/q ~ N(0,1), contiguous cache,
+                   quantize then one decode step (append 1 token, attend over 257)
+  llama2-7b-layer  B=8, H=32, L=8192, int4, K/V ~ N(0,1) with 4 channels per
+                   head (separately for K and V, the same for every token and
+                   sequence) scaled x10, contiguous cache; decode
+  long-context     B=16, H=32, L=32768, int4, each (head, channel) an outlier
+                   x10 with probability 0.01, contiguous cache; decode
+  paged-int8       64 sequences, L uniform in [512, 16384], H=32, int8 with a
+                   per-(page, head) scale, 64-token pages in a randomly
+                   permuted block table; decode
+  prefill-append   262144 new tokens as 64 sequences x 4096, H=32, K/V ~
+                   N(0, 1.5^2), int4, randomly permuted pages; append/quantize
+
+D = 128 and 64-token blocks throughout.  q ~ N(0, 1).  All values are fp16.
+"""
+import numpy as np
+
+from . import (BLOCK_TABLE, K_HIST, K_OUTLIER, LENGTHS, QUERY, V_HIST, V_OUTLIER, fill_f16_device,
+               fill_f16_host, outliers_bernoulli, outliers_per_head, permutation, stream_id,
+               uniform_int)
+
+INT4 = 0
+INT8 = 1
+PAGE = 64
+
+CONFIGS = {
+    1: dict(name="tiny", B=2, H=4, D=128, L=256, fmt=INT4, sigma=1.0, outliers=None, table="contiguous"),
+    2: dict(name="llama2-7b-layer", B=8, H=32, D=128, L=8192, fmt=INT4, sigma=1.0,
+            outliers=("per_head", 4, 10.0), table="contiguous"),
+    3: dict(name="long-context", B=16, H=32, D=128, L=32768, fmt=INT4, sigma=1.0,
+            outliers=("bernoulli", 0.01, 10.0), table="contiguous"),
+    4: dict(name="paged-int8", B=64, H=32, D=128, L=("uniform", 512, 16384), fmt=INT8, sigma=1.0,
+            outliers=None, table="permuted"),
+    5: dict(name="prefill-append", B=64, H=32, D=128, L=4096, fmt=INT4, sigma=1.5, outliers=None,
+            table="permuted"),
+}
+
+
+class Workload:
+    """One seeded instance of a workload.
+
+    lens[b]      tokens already in the cache for sequence b (the decode history,
+                 or for prefill-append the tokens to append)
+    extra_tokens room reserved per sequence beyond lens (decode steps)
+    block_table  int32 [B][max_blocks]; num_pages = B * max_blocks
+    """
+
+    def __init__(self, B, H, D, lens, fmt, sigma=1.0, outliers=None, table="contiguous", seed=0,
+                 extra_tokens=0, name="custom"):
+        self.name = name
+        self.B, self.H, self.D = int(B), int(H), int(D)
+        self.lens = np.asarray(lens, dtype=np.int32).reshape(self.B)
+        self.fmt = int(fmt)
+        self.sigma = float(sigma)
+        self.seed = int(seed)
+        self.extra_tokens = int(extra_tokens)
+        cap = int(self.lens.max(initial=0)) + self.extra_tokens
+        self.max_blocks = max(1, (cap + PAGE - 1) // PAGE)
+        self.num_pages = self.B * self.max_blocks
+        if table == "contiguous":
+            self.block_table = np.arange(self.num_pages, dtype=np.int32).reshape(self.B, self.max_blocks)
+        elif table == "permuted":
+            self.block_table = permutation(self.num_pages, self.seed,
+                                           stream_id(BLOCK_TABLE)).reshape(self.B, self.max_blocks)
+        else:
+            raise ValueError(table)
+        self.table = table
+        self.outlier_mult = 1.0
+        self.k_mask = self.v_mask = None
+        if outliers is not None:
+            kind, param, mult = outliers
+            self.outlier_mult = float(mult)
+            if kind == "per_head":
+                self.k_mask = outliers_per_head(self.H, self.D, int(param), self.seed, stream_id(K_OUTLIER))
+                self.v_mask = outliers_per_head(self.H, self.D, int(param), self.seed, stream_id(V_OUTLIER))
+            elif kind == "bernoulli":
+                self.k_mask = outliers_bernoulli(self.H, self.D, float(param), self.seed, stream_id(K_OUTLIER))
+                self.v_mask = outliers_bernoulli(self.H, self.D, float(param), self.seed, stream_id(V_OUTLIER))
+            else:
+                raise ValueError(kind)
+        self._dev_masks = {}
+
+    # ---- host (numpy) -------------------------------------------------
+    def kv_host(self, which, b, t0, t1):
+        """fp16 bits [t1-t0][H][D] of the key ('k') or value ('v') history of sequence b."""
+        kind, mask = (K_HIST, self.k_mask) if which == "k" else (V_HIST, self.v_mask)
+        n = (t1 - t0) * self.H * self.D
+        x = fill_f16_host(n, self.seed, stream_id(kind, b), t0 * self.H * self.D, self.sigma, mask,
+                          self.outlier_mult)
+        return x.reshape(t1 - t0, self.H, self.D)
+
+    def q_host(self, step=0):
+        """fp16 bits [B][H][D] of the query of decode step `step`."""
+        n = self.B * self.H * self.D
+        return fill_f16_host(n, self.seed, stream_id(QUERY, step), 0, 1.0).reshape(self.B, self.H, self.D)
+
+    # ---- device (torch) -----------------------------------------------
+    def _mask_dev(self, which, device):
+        import torch
+        key = (which, str(device))
+        mask = self.k_mask if which == "k" else self.v_mask
+        if mask is None:
+            return None
+        if key not in self._dev_masks:
+            self._dev_masks[key] = torch.from_numpy(mask.reshape(-1).copy()).to(device)
+        return self._dev_masks[key]
+
+    def kv_device(self, which, b, t0, t1, out):
+        """Fill out (CUDA, 2-byte elements, (t1-t0)*H*D elements) with the same bits as kv_host."""
+        kind = K_HIST if which == "k" else V_HIST
+        assert out.numel() == (t1 - t0) * self.H * self.D
+        return fill_f16_device(out, self.seed, stream_id(kind, b), t0 * self.H * self.D, self.sigma,
+                               self._mask_dev(which, out.device), self.outlier_mult)
+
+    def q_device(self, out, step=0):
+        assert out.numel() == self.B * self.H * self.D
+        return fill_f16_device(out, self.seed, stream_id(QUERY, step), 0, 1.0)
+
+    # ---- sizes ---------------------------------------------------------
+    @property
+    def row_bytes(self):
+        return self.D // 2 if self.fmt == INT4 else self.D
+
+    def page_bytes(self):
+        return PAGE * self.H * self.row_bytes
+
+    def decode_bytes(self, lens=None):
+        """Algorithmic HBM bytes of one decode-attention call over lengths `lens`:
+        K and V codes of every valid token, one K and one V scale per touched
+        (page, head), the query read and the output written."""
+        lens = self.lens if lens is None else np.asarray(lens)
+        tok = int(lens.sum())
+        pages = int(((lens + PAGE - 1) // PAGE).sum())
+        return (2 * tok * self.H * self.row_bytes + 2 * pages * self.H * 4 +
+                2 * self.B * self.H * self.D * 2)
+
+    def quantize_bytes(self, ntok):
+        """Algorithmic bytes of quantizing ntok tokens of K and V into full blocks:
+        fp16 read, codes written, one scale per (block, head)."""
+        blocks = (ntok + PAGE - 1) // PAGE
+        return 2 * (ntok * self.H * self.D * 2 + ntok * self.H * self.row_bytes + blocks * self.H * 4)
+
+
+def make_workload(cfg, seed=0, extra_tokens=0):
+    c = CONFIGS[cfg]
+    B = c["B"]
+    if isinstance(c["L"], tuple):
+        _, lo, hi = c["L"]
+        lens = uniform_int(B, lo, hi, seed, stream_id(LENGTHS))
+    else:
+        lens = np.full(B, c["L"], dtype=np.int32)
+    return Workload(B, c["H"], c["D"], lens, c["fmt"], c["sigma"], c["outliers"], c["table"], seed,
+                    extra_tokens, c["name"])
