@@ -1,0 +1,410 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized-KV decode step on one GB300 (or N, as replicas).
+
+Workload (llama2-7b-layer): B=8 sequences, H=32 heads, D=128, context 8192,
+int4 64-token blocks, K/V ~ N(0,1) with 4 outlier channels per head x10,
+inputs generated in HBM by the seeded generator.  One step = the whole hot
+path once: append one token per sequence (re-quantizing each open block from
+its fp16 originals: absmax, scale, quantize, pack) and decode attention of the
+step's query over every sequence (split pass + merge pass).  The decode
+position cycles through one 64-token block, so the context stays 8193..8256
+tokens and the working set (~270 MB of codes) stays larger than L2 (129 MB).
+
+value    decode tokens/s = sequences advanced one token through one layer's
+         attention per second, summed over ranks (weak scaling: every rank runs
+         its own batch; no collective on the data path)
+e2e      the same steps through the C ABI with host buffers: each step copies its
+         new K/V rows and query from pinned host memory and its output back
+roofline the split decode kernel's algorithmic bytes / its CUDA-event time
+cpu_baseline / --impl reference: the CPU oracle timed on host cores on a
+         bounded sample of the same step
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CONFIG = 2
+METRIC = "quantized-KV decode attention tokens/s and KV GB/s vs HBM roofline; quantize GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for f in ("kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h"):
+        with open(os.path.join(ROOT, "quantized_kv_cache_09_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """dram bytes per launch of `kernel` from the committed ncu summary, or None
+    when the summary is missing or was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest()
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or "=" not in line:
+                continue
+            kv = dict(p.split("=", 1) for p in line.split())
+            if kv.get("kernel") == kernel and kv.get("source_sha256") == digest:
+                return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.window = (0.0, 0.0)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [p.strip() for p in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        t0, t1 = self.window
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        use = inside if inside else [s for _, s in self.samples]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm = []
+        mx = None
+        for s in use:
+            try:
+                sm.append(float(s[0]))
+                mx = float(s[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, s[3:7]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle on a bounded sample of the same step
+# --------------------------------------------------------------------------
+def oracle_step_rate(seconds, seed, threads=None):
+    """Oracle decode steps of the 7B-layer workload: for each sampled sequence,
+    re-quantize its open block (oracle quantize of the 64-token block holding
+    the new token) and attend over its 8193 tokens, all 32 heads, binary64.
+    Threads run independent sequences (the oracle releases the GIL).
+    Returns (steps per second, threads, description)."""
+    import numpy as np
+
+    from oracle import oracle as orc
+    from quantized_kv_cache_09_gb300.synth import workloads as W
+
+    wl = W.make_workload(CONFIG, seed=seed, extra_tokens=64)
+    threads = threads or max(1, min(16, os.cpu_count() or 1))
+    L = int(wl.lens[0])
+    sm = np.float32(1.0 / math.sqrt(wl.D))
+
+    # untimed setup: the oracle's cache of each sampled sequence's history
+    nseq = min(wl.B, threads)
+    caches = []
+    for b in range(nseq):
+        kc, ks = orc.quantize(wl.fmt, wl.kv_host("k", b, 0, L))
+        vc, vs = orc.quantize(wl.fmt, wl.kv_host("v", b, 0, L))
+        nb = kc.shape[0]
+        kc = np.concatenate([kc, np.zeros_like(kc[:1])])
+        vc = np.concatenate([vc, np.zeros_like(vc[:1])])
+        ks = np.concatenate([ks, np.zeros_like(ks[:1])])
+        vs = np.concatenate([vs, np.zeros_like(vs[:1])])
+        k_new = wl.kv_host("k", b, L, L + 1)
+        v_new = wl.kv_host("v", b, L, L + 1)
+        q = wl.q_host(0)[b:b + 1]
+        caches.append((kc, vc, ks, vs, nb, k_new, v_new, q))
+
+    done = [0] * nseq
+    stop = time.time() + seconds
+
+    def work(i):
+        kc, vc, ks, vs, nb, k_new, v_new, q = caches[i]
+        bt = np.arange(nb + 1, dtype=np.int32)[None, :]
+        while time.time() < stop:
+            # append: the new token opens block nb; re-quantize it
+            c, s = orc.quantize(wl.fmt, k_new)
+            kc[nb], ks[nb] = c[0], s[0]
+            c, s = orc.quantize(wl.fmt, v_new)
+            vc[nb], vs[nb] = c[0], s[0]
+            orc.decode_attention(wl.fmt, kc, vc, ks, vs, bt, np.array([L + 1]), q, sm)
+            done[i] += 1
+
+    t0 = time.time()
+    ths = [threading.Thread(target=work, args=(i,)) for i in range(nseq)]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
+    el = time.time() - t0
+    steps = sum(done)
+    desc = (f"{steps} oracle sequence-steps (append 1 token + binary64 attention over {L + 1} tokens x "
+            f"{wl.H} heads), {nseq} sequences on {nseq} threads for {el:.1f} s")
+    return steps / el, nseq, desc
+
+
+# --------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return
+    rate, cores, desc = oracle_step_rate(args.cpu_seconds, args.seed)
+    line = {"metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 / rate if rate else None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama2-7b-layer", "B": 8, "H": 32, "D": 128, "context": 8192,
+                       "format": "int4-b64", "step": "append 1 token + decode attention"},
+            "impl": "reference",
+            "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from quantized_kv_cache_09_gb300 import kvq
+    from quantized_kv_cache_09_gb300.runner import DecodeStep, DeviceWorkload
+    from quantized_kv_cache_09_gb300.synth import workloads as W
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    seed = args.seed + rank
+    wl = W.make_workload(CONFIG, seed=seed, extra_tokens=64)
+    dw = DeviceWorkload(wl, device=dev)
+    dw.prefill()
+    B, H, D = wl.B, wl.H, wl.D
+    L = int(wl.lens[0])
+    step = DecodeStep(dw)
+
+    # per-step inputs resident in HBM: 64 distinct steps, cycled
+    NS = 64
+    k_steps, v_steps, q_steps = [], [], []
+    for s in range(NS):
+        k1, v1, q = dw.new_token_tensors(s)
+        k_steps.append(k1)
+        v_steps.append(v1)
+        q_steps.append(q)
+    lens_b = [torch.full((B,), L + s, dtype=torch.int32, device=dev) for s in range(NS)]
+    lens_a = [torch.full((B,), L + s + 1, dtype=torch.int32, device=dev) for s in range(NS)]
+    # the step at cycle position s appends position L + s: its history rows 0..s-1
+    # of the open block are the tokens appended by the previous s steps, which the
+    # warm-up establishes; prime the tail with one full cycle
+    stream = torch.cuda.current_stream(dev)
+    for s in range(NS):
+        step.run(lens_b[s], lens_a[s], k_steps[s], v_steps[s], q_steps[s])
+    torch.cuda.synchronize(dev)
+
+    K, Wm = args.steps, args.warmup
+    for i in range(Wm):
+        s = i % NS
+        step.run(lens_b[s], lens_a[s], k_steps[s], v_steps[s], q_steps[s])
+    torch.cuda.synchronize(dev)
+    rc, flags = kvq.kvq_get_device_status(dw.cache)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} flags {flags:#x} after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(K):
+        s = (Wm + i) % NS
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        kvq.kvq_append(dw.cache, k_steps[s], v_steps[s], step.cu, dw.block_table, lens_b[s], 1)
+        e1.record(stream)
+        kvq.kvq_decode_attention(dw.cache, q_steps[s], dw.block_table, lens_a[s], dw.softmax_scale, step.out,
+                                 dw.workspace)
+        e2.record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    t_wall1 = time.time()
+    clocks.window = (t_wall0, t_wall1)
+    total_ms = start.elapsed_time(end)
+    app_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    rc, flags = kvq.kvq_get_device_status(dw.cache)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} flags {flags:#x} after timed steps")
+
+    # ---- end to end through the C ABI with host buffers ----
+    pin_k = [k.cpu().pin_memory() for k in k_steps]
+    pin_v = [v.cpu().pin_memory() for v in v_steps]
+    pin_q = [q.cpu().pin_memory() for q in q_steps]
+    pin_o = torch.empty((B, H, D), dtype=torch.float16).pin_memory()
+    dk = torch.empty_like(k_steps[0])
+    dv = torch.empty_like(v_steps[0])
+    dq = torch.empty_like(q_steps[0])
+    Ke = max(1, K // 2)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e2e_s = torch.cuda.Event(enable_timing=True)
+    e2e_e = torch.cuda.Event(enable_timing=True)
+    e2e_s.record(stream)
+    for i in range(Ke):
+        s = (Wm + K + i) % NS
+        dk.copy_(pin_k[s], non_blocking=True)
+        dv.copy_(pin_v[s], non_blocking=True)
+        dq.copy_(pin_q[s], non_blocking=True)
+        kvq.kvq_append(dw.cache, dk, dv, step.cu, dw.block_table, lens_b[s], 1)
+        kvq.kvq_decode_attention(dw.cache, dq, dw.block_table, lens_a[s], dw.softmax_scale, step.out, dw.workspace)
+        pin_o.copy_(step.out, non_blocking=True)
+    e2e_e.record(stream)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e2e_ms = e2e_s.elapsed_time(e2e_e)
+    clocks.stop()
+
+    # ---- aggregate over ranks (max time) ----
+    def max_over_ranks(x):
+        if not pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    total_ms = max_over_ranks(total_ms)
+    e2e_ms = max_over_ranks(e2e_ms)
+    dec_mean = max_over_ranks(sum(dec_ms) / K)
+    app_mean = max_over_ranks(sum(app_ms) / K)
+
+    # algorithmic bytes (per launch, averaged over the cycle of context lengths)
+    ctx = [L + ((Wm + i) % NS) + 1 for i in range(K)]
+    dec_bytes = sum(wl.decode_bytes(np.full(B, c)) for c in ctx) / K
+    peak, peak_kind = measured_peak()
+    achieved = dec_bytes / (dec_mean * 1e-3) / 1e9
+    traffic = ncu_traffic("decode_split_kernel")
+    ms_step = total_ms / K
+    value = world * B * K / (total_ms * 1e-3)
+    e2e_val = world * B * Ke / (e2e_ms * 1e-3)
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int4 codes, fp32 math", "data": "synthetic (seeded generator in HBM)",
+            "config": {"workload": "llama2-7b-layer", "B": B, "H": H, "D": D, "context": f"{L + 1}..{L + NS}",
+                       "format": "int4-b64", "step": "append 1 token + decode attention",
+                       "parallelism": f"replicas x{world} (sequence-sharded, no collective)",
+                       "l2": "inputs larger than L2 (270 MB of codes vs 129 MB)"},
+            "kv_gb_per_s": dec_bytes / (dec_mean * 1e-3) / 1e9,
+            "decode_us": dec_mean * 1e3, "append_us": app_mean * 1e3,
+            "roofline": {"kernel": "kvq_decode_attention (split + merge launches)", "bound": "hbm",
+                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": dec_bytes},
+            "e2e": {"value": e2e_val, "unit": "tokens/s",
+                    "h2d_bytes_per_step": 3 * B * H * D * 2, "d2h_bytes_per_step": B * H * D * 2},
+            "gpu_launches": 3 * K,
+            "clocks": clocks.summary()}
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, cores, desc = oracle_step_rate(args.cpu_seconds, args.seed)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * kvq.h -- C ABI of the block-quantized KV cache and its decode attention,
+ * built for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The method (three scraped articles on DeepSeek-R1 inference tuning):
+ *   - quantize_block, "DeepSeek-R1 inference latency ... hardware-aware
+ *     scheduling" (jsqmd.com/news/887038), section 2.1: per block of 64
+ *     tokens, scale = max|x| / 7.5 and codes = round(x / scale) clamped to
+ *     [-8, 7];
+ *   - the symmetric per-chunk INT8 variant, "DeepSeek R1 performance
+ *     overview" (aicoding.csdn.net), section 2.2, and decode reading an INT8
+ *     KV cache, same page, section 3.1;
+ *   - KV pages addressed through a block table, "DeepSeek R1 performance
+ *     tips" (ddd.cn), section 4 (vLLM PagedAttention).
+ *
+ * Readings fixed by this library where the pages are silent or inconsistent:
+ *   - a block is (sequence, head, 64 consecutive tokens); the last block of a
+ *     sequence is scaled over its valid rows only and its unused rows hold
+ *     code 0;
+ *   - binary32 arithmetic: scale = a / 7.5f (int4) or a / 127.0f (int8),
+ *     y = x / scale, both correctly rounded; code = clamp(rint(y)) with
+ *     round-half-to-even; clamp [-8, 7] (int4) or [-127, 127] (int8); no
+ *     zero-point; an all-zero block has scale 0 and codes 0;
+ *   - int4 codes are packed: byte j of a row holds element 2j in its low
+ *     nibble and element 2j+1 in its high nibble, 4-bit two's complement;
+ *   - decode attention is softmax(q . k^ * softmax_scale) . v^ with
+ *     k^ = code * scale, one query per (sequence, head); the output of an
+ *     empty sequence is 0.
+ *
+ * Layouts (all little-endian, all pointers device memory unless stated):
+ *   fp16 tensors are IEEE binary16 bit patterns (uint16_t).
+ *   token rows: x[T][H][D], head_dim D = 128 contiguous per (token, head).
+ *   codes of one (page, head): 64 rows of D/2 bytes (int4) or D bytes (int8);
+ *   code arrays: [num_pages][H][64][D/2 or D];  scale arrays: [num_pages][H].
+ *
+ * Ownership: the caller allocates and frees every buffer, workspaces
+ * included; the library allocates no device memory and keeps no state
+ * between calls.  Every call is asynchronous on the caller's stream: argument
+ * checks run on the host first (a rejected call launches nothing); problems
+ * only the device can see (a block-table entry out of range, a length beyond
+ * the table, a wait that timed out) set bits in the cache's device status word
+ * instead of faulting, and kvq_get_device_status() reads them.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* the caller's CUDA stream (a cudaStream_t); NULL is the legacy default stream */
+typedef struct CUstream_st *kvq_stream_t;
+
+typedef enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = 1,     /* null pointer, negative size, misaligned buffer */
+    KVQ_ERR_UNSUPPORTED = 2,     /* head_dim != 128, page_tokens != 64, unknown format */
+    KVQ_ERR_CUDA = 3,            /* a CUDA runtime call or launch failed */
+    KVQ_ERR_BAD_BLOCK_TABLE = 4, /* device: a block-table entry outside [0, num_pages) */
+    KVQ_ERR_TIMEOUT = 5,         /* device: a bounded wait on a copy ran out */
+    KVQ_ERR_WORKSPACE = 6,       /* workspace missing or smaller than kvq_decode_workspace_bytes */
+    KVQ_ERR_BAD_LENGTH = 7       /* device: a length beyond the block table, or new tokens beyond max */
+} kvq_status;
+
+typedef enum kvq_format {
+    KVQ_INT4_B64 = 0,   /* packed int4, scale = absmax / 7.5 per (block, head) */
+    KVQ_INT8_PAGE = 1   /* int8, scale = absmax / 127 per (page, head) */
+} kvq_format;
+
+/* bits of the device status word */
+#define KVQ_FLAG_BAD_PAGE 0x1    /* a block-table entry was out of range (that page was not touched) */
+#define KVQ_FLAG_BAD_LENGTH 0x2  /* a sequence length exceeded max_blocks_per_seq * 64 */
+#define KVQ_FLAG_TIMEOUT 0x4     /* a bounded wait for a shared-memory copy ran out */
+#define KVQ_FLAG_NO_TAIL 0x8     /* an append into a partial block found no fp16 tail buffer */
+#define KVQ_FLAG_BAD_APPEND 0x10 /* cu_seqlens not increasing, or more new tokens than max_new_tokens */
+
+/*
+ * The paged cache.  All pointers are caller-owned device memory.
+ *   k_codes, v_codes   [num_pages][num_heads][64][head_dim/2 or head_dim]
+ *   k_scales, v_scales [num_pages][num_heads] binary32
+ *   k_tail, v_tail     fp16 [max_seqs][num_heads][64][head_dim]: the original
+ *                      rows of each sequence's open (partial) block, so an
+ *                      append can re-quantize that block from the originals.
+ *                      Sequence b of an append call uses row b.  May be NULL
+ *                      when every append ends on a 64-token boundary.
+ *   status             one int32 the kernels OR KVQ_FLAG_* bits into; may be
+ *                      NULL (then device-side problems go unreported).  Zero it
+ *                      before first use.
+ */
+typedef struct kvq_cache {
+    int32_t fmt;          /* kvq_format */
+    int32_t num_heads;
+    int32_t head_dim;     /* must be 128 */
+    int32_t page_tokens;  /* must be 64 */
+    int32_t num_pages;
+    int32_t max_seqs;     /* rows of the tail buffers */
+    uint8_t *k_codes;
+    uint8_t *v_codes;
+    float *k_scales;
+    float *v_scales;
+    uint16_t *k_tail;
+    uint16_t *v_tail;
+    int32_t *status;
+} kvq_cache;
+
+/*
+ * kvq_quantize -- quantize_block of one contiguous tensor (jsqmd.com/news/887038
+ * section 2.1; INT8: aicoding.csdn.net section 2.2).
+ *   x       fp16 [num_tokens][num_heads][head_dim], 16-byte aligned
+ *   codes   [ceil(num_tokens/64)][num_heads][64][head_dim/2 (int4) or head_dim (int8)],
+ *           16-byte aligned; rows past num_tokens in the last block are written as 0
+ *   scales  [ceil(num_tokens/64)][num_heads]
+ * num_tokens == 0 is a no-op.  Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED,
+ * KVQ_ERR_CUDA.
+ */
+kvq_status kvq_quantize(kvq_format fmt, const uint16_t *x, int64_t num_tokens, int32_t num_heads,
+                        int32_t head_dim, uint8_t *codes, float *scales, kvq_stream_t stream);
+
+/*
+ * kvq_append -- append new tokens to every sequence of a batch and keep the
+ * cache equal to quantize_block of each sequence's whole history: full blocks
+ * are quantized once; the open block is re-quantized from its fp16 originals
+ * (tail buffer + new rows) and its tail rows are updated.
+ *   k_new, v_new     fp16 [total_new][num_heads][head_dim], sequences back to
+ *                    back, sequence b in rows [cu_seqlens[b], cu_seqlens[b+1])
+ *   cu_seqlens       device int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
+ *                    cu_seqlens[num_seqs] <= total_new_tokens
+ *   block_table      device int32 [num_seqs][max_blocks_per_seq]: page of block j
+ *   seq_lens_before  device int32 [num_seqs]: tokens already in each sequence
+ *   total_new_tokens rows of k_new and v_new (a sequence whose rows would fall
+ *                    beyond them is skipped and flagged)
+ *   max_new_tokens   host bound on cu_seqlens[b+1] - cu_seqlens[b] (sizes the grid)
+ * Device-detected problems set KVQ_FLAG_* bits in cache->status and skip the
+ * affected blocks.  Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA.
+ */
+kvq_status kvq_append(const kvq_cache *cache, const uint16_t *k_new, const uint16_t *v_new,
+                      const int32_t *cu_seqlens, const int32_t *block_table, int32_t max_blocks_per_seq,
+                      const int32_t *seq_lens_before, int32_t num_seqs, int64_t total_new_tokens,
+                      int32_t max_new_tokens, kvq_stream_t stream);
+
+/*
+ * kvq_decode_workspace_bytes -- device scratch that kvq_decode_attention
+ * needs on the current device (split partials and the per-sequence unit
+ * prefix).  Depends on the format, the head dimension and the device's SM
+ * count only.  Returns 0 for unsupported arguments.
+ */
+size_t kvq_decode_workspace_bytes(kvq_format fmt, int32_t num_heads, int32_t head_dim);
+
+/*
+ * kvq_decode_attention -- single-token decode attention over the quantized
+ * paged cache (decode reading a quantized KV cache: aicoding.csdn.net
+ * section 3.1; paging: ddd.cn section 4).  For every (b, h):
+ *   s_t = softmax_scale * sum_d q[b][h][d] * k^_t[d],   t < seq_lens[b]
+ *   out[b][h][:] = sum_t softmax(s)_t * v^_t[:]
+ * computed in binary32 with an online softmax over splits of the sequence and
+ * a second pass that merges the splits.
+ *   q, out           fp16 [num_seqs][num_heads][head_dim], 16-byte aligned
+ *   block_table      device int32 [num_seqs][max_blocks_per_seq]
+ *   seq_lens         device int32 [num_seqs] (0 allowed: that output is 0)
+ *   softmax_scale    normally 1/sqrt(head_dim)
+ *   workspace        >= kvq_decode_workspace_bytes(...) bytes, 16-byte aligned;
+ *                    contents need no initialisation; do not share one
+ *                    workspace between calls that may run concurrently
+ * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE,
+ * KVQ_ERR_CUDA; device-side problems set KVQ_FLAG_* bits in cache->status.
+ */
+kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const int32_t *block_table,
+                                int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                                float softmax_scale, uint16_t *out, void *workspace,
+                                size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * kvq_get_device_status -- synchronise the stream, read and clear the cache's
+ * device status word.  *flags_out (host, may be NULL) receives the KVQ_FLAG_*
+ * bits.  Returns KVQ_OK when no bit was set, else the kvq_status of the most
+ * serious bit (bad page, then bad length, then timeout, then append errors).
+ */
+kvq_status kvq_get_device_status(const kvq_cache *cache, kvq_stream_t stream, int32_t *flags_out);
+
+/* a static, human-readable name of a status code */
+const char *kvq_status_string(kvq_status status);
+
+/* library version: major * 10000 + minor * 100 + patch */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -5,11 +5,12 @@ path.  Plain gcc, no fast-math and no FMA contraction, so that every binary32
 operation of the codec is one IEEE-rounded operation as written in the source.
 """
 import os
+import platform
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "kvq_oracle.c")
-LIB = os.path.join(HERE, "liboracle.so")
+LIB = os.path.join(HERE, "_build", platform.machine() or "unknown", "liboracle.so")
 
 CFLAGS = ["-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared",
           "-Wall", "-Wextra", "-Wno-unused-parameter"]
@@ -19,6 +20,7 @@ def build(force: bool = False) -> str:
     if (not force and os.path.exists(LIB)
             and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
         return LIB
+    os.makedirs(os.path.dirname(LIB), exist_ok=True)
     tmp = LIB + f".tmp{os.getpid()}"
     subprocess.check_call(["gcc", *CFLAGS, SRC, "-o", tmp, "-lm"])
     os.replace(tmp, LIB)

@@ -1,8 +1,11 @@
 """Build the native libraries of the package, in-tree, for sm_103a.
 
-  lib/libkvq.so           the CUDA library behind include/kvq.h
-  lib/libkvqsynth.so      host build of the synthetic-input generator (plain C)
-  lib/libkvqsynth_cuda.so device build of the synthetic-input generator
+  lib/<arch>/libkvq.so           the CUDA library behind include/kvq.h
+  lib/<arch>/libkvqsynth.so      host build of the synthetic-input generator (plain C)
+  lib/<arch>/libkvqsynth_cuda.so device build of the synthetic-input generator
+
+Outputs live under the machine architecture (x86_64, aarch64) so that a tree
+copied between machines never links or loads objects built for the other.
 
 Translation units compile in parallel; every nvcc call uses one -gencode
 (compute_103a -> sm_103a).  Rebuilds only what is older than its sources.
@@ -10,12 +13,14 @@ Translation units compile in parallel; every nvcc call uses one -gencode
 import concurrent.futures as cf
 import glob
 import os
+import platform
 import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-LIBDIR = os.path.join(PKG, "lib")
-OBJDIR = os.path.join(PKG, "_build")
+ARCH = platform.machine() or "unknown"
+LIBDIR = os.path.join(PKG, "lib", ARCH)
+OBJDIR = os.path.join(PKG, "_build", ARCH)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 SYNTH = os.path.join(PKG, "synth")
@@ -62,7 +67,7 @@ def _compile_cu(src, obj, extra=()):
 
 def _link(objs, out):
     tmp = out + f".tmp{os.getpid()}"
-    _run([_nvcc(), "-shared", *GENCODE, *objs, "-o", tmp, "-lcuda"])
+    _run([_nvcc(), "-shared", *GENCODE, *objs, "-o", tmp])
     os.replace(tmp, out)
 
 

@@ -1,0 +1,182 @@
+// kvq_api.cu -- the C ABI declared in include/kvq.h: host-side argument checks,
+// sub-batching, and launches of the kernels on the caller's stream.  No device
+// memory is allocated here; every buffer belongs to the caller.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+bool fmt_ok(int fmt) { return fmt == KVQ_INT4_B64 || fmt == KVQ_INT8_PAGE; }
+
+kvq_status check_cache(const kvq_cache *c)
+{
+    if (!c) return KVQ_ERR_INVALID_ARG;
+    if (!fmt_ok(c->fmt)) return KVQ_ERR_UNSUPPORTED;
+    if (c->head_dim != kvq::kHeadDim || c->page_tokens != kvq::kPage) return KVQ_ERR_UNSUPPORTED;
+    if (c->num_heads <= 0 || c->num_pages <= 0) return KVQ_ERR_INVALID_ARG;
+    if (!c->k_codes || !c->v_codes || !c->k_scales || !c->v_scales) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(c->k_codes) || !aligned16(c->v_codes)) return KVQ_ERR_INVALID_ARG;
+    if ((c->k_tail && !aligned16(c->k_tail)) || (c->v_tail && !aligned16(c->v_tail))) return KVQ_ERR_INVALID_ARG;
+    if ((c->k_tail == nullptr) != (c->v_tail == nullptr)) return KVQ_ERR_INVALID_ARG;
+    return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_quantize(kvq_format fmt, const uint16_t *x, int64_t num_tokens, int32_t num_heads,
+                        int32_t head_dim, uint8_t *codes, float *scales, kvq_stream_t stream)
+{
+    if (!fmt_ok(fmt) || head_dim != kvq::kHeadDim) return KVQ_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || num_heads <= 0) return KVQ_ERR_INVALID_ARG;
+    if (num_tokens == 0) return KVQ_OK;
+    if (!x || !codes || !scales || !aligned16(x) || !aligned16(codes)) return KVQ_ERR_INVALID_ARG;
+    return from_cuda(kvq::launch_quantize(fmt, x, num_tokens, num_heads, codes, scales,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_append(const kvq_cache *cache, const uint16_t *k_new, const uint16_t *v_new,
+                      const int32_t *cu_seqlens, const int32_t *block_table, int32_t max_blocks_per_seq,
+                      const int32_t *seq_lens_before, int32_t num_seqs, int64_t total_new_tokens,
+                      int32_t max_new_tokens, kvq_stream_t stream)
+{
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (num_seqs < 0 || max_new_tokens < 0 || max_blocks_per_seq <= 0 || total_new_tokens < 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (num_seqs == 0 || max_new_tokens == 0) return KVQ_OK;
+    if (!k_new || !v_new || !cu_seqlens || !block_table || !seq_lens_before) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+    if (cache->k_tail && num_seqs > cache->max_seqs) return KVQ_ERR_INVALID_ARG;
+    kvq::AppendParams p;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.cu_seqlens = cu_seqlens;
+    p.block_table = block_table;
+    p.seq_lens_before = seq_lens_before;
+    p.k_codes = cache->k_codes;
+    p.v_codes = cache->v_codes;
+    p.k_scales = cache->k_scales;
+    p.v_scales = cache->v_scales;
+    p.k_tail = cache->k_tail;
+    p.v_tail = cache->v_tail;
+    p.status = cache->status;
+    p.num_heads = cache->num_heads;
+    p.num_pages = cache->num_pages;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_new_tokens = max_new_tokens;
+    p.total_new = total_new_tokens;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // grid.y holds the sequence: launch in slices of at most 65535 sequences
+    for (int32_t b0 = 0; b0 < num_seqs; b0 += 65535) {
+        kvq::AppendParams q = p;
+        q.num_seqs = (num_seqs - b0) < 65535 ? (num_seqs - b0) : 65535;
+        q.cu_seqlens = cu_seqlens + b0;
+        q.block_table = block_table + (int64_t)b0 * max_blocks_per_seq;
+        q.seq_lens_before = seq_lens_before + b0;
+        if (q.k_tail) {
+            q.k_tail = cache->k_tail + (int64_t)b0 * cache->num_heads * kvq::kPage * kvq::kHeadDim;
+            q.v_tail = cache->v_tail + (int64_t)b0 * cache->num_heads * kvq::kPage * kvq::kHeadDim;
+        }
+        cudaError_t e = kvq::launch_append(cache->fmt, q, s);
+        if (e != cudaSuccess) return KVQ_ERR_CUDA;
+    }
+    return KVQ_OK;
+}
+
+size_t kvq_decode_workspace_bytes(kvq_format fmt, int32_t num_heads, int32_t head_dim)
+{
+    if (!fmt_ok(fmt) || head_dim != kvq::kHeadDim || num_heads <= 0) return 0;
+    return kvq::decode_workspace_bytes(fmt);
+}
+
+kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const int32_t *block_table,
+                                int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                                float softmax_scale, uint16_t *out, void *workspace, size_t workspace_bytes,
+                                kvq_stream_t stream)
+{
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || !isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+    if (num_seqs == 0) return KVQ_OK;
+    if (!q || !block_table || !seq_lens || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+    const size_t need = kvq::decode_workspace_bytes(cache->fmt);
+    if (need == 0) return KVQ_ERR_CUDA;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+    const int grid_warps = kvq::decode_grid_warps(cache->fmt);
+    kvq::DecodeParams p;
+    p.k_codes = cache->k_codes;
+    p.v_codes = cache->v_codes;
+    p.k_scales = cache->k_scales;
+    p.v_scales = cache->v_scales;
+    p.status = cache->status;
+    p.num_heads = cache->num_heads;
+    p.num_pages = cache->num_pages;
+    p.max_blocks = max_blocks_per_seq;
+    p.score_scale = softmax_scale * 1.4426950408889634f;
+    p.partials = reinterpret_cast<float *>(workspace);
+    p.cu_units = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(workspace) +
+                                             (size_t)grid_warps * 2 * kvq::kPartialStride * sizeof(float));
+    const int64_t HD = (int64_t)cache->num_heads * kvq::kHeadDim;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int32_t b0 = 0; b0 < num_seqs; b0 += kvq::kMaxSeqsPerLaunch) {
+        kvq::DecodeParams d = p;
+        d.num_seqs = (num_seqs - b0) < kvq::kMaxSeqsPerLaunch ? (num_seqs - b0) : kvq::kMaxSeqsPerLaunch;
+        d.q = q + b0 * HD;
+        d.out = out + b0 * HD;
+        d.seq_lens = seq_lens + b0;
+        d.block_table = block_table + (int64_t)b0 * max_blocks_per_seq;
+        cudaError_t e = kvq::launch_decode(cache->fmt, d, s);
+        if (e != cudaSuccess) return KVQ_ERR_CUDA;
+    }
+    return KVQ_OK;
+}
+
+kvq_status kvq_get_device_status(const kvq_cache *cache, kvq_stream_t stream, int32_t *flags_out)
+{
+    if (!cache) return KVQ_ERR_INVALID_ARG;
+    int32_t flags = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cache->status) {
+        if (cudaMemcpyAsync(&flags, cache->status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return KVQ_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
+        if (flags && cudaMemsetAsync(cache->status, 0, sizeof(int32_t), s) != cudaSuccess) return KVQ_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
+    } else if (cudaStreamSynchronize(s) != cudaSuccess) {
+        return KVQ_ERR_CUDA;
+    }
+    if (flags_out) *flags_out = flags;
+    if (flags & KVQ_FLAG_BAD_PAGE) return KVQ_ERR_BAD_BLOCK_TABLE;
+    if (flags & KVQ_FLAG_BAD_LENGTH) return KVQ_ERR_BAD_LENGTH;
+    if (flags & KVQ_FLAG_TIMEOUT) return KVQ_ERR_TIMEOUT;
+    if (flags & (KVQ_FLAG_NO_TAIL | KVQ_FLAG_BAD_APPEND)) return KVQ_ERR_BAD_LENGTH;
+    return KVQ_OK;
+}
+
+const char *kvq_status_string(kvq_status status)
+{
+    switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_BAD_BLOCK_TABLE: return "block-table entry out of range";
+    case KVQ_ERR_TIMEOUT: return "bounded wait timed out";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVQ_ERR_BAD_LENGTH: return "sequence length or append bounds invalid";
+    }
+    return "unknown status";
+}
+
+int32_t kvq_version(void) { return 100; }
+
+}  // extern "C"

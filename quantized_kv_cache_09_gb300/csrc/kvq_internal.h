@@ -1,0 +1,70 @@
+// kvq_internal.h -- launch parameters and launchers shared between the C ABI
+// (kvq_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kHeadDim = 128;
+constexpr int kPage = 64;
+
+struct AppendParams {
+    const uint16_t *k_new;
+    const uint16_t *v_new;
+    const int32_t *cu_seqlens;
+    const int32_t *block_table;
+    const int32_t *seq_lens_before;
+    uint8_t *k_codes;
+    uint8_t *v_codes;
+    float *k_scales;
+    float *v_scales;
+    uint16_t *k_tail;
+    uint16_t *v_tail;
+    int32_t *status;
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t num_pages;
+    int32_t max_blocks;
+    int32_t max_new_tokens;
+    int64_t total_new;
+};
+
+struct DecodeParams {
+    const uint8_t *k_codes;
+    const uint8_t *v_codes;
+    const float *k_scales;
+    const float *v_scales;
+    const uint16_t *q;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    uint16_t *out;
+    float *partials;   // [grid warps][2][kPartialStride]
+    int32_t *cu_units; // [num_seqs + 1] written by CTA 0 of the split kernel for the merge kernel
+    int32_t *status;
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t num_pages;
+    int32_t max_blocks;
+    float score_scale;  // softmax_scale * log2(e): scores are kept in the base-2 domain
+};
+
+// floats per split partial: m, l, 2 pad, acc[128]
+constexpr int kPartialStride = 132;
+// sequences per split-kernel launch (the per-CTA prefix lives in shared memory)
+constexpr int kMaxSeqsPerLaunch = 512;
+
+cudaError_t launch_quantize(int fmt, const uint16_t *x, int64_t T, int H, uint8_t *codes, float *scales,
+                            cudaStream_t s);
+cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s);
+
+// number of warps of the persistent split grid on the current device (0 on error)
+int decode_grid_warps(int fmt);
+size_t decode_workspace_bytes(int fmt);
+cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s);
+
+}  // namespace kvq

@@ -1,0 +1,224 @@
+"""Python binding of the kvq C ABI (include/kvq.h): ctypes over lib/libkvq.so.
+
+Argument marshalling only -- torch tensors in, raw device pointers, sizes and
+the current CUDA stream out; every step of the work runs in the CUDA kernels.
+There is no fallback: if the library is missing the first call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+KVQ_INT4_B64 = 0
+KVQ_INT8_PAGE = 1
+HEAD_DIM = 128
+PAGE_TOKENS = 64
+
+KVQ_FLAG_BAD_PAGE = 0x1
+KVQ_FLAG_BAD_LENGTH = 0x2
+KVQ_FLAG_TIMEOUT = 0x4
+KVQ_FLAG_NO_TAIL = 0x8
+KVQ_FLAG_BAD_APPEND = 0x10
+
+STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CUDA",
+                4: "KVQ_ERR_BAD_BLOCK_TABLE", 5: "KVQ_ERR_TIMEOUT", 6: "KVQ_ERR_WORKSPACE",
+                7: "KVQ_ERR_BAD_LENGTH"}
+
+# every symbol include/kvq.h declares
+EXPORTS = ("kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attention",
+           "kvq_get_device_status", "kvq_status_string", "kvq_version")
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({kvq_status_string(status)})")
+
+
+class kvq_cache(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_tokens", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
+                ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
+                ("v_scales", ctypes.c_void_p), ("k_tail", ctypes.c_void_p), ("v_tail", ctypes.c_void_p),
+                ("status", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def library_path():
+    return _build.LIB_KVQ
+
+
+def lib():
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"kvq CUDA library not built ({path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        cp = ctypes.POINTER(kvq_cache)
+        L.kvq_quantize.argtypes = [ctypes.c_int, vp, i64, i32, i32, vp, vp, vp]
+        L.kvq_quantize.restype = ctypes.c_int
+        L.kvq_append.argtypes = [cp, vp, vp, vp, vp, i32, vp, i32, i64, i32, vp]
+        L.kvq_append.restype = ctypes.c_int
+        L.kvq_decode_workspace_bytes.argtypes = [ctypes.c_int, i32, i32]
+        L.kvq_decode_workspace_bytes.restype = sz
+        L.kvq_decode_attention.argtypes = [cp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, sz, vp]
+        L.kvq_decode_attention.restype = ctypes.c_int
+        L.kvq_get_device_status.argtypes = [cp, vp, ctypes.POINTER(i32)]
+        L.kvq_get_device_status.restype = ctypes.c_int
+        L.kvq_status_string.argtypes = [ctypes.c_int]
+        L.kvq_status_string.restype = ctypes.c_char_p
+        L.kvq_version.argtypes = []
+        L.kvq_version.restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device=None):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise KvqError(rc, what)
+
+
+def _cuda(t, dtype, name):
+    if not (t.is_cuda and t.is_contiguous() and t.dtype == dtype):
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def kvq_status_string(status):
+    return lib().kvq_status_string(int(status)).decode()
+
+
+def kvq_version():
+    return lib().kvq_version()
+
+
+def kvq_quantize(fmt, x, codes, scales, stream=None):
+    """x fp16 [T][H][128] -> codes uint8 [ceil(T/64)][H][64][64 or 128], scales fp32 [ceil(T/64)][H]."""
+    _cuda(x, torch.float16, "x")
+    _cuda(codes, torch.uint8, "codes")
+    _cuda(scales, torch.float32, "scales")
+    T, H, D = x.shape
+    nb = (T + PAGE_TOKENS - 1) // PAGE_TOKENS
+    rb = D // 2 if fmt == KVQ_INT4_B64 else D
+    if codes.numel() < nb * H * PAGE_TOKENS * rb or scales.numel() < nb * H:
+        raise ValueError("codes or scales too small")
+    _check(lib().kvq_quantize(int(fmt), _ptr(x), T, H, D, _ptr(codes), _ptr(scales), _stream(stream, x.device)),
+           "kvq_quantize")
+
+
+def kvq_append(cache, k_new, v_new, cu_seqlens, block_table, seq_lens_before, max_new_tokens, stream=None):
+    """Append the rows of k_new/v_new fp16 [total][H][128] to every sequence (see kvq.h)."""
+    _cuda(k_new, torch.float16, "k_new")
+    _cuda(v_new, torch.float16, "v_new")
+    for t, n in ((cu_seqlens, "cu_seqlens"), (block_table, "block_table"), (seq_lens_before, "seq_lens_before")):
+        _cuda(t, torch.int32, n)
+    B = seq_lens_before.numel()
+    if cu_seqlens.numel() != B + 1 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("cu_seqlens must have num_seqs + 1 entries and block_table num_seqs rows")
+    if k_new.shape != v_new.shape or k_new.dim() != 3:
+        raise ValueError("k_new and v_new must both be [total][H][128]")
+    _check(lib().kvq_append(ctypes.byref(cache.struct), _ptr(k_new), _ptr(v_new), _ptr(cu_seqlens),
+                            _ptr(block_table), block_table.shape[1], _ptr(seq_lens_before), B,
+                            k_new.shape[0], int(max_new_tokens), _stream(stream, k_new.device)), "kvq_append")
+
+
+def kvq_decode_workspace_bytes(fmt, num_heads, head_dim=HEAD_DIM):
+    return int(lib().kvq_decode_workspace_bytes(int(fmt), int(num_heads), int(head_dim)))
+
+
+def kvq_decode_attention(cache, q, block_table, seq_lens, softmax_scale, out, workspace, stream=None):
+    """out fp16 [B][H][128] = decode attention of q fp16 [B][H][128] over the cache."""
+    _cuda(q, torch.float16, "q")
+    _cuda(out, torch.float16, "out")
+    _cuda(block_table, torch.int32, "block_table")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    _cuda(workspace, torch.uint8, "workspace")
+    B = q.shape[0]
+    if out.shape != q.shape or seq_lens.numel() != B or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("q/out/seq_lens/block_table shapes disagree")
+    _check(lib().kvq_decode_attention(ctypes.byref(cache.struct), _ptr(q), _ptr(block_table), block_table.shape[1],
+                                      _ptr(seq_lens), B, float(softmax_scale), _ptr(out), _ptr(workspace),
+                                      workspace.numel(), _stream(stream, q.device)), "kvq_decode_attention")
+
+
+def kvq_get_device_status(cache, stream=None):
+    """(status, flags): reads and clears the cache's device status word (synchronises the stream)."""
+    flags = ctypes.c_int32(0)
+    rc = lib().kvq_get_device_status(ctypes.byref(cache.struct), _stream(stream), ctypes.byref(flags))
+    return rc, flags.value
+
+
+class PagedKVCache:
+    """Device buffers of one paged cache (allocated with torch) and the
+    kvq_cache descriptor that points at them."""
+
+    def __init__(self, fmt, num_pages, num_heads, max_seqs=0, device="cuda", with_tail=True):
+        self.fmt = int(fmt)
+        self.num_pages = int(num_pages)
+        self.num_heads = int(num_heads)
+        self.max_seqs = int(max_seqs)
+        rb = HEAD_DIM // 2 if self.fmt == KVQ_INT4_B64 else HEAD_DIM
+        self.row_bytes = rb
+        shape = (self.num_pages, self.num_heads, PAGE_TOKENS, rb)
+        self.k_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
+        self.v_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
+        self.k_scales = torch.zeros((self.num_pages, self.num_heads), dtype=torch.float32, device=device)
+        self.v_scales = torch.zeros((self.num_pages, self.num_heads), dtype=torch.float32, device=device)
+        if with_tail and self.max_seqs > 0:
+            tshape = (self.max_seqs, self.num_heads, PAGE_TOKENS, HEAD_DIM)
+            self.k_tail = torch.zeros(tshape, dtype=torch.float16, device=device)
+            self.v_tail = torch.zeros(tshape, dtype=torch.float16, device=device)
+        else:
+            self.k_tail = self.v_tail = None
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.struct = kvq_cache(self.fmt, self.num_heads, HEAD_DIM, PAGE_TOKENS, self.num_pages, self.max_seqs,
+                                self.k_codes.data_ptr(), self.v_codes.data_ptr(), self.k_scales.data_ptr(),
+                                self.v_scales.data_ptr(),
+                                None if self.k_tail is None else self.k_tail.data_ptr(),
+                                None if self.v_tail is None else self.v_tail.data_ptr(),
+                                self.status.data_ptr())
+
+    def rows_from(self, b0):
+        """A descriptor of the same cache whose tail rows start at sequence row b0,
+        for an append call that covers sequences b0, b0+1, ... of a larger batch."""
+        view = type("PagedKVCacheRows", (), {})()
+        step = self.num_heads * PAGE_TOKENS * HEAD_DIM * 2
+        s = self.struct
+        view.struct = kvq_cache(s.fmt, s.num_heads, s.head_dim, s.page_tokens, s.num_pages,
+                                max(0, self.max_seqs - b0), s.k_codes, s.v_codes, s.k_scales, s.v_scales,
+                                None if s.k_tail is None else s.k_tail + b0 * step,
+                                None if s.v_tail is None else s.v_tail + b0 * step, s.status)
+        return view
+
+    def workspace(self):
+        n = kvq_decode_workspace_bytes(self.fmt, self.num_heads)
+        if n <= 0:
+            raise RuntimeError("kvq_decode_workspace_bytes returned 0")
+        return torch.empty(n, dtype=torch.uint8, device=self.k_codes.device)
+
+    def bytes(self):
+        t = [self.k_codes, self.v_codes, self.k_scales, self.v_scales]
+        return sum(x.numel() * x.element_size() for x in t)
+
+
+__all__ = ["KVQ_INT4_B64", "KVQ_INT8_PAGE", "HEAD_DIM", "PAGE_TOKENS", "EXPORTS", "KvqError", "kvq_cache",
+           "PagedKVCache", "lib", "library_path", "kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes",
+           "kvq_decode_attention", "kvq_get_device_status", "kvq_status_string", "kvq_version"]

@@ -26,6 +26,7 @@ K_OUTLIER = 16
 V_OUTLIER = 17
 BLOCK_TABLE = 32
 LENGTHS = 48
+SAMPLE = 64
 
 _host = None
 _dev = None
@@ -126,7 +127,14 @@ def uniform_int(n, lo, hi, seed, stream):
     return out
 
 
+def synth_sample_heads(B, H, n, seed):
+    """n seeded (sequence, head) pairs, for sampled full-size parity checks."""
+    bs = uniform_int(n, 0, B - 1, seed, stream_id(SAMPLE, 0))
+    hs = uniform_int(n, 0, H - 1, seed, stream_id(SAMPLE, 1))
+    return [(int(b), int(h)) for b, h in zip(bs, hs)]
+
+
 from .workloads import Workload, make_workload, CONFIGS  # noqa: E402
 
 __all__ = ["fill_f16_host", "fill_f16_device", "outliers_per_head", "outliers_bernoulli", "permutation",
-           "uniform_int", "stream_id", "Workload", "make_workload", "CONFIGS", "f32_to_f16_bits"]
+           "uniform_int", "stream_id", "synth_sample_heads", "Workload", "make_workload", "CONFIGS", "f32_to_f16_bits"]

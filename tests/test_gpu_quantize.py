@@ -1,0 +1,164 @@
+"""GPU parity of the fused quantize kernel (kvq_quantize, kvq_append) against
+the CPU oracle: codes and scales must be bit-exact.  Definition: quantize_block
+(jsqmd.com/news/887038 section 2.1) and the per-chunk INT8 variant
+(aicoding.csdn.net section 2.2)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from quantized_kv_cache_09_gb300 import kvq
+from quantized_kv_cache_09_gb300.synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+FMTS = [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE]
+D = 128
+
+
+def _gpu_quantize(fmt, x_bits):
+    T, H, _ = x_bits.shape
+    nb = (T + 63) // 64
+    rb = 64 if fmt == kvq.KVQ_INT4_B64 else 128
+    x = torch.from_numpy(x_bits.view(np.float16)).cuda()
+    codes = torch.full((nb, H, 64, rb), 0xA5, dtype=torch.uint8, device="cuda")  # poison
+    scales = torch.full((nb, H), -1.0, dtype=torch.float32, device="cuda")
+    kvq.kvq_quantize(fmt, x, codes, scales)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), scales.cpu().numpy()
+
+
+def _assert_same(fmt, x_bits):
+    gc, gs = _gpu_quantize(fmt, x_bits)
+    oc, os_ = orc.quantize(fmt, x_bits)
+    assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32)), "scales differ"
+    if not np.array_equal(gc, oc):
+        bad = np.argwhere(gc != oc)
+        raise AssertionError(f"{len(bad)} code bytes differ, first at {bad[0].tolist()}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 64 * 3 + 17])
+def test_random_tensors_bit_exact(cuda_ok, fmt, T):
+    rng = np.random.default_rng(T + 100 * fmt)
+    x = rng.standard_normal((T, 5, D)) * rng.uniform(0.01, 20.0)
+    x[rng.random(x.shape) < 0.01] *= 10
+    _assert_same(fmt, x.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_exact_rounding_ties_bit_exact(cuda_ok, fmt):
+    """Blocks whose quotients are exact half-integers (x = k/2 with max|x| = 7.5
+    or 127, scale = 1): every tie must round to even, as the oracle does."""
+    rng = np.random.default_rng(5)
+    top = 7.5 if fmt == kvq.KVQ_INT4_B64 else 127.0
+    x = rng.integers(-int(2 * top), int(2 * top) + 1, (64 * 6, 3, D)).astype(np.float64) / 2
+    x[::64, :, 0] = top
+    _assert_same(fmt, x.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_every_fp16_absmax_bit_exact(cuda_ok, fmt):
+    """One block per positive finite fp16 magnitude a, row 0 = (a, -a, a/3, ...):
+    scale and the codes of +-a (where the binary32 quotient decides between -8
+    and -7 for int4) match the oracle for all 31743 magnitudes."""
+    mags = np.arange(1, 0x7C00, dtype=np.uint16)
+    n = mags.size
+    x = np.zeros((64 * n, 1, D), dtype=np.uint16)
+    x[0::64, 0, 0] = mags
+    x[0::64, 0, 1] = mags | 0x8000
+    af = mags.view(np.float16).astype(np.float32)
+    for k, frac in enumerate([1 / 3, -0.5, 0.2, -0.7333, 1 / 15, 0.4667]):
+        x[0::64, 0, 2 + k] = (af * np.float32(frac)).astype(np.float16).view(np.uint16)
+    _assert_same(fmt, x)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_zero_and_tiny_blocks(cuda_ok, fmt):
+    x = np.zeros((64 * 3, 2, D), dtype=np.float16)
+    x[64:128, 1, 5] = np.float16(6e-8)       # smallest subnormal
+    x[128:, 0, :] = np.float16(-3e-5)
+    _assert_same(fmt, x.view(np.uint16))
+
+
+def test_llama_layer_sequence_bit_exact(cuda_ok):
+    """One full sequence of the 7B-layer workload (8192 tokens x 32 heads, 4 x10
+    outlier channels per head), generated on the device and quantized there;
+    the oracle regenerates the same bits on the host."""
+    wl = W.make_workload(2)
+    x = torch.empty((8192, 32, D), dtype=torch.float16, device="cuda")
+    wl.kv_device("k", 3, 0, 8192, x)
+    codes = torch.empty((128, 32, 64, 64), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((128, 32), dtype=torch.float32, device="cuda")
+    kvq.kvq_quantize(kvq.KVQ_INT4_B64, x, codes, scales)
+    oc, os_ = orc.quantize(orc.INT4, wl.kv_host("k", 3, 0, 8192))
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_append_chunkings_equal_full_history(cuda_ok, fmt):
+    """Any sequence of appends (ragged chunks, single tokens, whole blocks,
+    block-crossing chunks) leaves the paged cache byte-identical to the oracle's
+    quantize_block of each sequence's full history."""
+    H = 3
+    B = 3
+    chunks = [[37, 1, 64, 100, 1, 27, 65, 129],   # ends at 424
+              [64, 64, 1, 63, 200],                # 392
+              [1] * 70 + [5]]                      # 75
+    lens = [sum(c) for c in chunks]
+    maxb = max((L + 63) // 64 for L in lens)
+    wl = W.Workload(B, H, D, lens, fmt, 1.3, None, "permuted", seed=9)
+    bt = torch.from_numpy(wl.block_table.copy()).cuda()
+    cache = kvq.PagedKVCache(fmt, wl.num_pages, H, max_seqs=B)
+    done = [0] * B
+    step = 0
+    while any(step < len(c) for c in chunks):
+        adds = [c[step] if step < len(c) else 0 for c in chunks]
+        cu = np.concatenate([[0], np.cumsum(adds)]).astype(np.int32)
+        k = np.concatenate([wl.kv_host("k", b, done[b], done[b] + adds[b]) for b in range(B)])
+        v = np.concatenate([wl.kv_host("v", b, done[b], done[b] + adds[b]) for b in range(B)])
+        kvq.kvq_append(cache, torch.from_numpy(k.view(np.float16)).cuda(),
+                       torch.from_numpy(v.view(np.float16)).cuda(), torch.from_numpy(cu).cuda(), bt,
+                       torch.tensor(done, dtype=torch.int32, device="cuda"), max(adds))
+        done = [done[b] + adds[b] for b in range(B)]
+        step += 1
+    rc, flags = kvq.kvq_get_device_status(cache)
+    assert rc == 0 and flags == 0
+    ko = np.zeros_like(cache.k_codes.cpu().numpy())
+    vo = np.zeros_like(ko)
+    kso = np.zeros((wl.num_pages, H), np.float32)
+    vso = np.zeros_like(kso)
+    for b in range(B):
+        orc.quantize_into_pages(fmt, wl.kv_host("k", b, 0, lens[b]), wl.block_table[b], ko, kso)
+        orc.quantize_into_pages(fmt, wl.kv_host("v", b, 0, lens[b]), wl.block_table[b], vo, vso)
+    used = np.unique(np.concatenate([wl.block_table[b, :(lens[b] + 63) // 64] for b in range(B)]))
+    assert np.array_equal(cache.k_scales.cpu().numpy()[used].view(np.uint32), kso[used].view(np.uint32))
+    assert np.array_equal(cache.v_scales.cpu().numpy()[used].view(np.uint32), vso[used].view(np.uint32))
+    assert np.array_equal(cache.k_codes.cpu().numpy()[used], ko[used])
+    assert np.array_equal(cache.v_codes.cpu().numpy()[used], vo[used])
+    # the tail buffers hold the originals of each open block
+    for b in range(B):
+        r = lens[b] % 64
+        if r:
+            want = wl.kv_host("k", b, lens[b] - r, lens[b]).transpose(1, 0, 2)
+            got = cache.k_tail[b, :, :r].cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, want)
+
+
+def test_append_reports_device_problems(cuda_ok):
+    """A block-table entry out of range, a length beyond the table, an open
+    block without a tail buffer: flagged in the status word, nothing faults."""
+    fmt = kvq.KVQ_INT4_B64
+    cache = kvq.PagedKVCache(fmt, 4, 2, max_seqs=0, with_tail=False)
+    k = torch.zeros((10, 2, D), dtype=torch.float16, device="cuda")
+    cu = torch.tensor([0, 10], dtype=torch.int32, device="cuda")
+    bt = torch.tensor([[7, 1]], dtype=torch.int32, device="cuda")
+    kvq.kvq_append(cache, k, k, cu, bt, torch.tensor([0], dtype=torch.int32, device="cuda"), 10)
+    assert kvq.kvq_get_device_status(cache)[0] == 4
+    kvq.kvq_append(cache, k, k, cu, bt, torch.tensor([120], dtype=torch.int32, device="cuda"), 10)
+    assert kvq.kvq_get_device_status(cache)[0] == 7
+    bt2 = torch.tensor([[0, 1]], dtype=torch.int32, device="cuda")
+    kvq.kvq_append(cache, k, k, cu, bt2, torch.tensor([5], dtype=torch.int32, device="cuda"), 10)
+    rc, flags = kvq.kvq_get_device_status(cache)
+    assert flags & kvq.KVQ_FLAG_NO_TAIL
+    assert kvq.kvq_get_device_status(cache) == (0, 0)   # the word was cleared
