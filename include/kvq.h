@@ -173,6 +173,32 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
                                 size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * kvq_decode_attention_noalloc -- kvq_decode_attention without a caller
+ * workspace.  The pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory when they run decode attention:
+ * an inference-engine plugin whose execute step must not allocate, a process
+ * whose device memory is reserved up front by another allocator, or a loop
+ * that cannot afford the device-wide synchronisation cudaMalloc / cudaFree
+ * may cause.  It allocates nothing.
+ *
+ * The scratch is one fixed array of KVQ_NOALLOC_SCRATCH_BYTES (4 MiB) of
+ * device memory inside the library; every GPU that loads the library holds it
+ * until the process exits.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current) and keeps
+ * it, so make that first call before any stream capture.  A device whose split
+ * grid needs more scratch than the array (more than about 330 SMs' worth of
+ * partials) gets KVQ_ERR_WORKSPACE.  Every call uses the same array and it
+ * keeps the last call's contents: calls that may overlap on the GPU (other
+ * streams, other threads) race on it, so the caller must serialise them.
+ * Nothing in it has to start at zero.  Arguments, results and other errors are
+ * those of kvq_decode_attention.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const uint16_t *q, const int32_t *block_table,
+                                        int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                                        float softmax_scale, uint16_t *out, kvq_stream_t stream);
+
+/*
  * kvq_get_device_status -- synchronise the stream, read and clear the cache's
  * device status word.  *flags_out (host, may be NULL) receives the KVQ_FLAG_*
  * bits.  Returns KVQ_OK when no bit was set, else the kvq_status of the most

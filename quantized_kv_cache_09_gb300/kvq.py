@@ -28,7 +28,8 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
 
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attention",
-           "kvq_get_device_status", "kvq_status_string", "kvq_version")
+           "kvq_decode_attention_noalloc", "kvq_get_device_status", "kvq_status_string", "kvq_version")
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class KvqError(RuntimeError):
@@ -70,6 +71,8 @@ def lib():
         L.kvq_decode_workspace_bytes.restype = sz
         L.kvq_decode_attention.argtypes = [cp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, sz, vp]
         L.kvq_decode_attention.restype = ctypes.c_int
+        L.kvq_decode_attention_noalloc.argtypes = [cp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp]
+        L.kvq_decode_attention_noalloc.restype = ctypes.c_int
         L.kvq_get_device_status.argtypes = [cp, vp, ctypes.POINTER(i32)]
         L.kvq_get_device_status.restype = ctypes.c_int
         L.kvq_status_string.argtypes = [ctypes.c_int]
@@ -159,6 +162,25 @@ def kvq_decode_attention(cache, q, block_table, seq_lens, softmax_scale, out, wo
                                       workspace.numel(), _stream(stream, q.device)), "kvq_decode_attention")
 
 
+def kvq_decode_attention_noalloc(cache, q, block_table, seq_lens, softmax_scale, out, stream=None):
+    """kvq_decode_attention without a workspace, for callers that cannot
+    allocate device memory when they run decode attention (a plugin whose
+    execute step must not allocate, memory reserved up front by another
+    allocator, a loop that cannot afford cudaMalloc's synchronisation): the
+    scratch is a fixed 4 MiB array inside the library, shared by every call, so
+    calls that may overlap on the GPU must be serialised by the caller."""
+    _cuda(q, torch.float16, "q")
+    _cuda(out, torch.float16, "out")
+    _cuda(block_table, torch.int32, "block_table")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    B = q.shape[0]
+    if out.shape != q.shape or seq_lens.numel() != B or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("q/out/seq_lens/block_table shapes disagree")
+    _check(lib().kvq_decode_attention_noalloc(ctypes.byref(cache.struct), _ptr(q), _ptr(block_table),
+                                              block_table.shape[1], _ptr(seq_lens), B, float(softmax_scale),
+                                              _ptr(out), _stream(stream, q.device)), "kvq_decode_attention_noalloc")
+
+
 def kvq_get_device_status(cache, stream=None):
     """(status, flags): reads and clears the cache's device status word (synchronises the stream)."""
     flags = ctypes.c_int32(0)
@@ -221,4 +243,5 @@ class PagedKVCache:
 
 __all__ = ["KVQ_INT4_B64", "KVQ_INT8_PAGE", "HEAD_DIM", "PAGE_TOKENS", "EXPORTS", "KvqError", "kvq_cache",
            "PagedKVCache", "lib", "library_path", "kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes",
-           "kvq_decode_attention", "kvq_get_device_status", "kvq_status_string", "kvq_version"]
+           "kvq_decode_attention", "kvq_decode_attention_noalloc", "kvq_get_device_status", "kvq_status_string",
+           "kvq_version"]
