@@ -47,6 +47,10 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", default="llama2-7b-layer",
+                    choices=["tiny", "llama2-7b-layer", "long-context", "paged-int8", "prefill-append"])
+    ap.add_argument("--prefill-seqs", type=int, default=64)
+    ap.add_argument("--no-extras", dest="extras", action="store_false")
     return ap.parse_args()
 
 
@@ -231,7 +235,21 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args):
+DECODE_WORKLOADS = {"tiny": 1, "llama2-7b-layer": 2, "long-context": 3, "paged-int8": 4}
+
+
+def _sync_all(pg, dev):
+    import torch
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+
+
+def measure_decode(name, K, Wm, seed, dev, pg):
+    """Decode steps (append one token per sequence + decode attention) on a
+    decode workload.  64-aligned histories cycle the appended position through
+    one block (a real decode progression); ragged histories re-append the token
+    at their end every step, which leaves the cache in the same state."""
     import numpy as np
     import torch
 
@@ -239,44 +257,26 @@ def run_ours(args):
     from quantized_kv_cache_09_gb300.runner import DecodeStep, DeviceWorkload
     from quantized_kv_cache_09_gb300.synth import workloads as W
 
-    world, rank, local = dist_env()
-    if not torch.cuda.is_available():
-        raise RuntimeError("bench.py needs a CUDA device")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
-
-    seed = args.seed + rank
-    wl = W.make_workload(CONFIG, seed=seed, extra_tokens=64)
+    wl = W.make_workload(DECODE_WORKLOADS[name], seed=seed, extra_tokens=64)
     dw = DeviceWorkload(wl, device=dev)
-    dw.prefill()
+    dw.prefill(max_tokens_per_call=1 << 18)
     B, H, D = wl.B, wl.H, wl.D
-    L = int(wl.lens[0])
+    aligned = bool(np.all(wl.lens % 64 == 0))
     step = DecodeStep(dw)
-
-    # per-step inputs resident in HBM: 64 distinct steps, cycled
     NS = 64
-    k_steps, v_steps, q_steps = [], [], []
+    k_steps, v_steps, q_steps, lens_b, lens_a = [], [], [], [], []
     for s in range(NS):
-        k1, v1, q = dw.new_token_tensors(s)
+        k1, v1, q = dw.new_token_tensors(s if aligned else 0)
+        if not aligned:
+            wl.q_device(q, s)
         k_steps.append(k1)
         v_steps.append(v1)
         q_steps.append(q)
-    lens_b = [torch.full((B,), L + s, dtype=torch.int32, device=dev) for s in range(NS)]
-    lens_a = [torch.full((B,), L + s + 1, dtype=torch.int32, device=dev) for s in range(NS)]
-    # the step at cycle position s appends position L + s: its history rows 0..s-1
-    # of the open block are the tokens appended by the previous s steps, which the
-    # warm-up establishes; prime the tail with one full cycle
-    stream = torch.cuda.current_stream(dev)
-    for s in range(NS):
+        off = s if aligned else 0
+        lens_b.append(torch.from_numpy(wl.lens + off).to(dev))
+        lens_a.append(torch.from_numpy(wl.lens + off + 1).to(dev))
+    for s in range(NS):   # one full cycle establishes the open block's tail rows
         step.run(lens_b[s], lens_a[s], k_steps[s], v_steps[s], q_steps[s])
-    torch.cuda.synchronize(dev)
-
-    K, Wm = args.steps, args.warmup
     for i in range(Wm):
         s = i % NS
         step.run(lens_b[s], lens_a[s], k_steps[s], v_steps[s], q_steps[s])
@@ -285,13 +285,12 @@ def run_ours(args):
     if rc != 0:
         raise RuntimeError(f"device status {rc} flags {flags:#x} after warm-up")
 
+    stream = torch.cuda.current_stream(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index or 0)
     clocks.start()
     time.sleep(0.3)
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize(dev)
+    _sync_all(pg, dev)
     t_wall0 = time.time()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -306,30 +305,23 @@ def run_ours(args):
                                  dw.workspace)
         e2.record(stream)
     end.record(stream)
-    torch.cuda.synchronize(dev)
-    if pg:
-        pg.barrier()
-    t_wall1 = time.time()
-    clocks.window = (t_wall0, t_wall1)
+    _sync_all(pg, dev)
+    clocks.window = (t_wall0, time.time())
     total_ms = start.elapsed_time(end)
-    app_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    app_ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
+    dec_ms = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(K)) / K
     rc, flags = kvq.kvq_get_device_status(dw.cache)
     if rc != 0:
         raise RuntimeError(f"device status {rc} flags {flags:#x} after timed steps")
 
-    # ---- end to end through the C ABI with host buffers ----
+    # end to end through the C ABI with host buffers
     pin_k = [k.cpu().pin_memory() for k in k_steps]
     pin_v = [v.cpu().pin_memory() for v in v_steps]
     pin_q = [q.cpu().pin_memory() for q in q_steps]
     pin_o = torch.empty((B, H, D), dtype=torch.float16).pin_memory()
-    dk = torch.empty_like(k_steps[0])
-    dv = torch.empty_like(v_steps[0])
-    dq = torch.empty_like(q_steps[0])
+    dk, dv, dq = (torch.empty_like(k_steps[0]), torch.empty_like(v_steps[0]), torch.empty_like(q_steps[0]))
     Ke = max(1, K // 2)
-    torch.cuda.synchronize(dev)
-    if pg:
-        pg.barrier()
+    _sync_all(pg, dev)
     e2e_s = torch.cuda.Event(enable_timing=True)
     e2e_e = torch.cuda.Event(enable_timing=True)
     e2e_s.record(stream)
@@ -342,13 +334,77 @@ def run_ours(args):
         kvq.kvq_decode_attention(dw.cache, dq, dw.block_table, lens_a[s], dw.softmax_scale, step.out, dw.workspace)
         pin_o.copy_(step.out, non_blocking=True)
     e2e_e.record(stream)
-    torch.cuda.synchronize(dev)
-    if pg:
-        pg.barrier()
+    _sync_all(pg, dev)
     e2e_ms = e2e_s.elapsed_time(e2e_e)
     clocks.stop()
 
-    # ---- aggregate over ranks (max time) ----
+    ctx = [(wl.lens + ((Wm + i) % NS if aligned else 0) + 1) for i in range(K)]
+    dec_bytes = sum(wl.decode_bytes(c) for c in ctx) / K
+    res = dict(wl=wl, B=B, H=H, D=D, aligned=aligned, total_ms=total_ms, app_ms=app_ms, dec_ms=dec_ms,
+               e2e_ms=e2e_ms, Ke=Ke, dec_bytes=dec_bytes, clocks=clocks.summary(),
+               h2d=3 * B * H * D * 2, d2h=B * H * D * 2, launches=3 * K)
+    del dw
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_prefill(K, Wm, seed, dev, nseqs=64):
+    """prefill-append: one kvq_append of nseqs x 4096 new tokens (H=32) into
+    randomly permuted empty pages; repeated calls write the same bytes."""
+    import torch
+
+    from quantized_kv_cache_09_gb300 import kvq
+    from quantized_kv_cache_09_gb300.runner import DeviceWorkload
+    from quantized_kv_cache_09_gb300.synth import workloads as W
+
+    c = W.CONFIGS[5]
+    wl = W.Workload(nseqs, c["H"], c["D"], [c["L"]] * nseqs, c["fmt"], c["sigma"], None, "permuted", seed,
+                    0, c["name"])
+    dw = DeviceWorkload(wl, device=dev)
+    L = c["L"]
+    k_new = torch.empty((nseqs * L, wl.H, wl.D), dtype=torch.float16, device=dev)
+    v_new = torch.empty_like(k_new)
+    for b in range(nseqs):
+        wl.kv_device("k", b, 0, L, k_new[b * L:(b + 1) * L])
+        wl.kv_device("v", b, 0, L, v_new[b * L:(b + 1) * L])
+    cu = torch.arange(0, nseqs * L + 1, L, dtype=torch.int32, device=dev)
+    zero = torch.zeros(nseqs, dtype=torch.int32, device=dev)
+    for _ in range(Wm):
+        kvq.kvq_append(dw.cache, k_new, v_new, cu, dw.block_table, zero, L)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        ev[i][0].record(stream)
+        kvq.kvq_append(dw.cache, k_new, v_new, cu, dw.block_table, zero, L)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    rc, flags = kvq.kvq_get_device_status(dw.cache)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} flags {flags:#x} in prefill-append")
+    nbytes = wl.quantize_bytes(L) * nseqs
+    del k_new, v_new, dw
+    torch.cuda.empty_cache()
+    return dict(ms=ms, bytes=nbytes, tokens=nseqs * L)
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    seed = args.seed + rank
+    peak, peak_kind = measured_peak()
+
     def max_over_ranks(x):
         if not pg:
             return x
@@ -356,38 +412,61 @@ def run_ours(args):
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         return float(t.item())
 
-    total_ms = max_over_ranks(total_ms)
-    e2e_ms = max_over_ranks(e2e_ms)
-    dec_mean = max_over_ranks(sum(dec_ms) / K)
-    app_mean = max_over_ranks(sum(app_ms) / K)
+    K, Wm = args.steps, args.warmup
+    if args.workload == "prefill-append":
+        r = measure_prefill(K, max(Wm, 1), seed, dev, args.prefill_seqs)
+        ms = max_over_ranks(r["ms"])
+        gbs = r["bytes"] / (ms * 1e-3) / 1e9
+        line = {"metric": METRIC, "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm,
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "fp16 in, int4 codes out, fp32 math", "data": "synthetic (seeded generator in HBM)",
+                "config": {"workload": "prefill-append", "new_tokens": r["tokens"], "H": 32, "D": 128,
+                           "format": "int4-b64", "step": "one kvq_append of all new tokens"},
+                "roofline": {"kernel": "append_kernel", "bound": "hbm", "achieved": gbs, "peak": peak,
+                             "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
+                             "traffic": ncu_traffic("append_kernel"), "algorithmic_bytes_per_launch": r["bytes"]},
+                "gpu_launches": K}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if pg:
+            pg.destroy_process_group()
+        return
 
-    # algorithmic bytes (per launch, averaged over the cycle of context lengths)
-    ctx = [L + ((Wm + i) % NS) + 1 for i in range(K)]
-    dec_bytes = sum(wl.decode_bytes(np.full(B, c)) for c in ctx) / K
-    peak, peak_kind = measured_peak()
-    achieved = dec_bytes / (dec_mean * 1e-3) / 1e9
-    traffic = ncu_traffic("decode_split_kernel")
-    ms_step = total_ms / K
+    r = measure_decode(args.workload, K, Wm, seed, dev, pg)
+    total_ms = max_over_ranks(r["total_ms"])
+    e2e_ms = max_over_ranks(r["e2e_ms"])
+    dec_ms = max_over_ranks(r["dec_ms"])
+    app_ms = max_over_ranks(r["app_ms"])
+    B = r["B"]
+    wl = r["wl"]
+    achieved = r["dec_bytes"] / (dec_ms * 1e-3) / 1e9
     value = world * B * K / (total_ms * 1e-3)
-    e2e_val = world * B * Ke / (e2e_ms * 1e-3)
-
+    lens = wl.lens
+    ctx = (f"{int(lens[0]) + 1}..{int(lens[0]) + 64}" if r["aligned"] and lens.min() == lens.max()
+           else f"{int(lens.min()) + 1}..{int(lens.max()) + 1} (sum {int(lens.sum()) + len(lens)})")
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
-            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "int4 codes, fp32 math", "data": "synthetic (seeded generator in HBM)",
-            "config": {"workload": "llama2-7b-layer", "B": B, "H": H, "D": D, "context": f"{L + 1}..{L + NS}",
-                       "format": "int4-b64", "step": "append 1 token + decode attention",
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": ("int4" if wl.fmt == 0 else "int8") + " codes, fp32 math",
+            "data": "synthetic (seeded generator in HBM)",
+            "config": {"workload": args.workload, "B": B, "H": r["H"], "D": r["D"], "context": ctx,
+                       "format": "int4-b64" if wl.fmt == 0 else "int8-page",
+                       "step": "append 1 token + decode attention",
                        "parallelism": f"replicas x{world} (sequence-sharded, no collective)",
-                       "l2": "inputs larger than L2 (270 MB of codes vs 129 MB)"},
-            "kv_gb_per_s": dec_bytes / (dec_mean * 1e-3) / 1e9,
-            "decode_us": dec_mean * 1e3, "append_us": app_mean * 1e3,
+                       "l2": "inputs larger than L2" if r["dec_bytes"] > 129e6 else "fits in L2 (no flush)"},
+            "kv_gb_per_s": achieved, "decode_us": dec_ms * 1e3, "append_us": app_ms * 1e3,
             "roofline": {"kernel": "kvq_decode_attention (split + merge launches)", "bound": "hbm",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": dec_bytes},
-            "e2e": {"value": e2e_val, "unit": "tokens/s",
-                    "h2d_bytes_per_step": 3 * B * H * D * 2, "d2h_bytes_per_step": B * H * D * 2},
-            "gpu_launches": 3 * K,
-            "clocks": clocks.summary()}
+                         "frac": achieved / peak, "traffic": ncu_traffic("decode_split_kernel"),
+                         "algorithmic_bytes_per_launch": r["dec_bytes"]},
+            "e2e": {"value": world * B * r["Ke"] / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": r["launches"], "clocks": r["clocks"]}
+    if args.extras and args.workload == "llama2-7b-layer":
+        q = measure_prefill(5, 2, seed, dev, args.prefill_seqs)
+        qms = max_over_ranks(q["ms"])
+        qg = q["bytes"] / (qms * 1e-3) / 1e9
+        line["quantize"] = {"workload": "prefill-append", "new_tokens": q["tokens"], "gb_per_s": qg,
+                            "frac": qg / peak, "ms": qms}
     if rank == 0 and not args.no_cpu_baseline:
         rate, cores, desc = oracle_step_rate(args.cpu_seconds, args.seed)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}

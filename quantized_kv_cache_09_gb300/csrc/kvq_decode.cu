@@ -100,33 +100,6 @@ __device__ __forceinline__ void widen_int8(uint32_t w, __half2 c[2])
     c[1] = __hsub2(*reinterpret_cast<const __half2 *>(&b), k1152);
 }
 
-// sum_j q[j] c[j] over the 8 elements of one int4 word; q in element order
-__device__ __forceinline__ float dot8_int4(uint32_t w, const float *q, float acc)
-{
-    __half2 c[4];
-    widen_int4(w, c);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const float2 f = __half22float2(c[i]);
-        acc = fmaf(q[i], f.x, acc);
-        acc = fmaf(q[i + 4], f.y, acc);
-    }
-    return acc;
-}
-
-// acc[j] += p * c[j] over the 8 elements of one int4 word
-__device__ __forceinline__ void axpy8_int4(uint32_t w, float p, float *acc)
-{
-    __half2 c[4];
-    widen_int4(w, c);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const float2 f = __half22float2(c[i]);
-        acc[i] = fmaf(p, f.x, acc[i]);
-        acc[i + 4] = fmaf(p, f.y, acc[i + 4]);
-    }
-}
-
 __device__ __forceinline__ float dot4_int8(uint32_t w, const float *q, float acc)
 {
     __half2 c[2];
@@ -169,6 +142,396 @@ __device__ __forceinline__ float warp_sum(float v)
 __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 __device__ __forceinline__ int units_of(int len, int unit_tok) { return (len + unit_tok - 1) / unit_tok; }
+
+
+// ---------------------------------------------------------------------------
+// Per-format consumers: the math of one unit and the segment epilogue.
+// ---------------------------------------------------------------------------
+template <int FMT>
+struct Consumer;
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
+
+// The masks and magic words of the widening, held in registers: a SASS lop3
+// takes at most one immediate, so (x & mask) ^ magic with both as literals
+// costs two lop3 on the half-rate integer pipe; with both in registers it is
+// one.  The empty asm makes the values opaque so they are not folded back
+// into immediates.
+struct Magic {
+    uint32_t m_lo, m_hi, x_lo, x_hi;  // 0x000f000f, 0x00f000f0, 0x64086408, 0x64806480
+    __device__ __forceinline__ void init()
+    {
+        m_lo = 0x000f000fu;
+        m_hi = 0x00f000f0u;
+        x_lo = 0x64086408u;
+        x_hi = 0x64806480u;
+        asm volatile("" : "+r"(m_lo), "+r"(m_hi), "+r"(x_lo), "+r"(x_hi));
+    }
+};
+
+__device__ __forceinline__ uint32_t lop_and_xor(uint32_t x, uint32_t m, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(d) : "r"(x), "r"(m), "r"(c));  // (x & m) ^ c
+    return d;
+}
+
+// low nibble of each 16-bit half -> exact fp16 of its signed value: 1024 + (n ^ 8) - 1032
+__device__ __forceinline__ uint32_t nib_lo(uint32_t x, const Magic &k)
+{
+    const uint32_t a = lop_and_xor(x, k.m_lo, k.x_lo);
+    return h2_bits(__hsub2(*reinterpret_cast<const __half2 *>(&a), __float2half2_rn(1032.0f)));
+}
+
+// bits 4..7 of each 16-bit half -> exact fp16 of its signed value: (1024 + 16 (n ^ 8)) / 16 - 72
+__device__ __forceinline__ uint32_t nib_hi(uint32_t x, const Magic &k)
+{
+    const uint32_t b = lop_and_xor(x, k.m_hi, k.x_hi);
+    return h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&b), __float2half2_rn(0.0625f),
+                           __float2half2_rn(-72.0f)));
+}
+
+// int4 word -> exact fp16 pairs {c0,c4},{c1,c5},{c2,c6},{c3,c7}
+__device__ __forceinline__ void widen_int4_u32(uint32_t w, uint32_t c[4], const Magic &k)
+{
+    const uint32_t hi = w >> 8;
+    c[0] = nib_lo(w, k);
+    c[1] = nib_hi(w, k);
+    c[2] = nib_lo(hi, k);
+    c[3] = nib_hi(hi, k);
+}
+
+// the fp16 pair held by nibble `odd` of each 16-bit half of x (two tokens, one element)
+__device__ __forceinline__ uint32_t nib_pair(uint32_t x, bool odd, const Magic &k)
+{
+    return odd ? nib_hi(x, k) : nib_lo(x, k);
+}
+
+// D += A * B, m16n8k16, fp16 operands, fp32 accumulators
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// a softmax weight as the pair {RN16(p), RN16(p - RN16(p))}: ~22 significant bits
+__device__ __forceinline__ uint32_t hi_lo_pair(float x)
+{
+    const __half hi = __float2half_rn(x);
+    const __half lo = __float2half_rn(x - __half2float(hi));
+    return (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
+}
+
+// int4: both contractions of a unit on the tensor cores (mma.sync m16n8k16),
+// codes widened exactly to fp16 in registers, fp32 accumulation.
+//   QK: A = 16 tokens x 16 head elements of K, B column 0 = q (other columns 0);
+//       lane (g, t) feeds rows g, g+8 from its 16-byte slice (elements 32t..32t+31)
+//       of each token row, so the k index is a fixed permutation of the head
+//       dimension that q's fragment repeats.
+//   PV: A = V^T (16 head elements x 16 tokens): prmt pairs the same element of
+//       two tokens; B = softmax weights, column 0 = RN16(p), column 1 = the
+//       remainder, so p keeps ~22 bits.
+//   Unit = 32 tokens: 2 token tiles for QK, 2 k-tiles for PV, 8 output tiles.
+// The three phases (qk, softmax, pv) are separate so the caller can overlap
+// qk of the next unit with pv of this one.
+template <>
+struct Consumer<KVQ_INT4_B64> {
+    uint32_t qb[8][2];
+    float acc[8][4];
+    float m_run;
+    float l_lane;
+    Magic mk;
+
+    __device__ __forceinline__ void reset()
+    {
+        mk.init();
+        m_run = -INFINITY;
+        l_lane = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) acc[i][j] = 0.0f;
+    }
+
+    __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + 32 * t);
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const uint4 v = q4[m];  // elements 32t + 8m .. +7 as pairs (0,1) (2,3) (4,5) (6,7)
+            const bool on = g == 0;
+            qb[2 * m][0] = on ? __byte_perm(v.x, v.z, 0x5410) : 0u;      // {e0, e4}
+            qb[2 * m][1] = on ? __byte_perm(v.x, v.z, 0x7632) : 0u;      // {e1, e5}
+            qb[2 * m + 1][0] = on ? __byte_perm(v.y, v.w, 0x5410) : 0u;  // {e2, e6}
+            qb[2 * m + 1][1] = on ? __byte_perm(v.y, v.w, 0x7632) : 0u;  // {e3, e7}
+        }
+    }
+
+    // raw dot products q . c of tokens g, g+8, 16+g, 24+g (valid in lanes with t == 0)
+    __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[4]) const
+    {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int tau = 0; tau < 2; tau++) {
+            float c0[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float c1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint4 wa = *reinterpret_cast<const uint4 *>(ks + (16 * tau + g) * 64 + 16 * t);
+            const uint4 wb = *reinterpret_cast<const uint4 *>(ks + (16 * tau + g + 8) * 64 + 16 * t);
+            const uint32_t ua[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t ub[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                uint32_t ca[4], cb[4];
+                widen_int4_u32(ua[m], ca, mk);
+                widen_int4_u32(ub[m], cb, mk);
+                float(&c)[4] = (m & 1) ? c1 : c0;
+                mma16816(c, ca[0], cb[0], ca[1], cb[1], qb[2 * m][0], qb[2 * m][1]);
+                mma16816(c, ca[2], cb[2], ca[3], cb[3], qb[2 * m + 1][0], qb[2 * m + 1][1]);
+            }
+            sc[2 * tau] = c0[0] + c1[0];
+            sc[2 * tau + 1] = c0[2] + c1[2];
+        }
+    }
+
+    // online softmax over the unit's scores; pf[i] = {hi, lo} fp16 of p_i * sv
+    __device__ __forceinline__ void softmax(const float sc[4], int ntok, float fac, float sv, int lane,
+                                            uint32_t pf[4])
+    {
+        const int g = lane >> 2, t = lane & 3;
+        float s2[4];
+        float lm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int tok = 16 * (i >> 1) + g + 8 * (i & 1);
+            s2[i] = (t == 0 && tok < ntok) ? sc[i] * fac : -INFINITY;
+            lm = fmaxf(lm, s2[i]);
+        }
+        if (__any_sync(kFull, lm > m_run)) {  // the running maximum moves: rescale
+            const float mu = warp_max(lm);
+            const float alpha = ex2_approx(m_run - mu);
+            l_lane *= alpha;
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+                for (int j = 0; j < 4; j++) acc[i][j] *= alpha;
+            m_run = mu;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float pe = ex2_approx(s2[i] - m_run);
+            l_lane += pe;
+            pf[i] = hi_lo_pair(pe * sv);
+        }
+    }
+
+    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t pf[4], int lane)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        // column 0 of B takes the hi halves, column 1 the lo halves, other columns 0
+        const uint32_t sel = (g == 0) ? 0x5410u : 0x7632u;
+#pragma unroll
+        for (int kap = 0; kap < 2; kap++) {
+            // weights of tokens 16kap + {2t, 2t+1, 2t+8, 2t+9} from the lanes that scored them
+            const uint32_t ua = __shfl_sync(kFull, pf[2 * kap], 8 * t);
+            const uint32_t ub = __shfl_sync(kFull, pf[2 * kap], 8 * t + 4);
+            const uint32_t uc = __shfl_sync(kFull, pf[2 * kap + 1], 8 * t);
+            const uint32_t ud = __shfl_sync(kFull, pf[2 * kap + 1], 8 * t + 4);
+            const uint32_t b0 = g < 2 ? __byte_perm(ua, ub, sel) : 0u;
+            const uint32_t b1 = g < 2 ? __byte_perm(uc, ud, sel) : 0u;
+#pragma unroll
+            for (int R = 0; R < 2; R++) {
+                // word 8R + g (elements 64R + 8g .. +7) of tokens 16kap + 2t, +1, +8, +9
+                const uint8_t *vb = vs + (16 * kap + 2 * t) * 64 + 4 * (8 * R + g);
+                const uint32_t wa = *reinterpret_cast<const uint32_t *>(vb);
+                const uint32_t wb = *reinterpret_cast<const uint32_t *>(vb + 64);
+                const uint32_t wc = *reinterpret_cast<const uint32_t *>(vb + 8 * 64);
+                const uint32_t wd = *reinterpret_cast<const uint32_t *>(vb + 9 * 64);
+                uint32_t xab[4], xcd[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    // selector nibbles: result bytes = [wa.k, wa.k, wb.k, wb.k]
+                    const uint32_t bsel = (uint32_t)k | ((uint32_t)k << 4) | ((uint32_t)(4 + k) << 8) |
+                                          ((uint32_t)(4 + k) << 12);
+                    xab[k] = __byte_perm(wa, wb, bsel);
+                    xcd[k] = __byte_perm(wc, wd, bsel);
+                }
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++) {
+                    const bool odd = jj & 1;
+                    mma16816(acc[4 * R + jj], nib_pair(xab[jj >> 1], odd, mk), nib_pair(xab[2 + (jj >> 1)], odd, mk),
+                             nib_pair(xcd[jj >> 1], odd, mk), nib_pair(xcd[2 + (jj >> 1)], odd, mk), b0, b1);
+                }
+            }
+        }
+    }
+
+    // out row (final) or partial slot: lanes with t == 0 hold elements
+    // 64R + 8g + e (e < 4: tile 4R+e rows g; e >= 4: tile 4R+e-4 rows g+8)
+    __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
+    {
+        const float l = warp_sum(l_lane);
+        const int g = lane >> 2, t = lane & 3;
+        if (t != 0) return;
+#pragma unroll
+        for (int R = 0; R < 2; R++) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                v[e] = acc[4 * R + e][0] + acc[4 * R + e][1];
+                v[4 + e] = acc[4 * R + e][2] + acc[4 * R + e][3];
+            }
+            if (orow) {
+                const float inv = 1.0f / l;
+                uint4 o;
+                o.x = h2_bits(__floats2half2_rn(v[0] * inv, v[1] * inv));
+                o.y = h2_bits(__floats2half2_rn(v[2] * inv, v[3] * inv));
+                o.z = h2_bits(__floats2half2_rn(v[4] * inv, v[5] * inv));
+                o.w = h2_bits(__floats2half2_rn(v[6] * inv, v[7] * inv));
+                *reinterpret_cast<uint4 *>(orow + 64 * R + 8 * g) = o;
+            } else {
+                float4 *d4 = reinterpret_cast<float4 *>(part + 4 + 64 * R + 8 * g);
+                d4[0] = make_float4(v[0], v[1], v[2], v[3]);
+                d4[1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+        }
+        if (part && lane == 0) {
+            part[0] = m_run;
+            part[1] = l;
+        }
+    }
+};
+
+// int8: CUDA-core path.  K: lane = (token group g = lane >> 3, 16-element
+// chunk r = lane & 7), 4 passes of 4 tokens, reduce-scatter over the 8 lanes of
+// a token; V: lane = (16-element chunk, token subset), weights shuffled from
+// the lanes that scored them.
+template <>
+struct Consumer<KVQ_INT8_PAGE> {
+    float qf[16];
+    float acc[16];
+    float m_run;
+    float l_lane;
+
+    __device__ __forceinline__ void reset()
+    {
+        m_run = -INFINITY;
+        l_lane = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; i++) acc[i] = 0.0f;
+    }
+
+    __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
+    {
+        const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + (lane & 7) * 16);
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const uint4 v = q4[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+                qf[8 * i + 2 * k] = f.x;
+                qf[8 * i + 2 * k + 1] = f.y;
+            }
+        }
+    }
+
+    // sc[0]: the raw dot product of this lane's token (lanes l and l ^ 4 share one)
+    __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[4]) const
+    {
+        constexpr int RB = 128;
+        const int g = lane >> 3, r = lane & 7;
+        float P[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(ks + (4 * k + g) * RB + r * 16);
+            float a = 0.0f;
+            a = dot4_int8(w.x, qf + 0, a);
+            a = dot4_int8(w.y, qf + 4, a);
+            a = dot4_int8(w.z, qf + 8, a);
+            a = dot4_int8(w.w, qf + 12, a);
+            P[k] = a;
+        }
+        const bool o1 = r & 1;
+        float k0 = o1 ? P[2] : P[0], k1 = o1 ? P[3] : P[1];
+        const float s0 = o1 ? P[0] : P[2], s1 = o1 ? P[1] : P[3];
+        k0 += __shfl_xor_sync(kFull, s0, 1);
+        k1 += __shfl_xor_sync(kFull, s1, 1);
+        const bool o2 = r & 2;
+        const float x = (o2 ? k1 : k0) + __shfl_xor_sync(kFull, o2 ? k0 : k1, 2);
+        sc[0] = x + __shfl_xor_sync(kFull, x, 4);
+    }
+
+    __device__ __forceinline__ void softmax(const float sc[4], int ntok, float fac, float sv, int lane,
+                                            uint32_t pf[4])
+    {
+        const int g = lane >> 3, r = lane & 7;
+        const int tok = 4 * (2 * (r & 1) + ((r >> 1) & 1)) + g;
+        const float s2 = (tok < ntok) ? sc[0] * fac : -INFINITY;
+        if (__any_sync(kFull, s2 > m_run)) {
+            const float mu = warp_max(s2);
+            const float alpha = ex2_approx(m_run - mu);
+            l_lane *= alpha;
+#pragma unroll
+            for (int i = 0; i < 16; i++) acc[i] *= alpha;
+            m_run = mu;
+        }
+        const float pe = ex2_approx(s2 - m_run);
+        l_lane += (lane & 4) ? 0.0f : pe;  // each token is held by two lanes
+        pf[0] = __float_as_uint(pe * sv);
+    }
+
+    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t pf[4], int lane)
+    {
+        constexpr int RB = 128;
+        const float pv = __uint_as_float(pf[0]);
+        const int vc = lane & 7, ts = lane >> 3;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int tv = 4 * j + ts;
+            const int src = ts * 8 + ((j & 1) << 1) + (j >> 1);
+            const float pt = __shfl_sync(kFull, pv, src);
+            const uint4 w = *reinterpret_cast<const uint4 *>(vs + tv * RB + vc * 16);
+            axpy4_int8(w.x, pt, acc);
+            axpy4_int8(w.y, pt, acc + 4);
+            axpy4_int8(w.z, pt, acc + 8);
+            axpy4_int8(w.w, pt, acc + 12);
+        }
+    }
+
+    __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
+    {
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            acc[i] += __shfl_xor_sync(kFull, acc[i], 8);
+            acc[i] += __shfl_xor_sync(kFull, acc[i], 16);
+        }
+        const float l = warp_sum(l_lane);
+        const int vc = lane & 7;
+        if (lane >= 8) return;
+        if (orow) {
+            const float inv = 1.0f / l;
+            uint32_t hw[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) hw[i] = h2_bits(__floats2half2_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv));
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + vc * 16);
+            dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        } else {
+            if (lane == 0) {
+                part[0] = m_run;
+                part[1] = l;
+            }
+            float4 *d4 = reinterpret_cast<float4 *>(part + 4 + vc * 16);
+#pragma unroll
+            for (int i = 0; i < 4; i++) d4[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        }
+    }
+};
 
 template <int FMT>
 __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
@@ -244,7 +607,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
     }
     __syncwarp();
 
-    // ---- issue cursor: unit xi = (ib, ih, ic) ----
+    // ---- issue cursor: unit x0 + ni = (ib, ih, ic) ----
     int ib, ih, ic;
     {
         int lo = 0, hi = B - 1;
@@ -258,14 +621,18 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
         ih = off / n;
         ic = off % n;
     }
+    int inb = units_of(s_len[ib], UT);  // units of the issue cursor's sequence
     // page ring: lane l holds page slot ring_j0 + l of (ring_b, ring_h)
     int ring_b = -1, ring_h = -1, ring_j0 = 0;
     int r_page = 0;
     float r_sk = 0.0f, r_sv = 0.0f;
+    const int N = (int)(x1 - x0);  // units of this warp
+    constexpr uint32_t kPageBytes = kPage * RB;
 
-    auto issue = [&](int64_t xi, int s) {
+    auto issue = [&](int ni) {
+        const int s = ni & (kStages - 1);
         const int j = ic / UPP;
-        if (ib != ring_b || ih != ring_h || j < ring_j0 || j >= ring_j0 + 32) {
+        if (ib != ring_b || ih != ring_h || j >= ring_j0 + 32) {
             ring_b = ib;
             ring_h = ih;
             ring_j0 = j;
@@ -289,225 +656,110 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
         const int pg = __shfl_sync(kFull, r_page, j - ring_j0);
         const float sk = __shfl_sync(kFull, r_sk, j - ring_j0);
         const float sv = __shfl_sync(kFull, r_sv, j - ring_j0);
-        const bool new_seg = (xi == x0) || (ic == 0);
+        const bool new_seg = (ni == 0) || (ic == 0);
         if (lane == 0) {
-            StageMeta &mt = ws.meta[s];
-            mt.b = ib;
-            mt.h = ih;
-            mt.c = ic;
-            mt.ntok = min(UT, s_len[ib] - ic * UT);
-            mt.sk = sk;
-            mt.sv = sv;
-            mt.new_seg = new_seg ? 1 : 0;
+            const int ntok = min(UT, s_len[ib] - ic * UT);
+            *reinterpret_cast<int4 *>(&ws.meta[s].b) = make_int4(ib, ih, ic, ntok);
+            *reinterpret_cast<float4 *>(&ws.meta[s].sk) =
+                make_float4(sk, sv, __int_as_float(new_seg ? 1 : 0), 0.0f);
             fence_proxy_async_smem();
             const uint32_t bytes = 2 * kUnitBytes + (new_seg ? kHeadDim * 2 : 0);
             mbar_arrive_expect_tx(&ws.full[s], bytes);
-            const int64_t off = ((int64_t)pg * H + ih) * (kPage * RB) + (int64_t)(ic % UPP) * (UT * RB);
+            const size_t off = ((size_t)pg * H + ih) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
             bulk_copy_g2s(ws.k[s], p.k_codes + off, kUnitBytes, &ws.full[s]);
             bulk_copy_g2s(ws.v[s], p.v_codes + off, kUnitBytes, &ws.full[s]);
             if (new_seg)
-                bulk_copy_g2s(ws.q[s], p.q + ((int64_t)ib * H + ih) * kHeadDim, kHeadDim * 2, &ws.full[s]);
+                bulk_copy_g2s(ws.q[s], p.q + ((size_t)ib * H + ih) * kHeadDim, kHeadDim * 2, &ws.full[s]);
         }
         // advance the cursor
-        if (++ic == units_of(s_len[ib], UT)) {
+        if (++ic == inb) {
             ic = 0;
             if (++ih == H) {
                 ih = 0;
                 ++ib;
                 while (ib < B && s_len[ib] == 0) ++ib;
+                if (ib < B) inb = units_of(s_len[ib], UT);
             }
         }
     };
 
-    int64_t xi = x0;
-    for (int s = 0; s < kStages && xi < x1; s++, xi++) issue(xi, s);
+    int ni = 0;  // next unit to issue (relative to x0)
+    for (; ni < kStages && ni < N; ni++) issue(ni);
+    __syncwarp();
 
-    // ---- consumer state ----
-    constexpr int QN = (FMT == KVQ_INT4_B64) ? 32 : 16;  // query elements per lane
-    float qf[QN];
-    float acc[16];
-    float m_run = -INFINITY;
-    float l_lane = 0.0f;
+    // ---- consumer: qk of unit n+1 overlaps pv of unit n ----
+    Consumer<FMT> cs;
+    cs.reset();
     int cur_b = -1, cur_h = -1;
-    int64_t seg_x = x0;
-    bool timed_out = false;
+    int seg_n = 0;
 
-    auto flush = [&](int b, int h, int64_t sa, int64_t sb) {
+    auto flush = [&](int b, int h, int na, int nb) {
         const int n = units_of(s_len[b], UT);
         const int64_t u0 = s_cu[b] + (int64_t)h * n;
-        const int64_t u1 = u0 + n;
-#pragma unroll
-        for (int i = 0; i < 16; i++) {
-            acc[i] += __shfl_xor_sync(kFull, acc[i], 8);
-            acc[i] += __shfl_xor_sync(kFull, acc[i], 16);
-        }
-        const float l = warp_sum(l_lane);
-        const int vc = lane & 7;
-        if (sa == u0 && sb == u1) {
-            if (lane < 8) {
-                const float inv = 1.0f / l;
-                uint32_t hw[8];
-#pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    const __half2 t = __floats2half2_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-                    hw[i] = *reinterpret_cast<const uint32_t *>(&t);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((int64_t)b * H + h) * kHeadDim + vc * 16);
-                dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-            }
-        } else {
-            const int slot = (sa == x0) ? 0 : 1;
-            float *dst = p.partials + ((int64_t)gw * 2 + slot) * kPartialStride;
-            if (lane == 0) {
-                dst[0] = m_run;
-                dst[1] = l;
-            }
-            if (lane < 8) {
-                float4 *d4 = reinterpret_cast<float4 *>(dst + 4 + vc * 16);
-#pragma unroll
-                for (int i = 0; i < 4; i++) d4[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-            }
+        const int64_t sa = x0 + na, sb = x0 + nb;
+        if (sa == u0 && sb == u0 + n) {
+            cs.finish(lane, p.out + ((int64_t)b * H + h) * kHeadDim, nullptr);
+        } else {  // cut by a range boundary: the first segment of the warp goes to slot 0, the last to slot 1
+            cs.finish(lane, nullptr, p.partials + ((int64_t)gw * 2 + (na == 0 ? 0 : 1)) * kPartialStride);
         }
     };
+    auto drain = [&](int from) {  // after a timeout: let the copies still in flight land
+        for (int y = from; y < ni; y++)
+            mbar_wait_bounded(&ws.full[y & (kStages - 1)], (uint32_t)((y / kStages) & 1));
+    };
 
-    for (int64_t x = x0; x < x1; x++) {
-        const int s = (int)((x - x0) % kStages);
-        const uint32_t parity = (uint32_t)(((x - x0) / kStages) & 1);
-        if (!mbar_wait_bounded(&ws.full[s], parity)) {
-            if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
-            // let the copies still in flight land before the warp leaves
-            for (int64_t y = x + 1; y < xi; y++) {
-                const int s2 = (int)((y - x0) % kStages);
-                mbar_wait_bounded(&ws.full[s2], (uint32_t)(((y - x0) / kStages) & 1));
+    // unit 0
+    if (!mbar_wait_bounded(&ws.full[0], 0u)) {
+        if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
+        drain(1);
+        return;
+    }
+    int4 mi = *reinterpret_cast<const int4 *>(&ws.meta[0].b);
+    float4 mf = *reinterpret_cast<const float4 *>(&ws.meta[0].sk);
+    cur_b = mi.x;
+    cur_h = mi.y;
+    cs.load_q(ws.q[0], lane);
+    float sc[4];
+    uint32_t pf[4];
+    cs.qk(ws.k[0], lane, sc);
+    cs.softmax(sc, mi.w, mf.x * p.score_scale, mf.y, lane, pf);
+
+    for (int n = 0; n < N; n++) {
+        const int s = n & (kStages - 1);
+        const bool more = n + 1 < N;
+        int4 mi1 = make_int4(0, 0, 0, 0);
+        float4 mf1 = make_float4(0.f, 0.f, 0.f, 0.f);
+        float sc1[4];
+        if (more) {
+            const int s1 = (n + 1) & (kStages - 1);
+            if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((n + 1) / kStages) & 1))) {
+                if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
+                drain(n + 2);
+                return;
             }
-            timed_out = true;
-            break;
+            mi1 = *reinterpret_cast<const int4 *>(&ws.meta[s1].b);
+            mf1 = *reinterpret_cast<const float4 *>(&ws.meta[s1].sk);
+            if (__float_as_int(mf1.z)) cs.load_q(ws.q[s1], lane);
+            cs.qk(ws.k[s1], lane, sc1);  // unit n+1: independent of the pv below
         }
-        const StageMeta mt = ws.meta[s];
-        if (mt.new_seg) {
-            if (cur_b >= 0) flush(cur_b, cur_h, seg_x, x);
-            cur_b = mt.b;
-            cur_h = mt.h;
-            seg_x = x;
-            m_run = -INFINITY;
-            l_lane = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; i++) acc[i] = 0.0f;
-            // this lane's query slice: dims (lane & 3) * 32 .. +32 (int4) or (lane & 7) * 16 .. +16 (int8)
-            const int q0 = (FMT == KVQ_INT4_B64) ? (lane & 3) * 32 : (lane & 7) * 16;
-            const uint4 *qs = reinterpret_cast<const uint4 *>(ws.q[s] + q0);
-#pragma unroll
-            for (int i = 0; i < QN / 8; i++) {
-                const uint4 v = qs[i];
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
-                    qf[8 * i + 2 * k] = f.x;
-                    qf[8 * i + 2 * k + 1] = f.y;
-                }
-            }
-        }
-        const uint8_t *ks = ws.k[s];
-        const uint8_t *vs = ws.v[s];
-        float score;
-        int tok;
-        if constexpr (FMT == KVQ_INT4_B64) {
-            // K: lane -> token group g = lane >> 2, 32-dim chunk r = lane & 3; pass k covers token 8k + g
-            const int g = lane >> 2, r = lane & 3;
-            float P[4];
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(ks + (8 * k + g) * RB + r * 16);
-                float a = 0.0f;
-                a = dot8_int4(w.x, qf + 0, a);
-                a = dot8_int4(w.y, qf + 8, a);
-                a = dot8_int4(w.z, qf + 16, a);
-                a = dot8_int4(w.w, qf + 24, a);
-                P[k] = a;
-            }
-            // reduce-scatter over the 4 lanes of a token group: lane keeps pass 2 (r & 1) + (r >> 1)
-            const bool o1 = r & 1;
-            float k0 = o1 ? P[2] : P[0], k1 = o1 ? P[3] : P[1];
-            const float s0 = o1 ? P[0] : P[2], s1 = o1 ? P[1] : P[3];
-            k0 += __shfl_xor_sync(kFull, s0, 1);
-            k1 += __shfl_xor_sync(kFull, s1, 1);
-            const bool o2 = r & 2;
-            score = (o2 ? k1 : k0) + __shfl_xor_sync(kFull, o2 ? k0 : k1, 2);
-            tok = 8 * (2 * (r & 1) + (r >> 1)) + g;
-        } else {
-            // K: lane -> token group g = lane >> 3, 16-dim chunk r = lane & 7; pass k covers token 4k + g
-            const int g = lane >> 3, r = lane & 7;
-            float P[4];
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(ks + (4 * k + g) * RB + r * 16);
-                float a = 0.0f;
-                a = dot4_int8(w.x, qf + 0, a);
-                a = dot4_int8(w.y, qf + 4, a);
-                a = dot4_int8(w.z, qf + 8, a);
-                a = dot4_int8(w.w, qf + 12, a);
-                P[k] = a;
-            }
-            const bool o1 = r & 1;
-            float k0 = o1 ? P[2] : P[0], k1 = o1 ? P[3] : P[1];
-            const float s0 = o1 ? P[0] : P[2], s1 = o1 ? P[1] : P[3];
-            k0 += __shfl_xor_sync(kFull, s0, 1);
-            k1 += __shfl_xor_sync(kFull, s1, 1);
-            const bool o2 = r & 2;
-            float sc = (o2 ? k1 : k0) + __shfl_xor_sync(kFull, o2 ? k0 : k1, 2);
-            score = sc + __shfl_xor_sync(kFull, sc, 4);  // lanes l and l ^ 4 hold the same token
-            tok = 4 * (2 * (r & 1) + ((r >> 1) & 1)) + g;
-        }
-        const float s2 = (tok < mt.ntok) ? score * (mt.sk * p.score_scale) : -INFINITY;
-        const float mu = warp_max(s2);
-        if (mu > m_run) {
-            const float alpha = ex2_approx(m_run - mu);
-            l_lane *= alpha;
-#pragma unroll
-            for (int i = 0; i < 16; i++) acc[i] *= alpha;
-            m_run = mu;
-        }
-        const float pe = ex2_approx(s2 - m_run);
-        if constexpr (FMT == KVQ_INT4_B64) {
-            l_lane += pe;
-        } else {
-            l_lane += (lane & 4) ? 0.0f : pe;  // each token is held by two lanes
-        }
-        const float pv = pe * mt.sv;
-        // V: lane -> 16-dim chunk vc = lane & 7, token subset ts = lane >> 3
-        const int vc = lane & 7, ts = lane >> 3;
-        if constexpr (FMT == KVQ_INT4_B64) {
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const int t = 4 * j + ts;
-                const int src = (4 * (j & 1) + ts) * 4 + (((j >> 1) & 1) << 1) + (j >> 2);
-                const float pt = __shfl_sync(kFull, pv, src);
-                const uint2 w = *reinterpret_cast<const uint2 *>(vs + t * RB + vc * 8);
-                axpy8_int4(w.x, pt, acc);
-                axpy8_int4(w.y, pt, acc + 8);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int t = 4 * j + ts;
-                const int src = ts * 8 + ((j & 1) << 1) + (j >> 1);
-                const float pt = __shfl_sync(kFull, pv, src);
-                const uint4 w = *reinterpret_cast<const uint4 *>(vs + t * RB + vc * 16);
-                axpy4_int8(w.x, pt, acc);
-                axpy4_int8(w.y, pt, acc + 4);
-                axpy4_int8(w.z, pt, acc + 8);
-                axpy4_int8(w.w, pt, acc + 12);
-            }
-        }
+        cs.pv(ws.v[s], pf, lane);        // unit n
         __syncwarp();
-        if (xi < x1) {
-            issue(xi, s);
-            ++xi;
+        if (ni < N) {                    // stage s is free: refill it with unit n + kStages
+            issue(ni);
+            ++ni;
+        }
+        if (more) {
+            if (__float_as_int(mf1.z)) {  // unit n+1 starts a new (sequence, head)
+                flush(cur_b, cur_h, seg_n, n + 1);
+                cs.reset();
+                cur_b = mi1.x;
+                cur_h = mi1.y;
+                seg_n = n + 1;
+            }
+            cs.softmax(sc1, mi1.w, mf1.x * p.score_scale, mf1.y, lane, pf);
         }
     }
-    if (!timed_out && cur_b >= 0) flush(cur_b, cur_h, seg_x, x1);
+    flush(cur_b, cur_h, seg_n, N);
 }
 
 // one warp per (sequence, head): combine the split partials of a (sequence,
@@ -533,24 +785,35 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, int g
     const int64_t gf = ((u0 + 1) * G - 1) / U;
     const int64_t gl = (u1 * G - 1) / U;
     if (gf == gl) return;  // written whole by the split kernel
-    float M = -INFINITY;
-    for (int64_t g = gf; g <= gl; g++) {
+    // the partial of warp g: slot 1 when (b, h) starts inside g's range, else slot 0
+    auto part = [&](int64_t g) {
         const int slot = (g == gf && (U * g / G) != u0) ? 1 : 0;
-        M = fmaxf(M, p.partials[(g * 2 + slot) * kPartialStride]);
-    }
+        return p.partials + (g * 2 + slot) * kPartialStride;
+    };
+    float M = -INFINITY;
+    for (int64_t g = gf + lane; g <= gl; g += 32) M = fmaxf(M, part(g)[0]);
+    M = warp_max(M);
     float L = 0.0f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t g = gf; g <= gl; g++) {
-        const int slot = (g == gf && (U * g / G) != u0) ? 1 : 0;
-        const float *src = p.partials + (g * 2 + slot) * kPartialStride;
-        const float wgt = ex2_approx(src[0] - M);
-        L += src[1] * wgt;
-        const float4 a = reinterpret_cast<const float4 *>(src + 4)[lane];
-        o.x += a.x * wgt;
-        o.y += a.y * wgt;
-        o.z += a.z * wgt;
-        o.w += a.w * wgt;
+    for (int64_t g0 = gf; g0 <= gl; g0 += 32) {
+        const int64_t gm = g0 + lane;
+        float wl = 0.0f;
+        if (gm <= gl) {
+            const float *src = part(gm);
+            wl = ex2_approx(src[0] - M);
+            L += src[1] * wl;
+        }
+        const int cnt = (int)((gl - g0 + 1) < 32 ? (gl - g0 + 1) : 32);
+        for (int i = 0; i < cnt; i++) {
+            const float wgt = __shfl_sync(kFull, wl, i);
+            const float4 a = reinterpret_cast<const float4 *>(part(g0 + i) + 4)[lane];
+            o.x += a.x * wgt;
+            o.y += a.y * wgt;
+            o.z += a.z * wgt;
+            o.w += a.w * wgt;
+        }
     }
+    L = warp_sum(L);
     const float inv = 1.0f / L;
     const __half2 lo = __floats2half2_rn(o.x * inv, o.y * inv);
     const __half2 hi = __floats2half2_rn(o.z * inv, o.w * inv);
