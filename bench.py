@@ -61,6 +61,26 @@ def dist_env():
     return world, rank, local
 
 
+def rank_seed(base_seed, rank):
+    """Weak scaling: every rank runs its own batch, drawn with its own seed."""
+    return int(base_seed) + int(rank)
+
+
+def max_over_ranks(pg, x, device):
+    """The slowest rank's time (every rank gets it); x unchanged without a group."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, seconds):
+    """Units all ranks processed per second of the slowest rank."""
+    return world * units_per_rank / seconds
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -402,22 +422,15 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
-    seed = args.seed + rank
+    seed = rank_seed(args.seed, rank)
     peak, peak_kind = measured_peak()
-
-    def max_over_ranks(x):
-        if not pg:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        return float(t.item())
 
     K, Wm = args.steps, args.warmup
     if args.workload == "prefill-append":
         r = measure_prefill(K, max(Wm, 1), seed, dev, args.prefill_seqs)
-        ms = max_over_ranks(r["ms"])
+        ms = max_over_ranks(pg, r["ms"], dev)
         gbs = r["bytes"] / (ms * 1e-3) / 1e9
-        line = {"metric": METRIC, "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        line = {"metric": METRIC, "value": whole_job_rate(world, r["bytes"] / 1e9, ms * 1e-3), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm,
                 "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "fp16 in, int4 codes out, fp32 math", "data": "synthetic (seeded generator in HBM)",
                 "config": {"workload": "prefill-append", "new_tokens": r["tokens"], "H": 32, "D": 128,
@@ -433,14 +446,14 @@ def run_ours(args):
         return
 
     r = measure_decode(args.workload, K, Wm, seed, dev, pg)
-    total_ms = max_over_ranks(r["total_ms"])
-    e2e_ms = max_over_ranks(r["e2e_ms"])
-    dec_ms = max_over_ranks(r["dec_ms"])
-    app_ms = max_over_ranks(r["app_ms"])
+    total_ms = max_over_ranks(pg, r["total_ms"], dev)
+    e2e_ms = max_over_ranks(pg, r["e2e_ms"], dev)
+    dec_ms = max_over_ranks(pg, r["dec_ms"], dev)
+    app_ms = max_over_ranks(pg, r["app_ms"], dev)
     B = r["B"]
     wl = r["wl"]
     achieved = r["dec_bytes"] / (dec_ms * 1e-3) / 1e9
-    value = world * B * K / (total_ms * 1e-3)
+    value = whole_job_rate(world, B * K, total_ms * 1e-3)
     lens = wl.lens
     ctx = (f"{int(lens[0]) + 1}..{int(lens[0]) + 64}" if r["aligned"] and lens.min() == lens.max()
            else f"{int(lens.min()) + 1}..{int(lens.max()) + 1} (sum {int(lens.sum()) + len(lens)})")
@@ -458,12 +471,12 @@ def run_ours(args):
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": ncu_traffic("decode_split_kernel"),
                          "algorithmic_bytes_per_launch": r["dec_bytes"]},
-            "e2e": {"value": world * B * r["Ke"] / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": whole_job_rate(world, B * r["Ke"], e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": r["launches"], "clocks": r["clocks"]}
     if args.extras and args.workload == "llama2-7b-layer":
         q = measure_prefill(5, 2, seed, dev, args.prefill_seqs)
-        qms = max_over_ranks(q["ms"])
+        qms = max_over_ranks(pg, q["ms"], dev)
         qg = q["bytes"] / (qms * 1e-3) / 1e9
         line["quantize"] = {"workload": "prefill-append", "new_tokens": q["tokens"], "gb_per_s": qg,
                             "frac": qg / peak, "ms": qms}

@@ -3,20 +3,24 @@
 // aicoding.csdn.net section 2.2), for a contiguous tensor and for appends into
 // the paged cache.
 //
-// One warp owns one (block, head): 64 rows x 128 fp16 = 16 KiB, read once from
-// HBM with 16-byte loads into registers (lane = row parity x 16-byte chunk, so
-// each warp load covers two whole 256-byte rows), reduced to max|x| with packed
-// half2 max and one warp redux, then quantized from registers and stored as
-// whole rows of codes.  The pages' two-pass design (an extrema pass, then an
-// elementwise kernel) becomes a single pass with one HBM read.
+// One warp owns one (block, head): 64 rows x 128 fp16 = 16 KiB.  Its lanes
+// stage the rows in shared memory with 16-byte cp.async copies (lane = row
+// parity x 16-byte chunk, so each warp copy covers two whole 256-byte rows;
+// rows past the end are zero-filled), reduce max|x| with packed half2 max and
+// one warp redux, then quantize from shared memory and store whole rows of
+// codes.  The pages' two-pass design (an extrema pass, then an elementwise
+// kernel) becomes one pass over HBM.
 //
 // Exactness: the code must equal clamp(rint(RN(x / scale))).  The fast path
 // multiplies by r = RN(1 / scale); |RN(x*r) - RN(x/scale)| < 1.5 * 2^-23 * |y|,
 // so the rounded integer can differ only when y lies within that distance of a
 // half-integer.  Any group of 8 elements with |y - rint(y)| > 1/2 - eps
 // (eps = 2^-17 for int4, |y| <= 8; 2^-14 for int8, |y| <= 128) is recomputed
-// with the correctly rounded division __fdiv_rn.  Clamping before rounding is
-// safe because the clamp bounds are integers.
+// with the correctly rounded division __fdiv_rn.  Bounds: |x| <= a, so
+// |y| <= 7.5 (1 + 2^-22) for int4 -- only the upper clamp at 7 can act
+// (rint(-7.5) = -8 already), and only when y >= 7.5, which the tie test above
+// always sends to the exact path, so the fast path needs no clamp -- and
+// |y| <= 127 (1 + 2^-22) for int8, where rint never leaves [-127, 127].
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -29,9 +33,7 @@ template <>
 struct Codec<KVQ_INT4_B64> {
     static constexpr int kRowBytes = 64;
     static constexpr float kDiv = 7.5f;
-    static constexpr float kLo = -8.0f;
-    static constexpr float kHi = 7.0f;
-    static constexpr float kMagic = 12582920.0f;      // 1.5 * 2^23 + 8: low nibble = code + 8
+    static constexpr float kMagic = 12582920.0f;       // 1.5 * 2^23 + 8: low nibble = code + 8
     static constexpr float kEps = 7.62939453125e-06f;  // 2^-17
 };
 
@@ -39,109 +41,193 @@ template <>
 struct Codec<KVQ_INT8_PAGE> {
     static constexpr int kRowBytes = 128;
     static constexpr float kDiv = 127.0f;
-    static constexpr float kLo = -127.0f;
-    static constexpr float kHi = 127.0f;
     static constexpr float kMagic = 12583040.0f;       // 1.5 * 2^23 + 128: low byte = code + 128
     static constexpr float kEps = 6.103515625e-05f;    // 2^-14
 };
 
-// quantize 8 fp16 values; m[j] receives the bits of kMagic + code
+constexpr uint32_t kMagicBits = 0x4b400000u;  // bits of 1.5 * 2^23
+
+// ---- packed binary32 pairs (Blackwell f32x2 arithmetic) --------------------
+__device__ __forceinline__ uint64_t pk2(float a, float b)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// fast path for 8 fp16 values: m[j] = bits of RN(RN(x_j * r) + kMagic), and
+// tmax = max(tmax, |y_j - rint(y_j)|) over them
 template <int FMT>
-__device__ __forceinline__ void quant8(const uint4 &v, float r, float scale, uint32_t m[8])
+__device__ __forceinline__ void quant8_fast(const uint4 &v, uint64_t rr, uint32_t m[8], float &tmax)
 {
     using C = Codec<FMT>;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float x[8];
+    const uint64_t magic = pk2(C::kMagic, C::kMagic);
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
+        const uint64_t y = mul2(pk2(f.x, f.y), rr);
+        const uint64_t mf = add2(y, magic);
+        const uint64_t d = sub2(y, sub2(mf, magic));  // y - rint(y), exact
+        float m0, m1, d0, d1;
+        upk2(mf, m0, m1);
+        upk2(d, d0, d1);
+        tmax = fmaxf(tmax, fmaxf(fabsf(d0), fabsf(d1)));
+        m[2 * i] = __float_as_uint(m0);
+        m[2 * i + 1] = __float_as_uint(m1);
     }
-    float tmax = 0.0f;
+}
+
+// exact path for a group of 8 that has a near-tie: per element, keep the fast
+// value unless the element itself is within eps of a half-integer; then an
+// element equal to +-a takes the block's precomputed code (+-ya = RN(a / scale),
+// so the whole block needs one division for its extreme elements), any other
+// takes the correctly rounded quotient.  Codes are clamped here (int4: y may
+// reach 7.5 only in this path).
+template <int FMT>
+__device__ __forceinline__ void quant8_exact(const uint4 &v, uint64_t rr, float scale, float a, float ya,
+                                             uint32_t m[8])
+{
+    using C = Codec<FMT>;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-        const float y = __fmul_rn(x[j], r);
-        const float yc = fminf(fmaxf(y, C::kLo), C::kHi);
-        const float mf = __fadd_rn(yc, C::kMagic);
-        tmax = fmaxf(tmax, fabsf(__fsub_rn(yc, __fsub_rn(mf, C::kMagic))));
-        m[j] = __float_as_uint(mf);
-    }
-    if (tmax > 0.5f - C::kEps) {  // near a rounding tie: take the correctly rounded quotient
+    for (int i = 0; i < 4; i++) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+        const float xs[2] = {f.x, f.y};
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const float y = __fdiv_rn(x[j], scale);
-            const float yc = fminf(fmaxf(y, C::kLo), C::kHi);
-            m[j] = __float_as_uint(__fadd_rn(yc, C::kMagic));
+        for (int e = 0; e < 2; e++) {
+            const float x = xs[e];
+            const float y0 = __fmul_rn(x, __uint_as_float((uint32_t)rr));
+            const float d = y0 - (__fadd_rn(y0, C::kMagic) - C::kMagic);
+            if (fabsf(d) > 0.5f - C::kEps) {
+                float y = fabsf(x) == a ? copysignf(ya, x) : __fdiv_rn(x, scale);
+                if constexpr (FMT == KVQ_INT4_B64) y = fminf(y, 7.0f);
+                m[2 * i + e] = __float_as_uint(__fadd_rn(y, C::kMagic));
+            }
         }
     }
 }
 
+// 8 codes -> one word of 4-bit two's-complement nibbles, element j at bits 4j.
+// m[j] = kMagicBits + (code + 8): Horner in base 16 with integer multiply-adds,
+// minus the accumulated magic, then flip each nibble's top bit.
 __device__ __forceinline__ uint32_t pack8_int4(const uint32_t m[8])
 {
-    uint32_t w = 0;
+    constexpr uint32_t kBias = kMagicBits * 0x11111111u;  // sum_j kMagicBits * 16^j mod 2^32
+    uint32_t acc = m[7];
 #pragma unroll
-    for (int j = 0; j < 8; j++) w |= (m[j] & 0xfu) << (4 * j);
-    return w ^ 0x88888888u;  // offset binary (code + 8) -> two's complement nibbles
+    for (int j = 6; j >= 0; j--) acc = acc * 16u + m[j];
+    return (acc - kBias) ^ 0x88888888u;
 }
 
+// 8 codes -> two words of two's-complement bytes; m[j] = kMagicBits + (code + 128)
 __device__ __forceinline__ uint2 pack8_int8(const uint32_t m[8])
 {
-    uint2 o;
-    o.x = __byte_perm(__byte_perm(m[0], m[1], 0x0040), __byte_perm(m[2], m[3], 0x0040), 0x5410);
-    o.y = __byte_perm(__byte_perm(m[4], m[5], 0x0040), __byte_perm(m[6], m[7], 0x0040), 0x5410);
-    o.x ^= 0x80808080u;  // offset binary (code + 128) -> two's complement bytes
-    o.y ^= 0x80808080u;
-    return o;
+    constexpr uint32_t kBias = kMagicBits * 0x01010101u;
+    uint32_t lo = m[3], hi = m[7];
+#pragma unroll
+    for (int j = 2; j >= 0; j--) {
+        lo = lo * 256u + m[j];
+        hi = hi * 256u + m[4 + j];
+    }
+    return make_uint2((lo - kBias) ^ 0x80808080u, (hi - kBias) ^ 0x80808080u);
 }
 
-// Row pointers of one (block, head) for the contiguous layout x[T][H][D].
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Row sources of one (block, head) for the contiguous layout x[T][H][D].
 struct ContigRows {
-    const uint16_t *base;  // row 0 of the block
+    const uint16_t *base;  // row 0 of the block, head h
     int64_t stride;        // elements between rows (H * D)
-    __device__ __forceinline__ uint4 load(int r, int chunk) const
+    // copy rows 2i + rpar (i < 32) of this lane's 16-byte chunk; rows >= nrows are zero-filled
+    __device__ __forceinline__ void stage(uint32_t s0, int chunk, int rpar, int nrows) const
     {
-        return ld_stream_v4(base + r * stride + 8 * chunk);
+        const uint16_t *src = base + rpar * stride + 8 * chunk;
+        const uint16_t *valid = base + 8 * chunk;
+#pragma unroll 8
+        for (int i = 0; i < 32; i++, src += 2 * stride) {
+            const bool live = 2 * i + rpar < nrows;
+            cp_async16(s0 + (uint32_t)i * (2 * kHeadDim * 2), live ? src : valid, live ? 16u : 0u);
+        }
     }
 };
 
-// Row pointers of one (block, head) of an append: rows before n_old come from
-// the fp16 tail buffer (written by this kernel too, so no read-only path),
-// later rows from the new tokens.
+// Row sources of one (block, head) of an append: rows before n_old come from
+// the fp16 tail buffer, later rows from the new tokens.
 struct AppendRows {
-    const uint16_t *tail;  // tail[b][h] row 0, or nullptr
-    const uint16_t *fresh; // head h of new-token row 0
-    int64_t row0;          // new-token row that would land in block row 0 (negative when n_old > 0)
+    const uint16_t *tail;   // tail[b][h] row 0, or nullptr
+    const uint16_t *fresh;  // head h of new-token row 0
+    int64_t row0;           // new-token row that would land in block row 0 (negative when n_old > 0)
     int n_old;
-    int64_t stride;        // elements between new-token rows (H * D)
-    __device__ __forceinline__ uint4 load(int r, int chunk) const
+    int64_t stride;         // elements between new-token rows (H * D)
+    __device__ __forceinline__ void stage(uint32_t s0, int chunk, int rpar, int nrows) const
     {
-        if (r < n_old) return *reinterpret_cast<const uint4 *>(tail + r * kHeadDim + 8 * chunk);
-        return ld_stream_v4(fresh + (row0 + r) * stride + 8 * chunk);
+        int i = 0;
+        for (; 2 * i + rpar < n_old; i++)  // old rows of the open block
+            cp_async16(s0 + (uint32_t)i * (2 * kHeadDim * 2), tail + (2 * i + rpar) * kHeadDim + 8 * chunk, 16u);
+        const uint16_t *src = fresh + (row0 + 2 * i + rpar) * stride + 8 * chunk;
+        const uint16_t *valid = fresh + (row0 + n_old) * stride + 8 * chunk;  // first new row
+        for (; i < 32; i++, src += 2 * stride) {
+            const bool live = 2 * i + rpar < nrows;
+            cp_async16(s0 + (uint32_t)i * (2 * kHeadDim * 2), live ? src : valid, live ? 16u : 0u);
+        }
     }
 };
 
+constexpr int kQuantWarps = 3;  // 3 x 16 KiB of staging = the 48 KiB static shared-memory limit
+constexpr int kBlockElems = kPage * kHeadDim;  // fp16 elements of one (block, head)
+
+// One (block, head): stage, reduce, quantize, store.  sbuf: 16 KiB of this
+// warp's shared memory.  Only the lane that staged a 16-byte chunk reads it
+// back, so no cross-lane ordering is needed beyond cp.async's own wait.
+// nrows >= 1 (the first valid row is the source address of the zero-fill copies).
 template <int FMT, class Rows>
-__device__ __forceinline__ void quantize_block_warp(const Rows &rows, int nrows, uint8_t *__restrict__ codes,
-                                                    float *__restrict__ scale_out)
+__device__ __forceinline__ void quantize_block_warp(const Rows &rows, int nrows, uint16_t *sbuf,
+                                                    uint8_t *__restrict__ codes, float *__restrict__ scale_out)
 {
     using C = Codec<FMT>;
     const int lane = threadIdx.x & 31;
-    const int chunk = lane & 15;  // dims 8*chunk .. 8*chunk+7
+    const int chunk = lane & 15;  // elements 8*chunk .. 8*chunk+7 of a row
     const int rpar = lane >> 4;   // rows 2i + rpar
-    uint4 v[32];
-#pragma unroll
-    for (int i = 0; i < 32; i++) {
-        const int r = 2 * i + rpar;
-        v[i] = (r < nrows) ? rows.load(r, chunk) : make_uint4(0u, 0u, 0u, 0u);
-    }
+    const uint32_t s0 = smem_addr(sbuf) + (uint32_t)(rpar * kHeadDim + 8 * chunk) * 2u;
+    rows.stage(s0, chunk, rpar, nrows);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+
+    const uint4 *sv = reinterpret_cast<const uint4 *>(sbuf + rpar * kHeadDim + 8 * chunk);
+    constexpr int kStep = 2 * kHeadDim / 8;  // uint4 between rows 2i and 2i + 2
     __half2 mx = __float2half2_rn(0.0f);
-#pragma unroll
+#pragma unroll 8
     for (int i = 0; i < 32; i++) {
-        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v[i].x)));
-        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v[i].y)));
-        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v[i].z)));
-        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v[i].w)));
+        const uint4 v = sv[i * kStep];
+        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v.x)));
+        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v.y)));
+        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v.z)));
+        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v.w)));
     }
     const uint32_t mb = *reinterpret_cast<const uint32_t *>(&mx);
     uint32_t abits = max(mb & 0xffffu, mb >> 16);  // non-negative fp16: bit order = value order
@@ -149,25 +235,25 @@ __device__ __forceinline__ void quantize_block_warp(const Rows &rows, int nrows,
     const float a = __half2float(__ushort_as_half(static_cast<unsigned short>(abits)));
     const float scale = __fdiv_rn(a, C::kDiv);
     if (lane == 0) *scale_out = scale;
-    const bool zero = !(scale > 0.0f);
-    const float r = zero ? 0.0f : __frcp_rn(scale);
-#pragma unroll
-    for (int i = 0; i < 32; i++) {
-        const int row = 2 * i + rpar;
-        const bool live = (row < nrows) && !zero;
+    // rows past nrows are zero in shared memory and quantize to code 0; an
+    // all-zero block has scale 0 and r = 0, so every code is 0 there too
+    const float r = scale > 0.0f ? __frcp_rn(scale) : 0.0f;
+    const float ya = scale > 0.0f ? __fdiv_rn(a, scale) : 0.0f;  // the quotient of the extreme elements
+    const uint64_t rr = pk2(r, r);
+    uint8_t *out = codes + rpar * C::kRowBytes + (FMT == KVQ_INT4_B64 ? 4 : 8) * chunk;
+#pragma unroll 4
+    for (int i = 0; i < 32; i++) {  // rows 2i + rpar
+        const uint4 v = sv[i * kStep];
         uint32_t m[8];
-        if (live) quant8<FMT>(v[i], r, scale, m);
-        if constexpr (FMT == KVQ_INT4_B64) {
-            const uint32_t w = live ? pack8_int4(m) : 0u;
-            *reinterpret_cast<uint32_t *>(codes + row * C::kRowBytes + 4 * chunk) = w;
-        } else {
-            const uint2 w = live ? pack8_int8(m) : make_uint2(0u, 0u);
-            *reinterpret_cast<uint2 *>(codes + row * C::kRowBytes + 8 * chunk) = w;
-        }
+        float tmax = 0.0f;
+        quant8_fast<FMT>(v, rr, m, tmax);
+        if (tmax > 0.5f - C::kEps) quant8_exact<FMT>(v, rr, scale, a, ya, m);  // a near-tie (rare)
+        if constexpr (FMT == KVQ_INT4_B64)
+            *reinterpret_cast<uint32_t *>(out + i * 2 * C::kRowBytes) = pack8_int4(m);
+        else
+            *reinterpret_cast<uint2 *>(out + i * 2 * C::kRowBytes) = pack8_int8(m);
     }
 }
-
-constexpr int kQuantWarps = 4;
 
 template <int FMT>
 __global__ void __launch_bounds__(kQuantWarps * 32)
@@ -175,14 +261,16 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
                            uint8_t *__restrict__ codes, float *__restrict__ scales)
 {
     using C = Codec<FMT>;
-    const int64_t w = (int64_t)blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+    __shared__ __align__(128) uint16_t sbuf[kQuantWarps][kBlockElems];
+    const int warp = threadIdx.x >> 5;
+    const int64_t w = (int64_t)blockIdx.x * kQuantWarps + warp;
     if (w >= nblocks * H) return;
     const int64_t j = w / H;
     const int h = (int)(w % H);
     const int64_t rem = T - j * kPage;
     const int nrows = rem < kPage ? (int)rem : kPage;
     ContigRows rows{x + (j * kPage * H + h) * kHeadDim, (int64_t)H * kHeadDim};
-    quantize_block_warp<FMT>(rows, nrows, codes + (j * H + h) * (int64_t)kPage * C::kRowBytes,
+    quantize_block_warp<FMT>(rows, nrows, sbuf[warp], codes + (j * H + h) * (int64_t)kPage * C::kRowBytes,
                              scales + j * H + h);
 }
 
@@ -192,10 +280,12 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     append_kernel(AppendParams p)
 {
     using C = Codec<FMT>;
+    __shared__ __align__(128) uint16_t sbuf[kQuantWarps][kBlockElems];
     const int b = blockIdx.y;
     const bool is_v = blockIdx.z != 0;
     const int H = p.num_heads;
-    const int wi = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+    const int warp = threadIdx.x >> 5;
+    const int wi = blockIdx.x * kQuantWarps + warp;
     const int lane = threadIdx.x & 31;
     const int c0 = p.cu_seqlens[b];
     const int T = p.cu_seqlens[b + 1] - c0;
@@ -235,7 +325,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         const int nrows = min(kPage, L1 - j * kPage);
         uint8_t *codes = (is_v ? p.v_codes : p.k_codes) + ((int64_t)page * H + h) * kPage * C::kRowBytes;
         float *scale = (is_v ? p.v_scales : p.k_scales) + (int64_t)page * H + h;
-        quantize_block_warp<FMT>(rows, nrows, codes, scale);
+        quantize_block_warp<FMT>(rows, nrows, sbuf[warp], codes, scale);
     }
     // The warp of the first touched block is the only reader of this (b, h)'s
     // tail, so it also writes the new tail rows: no other warp can race with it.
