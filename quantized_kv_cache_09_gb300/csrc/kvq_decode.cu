@@ -552,6 +552,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
     const int B = p.num_seqs;
     const int H = p.num_heads;
     const int max_len = p.max_blocks * kPage;
+    pdl_launch_dependents();
+    pdl_wait();
 
     // ---- per-sequence lengths and the (H x units) prefix, in shared memory ----
     for (int b = tid; b < B; b += blockDim.x) {
@@ -662,7 +664,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
             *reinterpret_cast<int4 *>(&ws.meta[s].b) = make_int4(ib, ih, ic, ntok);
             *reinterpret_cast<float4 *>(&ws.meta[s].sk) =
                 make_float4(sk, sv, __int_as_float(new_seg ? 1 : 0), 0.0f);
-            fence_proxy_async_smem();
+            // The refill of stage s follows the warp's reads of it: every lane
+            // consumed those values (mma operands) before the __syncwarp that
+            // precedes this issue, so the copy cannot overtake them.
             const uint32_t bytes = 2 * kUnitBytes + (new_seg ? kHeadDim * 2 : 0);
             mbar_arrive_expect_tx(&ws.full[s], bytes);
             const size_t off = ((size_t)pg * H + ih) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
@@ -766,6 +770,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
 // head) cut by warp-range boundaries; write zeros for empty sequences
 __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, int grid_warps)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int w = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int B = p.num_seqs, H = p.num_heads;
@@ -785,28 +791,29 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, int g
     const int64_t gf = ((u0 + 1) * G - 1) / U;
     const int64_t gl = (u1 * G - 1) / U;
     if (gf == gl) return;  // written whole by the split kernel
-    // the partial of warp g: slot 1 when (b, h) starts inside g's range, else slot 0
-    auto part = [&](int64_t g) {
-        const int slot = (g == gf && (U * g / G) != u0) ? 1 : 0;
-        return p.partials + (g * 2 + slot) * kPartialStride;
-    };
+    // the partial of warp g: slot 1 for warp gf when (b, h) starts inside its
+    // range (it is that warp's last segment), slot 0 otherwise
+    const int first_slot = ((U * gf) / G != u0) ? 1 : 0;
+    const int cnt_all = (int)(gl - gf + 1);
+    const float *pbase = p.partials + gf * 2 * kPartialStride;
+    auto part = [&](int i) { return pbase + ((int64_t)i * 2 + (i == 0 ? first_slot : 0)) * kPartialStride; };
     float M = -INFINITY;
-    for (int64_t g = gf + lane; g <= gl; g += 32) M = fmaxf(M, part(g)[0]);
+    for (int i = lane; i < cnt_all; i += 32) M = fmaxf(M, part(i)[0]);
     M = warp_max(M);
     float L = 0.0f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t g0 = gf; g0 <= gl; g0 += 32) {
-        const int64_t gm = g0 + lane;
+    for (int i0 = 0; i0 < cnt_all; i0 += 32) {
         float wl = 0.0f;
-        if (gm <= gl) {
-            const float *src = part(gm);
+        if (i0 + lane < cnt_all) {
+            const float *src = part(i0 + lane);
             wl = ex2_approx(src[0] - M);
             L += src[1] * wl;
         }
-        const int cnt = (int)((gl - g0 + 1) < 32 ? (gl - g0 + 1) : 32);
+        const int cnt = min(32, cnt_all - i0);
+#pragma unroll 4
         for (int i = 0; i < cnt; i++) {
             const float wgt = __shfl_sync(kFull, wl, i);
-            const float4 a = reinterpret_cast<const float4 *>(part(g0 + i) + 4)[lane];
+            const float4 a = reinterpret_cast<const float4 *>(part(i0 + i) + 4)[lane];
             o.x += a.x * wgt;
             o.y += a.y * wgt;
             o.z += a.z * wgt;
@@ -862,15 +869,13 @@ cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s)
     const int gw = decode_grid_warps(fmt);
     if (gw <= 0) return cudaErrorInvalidDevice;
     const int ctas = gw / kDecWarps;
-    if (fmt == KVQ_INT4_B64)
-        decode_split_kernel<KVQ_INT4_B64><<<ctas, kDecWarps * 32, kDecSmemBytes, s>>>(p, gw);
-    else
-        decode_split_kernel<KVQ_INT8_PAGE><<<ctas, kDecWarps * 32, kDecSmemBytes, s>>>(p, gw);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = (fmt == KVQ_INT4_B64)
+                        ? launch_pdl(decode_split_kernel<KVQ_INT4_B64>, dim3(ctas), dim3(kDecWarps * 32), kDecSmemBytes, s, p, gw)
+                        : launch_pdl(decode_split_kernel<KVQ_INT8_PAGE>, dim3(ctas), dim3(kDecWarps * 32), kDecSmemBytes, s, p, gw);
     if (e != cudaSuccess) return e;
     const int mblocks = (p.num_seqs * p.num_heads + 3) / 4;
-    if (mblocks > 0) decode_merge_kernel<<<mblocks, 128, 0, s>>>(p, gw);
-    return cudaGetLastError();
+    if (mblocks > 0) e = launch_pdl(decode_merge_kernel, dim3(mblocks), dim3(128), 0, s, p, gw);
+    return e;
 }
 
 }  // namespace kvq

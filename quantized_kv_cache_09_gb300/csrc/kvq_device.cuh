@@ -94,6 +94,20 @@ __device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gsrc, 
         : "memory");
 }
 
+// Programmatic dependent launch.  Every kvq kernel is launched so that it may
+// start while the previous kernel of the stream is still running: it first
+// lets its own dependents launch, does setup that needs only its parameters,
+// and then waits for the previous grid to complete (and its memory to be
+// visible) before it reads or writes any global memory.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;

@@ -58,6 +58,24 @@ constexpr int kPartialStride = 132;
 // sequences per split-kernel launch (the per-CTA prefix lives in shared memory)
 constexpr int kMaxSeqsPerLaunch = 512;
 
+// launch `kernel` with programmatic stream serialization (see pdl_wait)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_quantize(int fmt, const uint16_t *x, int64_t T, int H, uint8_t *codes, float *scales,
                             cudaStream_t s);
 cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s);

@@ -164,13 +164,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
 struct ContigRows {
     const uint16_t *base;  // row 0 of the block, head h
     int64_t stride;        // elements between rows (H * D)
-    // copy rows 2i + rpar (i < 32) of this lane's 16-byte chunk; rows >= nrows are zero-filled
-    __device__ __forceinline__ void stage(uint32_t s0, int chunk, int rpar, int nrows) const
+    // copy rows 2i + rpar (i < npairs) of this lane's 16-byte chunk; rows >= nrows are zero-filled
+    __device__ __forceinline__ void stage(uint32_t s0, int chunk, int rpar, int nrows, int npairs) const
     {
         const uint16_t *src = base + rpar * stride + 8 * chunk;
         const uint16_t *valid = base + 8 * chunk;
 #pragma unroll 8
-        for (int i = 0; i < 32; i++, src += 2 * stride) {
+        for (int i = 0; i < npairs; i++, src += 2 * stride) {
             const bool live = 2 * i + rpar < nrows;
             cp_async16(s0 + (uint32_t)i * (2 * kHeadDim * 2), live ? src : valid, live ? 16u : 0u);
         }
@@ -185,14 +185,14 @@ struct AppendRows {
     int64_t row0;           // new-token row that would land in block row 0 (negative when n_old > 0)
     int n_old;
     int64_t stride;         // elements between new-token rows (H * D)
-    __device__ __forceinline__ void stage(uint32_t s0, int chunk, int rpar, int nrows) const
+    __device__ __forceinline__ void stage(uint32_t s0, int chunk, int rpar, int nrows, int npairs) const
     {
         int i = 0;
         for (; 2 * i + rpar < n_old; i++)  // old rows of the open block
             cp_async16(s0 + (uint32_t)i * (2 * kHeadDim * 2), tail + (2 * i + rpar) * kHeadDim + 8 * chunk, 16u);
         const uint16_t *src = fresh + (row0 + 2 * i + rpar) * stride + 8 * chunk;
         const uint16_t *valid = fresh + (row0 + n_old) * stride + 8 * chunk;  // first new row
-        for (; i < 32; i++, src += 2 * stride) {
+        for (; i < npairs; i++, src += 2 * stride) {
             const bool live = 2 * i + rpar < nrows;
             cp_async16(s0 + (uint32_t)i * (2 * kHeadDim * 2), live ? src : valid, live ? 16u : 0u);
         }
@@ -206,8 +206,11 @@ constexpr int kBlockElems = kPage * kHeadDim;  // fp16 elements of one (block, h
 // warp's shared memory.  Only the lane that staged a 16-byte chunk reads it
 // back, so no cross-lane ordering is needed beyond cp.async's own wait.
 // nrows >= 1 (the first valid row is the source address of the zero-fill copies).
+// Rows 2i + rpar for i < npairs are processed (npairs = 32 writes the whole
+// block, rows past nrows as code 0; a smaller npairs leaves rows >= 2 npairs
+// untouched, which hold the zeros written when the block was first filled).
 template <int FMT, class Rows>
-__device__ __forceinline__ void quantize_block_warp(const Rows &rows, int nrows, uint16_t *sbuf,
+__device__ __forceinline__ void quantize_block_warp(const Rows &rows, int nrows, int npairs, uint16_t *sbuf,
                                                     uint8_t *__restrict__ codes, float *__restrict__ scale_out)
 {
     using C = Codec<FMT>;
@@ -215,14 +218,14 @@ __device__ __forceinline__ void quantize_block_warp(const Rows &rows, int nrows,
     const int chunk = lane & 15;  // elements 8*chunk .. 8*chunk+7 of a row
     const int rpar = lane >> 4;   // rows 2i + rpar
     const uint32_t s0 = smem_addr(sbuf) + (uint32_t)(rpar * kHeadDim + 8 * chunk) * 2u;
-    rows.stage(s0, chunk, rpar, nrows);
+    rows.stage(s0, chunk, rpar, nrows, npairs);
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 
     const uint4 *sv = reinterpret_cast<const uint4 *>(sbuf + rpar * kHeadDim + 8 * chunk);
     constexpr int kStep = 2 * kHeadDim / 8;  // uint4 between rows 2i and 2i + 2
     __half2 mx = __float2half2_rn(0.0f);
 #pragma unroll 8
-    for (int i = 0; i < 32; i++) {
+    for (int i = 0; i < npairs; i++) {
         const uint4 v = sv[i * kStep];
         mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v.x)));
         mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v.y)));
@@ -242,7 +245,7 @@ __device__ __forceinline__ void quantize_block_warp(const Rows &rows, int nrows,
     const uint64_t rr = pk2(r, r);
     uint8_t *out = codes + rpar * C::kRowBytes + (FMT == KVQ_INT4_B64 ? 4 : 8) * chunk;
 #pragma unroll 4
-    for (int i = 0; i < 32; i++) {  // rows 2i + rpar
+    for (int i = 0; i < npairs; i++) {  // rows 2i + rpar
         const uint4 v = sv[i * kStep];
         uint32_t m[8];
         float tmax = 0.0f;
@@ -262,6 +265,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 {
     using C = Codec<FMT>;
     __shared__ __align__(128) uint16_t sbuf[kQuantWarps][kBlockElems];
+    pdl_launch_dependents();
+    pdl_wait();
     const int warp = threadIdx.x >> 5;
     const int64_t w = (int64_t)blockIdx.x * kQuantWarps + warp;
     if (w >= nblocks * H) return;
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     const int64_t rem = T - j * kPage;
     const int nrows = rem < kPage ? (int)rem : kPage;
     ContigRows rows{x + (j * kPage * H + h) * kHeadDim, (int64_t)H * kHeadDim};
-    quantize_block_warp<FMT>(rows, nrows, sbuf[warp], codes + (j * H + h) * (int64_t)kPage * C::kRowBytes,
+    quantize_block_warp<FMT>(rows, nrows, 32, sbuf[warp], codes + (j * H + h) * (int64_t)kPage * C::kRowBytes,
                              scales + j * H + h);
 }
 
@@ -281,6 +286,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 {
     using C = Codec<FMT>;
     __shared__ __align__(128) uint16_t sbuf[kQuantWarps][kBlockElems];
+    pdl_launch_dependents();
+    pdl_wait();
     const int b = blockIdx.y;
     const bool is_v = blockIdx.z != 0;
     const int H = p.num_heads;
@@ -323,9 +330,11 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         // new token index i = 64*j + r - L0 lives at row (c0 + i) of the new-token tensor
         AppendRows rows{tail_bh, src + (int64_t)h * kHeadDim, (int64_t)c0 + (int64_t)j * kPage - L0, n_old, HD};
         const int nrows = min(kPage, L1 - j * kPage);
+        // a block opened by an earlier append already holds zeros past its end
+        const int npairs = n_old > 0 ? (nrows + 1) / 2 : 32;
         uint8_t *codes = (is_v ? p.v_codes : p.k_codes) + ((int64_t)page * H + h) * kPage * C::kRowBytes;
         float *scale = (is_v ? p.v_scales : p.k_scales) + (int64_t)page * H + h;
-        quantize_block_warp<FMT>(rows, nrows, sbuf[warp], codes, scale);
+        quantize_block_warp<FMT>(rows, nrows, npairs, sbuf[warp], codes, scale);
     }
     // The warp of the first touched block is the only reader of this (b, h)'s
     // tail, so it also writes the new tail rows: no other warp can race with it.
@@ -351,11 +360,10 @@ cudaError_t launch_quantize(int fmt, const uint16_t *x, int64_t T, int H, uint8_
     const int64_t blocks = (warps + kQuantWarps - 1) / kQuantWarps;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)blocks), block(kQuantWarps * 32);
     if (fmt == KVQ_INT4_B64)
-        quantize_contig_kernel<KVQ_INT4_B64><<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(x, T, H, nb, codes, scales);
-    else
-        quantize_contig_kernel<KVQ_INT8_PAGE><<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(x, T, H, nb, codes, scales);
-    return cudaGetLastError();
+        return launch_pdl(quantize_contig_kernel<KVQ_INT4_B64>, grid, block, 0, s, x, T, H, nb, codes, scales);
+    return launch_pdl(quantize_contig_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, x, T, H, nb, codes, scales);
 }
 
 cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s)
@@ -365,12 +373,9 @@ cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s)
     const int64_t warps = touched * p.num_heads;
     const int64_t bx = (warps + kQuantWarps - 1) / kQuantWarps;
     if (bx > 0x7fffffffLL || p.num_seqs > 65535) return cudaErrorInvalidValue;
-    dim3 grid((unsigned)bx, (unsigned)p.num_seqs, 2);
-    if (fmt == KVQ_INT4_B64)
-        append_kernel<KVQ_INT4_B64><<<grid, kQuantWarps * 32, 0, s>>>(p);
-    else
-        append_kernel<KVQ_INT8_PAGE><<<grid, kQuantWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    const dim3 grid((unsigned)bx, (unsigned)p.num_seqs, 2), block(kQuantWarps * 32);
+    if (fmt == KVQ_INT4_B64) return launch_pdl(append_kernel<KVQ_INT4_B64>, grid, block, 0, s, p);
+    return launch_pdl(append_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, p);
 }
 
 }  // namespace kvq
