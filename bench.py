@@ -90,27 +90,36 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest():
+KERNEL_SOURCES = {
+    "decode_split_kernel": ("kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h"),
+    "append_kernel": ("kvq_quantize.cu", "kvq_device.cuh", "kvq_internal.h"),
+}
+
+
+def source_digest(kernel):
+    """Digest of the sources a kernel is built from (ties a profile to them)."""
     h = hashlib.sha256()
-    for f in ("kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "quantized_kv_cache_09_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel):
-    """dram bytes per launch of `kernel` from the committed ncu summary, or None
-    when the summary is missing or was taken on other kernel sources."""
+def ncu_traffic(kernel, workload):
+    """dram bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, or None when the summary is missing or was taken on other kernel
+    sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = source_digest()
+    digest = source_digest(kernel)
     with open(path) as f:
         for line in f:
             if line.startswith("#") or "=" not in line:
                 continue
             kv = dict(p.split("=", 1) for p in line.split())
-            if kv.get("kernel") == kernel and kv.get("source_sha256") == digest:
+            if (kv.get("kernel") == kernel and kv.get("workload") == workload
+                    and kv.get("source_sha256") == digest):
                 return float(kv["dram_bytes_per_launch"])
     return None
 
@@ -437,7 +446,7 @@ def run_ours(args):
                            "format": "int4-b64", "step": "one kvq_append of all new tokens"},
                 "roofline": {"kernel": "append_kernel", "bound": "hbm", "achieved": gbs, "peak": peak,
                              "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
-                             "traffic": ncu_traffic("append_kernel"), "algorithmic_bytes_per_launch": r["bytes"]},
+                             "traffic": ncu_traffic("append_kernel", "prefill-append"), "algorithmic_bytes_per_launch": r["bytes"]},
                 "gpu_launches": K}
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -469,7 +478,7 @@ def run_ours(args):
             "kv_gb_per_s": achieved, "decode_us": dec_ms * 1e3, "append_us": app_ms * 1e3,
             "roofline": {"kernel": "kvq_decode_attention (split + merge launches)", "bound": "hbm",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": ncu_traffic("decode_split_kernel"),
+                         "frac": achieved / peak, "traffic": ncu_traffic("decode_split_kernel", args.workload),
                          "algorithmic_bytes_per_launch": r["dec_bytes"]},
             "e2e": {"value": whole_job_rate(world, B * r["Ke"], e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
