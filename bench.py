@@ -6,7 +6,7 @@ int4 64-token blocks, K/V ~ N(0,1) with 4 outlier channels per head x10,
 inputs generated in HBM by the seeded generator.  One step = the whole hot
 path once: append one token per sequence (re-quantizing each open block from
 its fp16 originals: absmax, scale, quantize, pack) and decode attention of the
-step's query over every sequence (split pass + merge pass).  The decode
+step's query over every sequence (one split-K launch that also merges).  The decode
 position cycles through one 64-token block, so the context stays 8193..8256
 tokens and the working set (~270 MB of codes) stays larger than L2 (129 MB).
 
@@ -321,11 +321,23 @@ def measure_decode(name, K, Wm, seed, dev, pg):
     time.sleep(0.3)
     _sync_all(pg, dev)
     t_wall0 = time.time()
+    # (1) the headline: K whole steps back to back, events only around them, so
+    # each launch overlaps the previous one's tail as in a serving loop
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(K):
         s = (Wm + i) % NS
+        kvq.kvq_append(dw.cache, k_steps[s], v_steps[s], step.cu, dw.block_table, lens_b[s], 1)
+        kvq.kvq_decode_attention(dw.cache, q_steps[s], dw.block_table, lens_a[s], dw.softmax_scale, step.out,
+                                 dw.workspace)
+    end.record(stream)
+    _sync_all(pg, dev)
+    total_ms = start.elapsed_time(end)
+    # (2) the same K steps again with an event before, between and after the two
+    # calls: each call's own duration (the events serialise the launches)
+    for i in range(K):
+        s = (Wm + K + i) % NS
         e0, e1, e2 = ev[i]
         e0.record(stream)
         kvq.kvq_append(dw.cache, k_steps[s], v_steps[s], step.cu, dw.block_table, lens_b[s], 1)
@@ -333,12 +345,11 @@ def measure_decode(name, K, Wm, seed, dev, pg):
         kvq.kvq_decode_attention(dw.cache, q_steps[s], dw.block_table, lens_a[s], dw.softmax_scale, step.out,
                                  dw.workspace)
         e2.record(stream)
-    end.record(stream)
     _sync_all(pg, dev)
     clocks.window = (t_wall0, time.time())
-    total_ms = start.elapsed_time(end)
     app_ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
     dec_ms = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(K)) / K
+    split_ms = ev[0][0].elapsed_time(ev[K - 1][2])
     rc, flags = kvq.kvq_get_device_status(dw.cache)
     if rc != 0:
         raise RuntimeError(f"device status {rc} flags {flags:#x} after timed steps")
@@ -355,7 +366,7 @@ def measure_decode(name, K, Wm, seed, dev, pg):
     e2e_e = torch.cuda.Event(enable_timing=True)
     e2e_s.record(stream)
     for i in range(Ke):
-        s = (Wm + K + i) % NS
+        s = (Wm + 2 * K + i) % NS
         dk.copy_(pin_k[s], non_blocking=True)
         dv.copy_(pin_v[s], non_blocking=True)
         dq.copy_(pin_q[s], non_blocking=True)
@@ -367,11 +378,11 @@ def measure_decode(name, K, Wm, seed, dev, pg):
     e2e_ms = e2e_s.elapsed_time(e2e_e)
     clocks.stop()
 
-    ctx = [(wl.lens + ((Wm + i) % NS if aligned else 0) + 1) for i in range(K)]
+    ctx = [(wl.lens + ((Wm + K + i) % NS if aligned else 0) + 1) for i in range(K)]
     dec_bytes = sum(wl.decode_bytes(c) for c in ctx) / K
     res = dict(wl=wl, B=B, H=H, D=D, aligned=aligned, total_ms=total_ms, app_ms=app_ms, dec_ms=dec_ms,
-               e2e_ms=e2e_ms, Ke=Ke, dec_bytes=dec_bytes, clocks=clocks.summary(),
-               h2d=3 * B * H * D * 2, d2h=B * H * D * 2, launches=3 * K)
+               e2e_ms=e2e_ms, Ke=Ke, dec_bytes=dec_bytes, clocks=clocks.summary(), split_ms=split_ms,
+               h2d=3 * B * H * D * 2, d2h=B * H * D * 2, launches=(1 + -(-B // 512)) * K)
     del dw
     torch.cuda.empty_cache()
     return res
@@ -476,7 +487,8 @@ def run_ours(args):
                        "parallelism": f"replicas x{world} (sequence-sharded, no collective)",
                        "l2": "inputs larger than L2" if r["dec_bytes"] > 129e6 else "fits in L2 (no flush)"},
             "kv_gb_per_s": achieved, "decode_us": dec_ms * 1e3, "append_us": app_ms * 1e3,
-            "roofline": {"kernel": "kvq_decode_attention (split + merge launches)", "bound": "hbm",
+            "step_us_events_between_calls": r["split_ms"] / K * 1e3,
+            "roofline": {"kernel": "kvq_decode_attention (decode_split_kernel, merge fused)", "bound": "hbm",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": ncu_traffic("decode_split_kernel", args.workload),
                          "algorithmic_bytes_per_launch": r["dec_bytes"]},

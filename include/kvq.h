@@ -155,8 +155,9 @@ size_t kvq_decode_workspace_bytes(kvq_format fmt, int32_t num_heads, int32_t hea
  * section 3.1; paging: ddd.cn section 4).  For every (b, h):
  *   s_t = softmax_scale * sum_d q[b][h][d] * k^_t[d],   t < seq_lens[b]
  *   out[b][h][:] = sum_t softmax(s)_t * v^_t[:]
- * computed in binary32 with an online softmax over splits of the sequence and
- * a second pass that merges the splits.
+ * computed in binary32 with an online softmax over splits of the sequence;
+ * the warp that finishes the last split of a (b, h) merges the splits, all in
+ * one kernel launch.
  *   q, out           fp16 [num_seqs][num_heads][head_dim], 16-byte aligned
  *   block_table      device int32 [num_seqs][max_blocks_per_seq]
  *   seq_lens         device int32 [num_seqs] (0 allowed: that output is 0)

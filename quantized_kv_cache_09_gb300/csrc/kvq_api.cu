@@ -123,8 +123,8 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
     p.max_blocks = max_blocks_per_seq;
     p.score_scale = softmax_scale * 1.4426950408889634f;
     p.partials = reinterpret_cast<float *>(workspace);
-    p.cu_units = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(workspace) +
-                                             (size_t)grid_warps * 2 * kvq::kPartialStride * sizeof(float));
+    p.pieces = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(workspace) +
+                                                      (size_t)grid_warps * 2 * kvq::kPartialStride * sizeof(float));
     const int64_t HD = (int64_t)cache->num_heads * kvq::kHeadDim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (int32_t b0 = 0; b0 < num_seqs; b0 += kvq::kMaxSeqsPerLaunch) {

@@ -10,43 +10,53 @@
 //   unit   = 32 tokens (int4) or 16 tokens (int8) of one (sequence, head):
 //            2 KiB of K codes + 2 KiB of V codes, contiguous inside one page;
 //   order  = sequence-major, then head, then unit;
-//   warps  = a persistent grid of (SMs x CTAs/SM x 4) warps; warp g owns the
+//   warps  = a persistent grid of (SMs x 3 or 4 CTAs/SM x 4) warps; warp g owns the
 //            contiguous unit range [U g / G, U (g+1) / G), so every warp
 //            streams the same number of bytes whatever the length mix;
-//   stream = each warp runs its own 4-stage ring of shared-memory stages
+//   stream = each warp runs its own ring of 4 (int4) / 3 (int8) shared-memory stages
 //            filled by bulk async copies (cp.async.bulk, completing on one
-//            mbarrier per stage), issued kStages units ahead by lane 0;
+//            mbarrier per stage), issued one ring ahead by lane 0;
 //   math   = codes are widened to fp16 exactly in registers (magic-number
 //            bias trick), then fp32 FMAs: s = scale_k * (q . c) * softmax_scale,
 //            online softmax in fp32 (base 2), acc += p * scale_v * c;
 //   split  = a (sequence, head) wholly inside one warp's range is written as
-//            the final output; one cut by range boundaries leaves (m, l, acc)
-//            partials that the merge kernel combines:
+//            the final output; one cut by range boundaries leaves an (m, l, acc)
+//            partial per piece, and the warp that writes the last piece
+//            combines them in the same launch:
 //            m = max m_i, l = sum l_i 2^(m_i - m), o = sum acc_i 2^(m_i - m) / l.
+//            "Last" is decided by an atomic count per (sequence, head) tagged
+//            with the launch's epoch, so nothing waits and the workspace needs
+//            no clearing between launches.
+#include <atomic>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
 
 constexpr int kDecWarps = 4;
-constexpr int kStages = 4;
 constexpr int kUnitBytes = 2048;
 constexpr int kMinUnitsPerWarp = 2;
-constexpr int kDecCtasPerSm = 3;
 
 template <int FMT>
 struct DecFmt;
+// int4 keeps 4 stages per warp at 3 CTAs per SM; int8 (lighter math, more
+// latency-bound) runs 3 stages per warp at 4 CTAs per SM
 template <>
 struct DecFmt<KVQ_INT4_B64> {
     static constexpr int kRowBytes = 64;
     static constexpr int kUnitTok = 32;
     static constexpr int kUnitsPerPage = 2;
+    static constexpr int kStages = 4;
+    static constexpr int kCtasPerSm = 3;
 };
 template <>
 struct DecFmt<KVQ_INT8_PAGE> {
     static constexpr int kRowBytes = 128;
     static constexpr int kUnitTok = 16;
     static constexpr int kUnitsPerPage = 4;
+    static constexpr int kStages = 3;
+    static constexpr int kCtasPerSm = 4;
 };
 
 struct alignas(16) StageMeta {
@@ -55,6 +65,7 @@ struct alignas(16) StageMeta {
     int32_t new_seg, pad;
 };
 
+template <int kStages>
 struct alignas(128) WarpSmem {
     uint8_t k[kStages][kUnitBytes];
     uint8_t v[kStages][kUnitBytes];
@@ -64,7 +75,11 @@ struct alignas(128) WarpSmem {
 };
 
 constexpr size_t kSeqSmemBytes = ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 127) / 128 * 128;
-constexpr size_t kDecSmemBytes = kDecWarps * sizeof(WarpSmem) + kSeqSmemBytes;
+template <int FMT>
+constexpr size_t dec_smem_bytes()
+{
+    return kDecWarps * sizeof(WarpSmem<DecFmt<FMT>::kStages>) + kSeqSmemBytes;
+}
 
 // ---------------------------------------------------------------------------
 // exact widening of packed codes to fp16 pairs
@@ -533,17 +548,97 @@ struct Consumer<KVQ_INT8_PAGE> {
     }
 };
 
+// ---------------------------------------------------------------------------
+// Combining the pieces of a (sequence, head) cut by warp-range boundaries.
+// ---------------------------------------------------------------------------
+
+// Called by every lane of a warp right after it wrote one piece's partial:
+// counts the piece in the (sequence, head)'s slot and returns true in the warp
+// that wrote the last one.  The slot holds {epoch, count}; a slot left by an
+// earlier launch (another epoch) counts as empty, so the workspace is never
+// cleared.  The fences order every lane's partial stores before the count
+// and, in the last warp, the count before its reads of the other partials.
+__device__ __forceinline__ bool last_piece(unsigned long long *slot, uint32_t pieces, uint32_t epoch, int lane,
+                                           int32_t *status)
+{
+    __threadfence();
+    __syncwarp();
+    uint32_t count = 0;
+    if (lane == 0) {
+        const unsigned long long tag = (unsigned long long)epoch << 32;
+        unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(slot);
+        // lock-free retry: each failure means another warp's update landed, so
+        // at most `pieces` rounds; the bound only guards against a corrupt slot
+        for (int it = 0; it < 4096; it++) {
+            const unsigned long long next = ((cur >> 32) == epoch) ? cur + 1 : (tag | 1ull);
+            const unsigned long long prev = atomicCAS(slot, cur, next);
+            if (prev == cur) {
+                count = (uint32_t)next;
+                break;
+            }
+            cur = prev;
+        }
+        if (count == 0) set_flag(status, KVQ_FLAG_TIMEOUT);
+    }
+    count = __shfl_sync(kFull, count, 0);
+    if (count != pieces) return false;
+    __threadfence();
+    return true;
+}
+
+// One warp: combine the partials of warps gf .. gf + cnt - 1 (slot 1 of warp
+// gf when the (sequence, head) is that warp's last segment, slot 0 of the
+// others) into one fp16 output row.  Partials are read from L2 (ld.cg): other
+// SMs wrote them during this launch.
+__device__ __forceinline__ void merge_pieces(const float *partials, int64_t gf, int cnt, int first_slot,
+                                             uint16_t *out_row, int lane)
+{
+    const float *pbase = partials + gf * 2 * kPartialStride;
+    auto part = [&](int i) { return pbase + ((int64_t)i * 2 + (i == 0 ? first_slot : 0)) * kPartialStride; };
+    float M = -INFINITY;
+    for (int i = lane; i < cnt; i += 32) M = fmaxf(M, __ldcg(part(i)));
+    M = warp_max(M);
+    float L = 0.0f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < cnt; i0 += 32) {
+        float wl = 0.0f;
+        if (i0 + lane < cnt) {
+            const float *src = part(i0 + lane);
+            wl = ex2_approx(__ldcg(src) - M);
+            L += __ldcg(src + 1) * wl;
+        }
+        const int c = min(32, cnt - i0);
+#pragma unroll 4
+        for (int i = 0; i < c; i++) {
+            const float wgt = __shfl_sync(kFull, wl, i);
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(part(i0 + i) + 4) + lane);
+            o.x += a.x * wgt;
+            o.y += a.y * wgt;
+            o.z += a.z * wgt;
+            o.w += a.w * wgt;
+        }
+    }
+    L = warp_sum(L);
+    const float inv = 1.0f / L;
+    const __half2 lo = __floats2half2_rn(o.x * inv, o.y * inv);
+    const __half2 hi = __floats2half2_rn(o.z * inv, o.w * inv);
+    reinterpret_cast<uint2 *>(out_row)[lane] =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+}
+
 template <int FMT>
-__global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
+__global__ void __launch_bounds__(kDecWarps * 32, DecFmt<FMT>::kCtasPerSm)
     decode_split_kernel(DecodeParams p, int grid_warps)
 {
     using F = DecFmt<FMT>;
+    constexpr int kStages = F::kStages;
+    using WS = WarpSmem<kStages>;
     constexpr int UT = F::kUnitTok;
     constexpr int UPP = F::kUnitsPerPage;
     constexpr int RB = F::kRowBytes;
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    WarpSmem *wsm_all = reinterpret_cast<WarpSmem *>(smem_raw);
-    int32_t *s_cu = reinterpret_cast<int32_t *>(smem_raw + kDecWarps * sizeof(WarpSmem));
+    WS *wsm_all = reinterpret_cast<WS *>(smem_raw);
+    int32_t *s_cu = reinterpret_cast<int32_t *>(smem_raw + kDecWarps * sizeof(WS));
     int32_t *s_len = s_cu + kMaxSeqsPerLaunch + 1;
 
     const int tid = threadIdx.x;
@@ -589,8 +684,18 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
         if (lane == 31) s_cu[B] = incl;
     }
     __syncthreads();
-    if (blockIdx.x == 0)
-        for (int b = tid; b <= B; b += blockDim.x) p.cu_units[b] = s_cu[b];
+    if (warp == 0) {  // no warp owns a unit of an empty sequence: its rows are zeros
+        for (int base = 0; base < B; base += 32) {
+            uint32_t m = __ballot_sync(kFull, base + lane < B && s_len[base + lane] == 0);
+            while (m) {
+                const int b = base + __ffs(m) - 1;
+                m &= m - 1;
+                if (b % (int)gridDim.x != (int)blockIdx.x) continue;
+                uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)b * H * kHeadDim);
+                for (int e = lane; e < H * (kHeadDim / 8); e += 32) row[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
 
     const int64_t U = s_cu[B];
     if (U == 0) return;
@@ -601,7 +706,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
     const int64_t x1 = U * (gw + 1) / G;
     if (x0 >= x1) return;
 
-    WarpSmem &ws = wsm_all[warp];
+    WS &ws = wsm_all[warp];
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; s++) mbar_init(&ws.full[s], 1);
@@ -632,7 +737,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
     constexpr uint32_t kPageBytes = kPage * RB;
 
     auto issue = [&](int ni) {
-        const int s = ni & (kStages - 1);
+        const int s = ni % kStages;
         const int j = ic / UPP;
         if (ib != ring_b || ih != ring_h || j >= ring_j0 + 32) {
             ring_b = ib;
@@ -705,11 +810,17 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
             cs.finish(lane, p.out + ((int64_t)b * H + h) * kHeadDim, nullptr);
         } else {  // cut by a range boundary: the first segment of the warp goes to slot 0, the last to slot 1
             cs.finish(lane, nullptr, p.partials + ((int64_t)gw * 2 + (na == 0 ? 0 : 1)) * kPartialStride);
+            const int64_t u1 = u0 + n;
+            const int64_t gf = ((u0 + 1) * G - 1) / U;  // warp owning unit u0
+            const int64_t gl = (u1 * G - 1) / U;        // warp owning unit u1 - 1
+            if (last_piece(p.pieces + gl, (uint32_t)(gl - gf + 1), p.epoch, lane, p.status))
+                merge_pieces(p.partials, gf, (int)(gl - gf + 1), ((U * gf) / G != u0) ? 1 : 0,
+                             p.out + ((int64_t)b * H + h) * kHeadDim, lane);
         }
     };
     auto drain = [&](int from) {  // after a timeout: let the copies still in flight land
         for (int y = from; y < ni; y++)
-            mbar_wait_bounded(&ws.full[y & (kStages - 1)], (uint32_t)((y / kStages) & 1));
+            mbar_wait_bounded(&ws.full[y % kStages], (uint32_t)((y / kStages) & 1));
     };
 
     // unit 0
@@ -729,13 +840,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
     cs.softmax(sc, mi.w, mf.x * p.score_scale, mf.y, lane, pf);
 
     for (int n = 0; n < N; n++) {
-        const int s = n & (kStages - 1);
+        const int s = n % kStages;
         const bool more = n + 1 < N;
         int4 mi1 = make_int4(0, 0, 0, 0);
         float4 mf1 = make_float4(0.f, 0.f, 0.f, 0.f);
         float sc1[4];
         if (more) {
-            const int s1 = (n + 1) & (kStages - 1);
+            const int s1 = (n + 1) % kStages;
             if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((n + 1) / kStages) & 1))) {
                 if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
                 drain(n + 2);
@@ -766,67 +877,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm)
     flush(cur_b, cur_h, seg_n, N);
 }
 
-// one warp per (sequence, head): combine the split partials of a (sequence,
-// head) cut by warp-range boundaries; write zeros for empty sequences
-__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, int grid_warps)
-{
-    pdl_launch_dependents();
-    pdl_wait();
-    const int w = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const int B = p.num_seqs, H = p.num_heads;
-    if (w >= B * H) return;
-    const int b = w / H, h = w % H;
-    const int64_t U = p.cu_units[B];
-    const int64_t cb = p.cu_units[b];
-    const int64_t n = (p.cu_units[b + 1] - cb) / H;
-    uint2 *orow = reinterpret_cast<uint2 *>(p.out + ((int64_t)b * H + h) * kHeadDim) + lane;
-    if (n == 0) {
-        *orow = make_uint2(0u, 0u);
-        return;
-    }
-    const int64_t G = imin64((int64_t)grid_warps, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);
-    const int64_t u0 = cb + h * n;
-    const int64_t u1 = u0 + n;
-    const int64_t gf = ((u0 + 1) * G - 1) / U;
-    const int64_t gl = (u1 * G - 1) / U;
-    if (gf == gl) return;  // written whole by the split kernel
-    // the partial of warp g: slot 1 for warp gf when (b, h) starts inside its
-    // range (it is that warp's last segment), slot 0 otherwise
-    const int first_slot = ((U * gf) / G != u0) ? 1 : 0;
-    const int cnt_all = (int)(gl - gf + 1);
-    const float *pbase = p.partials + gf * 2 * kPartialStride;
-    auto part = [&](int i) { return pbase + ((int64_t)i * 2 + (i == 0 ? first_slot : 0)) * kPartialStride; };
-    float M = -INFINITY;
-    for (int i = lane; i < cnt_all; i += 32) M = fmaxf(M, part(i)[0]);
-    M = warp_max(M);
-    float L = 0.0f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < cnt_all; i0 += 32) {
-        float wl = 0.0f;
-        if (i0 + lane < cnt_all) {
-            const float *src = part(i0 + lane);
-            wl = ex2_approx(src[0] - M);
-            L += src[1] * wl;
-        }
-        const int cnt = min(32, cnt_all - i0);
-#pragma unroll 4
-        for (int i = 0; i < cnt; i++) {
-            const float wgt = __shfl_sync(kFull, wl, i);
-            const float4 a = reinterpret_cast<const float4 *>(part(i0 + i) + 4)[lane];
-            o.x += a.x * wgt;
-            o.y += a.y * wgt;
-            o.z += a.z * wgt;
-            o.w += a.w * wgt;
-        }
-    }
-    L = warp_sum(L);
-    const float inv = 1.0f / L;
-    const __half2 lo = __floats2half2_rn(o.x * inv, o.y * inv);
-    const __half2 hi = __floats2half2_rn(o.z * inv, o.w * inv);
-    *orow = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
-}
-
 template <int FMT>
 static int ctas_per_sm()
 {
@@ -835,13 +885,14 @@ static int ctas_per_sm()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev] == 0) {
         if (cudaFuncSetAttribute(decode_split_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kDecSmemBytes) != cudaSuccess)
+                                 (int)dec_smem_bytes<FMT>()) != cudaSuccess)
             return 0;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<FMT>, kDecWarps * 32,
-                                                          kDecSmemBytes) != cudaSuccess)
+                                                          dec_smem_bytes<FMT>()) != cudaSuccess)
             return 0;
-        cached[dev] = n < 1 ? 1 : (n > kDecCtasPerSm ? kDecCtasPerSm : n);
+        constexpr int cap = DecFmt<FMT>::kCtasPerSm;
+        cached[dev] = n < 1 ? 1 : (n > cap ? cap : n);
     }
     return cached[dev];
 }
@@ -860,22 +911,22 @@ size_t decode_workspace_bytes(int fmt)
     const int gw = decode_grid_warps(fmt);
     if (gw <= 0) return 0;
     const size_t partial = (size_t)gw * 2 * kPartialStride * sizeof(float);
-    const size_t cu = ((kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 15) / 16 * 16;
-    return partial + cu;
+    return partial + (size_t)gw * sizeof(unsigned long long);
 }
 
 cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s)
 {
+    static std::atomic<uint32_t> next_epoch{1};
     const int gw = decode_grid_warps(fmt);
     if (gw <= 0) return cudaErrorInvalidDevice;
     const int ctas = gw / kDecWarps;
-    cudaError_t e = (fmt == KVQ_INT4_B64)
-                        ? launch_pdl(decode_split_kernel<KVQ_INT4_B64>, dim3(ctas), dim3(kDecWarps * 32), kDecSmemBytes, s, p, gw)
-                        : launch_pdl(decode_split_kernel<KVQ_INT8_PAGE>, dim3(ctas), dim3(kDecWarps * 32), kDecSmemBytes, s, p, gw);
-    if (e != cudaSuccess) return e;
-    const int mblocks = (p.num_seqs * p.num_heads + 3) / 4;
-    if (mblocks > 0) e = launch_pdl(decode_merge_kernel, dim3(mblocks), dim3(128), 0, s, p, gw);
-    return e;
+    DecodeParams d = p;
+    do d.epoch = next_epoch.fetch_add(1, std::memory_order_relaxed); while (d.epoch == 0);
+    return (fmt == KVQ_INT4_B64)
+               ? launch_pdl(decode_split_kernel<KVQ_INT4_B64>, dim3(ctas), dim3(kDecWarps * 32),
+                            dec_smem_bytes<KVQ_INT4_B64>(), s, d, gw)
+               : launch_pdl(decode_split_kernel<KVQ_INT8_PAGE>, dim3(ctas), dim3(kDecWarps * 32),
+                            dec_smem_bytes<KVQ_INT8_PAGE>(), s, d, gw);
 }
 
 }  // namespace kvq

@@ -43,14 +43,15 @@ struct DecodeParams {
     const int32_t *block_table;
     const int32_t *seq_lens;
     uint16_t *out;
-    float *partials;   // [grid warps][2][kPartialStride]
-    int32_t *cu_units; // [num_seqs + 1] written by CTA 0 of the split kernel for the merge kernel
+    float *partials;              // [grid warps][2][kPartialStride]
+    unsigned long long *pieces;   // [grid warps]: {epoch, pieces written} of the (sequence, head) ending in warp g
     int32_t *status;
     int32_t num_seqs;
     int32_t num_heads;
     int32_t num_pages;
     int32_t max_blocks;
     float score_scale;  // softmax_scale * log2(e): scores are kept in the base-2 domain
+    uint32_t epoch;     // non-zero, different for every launch: tags this launch's piece counts
 };
 
 // floats per split partial: m, l, 2 pad, acc[128]
@@ -73,6 +74,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// the same launch without the attribute: the kernel starts only after the
+// previous work on the stream has completed
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                         Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 

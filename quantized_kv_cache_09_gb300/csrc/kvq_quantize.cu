@@ -352,6 +352,151 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Short appends (at most 64 new tokens per sequence, e.g. one decode step):
+// one CTA of 8 warps per touched (block, head, K/V), so re-quantizing an open
+// block takes 4 short rounds per lane instead of one warp's 32.  Lane
+// (rpar, chunk) of warp w holds rows 16 i + 2 w + rpar (i < 4) in registers;
+// max|x| goes through one shared-memory exchange.  If the new rows leave the
+// block's scale unchanged, the block's max|x| is unchanged too (a -> RN(a / d)
+// is strictly increasing on binary16 magnitudes), and the old rows' codes,
+// a function of (x, scale) alone, are already in the cache: only the new
+// rows are written.
+// ---------------------------------------------------------------------------
+constexpr int kShortWarps = 8;
+constexpr int kShortRounds = kPage / (2 * kShortWarps);
+
+template <int FMT>
+__global__ void __launch_bounds__(kShortWarps * 32)
+    append_short_kernel(AppendParams p)
+{
+    using C = Codec<FMT>;
+    __shared__ uint32_t s_max[kShortWarps];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = blockIdx.y;
+    const bool is_v = blockIdx.z != 0;
+    const int H = p.num_heads;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const bool leader = blockIdx.x == 0 && tid == 0 && !is_v;
+    const int c0 = p.cu_seqlens[b];
+    const int T = p.cu_seqlens[b + 1] - c0;
+    const int L0 = p.seq_lens_before[b];
+    if (T < 0 || T > p.max_new_tokens || c0 < 0 || (int64_t)c0 + T > p.total_new) {
+        if (leader) set_flag(p.status, KVQ_FLAG_BAD_APPEND);
+        return;
+    }
+    if (T == 0) return;
+    const int L1 = L0 + T;
+    if (L0 < 0 || (int64_t)L1 > (int64_t)p.max_blocks * kPage) {
+        if (leader) set_flag(p.status, KVQ_FLAG_BAD_LENGTH);
+        return;
+    }
+    const int j0 = L0 / kPage;
+    const int j1 = (L1 - 1) / kPage;
+    const int jrel = blockIdx.x / H;
+    const int h = blockIdx.x % H;
+    if (jrel > j1 - j0) return;
+    const int j = j0 + jrel;
+    const int64_t HD = (int64_t)H * kHeadDim;
+    const uint16_t *fresh = (is_v ? p.v_new : p.k_new) + (int64_t)h * kHeadDim;
+    uint16_t *tail = is_v ? p.v_tail : p.k_tail;
+    uint16_t *tail_bh = tail ? tail + ((int64_t)b * H + h) * kPage * kHeadDim : nullptr;
+    const int n_old = (j == j0) ? (L0 - j0 * kPage) : 0;
+    if (n_old > 0 && tail_bh == nullptr) {
+        if (tid == 0) set_flag(p.status, KVQ_FLAG_NO_TAIL);
+        return;
+    }
+    const int page = p.block_table[(int64_t)b * p.max_blocks + j];
+    const bool page_ok = page >= 0 && page < p.num_pages;
+    if (!page_ok && tid == 0) set_flag(p.status, KVQ_FLAG_BAD_PAGE);
+    const int64_t pg = page_ok ? page : 0;
+    float *scale_ptr = (is_v ? p.v_scales : p.k_scales) + pg * H + h;
+    const float s_old = (n_old > 0 && page_ok) ? *scale_ptr : -1.0f;
+
+    const int nrows = min(kPage, L1 - j * kPage);
+    const int R = n_old > 0 ? nrows : kPage;  // rows rewritten when the scale moves
+    const int64_t row0 = (int64_t)c0 + (int64_t)j * kPage - L0;  // new-token row of block row 0
+    const int chunk = lane & 15;
+    const int rbase = 2 * warp + (lane >> 4);
+    uint4 v[kShortRounds];
+    __half2 mx = __float2half2_rn(0.0f);
+#pragma unroll
+    for (int i = 0; i < kShortRounds; i++) {
+        const int r = 16 * i + rbase;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < n_old)
+            v[i] = *reinterpret_cast<const uint4 *>(tail_bh + r * kHeadDim + 8 * chunk);
+        else if (r < nrows)
+            v[i] = ld_stream_v4(fresh + (row0 + r) * HD + 8 * chunk);
+    }
+#pragma unroll
+    for (int i = 0; i < kShortRounds; i++) {
+        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v[i].x)));
+        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v[i].y)));
+        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v[i].z)));
+        mx = __hmax2(mx, __habs2(*reinterpret_cast<const __half2 *>(&v[i].w)));
+    }
+    const uint32_t mb = *reinterpret_cast<const uint32_t *>(&mx);
+    const uint32_t wmax = __reduce_max_sync(kFull, max(mb & 0xffffu, mb >> 16));
+    if (lane == 0) s_max[warp] = wmax;
+    __syncthreads();  // also orders every read of the tail before the tail writes below
+    uint32_t abits = s_max[0];
+#pragma unroll
+    for (int w = 1; w < kShortWarps; w++) abits = max(abits, s_max[w]);
+    const float a = __half2float(__ushort_as_half(static_cast<unsigned short>(abits)));
+    const float scale = __fdiv_rn(a, C::kDiv);
+    const int r_first = (scale == s_old) ? n_old : 0;  // unchanged scale: old rows keep their codes
+
+    if (page_ok) {
+        if (tid == 0) *scale_ptr = scale;
+        const float rcp = scale > 0.0f ? __frcp_rn(scale) : 0.0f;
+        const float ya = scale > 0.0f ? __fdiv_rn(a, scale) : 0.0f;
+        const uint64_t rr = pk2(rcp, rcp);
+        uint8_t *codes = (is_v ? p.v_codes : p.k_codes) + (pg * H + h) * kPage * C::kRowBytes +
+                         (FMT == KVQ_INT4_B64 ? 4 : 8) * chunk;
+#pragma unroll
+        for (int i = 0; i < kShortRounds; i++) {
+            const int r = 16 * i + rbase;
+            if (r < r_first || r >= R) continue;
+            uint32_t m[8];
+            float tmax = 0.0f;
+            quant8_fast<FMT>(v[i], rr, m, tmax);
+            if (tmax > 0.5f - C::kEps) quant8_exact<FMT>(v[i], rr, scale, a, ya, m);
+            if constexpr (FMT == KVQ_INT4_B64)
+                *reinterpret_cast<uint32_t *>(codes + r * C::kRowBytes) = pack8_int4(m);
+            else
+                *reinterpret_cast<uint2 *>(codes + r * C::kRowBytes) = pack8_int8(m);
+        }
+    }
+    // the CTA of the first touched block is the only reader of this (b, h)'s
+    // tail; after the barrier above it writes the rows of the block left open
+    if (j == j0 && tail_bh != nullptr && (L1 % kPage) != 0) {
+        if (j1 == j0) {  // the open block stays open: its new rows are in registers
+#pragma unroll
+            for (int i = 0; i < kShortRounds; i++) {
+                const int r = 16 * i + rbase;
+                if (r >= n_old && r < nrows) *reinterpret_cast<uint4 *>(tail_bh + r * kHeadDim + 8 * chunk) = v[i];
+            }
+        } else {  // a later block is left open: copy its rows from the new tokens
+            const int re = L1 - j1 * kPage;
+            const int64_t row1 = (int64_t)c0 + (int64_t)j1 * kPage - L0;
+            for (int e = tid; e < re * 16; e += kShortWarps * 32) {
+                const int r = e >> 4, ch = e & 15;
+                const uint4 val = ld_stream_v4(fresh + (row1 + r) * HD + 8 * ch);
+                *reinterpret_cast<uint4 *>(tail_bh + r * kHeadDim + 8 * ch) = val;
+            }
+        }
+    }
+}
+
+// Quantize and append launch without programmatic dependent launch: in a
+// decode loop the kernel before them is the persistent decode grid, and their
+// CTAs placed early (waiting for it to finish) were measured to delay the next
+// decode grid on part of the SMs, costing more than the launch latency they
+// hide.  The decode launch that follows still overlaps their tail.
 cudaError_t launch_quantize(int fmt, const uint16_t *x, int64_t T, int H, uint8_t *codes, float *scales,
                             cudaStream_t s)
 {
@@ -362,20 +507,28 @@ cudaError_t launch_quantize(int fmt, const uint16_t *x, int64_t T, int H, uint8_
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)blocks), block(kQuantWarps * 32);
     if (fmt == KVQ_INT4_B64)
-        return launch_pdl(quantize_contig_kernel<KVQ_INT4_B64>, grid, block, 0, s, x, T, H, nb, codes, scales);
-    return launch_pdl(quantize_contig_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, x, T, H, nb, codes, scales);
+        return launch_plain(quantize_contig_kernel<KVQ_INT4_B64>, grid, block, 0, s, x, T, H, nb, codes, scales);
+    return launch_plain(quantize_contig_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, x, T, H, nb, codes, scales);
 }
 
 cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s)
 {
-    if (p.num_seqs == 0 || p.max_new_tokens == 0) return cudaSuccess;
-    const int64_t touched = (int64_t)(p.max_new_tokens + kPage - 1) / kPage + 1;
+    if (p.num_seqs == 0 || p.max_new_tokens <= 0) return cudaSuccess;
+    // T new tokens starting anywhere touch at most (T - 1 + 63) / 64 + 1 blocks
+    const int64_t touched = ((int64_t)p.max_new_tokens + kPage - 2) / kPage + 1;
+    if (p.max_new_tokens <= kPage) {
+        const int64_t bx = touched * p.num_heads;
+        if (bx > 0x7fffffffLL || p.num_seqs > 65535) return cudaErrorInvalidValue;
+        const dim3 grid((unsigned)bx, (unsigned)p.num_seqs, 2), block(kShortWarps * 32);
+        if (fmt == KVQ_INT4_B64) return launch_plain(append_short_kernel<KVQ_INT4_B64>, grid, block, 0, s, p);
+        return launch_plain(append_short_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, p);
+    }
     const int64_t warps = touched * p.num_heads;
     const int64_t bx = (warps + kQuantWarps - 1) / kQuantWarps;
     if (bx > 0x7fffffffLL || p.num_seqs > 65535) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)bx, (unsigned)p.num_seqs, 2), block(kQuantWarps * 32);
-    if (fmt == KVQ_INT4_B64) return launch_pdl(append_kernel<KVQ_INT4_B64>, grid, block, 0, s, p);
-    return launch_pdl(append_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, p);
+    if (fmt == KVQ_INT4_B64) return launch_plain(append_kernel<KVQ_INT4_B64>, grid, block, 0, s, p);
+    return launch_plain(append_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, p);
 }
 
 }  // namespace kvq

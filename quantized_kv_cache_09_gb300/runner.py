@@ -90,7 +90,7 @@ class DecodeStep:
 
 def kernel_names():
     """Substrings of the kernel names the CUDA path launches."""
-    return ["quantize_contig_kernel", "append_kernel", "decode_split_kernel", "decode_merge_kernel"]
+    return ["quantize_contig_kernel", "append_kernel", "append_short_kernel", "decode_split_kernel"]
 
 
 __all__ = ["DeviceWorkload", "DecodeStep", "kernel_names", "W"]

@@ -170,3 +170,22 @@ def test_host_rejects_bad_arguments(cuda_ok):
         kvq.kvq_quantize(kvq.KVQ_INT4_B64, x, torch.empty(8192, dtype=torch.uint8, device="cuda"),
                          torch.empty(4, dtype=torch.float32, device="cuda"))
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE])
+def test_one_head_split_over_the_whole_grid(cuda_ok, fmt):
+    """One (sequence, head) long enough to be cut into about a thousand pieces:
+    the warp that writes the last piece merges them all (more than one round of
+    32 lanes), with a workspace full of garbage and then reused."""
+    lens = [65536 + 17]
+    wl = W.Workload(1, 1, D, lens, fmt, 1.0, None, "permuted", seed=8)
+    dw = DeviceWorkload(wl)
+    dw.prefill()
+    dw.workspace.copy_(torch.randint(0, 256, dw.workspace.shape, dtype=torch.uint8, device="cuda"))
+    q_np, out = _run_decode(dw)
+    _check_decode(wl, wl.lens, q_np, out)
+    dw.workspace.fill_(0xFF)
+    _, out2 = _run_decode(dw, q_np)
+    _, out3 = _run_decode(dw, q_np)
+    assert torch.equal(out, out2) and torch.equal(out, out3)
+    assert kvq.kvq_get_device_status(dw.cache) == (0, 0)

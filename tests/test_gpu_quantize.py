@@ -162,3 +162,47 @@ def test_append_reports_device_problems(cuda_ok):
     rc, flags = kvq.kvq_get_device_status(cache)
     assert flags & kvq.KVQ_FLAG_NO_TAIL
     assert kvq.kvq_get_device_status(cache) == (0, 0)   # the word was cleared
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_single_token_appends_keep_or_raise_scale(cuda_ok, fmt):
+    """Decode-style appends, one token per sequence per call, through two whole
+    blocks: tokens that raise the block's max|x|, tie it exactly, or stay below
+    it (where only the new row's codes change).  After every call the open
+    block's codes and scale equal the oracle's quantize_block of the history."""
+    H, B, steps = 4, 3, 130
+    rng = np.random.default_rng(17 + fmt)
+    hist = rng.standard_normal((B, steps, H, D)) * np.array([0.5, 2.0, 8.0])[:, None, None, None]
+    # sequence 0: magnitudes grow every token (the scale moves every call);
+    # sequence 1: token 5 sets a max that tokens 9, 20 and 40 repeat exactly
+    hist[0] *= np.linspace(0.1, 3.0, steps)[:, None, None]
+    hist[1, 5, :, 7] = 30.0
+    for t in (9, 20, 40):
+        hist[1, t, :, 3] = -30.0
+    bits = hist.astype(np.float16).view(np.uint16)
+    wl = W.Workload(B, H, D, [steps] * B, fmt, 1.0, None, "permuted", seed=21)
+    bt = torch.from_numpy(wl.block_table.copy()).cuda()
+    cache = kvq.PagedKVCache(fmt, wl.num_pages, H, max_seqs=B)
+    cu = torch.arange(B + 1, dtype=torch.int32, device="cuda")
+    for t in range(steps):
+        k = torch.from_numpy(np.ascontiguousarray(bits[:, t]).view(np.float16)).cuda()
+        v = torch.from_numpy(np.ascontiguousarray(bits[:, t, :, ::-1]).view(np.float16)).cuda()
+        before = torch.full((B,), t, dtype=torch.int32, device="cuda")
+        kvq.kvq_append(cache, k, v, cu, bt, before, 1)
+        if t % 13 != 12 and t != steps - 1:
+            continue
+        L = t + 1
+        torch.cuda.synchronize()
+        for b in range(B):
+            pages = wl.block_table[b, :(L + 63) // 64]
+            kc = np.zeros_like(cache.k_codes.cpu().numpy())
+            ks = np.zeros((wl.num_pages, H), np.float32)
+            orc.quantize_into_pages(fmt, np.ascontiguousarray(bits[b, :L]), wl.block_table[b], kc, ks)
+            vc = np.zeros_like(kc)
+            vs = np.zeros_like(ks)
+            orc.quantize_into_pages(fmt, np.ascontiguousarray(bits[b, :L, :, ::-1]), wl.block_table[b], vc, vs)
+            assert np.array_equal(cache.k_scales.cpu().numpy()[pages].view(np.uint32), ks[pages].view(np.uint32)), (t, b)
+            assert np.array_equal(cache.v_scales.cpu().numpy()[pages].view(np.uint32), vs[pages].view(np.uint32)), (t, b)
+            assert np.array_equal(cache.k_codes.cpu().numpy()[pages], kc[pages]), (t, b)
+            assert np.array_equal(cache.v_codes.cpu().numpy()[pages], vc[pages]), (t, b)
+    assert kvq.kvq_get_device_status(cache) == (0, 0)
