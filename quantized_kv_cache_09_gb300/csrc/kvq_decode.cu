@@ -34,20 +34,24 @@
 
 namespace kvq {
 
-constexpr int kDecWarps = 4;
 constexpr int kUnitBytes = 2048;
 constexpr int kMinUnitsPerWarp = 2;
 
 template <int FMT>
 struct DecFmt;
-// int4 keeps 4 stages per warp at 3 CTAs per SM; int8 (lighter math, more
-// latency-bound) runs 3 stages per warp at 4 CTAs per SM
+// A stage holds up to kUnitsPerStage consecutive units of one page (one bulk
+// copy each for K and V).  int4: a stage is a whole page (both 32-token
+// units), two stages per warp, 3 CTAs of 4 warps per SM; int8 (lighter math,
+// more latency-bound): one 16-token unit per stage, 3 stages, one CTA of 16
+// warps per SM (measured faster than 4 CTAs of 4 warps).
 template <>
 struct DecFmt<KVQ_INT4_B64> {
     static constexpr int kRowBytes = 64;
     static constexpr int kUnitTok = 32;
     static constexpr int kUnitsPerPage = 2;
-    static constexpr int kStages = 4;
+    static constexpr int kUnitsPerStage = 2;
+    static constexpr int kStages = 2;
+    static constexpr int kWarps = 4;
     static constexpr int kCtasPerSm = 3;
 };
 template <>
@@ -55,20 +59,23 @@ struct DecFmt<KVQ_INT8_PAGE> {
     static constexpr int kRowBytes = 128;
     static constexpr int kUnitTok = 16;
     static constexpr int kUnitsPerPage = 4;
+    static constexpr int kUnitsPerStage = 1;
     static constexpr int kStages = 3;
-    static constexpr int kCtasPerSm = 4;
+    static constexpr int kWarps = 16;
+    static constexpr int kCtasPerSm = 1;
 };
 
+// what a stage holds: units c .. c + nunits - 1 of (b, h), ntok tokens in all
 struct alignas(16) StageMeta {
     int32_t b, h, c, ntok;
     float sk, sv;
-    int32_t new_seg, pad;
+    int32_t new_seg, nunits;
 };
 
-template <int kStages>
+template <int kStages, int kStageBytes>
 struct alignas(128) WarpSmem {
-    uint8_t k[kStages][kUnitBytes];
-    uint8_t v[kStages][kUnitBytes];
+    uint8_t k[kStages][kStageBytes];
+    uint8_t v[kStages][kStageBytes];
     uint16_t q[kStages][kHeadDim];
     StageMeta meta[kStages];
     uint64_t full[kStages];
@@ -78,7 +85,8 @@ constexpr size_t kSeqSmemBytes = ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) 
 template <int FMT>
 constexpr size_t dec_smem_bytes()
 {
-    return kDecWarps * sizeof(WarpSmem<DecFmt<FMT>::kStages>) + kSeqSmemBytes;
+    using F = DecFmt<FMT>;
+    return F::kWarps * sizeof(WarpSmem<F::kStages, F::kUnitsPerStage * kUnitBytes>) + kSeqSmemBytes;
 }
 
 // ---------------------------------------------------------------------------
@@ -232,23 +240,37 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// a softmax weight as the pair {RN16(p), RN16(p - RN16(p))}: ~22 significant bits
-__device__ __forceinline__ uint32_t hi_lo_pair(float x)
+// {RN16(x0), RN16(x1)} as one fp16 pair (x0 in the low half)
+__device__ __forceinline__ uint32_t f16x2_rn(float x0, float x1)
 {
-    const __half hi = __float2half_rn(x);
-    const __half lo = __float2half_rn(x - __half2float(hi));
-    return (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(x1), "f"(x0));
+    return d;
+}
+
+// two softmax weights split into fp16 pairs hi = {RN16(x0), RN16(x1)} and
+// lo = {RN16(x0 - hi0), RN16(x1 - hi1)}: hi + lo keeps ~22 significant bits
+__device__ __forceinline__ void hi_lo_pairs(uint64_t x, uint32_t &hi, uint32_t &lo)
+{
+    float x0, x1;
+    upk2(x, x0, x1);
+    hi = f16x2_rn(x0, x1);
+    const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+    float r0, r1;
+    upk2(sub2(x, pk2(h.x, h.y)), r0, r1);
+    lo = f16x2_rn(r0, r1);
 }
 
 // int4: both contractions of a unit on the tensor cores (mma.sync m16n8k16),
 // codes widened exactly to fp16 in registers, fp32 accumulation.
-//   QK: A = 16 tokens x 16 head elements of K, B column 0 = q (other columns 0);
-//       lane (g, t) feeds rows g, g+8 from its 16-byte slice (elements 32t..32t+31)
-//       of each token row, so the k index is a fixed permutation of the head
-//       dimension that q's fragment repeats.
+//   QK: A = 16 tokens x 16 head elements of K, every column of B = q, so every
+//       lane receives the scores of its rows (tokens g, g+8 of each tile);
+//       lane (g, t) feeds rows g, g+8 from its 16-byte slice (elements
+//       32t..32t+31) of each token row, so the k index is a fixed permutation
+//       of the head dimension that q's fragment repeats.
 //   PV: A = V^T (16 head elements x 16 tokens): prmt pairs the same element of
-//       two tokens; B = softmax weights, column 0 = RN16(p), column 1 = the
-//       remainder, so p keeps ~22 bits.
+//       two tokens; B column 0 = RN16(p), column 1 = the remainder, so p keeps
+//       ~22 bits (columns 2..7 carry copies and are never read).
 //   Unit = 32 tokens: 2 token tiles for QK, 2 k-tiles for PV, 8 output tiles.
 // The three phases (qk, softmax, pv) are separate so the caller can overlap
 // qk of the next unit with pv of this one.
@@ -257,14 +279,14 @@ struct Consumer<KVQ_INT4_B64> {
     uint32_t qb[8][2];
     float acc[8][4];
     float m_run;
-    float l_lane;
+    uint64_t l2;  // running sum of the weights in this lane's slots, as a pair
     Magic mk;
 
     __device__ __forceinline__ void reset()
     {
         mk.init();
         m_run = -INFINITY;
-        l_lane = 0.0f;
+        l2 = pk2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 8; i++)
 #pragma unroll
@@ -273,27 +295,30 @@ struct Consumer<KVQ_INT4_B64> {
 
     __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
     {
-        const int g = lane >> 2, t = lane & 3;
+        const int t = lane & 3;
         const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + 32 * t);
 #pragma unroll
         for (int m = 0; m < 4; m++) {
             const uint4 v = q4[m];  // elements 32t + 8m .. +7 as pairs (0,1) (2,3) (4,5) (6,7)
-            const bool on = g == 0;
-            qb[2 * m][0] = on ? __byte_perm(v.x, v.z, 0x5410) : 0u;      // {e0, e4}
-            qb[2 * m][1] = on ? __byte_perm(v.x, v.z, 0x7632) : 0u;      // {e1, e5}
-            qb[2 * m + 1][0] = on ? __byte_perm(v.y, v.w, 0x5410) : 0u;  // {e2, e6}
-            qb[2 * m + 1][1] = on ? __byte_perm(v.y, v.w, 0x7632) : 0u;  // {e3, e7}
+            qb[2 * m][0] = __byte_perm(v.x, v.z, 0x5410);      // {e0, e4}
+            qb[2 * m][1] = __byte_perm(v.x, v.z, 0x7632);      // {e1, e5}
+            qb[2 * m + 1][0] = __byte_perm(v.y, v.w, 0x5410);  // {e2, e6}
+            qb[2 * m + 1][1] = __byte_perm(v.y, v.w, 0x7632);  // {e3, e7}
         }
     }
 
-    // raw dot products q . c of tokens g, g+8, 16+g, 24+g (valid in lanes with t == 0)
+    // raw dot products q . c of tokens g, g+8, 16+g, 24+g (every lane); four
+    // accumulator chains per tile keep the mma dependency chains short
     __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[4]) const
     {
         const int g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int tau = 0; tau < 2; tau++) {
-            float c0[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            float c1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float c[4][4];
+#pragma unroll
+            for (int m = 0; m < 4; m++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) c[m][e] = 0.0f;
             const uint4 wa = *reinterpret_cast<const uint4 *>(ks + (16 * tau + g) * 64 + 16 * t);
             const uint4 wb = *reinterpret_cast<const uint4 *>(ks + (16 * tau + g + 8) * 64 + 16 * t);
             const uint32_t ua[4] = {wa.x, wa.y, wa.z, wa.w};
@@ -303,60 +328,67 @@ struct Consumer<KVQ_INT4_B64> {
                 uint32_t ca[4], cb[4];
                 widen_int4_u32(ua[m], ca, mk);
                 widen_int4_u32(ub[m], cb, mk);
-                float(&c)[4] = (m & 1) ? c1 : c0;
-                mma16816(c, ca[0], cb[0], ca[1], cb[1], qb[2 * m][0], qb[2 * m][1]);
-                mma16816(c, ca[2], cb[2], ca[3], cb[3], qb[2 * m + 1][0], qb[2 * m + 1][1]);
+                mma16816(c[m], ca[0], cb[0], ca[1], cb[1], qb[2 * m][0], qb[2 * m][1]);
+                mma16816(c[m], ca[2], cb[2], ca[3], cb[3], qb[2 * m + 1][0], qb[2 * m + 1][1]);
             }
-            sc[2 * tau] = c0[0] + c1[0];
-            sc[2 * tau + 1] = c0[2] + c1[2];
+            sc[2 * tau] = (c[0][0] + c[1][0]) + (c[2][0] + c[3][0]);
+            sc[2 * tau + 1] = (c[0][2] + c[1][2]) + (c[2][2] + c[3][2]);
         }
     }
 
-    // online softmax over the unit's scores; pf[i] = {hi, lo} fp16 of p_i * sv
+    // online softmax over the unit's scores.  px[k] = the fp16 pair of this
+    // lane's two tokens of tile k (16k + g, 16k + 8 + g) of x = p * sv: the
+    // rounded values in lanes t == 0, the remainders elsewhere (pv takes
+    // column 0 of its weights from t == 0 lanes and column 1 from t == 1).
     __device__ __forceinline__ void softmax(const float sc[4], int ntok, float fac, float sv, int lane,
-                                            uint32_t pf[4])
+                                            uint32_t px[2])
     {
         const int g = lane >> 2, t = lane & 3;
+        const uint64_t ff = pk2(fac, fac);
         float s2[4];
-        float lm = -INFINITY;
+        upk2(mul2(pk2(sc[0], sc[1]), ff), s2[0], s2[1]);
+        upk2(mul2(pk2(sc[2], sc[3]), ff), s2[2], s2[3]);
+        if (ntok < 32) {  // the last unit of a sequence: tokens past its end get no weight
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int tok = 16 * (i >> 1) + g + 8 * (i & 1);
-            s2[i] = (t == 0 && tok < ntok) ? sc[i] * fac : -INFINITY;
-            lm = fmaxf(lm, s2[i]);
+            for (int i = 0; i < 4; i++)
+                if (16 * (i >> 1) + 8 * (i & 1) + g >= ntok) s2[i] = -INFINITY;
         }
+        const float lm = fmaxf(fmaxf(s2[0], s2[1]), fmaxf(s2[2], s2[3]));
         if (__any_sync(kFull, lm > m_run)) {  // the running maximum moves: rescale
             const float mu = warp_max(lm);
             const float alpha = ex2_approx(m_run - mu);
-            l_lane *= alpha;
+            l2 = mul2(l2, pk2(alpha, alpha));
 #pragma unroll
             for (int i = 0; i < 8; i++)
 #pragma unroll
                 for (int j = 0; j < 4; j++) acc[i][j] *= alpha;
             m_run = mu;
         }
+        float pe[4];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const float pe = ex2_approx(s2[i] - m_run);
-            l_lane += pe;
-            pf[i] = hi_lo_pair(pe * sv);
-        }
+        for (int i = 0; i < 4; i++) pe[i] = ex2_approx(s2[i] - m_run);
+        const uint64_t p01 = pk2(pe[0], pe[1]), p23 = pk2(pe[2], pe[3]);
+        l2 = add2(l2, add2(p01, p23));
+        const uint64_t vv = pk2(sv, sv);
+        uint32_t hi, lo;
+        hi_lo_pairs(mul2(p01, vv), hi, lo);
+        px[0] = t == 0 ? hi : lo;
+        hi_lo_pairs(mul2(p23, vv), hi, lo);
+        px[1] = t == 0 ? hi : lo;
     }
 
-    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t pf[4], int lane)
+    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t px[2], int lane)
     {
         const int g = lane >> 2, t = lane & 3;
-        // column 0 of B takes the hi halves, column 1 the lo halves, other columns 0
-        const uint32_t sel = (g == 0) ? 0x5410u : 0x7632u;
+        // column g of B: lanes g == 0 read the rounded weights (from a t == 0
+        // lane), g == 1 the remainders (from a t == 1 lane); others any copy
+        const int src = 8 * t + (g & 3);
 #pragma unroll
         for (int kap = 0; kap < 2; kap++) {
-            // weights of tokens 16kap + {2t, 2t+1, 2t+8, 2t+9} from the lanes that scored them
-            const uint32_t ua = __shfl_sync(kFull, pf[2 * kap], 8 * t);
-            const uint32_t ub = __shfl_sync(kFull, pf[2 * kap], 8 * t + 4);
-            const uint32_t uc = __shfl_sync(kFull, pf[2 * kap + 1], 8 * t);
-            const uint32_t ud = __shfl_sync(kFull, pf[2 * kap + 1], 8 * t + 4);
-            const uint32_t b0 = g < 2 ? __byte_perm(ua, ub, sel) : 0u;
-            const uint32_t b1 = g < 2 ? __byte_perm(uc, ud, sel) : 0u;
+            const uint32_t ua = __shfl_sync(kFull, px[kap], src);      // tokens 2t, 2t+8 of tile kap
+            const uint32_t ub = __shfl_sync(kFull, px[kap], src + 4);  // tokens 2t+1, 2t+9
+            const uint32_t b0 = __byte_perm(ua, ub, 0x5410);
+            const uint32_t b1 = __byte_perm(ua, ub, 0x7632);
 #pragma unroll
             for (int R = 0; R < 2; R++) {
                 // word 8R + g (elements 64R + 8g .. +7) of tokens 16kap + 2t, +1, +8, +9
@@ -388,7 +420,9 @@ struct Consumer<KVQ_INT4_B64> {
     // 64R + 8g + e (e < 4: tile 4R+e rows g; e >= 4: tile 4R+e-4 rows g+8)
     __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
     {
-        const float l = warp_sum(l_lane);
+        float la, lb;
+        upk2(l2, la, lb);
+        const float l = warp_sum(la + lb) * 0.25f;  // the four lanes of a row group hold the same weights
         const int g = lane >> 2, t = lane & 3;
         if (t != 0) return;
 #pragma unroll
@@ -556,12 +590,24 @@ struct Consumer<KVQ_INT8_PAGE> {
 // counts the piece in the (sequence, head)'s slot and returns true in the warp
 // that wrote the last one.  The slot holds {epoch, count}; a slot left by an
 // earlier launch (another epoch) counts as empty, so the workspace is never
-// cleared.  The fences order every lane's partial stores before the count
-// and, in the last warp, the count before its reads of the other partials.
+// cleared.  Ordering: the warp barrier orders every lane's partial stores
+// before lane 0's acq_rel atomic (release), whose acquire side in the last
+// warp, followed by that warp's barrier, orders its reads of the other
+// pieces' partials after their writers' stores.
+__device__ __forceinline__ unsigned long long cas_acq_rel_gpu(unsigned long long *p, unsigned long long cmp,
+                                                              unsigned long long val)
+{
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+                 : "=l"(old)
+                 : "l"(p), "l"(cmp), "l"(val)
+                 : "memory");
+    return old;
+}
+
 __device__ __forceinline__ bool last_piece(unsigned long long *slot, uint32_t pieces, uint32_t epoch, int lane,
                                            int32_t *status)
 {
-    __threadfence();
     __syncwarp();
     uint32_t count = 0;
     if (lane == 0) {
@@ -571,7 +617,7 @@ __device__ __forceinline__ bool last_piece(unsigned long long *slot, uint32_t pi
         // at most `pieces` rounds; the bound only guards against a corrupt slot
         for (int it = 0; it < 4096; it++) {
             const unsigned long long next = ((cur >> 32) == epoch) ? cur + 1 : (tag | 1ull);
-            const unsigned long long prev = atomicCAS(slot, cur, next);
+            const unsigned long long prev = cas_acq_rel_gpu(slot, cur, next);
             if (prev == cur) {
                 count = (uint32_t)next;
                 break;
@@ -582,7 +628,7 @@ __device__ __forceinline__ bool last_piece(unsigned long long *slot, uint32_t pi
     }
     count = __shfl_sync(kFull, count, 0);
     if (count != pieces) return false;
-    __threadfence();
+    __syncwarp();
     return true;
 }
 
@@ -627,17 +673,19 @@ __device__ __forceinline__ void merge_pieces(const float *partials, int64_t gf, 
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kDecWarps * 32, DecFmt<FMT>::kCtasPerSm)
+__global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPerSm)
     decode_split_kernel(DecodeParams p, int grid_warps)
 {
     using F = DecFmt<FMT>;
     constexpr int kStages = F::kStages;
-    using WS = WarpSmem<kStages>;
+    constexpr int UPS = F::kUnitsPerStage;
+    using WS = WarpSmem<kStages, UPS * kUnitBytes>;
     constexpr int UT = F::kUnitTok;
     constexpr int UPP = F::kUnitsPerPage;
     constexpr int RB = F::kRowBytes;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     WS *wsm_all = reinterpret_cast<WS *>(smem_raw);
+    constexpr int kDecWarps = F::kWarps;
     int32_t *s_cu = reinterpret_cast<int32_t *>(smem_raw + kDecWarps * sizeof(WS));
     int32_t *s_len = s_cu + kMaxSeqsPerLaunch + 1;
 
@@ -736,9 +784,15 @@ __global__ void __launch_bounds__(kDecWarps * 32, DecFmt<FMT>::kCtasPerSm)
     const int N = (int)(x1 - x0);  // units of this warp
     constexpr uint32_t kPageBytes = kPage * RB;
 
-    auto issue = [&](int ni) {
-        const int s = ni % kStages;
+    int ci = 0;   // stages filled so far (chunk count)
+    int nis = 0;  // units issued so far
+    // fill stage ci % kStages with the next chunk: the cursor's unit and the
+    // following ones of the same stage-sized group of its page, within the
+    // (sequence, head) and the warp's range
+    auto issue = [&]() {
+        const int s = ci % kStages;
         const int j = ic / UPP;
+        const int nh = UPS > 1 ? min(min(UPS - ic % UPS, inb - ic), N - nis) : 1;
         if (ib != ring_b || ih != ring_h || j >= ring_j0 + 32) {
             ring_b = ib;
             ring_h = ih;
@@ -763,25 +817,27 @@ __global__ void __launch_bounds__(kDecWarps * 32, DecFmt<FMT>::kCtasPerSm)
         const int pg = __shfl_sync(kFull, r_page, j - ring_j0);
         const float sk = __shfl_sync(kFull, r_sk, j - ring_j0);
         const float sv = __shfl_sync(kFull, r_sv, j - ring_j0);
-        const bool new_seg = (ni == 0) || (ic == 0);
+        const bool new_seg = (ci == 0) || (ic == 0);
         if (lane == 0) {
-            const int ntok = min(UT, s_len[ib] - ic * UT);
+            const int ntok = min(nh * UT, s_len[ib] - ic * UT);
             *reinterpret_cast<int4 *>(&ws.meta[s].b) = make_int4(ib, ih, ic, ntok);
             *reinterpret_cast<float4 *>(&ws.meta[s].sk) =
-                make_float4(sk, sv, __int_as_float(new_seg ? 1 : 0), 0.0f);
+                make_float4(sk, sv, __int_as_float(new_seg ? 1 : 0), __int_as_float(nh));
             // The refill of stage s follows the warp's reads of it: every lane
             // consumed those values (mma operands) before the __syncwarp that
             // precedes this issue, so the copy cannot overtake them.
-            const uint32_t bytes = 2 * kUnitBytes + (new_seg ? kHeadDim * 2 : 0);
+            const uint32_t cb = (uint32_t)nh * kUnitBytes;
+            const uint32_t bytes = 2 * cb + (new_seg ? kHeadDim * 2 : 0);
             mbar_arrive_expect_tx(&ws.full[s], bytes);
             const size_t off = ((size_t)pg * H + ih) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
-            bulk_copy_g2s(ws.k[s], p.k_codes + off, kUnitBytes, &ws.full[s]);
-            bulk_copy_g2s(ws.v[s], p.v_codes + off, kUnitBytes, &ws.full[s]);
+            bulk_copy_g2s(ws.k[s], p.k_codes + off, cb, &ws.full[s]);
+            bulk_copy_g2s(ws.v[s], p.v_codes + off, cb, &ws.full[s]);
             if (new_seg)
                 bulk_copy_g2s(ws.q[s], p.q + ((size_t)ib * H + ih) * kHeadDim, kHeadDim * 2, &ws.full[s]);
         }
-        // advance the cursor
-        if (++ic == inb) {
+        // advance the cursor by the chunk
+        ic += nh;
+        if (ic == inb) {
             ic = 0;
             if (++ih == H) {
                 ih = 0;
@@ -790,10 +846,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, DecFmt<FMT>::kCtasPerSm)
                 if (ib < B) inb = units_of(s_len[ib], UT);
             }
         }
+        ++ci;
+        nis += nh;
     };
 
-    int ni = 0;  // next unit to issue (relative to x0)
-    for (; ni < kStages && ni < N; ni++) issue(ni);
+    for (int i = 0; i < kStages && nis < N; i++) issue();
     __syncwarp();
 
     // ---- consumer: qk of unit n+1 overlaps pv of unit n ----
@@ -819,11 +876,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, DecFmt<FMT>::kCtasPerSm)
         }
     };
     auto drain = [&](int from) {  // after a timeout: let the copies still in flight land
-        for (int y = from; y < ni; y++)
+        for (int y = from; y < ci; y++)
             mbar_wait_bounded(&ws.full[y % kStages], (uint32_t)((y / kStages) & 1));
     };
 
-    // unit 0
+    // chunk 0, unit 0
     if (!mbar_wait_bounded(&ws.full[0], 0u)) {
         if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
         drain(1);
@@ -831,47 +888,62 @@ __global__ void __launch_bounds__(kDecWarps * 32, DecFmt<FMT>::kCtasPerSm)
     }
     int4 mi = *reinterpret_cast<const int4 *>(&ws.meta[0].b);
     float4 mf = *reinterpret_cast<const float4 *>(&ws.meta[0].sk);
+    int cc = 0;                        // chunk being consumed (stage cc % kStages)
+    int k = 0;                         // its unit being consumed
+    int nh = UPS > 1 ? __float_as_int(mf.w) : 1;  // its units
     cur_b = mi.x;
     cur_h = mi.y;
     cs.load_q(ws.q[0], lane);
     float sc[4];
     uint32_t pf[4];
     cs.qk(ws.k[0], lane, sc);
-    cs.softmax(sc, mi.w, mf.x * p.score_scale, mf.y, lane, pf);
+    cs.softmax(sc, min(UT, mi.w), mf.x * p.score_scale, mf.y, lane, pf);
 
     for (int n = 0; n < N; n++) {
-        const int s = n % kStages;
+        const int s = cc % kStages;
         const bool more = n + 1 < N;
-        int4 mi1 = make_int4(0, 0, 0, 0);
-        float4 mf1 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const bool same = UPS > 1 && k + 1 < nh;  // unit n+1 is in the same chunk
+        int4 mi1 = mi;
+        float4 mf1 = mf;
+        int k1 = k + 1;
         float sc1[4];
         if (more) {
-            const int s1 = (n + 1) % kStages;
-            if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((n + 1) / kStages) & 1))) {
-                if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
-                drain(n + 2);
-                return;
+            int s1 = s;
+            if (!same) {
+                s1 = (cc + 1) % kStages;
+                if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((cc + 1) / kStages) & 1))) {
+                    if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
+                    drain(cc + 2);
+                    return;
+                }
+                mi1 = *reinterpret_cast<const int4 *>(&ws.meta[s1].b);
+                mf1 = *reinterpret_cast<const float4 *>(&ws.meta[s1].sk);
+                k1 = 0;
+                if (__float_as_int(mf1.z)) cs.load_q(ws.q[s1], lane);
             }
-            mi1 = *reinterpret_cast<const int4 *>(&ws.meta[s1].b);
-            mf1 = *reinterpret_cast<const float4 *>(&ws.meta[s1].sk);
-            if (__float_as_int(mf1.z)) cs.load_q(ws.q[s1], lane);
-            cs.qk(ws.k[s1], lane, sc1);  // unit n+1: independent of the pv below
+            cs.qk(ws.k[s1] + k1 * kUnitBytes, lane, sc1);  // unit n+1: independent of the pv below
         }
-        cs.pv(ws.v[s], pf, lane);        // unit n
-        __syncwarp();
-        if (ni < N) {                    // stage s is free: refill it with unit n + kStages
-            issue(ni);
-            ++ni;
+        cs.pv(ws.v[s] + k * kUnitBytes, pf, lane);     // unit n
+        if (!same) {  // chunk cc is consumed: refill its stage
+            __syncwarp();
+            if (nis < N) issue();
         }
         if (more) {
-            if (__float_as_int(mf1.z)) {  // unit n+1 starts a new (sequence, head)
-                flush(cur_b, cur_h, seg_n, n + 1);
-                cs.reset();
-                cur_b = mi1.x;
-                cur_h = mi1.y;
-                seg_n = n + 1;
+            if (!same) {
+                if (__float_as_int(mf1.z)) {  // unit n+1 starts a new (sequence, head)
+                    flush(cur_b, cur_h, seg_n, n + 1);
+                    cs.reset();
+                    cur_b = mi1.x;
+                    cur_h = mi1.y;
+                    seg_n = n + 1;
+                }
+                ++cc;
+                if (UPS > 1) nh = __float_as_int(mf1.w);
             }
-            cs.softmax(sc1, mi1.w, mf1.x * p.score_scale, mf1.y, lane, pf);
+            cs.softmax(sc1, min(UT, mi1.w - k1 * UT), mf1.x * p.score_scale, mf1.y, lane, pf);
+            k = k1;
+            mi = mi1;
+            mf = mf1;
         }
     }
     flush(cur_b, cur_h, seg_n, N);
@@ -888,7 +960,7 @@ static int ctas_per_sm()
                                  (int)dec_smem_bytes<FMT>()) != cudaSuccess)
             return 0;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<FMT>, kDecWarps * 32,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<FMT>, DecFmt<FMT>::kWarps * 32,
                                                           dec_smem_bytes<FMT>()) != cudaSuccess)
             return 0;
         constexpr int cap = DecFmt<FMT>::kCtasPerSm;
@@ -902,8 +974,8 @@ int decode_grid_warps(int fmt)
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    const int per = fmt == KVQ_INT4_B64 ? ctas_per_sm<KVQ_INT4_B64>() : ctas_per_sm<KVQ_INT8_PAGE>();
-    return sms * per * kDecWarps;
+    if (fmt == KVQ_INT4_B64) return sms * ctas_per_sm<KVQ_INT4_B64>() * DecFmt<KVQ_INT4_B64>::kWarps;
+    return sms * ctas_per_sm<KVQ_INT8_PAGE>() * DecFmt<KVQ_INT8_PAGE>::kWarps;
 }
 
 size_t decode_workspace_bytes(int fmt)
@@ -919,13 +991,13 @@ cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s)
     static std::atomic<uint32_t> next_epoch{1};
     const int gw = decode_grid_warps(fmt);
     if (gw <= 0) return cudaErrorInvalidDevice;
-    const int ctas = gw / kDecWarps;
+    const int ctas = gw / (fmt == KVQ_INT4_B64 ? DecFmt<KVQ_INT4_B64>::kWarps : DecFmt<KVQ_INT8_PAGE>::kWarps);
     DecodeParams d = p;
     do d.epoch = next_epoch.fetch_add(1, std::memory_order_relaxed); while (d.epoch == 0);
     return (fmt == KVQ_INT4_B64)
-               ? launch_pdl(decode_split_kernel<KVQ_INT4_B64>, dim3(ctas), dim3(kDecWarps * 32),
+               ? launch_pdl(decode_split_kernel<KVQ_INT4_B64>, dim3(ctas), dim3(DecFmt<KVQ_INT4_B64>::kWarps * 32),
                             dec_smem_bytes<KVQ_INT4_B64>(), s, d, gw)
-               : launch_pdl(decode_split_kernel<KVQ_INT8_PAGE>, dim3(ctas), dim3(kDecWarps * 32),
+               : launch_pdl(decode_split_kernel<KVQ_INT8_PAGE>, dim3(ctas), dim3(DecFmt<KVQ_INT8_PAGE>::kWarps * 32),
                             dec_smem_bytes<KVQ_INT8_PAGE>(), s, d, gw);
 }
 

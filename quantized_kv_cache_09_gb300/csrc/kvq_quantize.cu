@@ -47,36 +47,6 @@ struct Codec<KVQ_INT8_PAGE> {
 
 constexpr uint32_t kMagicBits = 0x4b400000u;  // bits of 1.5 * 2^23
 
-// ---- packed binary32 pairs (Blackwell f32x2 arithmetic) --------------------
-__device__ __forceinline__ uint64_t pk2(float a, float b)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void upk2(uint64_t v, float &a, float &b)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 // fast path for 8 fp16 values: m[j] = bits of RN(RN(x_j * r) + kMagic), and
 // tmax = max(tmax, |y_j - rint(y_j)|) over them
 template <int FMT>
@@ -354,16 +324,19 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 
 // ---------------------------------------------------------------------------
 // Short appends (at most 64 new tokens per sequence, e.g. one decode step):
-// one CTA of 8 warps per touched (block, head, K/V), so re-quantizing an open
-// block takes 4 short rounds per lane instead of one warp's 32.  Lane
-// (rpar, chunk) of warp w holds rows 16 i + 2 w + rpar (i < 4) in registers;
-// max|x| goes through one shared-memory exchange.  If the new rows leave the
-// block's scale unchanged, the block's max|x| is unchanged too (a -> RN(a / d)
-// is strictly increasing on binary16 magnitudes), and the old rows' codes,
-// a function of (x, scale) alone, are already in the cache: only the new
-// rows are written.
+// one CTA of 4 warps per touched (block, head, K/V); lane (rpar, chunk) of
+// warp w holds rows 8 i + 2 w + rpar (i < 8) in registers.
+//   1. Load the new rows only and reduce their max|x| -> a_new (one
+//      shared-memory exchange), and read the block's stored scale s_old.
+//   2. a -> RN(a / d) is strictly increasing on binary16 magnitudes, so
+//      RN(a_new / d) <= s_old exactly when the block's max|x| does not move:
+//      then the scale is s_old and the old rows' codes, a function of
+//      (x, scale) alone, are already in the cache -- only the new rows are
+//      quantized, and the fp16 tail is never read.
+//   3. Otherwise a_new is the block's max|x|: the old rows are loaded from the
+//      tail and every row is re-quantized with the new scale.
 // ---------------------------------------------------------------------------
-constexpr int kShortWarps = 8;
+constexpr int kShortWarps = 4;
 constexpr int kShortRounds = kPage / (2 * kShortWarps);
 
 template <int FMT>
@@ -417,20 +390,17 @@ __global__ void __launch_bounds__(kShortWarps * 32)
     const float s_old = (n_old > 0 && page_ok) ? *scale_ptr : -1.0f;
 
     const int nrows = min(kPage, L1 - j * kPage);
-    const int R = n_old > 0 ? nrows : kPage;  // rows rewritten when the scale moves
     const int64_t row0 = (int64_t)c0 + (int64_t)j * kPage - L0;  // new-token row of block row 0
     const int chunk = lane & 15;
     const int rbase = 2 * warp + (lane >> 4);
+    // 1. the new rows and their max|x|
     uint4 v[kShortRounds];
     __half2 mx = __float2half2_rn(0.0f);
 #pragma unroll
     for (int i = 0; i < kShortRounds; i++) {
-        const int r = 16 * i + rbase;
+        const int r = 8 * i + rbase;
         v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < n_old)
-            v[i] = *reinterpret_cast<const uint4 *>(tail_bh + r * kHeadDim + 8 * chunk);
-        else if (r < nrows)
-            v[i] = ld_stream_v4(fresh + (row0 + r) * HD + 8 * chunk);
+        if (r >= n_old && r < nrows) v[i] = ld_stream_v4(fresh + (row0 + r) * HD + 8 * chunk);
     }
 #pragma unroll
     for (int i = 0; i < kShortRounds; i++) {
@@ -442,24 +412,38 @@ __global__ void __launch_bounds__(kShortWarps * 32)
     const uint32_t mb = *reinterpret_cast<const uint32_t *>(&mx);
     const uint32_t wmax = __reduce_max_sync(kFull, max(mb & 0xffffu, mb >> 16));
     if (lane == 0) s_max[warp] = wmax;
-    __syncthreads();  // also orders every read of the tail before the tail writes below
+    __syncthreads();
     uint32_t abits = s_max[0];
 #pragma unroll
     for (int w = 1; w < kShortWarps; w++) abits = max(abits, s_max[w]);
-    const float a = __half2float(__ushort_as_half(static_cast<unsigned short>(abits)));
-    const float scale = __fdiv_rn(a, C::kDiv);
-    const int r_first = (scale == s_old) ? n_old : 0;  // unchanged scale: old rows keep their codes
-
+    const float a_new = __half2float(__ushort_as_half(static_cast<unsigned short>(abits)));
+    const float s_new = __fdiv_rn(a_new, C::kDiv);
+    // 2./3. keep the scale, or re-quantize the whole block
+    const bool keep = n_old > 0 && s_new <= s_old;
+    const float scale = keep ? s_old : s_new;
+    // the exact path's shortcut for elements equal to +-max|x| needs the
+    // block's max, known only when it moved; with the scale kept, every
+    // near-tie takes the correctly rounded division instead
+    const float a = keep ? INFINITY : a_new;
+    const int r_first = keep ? n_old : 0;
+    const int R = n_old > 0 ? nrows : kPage;  // rows rewritten (past nrows: code 0)
+    if (!keep && n_old > 0) {
+#pragma unroll
+        for (int i = 0; i < kShortRounds; i++) {
+            const int r = 8 * i + rbase;
+            if (r < n_old) v[i] = *reinterpret_cast<const uint4 *>(tail_bh + r * kHeadDim + 8 * chunk);
+        }
+    }
     if (page_ok) {
         if (tid == 0) *scale_ptr = scale;
         const float rcp = scale > 0.0f ? __frcp_rn(scale) : 0.0f;
-        const float ya = scale > 0.0f ? __fdiv_rn(a, scale) : 0.0f;
+        const float ya = (scale > 0.0f && !keep) ? __fdiv_rn(a, scale) : 0.0f;
         const uint64_t rr = pk2(rcp, rcp);
         uint8_t *codes = (is_v ? p.v_codes : p.k_codes) + (pg * H + h) * kPage * C::kRowBytes +
                          (FMT == KVQ_INT4_B64 ? 4 : 8) * chunk;
 #pragma unroll
         for (int i = 0; i < kShortRounds; i++) {
-            const int r = 16 * i + rbase;
+            const int r = 8 * i + rbase;
             if (r < r_first || r >= R) continue;
             uint32_t m[8];
             float tmax = 0.0f;
@@ -472,15 +456,16 @@ __global__ void __launch_bounds__(kShortWarps * 32)
         }
     }
     // the CTA of the first touched block is the only reader of this (b, h)'s
-    // tail; after the barrier above it writes the rows of the block left open
+    // tail; it writes the rows of the block left open
     if (j == j0 && tail_bh != nullptr && (L1 % kPage) != 0) {
-        if (j1 == j0) {  // the open block stays open: its new rows are in registers
+        if (j1 == j0) {  // the open block stays open: its new rows (never read here) are in registers
 #pragma unroll
             for (int i = 0; i < kShortRounds; i++) {
-                const int r = 16 * i + rbase;
+                const int r = 8 * i + rbase;
                 if (r >= n_old && r < nrows) *reinterpret_cast<uint4 *>(tail_bh + r * kHeadDim + 8 * chunk) = v[i];
             }
-        } else {  // a later block is left open: copy its rows from the new tokens
+        } else {  // a later block is left open: its rows overwrite tail rows read above
+            __syncthreads();
             const int re = L1 - j1 * kPage;
             const int64_t row1 = (int64_t)c0 + (int64_t)j1 * kPage - L0;
             for (int e = tid; e < re * 16; e += kShortWarps * 32) {
