@@ -61,7 +61,7 @@ typedef enum kvq_status {
     KVQ_ERR_CUDA = 3,            /* a CUDA runtime call or launch failed */
     KVQ_ERR_BAD_BLOCK_TABLE = 4, /* device: a block-table entry outside [0, num_pages) */
     KVQ_ERR_TIMEOUT = 5,         /* device: a bounded wait on a copy ran out */
-    KVQ_ERR_WORKSPACE = 6,       /* workspace missing or smaller than kvq_decode_workspace_bytes */
+    KVQ_ERR_WORKSPACE = 6,       /* workspace missing, too small, or (device) not zero-filled */
     KVQ_ERR_BAD_LENGTH = 7       /* device: a length beyond the block table, or new tokens beyond max */
 } kvq_status;
 
@@ -76,6 +76,7 @@ typedef enum kvq_format {
 #define KVQ_FLAG_TIMEOUT 0x4     /* a bounded wait for a shared-memory copy ran out */
 #define KVQ_FLAG_NO_TAIL 0x8     /* an append into a partial block found no fp16 tail buffer */
 #define KVQ_FLAG_BAD_APPEND 0x10 /* cu_seqlens not increasing, or more new tokens than max_new_tokens */
+#define KVQ_FLAG_BAD_WORKSPACE 0x20 /* a decode workspace was not zero-filled before its first use */
 
 /*
  * The paged cache.  All pointers are caller-owned device memory.
@@ -162,8 +163,11 @@ size_t kvq_decode_workspace_bytes(kvq_format fmt, int32_t num_heads, int32_t hea
  *   block_table      device int32 [num_seqs][max_blocks_per_seq]
  *   seq_lens         device int32 [num_seqs] (0 allowed: that output is 0)
  *   softmax_scale    normally 1/sqrt(head_dim)
- *   workspace        >= kvq_decode_workspace_bytes(...) bytes, 16-byte aligned;
- *                    contents need no initialisation; do not share one
+ *   workspace        >= kvq_decode_workspace_bytes(...) bytes, 16-byte aligned,
+ *                    zero-filled once before its first use (e.g. with
+ *                    cudaMemsetAsync); every call that completes leaves it
+ *                    ready for the next one.  After a call that set a
+ *                    KVQ_FLAG_* bit, zero it again.  Do not share one
  *                    workspace between calls that may run concurrently
  * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE,
  * KVQ_ERR_CUDA; device-side problems set KVQ_FLAG_* bits in cache->status.

@@ -158,6 +158,7 @@ kvq_status kvq_get_device_status(const kvq_cache *cache, kvq_stream_t stream, in
     if (flags & KVQ_FLAG_BAD_PAGE) return KVQ_ERR_BAD_BLOCK_TABLE;
     if (flags & KVQ_FLAG_BAD_LENGTH) return KVQ_ERR_BAD_LENGTH;
     if (flags & KVQ_FLAG_TIMEOUT) return KVQ_ERR_TIMEOUT;
+    if (flags & KVQ_FLAG_BAD_WORKSPACE) return KVQ_ERR_WORKSPACE;
     if (flags & (KVQ_FLAG_NO_TAIL | KVQ_FLAG_BAD_APPEND)) return KVQ_ERR_BAD_LENGTH;
     return KVQ_OK;
 }
@@ -171,7 +172,7 @@ const char *kvq_status_string(kvq_status status)
     case KVQ_ERR_CUDA: return "CUDA error";
     case KVQ_ERR_BAD_BLOCK_TABLE: return "block-table entry out of range";
     case KVQ_ERR_TIMEOUT: return "bounded wait timed out";
-    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVQ_ERR_WORKSPACE: return "workspace missing, too small or not zero-filled";
     case KVQ_ERR_BAD_LENGTH: return "sequence length or append bounds invalid";
     }
     return "unknown status";

@@ -24,11 +24,9 @@
 //            partial per piece, and the warp that writes the last piece
 //            combines them in the same launch:
 //            m = max m_i, l = sum l_i 2^(m_i - m), o = sum acc_i 2^(m_i - m) / l.
-//            "Last" is decided by an atomic count per (sequence, head) tagged
-//            with the launch's epoch, so nothing waits and the workspace needs
-//            no clearing between launches.
-#include <atomic>
-
+//            "Last" is decided by an atomic count per (sequence, head) that the
+//            last piece puts back to zero, so nothing waits and the workspace
+//            stays ready for the next launch.
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -53,6 +51,7 @@ struct DecFmt<KVQ_INT4_B64> {
     static constexpr int kStages = 2;
     static constexpr int kWarps = 4;
     static constexpr int kCtasPerSm = 3;
+    static constexpr int kMergeBatch = 8;  // pieces whose loads a merge issues at once
 };
 template <>
 struct DecFmt<KVQ_INT8_PAGE> {
@@ -63,6 +62,7 @@ struct DecFmt<KVQ_INT8_PAGE> {
     static constexpr int kStages = 3;
     static constexpr int kWarps = 16;
     static constexpr int kCtasPerSm = 1;
+    static constexpr int kMergeBatch = 4;  // within the 128-register budget of 16 warps
 };
 
 // what a stage holds: units c .. c + nunits - 1 of (b, h), ntok tokens in all
@@ -588,43 +588,31 @@ struct Consumer<KVQ_INT8_PAGE> {
 
 // Called by every lane of a warp right after it wrote one piece's partial:
 // counts the piece in the (sequence, head)'s slot and returns true in the warp
-// that wrote the last one.  The slot holds {epoch, count}; a slot left by an
-// earlier launch (another epoch) counts as empty, so the workspace is never
-// cleared.  Ordering: the warp barrier orders every lane's partial stores
-// before lane 0's acq_rel atomic (release), whose acquire side in the last
-// warp, followed by that warp's barrier, orders its reads of the other
-// pieces' partials after their writers' stores.
-__device__ __forceinline__ unsigned long long cas_acq_rel_gpu(unsigned long long *p, unsigned long long cmp,
-                                                              unsigned long long val)
+// that wrote the last one, which also puts the slot back to zero -- so the
+// slots start every launch at zero provided the workspace was zero-filled
+// once and every earlier launch completed.  One atomic round trip, no retries:
+// all pieces of a (sequence, head) finish at about the same time, and a
+// compare-and-swap there retried under contention for several microseconds.
+// Ordering: the warp barrier orders every lane's partial stores before lane
+// 0's acq_rel add (release), whose acquire side in the last warp, followed by
+// that warp's barrier, orders its reads of the other pieces' partials after
+// their writers' stores.
+__device__ __forceinline__ unsigned long long add_acq_rel_gpu(unsigned long long *p, unsigned long long v)
 {
     unsigned long long old;
-    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
-                 : "=l"(old)
-                 : "l"(p), "l"(cmp), "l"(val)
-                 : "memory");
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
     return old;
 }
 
-__device__ __forceinline__ bool last_piece(unsigned long long *slot, uint32_t pieces, uint32_t epoch, int lane,
-                                           int32_t *status)
+__device__ __noinline__ bool last_piece(unsigned long long *slot, uint32_t pieces, int lane, int32_t *status)
 {
     __syncwarp();
-    uint32_t count = 0;
+    unsigned long long count = 0;
     if (lane == 0) {
-        const unsigned long long tag = (unsigned long long)epoch << 32;
-        unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(slot);
-        // lock-free retry: each failure means another warp's update landed, so
-        // at most `pieces` rounds; the bound only guards against a corrupt slot
-        for (int it = 0; it < 4096; it++) {
-            const unsigned long long next = ((cur >> 32) == epoch) ? cur + 1 : (tag | 1ull);
-            const unsigned long long prev = cas_acq_rel_gpu(slot, cur, next);
-            if (prev == cur) {
-                count = (uint32_t)next;
-                break;
-            }
-            cur = prev;
-        }
-        if (count == 0) set_flag(status, KVQ_FLAG_TIMEOUT);
+        count = add_acq_rel_gpu(slot, 1ull) + 1;
+        if (count > pieces || count == 0)  // the slot was not zero: workspace not zero-filled, or an aborted launch
+            set_flag(status, KVQ_FLAG_BAD_WORKSPACE);
+        if (count == pieces) *slot = 0ull;
     }
     count = __shfl_sync(kFull, count, 0);
     if (count != pieces) return false;
@@ -635,36 +623,56 @@ __device__ __forceinline__ bool last_piece(unsigned long long *slot, uint32_t pi
 // One warp: combine the partials of warps gf .. gf + cnt - 1 (slot 1 of warp
 // gf when the (sequence, head) is that warp's last segment, slot 0 of the
 // others) into one fp16 output row.  Partials are read from L2 (ld.cg): other
-// SMs wrote them during this launch.
-__device__ __forceinline__ void merge_pieces(const float *partials, int64_t gf, int cnt, int first_slot,
+// SMs wrote them during this launch.  The loads of a batch of kBatch pieces
+// are independent of one another, so a merge of up to kBatch pieces costs one
+// round trip to L2.
+// (not inlined: a rare path, kept out of the streaming loop's register budget)
+template <int kBatch>
+__device__ __noinline__ void merge_pieces(const float *partials, int64_t gf, int cnt, int first_slot,
                                              uint16_t *out_row, int lane)
 {
     const float *pbase = partials + gf * 2 * kPartialStride;
     auto part = [&](int i) { return pbase + ((int64_t)i * 2 + (i == 0 ? first_slot : 0)) * kPartialStride; };
-    float M = -INFINITY;
-    for (int i = lane; i < cnt; i += 32) M = fmaxf(M, __ldcg(part(i)));
+    // lane i < cnt: (m, l) of piece i; every lane: its 4 elements of pieces
+    // 0 .. kBatch-1 and their m -- all issued before any of them is used
+    float2 ml = make_float2(-INFINITY, 0.0f);
+    if (lane < cnt) ml = __ldcg(reinterpret_cast<const float2 *>(part(lane)));
+    float4 a[kBatch];
+    float mj[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; j++) {
+        const float *src = part(j < cnt ? j : 0);
+        a[j] = __ldcg(reinterpret_cast<const float4 *>(src + 4) + lane);
+        mj[j] = j < cnt ? __ldcg(src) : -INFINITY;
+    }
+    float M = ml.x;
+    for (int i = lane + 32; i < cnt; i += 32) M = fmaxf(M, __ldcg(part(i)));
     M = warp_max(M);
-    float L = 0.0f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < cnt; i0 += 32) {
-        float wl = 0.0f;
-        if (i0 + lane < cnt) {
-            const float *src = part(i0 + lane);
-            wl = ex2_approx(__ldcg(src) - M);
-            L += __ldcg(src + 1) * wl;
-        }
-        const int c = min(32, cnt - i0);
-#pragma unroll 4
-        for (int i = 0; i < c; i++) {
-            const float wgt = __shfl_sync(kFull, wl, i);
-            const float4 a = __ldcg(reinterpret_cast<const float4 *>(part(i0 + i) + 4) + lane);
-            o.x += a.x * wgt;
-            o.y += a.y * wgt;
-            o.z += a.z * wgt;
-            o.w += a.w * wgt;
-        }
+    float L = lane < cnt ? ml.y * ex2_approx(ml.x - M) : 0.0f;
+    for (int i = lane + 32; i < cnt; i += 32) {
+        const float2 v = __ldcg(reinterpret_cast<const float2 *>(part(i)));
+        L += v.y * ex2_approx(v.x - M);
     }
     L = warp_sum(L);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < cnt; i0 += kBatch) {
+        if (i0 > 0) {
+#pragma unroll
+            for (int j = 0; j < kBatch; j++) {
+                const float *src = part(i0 + j < cnt ? i0 + j : 0);
+                a[j] = __ldcg(reinterpret_cast<const float4 *>(src + 4) + lane);
+                mj[j] = i0 + j < cnt ? __ldcg(src) : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; j++) {
+            const float w = ex2_approx(mj[j] - M);  // 0 for the padding entries
+            o.x += a[j].x * w;
+            o.y += a[j].y * w;
+            o.z += a[j].z * w;
+            o.w += a[j].w * w;
+        }
+    }
     const float inv = 1.0f / L;
     const __half2 lo = __floats2half2_rn(o.x * inv, o.y * inv);
     const __half2 hi = __floats2half2_rn(o.z * inv, o.w * inv);
@@ -870,8 +878,8 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             const int64_t u1 = u0 + n;
             const int64_t gf = ((u0 + 1) * G - 1) / U;  // warp owning unit u0
             const int64_t gl = (u1 * G - 1) / U;        // warp owning unit u1 - 1
-            if (last_piece(p.pieces + gl, (uint32_t)(gl - gf + 1), p.epoch, lane, p.status))
-                merge_pieces(p.partials, gf, (int)(gl - gf + 1), ((U * gf) / G != u0) ? 1 : 0,
+            if (last_piece(p.pieces + gl, (uint32_t)(gl - gf + 1), lane, p.status))
+                merge_pieces<F::kMergeBatch>(p.partials, gf, (int)(gl - gf + 1), ((U * gf) / G != u0) ? 1 : 0,
                              p.out + ((int64_t)b * H + h) * kHeadDim, lane);
         }
     };
@@ -988,12 +996,10 @@ size_t decode_workspace_bytes(int fmt)
 
 cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s)
 {
-    static std::atomic<uint32_t> next_epoch{1};
     const int gw = decode_grid_warps(fmt);
     if (gw <= 0) return cudaErrorInvalidDevice;
     const int ctas = gw / (fmt == KVQ_INT4_B64 ? DecFmt<KVQ_INT4_B64>::kWarps : DecFmt<KVQ_INT8_PAGE>::kWarps);
-    DecodeParams d = p;
-    do d.epoch = next_epoch.fetch_add(1, std::memory_order_relaxed); while (d.epoch == 0);
+    const DecodeParams &d = p;
     return (fmt == KVQ_INT4_B64)
                ? launch_pdl(decode_split_kernel<KVQ_INT4_B64>, dim3(ctas), dim3(DecFmt<KVQ_INT4_B64>::kWarps * 32),
                             dec_smem_bytes<KVQ_INT4_B64>(), s, d, gw)

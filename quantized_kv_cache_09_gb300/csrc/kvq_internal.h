@@ -44,14 +44,13 @@ struct DecodeParams {
     const int32_t *seq_lens;
     uint16_t *out;
     float *partials;              // [grid warps][2][kPartialStride]
-    unsigned long long *pieces;   // [grid warps]: {epoch, pieces written} of the (sequence, head) ending in warp g
+    unsigned long long *pieces;   // [grid warps]: pieces written so far of the (sequence, head) ending in warp g (0 between launches)
     int32_t *status;
     int32_t num_seqs;
     int32_t num_heads;
     int32_t num_pages;
     int32_t max_blocks;
     float score_scale;  // softmax_scale * log2(e): scores are kept in the base-2 domain
-    uint32_t epoch;     // non-zero, different for every launch: tags this launch's piece counts
 };
 
 // floats per split partial: m, l, 2 pad, acc[128]

@@ -14,8 +14,11 @@
 // host it names a host-side stand-in), so the first call on each device looks
 // the address up with cudaGetSymbolAddress while that device is current and
 // keeps it.  All calls share the one array: calls that may overlap on the GPU
-// race on it.  Nothing in it must start at zero -- every byte a decode call
-// reads was written earlier in the same call -- so nothing is cleared.
+// race on it.  Its piece counters must start at zero: a __device__ array is
+// zero when the module loads, and every decode call that completes leaves the
+// counters at zero again (after a call that set a KVQ_FLAG_* bit they may not
+// be, and the device status word of later calls may show
+// KVQ_FLAG_BAD_WORKSPACE).
 #include <cuda_runtime.h>
 
 #include <mutex>

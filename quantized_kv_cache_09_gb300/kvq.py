@@ -21,6 +21,7 @@ KVQ_FLAG_BAD_LENGTH = 0x2
 KVQ_FLAG_TIMEOUT = 0x4
 KVQ_FLAG_NO_TAIL = 0x8
 KVQ_FLAG_BAD_APPEND = 0x10
+KVQ_FLAG_BAD_WORKSPACE = 0x20
 
 STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CUDA",
                 4: "KVQ_ERR_BAD_BLOCK_TABLE", 5: "KVQ_ERR_TIMEOUT", 6: "KVQ_ERR_WORKSPACE",
@@ -234,7 +235,7 @@ class PagedKVCache:
         n = kvq_decode_workspace_bytes(self.fmt, self.num_heads)
         if n <= 0:
             raise RuntimeError("kvq_decode_workspace_bytes returned 0")
-        return torch.empty(n, dtype=torch.uint8, device=self.k_codes.device)
+        return torch.zeros(n, dtype=torch.uint8, device=self.k_codes.device)  # zero-filled before first use
 
     def bytes(self):
         t = [self.k_codes, self.v_codes, self.k_scales, self.v_scales]

@@ -176,16 +176,24 @@ def test_host_rejects_bad_arguments(cuda_ok):
 def test_one_head_split_over_the_whole_grid(cuda_ok, fmt):
     """One (sequence, head) long enough to be cut into about a thousand pieces:
     the warp that writes the last piece merges them all (more than one round of
-    32 lanes), with a workspace full of garbage and then reused."""
+    32 lanes).  The zero-filled workspace is reused without clearing (each call
+    leaves its piece counters at zero); one that was not zero-filled is
+    reported in the status word, and zero-filling it again recovers."""
     lens = [65536 + 17]
     wl = W.Workload(1, 1, D, lens, fmt, 1.0, None, "permuted", seed=8)
     dw = DeviceWorkload(wl)
     dw.prefill()
-    dw.workspace.copy_(torch.randint(0, 256, dw.workspace.shape, dtype=torch.uint8, device="cuda"))
     q_np, out = _run_decode(dw)
     _check_decode(wl, wl.lens, q_np, out)
-    dw.workspace.fill_(0xFF)
     _, out2 = _run_decode(dw, q_np)
     _, out3 = _run_decode(dw, q_np)
     assert torch.equal(out, out2) and torch.equal(out, out3)
+    assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
+    dw.workspace.fill_(0x7F)
+    _run_decode(dw, q_np)
+    rc, flags = kvq.kvq_get_device_status(dw.cache)
+    assert flags & kvq.KVQ_FLAG_BAD_WORKSPACE and rc == 6
+    dw.workspace.zero_()
+    _, out4 = _run_decode(dw, q_np)
+    assert torch.equal(out, out4)
     assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
