@@ -3,22 +3,25 @@
 // paging through a block table: ddd.cn section 4).
 //
 // Decode is a GEMV per (sequence, head): every cached byte is read once and
-// used for a handful of flops, so the kernel is built around HBM streaming on
-// CUDA cores, not tensor cores.
+// used for a handful of flops, so the kernel is built around HBM streaming.
+// The int4 path widens codes exactly to fp16 in registers and feeds the
+// legacy tensor-core mma (m16n8k16) because the widening, not the multiply,
+// is the cost; the int8 path stays on CUDA-core FMAs.
 //
 // Work decomposition (persistent, split-K over the sequence):
 //   unit   = 32 tokens (int4) or 16 tokens (int8) of one (sequence, head):
 //            2 KiB of K codes + 2 KiB of V codes, contiguous inside one page;
 //   order  = sequence-major, then head, then unit;
-//   warps  = a persistent grid of (SMs x 3 or 4 CTAs/SM x 4) warps; warp g owns the
-//            contiguous unit range [U g / G, U (g+1) / G), so every warp
-//            streams the same number of bytes whatever the length mix;
-//   stream = each warp runs its own ring of 4 (int4) / 3 (int8) shared-memory stages
+//   warps  = a persistent grid of one CTA per SM (12 warps int4, 16 warps
+//            int8); warp g owns the contiguous unit range [U g / G, U (g+1) / G),
+//            so every warp streams the same number of bytes whatever the
+//            length mix;
+//   stream = each warp runs its own ring of shared-memory stages (int4: 2
+//            stages of a whole page = 2 units; int8: 3 stages of 1 unit)
 //            filled by bulk async copies (cp.async.bulk, completing on one
-//            mbarrier per stage), issued one ring ahead by lane 0;
-//   math   = codes are widened to fp16 exactly in registers (magic-number
-//            bias trick), then fp32 FMAs: s = scale_k * (q . c) * softmax_scale,
-//            online softmax in fp32 (base 2), acc += p * scale_v * c;
+//            mbarrier per stage), issued by lane 0 as a stage frees;
+//   math   = s = scale_k * (q . c) * softmax_scale, online softmax in fp32
+//            (base 2), acc += p * scale_v * c with fp32 accumulation;
 //   split  = a (sequence, head) wholly inside one warp's range is written as
 //            the final output; one cut by range boundaries leaves an (m, l, acc)
 //            partial per piece, and the warp that writes the last piece
@@ -39,9 +42,11 @@ template <int FMT>
 struct DecFmt;
 // A stage holds up to kUnitsPerStage consecutive units of one page (one bulk
 // copy each for K and V).  int4: a stage is a whole page (both 32-token
-// units), two stages per warp, 3 CTAs of 4 warps per SM; int8 (lighter math,
-// more latency-bound): one 16-token unit per stage, 3 stages, one CTA of 16
-// warps per SM (measured faster than 4 CTAs of 4 warps).
+// units), two stages per warp; int8 (lighter math, more latency-bound): one
+// 16-token unit per stage, 3 stages.  One CTA per SM holds all the warps:
+// the warp scheduler favours older CTAs, so with several CTAs per SM the
+// warps of the youngest ran ~16% slower than those of the oldest and the SM
+// waited for them; the warps of one CTA progress at the same rate.
 template <>
 struct DecFmt<KVQ_INT4_B64> {
     static constexpr int kRowBytes = 64;
@@ -49,8 +54,8 @@ struct DecFmt<KVQ_INT4_B64> {
     static constexpr int kUnitsPerPage = 2;
     static constexpr int kUnitsPerStage = 2;
     static constexpr int kStages = 2;
-    static constexpr int kWarps = 4;
-    static constexpr int kCtasPerSm = 3;
+    static constexpr int kWarps = 12;
+    static constexpr int kCtasPerSm = 1;
     static constexpr int kMergeBatch = 8;  // pieces whose loads a merge issues at once
 };
 template <>
