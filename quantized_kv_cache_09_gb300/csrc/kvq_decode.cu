@@ -761,7 +761,9 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     const int64_t U = s_cu[B];
     if (U == 0) return;
     const int64_t G = imin64((int64_t)grid_warps, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);
-    const int gw = blockIdx.x * kDecWarps + warp;
+    // logical warp index, round-robin over the CTAs: when fewer than all warps
+    // have work (G < grid warps) the active ones spread over every SM
+    const int gw = warp * (int)gridDim.x + blockIdx.x;
     if (gw >= G) return;
     const int64_t x0 = U * gw / G;
     const int64_t x1 = U * (gw + 1) / G;

@@ -477,11 +477,13 @@ __global__ void __launch_bounds__(kShortWarps * 32)
     }
 }
 
-// Quantize and append launch without programmatic dependent launch: in a
-// decode loop the kernel before them is the persistent decode grid, and their
-// CTAs placed early (waiting for it to finish) were measured to delay the next
-// decode grid on part of the SMs, costing more than the launch latency they
-// hide.  The decode launch that follows still overlaps their tail.
+// Launch modes, as measured in a decode loop (append, then decode, whose grid
+// is one persistent CTA per SM that fills the SM's registers): the short
+// append uses programmatic dependent launch -- its CTAs cannot sit beside a
+// decode CTA, so they start as the decode grid drains and hide the launch
+// latency (about 2 us per step).  Quantize and the long append launch plainly:
+// their CTAs placed early delayed the next persistent grid on part of the SMs
+// when the decode ran several smaller CTAs per SM.
 cudaError_t launch_quantize(int fmt, const uint16_t *x, int64_t T, int H, uint8_t *codes, float *scales,
                             cudaStream_t s)
 {
@@ -505,8 +507,8 @@ cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s)
         const int64_t bx = touched * p.num_heads;
         if (bx > 0x7fffffffLL || p.num_seqs > 65535) return cudaErrorInvalidValue;
         const dim3 grid((unsigned)bx, (unsigned)p.num_seqs, 2), block(kShortWarps * 32);
-        if (fmt == KVQ_INT4_B64) return launch_plain(append_short_kernel<KVQ_INT4_B64>, grid, block, 0, s, p);
-        return launch_plain(append_short_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, p);
+        if (fmt == KVQ_INT4_B64) return launch_pdl(append_short_kernel<KVQ_INT4_B64>, grid, block, 0, s, p);
+        return launch_pdl(append_short_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, p);
     }
     const int64_t warps = touched * p.num_heads;
     const int64_t bx = (warps + kQuantWarps - 1) / kQuantWarps;
