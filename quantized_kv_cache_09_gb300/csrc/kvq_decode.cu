@@ -95,27 +95,10 @@ constexpr size_t dec_smem_bytes()
 }
 
 // ---------------------------------------------------------------------------
-// exact widening of packed codes to fp16 pairs
-//   int4 word (8 nibbles, element j at bits 4j): returns {c0,c4},{c1,c5},{c2,c6},{c3,c7}
-//   (1024 + (n ^ 8)) - 1032 = c  for the low nibble of each half;
-//   (1024 + 16 (n ^ 8)) / 16 - 72 = c for the high nibble.
+// exact widening of packed codes to fp16 pairs (magic-number bias)
+//   int4, low nibble n of a 16-bit half: (1024 + (n ^ 8)) - 1032 = c;
+//   int4, bits 4..7 of a half: (1024 + 16 (n ^ 8)) / 16 - 72 = c.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void widen_int4(uint32_t w, __half2 c[4])
-{
-    const uint32_t hi = w >> 8;
-    const uint32_t a = (w & 0x000f000fu) ^ 0x64086408u;
-    const uint32_t b = (w & 0x00f000f0u) ^ 0x64806480u;
-    const uint32_t d = (hi & 0x000f000fu) ^ 0x64086408u;
-    const uint32_t e = (hi & 0x00f000f0u) ^ 0x64806480u;
-    const __half2 k1032 = __float2half2_rn(1032.0f);
-    const __half2 k16 = __float2half2_rn(0.0625f);
-    const __half2 km72 = __float2half2_rn(-72.0f);
-    c[0] = __hsub2(*reinterpret_cast<const __half2 *>(&a), k1032);
-    c[1] = __hfma2(*reinterpret_cast<const __half2 *>(&b), k16, km72);
-    c[2] = __hsub2(*reinterpret_cast<const __half2 *>(&d), k1032);
-    c[3] = __hfma2(*reinterpret_cast<const __half2 *>(&e), k16, km72);
-}
-
 //   int8 word (4 bytes, element j in byte j): returns {c0,c1},{c2,c3}
 //   1024 + (byte ^ 0x80) - 1152 = c
 __device__ __forceinline__ void widen_int8(uint32_t w, __half2 c[2])
