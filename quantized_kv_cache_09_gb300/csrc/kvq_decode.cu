@@ -886,9 +886,6 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     }
     int4 mi = *reinterpret_cast<const int4 *>(&ws.meta[0].b);
     float4 mf = *reinterpret_cast<const float4 *>(&ws.meta[0].sk);
-    int cc = 0;                        // chunk being consumed (stage cc % kStages)
-    int k = 0;                         // its unit being consumed
-    int nh = UPS > 1 ? __float_as_int(mf.w) : 1;  // its units
     cur_b = mi.x;
     cur_h = mi.y;
     cs.load_q(ws.q[0], lane);
@@ -897,52 +894,51 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     cs.qk(ws.k[0], lane, sc);
     cs.softmax(sc, min(UT, mi.w), mf.x * p.score_scale, mf.y, lane, pf);
 
-    for (int n = 0; n < N; n++) {
+    // One iteration per chunk cc (stage cc % kStages), entered with the
+    // chunk's first unit scored (pf) and its units' qk / pv still to run:
+    // qk of the next unit is always issued before pv of the current one.
+    int n = 0;  // units of the warp's range before chunk cc
+    for (int cc = 0;; cc++) {
         const int s = cc % kStages;
-        const bool more = n + 1 < N;
-        const bool same = UPS > 1 && k + 1 < nh;  // unit n+1 is in the same chunk
+        const float fac = mf.x * p.score_scale;
+        const int nh = UPS > 1 ? __float_as_int(mf.w) : 1;
+        if (UPS > 1 && nh > 1) {  // the chunk's second unit (int4: the page's second half)
+            float sc1[4];
+            cs.qk(ws.k[s] + kUnitBytes, lane, sc1);
+            cs.pv(ws.v[s], pf, lane);
+            cs.softmax(sc1, mi.w - UT, fac, mf.y, lane, pf);
+        }
+        const bool more = cc + 1 < ci;  // chunk cc + 1 was issued before chunk cc was consumed
         int4 mi1 = mi;
         float4 mf1 = mf;
-        int k1 = k + 1;
         float sc1[4];
         if (more) {
-            int s1 = s;
-            if (!same) {
-                s1 = (cc + 1) % kStages;
-                if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((cc + 1) / kStages) & 1))) {
-                    if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
-                    drain(cc + 2);
-                    return;
-                }
-                mi1 = *reinterpret_cast<const int4 *>(&ws.meta[s1].b);
-                mf1 = *reinterpret_cast<const float4 *>(&ws.meta[s1].sk);
-                k1 = 0;
-                if (__float_as_int(mf1.z)) cs.load_q(ws.q[s1], lane);
+            const int s1 = (cc + 1) % kStages;
+            if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((cc + 1) / kStages) & 1))) {
+                if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
+                drain(cc + 2);
+                return;
             }
-            cs.qk(ws.k[s1] + k1 * kUnitBytes, lane, sc1);  // unit n+1: independent of the pv below
+            mi1 = *reinterpret_cast<const int4 *>(&ws.meta[s1].b);
+            mf1 = *reinterpret_cast<const float4 *>(&ws.meta[s1].sk);
+            if (__float_as_int(mf1.z)) cs.load_q(ws.q[s1], lane);
+            cs.qk(ws.k[s1], lane, sc1);  // the next chunk's first unit: independent of the pv below
         }
-        cs.pv(ws.v[s] + k * kUnitBytes, pf, lane);     // unit n
-        if (!same) {  // chunk cc is consumed: refill its stage
-            __syncwarp();
-            if (nis < N) issue();
+        cs.pv(ws.v[s] + (nh - 1) * kUnitBytes, pf, lane);  // the chunk's last unit
+        n += nh;
+        __syncwarp();  // every lane is done with stage s: refill it
+        if (nis < N) issue();
+        if (!more) break;
+        if (__float_as_int(mf1.z)) {  // the next chunk starts a new (sequence, head)
+            flush(cur_b, cur_h, seg_n, n);
+            cs.reset();
+            cur_b = mi1.x;
+            cur_h = mi1.y;
+            seg_n = n;
         }
-        if (more) {
-            if (!same) {
-                if (__float_as_int(mf1.z)) {  // unit n+1 starts a new (sequence, head)
-                    flush(cur_b, cur_h, seg_n, n + 1);
-                    cs.reset();
-                    cur_b = mi1.x;
-                    cur_h = mi1.y;
-                    seg_n = n + 1;
-                }
-                ++cc;
-                if (UPS > 1) nh = __float_as_int(mf1.w);
-            }
-            cs.softmax(sc1, min(UT, mi1.w - k1 * UT), mf1.x * p.score_scale, mf1.y, lane, pf);
-            k = k1;
-            mi = mi1;
-            mf = mf1;
-        }
+        cs.softmax(sc1, min(UT, mi1.w), mf1.x * p.score_scale, mf1.y, lane, pf);
+        mi = mi1;
+        mf = mf1;
     }
     flush(cur_b, cur_h, seg_n, N);
 }
