@@ -12,14 +12,14 @@
 //   unit   = 32 tokens (int4) or 16 tokens (int8) of one (sequence, head):
 //            2 KiB of K codes + 2 KiB of V codes, contiguous inside one page;
 //   order  = sequence-major, then head, then unit;
-//   warps  = a persistent grid of one CTA per SM (12 warps int4, 16 warps
-//            int8); warp g owns the contiguous unit range [U g / G, U (g+1) / G),
+//   warps  = a persistent grid of one CTA of 12 warps per SM; warp g owns
+//            the contiguous unit range [U g / G, U (g+1) / G),
 //            so every warp streams the same number of bytes whatever the
 //            length mix;
-//   stream = each warp runs its own ring of shared-memory stages (int4: 2
-//            stages of a whole page = 2 units; int8: 3 stages of 1 unit)
-//            filled by bulk async copies (cp.async.bulk, completing on one
-//            mbarrier per stage), issued by lane 0 as a stage frees;
+//   stream = each warp runs its own ring of 2 shared-memory stages of 2
+//            units (int4: a whole page; int8: half a page) filled by bulk
+//            async copies (cp.async.bulk, completing on one mbarrier per
+//            stage); lane 0 refills a stage as soon as it is consumed;
 //   math   = s = scale_k * (q . c) * softmax_scale, online softmax in fp32
 //            (base 2), acc += p * scale_v * c with fp32 accumulation;
 //   split  = a (sequence, head) wholly inside one warp's range is written as
@@ -41,9 +41,8 @@ constexpr int kMinUnitsPerWarp = 2;
 template <int FMT>
 struct DecFmt;
 // A stage holds up to kUnitsPerStage consecutive units of one page (one bulk
-// copy each for K and V).  int4: a stage is a whole page (both 32-token
-// units), two stages per warp; int8 (lighter math, more latency-bound): one
-// 16-token unit per stage, 3 stages.  One CTA per SM holds all the warps:
+// copy each for K and V): two 32-token units = a whole page for int4, two
+// 16-token units = half a page for int8; two stages per warp.  One CTA per SM holds all the warps:
 // the warp scheduler favours older CTAs, so with several CTAs per SM the
 // warps of the youngest ran ~16% slower than those of the oldest and the SM
 // waited for them; the warps of one CTA progress at the same rate.
@@ -63,11 +62,11 @@ struct DecFmt<KVQ_INT8_PAGE> {
     static constexpr int kRowBytes = 128;
     static constexpr int kUnitTok = 16;
     static constexpr int kUnitsPerPage = 4;
-    static constexpr int kUnitsPerStage = 1;
-    static constexpr int kStages = 3;
-    static constexpr int kWarps = 16;
+    static constexpr int kUnitsPerStage = 2;
+    static constexpr int kStages = 2;
+    static constexpr int kWarps = 12;
     static constexpr int kCtasPerSm = 1;
-    static constexpr int kMergeBatch = 4;  // within the 128-register budget of 16 warps
+    static constexpr int kMergeBatch = 4;
 };
 
 // what a stage holds: units c .. c + nunits - 1 of (b, h), ntok tokens in all
