@@ -216,6 +216,11 @@ static void attend_range(const double *qv, const double *kh, const double *vh, i
  * Decode attention over the paged cache, binary64 throughout:
  *   s_t = softmax_scale * sum_d q_d * k^_{t,d};  p = softmax(s);  o_d = sum_t p_t v^_{t,d}
  *
+ * Grouped query heads: the cache holds Hkv heads and q holds Hq = g * Hkv
+ * heads; query head i reads cache head i / g (consecutive query heads share a
+ * cache head, the grouping of grouped-query / multi-query attention).  g = 1
+ * is plain multi-head attention.
+ *
  * num_splits <= 1 evaluates the definition directly.  num_splits > 1 cuts the
  * tokens of every (sequence, head) into that many contiguous ranges, evaluates
  * (m_i, l_i, acc_i) per range and merges them:
@@ -223,23 +228,24 @@ static void attend_range(const double *qv, const double *kh, const double *vh, i
  * which equals the direct result up to rounding; tests use it to pin the merge
  * step of split decoding.
  *
- *   codes   : [num_pages][H][64][D/2 or D];  scales : [num_pages][H]
+ *   codes   : [num_pages][Hkv][64][D/2 or D];  scales : [num_pages][Hkv]
  *   block_table : [B][max_blocks]  page of block j of sequence b
  *   seq_lens    : [B]
- *   q           : fp16 bits [B][H][D]
- *   out         : binary64 [B][H][D]
- * returns 0, or -1 on bad arguments (a block-table entry outside
- * [0, num_pages) or a length beyond max_blocks * 64).
+ *   q           : fp16 bits [B][Hq][D]
+ *   out         : binary64 [B][Hq][D]
+ * returns 0, or -1 on bad arguments (Hq not a multiple of Hkv, a block-table
+ * entry outside [0, num_pages) or a length beyond max_blocks * 64).
  */
-int orc_decode_attention(int fmt, int32_t H, int32_t D, int32_t num_pages,
-                         const uint8_t *k_codes, const uint8_t *v_codes,
-                         const float *k_scales, const float *v_scales,
-                         const int32_t *block_table, int32_t max_blocks,
-                         const int32_t *seq_lens, int32_t B, const uint16_t *q,
-                         double softmax_scale, int32_t num_splits, double *out)
+int orc_decode_attention_gqa(int fmt, int32_t Hkv, int32_t Hq, int32_t D, int32_t num_pages,
+                             const uint8_t *k_codes, const uint8_t *v_codes,
+                             const float *k_scales, const float *v_scales,
+                             const int32_t *block_table, int32_t max_blocks,
+                             const int32_t *seq_lens, int32_t B, const uint16_t *q,
+                             double softmax_scale, int32_t num_splits, double *out)
 {
-    if ((fmt != ORC_INT4 && fmt != ORC_INT8) || H <= 0 || D <= 0 || (D % 2) || B < 0)
+    if ((fmt != ORC_INT4 && fmt != ORC_INT8) || Hkv <= 0 || Hq <= 0 || (Hq % Hkv) || D <= 0 || (D % 2) || B < 0)
         return -1;
+    const int32_t g = Hq / Hkv;
     for (int32_t b = 0; b < B; b++) {
         int32_t L = seq_lens[b];
         if (L < 0 || L > max_blocks * ORC_BLOCK) return -1;
@@ -254,16 +260,17 @@ int orc_decode_attention(int fmt, int32_t H, int32_t D, int32_t num_pages,
         int32_t L = seq_lens[b];
         double *kh = (double *)malloc(sizeof(double) * ((size_t)L * D + 1));
         double *vh = (double *)malloc(sizeof(double) * ((size_t)L * D + 1));
-        for (int32_t h = 0; h < H; h++) {
-            double *dst = out + ((size_t)b * H + h) * D;
+        for (int32_t hq = 0; hq < Hq; hq++) {
+            const int32_t h = hq / g;  /* the cache head this query head reads */
+            double *dst = out + ((size_t)b * Hq + hq) * D;
             if (L == 0) {
                 for (int d = 0; d < D; d++) dst[d] = 0.0;
                 continue;
             }
-            gather_dequant(fmt, H, D, k_codes, v_codes, k_scales, v_scales,
+            gather_dequant(fmt, Hkv, D, k_codes, v_codes, k_scales, v_scales,
                            block_table + (size_t)b * max_blocks, L, h, kh, vh);
             for (int d = 0; d < D; d++)
-                qv[d] = (double)orc_half_to_float(q[((size_t)b * H + h) * D + d]);
+                qv[d] = (double)orc_half_to_float(q[((size_t)b * Hq + hq) * D + d]);
             int32_t S = num_splits < 1 ? 1 : num_splits;
             if (S > L) S = L;
             double m_all = -INFINITY, l_all = 0.0;
@@ -293,6 +300,18 @@ int orc_decode_attention(int fmt, int32_t H, int32_t D, int32_t num_pages,
     free(qv);
     free(o);
     return 0;
+}
+
+/* multi-head attention: every query head has its own cache head (g = 1) */
+int orc_decode_attention(int fmt, int32_t H, int32_t D, int32_t num_pages,
+                         const uint8_t *k_codes, const uint8_t *v_codes,
+                         const float *k_scales, const float *v_scales,
+                         const int32_t *block_table, int32_t max_blocks,
+                         const int32_t *seq_lens, int32_t B, const uint16_t *q,
+                         double softmax_scale, int32_t num_splits, double *out)
+{
+    return orc_decode_attention_gqa(fmt, H, H, D, num_pages, k_codes, v_codes, k_scales, v_scales, block_table,
+                                    max_blocks, seq_lens, B, q, softmax_scale, num_splits, out);
 }
 
 /*

@@ -33,6 +33,10 @@ def lib():
                                            vp, vp, vp, vp, vp, ctypes.c_int32, vp, ctypes.c_int32, vp,
                                            ctypes.c_double, ctypes.c_int32, vp]
         L.orc_decode_attention.restype = ctypes.c_int
+        L.orc_decode_attention_gqa.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.c_int32, vp, vp, vp, vp, vp, ctypes.c_int32, vp,
+                                               ctypes.c_int32, vp, ctypes.c_double, ctypes.c_int32, vp]
+        L.orc_decode_attention_gqa.restype = ctypes.c_int
         L.orc_value_absmax.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int32, vp, vp, vp,
                                        ctypes.c_int32, vp, ctypes.c_int32, vp]
         L.orc_value_absmax.restype = ctypes.c_int
@@ -68,7 +72,9 @@ def quantize(fmt, x_bits):
 
 def decode_attention(fmt, k_codes, v_codes, k_scales, v_scales, block_table, seq_lens, q_bits,
                      softmax_scale, num_splits=1):
-    """Binary64 decode attention over a paged cache.  Returns float64 [B][H][D]."""
+    """Binary64 decode attention over a paged cache.  Returns float64 [B][Hq][D].
+    q may hold Hq = g * Hkv heads for a cache of Hkv heads (query head i reads
+    cache head i // g); Hq == Hkv is multi-head attention."""
     k_codes = np.ascontiguousarray(k_codes, dtype=np.uint8)
     v_codes = np.ascontiguousarray(v_codes, dtype=np.uint8)
     k_scales = np.ascontiguousarray(k_scales, dtype=np.float32)
@@ -76,12 +82,17 @@ def decode_attention(fmt, k_codes, v_codes, k_scales, v_scales, block_table, seq
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     q = np.ascontiguousarray(q_bits, dtype=np.uint16)
-    B, H, D = q.shape
-    num_pages = k_codes.shape[0]
-    out = np.zeros((B, H, D), dtype=np.float64)
-    rc = lib().orc_decode_attention(fmt, H, D, num_pages, _p(k_codes), _p(v_codes), _p(k_scales),
-                                    _p(v_scales), _p(bt), bt.shape[1], _p(sl), B, _p(q),
-                                    float(softmax_scale), int(num_splits), _p(out))
+    B, Hq, D = q.shape
+    num_pages, Hkv = k_codes.shape[0], k_codes.shape[1]
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    if Hq == Hkv:
+        rc = lib().orc_decode_attention(fmt, Hq, D, num_pages, _p(k_codes), _p(v_codes), _p(k_scales),
+                                        _p(v_scales), _p(bt), bt.shape[1], _p(sl), B, _p(q),
+                                        float(softmax_scale), int(num_splits), _p(out))
+    else:
+        rc = lib().orc_decode_attention_gqa(fmt, Hkv, Hq, D, num_pages, _p(k_codes), _p(v_codes), _p(k_scales),
+                                            _p(v_scales), _p(bt), bt.shape[1], _p(sl), B, _p(q),
+                                            float(softmax_scale), int(num_splits), _p(out))
     if rc != 0:
         raise ValueError("orc_decode_attention rejected its arguments")
     return out

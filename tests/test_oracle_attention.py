@@ -224,3 +224,37 @@ def test_matches_independent_numpy_softmax():
         s = K @ q[0, h].astype(np.float64) * SM
         p = np.exp(s - s.max())
         np.testing.assert_allclose(out[0, h], p @ V / p.sum(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8])
+@pytest.mark.parametrize("g", [2, 4])
+def test_grouped_heads_equal_multi_head_over_repeated_heads(fmt, g):
+    """Grouped query heads (Hq = g * Hkv, query head i reads cache head i // g)
+    give exactly the multi-head result over a cache whose head i is a copy of
+    cache head i // g: a wrong head mapping (i % Hkv, or the first head of the
+    group for all) fails this."""
+    Hkv = 3
+    kc, vc, ks, vs = _random_cache(fmt, 5, Hkv, 21)
+    rep = np.repeat(np.arange(Hkv), g)
+    kc2, vc2, ks2, vs2 = kc[:, rep], vc[:, rep], ks[:, rep], vs[:, rep]
+    bt = np.array([[4, 0, 2], [1, 3, 0]], np.int32)
+    lens = np.array([150, 77], np.int32)
+    q = np.random.default_rng(22).standard_normal((2, Hkv * g, D)).astype(np.float16).view(np.uint16)
+    gqa = orc.decode_attention(fmt, kc, vc, ks, vs, bt, lens, q, SM)
+    mha = orc.decode_attention(fmt, kc2, vc2, ks2, vs2, bt, lens, q, SM)
+    assert gqa.shape == (2, Hkv * g, D)
+    assert np.array_equal(gqa, mha)
+    # the heads of one group differ (their queries differ) and follow their own cache head
+    assert not np.array_equal(gqa[:, 0], gqa[:, 1])
+    K = _dequant(fmt, kc, ks, bt[0], 150, 1)
+    V = _dequant(fmt, vc, vs, bt[0], 150, 1)
+    s = K @ q[0, g].view(np.float16).astype(np.float64) * SM  # query head g reads cache head 1
+    p = np.exp(s - s.max())
+    np.testing.assert_allclose(gqa[0, g], p @ V / p.sum(), rtol=1e-12, atol=1e-12)
+
+
+def test_grouped_heads_reject_a_non_multiple():
+    kc, vc, ks, vs = _random_cache(orc.INT4, 2, 2, 23)
+    q = np.zeros((1, 3, D), np.uint16)
+    with pytest.raises(ValueError):
+        orc.decode_attention(orc.INT4, kc, vc, ks, vs, np.array([[0]], np.int32), np.array([10], np.int32), q, SM)
