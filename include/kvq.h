@@ -178,6 +178,27 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
                                 size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * kvq_decode_attention_gqa -- kvq_decode_attention with grouped query heads
+ * (grouped-query / multi-query attention; the pages' decode of MLA absorbed
+ * into MQA, "DeepSeek R1 performance tips", ddd.cn section 2).  q and out hold
+ * num_q_heads = g * cache->num_heads heads; query head i reads cache head
+ * i / g, so one pass over each cache head's codes serves its g query heads:
+ *   q, out           fp16 [num_seqs][num_q_heads][head_dim], 16-byte aligned
+ *   workspace        >= kvq_decode_workspace_bytes_gqa(...) bytes, zero-filled
+ *                    once before first use (as for kvq_decode_attention)
+ * g = 1 is kvq_decode_attention.  Supported: g = 1 for both formats, g = 2 and
+ * 4 for KVQ_INT4_B64; other g return KVQ_ERR_UNSUPPORTED, and num_q_heads not
+ * a multiple of cache->num_heads returns KVQ_ERR_INVALID_ARG.  Other errors as
+ * for kvq_decode_attention.
+ */
+size_t kvq_decode_workspace_bytes_gqa(kvq_format fmt, int32_t num_kv_heads, int32_t num_q_heads,
+                                      int32_t head_dim);
+kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, int32_t num_q_heads,
+                                    const int32_t *block_table, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                    int32_t num_seqs, float softmax_scale, uint16_t *out, void *workspace,
+                                    size_t workspace_bytes, kvq_stream_t stream);
+
+/*
  * kvq_decode_attention_noalloc -- kvq_decode_attention without a caller
  * workspace.  The pages have no counterpart to this entry point; it exists for
  * callers that cannot allocate device memory when they run decode attention:

@@ -92,10 +92,26 @@ kvq_status kvq_append(const kvq_cache *cache, const uint16_t *k_new, const uint1
     return KVQ_OK;
 }
 
+// query heads per cache head, or 0 when num_q_heads is not a supported
+// multiple of num_kv_heads
+static int group_of(int fmt, int32_t num_kv_heads, int32_t num_q_heads)
+{
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+    const int g = num_q_heads / num_kv_heads;
+    return kvq::decode_group_supported(fmt, g) ? g : 0;
+}
+
 size_t kvq_decode_workspace_bytes(kvq_format fmt, int32_t num_heads, int32_t head_dim)
 {
-    if (!fmt_ok(fmt) || head_dim != kvq::kHeadDim || num_heads <= 0) return 0;
-    return kvq::decode_workspace_bytes(fmt);
+    return kvq_decode_workspace_bytes_gqa(fmt, num_heads, num_heads, head_dim);
+}
+
+size_t kvq_decode_workspace_bytes_gqa(kvq_format fmt, int32_t num_kv_heads, int32_t num_q_heads, int32_t head_dim)
+{
+    if (!fmt_ok(fmt) || head_dim != kvq::kHeadDim) return 0;
+    const int g = group_of(fmt, num_kv_heads, num_q_heads);
+    if (g == 0) return 0;
+    return kvq::decode_workspace_bytes(fmt, g);
 }
 
 kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const int32_t *block_table,
@@ -103,12 +119,25 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
                                 float softmax_scale, uint16_t *out, void *workspace, size_t workspace_bytes,
                                 kvq_stream_t stream)
 {
+    if (!cache) return KVQ_ERR_INVALID_ARG;
+    return kvq_decode_attention_gqa(cache, q, cache->num_heads, block_table, max_blocks_per_seq, seq_lens,
+                                    num_seqs, softmax_scale, out, workspace, workspace_bytes, stream);
+}
+
+kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, int32_t num_q_heads,
+                                    const int32_t *block_table, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                    int32_t num_seqs, float softmax_scale, uint16_t *out, void *workspace,
+                                    size_t workspace_bytes, kvq_stream_t stream)
+{
     kvq_status st = check_cache(cache);
     if (st != KVQ_OK) return st;
     if (num_seqs < 0 || max_blocks_per_seq <= 0 || !isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_q_heads % cache->num_heads) return KVQ_ERR_INVALID_ARG;
+    const int g = group_of(cache->fmt, cache->num_heads, num_q_heads);
+    if (g == 0) return KVQ_ERR_UNSUPPORTED;
     if (num_seqs == 0) return KVQ_OK;
     if (!q || !block_table || !seq_lens || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
-    const size_t need = kvq::decode_workspace_bytes(cache->fmt);
+    const size_t need = kvq::decode_workspace_bytes(cache->fmt, g);
     if (need == 0) return KVQ_ERR_CUDA;
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     const int grid_warps = kvq::decode_grid_warps(cache->fmt);
@@ -122,10 +151,12 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
     p.num_pages = cache->num_pages;
     p.max_blocks = max_blocks_per_seq;
     p.score_scale = softmax_scale * 1.4426950408889634f;
+    p.group = g;
     p.partials = reinterpret_cast<float *>(workspace);
     p.pieces = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(workspace) +
-                                                      (size_t)grid_warps * 2 * kvq::kPartialStride * sizeof(float));
-    const int64_t HD = (int64_t)cache->num_heads * kvq::kHeadDim;
+                                                      (size_t)grid_warps * 2 * g * kvq::kPartialStride *
+                                                          sizeof(float));
+    const int64_t HD = (int64_t)num_q_heads * kvq::kHeadDim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (int32_t b0 = 0; b0 < num_seqs; b0 += kvq::kMaxSeqsPerLaunch) {
         kvq::DecodeParams d = p;

@@ -13,7 +13,8 @@
 //            2 KiB of K codes + 2 KiB of V codes, contiguous inside one page;
 //   order  = sequence-major, then head, then unit;
 //   warps  = a persistent grid of one CTA of 12 warps per SM; warp g owns
-//            the contiguous unit range [U g / G, U (g+1) / G),
+//            the contiguous unit range [U g / GW, U (g+1) / GW) (GW warps
+//            have work),
 //            so every warp streams the same number of bytes whatever the
 //            length mix;
 //   stream = each warp runs its own ring of 2 shared-memory stages of 2
@@ -76,21 +77,21 @@ struct alignas(16) StageMeta {
     int32_t new_seg, nunits;
 };
 
-template <int kStages, int kStageBytes>
+template <int kStages, int kStageBytes, int kQRows>
 struct alignas(128) WarpSmem {
     uint8_t k[kStages][kStageBytes];
     uint8_t v[kStages][kStageBytes];
-    uint16_t q[kStages][kHeadDim];
+    uint16_t q[kStages][kQRows * kHeadDim];  // the query rows of the stage's cache head
     StageMeta meta[kStages];
     uint64_t full[kStages];
 };
 
 constexpr size_t kSeqSmemBytes = ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 127) / 128 * 128;
-template <int FMT>
+template <int FMT, int G>
 constexpr size_t dec_smem_bytes()
 {
     using F = DecFmt<FMT>;
-    return F::kWarps * sizeof(WarpSmem<F::kStages, F::kUnitsPerStage * kUnitBytes>) + kSeqSmemBytes;
+    return F::kWarps * sizeof(WarpSmem<F::kStages, F::kUnitsPerStage * kUnitBytes, G>) + kSeqSmemBytes;
 }
 
 // ---------------------------------------------------------------------------
@@ -441,6 +442,233 @@ struct Consumer<KVQ_INT4_B64> {
     }
 };
 
+// int4 with grouped query heads: G = 2 or 4 query heads share each cache
+// head, and one pass over the codes serves all G (the mma columns that the
+// multi-head consumer fills with copies of q carry the group's other heads).
+// Lane (grp = lane >> 2, t = lane & 3):
+//   QK: column c of B holds q of head hq(c) = (((c >> 2) << 1) | (c & 1)) % G,
+//       so the lane receives, for tokens grp and grp + 8 of each tile, the
+//       scores of its head slots c = 0, 1: heads (2 (t >> 1) + c) % G.
+//   PV: column c of B holds part (c >> 1) & 1 (0: RN16(x), 1: the remainder)
+//       of head hq(c); the lane's accumulators are then exactly its slot
+//       heads, part t & 1, so a rescale of a head's running max is local.
+//   The weights of column grp_d come from lane 4 * token + (grp_d >> 1),
+//   slot grp_d & 1 (that lane holds head hq(grp_d) and produces part
+//   (grp_d >> 1) & 1).
+template <int G>
+struct ConsumerGqa {
+    static_assert(G == 2 || G == 4, "query heads per cache head");
+    uint32_t qb[8][2];
+    float acc[8][4];
+    float m_run[2];
+    float l_lane[2];
+    Magic mk;
+
+    __device__ __forceinline__ void reset()
+    {
+        mk.init();
+        m_run[0] = m_run[1] = -INFINITY;
+        l_lane[0] = l_lane[1] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) acc[i][j] = 0.0f;
+    }
+
+    // qs: the group's G query rows (fp16 [G][128])
+    __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        const int head = (((g >> 2) << 1) | (g & 1)) % G;  // column g of B
+        const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + head * kHeadDim + 32 * t);
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const uint4 v = q4[m];
+            qb[2 * m][0] = __byte_perm(v.x, v.z, 0x5410);
+            qb[2 * m][1] = __byte_perm(v.x, v.z, 0x7632);
+            qb[2 * m + 1][0] = __byte_perm(v.y, v.w, 0x5410);
+            qb[2 * m + 1][1] = __byte_perm(v.y, v.w, 0x7632);
+        }
+    }
+
+    // raw dot products: sc[4 tau + 2 r + c] = token 16 tau + grp + 8 r, head slot c
+    __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[8]) const
+    {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int tau = 0; tau < 2; tau++) {
+            float c[4][4];
+#pragma unroll
+            for (int m = 0; m < 4; m++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) c[m][e] = 0.0f;
+            const uint4 wa = *reinterpret_cast<const uint4 *>(ks + (16 * tau + g) * 64 + 16 * t);
+            const uint4 wb = *reinterpret_cast<const uint4 *>(ks + (16 * tau + g + 8) * 64 + 16 * t);
+            const uint32_t ua[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t ub[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                uint32_t ca[4], cb[4];
+                widen_int4_u32(ua[m], ca, mk);
+                widen_int4_u32(ub[m], cb, mk);
+                mma16816(c[m], ca[0], cb[0], ca[1], cb[1], qb[2 * m][0], qb[2 * m][1]);
+                mma16816(c[m], ca[2], cb[2], ca[3], cb[3], qb[2 * m + 1][0], qb[2 * m + 1][1]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; e++) sc[4 * tau + e] = (c[0][e] + c[1][e]) + (c[2][e] + c[3][e]);
+        }
+    }
+
+    // online softmax over the unit, per head slot.  px[2 tau + c] = this
+    // lane's part (t & 1) of x = p * sv for tokens (grp, grp + 8) of tile tau,
+    // head slot c, as an fp16 pair
+    __device__ __forceinline__ void softmax(const float sc[8], int ntok, float fac, float sv, int lane,
+                                            uint32_t px[4])
+    {
+        const int g = lane >> 2, t = lane & 3;
+        const uint64_t ff = pk2(fac, fac);
+        float s2[8];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) upk2(mul2(pk2(sc[i], sc[i + 1]), ff), s2[i], s2[i + 1]);
+        if (ntok < 32) {  // the last unit of a sequence: tokens past its end get no weight
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                if (16 * (i >> 2) + 8 * ((i >> 1) & 1) + g >= ntok) s2[i] = -INFINITY;
+        }
+        float lm[2];
+#pragma unroll
+        for (int c = 0; c < 2; c++) lm[c] = fmaxf(fmaxf(s2[c], s2[2 + c]), fmaxf(s2[4 + c], s2[6 + c]));
+        if (__any_sync(kFull, lm[0] > m_run[0] || lm[1] > m_run[1])) {  // a running maximum moves: rescale
+#pragma unroll
+            for (int c = 0; c < 2; c++) {
+                float mu = lm[c];  // max over the 8 lanes of this t (the tokens of the unit)
+                mu = fmaxf(mu, __shfl_xor_sync(kFull, mu, 4));
+                mu = fmaxf(mu, __shfl_xor_sync(kFull, mu, 8));
+                mu = fmaxf(mu, __shfl_xor_sync(kFull, mu, 16));
+                mu = fmaxf(mu, m_run[c]);
+                const float alpha = ex2_approx(m_run[c] - mu);
+                l_lane[c] *= alpha;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    acc[i][c] *= alpha;
+                    acc[i][2 + c] *= alpha;
+                }
+                m_run[c] = mu;
+            }
+        }
+        float pe[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) pe[i] = ex2_approx(s2[i] - m_run[i & 1]);
+        l_lane[0] += (pe[0] + pe[2]) + (pe[4] + pe[6]);
+        l_lane[1] += (pe[1] + pe[3]) + (pe[5] + pe[7]);
+        const uint64_t vv = pk2(sv, sv);
+        const bool lo_part = t & 1;
+#pragma unroll
+        for (int tau = 0; tau < 2; tau++)
+#pragma unroll
+            for (int c = 0; c < 2; c++) {
+                uint32_t hi, lo;
+                hi_lo_pairs(mul2(pk2(pe[4 * tau + c], pe[4 * tau + 2 + c]), vv), hi, lo);
+                px[2 * tau + c] = lo_part ? lo : hi;
+            }
+    }
+
+    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t px[4], int lane)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        // column g of B: head slot g & 1, part (g >> 1) & 1, from lanes 4 token + (g >> 1)
+        const int src = 8 * t + (g >> 1);
+        const bool slot1 = g & 1;
+#pragma unroll
+        for (int kap = 0; kap < 2; kap++) {
+            const uint32_t a0 = __shfl_sync(kFull, px[2 * kap], src);          // tokens 2t, 2t+8
+            const uint32_t a1 = __shfl_sync(kFull, px[2 * kap + 1], src);
+            const uint32_t c0 = __shfl_sync(kFull, px[2 * kap], src + 4);      // tokens 2t+1, 2t+9
+            const uint32_t c1 = __shfl_sync(kFull, px[2 * kap + 1], src + 4);
+            const uint32_t ua = slot1 ? a1 : a0;
+            const uint32_t ub = slot1 ? c1 : c0;
+            const uint32_t b0 = __byte_perm(ua, ub, 0x5410);
+            const uint32_t b1 = __byte_perm(ua, ub, 0x7632);
+#pragma unroll
+            for (int R = 0; R < 2; R++) {
+                // word 8R + g (elements 64R + 8g .. +7) of tokens 16kap + 2t, +1, +8, +9
+                const uint8_t *vb = vs + (16 * kap + 2 * t) * 64 + 4 * (8 * R + g);
+                const uint32_t wa = *reinterpret_cast<const uint32_t *>(vb);
+                const uint32_t wb = *reinterpret_cast<const uint32_t *>(vb + 64);
+                const uint32_t wc = *reinterpret_cast<const uint32_t *>(vb + 8 * 64);
+                const uint32_t wd = *reinterpret_cast<const uint32_t *>(vb + 9 * 64);
+                uint32_t xab[4], xcd[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    // selector nibbles: result bytes = [wa.k, wa.k, wb.k, wb.k]
+                    const uint32_t bsel = (uint32_t)k | ((uint32_t)k << 4) | ((uint32_t)(4 + k) << 8) |
+                                          ((uint32_t)(4 + k) << 12);
+                    xab[k] = __byte_perm(wa, wb, bsel);
+                    xcd[k] = __byte_perm(wc, wd, bsel);
+                }
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++) {
+                    const bool odd = jj & 1;
+                    mma16816(acc[4 * R + jj], nib_pair(xab[jj >> 1], odd, mk), nib_pair(xab[2 + (jj >> 1)], odd, mk),
+                             nib_pair(xcd[jj >> 1], odd, mk), nib_pair(xcd[2 + (jj >> 1)], odd, mk), b0, b1);
+                }
+            }
+        }
+    }
+
+
+    // the group's output rows (orow: G rows) or partial slots (part: G
+    // partials of kPartialStride floats).  The two parts of a head are in lanes
+    // t and t ^ 1; lanes with even t, t >> 1 < G / 2, write heads 2 (t >> 1) + c.
+    __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        float l[2];
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+            float v = l_lane[c];
+            v += __shfl_xor_sync(kFull, v, 4);
+            v += __shfl_xor_sync(kFull, v, 8);
+            v += __shfl_xor_sync(kFull, v, 16);
+            l[c] = v;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) acc[i][j] += __shfl_xor_sync(kFull, acc[i][j], 1);
+        if ((t & 1) || 2 * (t >> 1) >= G) return;
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+            const int head = 2 * (t >> 1) + c;
+#pragma unroll
+            for (int R = 0; R < 2; R++) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    v[e] = acc[4 * R + e][c];
+                    v[4 + e] = acc[4 * R + e][2 + c];
+                }
+                if (orow) {
+                    const float inv = 1.0f / l[c];
+                    uint4 o;
+                    o.x = h2_bits(__floats2half2_rn(v[0] * inv, v[1] * inv));
+                    o.y = h2_bits(__floats2half2_rn(v[2] * inv, v[3] * inv));
+                    o.z = h2_bits(__floats2half2_rn(v[4] * inv, v[5] * inv));
+                    o.w = h2_bits(__floats2half2_rn(v[6] * inv, v[7] * inv));
+                    *reinterpret_cast<uint4 *>(orow + head * kHeadDim + 64 * R + 8 * g) = o;
+                } else {
+                    float4 *d4 = reinterpret_cast<float4 *>(part + head * kPartialStride + 4 + 64 * R + 8 * g);
+                    d4[0] = make_float4(v[0], v[1], v[2], v[3]);
+                    d4[1] = make_float4(v[4], v[5], v[6], v[7]);
+                }
+            }
+            if (part && g == 0) {
+                part[head * kPartialStride] = m_run[c];
+                part[head * kPartialStride + 1] = l[c];
+            }
+        }
+    }
+};
 // int8: CUDA-core path.  K: lane = (token group g = lane >> 3, 16-element
 // chunk r = lane & 7), 4 passes of 4 tokens, reduce-scatter over the 8 lanes of
 // a token; V: lane = (16-element chunk, token subset), weights shuffled from
@@ -614,12 +842,14 @@ __device__ __noinline__ bool last_piece(unsigned long long *slot, uint32_t piece
 // are independent of one another, so a merge of up to kBatch pieces costs one
 // round trip to L2.
 // (not inlined: a rare path, kept out of the streaming loop's register budget)
+// slot_floats: floats per partial slot (G partials of a group of query
+// heads); head: which of them.
 template <int kBatch>
-__device__ __noinline__ void merge_pieces(const float *partials, int64_t gf, int cnt, int first_slot,
-                                             uint16_t *out_row, int lane)
+__device__ __noinline__ void merge_pieces(const float *partials, int64_t slot_floats, int head, int64_t gf, int cnt,
+                                          int first_slot, uint16_t *out_row, int lane)
 {
-    const float *pbase = partials + gf * 2 * kPartialStride;
-    auto part = [&](int i) { return pbase + ((int64_t)i * 2 + (i == 0 ? first_slot : 0)) * kPartialStride; };
+    const float *pbase = partials + gf * 2 * slot_floats + (int64_t)head * kPartialStride;
+    auto part = [&](int i) { return pbase + ((int64_t)i * 2 + (i == 0 ? first_slot : 0)) * slot_floats; };
     // lane i < cnt: (m, l) of piece i; every lane: its 4 elements of pieces
     // 0 .. kBatch-1 and their m -- all issued before any of them is used
     float2 ml = make_float2(-INFINITY, 0.0f);
@@ -667,14 +897,25 @@ __device__ __noinline__ void merge_pieces(const float *partials, int64_t gf, int
         make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
 }
 
+template <int FMT, int G>
+struct ConsumerFor {
+    using type = ConsumerGqa<G>;
+};
 template <int FMT>
+struct ConsumerFor<FMT, 1> {
+    using type = Consumer<FMT>;
+};
+
+// G: query heads per cache head (1: multi-head attention)
+template <int FMT, int G>
 __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPerSm)
     decode_split_kernel(DecodeParams p, int grid_warps)
 {
     using F = DecFmt<FMT>;
     constexpr int kStages = F::kStages;
     constexpr int UPS = F::kUnitsPerStage;
-    using WS = WarpSmem<kStages, UPS * kUnitBytes>;
+    using WS = WarpSmem<kStages, UPS * kUnitBytes, G>;
+    constexpr int64_t kSlotFloats = (int64_t)G * kPartialStride;  // one piece's partials
     constexpr int UT = F::kUnitTok;
     constexpr int UPP = F::kUnitsPerPage;
     constexpr int RB = F::kRowBytes;
@@ -734,21 +975,21 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
                 const int b = base + __ffs(m) - 1;
                 m &= m - 1;
                 if (b % (int)gridDim.x != (int)blockIdx.x) continue;
-                uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)b * H * kHeadDim);
-                for (int e = lane; e < H * (kHeadDim / 8); e += 32) row[e] = make_uint4(0u, 0u, 0u, 0u);
+                uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)b * H * G * kHeadDim);
+                for (int e = lane; e < H * G * (kHeadDim / 8); e += 32) row[e] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
     }
 
     const int64_t U = s_cu[B];
     if (U == 0) return;
-    const int64_t G = imin64((int64_t)grid_warps, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);
+    const int64_t GW = imin64((int64_t)grid_warps, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);  // active warps
     // logical warp index, round-robin over the CTAs: when fewer than all warps
     // have work (G < grid warps) the active ones spread over every SM
     const int gw = warp * (int)gridDim.x + blockIdx.x;
-    if (gw >= G) return;
-    const int64_t x0 = U * gw / G;
-    const int64_t x1 = U * (gw + 1) / G;
+    if (gw >= GW) return;
+    const int64_t x0 = U * gw / GW;
+    const int64_t x1 = U * (gw + 1) / GW;
     if (x0 >= x1) return;
 
     WS &ws = wsm_all[warp];
@@ -824,13 +1065,13 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             // consumed those values (mma operands) before the __syncwarp that
             // precedes this issue, so the copy cannot overtake them.
             const uint32_t cb = (uint32_t)nh * kUnitBytes;
-            const uint32_t bytes = 2 * cb + (new_seg ? kHeadDim * 2 : 0);
+            const uint32_t bytes = 2 * cb + (new_seg ? G * kHeadDim * 2 : 0);
             mbar_arrive_expect_tx(&ws.full[s], bytes);
             const size_t off = ((size_t)pg * H + ih) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
             bulk_copy_g2s(ws.k[s], p.k_codes + off, cb, &ws.full[s]);
             bulk_copy_g2s(ws.v[s], p.v_codes + off, cb, &ws.full[s]);
             if (new_seg)
-                bulk_copy_g2s(ws.q[s], p.q + ((size_t)ib * H + ih) * kHeadDim, kHeadDim * 2, &ws.full[s]);
+                bulk_copy_g2s(ws.q[s], p.q + ((size_t)ib * H + ih) * G * kHeadDim, G * kHeadDim * 2, &ws.full[s]);
         }
         // advance the cursor by the chunk
         ic += nh;
@@ -851,7 +1092,7 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     __syncwarp();
 
     // ---- consumer: qk of unit n+1 overlaps pv of unit n ----
-    Consumer<FMT> cs;
+    typename ConsumerFor<FMT, G>::type cs;
     cs.reset();
     int cur_b = -1, cur_h = -1;
     int seg_n = 0;
@@ -861,15 +1102,17 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         const int64_t u0 = s_cu[b] + (int64_t)h * n;
         const int64_t sa = x0 + na, sb = x0 + nb;
         if (sa == u0 && sb == u0 + n) {
-            cs.finish(lane, p.out + ((int64_t)b * H + h) * kHeadDim, nullptr);
+            cs.finish(lane, p.out + ((int64_t)b * H + h) * G * kHeadDim, nullptr);
         } else {  // cut by a range boundary: the first segment of the warp goes to slot 0, the last to slot 1
-            cs.finish(lane, nullptr, p.partials + ((int64_t)gw * 2 + (na == 0 ? 0 : 1)) * kPartialStride);
+            cs.finish(lane, nullptr, p.partials + ((int64_t)gw * 2 + (na == 0 ? 0 : 1)) * kSlotFloats);
             const int64_t u1 = u0 + n;
-            const int64_t gf = ((u0 + 1) * G - 1) / U;  // warp owning unit u0
-            const int64_t gl = (u1 * G - 1) / U;        // warp owning unit u1 - 1
+            const int64_t gf = ((u0 + 1) * GW - 1) / U;  // warp owning unit u0
+            const int64_t gl = (u1 * GW - 1) / U;        // warp owning unit u1 - 1
             if (last_piece(p.pieces + gl, (uint32_t)(gl - gf + 1), lane, p.status))
-                merge_pieces<F::kMergeBatch>(p.partials, gf, (int)(gl - gf + 1), ((U * gf) / G != u0) ? 1 : 0,
-                             p.out + ((int64_t)b * H + h) * kHeadDim, lane);
+                for (int j = 0; j < G; j++)
+                    merge_pieces<F::kMergeBatch>(p.partials, kSlotFloats, j, gf, (int)(gl - gf + 1),
+                                                 ((U * gf) / GW != u0) ? 1 : 0,
+                                                 p.out + (((int64_t)b * H + h) * G + j) * kHeadDim, lane);
         }
     };
     auto drain = [&](int from) {  // after a timeout: let the copies still in flight land
@@ -888,7 +1131,8 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     cur_b = mi.x;
     cur_h = mi.y;
     cs.load_q(ws.q[0], lane);
-    float sc[4];
+    constexpr int kScores = G == 1 ? 4 : 8;  // scores a lane holds per unit
+    float sc[kScores];
     uint32_t pf[4];
     cs.qk(ws.k[0], lane, sc);
     cs.softmax(sc, min(UT, mi.w), mf.x * p.score_scale, mf.y, lane, pf);
@@ -902,7 +1146,7 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         const float fac = mf.x * p.score_scale;
         const int nh = UPS > 1 ? __float_as_int(mf.w) : 1;
         if (UPS > 1 && nh > 1) {  // the chunk's second unit (int4: the page's second half)
-            float sc1[4];
+            float sc1[kScores];
             cs.qk(ws.k[s] + kUnitBytes, lane, sc1);
             cs.pv(ws.v[s], pf, lane);
             cs.softmax(sc1, mi.w - UT, fac, mf.y, lane, pf);
@@ -910,7 +1154,7 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         const bool more = cc + 1 < ci;  // chunk cc + 1 was issued before chunk cc was consumed
         int4 mi1 = mi;
         float4 mf1 = mf;
-        float sc1[4];
+        float sc1[kScores];
         if (more) {
             const int s1 = (cc + 1) % kStages;
             if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((cc + 1) / kStages) & 1))) {
@@ -942,19 +1186,19 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     flush(cur_b, cur_h, seg_n, N);
 }
 
-template <int FMT>
+template <int FMT, int G>
 static int ctas_per_sm()
 {
     static int cached[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev] == 0) {
-        if (cudaFuncSetAttribute(decode_split_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)dec_smem_bytes<FMT>()) != cudaSuccess)
+        if (cudaFuncSetAttribute(decode_split_kernel<FMT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)dec_smem_bytes<FMT, G>()) != cudaSuccess)
             return 0;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<FMT>, DecFmt<FMT>::kWarps * 32,
-                                                          dec_smem_bytes<FMT>()) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<FMT, G>, DecFmt<FMT>::kWarps * 32,
+                                                          dec_smem_bytes<FMT, G>()) != cudaSuccess)
             return 0;
         constexpr int cap = DecFmt<FMT>::kCtasPerSm;
         cached[dev] = n < 1 ? 1 : (n > cap ? cap : n);
@@ -967,15 +1211,20 @@ int decode_grid_warps(int fmt)
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (fmt == KVQ_INT4_B64) return sms * ctas_per_sm<KVQ_INT4_B64>() * DecFmt<KVQ_INT4_B64>::kWarps;
-    return sms * ctas_per_sm<KVQ_INT8_PAGE>() * DecFmt<KVQ_INT8_PAGE>::kWarps;
+    if (fmt == KVQ_INT4_B64) return sms * ctas_per_sm<KVQ_INT4_B64, 1>() * DecFmt<KVQ_INT4_B64>::kWarps;
+    return sms * ctas_per_sm<KVQ_INT8_PAGE, 1>() * DecFmt<KVQ_INT8_PAGE>::kWarps;
 }
 
-size_t decode_workspace_bytes(int fmt)
+bool decode_group_supported(int fmt, int group)
+{
+    return group == 1 || (fmt == KVQ_INT4_B64 && (group == 2 || group == 4));
+}
+
+size_t decode_workspace_bytes(int fmt, int group)
 {
     const int gw = decode_grid_warps(fmt);
-    if (gw <= 0) return 0;
-    const size_t partial = (size_t)gw * 2 * kPartialStride * sizeof(float);
+    if (gw <= 0 || !decode_group_supported(fmt, group)) return 0;
+    const size_t partial = (size_t)gw * 2 * group * kPartialStride * sizeof(float);
     return partial + (size_t)gw * sizeof(unsigned long long);
 }
 
@@ -984,12 +1233,28 @@ cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s)
     const int gw = decode_grid_warps(fmt);
     if (gw <= 0) return cudaErrorInvalidDevice;
     const int ctas = gw / (fmt == KVQ_INT4_B64 ? DecFmt<KVQ_INT4_B64>::kWarps : DecFmt<KVQ_INT8_PAGE>::kWarps);
-    const DecodeParams &d = p;
-    return (fmt == KVQ_INT4_B64)
-               ? launch_pdl(decode_split_kernel<KVQ_INT4_B64>, dim3(ctas), dim3(DecFmt<KVQ_INT4_B64>::kWarps * 32),
-                            dec_smem_bytes<KVQ_INT4_B64>(), s, d, gw)
-               : launch_pdl(decode_split_kernel<KVQ_INT8_PAGE>, dim3(ctas), dim3(DecFmt<KVQ_INT8_PAGE>::kWarps * 32),
-                            dec_smem_bytes<KVQ_INT8_PAGE>(), s, d, gw);
+    const dim3 grid(ctas);
+    if (fmt == KVQ_INT8_PAGE) {
+        if (p.group != 1) return cudaErrorInvalidValue;
+        return launch_pdl(decode_split_kernel<KVQ_INT8_PAGE, 1>, grid, dim3(DecFmt<KVQ_INT8_PAGE>::kWarps * 32),
+                          dec_smem_bytes<KVQ_INT8_PAGE, 1>(), s, p, gw);
+    }
+    const dim3 block(DecFmt<KVQ_INT4_B64>::kWarps * 32);
+    switch (p.group) {
+    case 1:
+        return launch_pdl(decode_split_kernel<KVQ_INT4_B64, 1>, grid, block, dec_smem_bytes<KVQ_INT4_B64, 1>(), s, p,
+                          gw);
+    case 2:
+        if (ctas_per_sm<KVQ_INT4_B64, 2>() < 1) return cudaErrorInvalidDevice;  // also sets the smem attribute
+        return launch_pdl(decode_split_kernel<KVQ_INT4_B64, 2>, grid, block, dec_smem_bytes<KVQ_INT4_B64, 2>(), s, p,
+                          gw);
+    case 4:
+        if (ctas_per_sm<KVQ_INT4_B64, 4>() < 1) return cudaErrorInvalidDevice;
+        return launch_pdl(decode_split_kernel<KVQ_INT4_B64, 4>, grid, block, dec_smem_bytes<KVQ_INT4_B64, 4>(), s, p,
+                          gw);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace kvq

@@ -51,6 +51,7 @@ struct DecodeParams {
     int32_t num_pages;
     int32_t max_blocks;
     float score_scale;  // softmax_scale * log2(e): scores are kept in the base-2 domain
+    int32_t group;      // query heads per cache head: q and out hold num_heads * group heads
 };
 
 // floats per split partial: m, l, 2 pad, acc[128]
@@ -98,7 +99,8 @@ cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s);
 
 // number of warps of the persistent split grid on the current device (0 on error)
 int decode_grid_warps(int fmt);
-size_t decode_workspace_bytes(int fmt);
+bool decode_group_supported(int fmt, int group);
+size_t decode_workspace_bytes(int fmt, int group);
 cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s);
 
 }  // namespace kvq

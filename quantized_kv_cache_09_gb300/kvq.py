@@ -29,6 +29,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
 
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attention",
+           "kvq_decode_workspace_bytes_gqa", "kvq_decode_attention_gqa",
            "kvq_decode_attention_noalloc", "kvq_get_device_status", "kvq_status_string", "kvq_version")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -72,6 +73,10 @@ def lib():
         L.kvq_decode_workspace_bytes.restype = sz
         L.kvq_decode_attention.argtypes = [cp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, sz, vp]
         L.kvq_decode_attention.restype = ctypes.c_int
+        L.kvq_decode_workspace_bytes_gqa.argtypes = [ctypes.c_int, i32, i32, i32]
+        L.kvq_decode_workspace_bytes_gqa.restype = sz
+        L.kvq_decode_attention_gqa.argtypes = [cp, vp, i32, vp, i32, vp, i32, ctypes.c_float, vp, vp, sz, vp]
+        L.kvq_decode_attention_gqa.restype = ctypes.c_int
         L.kvq_decode_attention_noalloc.argtypes = [cp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp]
         L.kvq_decode_attention_noalloc.restype = ctypes.c_int
         L.kvq_get_device_status.argtypes = [cp, vp, ctypes.POINTER(i32)]
@@ -163,6 +168,27 @@ def kvq_decode_attention(cache, q, block_table, seq_lens, softmax_scale, out, wo
                                       workspace.numel(), _stream(stream, q.device)), "kvq_decode_attention")
 
 
+def kvq_decode_workspace_bytes_gqa(fmt, num_kv_heads, num_q_heads, head_dim=HEAD_DIM):
+    return int(lib().kvq_decode_workspace_bytes_gqa(int(fmt), int(num_kv_heads), int(num_q_heads), int(head_dim)))
+
+
+def kvq_decode_attention_gqa(cache, q, block_table, seq_lens, softmax_scale, out, workspace, stream=None):
+    """out fp16 [B][Hq][128] = decode attention of q fp16 [B][Hq][128] over the
+    cache, Hq = g * cache heads, query head i reading cache head i // g."""
+    _cuda(q, torch.float16, "q")
+    _cuda(out, torch.float16, "out")
+    _cuda(block_table, torch.int32, "block_table")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    _cuda(workspace, torch.uint8, "workspace")
+    B = q.shape[0]
+    if out.shape != q.shape or seq_lens.numel() != B or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("q/out/seq_lens/block_table shapes disagree")
+    _check(lib().kvq_decode_attention_gqa(ctypes.byref(cache.struct), _ptr(q), q.shape[1], _ptr(block_table),
+                                          block_table.shape[1], _ptr(seq_lens), B, float(softmax_scale), _ptr(out),
+                                          _ptr(workspace), workspace.numel(), _stream(stream, q.device)),
+           "kvq_decode_attention_gqa")
+
+
 def kvq_decode_attention_noalloc(cache, q, block_table, seq_lens, softmax_scale, out, stream=None):
     """kvq_decode_attention without a workspace, for callers that cannot
     allocate device memory when they run decode attention (a plugin whose
@@ -231,8 +257,8 @@ class PagedKVCache:
                                 None if s.v_tail is None else s.v_tail + b0 * step, s.status)
         return view
 
-    def workspace(self):
-        n = kvq_decode_workspace_bytes(self.fmt, self.num_heads)
+    def workspace(self, num_q_heads=None):
+        n = kvq_decode_workspace_bytes_gqa(self.fmt, self.num_heads, num_q_heads or self.num_heads)
         if n <= 0:
             raise RuntimeError("kvq_decode_workspace_bytes returned 0")
         return torch.zeros(n, dtype=torch.uint8, device=self.k_codes.device)  # zero-filled before first use
