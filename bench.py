@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="llama2-7b-layer",
-                    choices=["tiny", "llama2-7b-layer", "long-context", "paged-int8", "prefill-append"])
+                    choices=["tiny", "llama2-7b-layer", "long-context", "paged-int8", "prefill-append",
+                             "llama3-8b-layer-gqa"])
     ap.add_argument("--prefill-seqs", type=int, default=64)
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     return ap.parse_args()
@@ -187,10 +188,11 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 # the CPU oracle on a bounded sample of the same step
 # --------------------------------------------------------------------------
-def oracle_step_rate(seconds, seed, threads=None):
-    """Oracle decode steps of the 7B-layer workload: for each sampled sequence,
-    re-quantize its open block (oracle quantize of the 64-token block holding
-    the new token) and attend over its 8193 tokens, all 32 heads, binary64.
+def oracle_step_rate(seconds, seed, threads=None, cfg=None):
+    """Oracle decode steps of a uniform-length decode workload (default: the 7B
+    layer): for each sampled sequence, re-quantize its open block (oracle
+    quantize of the 64-token block holding the new token) and attend over its
+    L + 1 tokens, every query head, binary64.
     Threads run independent sequences (the oracle releases the GIL).
     Returns (steps per second, threads, description)."""
     import numpy as np
@@ -198,7 +200,7 @@ def oracle_step_rate(seconds, seed, threads=None):
     from oracle import oracle as orc
     from quantized_kv_cache_09_gb300.synth import workloads as W
 
-    wl = W.make_workload(CONFIG, seed=seed, extra_tokens=64)
+    wl = W.make_workload(cfg or CONFIG, seed=seed, extra_tokens=64)
     threads = threads or max(1, min(16, os.cpu_count() or 1))
     L = int(wl.lens[0])
     sm = np.float32(1.0 / math.sqrt(wl.D))
@@ -242,8 +244,9 @@ def oracle_step_rate(seconds, seed, threads=None):
         t.join()
     el = time.time() - t0
     steps = sum(done)
+    heads = f"{wl.H} heads" if wl.Hq == wl.H else f"{wl.Hq} query heads over {wl.H} cache heads"
     desc = (f"{steps} oracle sequence-steps (append 1 token + binary64 attention over {L + 1} tokens x "
-            f"{wl.H} heads), {nseq} sequences on {nseq} threads for {el:.1f} s")
+            f"{heads}), {nseq} sequences on {nseq} threads for {el:.1f} s")
     return steps / el, nseq, desc
 
 
@@ -252,19 +255,25 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if world > 1 and rank != 0:
         return
-    rate, cores, desc = oracle_step_rate(args.cpu_seconds, args.seed)
+    from quantized_kv_cache_09_gb300.synth import workloads as W
+    name = args.workload if args.workload in ORACLE_WORKLOADS else "llama2-7b-layer"
+    cfg = W.CONFIGS[ORACLE_WORKLOADS[name]]
+    rate, cores, desc = oracle_step_rate(args.cpu_seconds, args.seed, cfg=ORACLE_WORKLOADS[name])
     line = {"metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000.0 / rate if rate else None, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "llama2-7b-layer", "B": 8, "H": 32, "D": 128, "context": 8192,
-                       "format": "int4-b64", "step": "append 1 token + decode attention"},
+            "config": {"workload": name, "B": cfg["B"], "H": cfg["H"], "Hq": cfg.get("Hq", cfg["H"]), "D": 128,
+                       "context": cfg["L"], "format": "int4-b64", "step": "append 1 token + decode attention"},
             "impl": "reference",
             "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-DECODE_WORKLOADS = {"tiny": 1, "llama2-7b-layer": 2, "long-context": 3, "paged-int8": 4}
+DECODE_WORKLOADS = {"tiny": 1, "llama2-7b-layer": 2, "long-context": 3, "paged-int8": 4,
+                    "llama3-8b-layer-gqa": 6}
+# workloads whose cpu_baseline / reference arm samples their own shape (uniform lengths)
+ORACLE_WORKLOADS = {"llama2-7b-layer": 2, "llama3-8b-layer-gqa": 6}
 
 
 def _sync_all(pg, dev):
@@ -289,7 +298,7 @@ def measure_decode(name, K, Wm, seed, dev, pg):
     wl = W.make_workload(DECODE_WORKLOADS[name], seed=seed, extra_tokens=64)
     dw = DeviceWorkload(wl, device=dev)
     dw.prefill(max_tokens_per_call=1 << 18)
-    B, H, D = wl.B, wl.H, wl.D
+    B, H, D, Hq = wl.B, wl.H, wl.D, wl.Hq
     aligned = bool(np.all(wl.lens % 64 == 0))
     step = DecodeStep(dw)
     NS = 64
@@ -329,7 +338,7 @@ def measure_decode(name, K, Wm, seed, dev, pg):
     for i in range(K):
         s = (Wm + i) % NS
         kvq.kvq_append(dw.cache, k_steps[s], v_steps[s], step.cu, dw.block_table, lens_b[s], 1)
-        kvq.kvq_decode_attention(dw.cache, q_steps[s], dw.block_table, lens_a[s], dw.softmax_scale, step.out,
+        kvq.kvq_decode_attention_gqa(dw.cache, q_steps[s], dw.block_table, lens_a[s], dw.softmax_scale, step.out,
                                  dw.workspace)
     end.record(stream)
     _sync_all(pg, dev)
@@ -342,7 +351,7 @@ def measure_decode(name, K, Wm, seed, dev, pg):
         e0.record(stream)
         kvq.kvq_append(dw.cache, k_steps[s], v_steps[s], step.cu, dw.block_table, lens_b[s], 1)
         e1.record(stream)
-        kvq.kvq_decode_attention(dw.cache, q_steps[s], dw.block_table, lens_a[s], dw.softmax_scale, step.out,
+        kvq.kvq_decode_attention_gqa(dw.cache, q_steps[s], dw.block_table, lens_a[s], dw.softmax_scale, step.out,
                                  dw.workspace)
         e2.record(stream)
     _sync_all(pg, dev)
@@ -358,7 +367,7 @@ def measure_decode(name, K, Wm, seed, dev, pg):
     pin_k = [k.cpu().pin_memory() for k in k_steps]
     pin_v = [v.cpu().pin_memory() for v in v_steps]
     pin_q = [q.cpu().pin_memory() for q in q_steps]
-    pin_o = torch.empty((B, H, D), dtype=torch.float16).pin_memory()
+    pin_o = torch.empty((B, Hq, D), dtype=torch.float16).pin_memory()
     dk, dv, dq = (torch.empty_like(k_steps[0]), torch.empty_like(v_steps[0]), torch.empty_like(q_steps[0]))
     Ke = max(1, K // 2)
     _sync_all(pg, dev)
@@ -371,7 +380,8 @@ def measure_decode(name, K, Wm, seed, dev, pg):
         dv.copy_(pin_v[s], non_blocking=True)
         dq.copy_(pin_q[s], non_blocking=True)
         kvq.kvq_append(dw.cache, dk, dv, step.cu, dw.block_table, lens_b[s], 1)
-        kvq.kvq_decode_attention(dw.cache, dq, dw.block_table, lens_a[s], dw.softmax_scale, step.out, dw.workspace)
+        kvq.kvq_decode_attention_gqa(dw.cache, dq, dw.block_table, lens_a[s], dw.softmax_scale, step.out,
+                                     dw.workspace)
         pin_o.copy_(step.out, non_blocking=True)
     e2e_e.record(stream)
     _sync_all(pg, dev)
@@ -382,7 +392,7 @@ def measure_decode(name, K, Wm, seed, dev, pg):
     dec_bytes = sum(wl.decode_bytes(c) for c in ctx) / K
     res = dict(wl=wl, B=B, H=H, D=D, aligned=aligned, total_ms=total_ms, app_ms=app_ms, dec_ms=dec_ms,
                e2e_ms=e2e_ms, Ke=Ke, dec_bytes=dec_bytes, clocks=clocks.summary(), split_ms=split_ms,
-               h2d=3 * B * H * D * 2, d2h=B * H * D * 2, launches=(1 + -(-B // 512)) * K)
+               h2d=(2 * H + Hq) * B * D * 2, d2h=B * Hq * D * 2, launches=(1 + -(-B // 512)) * K, Hq=Hq)
     del dw
     torch.cuda.empty_cache()
     return res
@@ -481,7 +491,7 @@ def run_ours(args):
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("int4" if wl.fmt == 0 else "int8") + " codes, fp32 math",
             "data": "synthetic (seeded generator in HBM)",
-            "config": {"workload": args.workload, "B": B, "H": r["H"], "D": r["D"], "context": ctx,
+            "config": {"workload": args.workload, "B": B, "H": r["H"], "Hq": r["Hq"], "D": r["D"], "context": ctx,
                        "format": "int4-b64" if wl.fmt == 0 else "int8-page",
                        "step": "append 1 token + decode attention",
                        "parallelism": f"replicas x{world} (sequence-sharded, no collective)",
@@ -502,7 +512,7 @@ def run_ours(args):
         line["quantize"] = {"workload": "prefill-append", "new_tokens": q["tokens"], "gb_per_s": qg,
                             "frac": qg / peak, "ms": qms}
     if rank == 0 and not args.no_cpu_baseline:
-        rate, cores, desc = oracle_step_rate(args.cpu_seconds, args.seed)
+        rate, cores, desc = oracle_step_rate(args.cpu_seconds, args.seed, cfg=ORACLE_WORKLOADS.get(args.workload))
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
     if rank == 0:
         print(json.dumps(line), flush=True)

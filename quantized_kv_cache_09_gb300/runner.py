@@ -21,7 +21,7 @@ class DeviceWorkload:
         self.block_table = torch.from_numpy(np.ascontiguousarray(wl.block_table)).to(device)
         self.lens = torch.from_numpy(wl.lens.copy()).to(device)
         self.lens_host = wl.lens.copy()
-        self.workspace = self.cache.workspace()
+        self.workspace = self.cache.workspace(wl.Hq)
         self.softmax_scale = 1.0 / math.sqrt(wl.D)
 
     def prefill(self, max_tokens_per_call=1 << 21):
@@ -64,7 +64,7 @@ class DeviceWorkload:
             t = int(self.lens_host[b]) + step
             wl.kv_device("k", b, t, t + 1, k[b:b + 1])
             wl.kv_device("v", b, t, t + 1, v[b:b + 1])
-        q = torch.empty((wl.B, wl.H, wl.D), dtype=torch.float16, device=self.device)
+        q = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=self.device)
         wl.q_device(q, step)
         return k, v, q
 
@@ -78,12 +78,12 @@ class DecodeStep:
         self.dw = dw
         B = dw.wl.B
         self.cu = torch.arange(B + 1, dtype=torch.int32, device=dw.device)
-        self.out = torch.empty((B, dw.wl.H, dw.wl.D), dtype=torch.float16, device=dw.device)
+        self.out = torch.empty((B, dw.wl.Hq, dw.wl.D), dtype=torch.float16, device=dw.device)
 
     def run(self, lens_before, lens_after, k1, v1, q, stream=None):
         dw = self.dw
         kvq.kvq_append(dw.cache, k1, v1, self.cu, dw.block_table, lens_before, 1, stream)
-        kvq.kvq_decode_attention(dw.cache, q, dw.block_table, lens_after, dw.softmax_scale, self.out,
+        kvq.kvq_decode_attention_gqa(dw.cache, q, dw.block_table, lens_after, dw.softmax_scale, self.out,
                                  dw.workspace, stream)
         return self.out
 

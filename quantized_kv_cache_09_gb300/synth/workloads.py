@@ -1,4 +1,4 @@
-"""The five synthetic workloads: shapes, value distributions and structure.
+"""The synthetic workloads: shapes, value distributions and structure.
 
   tiny             B=2, H=4, L=256, int4, K/V/q ~ N(0,1), contiguous cache,
                    quantize then one decode step (append 1 token, attend over 257)
@@ -12,6 +12,9 @@
                    permuted block table; decode
   prefill-append   262144 new tokens as 64 sequences x 4096, H=32, K/V ~
                    N(0, 1.5^2), int4, randomly permuted pages; append/quantize
+  llama3-8b-layer-gqa  B=8, 8 cache heads, 32 query heads (groups of 4),
+                   L=8192, int4, otherwise as llama2-7b-layer; decode with
+                   grouped query heads
 
 D = 128 and 64-token blocks throughout.  q ~ N(0, 1).  All values are fp16.
 """
@@ -35,6 +38,10 @@ CONFIGS = {
             outliers=None, table="permuted"),
     5: dict(name="prefill-append", B=64, H=32, D=128, L=4096, fmt=INT4, sigma=1.5, outliers=None,
             table="permuted"),
+    # grouped query heads (beyond the five configurations above): 32 query heads
+    # over 8 cache heads, the Llama-3-8B attention shape
+    6: dict(name="llama3-8b-layer-gqa", B=8, H=8, Hq=32, D=128, L=8192, fmt=INT4, sigma=1.0,
+            outliers=("per_head", 4, 10.0), table="contiguous"),
 }
 
 
@@ -48,9 +55,10 @@ class Workload:
     """
 
     def __init__(self, B, H, D, lens, fmt, sigma=1.0, outliers=None, table="contiguous", seed=0,
-                 extra_tokens=0, name="custom"):
+                 extra_tokens=0, name="custom", q_heads=None):
         self.name = name
         self.B, self.H, self.D = int(B), int(H), int(D)
+        self.Hq = self.H if q_heads is None else int(q_heads)  # query heads (a multiple of the cache heads H)
         self.lens = np.asarray(lens, dtype=np.int32).reshape(self.B)
         self.fmt = int(fmt)
         self.sigma = float(sigma)
@@ -92,9 +100,9 @@ class Workload:
         return x.reshape(t1 - t0, self.H, self.D)
 
     def q_host(self, step=0):
-        """fp16 bits [B][H][D] of the query of decode step `step`."""
-        n = self.B * self.H * self.D
-        return fill_f16_host(n, self.seed, stream_id(QUERY, step), 0, 1.0).reshape(self.B, self.H, self.D)
+        """fp16 bits [B][Hq][D] of the query of decode step `step`."""
+        n = self.B * self.Hq * self.D
+        return fill_f16_host(n, self.seed, stream_id(QUERY, step), 0, 1.0).reshape(self.B, self.Hq, self.D)
 
     # ---- device (torch) -----------------------------------------------
     def _mask_dev(self, which, device):
@@ -115,7 +123,7 @@ class Workload:
                                self._mask_dev(which, out.device), self.outlier_mult)
 
     def q_device(self, out, step=0):
-        assert out.numel() == self.B * self.H * self.D
+        assert out.numel() == self.B * self.Hq * self.D
         return fill_f16_device(out, self.seed, stream_id(QUERY, step), 0, 1.0)
 
     # ---- sizes ---------------------------------------------------------
@@ -134,7 +142,7 @@ class Workload:
         tok = int(lens.sum())
         pages = int(((lens + PAGE - 1) // PAGE).sum())
         return (2 * tok * self.H * self.row_bytes + 2 * pages * self.H * 4 +
-                2 * self.B * self.H * self.D * 2)
+                2 * self.B * self.Hq * self.D * 2)
 
     def quantize_bytes(self, ntok):
         """Algorithmic bytes of quantizing ntok tokens of K and V into full blocks:
@@ -152,4 +160,4 @@ def make_workload(cfg, seed=0, extra_tokens=0):
     else:
         lens = np.full(B, c["L"], dtype=np.int32)
     return Workload(B, c["H"], c["D"], lens, c["fmt"], c["sigma"], c["outliers"], c["table"], seed,
-                    extra_tokens, c["name"])
+                    extra_tokens, c["name"], c.get("Hq"))
