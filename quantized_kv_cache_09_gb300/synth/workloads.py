@@ -12,9 +12,11 @@
                    permuted block table; decode
   prefill-append   262144 new tokens as 64 sequences x 4096, H=32, K/V ~
                    N(0, 1.5^2), int4, randomly permuted pages; append/quantize
-  llama3-8b-layer-gqa  B=8, 8 cache heads, 32 query heads (groups of 4),
+  llama3-8b-layer-gqa  B=32, 8 cache heads, 32 query heads (groups of 4),
                    L=8192, int4, otherwise as llama2-7b-layer; decode with
-                   grouped query heads
+                   grouped query heads.  The batch of 32 puts the same KV
+                   bytes as llama2-7b-layer behind one step (268 MB, more
+                   than L2)
 
 D = 128 and 64-token blocks throughout.  q ~ N(0, 1).  All values are fp16.
 """
@@ -40,7 +42,7 @@ CONFIGS = {
             table="permuted"),
     # grouped query heads (beyond the five configurations above): 32 query heads
     # over 8 cache heads, the Llama-3-8B attention shape
-    6: dict(name="llama3-8b-layer-gqa", B=8, H=8, Hq=32, D=128, L=8192, fmt=INT4, sigma=1.0,
+    6: dict(name="llama3-8b-layer-gqa", B=32, H=8, Hq=32, D=128, L=8192, fmt=INT4, sigma=1.0,
             outliers=("per_head", 4, 10.0), table="contiguous"),
 }
 
