@@ -19,7 +19,11 @@
  *     with a scale taken from a prior per-chunk extrema pass, and section 3.1,
  *     where decode reads an INT8 KV cache.
  *   - "DeepSeek R1 performance tips" (ddd.cn), section 4: KV pages addressed
- *     through a block table (vLLM PagedAttention).
+ *     through a block table (vLLM PagedAttention); section 1: an FP8 KV cache
+ *     as the default on Blackwell.
+ *   - "hardware-aware scheduling" (jsqmd.com/news/887038), section 2.2: FP8
+ *     E4M3 with dynamic range scaling driven by max|x|, and its error bound
+ *     (half a unit in the last place of the 3-bit fraction).
  *
  * Readings taken where the pages are silent or inconsistent (each is listed in
  * the design notes):
@@ -35,6 +39,11 @@
  *   - int4 codes are packed two to a byte, the even element of the head
  *     dimension in the low nibble, as 4-bit two's complement; int8 codes are
  *     one two's-complement byte each;
+ *   - FP8: the same block, scale = a / 448.0f (448 = the largest finite E4M3
+ *     value, so max|x| maps to the top of the format), code = E4M3 of the
+ *     binary32 quotient x / scale rounded to nearest, ties to the even
+ *     fraction, saturating at +-448, sign kept (a quotient that rounds to
+ *     zero keeps its sign); an all-zero block has scale 0 and codes 0x00;
  *   - decode attention is exact softmax attention of one query per
  *     (sequence, head) over the dequantized keys and values k^ = code * scale,
  *     evaluated here in binary64; an empty sequence yields a zero output.
@@ -54,6 +63,7 @@
 
 #define ORC_INT4 0
 #define ORC_INT8 1
+#define ORC_FP8 2
 #define ORC_BLOCK 64
 
 /* ---------------------------------------------------------------------------
@@ -78,6 +88,53 @@ float orc_half_to_float(uint16_t h)
 }
 
 /* ---------------------------------------------------------------------------
+ * FP8 E4M3 (the OCP 8-bit format NVIDIA's E4M3 follows): 1 sign bit, 4
+ * exponent bits with bias 7, 3 fraction bits; exponent field 0 holds the
+ * subnormals f/8 * 2^-6; exponent field 15 with fraction 7 is NaN; there are no
+ * infinities, so the largest finite value is 1.75 * 2^8 = 448 (0x7e).
+ * ------------------------------------------------------------------------- */
+double orc_e4m3_to_double(uint8_t c)
+{
+    int sign = c >> 7;
+    int e = (c >> 3) & 0xf;
+    int f = c & 7;
+    double v;
+    if (e == 15 && f == 7) return NAN;
+    if (e == 0) v = ldexp((double)f, -9);          /* f/8 * 2^-6 */
+    else v = ldexp((double)(8 + f), e - 10);       /* (1 + f/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/*
+ * binary32 -> E4M3, round to nearest with ties to the even fraction,
+ * saturating: the code whose value is nearest to |y| among the 127 finite
+ * non-negative codes 0x00..0x7e (their values increase with the code), the
+ * even one of two equally near, then y's sign bit.  Found by bisection over
+ * that ordered table; |y| above 448 gets 0x7e.
+ */
+#define TAB(c) orc_e4m3_to_double((uint8_t)(c))
+uint8_t orc_float_to_e4m3(float y)
+{
+    double ay = fabs((double)y);
+    int lo = 0, hi = 126;
+    if (ay >= TAB(126)) {
+        lo = 126;
+    } else {
+        while (hi - lo > 1) {                  /* TAB(lo) <= ay < TAB(hi) */
+            int mid = (lo + hi) / 2;
+            if (TAB(mid) <= ay) lo = mid; else hi = mid;
+        }
+    }
+    int c = lo;                                /* the nearer of lo and lo + 1; a tie goes to the even code */
+    if (lo < 126) {
+        double dlo = ay - TAB(lo), dhi = TAB(lo + 1) - ay;
+        if (dhi < dlo || (dhi == dlo && ((lo + 1) & 1) == 0)) c = lo + 1;
+    }
+    return (uint8_t)(c | (signbit(y) ? 0x80 : 0));
+}
+#undef TAB
+
+/* ---------------------------------------------------------------------------
  * One block of quantize_block.
  *   x      : pointer to row 0, element 0 of the block (fp16 bits)
  *   rows   : number of valid rows (1..64); rows beyond it get code 0
@@ -97,12 +154,20 @@ static float quantize_one_block(int fmt, const uint16_t *x, int rows, int64_t ro
             if (v > a) a = v;
         }
     /* step 2: the scale */
-    float scale = (fmt == ORC_INT4) ? a / 7.5f : a / 127.0f;
+    float scale = (fmt == ORC_INT4) ? a / 7.5f : (fmt == ORC_INT8) ? a / 127.0f : a / 448.0f;
     int lo = (fmt == ORC_INT4) ? -8 : -127;
     int hi = (fmt == ORC_INT4) ? 7 : 127;
     int row_bytes = (fmt == ORC_INT4) ? D / 2 : D;
     memset(out, 0, (size_t)ORC_BLOCK * row_bytes);
     if (scale == 0.0f) return scale;               /* all-zero block: every code 0 */
+    if (fmt == ORC_FP8) {                          /* step 3 in E4M3: round the quotient to the format */
+        for (int r = 0; r < rows; r++)
+            for (int d = 0; d < D; d++) {
+                float y = orc_half_to_float(x[r * row_stride + d]) / scale;
+                out[r * row_bytes + d] = orc_float_to_e4m3(y);
+            }
+        return scale;
+    }
     /* step 3: codes = clamp(round_half_even(x / scale)) and step 4: store */
     for (int r = 0; r < rows; r++) {
         for (int d = 0; d < D; d++) {
@@ -134,7 +199,7 @@ static float quantize_one_block(int fmt, const uint16_t *x, int rows, int64_t ro
 int orc_quantize(int fmt, const uint16_t *x, int64_t T, int32_t H, int32_t D,
                  uint8_t *codes, float *scales)
 {
-    if ((fmt != ORC_INT4 && fmt != ORC_INT8) || T < 0 || H <= 0 || D <= 0 || (D % 2))
+    if ((fmt != ORC_INT4 && fmt != ORC_INT8 && fmt != ORC_FP8) || T < 0 || H <= 0 || D <= 0 || (D % 2))
         return -1;
     fesetround(FE_TONEAREST);
     int row_bytes = (fmt == ORC_INT4) ? D / 2 : D;
@@ -150,14 +215,16 @@ int orc_quantize(int fmt, const uint16_t *x, int64_t T, int32_t H, int32_t D,
     return 0;
 }
 
-/* the signed code of element (row, d) of one (page, head) code block */
-static int code_at(int fmt, const uint8_t *blk, int D, int row, int d)
+/* the value of the code of element (row, d) of one (page, head) code block
+ * (a signed integer for int4 / int8, an E4M3 value for FP8), exact in binary64 */
+static double code_at(int fmt, const uint8_t *blk, int D, int row, int d)
 {
     if (fmt == ORC_INT4) {
         uint8_t byte = blk[row * (D / 2) + d / 2];
         int nib = (d % 2 == 0) ? (byte & 0xf) : (byte >> 4);
         return nib >= 8 ? nib - 16 : nib;
     }
+    if (fmt == ORC_FP8) return orc_e4m3_to_double(blk[row * D + d]);
     return (int)(int8_t)blk[row * D + d];
 }
 
@@ -179,8 +246,8 @@ static void gather_dequant(int fmt, int32_t H, int32_t D, const uint8_t *k_codes
         double sk = (double)k_scales[(size_t)page * H + h];
         double sv = (double)v_scales[(size_t)page * H + h];
         for (int d = 0; d < D; d++) {
-            kh[(size_t)t * D + d] = (double)code_at(fmt, kb, D, row, d) * sk;
-            vh[(size_t)t * D + d] = (double)code_at(fmt, vb, D, row, d) * sv;
+            kh[(size_t)t * D + d] = code_at(fmt, kb, D, row, d) * sk;
+            vh[(size_t)t * D + d] = code_at(fmt, vb, D, row, d) * sv;
         }
     }
 }
@@ -243,7 +310,7 @@ int orc_decode_attention_gqa(int fmt, int32_t Hkv, int32_t Hq, int32_t D, int32_
                              const int32_t *seq_lens, int32_t B, const uint16_t *q,
                              double softmax_scale, int32_t num_splits, double *out)
 {
-    if ((fmt != ORC_INT4 && fmt != ORC_INT8) || Hkv <= 0 || Hq <= 0 || (Hq % Hkv) || D <= 0 || (D % 2) || B < 0)
+    if ((fmt != ORC_INT4 && fmt != ORC_INT8 && fmt != ORC_FP8) || Hkv <= 0 || Hq <= 0 || (Hq % Hkv) || D <= 0 || (D % 2) || B < 0)
         return -1;
     const int32_t g = Hq / Hkv;
     for (int32_t b = 0; b < B; b++) {
@@ -332,7 +399,7 @@ int orc_value_absmax(int fmt, int32_t H, int32_t D, const uint8_t *v_codes, cons
                 const uint8_t *vb = v_codes + ((size_t)page * H + h) * blk_bytes;
                 double sv = (double)v_scales[(size_t)page * H + h];
                 for (int d = 0; d < D; d++) {
-                    double v = fabs((double)code_at(fmt, vb, D, t % ORC_BLOCK, d) * sv);
+                    double v = fabs(code_at(fmt, vb, D, t % ORC_BLOCK, d) * sv);
                     if (v > mx) mx = v;
                 }
             }

@@ -14,6 +14,7 @@ from . import build as _build
 
 INT4 = 0
 INT8 = 1
+FP8 = 2
 BLOCK = 64
 
 _lib = None
@@ -27,6 +28,10 @@ def lib():
         vp = ctypes.c_void_p
         L.orc_half_to_float.argtypes = [ctypes.c_uint16]
         L.orc_half_to_float.restype = ctypes.c_float
+        L.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_to_double.restype = ctypes.c_double
+        L.orc_float_to_e4m3.argtypes = [ctypes.c_float]
+        L.orc_float_to_e4m3.restype = ctypes.c_uint8
         L.orc_quantize.argtypes = [ctypes.c_int, vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, vp]
         L.orc_quantize.restype = ctypes.c_int
         L.orc_decode_attention.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -54,6 +59,16 @@ def row_bytes(fmt, D):
 
 def half_to_float(bits):
     return lib().orc_half_to_float(int(bits))
+
+
+def e4m3_to_float(code):
+    """The value of one FP8 E4M3 code (binary64, exact; NaN for 0x7f / 0xff)."""
+    return lib().orc_e4m3_to_double(int(code))
+
+
+def float_to_e4m3(y):
+    """E4M3 code of a binary32 value: nearest, ties to even, saturating at 448."""
+    return int(lib().orc_float_to_e4m3(float(y)))
 
 
 def quantize(fmt, x_bits):
@@ -131,7 +146,7 @@ def normalized_error(out_test, out_ref, vmax):
     return float(r.max()) if r.size else 0.0
 
 
-__all__ = ["INT4", "INT8", "BLOCK", "lib", "quantize", "decode_attention", "value_absmax",
+__all__ = ["INT4", "INT8", "FP8", "BLOCK", "e4m3_to_float", "float_to_e4m3", "lib", "quantize", "decode_attention", "value_absmax",
            "quantize_into_pages", "normalized_error", "half_to_float", "row_bytes"]
 
 if os.environ.get("KVQ_ORACLE_EAGER"):

@@ -35,11 +35,14 @@ def _set_code(fmt, codes, page, h, row, d, c):
         nib = c & 0xF
         b = (b & 0xF0) | nib if d % 2 == 0 else (b & 0x0F) | (nib << 4)
         codes[page, h, row, d // 2] = b
+    elif fmt == orc.FP8:   # small integers are exact E4M3 values
+        codes[page, h, row, d] = orc.float_to_e4m3(c)
+        assert orc.e4m3_to_float(int(codes[page, h, row, d])) == c
     else:
         codes[page, h, row, d] = np.uint8(c & 0xFF)
 
 
-@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8])
+@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8, orc.FP8])
 def test_two_token_closed_form(fmt):
     """q = e_0.  Token 0: key code 7 at dim 0 (dim 1 code -3 is ignored by q),
     key scale 0.5 -> score 3.5/sqrt(128); token 1: key codes 0 -> score 0.
@@ -88,6 +91,9 @@ def _random_cache(fmt, num_pages, H, seed):
     if fmt == orc.INT8:   # -128 is outside the code range
         kc[kc == 0x80] = 0x81
         vc[vc == 0x80] = 0x81
+    if fmt == orc.FP8:    # 0x7f / 0xff are NaN, never written by the codec
+        kc[(kc & 0x7F) == 0x7F] &= 0xFE
+        vc[(vc & 0x7F) == 0x7F] &= 0xFE
     ks = rng.uniform(0.05, 0.6, (num_pages, H)).astype(np.float32)
     vs = rng.uniform(0.05, 0.6, (num_pages, H)).astype(np.float32)
     return kc, vc, ks, vs
@@ -104,13 +110,15 @@ def _dequant(fmt, codes, scales, bt_row, L, h):
             c = np.empty(D, np.int64)
             c[0::2] = np.where(lo >= 8, lo - 16, lo)
             c[1::2] = np.where(hi >= 8, hi - 16, hi)
+        elif fmt == orc.FP8:
+            c = np.array([orc.e4m3_to_float(int(v)) for v in r])
         else:
             c = r.view(np.int8).astype(np.int64)
         rows.append(c * float(scales[pg, h]))
     return np.array(rows)
 
 
-@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8])
+@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8, orc.FP8])
 def test_single_token_returns_its_value_row(fmt):
     kc, vc, ks, vs = _random_cache(fmt, 3, 2, 1)
     q = np.random.default_rng(2).standard_normal((1, 2, D)).astype(np.float16).view(np.uint16)
@@ -120,7 +128,7 @@ def test_single_token_returns_its_value_row(fmt):
         assert np.array_equal(out[0, h], _dequant(fmt, vc, vs, bt[0], 1, h)[0])
 
 
-@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8])
+@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8, orc.FP8])
 def test_zero_query_is_mean_of_values(fmt):
     kc, vc, ks, vs = _random_cache(fmt, 4, 2, 3)
     q = np.zeros((1, 2, D), np.uint16)
@@ -144,7 +152,7 @@ def test_one_dominant_key_selects_its_value():
     np.testing.assert_allclose(out[0, 0], _dequant(fmt, vc, vs, bt[0], 128, 0)[74], rtol=0, atol=1e-12)
 
 
-@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8])
+@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8, orc.FP8])
 def test_page_placement_invariance_and_tail_rows_ignored(fmt):
     """Moving pages (and their scales) to other slots with the block table
     following them changes nothing; codes in rows past the sequence end, and
@@ -168,7 +176,7 @@ def test_page_placement_invariance_and_tail_rows_ignored(fmt):
     assert np.array_equal(out[1], ref[1])
 
 
-@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8])
+@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8, orc.FP8])
 def test_split_merge_equals_direct(fmt):
     kc, vc, ks, vs = _random_cache(fmt, 6, 2, 7)
     q = np.random.default_rng(8).standard_normal((2, 2, D)).astype(np.float16).view(np.uint16)
@@ -226,7 +234,7 @@ def test_matches_independent_numpy_softmax():
         np.testing.assert_allclose(out[0, h], p @ V / p.sum(), rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8])
+@pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8, orc.FP8])
 @pytest.mark.parametrize("g", [2, 4])
 def test_grouped_heads_equal_multi_head_over_repeated_heads(fmt, g):
     """Grouped query heads (Hq = g * Hkv, query head i reads cache head i // g)
