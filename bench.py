@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="llama2-7b-layer",
                     choices=["tiny", "llama2-7b-layer", "long-context", "paged-int8", "prefill-append",
-                             "llama3-8b-layer-gqa"])
+                             "llama3-8b-layer-gqa", "llama2-7b-layer-fp8"])
     ap.add_argument("--prefill-seqs", type=int, default=64)
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     return ap.parse_args()
@@ -271,7 +271,8 @@ def run_reference(args):
 
 
 DECODE_WORKLOADS = {"tiny": 1, "llama2-7b-layer": 2, "long-context": 3, "paged-int8": 4,
-                    "llama3-8b-layer-gqa": 6}
+                    "llama3-8b-layer-gqa": 6, "llama2-7b-layer-fp8": 7}
+FORMAT_NAMES = {0: ("int4", "int4-b64"), 1: ("int8", "int8-page"), 2: ("fp8-e4m3", "fp8-e4m3-page")}
 # workloads whose cpu_baseline / reference arm samples their own shape (uniform lengths)
 ORACLE_WORKLOADS = {"llama2-7b-layer": 2, "llama3-8b-layer-gqa": 6}
 
@@ -489,10 +490,10 @@ def run_ours(args):
            else f"{int(lens.min()) + 1}..{int(lens.max()) + 1} (sum {int(lens.sum()) + len(lens)})")
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": ("int4" if wl.fmt == 0 else "int8") + " codes, fp32 math",
+            "dtype": FORMAT_NAMES[wl.fmt][0] + " codes, fp32 math",
             "data": "synthetic (seeded generator in HBM)",
             "config": {"workload": args.workload, "B": B, "H": r["H"], "Hq": r["Hq"], "D": r["D"], "context": ctx,
-                       "format": "int4-b64" if wl.fmt == 0 else "int8-page",
+                       "format": FORMAT_NAMES[wl.fmt][1],
                        "step": "append 1 token + decode attention",
                        "parallelism": f"replicas x{world} (sequence-sharded, no collective)",
                        "l2": "inputs larger than L2" if r["dec_bytes"] > 129e6 else "fits in L2 (no flush)"},

@@ -11,7 +11,9 @@
  *     overview" (aicoding.csdn.net), section 2.2, and decode reading an INT8
  *     KV cache, same page, section 3.1;
  *   - KV pages addressed through a block table, "DeepSeek R1 performance
- *     tips" (ddd.cn), section 4 (vLLM PagedAttention).
+ *     tips" (ddd.cn), section 4 (vLLM PagedAttention);
+ *   - an FP8 KV cache (same page, section 1) in E4M3 with dynamic range
+ *     scaling set by max|x| ("hardware-aware scheduling" page, section 2.2).
  *
  * Readings fixed by this library where the pages are silent or inconsistent:
  *   - a block is (sequence, head, 64 consecutive tokens); the last block of a
@@ -23,6 +25,11 @@
  *     zero-point; an all-zero block has scale 0 and codes 0;
  *   - int4 codes are packed: byte j of a row holds element 2j in its low
  *     nibble and element 2j+1 in its high nibble, 4-bit two's complement;
+ *   - FP8: scale = a / 448.0f (the largest finite E4M3 value), code = the
+ *     E4M3 value nearest to y = RN(x / scale), ties to the even fraction,
+ *     saturating at +-448, sign kept (-0.0 and negatives that round to zero
+ *     give 0x80); one byte per element, stored like int8; an all-zero block
+ *     has scale 0 and codes 0x00;
  *   - decode attention is softmax(q . k^ * softmax_scale) . v^ with
  *     k^ = code * scale, one query per (sequence, head); the output of an
  *     empty sequence is 0.
@@ -30,7 +37,7 @@
  * Layouts (all little-endian, all pointers device memory unless stated):
  *   fp16 tensors are IEEE binary16 bit patterns (uint16_t).
  *   token rows: x[T][H][D], head_dim D = 128 contiguous per (token, head).
- *   codes of one (page, head): 64 rows of D/2 bytes (int4) or D bytes (int8);
+ *   codes of one (page, head): 64 rows of D/2 bytes (int4) or D bytes (int8, FP8);
  *   code arrays: [num_pages][H][64][D/2 or D];  scale arrays: [num_pages][H].
  *
  * Ownership: the caller allocates and frees every buffer, workspaces
@@ -67,7 +74,8 @@ typedef enum kvq_status {
 
 typedef enum kvq_format {
     KVQ_INT4_B64 = 0,   /* packed int4, scale = absmax / 7.5 per (block, head) */
-    KVQ_INT8_PAGE = 1   /* int8, scale = absmax / 127 per (page, head) */
+    KVQ_INT8_PAGE = 1,  /* int8, scale = absmax / 127 per (page, head) */
+    KVQ_FP8_E4M3 = 2    /* FP8 E4M3, scale = absmax / 448 per (page, head) */
 } kvq_format;
 
 /* bits of the device status word */
@@ -111,7 +119,7 @@ typedef struct kvq_cache {
  * kvq_quantize -- quantize_block of one contiguous tensor (jsqmd.com/news/887038
  * section 2.1; INT8: aicoding.csdn.net section 2.2).
  *   x       fp16 [num_tokens][num_heads][head_dim], 16-byte aligned
- *   codes   [ceil(num_tokens/64)][num_heads][64][head_dim/2 (int4) or head_dim (int8)],
+ *   codes   [ceil(num_tokens/64)][num_heads][64][head_dim/2 (int4) or head_dim (int8, FP8)],
  *           16-byte aligned; rows past num_tokens in the last block are written as 0
  *   scales  [ceil(num_tokens/64)][num_heads]
  * num_tokens == 0 is a no-op.  Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED,
@@ -186,7 +194,7 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
  *   q, out           fp16 [num_seqs][num_q_heads][head_dim], 16-byte aligned
  *   workspace        >= kvq_decode_workspace_bytes_gqa(...) bytes, zero-filled
  *                    once before first use (as for kvq_decode_attention)
- * g = 1 is kvq_decode_attention.  Supported: g = 1 for both formats, g = 2 and
+ * g = 1 is kvq_decode_attention.  Supported: g = 1 for every format, g = 2 and
  * 4 for KVQ_INT4_B64; other g return KVQ_ERR_UNSUPPORTED, and num_q_heads not
  * a multiple of cache->num_heads returns KVQ_ERR_INVALID_ARG.  Other errors as
  * for kvq_decode_attention.

@@ -13,7 +13,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
-bool fmt_ok(int fmt) { return fmt == KVQ_INT4_B64 || fmt == KVQ_INT8_PAGE; }
+bool fmt_ok(int fmt) { return fmt == KVQ_INT4_B64 || fmt == KVQ_INT8_PAGE || fmt == KVQ_FP8_E4M3; }
 
 kvq_status check_cache(const kvq_cache *c)
 {

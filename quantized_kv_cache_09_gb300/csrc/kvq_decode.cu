@@ -69,6 +69,10 @@ struct DecFmt<KVQ_INT8_PAGE> {
     static constexpr int kCtasPerSm = 1;
     static constexpr int kMergeBatch = 4;
 };
+// FP8 E4M3: one byte per element like int8, so the same units, stages and grid
+template <>
+struct DecFmt<KVQ_FP8_E4M3> : DecFmt<KVQ_INT8_PAGE> {
+};
 
 // what a stage holds: units c .. c + nunits - 1 of (b, h), ntok tokens in all
 struct alignas(16) StageMeta {
@@ -111,10 +115,32 @@ __device__ __forceinline__ void widen_int8(uint32_t w, __half2 c[2])
     c[1] = __hsub2(*reinterpret_cast<const __half2 *>(&b), k1152);
 }
 
-__device__ __forceinline__ float dot4_int8(uint32_t w, const float *q, float acc)
+// FP8 E4M3 word (element j in byte j): returns {c0,c1},{c2,c3} by the hardware
+// conversion, exact (every finite E4M3 value is a binary16 value)
+__device__ __forceinline__ void widen_e4m3(uint32_t w, __half2 c[2])
+{
+    uint32_t a, b;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(a) : "h"(static_cast<unsigned short>(w & 0xffffu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b) : "h"(static_cast<unsigned short>(w >> 16)));
+    c[0] = *reinterpret_cast<const __half2 *>(&a);
+    c[1] = *reinterpret_cast<const __half2 *>(&b);
+}
+
+// the byte formats' widening, by format
+template <int FMT>
+__device__ __forceinline__ void widen_bytes(uint32_t w, __half2 c[2])
+{
+    if constexpr (FMT == KVQ_FP8_E4M3)
+        widen_e4m3(w, c);
+    else
+        widen_int8(w, c);
+}
+
+template <int FMT>
+__device__ __forceinline__ float dot4_bytes(uint32_t w, const float *q, float acc)
 {
     __half2 c[2];
-    widen_int8(w, c);
+    widen_bytes<FMT>(w, c);
     const float2 f0 = __half22float2(c[0]);
     const float2 f1 = __half22float2(c[1]);
     acc = fmaf(q[0], f0.x, acc);
@@ -124,10 +150,11 @@ __device__ __forceinline__ float dot4_int8(uint32_t w, const float *q, float acc
     return acc;
 }
 
-__device__ __forceinline__ void axpy4_int8(uint32_t w, float p, float *acc)
+template <int FMT>
+__device__ __forceinline__ void axpy4_bytes(uint32_t w, float p, float *acc)
 {
     __half2 c[2];
-    widen_int8(w, c);
+    widen_bytes<FMT>(w, c);
     const float2 f0 = __half22float2(c[0]);
     const float2 f1 = __half22float2(c[1]);
     acc[0] = fmaf(p, f0.x, acc[0]);
@@ -669,12 +696,13 @@ struct ConsumerGqa {
         }
     }
 };
-// int8: CUDA-core path.  K: lane = (token group g = lane >> 3, 16-element
-// chunk r = lane & 7), 4 passes of 4 tokens, reduce-scatter over the 8 lanes of
-// a token; V: lane = (16-element chunk, token subset), weights shuffled from
-// the lanes that scored them.
-template <>
-struct Consumer<KVQ_INT8_PAGE> {
+// int8 and FP8 E4M3 (one byte per element): CUDA-core path on codes widened
+// exactly to fp16, then fp32 FMAs.  K: lane = (token group g = lane >> 3,
+// 16-element chunk r = lane & 7), 4 passes of 4 tokens, reduce-scatter over the
+// 8 lanes of a token; V: lane = (16-element chunk, token subset), weights
+// shuffled from the lanes that scored them.
+template <int FMT>
+struct ConsumerBytes {
     float qf[16];
     float acc[16];
     float m_run;
@@ -714,10 +742,10 @@ struct Consumer<KVQ_INT8_PAGE> {
         for (int k = 0; k < 4; k++) {
             const uint4 w = *reinterpret_cast<const uint4 *>(ks + (4 * k + g) * RB + r * 16);
             float a = 0.0f;
-            a = dot4_int8(w.x, qf + 0, a);
-            a = dot4_int8(w.y, qf + 4, a);
-            a = dot4_int8(w.z, qf + 8, a);
-            a = dot4_int8(w.w, qf + 12, a);
+            a = dot4_bytes<FMT>(w.x, qf + 0, a);
+            a = dot4_bytes<FMT>(w.y, qf + 4, a);
+            a = dot4_bytes<FMT>(w.z, qf + 8, a);
+            a = dot4_bytes<FMT>(w.w, qf + 12, a);
             P[k] = a;
         }
         const bool o1 = r & 1;
@@ -760,10 +788,10 @@ struct Consumer<KVQ_INT8_PAGE> {
             const int src = ts * 8 + ((j & 1) << 1) + (j >> 1);
             const float pt = __shfl_sync(kFull, pv, src);
             const uint4 w = *reinterpret_cast<const uint4 *>(vs + tv * RB + vc * 16);
-            axpy4_int8(w.x, pt, acc);
-            axpy4_int8(w.y, pt, acc + 4);
-            axpy4_int8(w.z, pt, acc + 8);
-            axpy4_int8(w.w, pt, acc + 12);
+            axpy4_bytes<FMT>(w.x, pt, acc);
+            axpy4_bytes<FMT>(w.y, pt, acc + 4);
+            axpy4_bytes<FMT>(w.z, pt, acc + 8);
+            axpy4_bytes<FMT>(w.w, pt, acc + 12);
         }
     }
 
@@ -795,6 +823,13 @@ struct Consumer<KVQ_INT8_PAGE> {
             for (int i = 0; i < 4; i++) d4[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
         }
     }
+};
+
+template <>
+struct Consumer<KVQ_INT8_PAGE> : ConsumerBytes<KVQ_INT8_PAGE> {
+};
+template <>
+struct Consumer<KVQ_FP8_E4M3> : ConsumerBytes<KVQ_FP8_E4M3> {
 };
 
 // ---------------------------------------------------------------------------
@@ -1212,6 +1247,7 @@ int decode_grid_warps(int fmt)
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     if (fmt == KVQ_INT4_B64) return sms * ctas_per_sm<KVQ_INT4_B64, 1>() * DecFmt<KVQ_INT4_B64>::kWarps;
+    if (fmt == KVQ_FP8_E4M3) return sms * ctas_per_sm<KVQ_FP8_E4M3, 1>() * DecFmt<KVQ_FP8_E4M3>::kWarps;
     return sms * ctas_per_sm<KVQ_INT8_PAGE, 1>() * DecFmt<KVQ_INT8_PAGE>::kWarps;
 }
 
@@ -1232,12 +1268,18 @@ cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s)
 {
     const int gw = decode_grid_warps(fmt);
     if (gw <= 0) return cudaErrorInvalidDevice;
-    const int ctas = gw / (fmt == KVQ_INT4_B64 ? DecFmt<KVQ_INT4_B64>::kWarps : DecFmt<KVQ_INT8_PAGE>::kWarps);
-    const dim3 grid(ctas);
+    static_assert(DecFmt<KVQ_INT4_B64>::kWarps == DecFmt<KVQ_INT8_PAGE>::kWarps &&
+                  DecFmt<KVQ_FP8_E4M3>::kWarps == DecFmt<KVQ_INT8_PAGE>::kWarps, "one CTA size");
+    const dim3 grid(gw / DecFmt<KVQ_INT8_PAGE>::kWarps);
     if (fmt == KVQ_INT8_PAGE) {
         if (p.group != 1) return cudaErrorInvalidValue;
         return launch_pdl(decode_split_kernel<KVQ_INT8_PAGE, 1>, grid, dim3(DecFmt<KVQ_INT8_PAGE>::kWarps * 32),
                           dec_smem_bytes<KVQ_INT8_PAGE, 1>(), s, p, gw);
+    }
+    if (fmt == KVQ_FP8_E4M3) {
+        if (p.group != 1) return cudaErrorInvalidValue;
+        return launch_pdl(decode_split_kernel<KVQ_FP8_E4M3, 1>, grid, dim3(DecFmt<KVQ_FP8_E4M3>::kWarps * 32),
+                          dec_smem_bytes<KVQ_FP8_E4M3, 1>(), s, p, gw);
     }
     const dim3 block(DecFmt<KVQ_INT4_B64>::kWarps * 32);
     switch (p.group) {

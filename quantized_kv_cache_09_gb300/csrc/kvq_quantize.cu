@@ -1,7 +1,8 @@
 // kvq_quantize.cu -- fused absmax + quantize + pack of 64-token blocks
 // (quantize_block, jsqmd.com/news/887038 section 2.1; INT8 per-chunk variant,
-// aicoding.csdn.net section 2.2), for a contiguous tensor and for appends into
-// the paged cache.
+// aicoding.csdn.net section 2.2; FP8 E4M3 with the scale set by max|x|,
+// jsqmd.com/news/887038 section 2.2), for a contiguous tensor and for appends
+// into the paged cache.
 //
 // One warp owns one (block, head): 64 rows x 128 fp16 = 16 KiB.  Its lanes
 // stage the rows in shared memory with 16-byte cp.async copies (lane = row
@@ -21,6 +22,13 @@
 // (rint(-7.5) = -8 already), and only when y >= 7.5, which the tie test above
 // always sends to the exact path, so the fast path needs no clamp -- and
 // |y| <= 127 (1 + 2^-22) for int8, where rint never leaves [-127, 127].
+//
+// FP8 E4M3: code = E4M3(RN(x / scale)), nearest with ties to the even
+// fraction, saturating, by the hardware conversion.  The fast path converts
+// y' (1 - 2^-21) and y' (1 + 2^-21) for y' = RN(x * r): RN(x / scale) lies
+// between them (|y' - RN(x / scale)| < 1.5 * 2^-23 |y|), the conversion is
+// monotone, so equal codes are the code; a pair whose two ends differ (y near
+// a midpoint of the E4M3 grid) takes the correctly rounded division.
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -45,7 +53,42 @@ struct Codec<KVQ_INT8_PAGE> {
     static constexpr float kEps = 6.103515625e-05f;    // 2^-14
 };
 
+template <>
+struct Codec<KVQ_FP8_E4M3> {
+    static constexpr int kRowBytes = 128;
+    static constexpr float kDiv = 448.0f;  // the largest finite E4M3 value
+};
+
 constexpr uint32_t kMagicBits = 0x4b400000u;  // bits of 1.5 * 2^23
+
+// two binary32 values -> two E4M3 codes, x0 in the low byte (round to nearest
+// even, saturating at +-448; the sign of a zero result is kept)
+__device__ __forceinline__ uint32_t e4m3x2_rn(float x0, float x1)
+{
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(x1), "f"(x0));
+    return d;
+}
+
+// 8 fp16 values -> 8 E4M3 codes, element j in byte j; rr = (r, r), r = RN(1 / scale)
+__device__ __forceinline__ uint2 quant8_fp8(const uint4 &v, uint64_t rr, float scale)
+{
+    if (scale == 0.0f) return make_uint2(0u, 0u);  // all-zero block: codes 0x00 (also for -0.0)
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint64_t dn = pk2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f), up = pk2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f);
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+        const uint64_t y = mul2(pk2(f.x, f.y), rr);
+        float a0, a1, b0, b1;
+        upk2(mul2(y, dn), a0, a1);
+        upk2(mul2(y, up), b0, b1);
+        c[i] = e4m3x2_rn(a0, a1);
+        if (c[i] != e4m3x2_rn(b0, b1)) c[i] = e4m3x2_rn(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
 
 // fast path for 8 fp16 values: m[j] = bits of RN(RN(x_j * r) + kMagic), and
 // tmax = max(tmax, |y_j - rint(y_j)|) over them
@@ -123,6 +166,27 @@ __device__ __forceinline__ uint2 pack8_int8(const uint32_t m[8])
         hi = hi * 256u + m[4 + j];
     }
     return make_uint2((lo - kBias) ^ 0x80808080u, (hi - kBias) ^ 0x80808080u);
+}
+
+// quantize 8 consecutive elements of one row and store their codes at dst
+// (4 bytes int4, 8 bytes int8 / FP8).  rr = (r, r), r = RN(1 / scale); a, ya:
+// the block's max|x| and RN(a / scale) (integer formats' exact path)
+template <int FMT>
+__device__ __forceinline__ void store8(const uint4 &v, uint64_t rr, float scale, float a, float ya, uint8_t *dst)
+{
+    using C = Codec<FMT>;
+    if constexpr (FMT == KVQ_FP8_E4M3) {
+        *reinterpret_cast<uint2 *>(dst) = quant8_fp8(v, rr, scale);
+    } else {
+        uint32_t m[8];
+        float tmax = 0.0f;
+        quant8_fast<FMT>(v, rr, m, tmax);
+        if (tmax > 0.5f - C::kEps) quant8_exact<FMT>(v, rr, scale, a, ya, m);  // a near-tie (rare)
+        if constexpr (FMT == KVQ_INT4_B64)
+            *reinterpret_cast<uint32_t *>(dst) = pack8_int4(m);
+        else
+            *reinterpret_cast<uint2 *>(dst) = pack8_int8(m);
+    }
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
@@ -216,15 +280,7 @@ __device__ __forceinline__ void quantize_block_warp(const Rows &rows, int nrows,
     uint8_t *out = codes + rpar * C::kRowBytes + (FMT == KVQ_INT4_B64 ? 4 : 8) * chunk;
 #pragma unroll 4
     for (int i = 0; i < npairs; i++) {  // rows 2i + rpar
-        const uint4 v = sv[i * kStep];
-        uint32_t m[8];
-        float tmax = 0.0f;
-        quant8_fast<FMT>(v, rr, m, tmax);
-        if (tmax > 0.5f - C::kEps) quant8_exact<FMT>(v, rr, scale, a, ya, m);  // a near-tie (rare)
-        if constexpr (FMT == KVQ_INT4_B64)
-            *reinterpret_cast<uint32_t *>(out + i * 2 * C::kRowBytes) = pack8_int4(m);
-        else
-            *reinterpret_cast<uint2 *>(out + i * 2 * C::kRowBytes) = pack8_int8(m);
+        store8<FMT>(sv[i * kStep], rr, scale, a, ya, out + i * 2 * C::kRowBytes);
     }
 }
 
@@ -445,14 +501,7 @@ __global__ void __launch_bounds__(kShortWarps * 32)
         for (int i = 0; i < kShortRounds; i++) {
             const int r = 8 * i + rbase;
             if (r < r_first || r >= R) continue;
-            uint32_t m[8];
-            float tmax = 0.0f;
-            quant8_fast<FMT>(v[i], rr, m, tmax);
-            if (tmax > 0.5f - C::kEps) quant8_exact<FMT>(v[i], rr, scale, a, ya, m);
-            if constexpr (FMT == KVQ_INT4_B64)
-                *reinterpret_cast<uint32_t *>(codes + r * C::kRowBytes) = pack8_int4(m);
-            else
-                *reinterpret_cast<uint2 *>(codes + r * C::kRowBytes) = pack8_int8(m);
+            store8<FMT>(v[i], rr, scale, a, ya, codes + r * C::kRowBytes);
         }
     }
     // the CTA of the first touched block is the only reader of this (b, h)'s
@@ -495,6 +544,8 @@ cudaError_t launch_quantize(int fmt, const uint16_t *x, int64_t T, int H, uint8_
     const dim3 grid((unsigned)blocks), block(kQuantWarps * 32);
     if (fmt == KVQ_INT4_B64)
         return launch_plain(quantize_contig_kernel<KVQ_INT4_B64>, grid, block, 0, s, x, T, H, nb, codes, scales);
+    if (fmt == KVQ_FP8_E4M3)
+        return launch_plain(quantize_contig_kernel<KVQ_FP8_E4M3>, grid, block, 0, s, x, T, H, nb, codes, scales);
     return launch_plain(quantize_contig_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, x, T, H, nb, codes, scales);
 }
 
@@ -508,6 +559,7 @@ cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s)
         if (bx > 0x7fffffffLL || p.num_seqs > 65535) return cudaErrorInvalidValue;
         const dim3 grid((unsigned)bx, (unsigned)p.num_seqs, 2), block(kShortWarps * 32);
         if (fmt == KVQ_INT4_B64) return launch_pdl(append_short_kernel<KVQ_INT4_B64>, grid, block, 0, s, p);
+        if (fmt == KVQ_FP8_E4M3) return launch_pdl(append_short_kernel<KVQ_FP8_E4M3>, grid, block, 0, s, p);
         return launch_pdl(append_short_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, p);
     }
     const int64_t warps = touched * p.num_heads;
@@ -515,6 +567,7 @@ cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s)
     if (bx > 0x7fffffffLL || p.num_seqs > 65535) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)bx, (unsigned)p.num_seqs, 2), block(kQuantWarps * 32);
     if (fmt == KVQ_INT4_B64) return launch_plain(append_kernel<KVQ_INT4_B64>, grid, block, 0, s, p);
+    if (fmt == KVQ_FP8_E4M3) return launch_plain(append_kernel<KVQ_FP8_E4M3>, grid, block, 0, s, p);
     return launch_plain(append_kernel<KVQ_INT8_PAGE>, grid, block, 0, s, p);
 }
 

@@ -13,6 +13,7 @@ from . import build as _build
 
 KVQ_INT4_B64 = 0
 KVQ_INT8_PAGE = 1
+KVQ_FP8_E4M3 = 2
 HEAD_DIM = 128
 PAGE_TOKENS = 64
 
@@ -268,7 +269,7 @@ class PagedKVCache:
         return sum(x.numel() * x.element_size() for x in t)
 
 
-__all__ = ["KVQ_INT4_B64", "KVQ_INT8_PAGE", "HEAD_DIM", "PAGE_TOKENS", "EXPORTS", "KvqError", "kvq_cache",
+__all__ = ["KVQ_INT4_B64", "KVQ_INT8_PAGE", "KVQ_FP8_E4M3", "HEAD_DIM", "PAGE_TOKENS", "EXPORTS", "KvqError", "kvq_cache",
            "PagedKVCache", "lib", "library_path", "kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes",
            "kvq_decode_attention", "kvq_decode_attention_noalloc", "kvq_get_device_status", "kvq_status_string",
            "kvq_version"]

@@ -17,6 +17,8 @@
                    grouped query heads.  The batch of 32 puts the same KV
                    bytes as llama2-7b-layer behind one step (268 MB, more
                    than L2)
+  llama2-7b-layer-fp8  as llama2-7b-layer, FP8 E4M3 codes (one byte per
+                   element, 537 MB of K and V per step); decode
 
 D = 128 and 64-token blocks throughout.  q ~ N(0, 1).  All values are fp16.
 """
@@ -28,6 +30,7 @@ from . import (BLOCK_TABLE, K_HIST, K_OUTLIER, LENGTHS, QUERY, V_HIST, V_OUTLIER
 
 INT4 = 0
 INT8 = 1
+FP8 = 2
 PAGE = 64
 
 CONFIGS = {
@@ -43,6 +46,9 @@ CONFIGS = {
     # grouped query heads (beyond the five configurations above): 32 query heads
     # over 8 cache heads, the Llama-3-8B attention shape
     6: dict(name="llama3-8b-layer-gqa", B=32, H=8, Hq=32, D=128, L=8192, fmt=INT4, sigma=1.0,
+            outliers=("per_head", 4, 10.0), table="contiguous"),
+    # the FP8 E4M3 cache on the 7B-layer shape
+    7: dict(name="llama2-7b-layer-fp8", B=8, H=32, D=128, L=8192, fmt=FP8, sigma=1.0,
             outliers=("per_head", 4, 10.0), table="contiguous"),
 }
 

@@ -91,7 +91,7 @@ def test_tiny_config_quantize_plus_one_decode_step(cuda_ok):
     assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
 
 
-@pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE])
+@pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE, kvq.KVQ_FP8_E4M3])
 def test_ragged_lengths_and_edges(cuda_ok, fmt):
     """Lengths at every unit/page edge, an empty sequence, a permuted table."""
     lens = [1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 0, 257, 700, 1000]
@@ -107,7 +107,7 @@ def test_ragged_lengths_and_edges(cuda_ok, fmt):
     assert np.isfinite(got).all()
 
 
-@pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE])
+@pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE, kvq.KVQ_FP8_E4M3])
 def test_batch_context_does_not_change_results(cuda_ok, fmt):
     """The same (sequence, head) attended alone or inside a large batch (so cut
     into different splits and merged) agrees to fp32 rounding."""
@@ -172,7 +172,7 @@ def test_host_rejects_bad_arguments(cuda_ok):
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE])
+@pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE, kvq.KVQ_FP8_E4M3])
 def test_one_head_split_over_the_whole_grid(cuda_ok, fmt):
     """One (sequence, head) long enough to be cut into about a thousand pieces:
     the warp that writes the last piece merges them all (more than one round of

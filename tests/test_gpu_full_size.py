@@ -7,6 +7,9 @@ at a time from the host twin of the generator.
   long-context     B=16, H=32, L=32768 int4 (2.1 GB packed): decode
   paged-int8       64 seqs, L ~ U[512, 16384], int8, permuted pages: decode
   prefill-append   64 x 4096 tokens, H=32, int4 into permuted pages
+  llama3-8b-layer-gqa  B=32, 8 cache heads x 4 query heads, L=8192 int4:
+                   decode steps through kvq_decode_attention_gqa, as timed
+  llama2-7b-layer-fp8  B=8, H=32, L=8192, FP8 E4M3: decode steps, as timed
 """
 import math
 
@@ -25,27 +28,32 @@ TOL = 2e-3
 D = 128
 
 
-def _oracle_one(wl, b, h, L, q_bits):
-    """oracle codes/scales and attention output of one (sequence, head)."""
+def _oracle_one(wl, b, h, L, q_bits, hq=None):
+    """oracle codes/scales and attention output of one (sequence, cache head h),
+    for query head hq (default h)."""
+    hq = h if hq is None else hq
     k = np.ascontiguousarray(wl.kv_host("k", b, 0, L)[:, h:h + 1, :])
     v = np.ascontiguousarray(wl.kv_host("v", b, 0, L)[:, h:h + 1, :])
     kc, ks = orc.quantize(wl.fmt, k)
     vc, vs = orc.quantize(wl.fmt, v)
     nb = kc.shape[0]
     bt = np.arange(nb, dtype=np.int32)[None, :]
-    q = np.ascontiguousarray(q_bits[b:b + 1, h:h + 1, :])
+    q = np.ascontiguousarray(q_bits[b:b + 1, hq:hq + 1, :])
     ref = orc.decode_attention(wl.fmt, kc, vc, ks, vs, bt, np.array([L]), q, np.float32(1 / math.sqrt(D)))
     vmax = orc.value_absmax(wl.fmt, vc, vs, bt, np.array([L]), 1, D)
     return kc, ks, vc, vs, ref[0, 0], vmax[0, 0]
 
 
 def _check_pairs(dw, lens, q_bits, out, pairs):
+    """pairs: (sequence, query head); query head i reads cache head i // g"""
     wl = dw.wl
+    g = wl.Hq // wl.H
     got = out.float().cpu().numpy()
     worst = 0.0
-    for b, h in pairs:
+    for b, hq in pairs:
         L = int(lens[b])
-        kc, ks, vc, vs, ref, vmax = _oracle_one(wl, b, h, L, q_bits)
+        h = hq // g
+        kc, ks, vc, vs, ref, vmax = _oracle_one(wl, b, h, L, q_bits, hq)
         pages = wl.block_table[b, :kc.shape[0]]
         gk = dw.cache.k_codes[torch.from_numpy(pages).long().cuda(), h].cpu().numpy()
         gv = dw.cache.v_codes[torch.from_numpy(pages).long().cuda(), h].cpu().numpy()
@@ -53,14 +61,18 @@ def _check_pairs(dw, lens, q_bits, out, pairs):
         assert np.array_equal(gv, vc[:, 0]), (b, h)
         gks = dw.cache.k_scales[torch.from_numpy(pages).long().cuda(), h].cpu().numpy()
         assert np.array_equal(gks.view(np.uint32), ks[:, 0].view(np.uint32)), (b, h)
-        err = np.max(np.abs(got[b, h] - ref)) / vmax
-        assert err <= TOL, (b, h, err)
+        err = np.max(np.abs(got[b, hq] - ref)) / vmax
+        assert err <= TOL, (b, hq, err)
         worst = max(worst, err)
     return worst
 
 
-def test_llama_layer_decode_steps(cuda_ok):
-    wl = W.make_workload(2, extra_tokens=64)
+@pytest.mark.parametrize("cfg", [2, 6, 7])
+def test_layer_decode_steps(cuda_ok, cfg):
+    """llama2-7b-layer (int4), llama3-8b-layer-gqa, llama2-7b-layer-fp8: three
+    timed-style steps, then sampled (sequence, query head) outputs and their
+    cache pages against the oracle."""
+    wl = W.make_workload(cfg, extra_tokens=64)
     dw = DeviceWorkload(wl)
     dw.prefill()
     step = DecodeStep(dw)
@@ -73,7 +85,7 @@ def test_llama_layer_decode_steps(cuda_ok):
         lens = lens + 1
     torch.cuda.synchronize()
     assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
-    _check_pairs(dw, lens, wl.q_host(2), out, synth_sample_heads(wl.B, wl.H, 6, seed=1))
+    _check_pairs(dw, lens, wl.q_host(2), out, synth_sample_heads(wl.B, wl.Hq, 6, seed=1))
 
 
 def test_long_context_decode(cuda_ok):

@@ -1,7 +1,8 @@
 """GPU parity of the fused quantize kernel (kvq_quantize, kvq_append) against
 the CPU oracle: codes and scales must be bit-exact.  Definition: quantize_block
-(jsqmd.com/news/887038 section 2.1) and the per-chunk INT8 variant
-(aicoding.csdn.net section 2.2)."""
+(jsqmd.com/news/887038 section 2.1), the per-chunk INT8 variant
+(aicoding.csdn.net section 2.2) and FP8 E4M3 with the scale set by max|x|
+(jsqmd.com/news/887038 section 2.2)."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +12,7 @@ from quantized_kv_cache_09_gb300 import kvq
 from quantized_kv_cache_09_gb300.synth import workloads as W
 
 pytestmark = pytest.mark.gpu
-FMTS = [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE]
+FMTS = [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE, kvq.KVQ_FP8_E4M3]
 D = 128
 
 
@@ -45,7 +46,7 @@ def test_random_tensors_bit_exact(cuda_ok, fmt, T):
     _assert_same(fmt, x.astype(np.float16).view(np.uint16))
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", FMTS[:2])
 def test_exact_rounding_ties_bit_exact(cuda_ok, fmt):
     """Blocks whose quotients are exact half-integers (x = k/2 with max|x| = 7.5
     or 127, scale = 1): every tie must round to even, as the oracle does."""
@@ -54,6 +55,25 @@ def test_exact_rounding_ties_bit_exact(cuda_ok, fmt):
     x = rng.integers(-int(2 * top), int(2 * top) + 1, (64 * 6, 3, D)).astype(np.float64) / 2
     x[::64, :, 0] = top
     _assert_same(fmt, x.astype(np.float16).view(np.uint16))
+
+
+def test_fp8_grid_midpoints_and_signed_zeros_bit_exact(cuda_ok):
+    """Blocks with max|x| = 448 (scale 1) whose elements are E4M3 values, the
+    midpoints between neighbours (ties to even), one binary16 step either side
+    of them, -0.0 and negatives that round to zero (code 0x80), under other
+    scales too (max|x| = 448 * 2^k, still exact quotients)."""
+    vals = np.array([orc.e4m3_to_float(c) for c in range(127)])
+    mids = (vals[:-1] + vals[1:]) / 2
+    pool = np.concatenate([vals, mids]).astype(np.float16)
+    pool = np.concatenate([pool, np.nextafter(pool, np.float16(np.inf)), np.nextafter(pool, np.float16(-np.inf))])
+    pool = pool[np.isfinite(pool) & (np.abs(pool) <= 448)]
+    rng = np.random.default_rng(9)
+    x = rng.choice(pool, (64 * 8, 3, D)) * rng.choice([-1.0, 1.0], (64 * 8, 3, D))
+    x[::64, :, 0] = 448.0
+    x[1::64, :, :4] = [-0.0, -2.0 ** -11, -2.0 ** -12, 2.0 ** -11]
+    for k, blk in enumerate(range(4, 8)):   # scales 2^-3 .. 2^0 times larger quotients stay exact
+        x[64 * blk:64 * blk + 64] *= 2.0 ** (-k - 1)
+    _assert_same(kvq.KVQ_FP8_E4M3, x.astype(np.float16).view(np.uint16))
 
 
 @pytest.mark.parametrize("fmt", FMTS)
