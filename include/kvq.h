@@ -177,6 +177,12 @@ size_t kvq_decode_workspace_bytes(kvq_format fmt, int32_t num_heads, int32_t hea
  *                    ready for the next one.  After a call that set a
  *                    KVQ_FLAG_* bit, zero it again.  Do not share one
  *                    workspace between calls that may run concurrently
+ * Launch: with programmatic dependent launch, the kernel starts while the
+ * previous kernel of the stream finishes and reads seq_lens and block_table
+ * before waiting for it (the codes, scales, q and out only after).  No kvq_*
+ * call writes those two arrays; a caller's own kernel that writes them right
+ * before this call must not trigger its dependents early
+ * (griddepcontrol.launch_dependents) -- ordinary launches never do.
  * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE,
  * KVQ_ERR_CUDA; device-side problems set KVQ_FLAG_* bits in cache->status.
  */

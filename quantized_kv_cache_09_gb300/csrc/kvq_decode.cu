@@ -967,7 +967,11 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     const int H = p.num_heads;
     const int max_len = p.max_blocks * kPage;
     pdl_launch_dependents();
-    pdl_wait();
+    // Until pdl_wait below, the previous kernel of the stream may still be
+    // running.  Only the sequence lengths and the block table are read before
+    // it: no kernel of this library writes them (the codes, scales, query and
+    // output are touched only after the wait), so the prologue and the first
+    // block-table fetch overlap the previous kernel's tail.
 
     // ---- per-sequence lengths and the (H x units) prefix, in shared memory ----
     for (int b = tid; b < B; b += blockDim.x) {
@@ -1003,41 +1007,19 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         if (lane == 31) s_cu[B] = incl;
     }
     __syncthreads();
-    if (warp == 0) {  // no warp owns a unit of an empty sequence: its rows are zeros
-        for (int base = 0; base < B; base += 32) {
-            uint32_t m = __ballot_sync(kFull, base + lane < B && s_len[base + lane] == 0);
-            while (m) {
-                const int b = base + __ffs(m) - 1;
-                m &= m - 1;
-                if (b % (int)gridDim.x != (int)blockIdx.x) continue;
-                uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)b * H * G * kHeadDim);
-                for (int e = lane; e < H * G * (kHeadDim / 8); e += 32) row[e] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-    }
 
     const int64_t U = s_cu[B];
-    if (U == 0) return;
     const int64_t GW = imin64((int64_t)grid_warps, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);  // active warps
     // logical warp index, round-robin over the CTAs: when fewer than all warps
     // have work (G < grid warps) the active ones spread over every SM
     const int gw = warp * (int)gridDim.x + blockIdx.x;
-    if (gw >= GW) return;
-    const int64_t x0 = U * gw / GW;
-    const int64_t x1 = U * (gw + 1) / GW;
-    if (x0 >= x1) return;
-
-    WS &ws = wsm_all[warp];
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < kStages; s++) mbar_init(&ws.full[s], 1);
-        mbar_init_fence();
-    }
-    __syncwarp();
+    const int64_t x0 = gw < GW ? U * gw / GW : 0;
+    const int64_t x1 = gw < GW ? U * (gw + 1) / GW : 0;
+    const bool active = x0 < x1;
 
     // ---- issue cursor: unit x0 + ni = (ib, ih, ic) ----
-    int ib, ih, ic;
-    {
+    int ib = 0, ih = 0, ic = 0;
+    if (active) {
         int lo = 0, hi = B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -1050,10 +1032,55 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         ic = off % n;
     }
     int inb = units_of(s_len[ib], UT);  // units of the issue cursor's sequence
-    // page ring: lane l holds page slot ring_j0 + l of (ring_b, ring_h)
+    // page ring: lane l holds page slot ring_j0 + l of (ring_b, ring_h) and,
+    // once loaded (after the wait: appends write them), its two scales
     int ring_b = -1, ring_h = -1, ring_j0 = 0;
     int r_page = 0;
     float r_sk = 0.0f, r_sv = 0.0f;
+    bool ring_scales_due = false;
+    auto ring_pages = [&](int b, int h, int j) {
+        ring_b = b;
+        ring_h = h;
+        ring_j0 = j;
+        const int jl = j + lane;
+        const int npages = (s_len[b] + kPage - 1) / kPage;
+        int pg = 0;
+        if (jl < npages) {
+            pg = p.block_table[(int64_t)b * p.max_blocks + jl];
+            if (pg < 0 || pg >= p.num_pages) {
+                set_flag(p.status, KVQ_FLAG_BAD_PAGE);
+                pg = 0;
+            }
+        }
+        r_page = pg;
+        ring_scales_due = true;
+    };
+    if (active) ring_pages(ib, ih, ic / UPP);
+
+    pdl_wait();  // from here on, the previous kernel's writes are visible
+
+    if (warp == 0) {  // no warp owns a unit of an empty sequence: its rows are zeros
+        for (int base = 0; base < B; base += 32) {
+            uint32_t m = __ballot_sync(kFull, base + lane < B && s_len[base + lane] == 0);
+            while (m) {
+                const int b = base + __ffs(m) - 1;
+                m &= m - 1;
+                if (b % (int)gridDim.x != (int)blockIdx.x) continue;
+                uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)b * H * G * kHeadDim);
+                for (int e = lane; e < H * G * (kHeadDim / 8); e += 32) row[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
+    if (!active) return;
+
+    WS &ws = wsm_all[warp];
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; s++) mbar_init(&ws.full[s], 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
     const int N = (int)(x1 - x0);  // units of this warp
     constexpr uint32_t kPageBytes = kPage * RB;
 
@@ -1066,36 +1093,15 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         const int s = ci % kStages;
         const int j = ic / UPP;
         const int nh = UPS > 1 ? min(min(UPS - ic % UPS, inb - ic), N - nis) : 1;
-        if (ib != ring_b || ih != ring_h || j >= ring_j0 + 32) {
-            ring_b = ib;
-            ring_h = ih;
-            ring_j0 = j;
-            const int jl = j + lane;
-            const int npages = (s_len[ib] + kPage - 1) / kPage;
-            int pg = 0;
-            float sk = 0.0f, sv = 0.0f;
-            if (jl < npages) {
-                pg = p.block_table[(int64_t)ib * p.max_blocks + jl];
-                if (pg < 0 || pg >= p.num_pages) {
-                    set_flag(p.status, KVQ_FLAG_BAD_PAGE);
-                    pg = 0;
-                }
-                sk = p.k_scales[(int64_t)pg * H + ih];
-                sv = p.v_scales[(int64_t)pg * H + ih];
-            }
-            r_page = pg;
-            r_sk = sk;
-            r_sv = sv;
-        }
+        if (ib != ring_b || ih != ring_h || j >= ring_j0 + 32) ring_pages(ib, ih, j);
         const int pg = __shfl_sync(kFull, r_page, j - ring_j0);
-        const float sk = __shfl_sync(kFull, r_sk, j - ring_j0);
-        const float sv = __shfl_sync(kFull, r_sv, j - ring_j0);
         const bool new_seg = (ci == 0) || (ic == 0);
+        if (ring_scales_due) {  // the ring's scales (after the wait: appends write them)
+            r_sk = p.k_scales[(int64_t)r_page * H + ring_h];
+            r_sv = p.v_scales[(int64_t)r_page * H + ring_h];
+            ring_scales_due = false;
+        }
         if (lane == 0) {
-            const int ntok = min(nh * UT, s_len[ib] - ic * UT);
-            *reinterpret_cast<int4 *>(&ws.meta[s].b) = make_int4(ib, ih, ic, ntok);
-            *reinterpret_cast<float4 *>(&ws.meta[s].sk) =
-                make_float4(sk, sv, __int_as_float(new_seg ? 1 : 0), __int_as_float(nh));
             // The refill of stage s follows the warp's reads of it: every lane
             // consumed those values (mma operands) before the __syncwarp that
             // precedes this issue, so the copy cannot overtake them.
@@ -1107,6 +1113,14 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             bulk_copy_g2s(ws.v[s], p.v_codes + off, cb, &ws.full[s]);
             if (new_seg)
                 bulk_copy_g2s(ws.q[s], p.q + ((size_t)ib * H + ih) * G * kHeadDim, G * kHeadDim * 2, &ws.full[s]);
+        }
+        const float sk = __shfl_sync(kFull, r_sk, j - ring_j0);
+        const float sv = __shfl_sync(kFull, r_sv, j - ring_j0);
+        if (lane == 0) {
+            const int ntok = min(nh * UT, s_len[ib] - ic * UT);
+            *reinterpret_cast<int4 *>(&ws.meta[s].b) = make_int4(ib, ih, ic, ntok);
+            *reinterpret_cast<float4 *>(&ws.meta[s].sk) =
+                make_float4(sk, sv, __int_as_float(new_seg ? 1 : 0), __int_as_float(nh));
         }
         // advance the cursor by the chunk
         ic += nh;
