@@ -363,6 +363,25 @@ def measure_decode(name, K, Wm, seed, dev, pg):
     rc, flags = kvq.kvq_get_device_status(dw.cache)
     if rc != 0:
         raise RuntimeError(f"device status {rc} flags {flags:#x} after timed steps")
+    # (3) the steps replayed from one CUDA graph holding the 64-step input cycle
+    # (kvq_step_graph, captured before the timed loop): ceil(K / 64) replays
+    graph = kvq.StepGraph([step.graph_step(lens_b[s], lens_a[s], k_steps[s], v_steps[s], q_steps[s])
+                           for s in range(NS)])
+    graph.launch()
+    _sync_all(pg, dev)
+    reps = -(-K // NS)
+    g_s = torch.cuda.Event(enable_timing=True)
+    g_e = torch.cuda.Event(enable_timing=True)
+    g_s.record(stream)
+    for i in range(reps):
+        graph.launch()
+    g_e.record(stream)
+    _sync_all(pg, dev)
+    graph_ms = g_s.elapsed_time(g_e) * K / (reps * NS)  # per K steps
+    graph.close()
+    rc, flags = kvq.kvq_get_device_status(dw.cache)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} flags {flags:#x} after graph steps")
 
     # end to end through the C ABI with host buffers
     pin_k = [k.cpu().pin_memory() for k in k_steps]
@@ -391,7 +410,7 @@ def measure_decode(name, K, Wm, seed, dev, pg):
 
     ctx = [(wl.lens + ((Wm + K + i) % NS if aligned else 0) + 1) for i in range(K)]
     dec_bytes = sum(wl.decode_bytes(c) for c in ctx) / K
-    res = dict(wl=wl, B=B, H=H, D=D, aligned=aligned, total_ms=total_ms, app_ms=app_ms, dec_ms=dec_ms,
+    res = dict(wl=wl, B=B, H=H, D=D, aligned=aligned, total_ms=total_ms, app_ms=app_ms, dec_ms=dec_ms, graph_ms=graph_ms,
                e2e_ms=e2e_ms, Ke=Ke, dec_bytes=dec_bytes, clocks=clocks.summary(), split_ms=split_ms,
                h2d=(2 * H + Hq) * B * D * 2, d2h=B * Hq * D * 2, launches=(1 + -(-B // 512)) * K, Hq=Hq)
     del dw
@@ -481,6 +500,7 @@ def run_ours(args):
     e2e_ms = max_over_ranks(pg, r["e2e_ms"], dev)
     dec_ms = max_over_ranks(pg, r["dec_ms"], dev)
     app_ms = max_over_ranks(pg, r["app_ms"], dev)
+    graph_ms = max_over_ranks(pg, r["graph_ms"], dev)
     B = r["B"]
     wl = r["wl"]
     achieved = r["dec_bytes"] / (dec_ms * 1e-3) / 1e9
@@ -499,6 +519,8 @@ def run_ours(args):
                        "l2": "inputs larger than L2" if r["dec_bytes"] > 129e6 else "fits in L2 (no flush)"},
             "kv_gb_per_s": achieved, "decode_us": dec_ms * 1e3, "append_us": app_ms * 1e3,
             "step_us_events_between_calls": r["split_ms"] / K * 1e3,
+            "graph": {"ms_per_step": graph_ms / K, "value": whole_job_rate(world, B * K, graph_ms * 1e-3),
+                      "unit": "tokens/s", "how": "one kvq_step_graph of 64 steps (append + decode each), replayed"},
             "roofline": {"kernel": "kvq_decode_attention (decode_split_kernel, merge fused)", "bound": "hbm",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": ncu_traffic("decode_split_kernel", args.workload),

@@ -239,6 +239,72 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const uint16_t *
                                         float softmax_scale, uint16_t *out, kvq_stream_t stream);
 
 /*
+ * Decode step as a CUDA graph (CUDA Graph instance reuse: "hardware-aware
+ * scheduling" page, jsqmd.com/news/887038, section 4.1 -- capture once,
+ * rebind tensor addresses with cudaGraphExecUpdate instead of rebuilding).
+ *
+ * One step = kvq_append of the new tokens, then kvq_decode_attention_gqa
+ * over the grown sequences, with the arguments below (each field as in those
+ * two calls; seq_lens = the lengths after the append).  A graph holds a
+ * sequence of num_steps steps, step i on caches[i] with args[i] -- the layers
+ * of one model's decode step, or successive steps of one layer -- in that
+ * order, with the same programmatic-dependent-launch edges as eager calls
+ * on one stream, so consecutive launches inside the graph overlap as they
+ * would eagerly (between two graph launches they do not).  The graph records
+ * the launches with these pointers and sizes; every kvq_step_graph_launch
+ * replays them with whatever the buffers hold at that time, so per-step
+ * inputs are written into the same buffers (sequence lengths and contents may
+ * change freely between launches; the kernels read them from device memory).
+ */
+typedef struct kvq_step_args {
+    const uint16_t *k_new;          /* append: fp16 [total_new_tokens][H][128] */
+    const uint16_t *v_new;
+    const int32_t *cu_seqlens;      /* [num_seqs + 1] */
+    const int32_t *seq_lens_before; /* [num_seqs] */
+    int64_t total_new_tokens;
+    int32_t max_new_tokens;
+    const int32_t *block_table;     /* [num_seqs][max_blocks_per_seq], both calls */
+    int32_t max_blocks_per_seq;
+    int32_t num_seqs;
+    const uint16_t *q;              /* decode: fp16 [num_seqs][num_q_heads][128] */
+    int32_t num_q_heads;
+    const int32_t *seq_lens;        /* [num_seqs], lengths after the append */
+    float softmax_scale;
+    uint16_t *out;                  /* fp16 [num_seqs][num_q_heads][128] */
+    void *workspace;
+    size_t workspace_bytes;
+} kvq_step_args;
+
+typedef struct kvq_step_graph kvq_step_graph; /* opaque; host memory + one executable CUDA graph */
+
+/*
+ * kvq_step_graph_create -- check the arguments as the calls would, capture
+ * the num_steps >= 1 steps (caches[i], args[i]) on a private stream of the
+ * current device and instantiate them as one graph.
+ * *graph_out receives a handle owned by the caller (kvq_step_graph_destroy).
+ * Nothing is launched.  Errors: those of kvq_append and
+ * kvq_decode_attention_gqa, KVQ_ERR_CUDA for a failed capture.
+ */
+kvq_status kvq_step_graph_create(const kvq_cache *caches, const kvq_step_args *args, int32_t num_steps,
+                                 kvq_step_graph **graph_out);
+
+/*
+ * kvq_step_graph_update -- rebind the graph to new buffers / sizes: capture the
+ * steps again and update the executable graph in place (cudaGraphExecUpdate);
+ * when the launch structure changed (a different format, group size, number
+ * of launches or of steps) it is instantiated anew.  On an error the graph keeps
+ * its previous binding.
+ */
+kvq_status kvq_step_graph_update(kvq_step_graph *graph, const kvq_cache *caches, const kvq_step_args *args,
+                                 int32_t num_steps);
+
+/* kvq_step_graph_launch -- replay the steps on `stream` (asynchronous). */
+kvq_status kvq_step_graph_launch(const kvq_step_graph *graph, kvq_stream_t stream);
+
+/* kvq_step_graph_destroy -- release the graph (NULL is a no-op); no launch may be pending. */
+kvq_status kvq_step_graph_destroy(kvq_step_graph *graph);
+
+/*
  * kvq_get_device_status -- synchronise the stream, read and clear the cache's
  * device status word.  *flags_out (host, may be NULL) receives the KVQ_FLAG_*
  * bits.  Returns KVQ_OK when no bit was set, else the kvq_status of the most

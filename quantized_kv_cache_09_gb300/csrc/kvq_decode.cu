@@ -1270,6 +1270,19 @@ bool decode_group_supported(int fmt, int group)
     return group == 1 || (fmt == KVQ_INT4_B64 && (group == 2 || group == 4));
 }
 
+int decode_prepare(int fmt, int group)
+{
+    if (fmt == KVQ_INT4_B64) {
+        if (group == 1) return ctas_per_sm<KVQ_INT4_B64, 1>();
+        if (group == 2) return ctas_per_sm<KVQ_INT4_B64, 2>();
+        if (group == 4) return ctas_per_sm<KVQ_INT4_B64, 4>();
+        return 0;
+    }
+    if (group != 1) return 0;
+    if (fmt == KVQ_FP8_E4M3) return ctas_per_sm<KVQ_FP8_E4M3, 1>();
+    return ctas_per_sm<KVQ_INT8_PAGE, 1>();
+}
+
 size_t decode_workspace_bytes(int fmt, int group)
 {
     const int gw = decode_grid_warps(fmt);

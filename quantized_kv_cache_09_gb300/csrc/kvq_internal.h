@@ -101,6 +101,9 @@ cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s);
 int decode_grid_warps(int fmt);
 bool decode_group_supported(int fmt, int group);
 size_t decode_workspace_bytes(int fmt, int group);
+// resolves (and caches) the occupancy query and shared-memory attribute of the
+// decode kernel for (fmt, group); returns CTAs per SM, 0 when unsupported
+int decode_prepare(int fmt, int group);
 cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s);
 
 }  // namespace kvq

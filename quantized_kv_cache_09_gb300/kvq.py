@@ -31,7 +31,9 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attention",
            "kvq_decode_workspace_bytes_gqa", "kvq_decode_attention_gqa",
-           "kvq_decode_attention_noalloc", "kvq_get_device_status", "kvq_status_string", "kvq_version")
+           "kvq_decode_attention_noalloc", "kvq_step_graph_create", "kvq_step_graph_update",
+           "kvq_step_graph_launch", "kvq_step_graph_destroy", "kvq_get_device_status", "kvq_status_string",
+           "kvq_version")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -47,6 +49,15 @@ class kvq_cache(ctypes.Structure):
                 ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
                 ("v_scales", ctypes.c_void_p), ("k_tail", ctypes.c_void_p), ("v_tail", ctypes.c_void_p),
                 ("status", ctypes.c_void_p)]
+
+
+class kvq_step_args(ctypes.Structure):
+    _fields_ = [("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
+                ("seq_lens_before", ctypes.c_void_p), ("total_new_tokens", ctypes.c_int64),
+                ("max_new_tokens", ctypes.c_int32), ("block_table", ctypes.c_void_p),
+                ("max_blocks_per_seq", ctypes.c_int32), ("num_seqs", ctypes.c_int32), ("q", ctypes.c_void_p),
+                ("num_q_heads", ctypes.c_int32), ("seq_lens", ctypes.c_void_p), ("softmax_scale", ctypes.c_float),
+                ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -80,6 +91,15 @@ def lib():
         L.kvq_decode_attention_gqa.restype = ctypes.c_int
         L.kvq_decode_attention_noalloc.argtypes = [cp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp]
         L.kvq_decode_attention_noalloc.restype = ctypes.c_int
+        ap = ctypes.POINTER(kvq_step_args)
+        L.kvq_step_graph_create.argtypes = [cp, ap, i32, ctypes.POINTER(vp)]
+        L.kvq_step_graph_create.restype = ctypes.c_int
+        L.kvq_step_graph_update.argtypes = [vp, cp, ap, i32]
+        L.kvq_step_graph_update.restype = ctypes.c_int
+        L.kvq_step_graph_launch.argtypes = [vp, vp]
+        L.kvq_step_graph_launch.restype = ctypes.c_int
+        L.kvq_step_graph_destroy.argtypes = [vp]
+        L.kvq_step_graph_destroy.restype = ctypes.c_int
         L.kvq_get_device_status.argtypes = [cp, vp, ctypes.POINTER(i32)]
         L.kvq_get_device_status.restype = ctypes.c_int
         L.kvq_status_string.argtypes = [ctypes.c_int]
@@ -209,6 +229,78 @@ def kvq_decode_attention_noalloc(cache, q, block_table, seq_lens, softmax_scale,
                                               _ptr(out), _stream(stream, q.device)), "kvq_decode_attention_noalloc")
 
 
+class StepGraph:
+    """kvq_step_graph_*: a sequence of decode steps -- each appends one chunk of
+    new tokens per sequence, then runs decode attention over the grown
+    sequences -- captured once into one CUDA graph bound to these tensors;
+    launch() replays them with whatever the tensors hold then.  Per-step inputs
+    are written into the same tensors.
+
+    steps: a list of tuples (cache, k_new, v_new, cu_seqlens, block_table,
+    seq_lens_before, max_new_tokens, q, seq_lens, softmax_scale, out,
+    workspace), run in order (e.g. a model's layers)."""
+
+    def __init__(self, steps):
+        self._h = None
+        caches, args, keep = self._pack(steps)
+        h = ctypes.c_void_p()
+        _check(lib().kvq_step_graph_create(caches, args, len(steps), ctypes.byref(h)), "kvq_step_graph_create")
+        self._h, self._caches, self._args, self._keep = h, caches, args, keep
+        self._device = steps[0][7].device
+
+    @staticmethod
+    def _pack(steps):
+        if not steps:
+            raise ValueError("no steps")
+        n = len(steps)
+        caches = (kvq_cache * n)()
+        args = (kvq_step_args * n)()
+        keep = []
+        for i, st in enumerate(steps):
+            (cache, k_new, v_new, cu_seqlens, block_table, seq_lens_before, max_new_tokens, q, seq_lens,
+             softmax_scale, out, workspace) = st
+            for t, dt, name in ((k_new, torch.float16, "k_new"), (v_new, torch.float16, "v_new"),
+                                (cu_seqlens, torch.int32, "cu_seqlens"), (block_table, torch.int32, "block_table"),
+                                (seq_lens_before, torch.int32, "seq_lens_before"), (q, torch.float16, "q"),
+                                (seq_lens, torch.int32, "seq_lens"), (out, torch.float16, "out"),
+                                (workspace, torch.uint8, "workspace")):
+                _cuda(t, dt, name)
+            B = q.shape[0]
+            if (out.shape != q.shape or seq_lens.numel() != B or seq_lens_before.numel() != B or
+                    cu_seqlens.numel() != B + 1 or block_table.dim() != 2 or block_table.shape[0] != B or
+                    k_new.shape != v_new.shape or k_new.dim() != 3):
+                raise ValueError(f"step {i}: tensor shapes disagree")
+            caches[i] = cache.struct
+            args[i] = kvq_step_args(k_new.data_ptr(), v_new.data_ptr(), cu_seqlens.data_ptr(),
+                                    seq_lens_before.data_ptr(), k_new.shape[0], int(max_new_tokens),
+                                    block_table.data_ptr(), block_table.shape[1], B, q.data_ptr(), q.shape[1],
+                                    seq_lens.data_ptr(), float(softmax_scale), out.data_ptr(), workspace.data_ptr(),
+                                    workspace.numel())
+            keep.append(st)
+        return caches, args, keep
+
+    def update(self, steps):
+        """Rebind to other tensors (cudaGraphExecUpdate, or a new instance when the launches differ)."""
+        caches, args, keep = self._pack(steps)
+        _check(lib().kvq_step_graph_update(self._h, caches, args, len(steps)), "kvq_step_graph_update")
+        self._caches, self._args, self._keep = caches, args, keep
+
+    def launch(self, stream=None):
+        _check(lib().kvq_step_graph_launch(self._h, _stream(stream, self._device)), "kvq_step_graph_launch")
+
+    def close(self):
+        if self._h is not None:
+            torch.cuda.synchronize(self._device)
+            _check(lib().kvq_step_graph_destroy(self._h), "kvq_step_graph_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def kvq_get_device_status(cache, stream=None):
     """(status, flags): reads and clears the cache's device status word (synchronises the stream)."""
     flags = ctypes.c_int32(0)
@@ -272,4 +364,4 @@ class PagedKVCache:
 __all__ = ["KVQ_INT4_B64", "KVQ_INT8_PAGE", "KVQ_FP8_E4M3", "HEAD_DIM", "PAGE_TOKENS", "EXPORTS", "KvqError", "kvq_cache",
            "PagedKVCache", "lib", "library_path", "kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes",
            "kvq_decode_attention", "kvq_decode_attention_noalloc", "kvq_get_device_status", "kvq_status_string",
-           "kvq_version"]
+           "kvq_version", "StepGraph", "kvq_step_args"]

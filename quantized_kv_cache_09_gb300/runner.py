@@ -84,8 +84,18 @@ class DecodeStep:
         dw = self.dw
         kvq.kvq_append(dw.cache, k1, v1, self.cu, dw.block_table, lens_before, 1, stream)
         kvq.kvq_decode_attention_gqa(dw.cache, q, dw.block_table, lens_after, dw.softmax_scale, self.out,
-                                 dw.workspace, stream)
+                                     dw.workspace, stream)
         return self.out
+
+    def graph_step(self, lens_before, lens_after, k1, v1, q):
+        """This step's entry of a kvq.StepGraph (bound to these tensors and self.out)."""
+        dw = self.dw
+        return (dw.cache, k1, v1, self.cu, dw.block_table, lens_before, 1, q, lens_after, dw.softmax_scale,
+                self.out, dw.workspace)
+
+    def graph(self, lens_before, lens_after, k1, v1, q):
+        """The step as a one-step kvq.StepGraph."""
+        return kvq.StepGraph([self.graph_step(lens_before, lens_after, k1, v1, q)])
 
 
 def kernel_names():
