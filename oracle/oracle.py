@@ -113,6 +113,34 @@ def decode_attention(fmt, k_codes, v_codes, k_scales, v_scales, block_table, seq
     return out
 
 
+def prefill_attention(fmt, k_codes, v_codes, k_scales, v_scales, block_table, seq_lens, cu_seqlens_q, q_bits,
+                      softmax_scale):
+    """Binary64 causal attention of a chunk of new tokens over the paged cache
+    that already holds them.  Sequence b's chunk is its last
+    n_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] tokens: query i (row
+    cu_seqlens_q[b] + i of q [total][Hq][D]) sits at position
+    p = seq_lens[b] - n_b + i and attends to the keys at positions 0 .. p.
+    That is, by definition, decode attention of each query over the first
+    p + 1 tokens of its sequence -- evaluated here with decode_attention, one
+    query per row.  Returns float64 [total][Hq][D]."""
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.asarray(seq_lens, dtype=np.int64)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    total = int(cu[-1])
+    if total == 0:
+        return np.zeros((0,) + q.shape[1:], dtype=np.float64)
+    rows = np.zeros(total, dtype=np.int64)
+    lens = np.zeros(total, dtype=np.int32)
+    for b in range(len(sl)):
+        n = int(cu[b + 1] - cu[b])
+        if n > sl[b]:
+            raise ValueError("a chunk longer than its sequence")
+        rows[cu[b]:cu[b + 1]] = b
+        lens[cu[b]:cu[b + 1]] = sl[b] - n + 1 + np.arange(n)
+    return decode_attention(fmt, k_codes, v_codes, k_scales, v_scales, bt[rows], lens, q, softmax_scale)
+
+
 def value_absmax(fmt, v_codes, v_scales, block_table, seq_lens, H, D):
     """max |v^| per (sequence, head), float64 [B][H]."""
     v_codes = np.ascontiguousarray(v_codes, dtype=np.uint8)
@@ -146,7 +174,8 @@ def normalized_error(out_test, out_ref, vmax):
     return float(r.max()) if r.size else 0.0
 
 
-__all__ = ["INT4", "INT8", "FP8", "BLOCK", "e4m3_to_float", "float_to_e4m3", "lib", "quantize", "decode_attention", "value_absmax",
+__all__ = ["INT4", "INT8", "FP8", "BLOCK", "e4m3_to_float", "float_to_e4m3", "lib", "quantize", "decode_attention",
+           "prefill_attention", "value_absmax",
            "quantize_into_pages", "normalized_error", "half_to_float", "row_bytes"]
 
 if os.environ.get("KVQ_ORACLE_EAGER"):
