@@ -239,6 +239,30 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const uint16_t *
                                         float softmax_scale, uint16_t *out, kvq_stream_t stream);
 
 /*
+ * kvq_prefill_attention -- chunked-prefill attention over the quantized paged
+ * cache (dynamic chunked attention of new tokens: "R1 performance overview",
+ * aicoding.csdn.net; paging: ddd.cn section 4).  The chunk of sequence b is
+ * its last n_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] tokens, already in the
+ * cache (kvq_append); query i of it (row cu_seqlens_q[b] + i of q) sits at
+ * position p = seq_lens[b] - n_b + i and attends causally:
+ *   out[row][hq][:] = sum_{t <= p} softmax_t(softmax_scale q . k^_t) v^_t
+ * over cache head hq / g (g = num_q_heads / cache->num_heads, any g >= 1),
+ * binary32 accumulation on the tensor cores (fp16 codes, probabilities
+ * rounded to fp16 as the second operand).
+ *   q, out           fp16 [total_q][num_q_heads][head_dim], 16-byte aligned
+ *   cu_seqlens_q     device int32 [num_seqs + 1], non-decreasing, cu[0] >= 0
+ *   max_q_per_seq    host bound on every n_b (sizes the grid); 0 is a no-op
+ *   seq_lens         device int32 [num_seqs], n_b <= seq_lens[b] <= max_blocks_per_seq * 64
+ * A sequence that breaks a bound is skipped and KVQ_FLAG_BAD_LENGTH set; a
+ * block-table entry out of range sets KVQ_FLAG_BAD_PAGE (page 0 is read
+ * instead).  Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA.
+ */
+kvq_status kvq_prefill_attention(const kvq_cache *cache, const uint16_t *q, int32_t num_q_heads,
+                                 const int32_t *cu_seqlens_q, int64_t total_q, int32_t max_q_per_seq,
+                                 const int32_t *block_table, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                 int32_t num_seqs, float softmax_scale, uint16_t *out, kvq_stream_t stream);
+
+/*
  * Decode step as a CUDA graph (CUDA Graph instance reuse: "hardware-aware
  * scheduling" page, jsqmd.com/news/887038, section 4.1 -- capture once,
  * rebind tensor addresses with cudaGraphExecUpdate instead of rebuilding).

@@ -171,6 +171,43 @@ kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, i
     return KVQ_OK;
 }
 
+kvq_status kvq_prefill_attention(const kvq_cache *cache, const uint16_t *q, int32_t num_q_heads,
+                                 const int32_t *cu_seqlens_q, int64_t total_q, int32_t max_q_per_seq,
+                                 const int32_t *block_table, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                 int32_t num_seqs, float softmax_scale, uint16_t *out, kvq_stream_t stream)
+{
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (num_seqs < 0 || max_q_per_seq < 0 || total_q < 0 || max_blocks_per_seq <= 0 || !isfinite(softmax_scale))
+        return KVQ_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_q_heads % cache->num_heads) return KVQ_ERR_INVALID_ARG;
+    if (num_seqs == 0 || max_q_per_seq == 0 || total_q == 0) return KVQ_OK;
+    if (!q || !out || !cu_seqlens_q || !block_table || !seq_lens || !aligned16(q) || !aligned16(out))
+        return KVQ_ERR_INVALID_ARG;
+    if (num_seqs > 65535 || num_q_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    kvq::PrefillParams p;
+    p.k_codes = cache->k_codes;
+    p.v_codes = cache->v_codes;
+    p.k_scales = cache->k_scales;
+    p.v_scales = cache->v_scales;
+    p.q = q;
+    p.out = out;
+    p.cu_q = cu_seqlens_q;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    p.status = cache->status;
+    p.num_seqs = num_seqs;
+    p.num_heads = cache->num_heads;
+    p.num_q_heads = num_q_heads;
+    p.group = num_q_heads / cache->num_heads;
+    p.num_pages = cache->num_pages;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_q = max_q_per_seq;
+    p.total_q = total_q;
+    p.score_scale = softmax_scale * 1.4426950408889634f;
+    return from_cuda(kvq::launch_prefill(cache->fmt, p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_get_device_status(const kvq_cache *cache, kvq_stream_t stream, int32_t *flags_out)
 {
     if (!cache) return KVQ_ERR_INVALID_ARG;

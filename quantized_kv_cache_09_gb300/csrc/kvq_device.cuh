@@ -108,6 +108,52 @@ __device__ __forceinline__ void pdl_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ---- fp16 helpers shared by the attention kernels ----
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
+
+// {RN16(x0), RN16(x1)} as one fp16 pair (x0 in the low half)
+__device__ __forceinline__ uint32_t f16x2_rn(float x0, float x1)
+{
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(x1), "f"(x0));
+    return d;
+}
+
+// exact widening of one-byte codes to fp16 pairs
+//   int8 word (4 bytes, element j in byte j): returns {c0,c1},{c2,c3}
+//   1024 + (byte ^ 0x80) - 1152 = c
+__device__ __forceinline__ void widen_int8(uint32_t w, __half2 c[2])
+{
+    const uint32_t x = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
+    const __half2 k1152 = __float2half2_rn(1152.0f);
+    c[0] = __hsub2(*reinterpret_cast<const __half2 *>(&a), k1152);
+    c[1] = __hsub2(*reinterpret_cast<const __half2 *>(&b), k1152);
+}
+
+// FP8 E4M3 word (element j in byte j): returns {c0,c1},{c2,c3} by the hardware
+// conversion, exact (every finite E4M3 value is a binary16 value)
+__device__ __forceinline__ void widen_e4m3(uint32_t w, __half2 c[2])
+{
+    uint32_t a, b;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(a) : "h"(static_cast<unsigned short>(w & 0xffffu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b) : "h"(static_cast<unsigned short>(w >> 16)));
+    c[0] = *reinterpret_cast<const __half2 *>(&a);
+    c[1] = *reinterpret_cast<const __half2 *>(&b);
+}
+
+// D += A * B, m16n8k16, fp16 operands, fp32 accumulators
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;

@@ -59,6 +59,22 @@ constexpr int kPartialStride = 132;
 // sequences per split-kernel launch (the per-CTA prefix lives in shared memory)
 constexpr int kMaxSeqsPerLaunch = 512;
 
+struct PrefillParams {
+    const uint8_t *k_codes;
+    const uint8_t *v_codes;
+    const float *k_scales;
+    const float *v_scales;
+    const uint16_t *q;            // [total_q][num_q_heads][128]
+    uint16_t *out;                // [total_q][num_q_heads][128]
+    const int32_t *cu_q;          // [num_seqs + 1]: sequence b's queries are rows cu_q[b] .. cu_q[b+1]-1
+    const int32_t *seq_lens;      // [num_seqs]: lengths including the chunk
+    const int32_t *block_table;   // [num_seqs][max_blocks]
+    int32_t *status;
+    int num_seqs, num_heads, num_q_heads, group, num_pages, max_blocks, max_q;
+    int64_t total_q;
+    float score_scale;            // softmax_scale * log2(e)
+};
+
 // launch `kernel` with programmatic stream serialization (see pdl_wait)
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
@@ -105,5 +121,6 @@ size_t decode_workspace_bytes(int fmt, int group);
 // decode kernel for (fmt, group); returns CTAs per SM, 0 when unsupported
 int decode_prepare(int fmt, int group);
 cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s);
+cudaError_t launch_prefill(int fmt, const PrefillParams &p, cudaStream_t s);
 
 }  // namespace kvq

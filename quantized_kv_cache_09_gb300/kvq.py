@@ -31,7 +31,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attention",
            "kvq_decode_workspace_bytes_gqa", "kvq_decode_attention_gqa",
-           "kvq_decode_attention_noalloc", "kvq_step_graph_create", "kvq_step_graph_update",
+           "kvq_decode_attention_noalloc", "kvq_prefill_attention", "kvq_step_graph_create", "kvq_step_graph_update",
            "kvq_step_graph_launch", "kvq_step_graph_destroy", "kvq_get_device_status", "kvq_status_string",
            "kvq_version")
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -91,6 +91,8 @@ def lib():
         L.kvq_decode_attention_gqa.restype = ctypes.c_int
         L.kvq_decode_attention_noalloc.argtypes = [cp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp]
         L.kvq_decode_attention_noalloc.restype = ctypes.c_int
+        L.kvq_prefill_attention.argtypes = [cp, vp, i32, vp, i64, i32, vp, i32, vp, i32, ctypes.c_float, vp, vp]
+        L.kvq_prefill_attention.restype = ctypes.c_int
         ap = ctypes.POINTER(kvq_step_args)
         L.kvq_step_graph_create.argtypes = [cp, ap, i32, ctypes.POINTER(vp)]
         L.kvq_step_graph_create.restype = ctypes.c_int
@@ -229,6 +231,26 @@ def kvq_decode_attention_noalloc(cache, q, block_table, seq_lens, softmax_scale,
                                               _ptr(out), _stream(stream, q.device)), "kvq_decode_attention_noalloc")
 
 
+def kvq_prefill_attention(cache, q, cu_seqlens_q, max_q_per_seq, block_table, seq_lens, softmax_scale, out,
+                          stream=None):
+    """out fp16 [total][Hq][128] = causal attention of the chunk queries q fp16
+    [total][Hq][128] over the cache: sequence b's chunk is its last
+    cu[b+1] - cu[b] tokens (already appended); query i sits at position
+    seq_lens[b] - n_b + i.  Hq = g * cache heads."""
+    _cuda(q, torch.float16, "q")
+    _cuda(out, torch.float16, "out")
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (block_table, "block_table"), (seq_lens, "seq_lens")):
+        _cuda(t, torch.int32, n)
+    B = seq_lens.numel()
+    if (out.shape != q.shape or q.dim() != 3 or cu_seqlens_q.numel() != B + 1 or block_table.dim() != 2 or
+            block_table.shape[0] != B):
+        raise ValueError("q/out/cu_seqlens_q/seq_lens/block_table shapes disagree")
+    _check(lib().kvq_prefill_attention(ctypes.byref(cache.struct), _ptr(q), q.shape[1], _ptr(cu_seqlens_q),
+                                       q.shape[0], int(max_q_per_seq), _ptr(block_table), block_table.shape[1],
+                                       _ptr(seq_lens), B, float(softmax_scale), _ptr(out),
+                                       _stream(stream, q.device)), "kvq_prefill_attention")
+
+
 class StepGraph:
     """kvq_step_graph_*: a sequence of decode steps -- each appends one chunk of
     new tokens per sequence, then runs decode attention over the grown
@@ -364,4 +386,4 @@ class PagedKVCache:
 __all__ = ["KVQ_INT4_B64", "KVQ_INT8_PAGE", "KVQ_FP8_E4M3", "HEAD_DIM", "PAGE_TOKENS", "EXPORTS", "KvqError", "kvq_cache",
            "PagedKVCache", "lib", "library_path", "kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes",
            "kvq_decode_attention", "kvq_decode_attention_noalloc", "kvq_get_device_status", "kvq_status_string",
-           "kvq_version", "StepGraph", "kvq_step_args"]
+           "kvq_version", "StepGraph", "kvq_step_args", "kvq_prefill_attention"]

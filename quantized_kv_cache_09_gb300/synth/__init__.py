@@ -22,6 +22,7 @@ from .. import build as _build
 K_HIST = 1
 V_HIST = 2
 QUERY = 3
+CHUNK_QUERY = 4  # queries of a prefill chunk, one stream per sequence
 K_OUTLIER = 16
 V_OUTLIER = 17
 BLOCK_TABLE = 32

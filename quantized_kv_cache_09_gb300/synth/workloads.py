@@ -19,12 +19,15 @@
                    than L2)
   llama2-7b-layer-fp8  as llama2-7b-layer, FP8 E4M3 codes (one byte per
                    element, 537 MB of K and V per step); decode
+  chunked-prefill  B=8, H=32, L=8192 of which the last 512 tokens are a new
+                   chunk (already appended), int4, K/V as llama2-7b-layer,
+                   chunk queries ~ N(0,1); causal attention of the chunk
 
 D = 128 and 64-token blocks throughout.  q ~ N(0, 1).  All values are fp16.
 """
 import numpy as np
 
-from . import (BLOCK_TABLE, K_HIST, K_OUTLIER, LENGTHS, QUERY, V_HIST, V_OUTLIER, fill_f16_device,
+from . import (BLOCK_TABLE, CHUNK_QUERY, K_HIST, K_OUTLIER, LENGTHS, QUERY, V_HIST, V_OUTLIER, fill_f16_device,
                fill_f16_host, outliers_bernoulli, outliers_per_head, permutation, stream_id,
                uniform_int)
 
@@ -50,6 +53,9 @@ CONFIGS = {
     # the FP8 E4M3 cache on the 7B-layer shape
     7: dict(name="llama2-7b-layer-fp8", B=8, H=32, D=128, L=8192, fmt=FP8, sigma=1.0,
             outliers=("per_head", 4, 10.0), table="contiguous"),
+    # chunked prefill: the last 512 of 8192 tokens attend causally over the cache
+    8: dict(name="chunked-prefill", B=8, H=32, D=128, L=8192, chunk=512, fmt=INT4, sigma=1.0,
+            outliers=("per_head", 4, 10.0), table="contiguous"),
 }
 
 
@@ -63,8 +69,9 @@ class Workload:
     """
 
     def __init__(self, B, H, D, lens, fmt, sigma=1.0, outliers=None, table="contiguous", seed=0,
-                 extra_tokens=0, name="custom", q_heads=None):
+                 extra_tokens=0, name="custom", q_heads=None, chunk=0):
         self.name = name
+        self.chunk = int(chunk)  # new tokens per sequence for chunked prefill (the last `chunk` of lens)
         self.B, self.H, self.D = int(B), int(H), int(D)
         self.Hq = self.H if q_heads is None else int(q_heads)  # query heads (a multiple of the cache heads H)
         self.lens = np.asarray(lens, dtype=np.int32).reshape(self.B)
@@ -130,6 +137,24 @@ class Workload:
         return fill_f16_device(out, self.seed, stream_id(kind, b), t0 * self.H * self.D, self.sigma,
                                self._mask_dev(which, out.device), self.outlier_mult)
 
+    def chunk_q_host(self, b, i0, i1):
+        """fp16 bits [i1-i0][Hq][D] of queries i0 .. i1-1 of sequence b's prefill chunk."""
+        n = (i1 - i0) * self.Hq * self.D
+        return fill_f16_host(n, self.seed, stream_id(CHUNK_QUERY, b), i0 * self.Hq * self.D,
+                             1.0).reshape(i1 - i0, self.Hq, self.D)
+
+    def chunk_q_device(self, out, b, i0=0):
+        """Fill out (fp16, [n][Hq][D]) with queries i0 .. i0+n-1 of sequence b's prefill chunk."""
+        return fill_f16_device(out, self.seed, stream_id(CHUNK_QUERY, b), i0 * self.Hq * self.D, 1.0)
+
+    def prefill_flops(self, chunk=None):
+        """Algorithmic flops of chunked-prefill attention: 4 D per (query head,
+        causal key) -- QK and PV, a multiply and an add each -- summed over the
+        last `chunk` queries of every sequence (query i sees L - n + i + 1 keys)."""
+        n = self.chunk if chunk is None else int(chunk)
+        keys = sum(int(L) * n - n * (n - 1) // 2 for L in self.lens)
+        return 4 * self.D * self.Hq * keys
+
     def q_device(self, out, step=0):
         assert out.numel() == self.B * self.Hq * self.D
         return fill_f16_device(out, self.seed, stream_id(QUERY, step), 0, 1.0)
@@ -168,4 +193,4 @@ def make_workload(cfg, seed=0, extra_tokens=0):
     else:
         lens = np.full(B, c["L"], dtype=np.int32)
     return Workload(B, c["H"], c["D"], lens, c["fmt"], c["sigma"], c["outliers"], c["table"], seed,
-                    extra_tokens, c["name"], c.get("Hq"))
+                    extra_tokens, c["name"], c.get("Hq"), c.get("chunk", 0))
