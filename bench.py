@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="llama2-7b-layer",
                     choices=["tiny", "llama2-7b-layer", "long-context", "paged-int8", "prefill-append",
-                             "llama3-8b-layer-gqa", "llama2-7b-layer-fp8"])
+                             "llama3-8b-layer-gqa", "llama2-7b-layer-fp8", "chunked-prefill"])
     ap.add_argument("--prefill-seqs", type=int, default=64)
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     return ap.parse_args()
@@ -89,6 +89,17 @@ def measured_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense fp16/bf16 tensor peak in TFLOP/s: the measured cuBLAS bf16 burst
+    figure (fp16 and bf16 have the same nominal rate), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; fp16 same nominal rate)"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 KERNEL_SOURCES = {
@@ -459,6 +470,88 @@ def measure_prefill(K, Wm, seed, dev, nseqs=64):
     return dict(ms=ms, bytes=nbytes, tokens=nseqs * L)
 
 
+def measure_chunked_prefill(K, Wm, seed, dev):
+    """chunked-prefill: kvq_prefill_attention of the last 512 of 8192 tokens of
+    8 sequences (H=32, int4) over the cache that holds them."""
+    import torch
+
+    from quantized_kv_cache_09_gb300 import kvq
+    from quantized_kv_cache_09_gb300.runner import DeviceWorkload
+    from quantized_kv_cache_09_gb300.synth import workloads as W
+
+    wl = W.make_workload(8, seed=seed)
+    dw = DeviceWorkload(wl, device=dev)
+    dw.prefill(max_tokens_per_call=1 << 16)
+    n = wl.chunk
+    q = torch.empty((wl.B * n, wl.Hq, wl.D), dtype=torch.float16, device=dev)
+    for b in range(wl.B):
+        wl.chunk_q_device(q[b * n:(b + 1) * n], b)
+    out = torch.empty_like(q)
+    cu = torch.arange(0, wl.B * n + 1, n, dtype=torch.int32, device=dev)
+    for _ in range(Wm):
+        kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.3)
+    t_wall0 = time.time()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        ev[i][0].record(stream)
+        kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.window = (t_wall0, time.time())
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    # end to end: the chunk's queries from pinned host memory, the output back
+    pin_q = q.cpu().pin_memory()
+    pin_o = torch.empty_like(pin_q).pin_memory()
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    Ke = max(1, K // 2)
+    e_s.record(stream)
+    for _ in range(Ke):
+        q.copy_(pin_q, non_blocking=True)
+        kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out)
+        pin_o.copy_(out, non_blocking=True)
+    e_e.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e_s.elapsed_time(e_e) / Ke
+    clocks.stop()
+    rc, flags = kvq.kvq_get_device_status(dw.cache)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} flags {flags:#x} in chunked-prefill")
+    res = dict(ms=ms, e2e_ms=e2e_ms, flops=wl.prefill_flops(), tokens=wl.B * n, B=wl.B, H=wl.H, Hq=wl.Hq, n=n,
+               L=int(wl.lens[0]), qbytes=q.numel() * 2, clocks=clocks.summary())
+    del dw, q, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def oracle_prefill_rate(seconds, seed):
+    """The oracle's chunked-prefill rate on a sample of the workload: queries of
+    sequence 0, every head, each over its causal prefix (binary64), one thread."""
+    import numpy as np
+
+    from oracle import oracle as orc
+    from quantized_kv_cache_09_gb300.synth import workloads as W
+
+    wl = W.make_workload(8, seed=seed)
+    L, n = int(wl.lens[0]), wl.chunk
+    kc, ks = orc.quantize(wl.fmt, wl.kv_host("k", 0, 0, L))
+    vc, vs = orc.quantize(wl.fmt, wl.kv_host("v", 0, 0, L))
+    bt = np.arange(kc.shape[0], dtype=np.int32)[None, :]
+    t0 = time.time()
+    done = 0
+    while time.time() - t0 < seconds and done < n:
+        i = n - 1 - done
+        orc.decode_attention(wl.fmt, kc, vc, ks, vs, bt, np.array([L - n + i + 1]),
+                             wl.chunk_q_host(0, i, i + 1), np.float32(1.0 / np.sqrt(wl.D)))
+        done += 1
+    el = time.time() - t0
+    return done / el, 1, f"{done} chunk queries of sequence 0 (all {wl.Hq} heads, causal prefixes of ~{L} tokens, binary64) in {el:.1f} s"
+
+
 def run_ours(args):
     import torch
 
@@ -489,6 +582,38 @@ def run_ours(args):
                              "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
                              "traffic": ncu_traffic("append_kernel", "prefill-append"), "algorithmic_bytes_per_launch": r["bytes"]},
                 "gpu_launches": K}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    if args.workload == "chunked-prefill":
+        r = measure_chunked_prefill(K, max(Wm, 1), seed, dev)
+        ms = max_over_ranks(pg, r["ms"], dev)
+        e2e_ms = max_over_ranks(pg, r["e2e_ms"], dev)
+        tflops = r["flops"] / (ms * 1e-3) / 1e12
+        tpeak, tkind = measured_tensor_peak()
+        line = {"metric": "chunked-prefill attention tokens/s over the quantized cache (tensor roofline)",
+                "value": whole_job_rate(world, r["tokens"], ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+                "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "int4 codes, fp16 MMA operands, fp32 accumulation",
+                "data": "synthetic (seeded generator in HBM)",
+                "config": {"workload": "chunked-prefill", "B": r["B"], "H": r["H"], "Hq": r["Hq"], "D": 128,
+                           "context": r["L"], "chunk": r["n"], "format": "int4-b64",
+                           "step": "one kvq_prefill_attention of every chunk query",
+                           "l2": "codes (268 MB) larger than L2"},
+                "tflops": tflops,
+                "roofline": {"kernel": "prefill_attn_kernel", "bound": "tensor", "achieved": tflops, "peak": tpeak,
+                             "peak_kind": tkind, "unit": "TFLOP/s", "frac": tflops / tpeak, "traffic": None,
+                             "algorithmic_flops_per_launch": r["flops"]},
+                "e2e": {"value": whole_job_rate(world, r["tokens"], e2e_ms * 1e-3), "unit": "tokens/s",
+                        "h2d_bytes_per_step": r["qbytes"], "d2h_bytes_per_step": r["qbytes"]},
+                "gpu_launches": K, "clocks": r["clocks"]}
+        if rank == 0 and not args.no_cpu_baseline:
+            rate, cores, desc = oracle_prefill_rate(args.cpu_seconds, args.seed)
+            line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                    "sample": desc}
         if rank == 0:
             print(json.dumps(line), flush=True)
         if pg:

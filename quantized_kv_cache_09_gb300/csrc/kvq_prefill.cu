@@ -45,9 +45,8 @@ template <int FMT>
 struct alignas(128) PfSmem {
     uint8_t kc[2][kPage * PfFmt<FMT>::kRowBytes];  // codes of one page, two stages
     uint8_t vc[2][kPage * PfFmt<FMT>::kRowBytes];
-    uint16_t k[kPage * kRowH];  // the current page, widened to fp16
+    uint16_t k[kPage * kRowH];  // the current page, widened to fp16 (first the query rows, see below)
     uint16_t v[kPage * kRowH];
-    uint16_t q[kPfRows * kRowH];
     float scale[2][2];  // (key, value) scale of the page in each stage
     uint64_t full[2];
 };
@@ -137,7 +136,7 @@ __device__ __forceinline__ void widen_page(const uint8_t *codes, uint16_t *dst, 
 
 // grid: x = 64-row query tile of a sequence, y = query head, z = sequence
 template <int FMT>
-__global__ void __launch_bounds__(kPfWarps * 32) prefill_attn_kernel(PrefillParams p)
+__global__ void __launch_bounds__(kPfWarps * 32, 3) prefill_attn_kernel(PrefillParams p)
 {
     using S = PfSmem<FMT>;
     constexpr int RB = PfFmt<FMT>::kRowBytes;
@@ -192,12 +191,15 @@ __global__ void __launch_bounds__(kPfWarps * 32) prefill_attn_kernel(PrefillPara
         if (ntiles > 1) issue(1, 1);
     }
 
-    // the query rows (zero past the chunk), fp16, pitch kRowH
+    // the query rows (zero past the chunk), fp16, pitch kRowH, staged in the
+    // K tile's space (kPfRows == kPage rows) until they are in registers
+    static_assert(kPfRows == kPage, "the query rows fit the K tile");
+    uint16_t *sq = sm.k;
     for (int e = tid; e < kPfRows * (kHeadDim / 8); e += kPfWarps * 32) {
         const int r = e >> 4, c = e & 15;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (r < rows) v = *reinterpret_cast<const uint4 *>(p.q + ((int64_t)(c0 + i0 + r) * Hq + hq) * kHeadDim + 8 * c);
-        *reinterpret_cast<uint4 *>(sm.q + r * kRowH + 8 * c) = v;
+        *reinterpret_cast<uint4 *>(sq + r * kRowH + 8 * c) = v;
     }
     __syncthreads();
 
@@ -205,10 +207,11 @@ __global__ void __launch_bounds__(kPfWarps * 32) prefill_attn_kernel(PrefillPara
     uint32_t qa[8][4];
     {
         const int i = lane >> 3, r = lane & 7;
-        const uint32_t base = smem_addr(sm.q + (16 * warp + r + 8 * (i & 1)) * kRowH + 8 * (i >> 1));
+        const uint32_t base = smem_addr(sq + (16 * warp + r + 8 * (i & 1)) * kRowH + 8 * (i >> 1));
 #pragma unroll
         for (int ks = 0; ks < 8; ks++) ldsm_x4(base + ks * 32, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
     }
+    __syncthreads();  // every warp holds its rows before the first page overwrites them
 
     float o[16][4];
 #pragma unroll
