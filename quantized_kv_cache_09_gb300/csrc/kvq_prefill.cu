@@ -339,6 +339,367 @@ __global__ void __launch_bounds__(kPfWarps * 32, 3) prefill_attn_kernel(PrefillP
     }
 }
 
+// ---------------------------------------------------------------------------
+// The same attention on the 5th-generation tensor cores (tcgen05): one CTA of
+// 4 warps owns 128 query rows; S (128 x 64 keys) and O (128 x 128) live in
+// tensor memory, the operands in shared memory in the K-major 128-byte
+// swizzled layout (8-row x 128-byte atoms, 16-byte chunks XOR-ed with the row).
+// One thread issues the MMAs; every thread owns one query row (its TMEM lane).
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kTcRows = 128;  // query rows per CTA (TMEM lanes)
+constexpr uint32_t kTmemCols = 256;  // S: columns 0..63, O: columns 128..255
+constexpr uint32_t kIdescS = (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);   // f32 += f16 x f16, 128 x 64, K-major
+constexpr uint32_t kIdescO = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);  // 128 x 128
+constexpr float kLazy = 8.0f;  // O is rescaled only when a row's max grows by more than 2^8
+
+// byte offset of f16 element (r, k) in a K-major, 128-byte-swizzled tile of R rows
+__device__ __forceinline__ uint32_t sw128(int r, int k, int R)
+{
+    return (uint32_t)((k >> 6) * (R * 128) + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4) + ((k & 7) << 1));
+}
+
+// shared-memory matrix descriptor: start address, 1024-byte stride between
+// 8-row groups, 128-byte swizzle (leading offset unused for K-major swizzled)
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+        "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+        "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+// 8 elements (one row of an 8 x 8 block, fp16 pairs) of 8 rows -> the block
+// transposed: x[j] = column j as 8 fp16 values
+__device__ __forceinline__ void transpose8(const uint4 (&w)[8], uint4 (&x)[8])
+{
+#pragma unroll
+    for (int m = 0; m < 4; m++) {  // columns 2m, 2m + 1
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int n = 0; n < 4; n++) {
+            const uint32_t a = (&w[2 * n].x)[m], b = (&w[2 * n + 1].x)[m];
+            lo[n] = __byte_perm(a, b, 0x5410);
+            hi[n] = __byte_perm(a, b, 0x7632);
+        }
+        x[2 * m] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        x[2 * m + 1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    }
+}
+
+// 8 codes of row `row` (elements 8c .. 8c + 7) as 8 fp16 values
+template <int FMT>
+__device__ __forceinline__ uint4 codes8(const uint8_t *page, int row, int c)
+{
+    if constexpr (FMT == KVQ_INT4_B64) {
+        return widen8_int4(*reinterpret_cast<const uint32_t *>(page + row * 64 + 4 * c));
+    } else {
+        const uint2 w = *reinterpret_cast<const uint2 *>(page + row * 128 + 8 * c);
+        __half2 a[2], b[2];
+        if constexpr (FMT == KVQ_FP8_E4M3) {
+            widen_e4m3(w.x, a);
+            widen_e4m3(w.y, b);
+        } else {
+            widen_int8(w.x, a);
+            widen_int8(w.y, b);
+        }
+        return make_uint4(h2_bits(a[0]), h2_bits(a[1]), h2_bits(b[0]), h2_bits(b[1]));
+    }
+}
+
+template <int FMT>
+struct alignas(1024) TcSmem {
+    uint8_t q[kTcRows * kHeadDim * 2];        // 32 KB: query rows x elements
+    uint8_t k[kPage * kHeadDim * 2];          // 16 KB: keys x elements
+    uint8_t vt[kHeadDim * kPage * 2];         // 16 KB: elements x keys (V transposed)
+    uint8_t p[kTcRows * kPage * 2];           // 16 KB: query rows x keys
+    uint8_t kc[2][kPage * PfFmt<FMT>::kRowBytes];  // codes of one page, two stages
+    uint8_t vc[2][kPage * PfFmt<FMT>::kRowBytes];
+    float scale[2][2];
+    float s_ref;
+    uint32_t tmem;
+    uint64_t full[2];
+    uint64_t mma;
+};
+
+}  // namespace
+
+template <int FMT>
+__global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(PrefillParams p)
+{
+    using S = TcSmem<FMT>;
+    constexpr int RB = PfFmt<FMT>::kRowBytes;
+    constexpr uint32_t kPageBytes = kPage * RB;
+    extern __shared__ __align__(1024) uint8_t smem_tc[];
+    // the swizzle pattern follows address bits: place the tiles on a 1024-byte boundary
+    S &sm = *reinterpret_cast<S *>(smem_tc + ((1024u - (smem_addr(smem_tc) & 1023u)) & 1023u));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int b = blockIdx.z, hq = blockIdx.y;
+    const int H = p.num_heads, Hq = p.num_q_heads;
+    const int h = hq / p.group;
+    const int i0 = blockIdx.x * kTcRows;
+
+    const int c0 = p.cu_q[b];
+    const int n = p.cu_q[b + 1] - c0;
+    const int L = p.seq_lens[b];
+    if (n < 0 || n > p.max_q || n > L || L > p.max_blocks * kPage || c0 < 0 || (int64_t)c0 + n > p.total_q) {
+        if (blockIdx.x == 0 && hq == 0 && tid == 0) set_flag(p.status, KVQ_FLAG_BAD_LENGTH);
+        return;
+    }
+    if (i0 >= n) return;
+    const int rows = min(kTcRows, n - i0);
+    const int qpos0 = L - n + i0;
+    const int ntiles = (qpos0 + rows - 1) / kPage + 1;
+    const int32_t *bt = p.block_table + (int64_t)b * p.max_blocks;
+
+    auto page_of = [&](int j) {
+        int pg = bt[j];
+        if (pg < 0 || pg >= p.num_pages) {
+            set_flag(p.status, KVQ_FLAG_BAD_PAGE);
+            pg = 0;
+        }
+        return pg;
+    };
+    auto issue = [&](int j, int s) {  // thread 0: page j's codes and scales into stage s
+        const int pg = page_of(j);
+        sm.scale[s][0] = p.k_scales[(int64_t)pg * H + h];
+        sm.scale[s][1] = p.v_scales[(int64_t)pg * H + h];
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&sm.full[s], 2 * kPageBytes);
+        const size_t off = ((size_t)pg * H + h) * kPageBytes;
+        bulk_copy_g2s(sm.kc[s], p.k_codes + off, kPageBytes, &sm.full[s]);
+        bulk_copy_g2s(sm.vc[s], p.v_codes + off, kPageBytes, &sm.full[s]);
+    };
+
+    if (tid == 0) {
+        mbar_init(&sm.full[0], 1);
+        mbar_init(&sm.full[1], 1);
+        mbar_init(&sm.mma, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        // the largest value scale over the CTA's pages: P carries sv / s_ref <= 1
+        float mx = 0.0f;
+        for (int j = tid; j < ntiles; j += 32) mx = fmaxf(mx, p.v_scales[(int64_t)page_of(j) * H + h]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        if (tid == 0) sm.s_ref = mx > 0.0f ? mx : 1.0f;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        issue(0, 0);
+        if (ntiles > 1) issue(1, 1);
+    }
+    // the query rows (zero past the chunk) in the swizzled layout
+    for (int e = tid; e < kTcRows * (kHeadDim / 8); e += kPfWarps * 32) {
+        const int r = e >> 4, c = e & 15;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows) v = *reinterpret_cast<const uint4 *>(p.q + ((int64_t)(c0 + i0 + r) * Hq + hq) * kHeadDim + 8 * c);
+        *reinterpret_cast<uint4 *>(sm.q + sw128(r, 8 * c, kTcRows)) = v;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+    const uint32_t lane_tm = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
+    const float s_ref = sm.s_ref;
+    const uint32_t aq = smem_addr(sm.q), ak = smem_addr(sm.k), av = smem_addr(sm.vt), ap = smem_addr(sm.p);
+
+    const int row = tid;  // this thread's query row and TMEM lane
+    const int qpos = qpos0 + row;
+    float m_used = -INFINITY, l_run = 0.0f;
+    uint32_t mma_phase = 0;
+    int failed_at = -1;  // the tile whose codes never arrived
+
+    for (int j = 0; j < ntiles; j++) {
+        const int s = j & 1;
+        const bool ok = mbar_wait_bounded(&sm.full[s], (uint32_t)((j >> 1) & 1));
+        if (__syncthreads_and(ok) == 0) {
+            failed_at = j;
+            break;
+        }
+        const float sk = sm.scale[s][0] * p.score_scale, pv_scale = sm.scale[s][1] / s_ref;
+        // widen: K rows -> k (keys x elements); V -> vt (elements x keys), 8 x 8 blocks transposed
+#pragma unroll
+        for (int r = 0; r < (kPage * 16) / (kPfWarps * 32); r++) {
+            const int e = tid + kPfWarps * 32 * r;
+            const int key = e >> 4, c = e & 15;
+            *reinterpret_cast<uint4 *>(sm.k + sw128(key, 8 * c, kPage)) = codes8<FMT>(sm.kc[s], key, c);
+        }
+        {
+            const int kb = tid & 7, dc = tid >> 3;  // keys 8 kb .. +7, elements 8 dc .. +7
+            uint4 w[8], x[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) w[i] = codes8<FMT>(sm.vc[s], 8 * kb + i, dc);
+            transpose8(w, x);
+#pragma unroll
+            for (int i = 0; i < 8; i++) *reinterpret_cast<uint4 *>(sm.vt + sw128(8 * dc + i, 8 * kb, kHeadDim)) = x[i];
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();  // operands ready; stage s consumed
+        if (tid == 0) {
+            tc_fence_after();
+            if (j + 2 < ntiles) issue(j + 2, s);
+#pragma unroll
+            for (int ks = 0; ks < 8; ks++)
+                umma_f16(tmem, umma_desc(aq + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32),
+                         umma_desc(ak + (ks >> 2) * (kPage * 128) + (ks & 3) * 32), kIdescS, ks > 0);
+            umma_commit(&sm.mma);
+        }
+        if (!mbar_wait_bounded(&sm.mma, mma_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
+        mma_phase ^= 1u;
+        tc_fence_after();
+        // this row's 64 scores: scale, causal mask, lazy online softmax (base 2)
+        float sc[64];
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            float v[16];
+            tmem_ld16(lane_tm + 16 * c, v);
+#pragma unroll
+            for (int i = 0; i < 16; i++) sc[16 * c + i] = v[i] * sk;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; i++) {
+            if (j * kPage + i > qpos) sc[i] = -INFINITY;
+            mx = fmaxf(mx, sc[i]);
+        }
+        float factor = 1.0f;
+        if (j == 0) {
+            m_used = mx;  // key 0 is never masked
+        } else if (mx > m_used + kLazy) {
+            factor = ex2_approx(m_used - mx);
+            m_used = mx;
+        }
+        if (__any_sync(kFull, factor != 1.0f)) {  // rescale O (TMEM columns 128..255) of the rows that moved
+#pragma unroll
+            for (int c = 0; c < 8; c++) {
+                float v[16];
+                tmem_ld16(lane_tm + 128 + 16 * c, v);
+#pragma unroll
+                for (int i = 0; i < 16; i++) v[i] *= factor;
+                tmem_st16(lane_tm + 128 + 16 * c, v);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        l_run *= factor;
+#pragma unroll
+        for (int c = 0; c < 8; c++) {  // P row -> p (query rows x keys), 8 keys per 16-byte chunk
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const float p0 = ex2_approx(sc[8 * c + 2 * i] - m_used);
+                const float p1 = ex2_approx(sc[8 * c + 2 * i + 1] - m_used);
+                l_run += p0 + p1;
+                w[i] = f16x2_rn(p0 * pv_scale, p1 * pv_scale);
+            }
+            *reinterpret_cast<uint4 *>(sm.p + sw128(row, 8 * c, kTcRows)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();  // P ready, S read, O rescaled
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ks++)
+                umma_f16(tmem + 128, umma_desc(ap + ks * 32), umma_desc(av + ks * 32), kIdescO, (j > 0 || ks > 0));
+            umma_commit(&sm.mma);
+        }
+        if (!mbar_wait_bounded(&sm.mma, mma_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
+        mma_phase ^= 1u;
+        tc_fence_after();
+    }
+
+    if (failed_at >= 0) {  // flag, and let the other stage's copy land before the CTA exits
+        if (tid == 0) {
+            set_flag(p.status, KVQ_FLAG_TIMEOUT);
+            const int j = failed_at + 1;
+            if (j < ntiles) mbar_wait_bounded(&sm.full[j & 1], (uint32_t)((j >> 1) & 1));
+        }
+    } else {  // out = s_ref * O / l; the TMEM loads are warp-wide, the stores only for rows of the chunk
+        const float inv = s_ref / l_run;
+        uint16_t *dst = p.out + ((int64_t)(c0 + i0 + row) * Hq + hq) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+            float v[16];
+            tmem_ld16(lane_tm + 128 + 16 * c, v);
+            if (row >= rows) continue;
+            uint4 o0, o1;
+            o0.x = f16x2_rn(v[0] * inv, v[1] * inv);
+            o0.y = f16x2_rn(v[2] * inv, v[3] * inv);
+            o0.z = f16x2_rn(v[4] * inv, v[5] * inv);
+            o0.w = f16x2_rn(v[6] * inv, v[7] * inv);
+            o1.x = f16x2_rn(v[8] * inv, v[9] * inv);
+            o1.y = f16x2_rn(v[10] * inv, v[11] * inv);
+            o1.z = f16x2_rn(v[12] * inv, v[13] * inv);
+            o1.w = f16x2_rn(v[14] * inv, v[15] * inv);
+            reinterpret_cast<uint4 *>(dst + 16 * c)[0] = o0;
+            reinterpret_cast<uint4 *>(dst + 16 * c)[1] = o1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+template <int FMT>
+static cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s)
+{
+    const size_t smem = sizeof(TcSmem<FMT>) + 1024;  // + room to align the tiles to 1024 bytes
+    cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((p.max_q + kTcRows - 1) / kTcRows), (unsigned)p.num_q_heads, (unsigned)p.num_seqs);
+    return launch_plain(prefill_attn_tc_kernel<FMT>, grid, dim3(kPfWarps * 32), smem, s, p);
+}
+
 template <int FMT>
 static cudaError_t launch_prefill_fmt(const PrefillParams &p, cudaStream_t s)
 {
@@ -354,9 +715,9 @@ cudaError_t launch_prefill(int fmt, const PrefillParams &p, cudaStream_t s)
 {
     if (p.num_seqs == 0 || p.max_q == 0) return cudaSuccess;
     if (p.num_seqs > 65535 || p.num_q_heads > 65535) return cudaErrorInvalidValue;
-    if (fmt == KVQ_INT4_B64) return launch_prefill_fmt<KVQ_INT4_B64>(p, s);
-    if (fmt == KVQ_FP8_E4M3) return launch_prefill_fmt<KVQ_FP8_E4M3>(p, s);
-    return launch_prefill_fmt<KVQ_INT8_PAGE>(p, s);
+    if (fmt == KVQ_INT4_B64) return launch_prefill_tc<KVQ_INT4_B64>(p, s);
+    if (fmt == KVQ_FP8_E4M3) return launch_prefill_tc<KVQ_FP8_E4M3>(p, s);
+    return launch_prefill_tc<KVQ_INT8_PAGE>(p, s);
 }
 
 }  // namespace kvq
