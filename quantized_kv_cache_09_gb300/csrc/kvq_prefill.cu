@@ -385,16 +385,25 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 16 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+// start loading 16 consecutive fp32 columns of this thread's TMEM lane (raw bits;
+// valid after tmem_ld_wait)
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16])
 {
-    uint32_t r[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    tmem_ld16_async(taddr, r);
+    tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
@@ -454,19 +463,25 @@ template <int FMT>
 struct alignas(1024) TcSmem {
     uint8_t q[kTcRows * kHeadDim * 2];        // 32 KB: query rows x elements
     uint8_t k[kPage * kHeadDim * 2];          // 16 KB: keys x elements
-    uint8_t vt[kHeadDim * kPage * 2];         // 16 KB: elements x keys (V transposed)
+    uint8_t vt[2][kHeadDim * kPage * 2];      // 2 x 16 KB: elements x keys (V transposed), two pages
     uint8_t p[kTcRows * kPage * 2];           // 16 KB: query rows x keys
-    uint8_t kc[2][kPage * PfFmt<FMT>::kRowBytes];  // codes of one page, two stages
-    uint8_t vc[2][kPage * PfFmt<FMT>::kRowBytes];
-    float scale[2][2];
+    uint8_t kc[kPage * PfFmt<FMT>::kRowBytes];  // codes of the next page
+    uint8_t vc[kPage * PfFmt<FMT>::kRowBytes];
+    float scale[2];
     float s_ref;
     uint32_t tmem;
-    uint64_t full[2];
-    uint64_t mma;
+    uint64_t full;   // codes landed
+    uint64_t s_done;  // S = Q K^T of a page complete
+    uint64_t o_done;  // O += P V of a page complete
 };
 
 }  // namespace
 
+// Per page j (S of page j already issued):
+//   wait S(j), load it; widen page j + 1 (after PV(j - 1) released its V
+//   buffer and P) and issue S(j + 1) into the other S buffer -- the tensor
+//   cores run it during the softmax of page j; softmax(j), lazy O rescale,
+//   P(j); issue PV(j), which runs during the next page's widening.
 template <int FMT>
 __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(PrefillParams p)
 {
@@ -503,21 +518,39 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
         }
         return pg;
     };
-    auto issue = [&](int j, int s) {  // thread 0: page j's codes and scales into stage s
+    auto issue = [&](int j) {  // thread 0: page j's codes and scales
         const int pg = page_of(j);
-        sm.scale[s][0] = p.k_scales[(int64_t)pg * H + h];
-        sm.scale[s][1] = p.v_scales[(int64_t)pg * H + h];
+        sm.scale[0] = p.k_scales[(int64_t)pg * H + h];
+        sm.scale[1] = p.v_scales[(int64_t)pg * H + h];
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&sm.full[s], 2 * kPageBytes);
+        mbar_arrive_expect_tx(&sm.full, 2 * kPageBytes);
         const size_t off = ((size_t)pg * H + h) * kPageBytes;
-        bulk_copy_g2s(sm.kc[s], p.k_codes + off, kPageBytes, &sm.full[s]);
-        bulk_copy_g2s(sm.vc[s], p.v_codes + off, kPageBytes, &sm.full[s]);
+        bulk_copy_g2s(sm.kc, p.k_codes + off, kPageBytes, &sm.full);
+        bulk_copy_g2s(sm.vc, p.v_codes + off, kPageBytes, &sm.full);
+    };
+    // all threads: page j's codes -> k (keys x elements) and vt[j & 1] (elements x keys)
+    auto widen = [&](int j) {
+#pragma unroll
+        for (int r = 0; r < (kPage * 16) / (kPfWarps * 32); r++) {
+            const int e = tid + kPfWarps * 32 * r;
+            const int key = e >> 4, c = e & 15;
+            *reinterpret_cast<uint4 *>(sm.k + sw128(key, 8 * c, kPage)) = codes8<FMT>(sm.kc, key, c);
+        }
+        // keys 8 kb .. +7, elements 8 dc .. +7; 8 lanes with consecutive kb store 8 different 16-byte chunks
+        const int kb = tid & 7, dc = tid >> 3;
+        uint4 w[8], x[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) w[i] = codes8<FMT>(sm.vc, 8 * kb + i, dc);
+        transpose8(w, x);
+        uint8_t *vt = sm.vt[j & 1];
+#pragma unroll
+        for (int i = 0; i < 8; i++) *reinterpret_cast<uint4 *>(vt + sw128(8 * dc + i, 8 * kb, kHeadDim)) = x[i];
     };
 
     if (tid == 0) {
-        mbar_init(&sm.full[0], 1);
-        mbar_init(&sm.full[1], 1);
-        mbar_init(&sm.mma, 1);
+        mbar_init(&sm.full, 1);
+        mbar_init(&sm.s_done, 1);
+        mbar_init(&sm.o_done, 1);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -532,10 +565,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
         if (tid == 0) sm.s_ref = mx > 0.0f ? mx : 1.0f;
     }
     __syncthreads();
-    if (tid == 0) {
-        issue(0, 0);
-        if (ntiles > 1) issue(1, 1);
-    }
+    if (tid == 0) issue(0);
     // the query rows (zero past the chunk) in the swizzled layout
     for (int e = tid; e < kTcRows * (kHeadDim / 8); e += kPfWarps * 32) {
         const int r = e >> 4, c = e & 15;
@@ -543,68 +573,86 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
         if (r < rows) v = *reinterpret_cast<const uint4 *>(p.q + ((int64_t)(c0 + i0 + r) * Hq + hq) * kHeadDim + 8 * c);
         *reinterpret_cast<uint4 *>(sm.q + sw128(r, 8 * c, kTcRows)) = v;
     }
+    const uint32_t aq = smem_addr(sm.q), ak = smem_addr(sm.k), ap = smem_addr(sm.p);
+    const uint32_t av0 = smem_addr(sm.vt[0]), av1 = smem_addr(sm.vt[1]);
+    auto issue_s = [&](uint32_t tmem, int j) {  // thread 0: S(j) = Q K^T into S buffer j & 1
+#pragma unroll
+        for (int ks = 0; ks < 8; ks++)
+            umma_f16(tmem + 64 * (j & 1), umma_desc(aq + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32),
+                     umma_desc(ak + (ks >> 2) * (kPage * 128) + (ks & 3) * 32), kIdescS, ks > 0);
+        umma_commit(&sm.s_done);
+    };
+
+    // page 0: codes, widen, S(0)
+    bool ok = mbar_wait_bounded(&sm.full, 0u);
+    bool failed = __syncthreads_and(ok) == 0;
+    float cur_sk = 0.0f, cur_sv = 0.0f;
+    if (!failed) {
+        widen(0);
+        cur_sk = sm.scale[0] * p.score_scale;
+        cur_sv = sm.scale[1];
+    }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
     const uint32_t lane_tm = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
     const float s_ref = sm.s_ref;
-    const uint32_t aq = smem_addr(sm.q), ak = smem_addr(sm.k), av = smem_addr(sm.vt), ap = smem_addr(sm.p);
+    if (tid == 0 && !failed) {  // the MMA first: the copy's block-table and scale loads take a while
+        issue_s(tmem, 0);
+        if (ntiles > 1) issue(1);
+    }
 
     const int row = tid;  // this thread's query row and TMEM lane
     const int qpos = qpos0 + row;
     float m_used = -INFINITY, l_run = 0.0f;
-    uint32_t mma_phase = 0;
-    int failed_at = -1;  // the tile whose codes never arrived
+    uint32_t s_phase = 0, o_phase = 0;
+    int o_pending = 0;  // PV launches not yet waited for (0 or 1)
 
-    for (int j = 0; j < ntiles; j++) {
-        const int s = j & 1;
-        const bool ok = mbar_wait_bounded(&sm.full[s], (uint32_t)((j >> 1) & 1));
-        if (__syncthreads_and(ok) == 0) {
-            failed_at = j;
-            break;
-        }
-        const float sk = sm.scale[s][0] * p.score_scale, pv_scale = sm.scale[s][1] / s_ref;
-        // widen: K rows -> k (keys x elements); V -> vt (elements x keys), 8 x 8 blocks transposed
-#pragma unroll
-        for (int r = 0; r < (kPage * 16) / (kPfWarps * 32); r++) {
-            const int e = tid + kPfWarps * 32 * r;
-            const int key = e >> 4, c = e & 15;
-            *reinterpret_cast<uint4 *>(sm.k + sw128(key, 8 * c, kPage)) = codes8<FMT>(sm.kc[s], key, c);
-        }
-        {
-            const int kb = tid & 7, dc = tid >> 3;  // keys 8 kb .. +7, elements 8 dc .. +7
-            uint4 w[8], x[8];
-#pragma unroll
-            for (int i = 0; i < 8; i++) w[i] = codes8<FMT>(sm.vc[s], 8 * kb + i, dc);
-            transpose8(w, x);
-#pragma unroll
-            for (int i = 0; i < 8; i++) *reinterpret_cast<uint4 *>(sm.vt + sw128(8 * dc + i, 8 * kb, kHeadDim)) = x[i];
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();  // operands ready; stage s consumed
-        if (tid == 0) {
-            tc_fence_after();
-            if (j + 2 < ntiles) issue(j + 2, s);
-#pragma unroll
-            for (int ks = 0; ks < 8; ks++)
-                umma_f16(tmem, umma_desc(aq + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32),
-                         umma_desc(ak + (ks >> 2) * (kPage * 128) + (ks & 3) * 32), kIdescS, ks > 0);
-            umma_commit(&sm.mma);
-        }
-        if (!mbar_wait_bounded(&sm.mma, mma_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
-        mma_phase ^= 1u;
+    for (int j = 0; j < ntiles && !failed; j++) {
+        // 1. this page's scores
+        if (!mbar_wait_bounded(&sm.s_done, s_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
+        s_phase ^= 1u;
         tc_fence_after();
-        // this row's 64 scores: scale, causal mask, lazy online softmax (base 2)
         float sc[64];
+        {
+            uint32_t r[4][16];
 #pragma unroll
-        for (int c = 0; c < 4; c++) {
-            float v[16];
-            tmem_ld16(lane_tm + 16 * c, v);
+            for (int c = 0; c < 4; c++) tmem_ld16_async(lane_tm + 64 * (j & 1) + 16 * c, r[c]);
+            tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; i++) sc[16 * c + i] = v[i] * sk;
+            for (int c = 0; c < 4; c++)
+#pragma unroll
+                for (int i = 0; i < 16; i++) sc[16 * c + i] = __uint_as_float(r[c][i]) * cur_sk;
         }
+        // 2. PV(j - 1) must be done before its V buffer, P and O are touched again
+        if (o_pending) {
+            if (!mbar_wait_bounded(&sm.o_done, o_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
+            o_phase ^= 1u;
+            o_pending = 0;
+            tc_fence_after();
+        }
+        float nxt_sk = cur_sk, nxt_sv = cur_sv;
+        if (j + 1 < ntiles) {  // the next page: codes, widen, and its S on the tensor cores
+            ok = mbar_wait_bounded(&sm.full, (uint32_t)((j + 1) & 1));
+            if (__syncthreads_and(ok) == 0) {
+                failed = true;
+                break;
+            }
+            widen(j + 1);
+            nxt_sk = sm.scale[0] * p.score_scale;
+            nxt_sv = sm.scale[1];
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();  // page j + 1's operands ready; its codes consumed
+            if (tid == 0) {
+                tc_fence_after();
+                issue_s(tmem, j + 1);
+                if (j + 2 < ntiles) issue(j + 2);
+            }
+        }
+        // 3. causal mask, lazy online softmax (base 2), O rescale
         float mx = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 64; i++) {
@@ -618,7 +666,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
             factor = ex2_approx(m_used - mx);
             m_used = mx;
         }
-        if (__any_sync(kFull, factor != 1.0f)) {  // rescale O (TMEM columns 128..255) of the rows that moved
+        if (__any_sync(kFull, factor != 1.0f)) {  // O (TMEM columns 128..255) of the rows whose max moved
 #pragma unroll
             for (int c = 0; c < 8; c++) {
                 float v[16];
@@ -630,6 +678,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
         l_run *= factor;
+        const float pv_scale = cur_sv / s_ref;
 #pragma unroll
         for (int c = 0; c < 8; c++) {  // P row -> p (query rows x keys), 8 keys per 16-byte chunk
             uint32_t w[4];
@@ -644,25 +693,26 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();  // P ready, S read, O rescaled
-        if (tid == 0) {
+        __syncthreads();  // P(j) ready, O rescaled
+        if (tid == 0) {  // 4. O += P(j) V(j)
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ks++)
-                umma_f16(tmem + 128, umma_desc(ap + ks * 32), umma_desc(av + ks * 32), kIdescO, (j > 0 || ks > 0));
-            umma_commit(&sm.mma);
+                umma_f16(tmem + 128, umma_desc(ap + ks * 32), umma_desc(((j & 1) ? av1 : av0) + ks * 32), kIdescO,
+                         (j > 0 || ks > 0));
+            umma_commit(&sm.o_done);
         }
-        if (!mbar_wait_bounded(&sm.mma, mma_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
-        mma_phase ^= 1u;
+        o_pending = 1;
+        cur_sk = nxt_sk;
+        cur_sv = nxt_sv;
+    }
+    if (o_pending) {
+        if (!mbar_wait_bounded(&sm.o_done, o_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
         tc_fence_after();
     }
 
-    if (failed_at >= 0) {  // flag, and let the other stage's copy land before the CTA exits
-        if (tid == 0) {
-            set_flag(p.status, KVQ_FLAG_TIMEOUT);
-            const int j = failed_at + 1;
-            if (j < ntiles) mbar_wait_bounded(&sm.full[j & 1], (uint32_t)((j >> 1) & 1));
-        }
+    if (failed) {  // codes never landed: flag (nothing else is in flight: each copy is waited for before the next)
+        if (tid == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
     } else {  // out = s_ref * O / l; the TMEM loads are warp-wide, the stores only for rows of the chunk
         const float inv = s_ref / l_run;
         uint16_t *dst = p.out + ((int64_t)(c0 + i0 + row) * Hq + hq) * kHeadDim;
