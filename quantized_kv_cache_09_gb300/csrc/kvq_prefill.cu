@@ -5,22 +5,28 @@
 // the cache and its pages as for decode: quantize_block, jsqmd.com/news/887038
 // section 2.1, and PagedAttention, ddd.cn section 4).
 //
-// One CTA of 4 warps owns 64 query rows of one (sequence, query head); query
-// head hq reads cache head hq / g.  Per 64-token page (one key tile):
+// On the 5th-generation tensor cores (tcgen05).  One CTA of 4 warps owns 128
+// query rows of one (sequence, query head); query head hq reads cache head
+// hq / g; every thread owns one query row, which is also its lane of tensor
+// memory.  Per 64-token page (one key tile):
 //   1. the page's K and V codes of the cache head arrive in shared memory by
-//      two bulk copies (double-buffered, completing on an mbarrier);
-//   2. the whole CTA widens them once to fp16 codes (exact: integers or E4M3
-//      values), the scales stay out of the fp16 operands;
-//   3. each warp (16 query rows) computes S = Q K^T on the tensor cores
-//      (mma.sync m16n8k16, operands by ldmatrix), scales it by the page's key
-//      scale, masks keys after each query's position on the diagonal tiles,
-//      and runs an online softmax in base 2;
-//   4. P (in [0, 1]) rounded to fp16 is the A operand of O += P V (V by
-//      ldmatrix.trans) -- the accumulator layout of S is the operand layout of
-//      P, so P never leaves registers.  O is kept in units of a running value
-//      scale: before a page with value scale sv it is multiplied by
-//      (previous scale / sv), so P never carries the scale into fp16.
-// fp32 accumulation throughout; the output is scale * O / l rounded to fp16.
+//      two bulk copies completing on an mbarrier;
+//   2. the CTA widens them once to fp16 codes (exact: integers or E4M3
+//      values) in the K-major 128-byte-swizzled layout the MMA reads -- K as
+//      keys x elements, V transposed (elements x keys), so every operand is
+//      K-major; the scales stay out of the fp16 operands;
+//   3. one thread issues S = Q K^T (M = 128, N = 64, 8 MMAs of K = 16) into
+//      one of two S buffers in tensor memory; the next page's S runs on the
+//      tensor cores while the threads work on this page's;
+//   4. each thread loads its row of S, scales it by the page's key scale,
+//      masks keys after its position, and runs an online softmax in base 2
+//      with a lazy running maximum (O is rescaled, in tensor memory, only
+//      when a row's maximum grows by more than 2^8);
+//   5. P * sv / s_ref (s_ref = the largest value scale over the CTA's pages,
+//      so the fp16 operand stays in [0, 256]) goes to shared memory and one
+//      thread issues O += P V (M = 128, N = 128, 4 MMAs of K = 16) into
+//      tensor memory.
+// fp32 accumulation throughout; the output is s_ref * O / l rounded to fp16.
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -29,8 +35,6 @@ namespace kvq {
 namespace {
 
 constexpr int kPfWarps = 4;
-constexpr int kPfRows = 16 * kPfWarps;  // query rows per CTA
-constexpr int kRowH = kHeadDim + 8;     // fp16 row pitch in shared memory: rows 16 bytes apart mod 128
 
 template <int FMT>
 struct PfFmt {
@@ -40,30 +44,6 @@ template <>
 struct PfFmt<KVQ_INT4_B64> {
     static constexpr int kRowBytes = 64;
 };
-
-template <int FMT>
-struct alignas(128) PfSmem {
-    uint8_t kc[2][kPage * PfFmt<FMT>::kRowBytes];  // codes of one page, two stages
-    uint8_t vc[2][kPage * PfFmt<FMT>::kRowBytes];
-    uint16_t k[kPage * kRowH];  // the current page, widened to fp16 (first the query rows, see below)
-    uint16_t v[kPage * kRowH];
-    float scale[2][2];  // (key, value) scale of the page in each stage
-    uint64_t full[2];
-};
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
 
 // 8 int4 codes (one word: element 2j in the low nibble of byte j, 4-bit two's
 // complement) -> 8 fp16 values in element order: biased bytes u ^ 8 = c + 8,
@@ -83,261 +63,7 @@ __device__ __forceinline__ uint4 widen8_int4(uint32_t w)
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// 16 one-byte codes -> 16 fp16 values
-template <int FMT>
-__device__ __forceinline__ void widen16_bytes(const uint4 &w, uint4 &a, uint4 &b)
-{
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    uint32_t r[8];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        __half2 c[2];
-        if constexpr (FMT == KVQ_FP8_E4M3)
-            widen_e4m3(ws[i], c);
-        else
-            widen_int8(ws[i], c);
-        r[2 * i] = h2_bits(c[0]);
-        r[2 * i + 1] = h2_bits(c[1]);
-    }
-    a = make_uint4(r[0], r[1], r[2], r[3]);
-    b = make_uint4(r[4], r[5], r[6], r[7]);
-}
-
-// widen one page of codes (64 rows) into fp16 rows of pitch kRowH; all 128 threads
-template <int FMT>
-__device__ __forceinline__ void widen_page(const uint8_t *codes, uint16_t *dst, int tid)
-{
-    if constexpr (FMT == KVQ_INT4_B64) {
-        // 64 rows x 16 words; thread: words tid + 128 r
-#pragma unroll
-        for (int r = 0; r < 8; r++) {
-            const int w = tid + kPfWarps * 32 * r;
-            const int row = w >> 4, c = w & 15;
-            const uint32_t word = reinterpret_cast<const uint32_t *>(codes)[w];
-            *reinterpret_cast<uint4 *>(dst + row * kRowH + 8 * c) = widen8_int4(word);
-        }
-    } else {
-        // 64 rows x 8 chunks of 16 bytes; thread: chunks tid + 128 r
-#pragma unroll
-        for (int r = 0; r < 4; r++) {
-            const int ch = tid + kPfWarps * 32 * r;
-            const int row = ch >> 3, c = ch & 7;
-            const uint4 w = reinterpret_cast<const uint4 *>(codes)[ch];
-            uint4 a, b;
-            widen16_bytes<FMT>(w, a, b);
-            uint4 *d = reinterpret_cast<uint4 *>(dst + row * kRowH + 16 * c);
-            d[0] = a;
-            d[1] = b;
-        }
-    }
-}
-
 }  // namespace
-
-// grid: x = 64-row query tile of a sequence, y = query head, z = sequence
-template <int FMT>
-__global__ void __launch_bounds__(kPfWarps * 32, 3) prefill_attn_kernel(PrefillParams p)
-{
-    using S = PfSmem<FMT>;
-    constexpr int RB = PfFmt<FMT>::kRowBytes;
-    constexpr uint32_t kPageBytes = kPage * RB;
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    S &sm = *reinterpret_cast<S *>(smem_raw);
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const int b = blockIdx.z, hq = blockIdx.y;
-    const int H = p.num_heads, Hq = p.num_q_heads;
-    const int h = hq / p.group;
-    const int i0 = blockIdx.x * kPfRows;
-
-    const int c0 = p.cu_q[b];
-    const int n = p.cu_q[b + 1] - c0;
-    const int L = p.seq_lens[b];
-    if (n < 0 || n > p.max_q || n > L || L > p.max_blocks * kPage || c0 < 0 || (int64_t)c0 + n > p.total_q) {
-        if (blockIdx.x == 0 && hq == 0 && tid == 0) set_flag(p.status, KVQ_FLAG_BAD_LENGTH);
-        return;
-    }
-    if (i0 >= n) return;
-    const int rows = min(kPfRows, n - i0);        // valid query rows of this CTA
-    const int qpos0 = L - n + i0;                 // position of the CTA's first query row
-    const int ntiles = (qpos0 + rows - 1) / kPage + 1;
-    const int32_t *bt = p.block_table + (int64_t)b * p.max_blocks;
-
-    if (tid == 0) {
-        mbar_init(&sm.full[0], 1);
-        mbar_init(&sm.full[1], 1);
-        mbar_init_fence();
-    }
-    __syncthreads();
-
-    // thread 0: fill stage s with page j's K and V codes and record its scales
-    auto issue = [&](int j, int s) {
-        int pg = bt[j];
-        if (pg < 0 || pg >= p.num_pages) {
-            set_flag(p.status, KVQ_FLAG_BAD_PAGE);
-            pg = 0;
-        }
-        sm.scale[s][0] = p.k_scales[(int64_t)pg * H + h];
-        sm.scale[s][1] = p.v_scales[(int64_t)pg * H + h];
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&sm.full[s], 2 * kPageBytes);
-        const size_t off = ((size_t)pg * H + h) * kPageBytes;
-        bulk_copy_g2s(sm.kc[s], p.k_codes + off, kPageBytes, &sm.full[s]);
-        bulk_copy_g2s(sm.vc[s], p.v_codes + off, kPageBytes, &sm.full[s]);
-    };
-    if (tid == 0) {
-        issue(0, 0);
-        if (ntiles > 1) issue(1, 1);
-    }
-
-    // the query rows (zero past the chunk), fp16, pitch kRowH, staged in the
-    // K tile's space (kPfRows == kPage rows) until they are in registers
-    static_assert(kPfRows == kPage, "the query rows fit the K tile");
-    uint16_t *sq = sm.k;
-    for (int e = tid; e < kPfRows * (kHeadDim / 8); e += kPfWarps * 32) {
-        const int r = e >> 4, c = e & 15;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < rows) v = *reinterpret_cast<const uint4 *>(p.q + ((int64_t)(c0 + i0 + r) * Hq + hq) * kHeadDim + 8 * c);
-        *reinterpret_cast<uint4 *>(sq + r * kRowH + 8 * c) = v;
-    }
-    __syncthreads();
-
-    // this warp's Q fragments: 8 k-steps of 16 elements
-    uint32_t qa[8][4];
-    {
-        const int i = lane >> 3, r = lane & 7;
-        const uint32_t base = smem_addr(sq + (16 * warp + r + 8 * (i & 1)) * kRowH + 8 * (i >> 1));
-#pragma unroll
-        for (int ks = 0; ks < 8; ks++) ldsm_x4(base + ks * 32, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-    }
-    __syncthreads();  // every warp holds its rows before the first page overwrites them
-
-    float o[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-    float m_run[2] = {-INFINITY, -INFINITY};  // rows g and g + 8 (base-2 scores)
-    float l_run[2] = {0.0f, 0.0f};            // this lane's part of the row sums
-    float s_run = 1.0f;                       // O holds the numerator in units of s_run
-    const int qp_lo = qpos0 + 16 * warp + g;  // positions of this lane's two rows
-    const int qp_hi = qp_lo + 8;
-
-    // ldmatrix lane addresses: K (non-transposed) and V (transposed)
-    const int li = lane >> 3, lr = lane & 7;
-    const uint32_t k_base = smem_addr(sm.k + (8 * (li >> 1) + lr) * kRowH + 8 * (li & 1));
-    const uint32_t v_base = smem_addr(sm.v + (8 * (li & 1) + lr) * kRowH + 8 * (li >> 1));
-
-    for (int j = 0; j < ntiles; j++) {
-        const int s = j & 1;
-        bool ok = mbar_wait_bounded(&sm.full[s], (uint32_t)((j >> 1) & 1));
-        if (__syncthreads_and(ok) == 0) {  // a copy never landed: flag, let the other stage land, stop
-            if (tid == 0) {
-                set_flag(p.status, KVQ_FLAG_TIMEOUT);
-                if (j + 1 < ntiles) mbar_wait_bounded(&sm.full[s ^ 1], (uint32_t)(((j + 1) >> 1) & 1));
-            }
-            return;
-        }
-        const float sk = sm.scale[s][0] * p.score_scale, sv = sm.scale[s][1];
-        widen_page<FMT>(sm.kc[s], sm.k, tid);
-        widen_page<FMT>(sm.vc[s], sm.v, tid);
-        __syncthreads();  // fp16 page ready; stage s consumed
-        if (tid == 0 && j + 2 < ntiles) issue(j + 2, s);
-
-        // S = Q K^T for this warp's 16 rows x 64 keys
-        float sc[8][4];
-#pragma unroll
-        for (int nt = 0; nt < 8; nt++) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ks++) {
-#pragma unroll
-            for (int np = 0; np < 4; np++) {  // key tiles 2 np, 2 np + 1
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(k_base + (np * 16 * kRowH + ks * 16) * 2, b0, b1, b2, b3);
-                mma16816(sc[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                mma16816(sc[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-            }
-        }
-        // scale, causal mask, online softmax (base 2)
-        const int kp0 = j * kPage + 2 * t;  // key position of sc[nt][0] is kp0 + 8 nt
-        const bool diag = j * kPage + kPage - 1 > qpos0 + 16 * warp;
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 8; nt++) {
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                float x = sc[nt][e] * sk;
-                if (diag) {
-                    const int kp = kp0 + 8 * nt + (e & 1);
-                    if (kp > ((e & 2) ? qp_hi : qp_lo)) x = -INFINITY;
-                }
-                sc[nt][e] = x;
-                mx[e >> 1] = fmaxf(mx[e >> 1], x);
-            }
-        }
-        // a page of all-zero values (scale 0) adds nothing: keep the running scale
-        const float fs = sv > 0.0f ? s_run / sv : 1.0f;
-        if (sv > 0.0f) s_run = sv;
-        float alpha[2];
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 2));
-            const float mn = fmaxf(m_run[r], mx[r]);
-            alpha[r] = ex2_approx(m_run[r] - mn);  // 0 on the first tile (m_run = -inf, mn finite)
-            m_run[r] = mn;
-            l_run[r] *= alpha[r];
-        }
-        const float f0 = alpha[0] * fs, f1 = alpha[1] * fs;
-#pragma unroll
-        for (int i = 0; i < 16; i++) {
-            o[i][0] *= f0;
-            o[i][1] *= f0;
-            o[i][2] *= f1;
-            o[i][3] *= f1;
-        }
-        uint32_t pa[8][2];  // P as fp16 pairs: pa[nt][0] row g, pa[nt][1] row g + 8
-#pragma unroll
-        for (int nt = 0; nt < 8; nt++) {
-            const float p0 = ex2_approx(sc[nt][0] - m_run[0]), p1 = ex2_approx(sc[nt][1] - m_run[0]);
-            const float p2 = ex2_approx(sc[nt][2] - m_run[1]), p3 = ex2_approx(sc[nt][3] - m_run[1]);
-            l_run[0] += p0 + p1;
-            l_run[1] += p2 + p3;
-            pa[nt][0] = f16x2_rn(p0, p1);
-            pa[nt][1] = f16x2_rn(p2, p3);
-        }
-        // O += P V: 4 k-steps of 16 keys x 16 tiles of 8 elements
-#pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
-#pragma unroll
-            for (int dp = 0; dp < 8; dp++) {  // element tiles 2 dp, 2 dp + 1
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(v_base + (kk * 16 * kRowH + dp * 16) * 2, b0, b1, b2, b3);
-                mma16816(o[2 * dp], pa[2 * kk][0], pa[2 * kk][1], pa[2 * kk + 1][0], pa[2 * kk + 1][1], b0, b1);
-                mma16816(o[2 * dp + 1], pa[2 * kk][0], pa[2 * kk][1], pa[2 * kk + 1][0], pa[2 * kk + 1][1], b2, b3);
-            }
-        }
-        __syncthreads();  // every warp is done with the fp16 page before the next one is widened
-    }
-
-    // out = O / l for the valid rows
-#pragma unroll
-    for (int r = 0; r < 2; r++) {
-        l_run[r] += __shfl_xor_sync(kFull, l_run[r], 1);
-        l_run[r] += __shfl_xor_sync(kFull, l_run[r], 2);
-    }
-    const float inv0 = s_run / l_run[0], inv1 = s_run / l_run[1];
-    const int r0 = 16 * warp + g, r1 = r0 + 8;
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-        const int d = 8 * i + 2 * t;
-        if (r0 < rows)
-            *reinterpret_cast<uint32_t *>(p.out + ((int64_t)(c0 + i0 + r0) * Hq + hq) * kHeadDim + d) =
-                f16x2_rn(o[i][0] * inv0, o[i][1] * inv0);
-        if (r1 < rows)
-            *reinterpret_cast<uint32_t *>(p.out + ((int64_t)(c0 + i0 + r1) * Hq + hq) * kHeadDim + d) =
-                f16x2_rn(o[i][2] * inv1, o[i][3] * inv1);
-    }
-}
 
 // ---------------------------------------------------------------------------
 // The same attention on the 5th-generation tensor cores (tcgen05): one CTA of
@@ -748,17 +474,6 @@ static cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s)
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((p.max_q + kTcRows - 1) / kTcRows), (unsigned)p.num_q_heads, (unsigned)p.num_seqs);
     return launch_plain(prefill_attn_tc_kernel<FMT>, grid, dim3(kPfWarps * 32), smem, s, p);
-}
-
-template <int FMT>
-static cudaError_t launch_prefill_fmt(const PrefillParams &p, cudaStream_t s)
-{
-    const size_t smem = sizeof(PfSmem<FMT>);
-    cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((p.max_q + kPfRows - 1) / kPfRows), (unsigned)p.num_q_heads, (unsigned)p.num_seqs);
-    return launch_plain(prefill_attn_kernel<FMT>, grid, dim3(kPfWarps * 32), smem, s, p);
 }
 
 cudaError_t launch_prefill(int fmt, const PrefillParams &p, cudaStream_t s)
