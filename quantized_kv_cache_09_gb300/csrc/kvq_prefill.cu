@@ -79,6 +79,10 @@ constexpr uint32_t kTmemCols = 256;  // S: columns 0..63, O: columns 128..255
 constexpr uint32_t kIdescS = (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);   // f32 += f16 x f16, 128 x 64, K-major
 constexpr uint32_t kIdescO = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);  // 128 x 128
 constexpr float kLazy = 8.0f;  // O is rescaled only when a row's max grows by more than 2^8
+// key scales below this are raised to it: a page of all-zero keys (scale 0)
+// then scores 1e-38 * raw instead of 0 (no difference in binary32 after the
+// max is subtracted) and a masked score stays -inf instead of -inf * 0
+constexpr float kMinScale = 1.17549435e-38f;
 
 // byte offset of f16 element (r, k) in a K-major, 128-byte-swizzled tile of R rows
 __device__ __forceinline__ uint32_t sw128(int r, int k, int R)
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
     float cur_sk = 0.0f, cur_sv = 0.0f;
     if (!failed) {
         widen(0);
-        cur_sk = sm.scale[0] * p.score_scale;
+        cur_sk = fmaxf(sm.scale[0] * fabsf(p.score_scale), kMinScale);
         cur_sv = sm.scale[1];
     }
     fence_proxy_async_smem();
@@ -332,6 +336,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
 
     const int row = tid;  // this thread's query row and TMEM lane
     const int qpos = qpos0 + row;
+    const bool neg_scale = p.score_scale < 0.0f;
     float m_used = -INFINITY, l_run = 0.0f;
     uint32_t s_phase = 0, o_phase = 0;
     int o_pending = 0;  // PV launches not yet waited for (0 or 1)
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
         if (!mbar_wait_bounded(&sm.s_done, s_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
         s_phase ^= 1u;
         tc_fence_after();
-        float sc[64];
+        float sc[64];  // raw scores q . code (the key scale is applied in the exponent)
         {
             uint32_t r[4][16];
 #pragma unroll
@@ -350,7 +355,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
 #pragma unroll
             for (int c = 0; c < 4; c++)
 #pragma unroll
-                for (int i = 0; i < 16; i++) sc[16 * c + i] = __uint_as_float(r[c][i]) * cur_sk;
+                for (int i = 0; i < 16; i++) sc[16 * c + i] = __uint_as_float(r[c][i]);
         }
         // 2. PV(j - 1) must be done before its V buffer, P and O are touched again
         if (o_pending) {
@@ -367,7 +372,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
                 break;
             }
             widen(j + 1);
-            nxt_sk = sm.scale[0] * p.score_scale;
+            nxt_sk = fmaxf(sm.scale[0] * fabsf(p.score_scale), kMinScale);
             nxt_sv = sm.scale[1];
             fence_proxy_async_smem();
             tc_fence_before();
@@ -378,13 +383,22 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
                 if (j + 2 < ntiles) issue(j + 2);
             }
         }
-        // 3. causal mask, lazy online softmax (base 2), O rescale
-        float mx = -INFINITY;
+        // 3. causal mask (pages that reach past a row's position), lazy online
+        // softmax in base 2 on x = raw * sk, O rescale.  The maximum is taken
+        // on the raw scores with sk >= 0 (a negative softmax scale flips them).
+        if (neg_scale) {
 #pragma unroll
-        for (int i = 0; i < 64; i++) {
-            if (j * kPage + i > qpos) sc[i] = -INFINITY;
-            mx = fmaxf(mx, sc[i]);
+            for (int i = 0; i < 64; i++) sc[i] = -sc[i];
         }
+        if (j * kPage + kPage - 1 > qpos0) {
+#pragma unroll
+            for (int i = 0; i < 64; i++)
+                if (j * kPage + i > qpos) sc[i] = -INFINITY;
+        }
+        float mraw = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; i++) mraw = fmaxf(mraw, sc[i]);
+        const float mx = mraw == -INFINITY ? -INFINITY : mraw * cur_sk;
         float factor = 1.0f;
         if (j == 0) {
             m_used = mx;  // key 0 is never masked
@@ -404,19 +418,25 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
         l_run *= factor;
-        const float pv_scale = cur_sv / s_ref;
+        // P * sv / s_ref = 2^(raw * sk - m + log2(sv / s_ref)): one FMA per element before ex2; the
+        // row sum of P is that sum times s_ref / sv (a page of all-zero values adds weights to l only)
+        const float pv_ratio = cur_sv / s_ref;
+        const float off = pv_ratio > 0.0f ? m_used - __log2f(pv_ratio) : m_used;
+        float psum = 0.0f;
 #pragma unroll
         for (int c = 0; c < 8; c++) {  // P row -> p (query rows x keys), 8 keys per 16-byte chunk
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; i++) {
-                const float p0 = ex2_approx(sc[8 * c + 2 * i] - m_used);
-                const float p1 = ex2_approx(sc[8 * c + 2 * i + 1] - m_used);
-                l_run += p0 + p1;
-                w[i] = f16x2_rn(p0 * pv_scale, p1 * pv_scale);
+                const float p0 = ex2_approx(fmaf(sc[8 * c + 2 * i], cur_sk, -off));
+                const float p1 = ex2_approx(fmaf(sc[8 * c + 2 * i + 1], cur_sk, -off));
+                psum += p0 + p1;
+                w[i] = f16x2_rn(p0, p1);
             }
             *reinterpret_cast<uint4 *>(sm.p + sw128(row, 8 * c, kTcRows)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        // (a page of all-zero values has codes 0: its P adds nothing to O, its weights count in l)
+        l_run += pv_ratio > 0.0f ? psum / pv_ratio : psum;
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();  // P(j) ready, O rescaled

@@ -142,3 +142,45 @@ def test_prefill_full_size_sampled(cuda_ok):
             ref = orc.decode_attention(wl.fmt, kc, vc, ks, vs, bt, np.array([L - n + i + 1]), qi, np.float32(SM))
             err = np.max(np.abs(got[b * n + i, h] - ref[0, 0])) / vmax
             assert err <= TOL, (b, h, i, err)
+
+
+@pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_FP8_E4M3])
+def test_prefill_zero_pages_and_negative_scale(cuda_ok, fmt):
+    """A page whose keys and values are all zero (scales 0) inside the causal
+    range, and a negative softmax scale: both as the oracle defines them."""
+    H, L, n = 2, 200, 100
+    rng = np.random.default_rng(71)
+    k = rng.standard_normal((L, H, D)).astype(np.float16)
+    v = rng.standard_normal((L, H, D)).astype(np.float16)
+    k[64:128] = 0
+    v[64:128] = 0
+    k[150:160, 1] = 0  # a partly zero page too
+    cache = kvq.PagedKVCache(fmt, 4, H, max_seqs=1)
+    bt = torch.tensor([[2, 0, 3, 1]], dtype=torch.int32, device="cuda")
+    kvq.kvq_append(cache, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                   torch.tensor([0, L], dtype=torch.int32, device="cuda"), bt,
+                   torch.zeros(1, dtype=torch.int32, device="cuda"), L)
+    lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    q = (rng.standard_normal((n, H, D)) * 3).astype(np.float16)
+    cu = np.array([0, n], dtype=np.int32)
+    rb = orc.row_bytes(fmt, D)
+    kc = np.zeros((4, H, 64, rb), np.uint8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((4, H), np.float32)
+    vs = np.zeros_like(ks)
+    bt_np = bt.cpu().numpy()
+    orc.quantize_into_pages(fmt, k.view(np.uint16), bt_np[0], kc, ks)
+    orc.quantize_into_pages(fmt, v.view(np.uint16), bt_np[0], vc, vs)
+    assert np.array_equal(cache.k_codes.cpu().numpy(), kc) and np.array_equal(cache.v_codes.cpu().numpy(), vc)
+    vmax = orc.value_absmax(fmt, vc, vs, bt_np, np.array([L]), H, D)
+    for sm_scale in (SM, -0.05):
+        out = torch.full((n, H, D), float("nan"), dtype=torch.float16, device="cuda")
+        kvq.kvq_prefill_attention(cache, torch.from_numpy(q).cuda(), torch.from_numpy(cu).cuda(), n, bt, lens,
+                                  sm_scale, out)
+        torch.cuda.synchronize()
+        assert kvq.kvq_get_device_status(cache) == (0, 0)
+        ref = orc.prefill_attention(fmt, kc, vc, ks, vs, bt_np, np.array([L]), cu, q.view(np.uint16),
+                                    np.float32(sm_scale))
+        got = out.float().cpu().numpy().astype(np.float64)
+        err = orc.normalized_error(got, ref, np.repeat(vmax, n, axis=0))
+        assert err <= TOL, (sm_scale, err)
