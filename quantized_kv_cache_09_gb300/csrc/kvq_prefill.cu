@@ -151,6 +151,28 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
         : "memory");
 }
 
+// 32 consecutive 32-bit columns of this thread's TMEM lane (completes at tcgen05.wait::st)
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&w)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]),
+        "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]), "r"(w[16]), "r"(w[17]), "r"(w[18]),
+        "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]), "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]),
+        "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
+        : "memory");
+}
+
+// D (tensor memory) += A (tensor memory) x B (shared-memory descriptor)
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
 // 8 elements (one row of an 8 x 8 block, fp16 pairs) of 8 rows -> the block
 // transposed: x[j] = column j as 8 fp16 values
 __device__ __forceinline__ void transpose8(const uint4 (&w)[8], uint4 (&x)[8])
@@ -194,7 +216,6 @@ struct alignas(1024) TcSmem {
     uint8_t q[kTcRows * kHeadDim * 2];        // 32 KB: query rows x elements
     uint8_t k[kPage * kHeadDim * 2];          // 16 KB: keys x elements
     uint8_t vt[2][kHeadDim * kPage * 2];      // 2 x 16 KB: elements x keys (V transposed), two pages
-    uint8_t p[kTcRows * kPage * 2];           // 16 KB: query rows x keys
     uint8_t kc[kPage * PfFmt<FMT>::kRowBytes];  // codes of the next page
     uint8_t vc[kPage * PfFmt<FMT>::kRowBytes];
     float scale[2];
@@ -258,14 +279,17 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
         bulk_copy_g2s(sm.kc, p.k_codes + off, kPageBytes, &sm.full);
         bulk_copy_g2s(sm.vc, p.v_codes + off, kPageBytes, &sm.full);
     };
-    // all threads: page j's codes -> k (keys x elements) and vt[j & 1] (elements x keys)
-    auto widen = [&](int j) {
+    // all threads: page j's key codes -> k (keys x elements)
+    auto widen_k = [&]() {
 #pragma unroll
         for (int r = 0; r < (kPage * 16) / (kPfWarps * 32); r++) {
             const int e = tid + kPfWarps * 32 * r;
             const int key = e >> 4, c = e & 15;
             *reinterpret_cast<uint4 *>(sm.k + sw128(key, 8 * c, kPage)) = codes8<FMT>(sm.kc, key, c);
         }
+    };
+    // all threads: page j's value codes -> vt[j & 1] (elements x keys)
+    auto widen_v = [&](int j) {
         // keys 8 kb .. +7, elements 8 dc .. +7; 8 lanes with consecutive kb store 8 different 16-byte chunks
         const int kb = tid & 7, dc = tid >> 3;
         uint4 w[8], x[8];
@@ -303,7 +327,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
         if (r < rows) v = *reinterpret_cast<const uint4 *>(p.q + ((int64_t)(c0 + i0 + r) * Hq + hq) * kHeadDim + 8 * c);
         *reinterpret_cast<uint4 *>(sm.q + sw128(r, 8 * c, kTcRows)) = v;
     }
-    const uint32_t aq = smem_addr(sm.q), ak = smem_addr(sm.k), ap = smem_addr(sm.p);
+    const uint32_t aq = smem_addr(sm.q), ak = smem_addr(sm.k);
     const uint32_t av0 = smem_addr(sm.vt[0]), av1 = smem_addr(sm.vt[1]);
     auto issue_s = [&](uint32_t tmem, int j) {  // thread 0: S(j) = Q K^T into S buffer j & 1
 #pragma unroll
@@ -318,7 +342,8 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
     bool failed = __syncthreads_and(ok) == 0;
     float cur_sk = 0.0f, cur_sv = 0.0f;
     if (!failed) {
-        widen(0);
+        widen_k();
+        widen_v(0);
         cur_sk = fmaxf(sm.scale[0] * fabsf(p.score_scale), kMinScale);
         cur_sv = sm.scale[1];
     }
@@ -357,21 +382,27 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
 #pragma unroll
                 for (int i = 0; i < 16; i++) sc[16 * c + i] = __uint_as_float(r[c][i]);
         }
-        // 2. PV(j - 1) must be done before its V buffer, P and O are touched again
-        if (o_pending) {
-            if (!mbar_wait_bounded(&sm.o_done, o_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
-            o_phase ^= 1u;
-            o_pending = 0;
-            tc_fence_after();
-        }
+        // 2. the next page: codes, widen, and its S on the tensor cores.  PV(j - 1)
+        // must be done before its V buffer is refilled, before O is rescaled and
+        // before S(j + 1) overwrites the P(j - 1) it reads (the K part is widened first)
+        auto wait_pv = [&]() {
+            if (o_pending) {
+                if (!mbar_wait_bounded(&sm.o_done, o_phase)) set_flag(p.status, KVQ_FLAG_TIMEOUT);
+                o_phase ^= 1u;
+                o_pending = 0;
+                tc_fence_after();
+            }
+        };
         float nxt_sk = cur_sk, nxt_sv = cur_sv;
-        if (j + 1 < ntiles) {  // the next page: codes, widen, and its S on the tensor cores
+        if (j + 1 < ntiles) {
             ok = mbar_wait_bounded(&sm.full, (uint32_t)((j + 1) & 1));
             if (__syncthreads_and(ok) == 0) {
                 failed = true;
                 break;
             }
-            widen(j + 1);
+            widen_k();
+            wait_pv();
+            widen_v(j + 1);
             nxt_sk = fmaxf(sm.scale[0] * fabsf(p.score_scale), kMinScale);
             nxt_sv = sm.scale[1];
             fence_proxy_async_smem();
@@ -383,6 +414,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
                 if (j + 2 < ntiles) issue(j + 2);
             }
         }
+        wait_pv();  // the last page: nothing to widen
         // 3. causal mask (pages that reach past a row's position), lazy online
         // softmax in base 2 on x = raw * sk, O rescale.  The maximum is taken
         // on the raw scores with sk >= 0 (a negative softmax scale flips them).
@@ -423,29 +455,28 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_attn_tc_kernel(Prefi
         const float pv_ratio = cur_sv / s_ref;
         const float off = pv_ratio > 0.0f ? m_used - __log2f(pv_ratio) : m_used;
         float psum = 0.0f;
+        {  // P row as 32 fp16 pairs (keys 2c, 2c + 1) over the first 32 columns of this page's S buffer
+            uint32_t w[32];
 #pragma unroll
-        for (int c = 0; c < 8; c++) {  // P row -> p (query rows x keys), 8 keys per 16-byte chunk
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const float p0 = ex2_approx(fmaf(sc[8 * c + 2 * i], cur_sk, -off));
-                const float p1 = ex2_approx(fmaf(sc[8 * c + 2 * i + 1], cur_sk, -off));
+            for (int c = 0; c < 32; c++) {
+                const float p0 = ex2_approx(fmaf(sc[2 * c], cur_sk, -off));
+                const float p1 = ex2_approx(fmaf(sc[2 * c + 1], cur_sk, -off));
                 psum += p0 + p1;
-                w[i] = f16x2_rn(p0, p1);
+                w[c] = f16x2_rn(p0, p1);
             }
-            *reinterpret_cast<uint4 *>(sm.p + sw128(row, 8 * c, kTcRows)) = make_uint4(w[0], w[1], w[2], w[3]);
+            tmem_st32(lane_tm + 64 * (j & 1), w);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
         // (a page of all-zero values has codes 0: its P adds nothing to O, its weights count in l)
         l_run += pv_ratio > 0.0f ? psum / pv_ratio : psum;
-        fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();  // P(j) ready, O rescaled
-        if (tid == 0) {  // 4. O += P(j) V(j)
+        __syncthreads();  // P(j) in tensor memory, O rescaled
+        if (tid == 0) {  // 4. O += P(j) V(j), P from tensor memory (8 packed columns per 16 keys)
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ks++)
-                umma_f16(tmem + 128, umma_desc(ap + ks * 32), umma_desc(((j & 1) ? av1 : av0) + ks * 32), kIdescO,
-                         (j > 0 || ks > 0));
+                umma_f16_ts(tmem + 128, tmem + 64 * (j & 1) + 8 * ks, umma_desc(((j & 1) ? av1 : av0) + ks * 32),
+                            kIdescO, (j > 0 || ks > 0));
             umma_commit(&sm.o_done);
         }
         o_pending = 1;
