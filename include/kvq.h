@@ -247,8 +247,8 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const uint16_t *
  * position p = seq_lens[b] - n_b + i and attends causally:
  *   out[row][hq][:] = sum_{t <= p} softmax_t(softmax_scale q . k^_t) v^_t
  * over cache head hq / g (g = num_q_heads / cache->num_heads, any g >= 1),
- * binary32 accumulation on the tensor cores (fp16 codes, probabilities
- * rounded to fp16 as the second operand).
+ * on the tensor cores (tcgen05): fp16 codes, fp16 q, probabilities rounded to
+ * fp16 as the PV operand, binary32 accumulation.  Any finite softmax_scale.
  *   q, out           fp16 [total_q][num_q_heads][head_dim], 16-byte aligned
  *   cu_seqlens_q     device int32 [num_seqs + 1], non-decreasing, cu[0] >= 0
  *   max_q_per_seq    host bound on every n_b (sizes the grid); 0 is a no-op
