@@ -890,6 +890,90 @@ __device__ __noinline__ void merge_pieces(const float *partials, int64_t slot_fl
         make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
 }
 
+// One warp: merge_pieces for all G query heads of one cache head at once.  A
+// piece holds the G heads' partials side by side; the loads of kBatch pieces x
+// G heads are issued together, so a merge of cnt pieces takes about cnt /
+// kBatch round trips to L2 instead of G times as many (kBatch = 8 / G keeps
+// the call within the kernel's register budget).
+template <int kBatch, int G>
+__device__ __noinline__ void merge_group(const float *partials, int64_t gf, int cnt, int first_slot,
+                                         uint16_t *out_rows, int lane)
+{
+    constexpr int64_t kSlot = (int64_t)G * kPartialStride;
+    const float *pbase = partials + gf * 2 * kSlot;
+    auto part = [&](int i) { return pbase + ((int64_t)i * 2 + (i == 0 ? first_slot : 0)) * kSlot; };
+    float2 ml[G];
+    float4 a[kBatch][G];
+    float mj[kBatch][G];
+#pragma unroll
+    for (int g = 0; g < G; g++)
+        ml[g] = lane < cnt ? __ldcg(reinterpret_cast<const float2 *>(part(lane) + g * kPartialStride))
+                           : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+    for (int j = 0; j < kBatch; j++) {
+        const float *src = part(j < cnt ? j : 0);
+#pragma unroll
+        for (int g = 0; g < G; g++) {
+            a[j][g] = __ldcg(reinterpret_cast<const float4 *>(src + g * kPartialStride + 4) + lane);
+            mj[j][g] = j < cnt ? __ldcg(src + g * kPartialStride) : -INFINITY;
+        }
+    }
+    float M[G], L[G];
+    float4 o[G];
+#pragma unroll
+    for (int g = 0; g < G; g++) M[g] = ml[g].x;
+    for (int i = lane + 32; i < cnt; i += 32)
+#pragma unroll
+        for (int g = 0; g < G; g++) M[g] = fmaxf(M[g], __ldcg(part(i) + g * kPartialStride));
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+        M[g] = warp_max(M[g]);
+        L[g] = lane < cnt ? ml[g].y * ex2_approx(ml[g].x - M[g]) : 0.0f;
+    }
+    for (int i = lane + 32; i < cnt; i += 32)
+#pragma unroll
+        for (int g = 0; g < G; g++) {
+            const float2 v = __ldcg(reinterpret_cast<const float2 *>(part(i) + g * kPartialStride));
+            L[g] += v.y * ex2_approx(v.x - M[g]);
+        }
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+        L[g] = warp_sum(L[g]);
+        o[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int i0 = 0; i0 < cnt; i0 += kBatch) {
+        if (i0 > 0) {
+#pragma unroll
+            for (int j = 0; j < kBatch; j++) {
+                const float *src = part(i0 + j < cnt ? i0 + j : 0);
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    a[j][g] = __ldcg(reinterpret_cast<const float4 *>(src + g * kPartialStride + 4) + lane);
+                    mj[j][g] = i0 + j < cnt ? __ldcg(src + g * kPartialStride) : -INFINITY;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; j++)
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+                const float w = ex2_approx(mj[j][g] - M[g]);
+                o[g].x += a[j][g].x * w;
+                o[g].y += a[j][g].y * w;
+                o[g].z += a[j][g].z * w;
+                o[g].w += a[j][g].w * w;
+            }
+    }
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+        const float inv = 1.0f / L[g];
+        const __half2 lo = __floats2half2_rn(o[g].x * inv, o[g].y * inv);
+        const __half2 hi = __floats2half2_rn(o[g].z * inv, o[g].w * inv);
+        reinterpret_cast<uint2 *>(out_rows + g * kHeadDim)[lane] =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+    }
+}
+
 template <int FMT, int G>
 struct ConsumerFor {
     using type = ConsumerGqa<G>;
@@ -1115,11 +1199,15 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             const int64_t u1 = u0 + n;
             const int64_t gf = ((u0 + 1) * GW - 1) / U;  // warp owning unit u0
             const int64_t gl = (u1 * GW - 1) / U;        // warp owning unit u1 - 1
-            if (last_piece(p.pieces + gl, (uint32_t)(gl - gf + 1), lane, p.status))
-                for (int j = 0; j < G; j++)
-                    merge_pieces<F::kMergeBatch>(p.partials, kSlotFloats, j, gf, (int)(gl - gf + 1),
-                                                 ((U * gf) / GW != u0) ? 1 : 0,
-                                                 p.out + (((int64_t)b * H + h) * G + j) * kHeadDim, lane);
+            if (last_piece(p.pieces + gl, (uint32_t)(gl - gf + 1), lane, p.status)) {
+                const int first_slot = ((U * gf) / GW != u0) ? 1 : 0;
+                uint16_t *orow = p.out + ((int64_t)b * H + h) * G * kHeadDim;
+                if constexpr (G == 1)
+                    merge_pieces<F::kMergeBatch>(p.partials, kSlotFloats, 0, gf, (int)(gl - gf + 1), first_slot,
+                                                 orow, lane);
+                else
+                    merge_group<8 / G, G>(p.partials, gf, (int)(gl - gf + 1), first_slot, orow, lane);
+            }
         }
     };
     auto drain = [&](int from) {  // after a timeout: let the copies still in flight land
