@@ -105,7 +105,7 @@ def measured_tensor_peak():
 KERNEL_SOURCES = {
     "decode_split_kernel": ("kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h"),
     "append_kernel": ("kvq_quantize.cu", "kvq_device.cuh", "kvq_internal.h"),
-    "prefill_attn_kernel": ("kvq_prefill.cu", "kvq_device.cuh", "kvq_internal.h"),
+    "prefill_attn_tc_kernel": ("kvq_prefill.cu", "kvq_device.cuh", "kvq_internal.h"),
 }
 
 
@@ -605,9 +605,9 @@ def run_ours(args):
                            "step": "one kvq_prefill_attention of every chunk query",
                            "l2": "codes (268 MB) larger than L2"},
                 "tflops": tflops,
-                "roofline": {"kernel": "prefill_attn_kernel", "bound": "tensor", "achieved": tflops, "peak": tpeak,
+                "roofline": {"kernel": "prefill_attn_tc_kernel", "bound": "tensor", "achieved": tflops, "peak": tpeak,
                              "peak_kind": tkind, "unit": "TFLOP/s", "frac": tflops / tpeak,
-                             "traffic": ncu_traffic("prefill_attn_kernel", "chunked-prefill"),
+                             "traffic": ncu_traffic("prefill_attn_tc_kernel", "chunked-prefill"),
                              "algorithmic_flops_per_launch": r["flops"]},
                 "e2e": {"value": whole_job_rate(world, r["tokens"], e2e_ms * 1e-3), "unit": "tokens/s",
                         "h2d_bytes_per_step": r["qbytes"], "d2h_bytes_per_step": r["qbytes"]},
