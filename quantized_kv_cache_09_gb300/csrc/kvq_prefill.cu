@@ -7,25 +7,25 @@
 //
 // On the 5th-generation tensor cores (tcgen05).  One CTA owns two tiles of
 // 128 query rows of one (sequence, query head); query head hq reads cache head
-// hq / g.  Its warps split into roles that hand work over through mbarriers:
-//   * 4 widening warps: a page's K and V codes of the cache head arrive in
-//     shared memory by two bulk copies; the warps widen them once, for both
-//     tiles, to fp16 codes (exact: integers or E4M3 values) in the K-major
-//     128-byte-swizzled layout the MMA reads -- K as keys x elements, V
-//     transposed (elements x keys) -- into one of 3 stages, and start the
-//     copy two pages ahead; the scales stay out of the fp16 operands;
-//   * 1 MMA thread: per tile, S = Q K^T (M = 128, N = 64, 8 MMAs of K = 16)
-//     into one of two S buffers in tensor memory and O += P V (M = 128,
-//     N = 128, 4 MMAs of K = 16) with P read from tensor memory;
+// hq / g.  Keys go in steps of 128 (two pages).  The CTA's warps split into
+// roles that hand work over through mbarriers:
+//   * 4 widening warps load the K and V codes of the cache head straight from
+//     global memory into registers (16-byte pieces, one page ahead) and widen
+//     them once, for both tiles, to fp16 codes (exact: integers or E4M3
+//     values) in shared memory, 128-byte swizzled, keys x elements; the same
+//     bytes are the K-major B operand of S and the MN-major B operand of PV.
+//     Two stages; the scales stay out of the fp16 operands;
+//   * 1 MMA thread: per tile, S = Q K^T (M = 128, N = 128 keys, 8 MMAs of
+//     K = 16) into tensor memory and O += P V (M = 128, N = 128, 8 MMAs) with
+//     P read from tensor memory where S was;
 //   * 8 softmax warps, one thread per query row (its lane of tensor memory):
 //     each loads its row of S, masks keys after its position and runs an
-//     online softmax in base 2 with the page's key scale in the exponent and
+//     online softmax in base 2 with each page's key scale in the exponent and
 //     a lazy running maximum (O is rescaled, in tensor memory, only when a
 //     row's maximum grows by more than 2^8); P * sv / s_ref (s_ref = the
 //     largest value scale over the CTA's pages, so the fp16 operand stays in
 //     [0, 256]) goes to tensor memory over the S it came from.
-// The two tiles' softmax warps alternate with the tensor cores: while one
-// tile's rows are in the softmax, the MMAs of the other run.
+// While one tile's rows are in the softmax, the tensor cores work on the other.
 // fp32 accumulation throughout; the output is s_ref * O / l rounded to fp16.
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
@@ -74,14 +74,15 @@ namespace {
 
 constexpr int kTcRows = 128;   // query rows per tile (TMEM lanes)
 constexpr int kTiles = 2;      // query tiles per CTA: each widened page serves both
-constexpr int kStages = 3;     // widened pages in shared memory
+constexpr int kStepKeys = 2 * kPage;  // keys per step: two pages, one S of N = 128 per tile
 constexpr int kWidenThreads = 128;
 // warps 0..7: softmax of the two tiles; 8..11: widening; 12: MMA issue
 constexpr int kTcThreads = kTiles * kPfWarps * 32 + kWidenThreads + 32;
-// tile t: S buffers at columns 256 t + 0..63 and 256 t + 64..127, O at 256 t + 128..255
+// tile t: S (and P over its first 64 columns) at columns 256 t + 0..127, O at 256 t + 128..255
 constexpr uint32_t kTmemCols = 256 * kTiles;
-constexpr uint32_t kIdescS = (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);   // f32 += f16 x f16, 128 x 64, K-major
-constexpr uint32_t kIdescO = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);  // 128 x 128
+// f32 += f16 x f16, M = 128, N = 128; S: both operands K-major; PV: B (V) MN-major
+constexpr uint32_t kIdescS = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescO = kIdescS | (1u << 16);
 constexpr float kLazy = 8.0f;  // O is rescaled only when a row's max grows by more than 2^8
 // key scales below this are raised to it: a page of all-zero keys (scale 0)
 // then scores 1e-38 * raw instead of 0 (no difference in binary32 after the
@@ -100,6 +101,14 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr)
 {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// the same with explicit leading (lbo) and stride (sbo) byte offsets; for an MN-major
+// swizzled operand lbo steps between 64-element atoms along MN, sbo between 8-row groups along K
+__device__ __forceinline__ uint64_t umma_desc_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
@@ -177,58 +186,43 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 
-// 8 elements (one row of an 8 x 8 block, fp16 pairs) of 8 rows -> the block
-// transposed: x[j] = column j as 8 fp16 values
-__device__ __forceinline__ void transpose8(const uint4 (&w)[8], uint4 (&x)[8])
-{
-#pragma unroll
-    for (int m = 0; m < 4; m++) {  // columns 2m, 2m + 1
-        uint32_t lo[4], hi[4];
-#pragma unroll
-        for (int n = 0; n < 4; n++) {
-            const uint32_t a = (&w[2 * n].x)[m], b = (&w[2 * n + 1].x)[m];
-            lo[n] = __byte_perm(a, b, 0x5410);
-            hi[n] = __byte_perm(a, b, 0x7632);
-        }
-        x[2 * m] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        x[2 * m + 1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    }
-}
-
-// 8 codes of row `row` (elements 8c .. 8c + 7) as 8 fp16 values
+// 16 code bytes (consecutive elements of one row) -> their fp16 values, 8 per uint4
 template <int FMT>
-__device__ __forceinline__ uint4 codes8(const uint8_t *page, int row, int c)
+__device__ __forceinline__ void widen16(uint4 c, uint4 (&out)[FMT == KVQ_INT4_B64 ? 4 : 2])
 {
     if constexpr (FMT == KVQ_INT4_B64) {
-        return widen8_int4(*reinterpret_cast<const uint32_t *>(page + row * 64 + 4 * c));
+        out[0] = widen8_int4(c.x);
+        out[1] = widen8_int4(c.y);
+        out[2] = widen8_int4(c.z);
+        out[3] = widen8_int4(c.w);
     } else {
-        const uint2 w = *reinterpret_cast<const uint2 *>(page + row * 128 + 8 * c);
-        __half2 a[2], b[2];
-        if constexpr (FMT == KVQ_FP8_E4M3) {
-            widen_e4m3(w.x, a);
-            widen_e4m3(w.y, b);
-        } else {
-            widen_int8(w.x, a);
-            widen_int8(w.y, b);
+        const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            __half2 a[2], b[2];
+            if constexpr (FMT == KVQ_FP8_E4M3) {
+                widen_e4m3(wd[2 * i], a);
+                widen_e4m3(wd[2 * i + 1], b);
+            } else {
+                widen_int8(wd[2 * i], a);
+                widen_int8(wd[2 * i + 1], b);
+            }
+            out[i] = make_uint4(h2_bits(a[0]), h2_bits(a[1]), h2_bits(b[0]), h2_bits(b[1]));
         }
-        return make_uint4(h2_bits(a[0]), h2_bits(a[1]), h2_bits(b[0]), h2_bits(b[1]));
     }
 }
 
 template <int FMT>
 struct alignas(1024) TcSmem {
-    uint8_t q[kTiles][kTcRows * kHeadDim * 2];     // 32 KB per tile: query rows x elements
-    uint8_t k[kStages][kPage * kHeadDim * 2];      // 16 KB per stage: keys x elements
-    uint8_t vt[kStages][kHeadDim * kPage * 2];     // 16 KB per stage: elements x keys (V transposed)
-    uint8_t kc[2][kPage * PfFmt<FMT>::kRowBytes];  // codes of the two pages in flight
-    uint8_t vc[2][kPage * PfFmt<FMT>::kRowBytes];
-    uint64_t code_full[2];       // a page's codes landed (bulk copies)
-    uint64_t kv_ready[kStages];  // a page's widened K and V written (every widening thread)
-    uint64_t kv_free[kStages];   // every MMA reading a stage complete (commit)
-    uint64_t s_full[kTiles];     // S of a tile's page complete (commit)
-    uint64_t p_full[kTiles];     // P of a tile's page in tensor memory, O rescaled (every row of the tile)
-    uint64_t o_done[kTiles];     // O += P V of a tile's page complete (commit)
-    uint64_t mma_done;           // every MMA issued complete (commit, at the end)
+    uint8_t q[kTiles][kTcRows * kHeadDim * 2];  // 32 KB per tile: query rows x elements (K-major)
+    uint8_t k[2][kStepKeys * kHeadDim * 2];     // 32 KB per stage: keys x elements (K-major)
+    uint8_t v[2][kStepKeys * kHeadDim * 2];     // 32 KB per stage: keys x elements (MN-major B of PV)
+    uint64_t kv_ready[2];   // a step's widened K and V written (every widening thread)
+    uint64_t kv_free[2];    // the MMAs reading a stage complete (commit)
+    uint64_t s_full[kTiles];  // S of a tile's step complete (commit); PV of the step before too
+    uint64_t p_full[kTiles];  // P of a tile's step in tensor memory, O rescaled (every row of the tile)
+    uint64_t o_done[kTiles];  // O += P V of a tile's step complete (commit)
+    uint64_t mma_done;        // every MMA issued complete (commit, at the end)
     float s_ref;
     uint32_t tmem;
 };
@@ -250,27 +244,29 @@ __device__ __forceinline__ bool widen_group_all(bool v)
         : "memory");
     return r != 0;
 }
-__device__ __forceinline__ void widen_group_sync()
+
+// byte offset of the 8 elements 8c .. 8c + 7 of key `key` in a stage's K tile (keys x
+// elements, K-major) and V tile (the same values MN-major: 64-element atoms of 128 keys)
+__device__ __forceinline__ uint32_t k_chunk(int key, int c) { return sw128(key, 8 * c, kStepKeys); }
+__device__ __forceinline__ uint32_t v_chunk(int key, int c)
 {
-    asm volatile("bar.sync 1, %0;" ::"n"(kWidenThreads) : "memory");
+    return (uint32_t)((c >> 3) * (kStepKeys * 128) + key * 128 + (((c & 7) ^ (key & 7)) << 4));
 }
 
 }  // namespace
 
-// Roles, per 64-token page j (all hand-offs are mbarriers, so each role runs
-// ahead as far as its buffers allow):
-//   widening warps  wait for the codes of page j and for stage j % kStages to
-//                   be free, widen K and V into it, start the copy of page
-//                   j + 2 into the code buffer just read;
-//   MMA thread      per tile: once P(j) is in tensor memory, O += P(j) V(j),
-//                   then S(j + 1) = Q K(j + 1)^T into the S buffer P(j - 1)
-//                   used; after both tiles, release stage j % kStages;
-//   softmax warps   per tile (one thread per query row): wait S(j), mask,
-//                   lazy online softmax, P(j) into tensor memory over S(j);
-//                   wait PV(j - 1) (O stable; this also frees P(j - 1)'s
-//                   buffer for S(j + 1)), rescale O if a row's max moved,
-//                   hand P(j) to the MMA thread.
-// While one tile's softmax runs, the tensor cores work on the other tile.
+// Roles, per step i of 128 keys (pages 2i and 2i + 1); all hand-offs are mbarriers:
+//   widening warps  wait for stage i & 1 to be free, widen the codes of both pages
+//                   (already in registers) into it -- a page past the last is zero --
+//                   loading each next page's codes while converting the current one;
+//   MMA thread      per tile: once P(i) is in tensor memory, O += P(i) V(i); once
+//                   that is complete (P(i) lives where S goes), S(i + 1) = Q K(i + 1)^T;
+//                   the last reader of a stage releases it;
+//   softmax warps   per tile (one thread per query row): wait S(i) (which also means
+//                   PV(i - 1) is complete), row max over the 128 keys, lazy online
+//                   softmax, P(i) into tensor memory over S(i), rescale O if a row's
+//                   max moved, hand P(i) to the MMA thread.
+// While one tile's rows are in the softmax, the tensor cores work on the other tile.
 template <int FMT>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillParams p)
 {
@@ -294,14 +290,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
         return;
     }
     if (i0 >= n) return;
-    const int rows = min(kTiles * kTcRows, n - i0);            // valid query rows of the CTA
-    const int active = (rows + kTcRows - 1) / kTcRows;        // tiles with at least one of them
-    const int qpos0 = L - n + i0;                             // position of the CTA's first query
-    // pages tile t reads: through the position of its last valid row
+    const int rows = min(kTiles * kTcRows, n - i0);      // valid query rows of the CTA
+    const int active = (rows + kTcRows - 1) / kTcRows;  // tiles with at least one of them
+    const int qpos0 = L - n + i0;                       // position of the CTA's first query
+    // pages and steps tile t reads: through the position of its last valid row
     auto pages_of = [&](int t) {
         return t < active ? (qpos0 + min(kTcRows * (t + 1), rows) - 1) / kPage + 1 : 0;
     };
+    auto steps_of = [&](int t) { return (pages_of(t) + 1) / 2; };
     const int npages = pages_of(active - 1);
+    const int nsteps = (npages + 1) / 2;
     const int32_t *bt = p.block_table + (int64_t)b * p.max_blocks;
 
     auto page_of = [&](int j) {
@@ -312,17 +310,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
         }
         return pg;
     };
-    auto issue = [&](int j) {  // one thread: page j's codes into code buffer j & 1
-        const size_t off = ((size_t)page_of(j) * H + h) * kPageBytes;
-        mbar_arrive_expect_tx(&sm.code_full[j & 1], 2 * kPageBytes);
-        bulk_copy_g2s(sm.kc[j & 1], p.k_codes + off, kPageBytes, &sm.code_full[j & 1]);
-        bulk_copy_g2s(sm.vc[j & 1], p.v_codes + off, kPageBytes, &sm.code_full[j & 1]);
-    };
 
     if (tid == 0) {
-        mbar_init(&sm.code_full[0], 1);
-        mbar_init(&sm.code_full[1], 1);
-        for (int s = 0; s < kStages; s++) {
+        for (int s = 0; s < 2; s++) {
             mbar_init(&sm.kv_ready[s], kWidenThreads);
             mbar_init(&sm.kv_free[s], 1);
         }
@@ -333,8 +323,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
         }
         mbar_init(&sm.mma_done, 1);
         mbar_init_fence();
-        issue(0);  // the first two pages' codes travel while the queries load
-        if (npages > 1) issue(1);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem)),
@@ -364,7 +352,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
     if (warp < kTiles * kPfWarps) {
         // ---- softmax: tile t, one query row per thread (its TMEM lane) ----
         const int t = warp / kPfWarps, row = tid % kTcRows;
-        const int nt = pages_of(t);
+        const int nst = steps_of(t);
         const uint32_t lane_tm = tmem + 256u * t + ((uint32_t)((warp % kPfWarps) * 32) << 16);
         const int tile_qpos0 = qpos0 + kTcRows * t;
         const int qpos = tile_qpos0 + row;  // this row's position in the sequence
@@ -372,97 +360,121 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
         const float sabs = fabsf(p.score_scale);
         const bool neg_scale = p.score_scale < 0.0f;
         float m_used = -INFINITY, l_run = 0.0f;
-        float sk = 0.0f, sv = 0.0f;  // the page's scales, loaded one page ahead
-        if (nt > 0) {
-            const int pg = page_of(0);
-            sk = p.k_scales[(int64_t)pg * H + h];
-            sv = p.v_scales[(int64_t)pg * H + h];
-        }
-        for (int j = 0; j < nt; j++) {
-            float nsk = 0.0f, nsv = 0.0f;
-            if (j + 1 < nt) {
-                const int pg = page_of(j + 1);
-                nsk = p.k_scales[(int64_t)pg * H + h];
-                nsv = p.v_scales[(int64_t)pg * H + h];
+        // the scales of a step's two pages (zero past the last page), loaded one step ahead
+        auto load_scales = [&](int i, float (&k2)[2], float (&v2)[2]) {
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                k2[hh] = 0.0f;
+                v2[hh] = 0.0f;
+                if (2 * i + hh < npages) {
+                    const int pg = page_of(2 * i + hh);
+                    k2[hh] = p.k_scales[(int64_t)pg * H + h];
+                    v2[hh] = p.v_scales[(int64_t)pg * H + h];
+                }
             }
-            const float cur_sk = fmaxf(sk * sabs, kMinScale);
-            ok = __all_sync(kFull, mbar_wait_bounded(&sm.s_full[t], (uint32_t)(j & 1)));
+        };
+        float sk[2] = {0.0f, 0.0f}, sv[2] = {0.0f, 0.0f};
+        if (nst > 0) load_scales(0, sk, sv);
+        for (int i = 0; i < nst; i++) {
+            float nsk[2] = {0.0f, 0.0f}, nsv[2] = {0.0f, 0.0f};
+            if (i + 1 < nst) load_scales(i + 1, nsk, nsv);
+            ok = __all_sync(kFull, mbar_wait_bounded(&sm.s_full[t], (uint32_t)(i & 1)));
             if (!ok) break;
             tc_fence_after();
-            float sc[64];  // raw scores q . code (the key scale is applied in the exponent)
-            {
+            const bool diag = i * kStepKeys + kStepKeys - 1 > tile_qpos0;  // keys past some row's position
+            // raw scores q . code of keys 64 hh .. 64 hh + 63 of the step: sign-flipped for a
+            // negative softmax scale (the key scale is applied in the exponent, >= 0), masked
+            auto load_half = [&](int hh, float (&sc)[64]) {
                 uint32_t r[4][16];
 #pragma unroll
-                for (int c = 0; c < 4; c++) tmem_ld16_async(lane_tm + 64 * (j & 1) + 16 * c, r[c]);
+                for (int c = 0; c < 4; c++) tmem_ld16_async(lane_tm + 64 * hh + 16 * c, r[c]);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 4; c++)
 #pragma unroll
-                    for (int i = 0; i < 16; i++) sc[16 * c + i] = __uint_as_float(r[c][i]);
-            }
-            // causal mask (pages that reach past a row's position); the maximum is
-            // taken on the raw scores with sk >= 0 (a negative softmax scale flips them)
-            if (neg_scale) {
+                    for (int x = 0; x < 16; x++) sc[16 * c + x] = __uint_as_float(r[c][x]);
+                if (neg_scale) {
 #pragma unroll
-                for (int i = 0; i < 64; i++) sc[i] = -sc[i];
-            }
-            if (j * kPage + kPage - 1 > tile_qpos0) {
+                    for (int x = 0; x < 64; x++) sc[x] = -sc[x];
+                }
+                if (diag) {
+                    const int k0 = i * kStepKeys + 64 * hh;
 #pragma unroll
-                for (int i = 0; i < 64; i++)
-                    if (j * kPage + i > qpos) sc[i] = -INFINITY;
-            }
-            float mraw = -INFINITY;
+                    for (int x = 0; x < 64; x++)
+                        if (k0 + x > qpos) sc[x] = -INFINITY;
+                }
+            };
+            // pass 1: the row maximum of x = raw * sk over the step
+            float cur_sk[2];
+            float mx = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 64; i++) mraw = fmaxf(mraw, sc[i]);
-            const float mx = mraw == -INFINITY ? -INFINITY : mraw * cur_sk;
+            for (int hh = 0; hh < 2; hh++) {
+                cur_sk[hh] = fmaxf(sk[hh] * sabs, kMinScale);
+                float sc[64];
+                load_half(hh, sc);
+                float m8[8];  // independent maxima, then a tree
+#pragma unroll
+                for (int x = 0; x < 8; x++) m8[x] = sc[x];
+#pragma unroll
+                for (int x = 8; x < 64; x++) m8[x & 7] = fmaxf(m8[x & 7], sc[x]);
+                const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                if (mraw != -INFINITY) mx = fmaxf(mx, mraw * cur_sk[hh]);
+            }
             float factor = 1.0f;
-            if (j == 0) {
+            if (i == 0) {
                 m_used = mx;  // key 0 is never masked
             } else if (mx > m_used + kLazy) {
                 factor = ex2_approx(m_used - mx);
                 m_used = mx;
             }
-            // P * sv / s_ref = 2^(raw * sk - m + log2(sv / s_ref)): one FMA per element before ex2;
-            // the row sum of P is that sum times s_ref / sv (a page of all-zero values adds to l only)
-            const float pv_ratio = sv / s_ref;
-            const float off = pv_ratio > 0.0f ? m_used - __log2f(pv_ratio) : m_used;
-            float psum = 0.0f;
-            {  // P row as 32 fp16 pairs (keys 2c, 2c + 1) over the first 32 columns of this page's S buffer
+            // pass 2: P * sv / s_ref = 2^(raw * sk - m + log2(sv / s_ref)), one FMA per element
+            // before ex2, as fp16 pairs over columns 32 hh .. 32 hh + 31 (S of those keys is read);
+            // the row sum of P is that sum times s_ref / sv (all-zero values add to l only)
+            float l_add = 0.0f;
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                float sc[64];
+                load_half(hh, sc);
+                const float ratio = sv[hh] / s_ref;
+                const float off = ratio > 0.0f ? m_used - __log2f(ratio) : m_used;
+                float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 uint32_t w[32];
 #pragma unroll
                 for (int c = 0; c < 32; c++) {
-                    const float p0 = ex2_approx(fmaf(sc[2 * c], cur_sk, -off));
-                    const float p1 = ex2_approx(fmaf(sc[2 * c + 1], cur_sk, -off));
-                    psum += p0 + p1;
+                    const float p0 = ex2_approx(fmaf(sc[2 * c], cur_sk[hh], -off));
+                    const float p1 = ex2_approx(fmaf(sc[2 * c + 1], cur_sk[hh], -off));
+                    ps[c & 3] += p0 + p1;
                     w[c] = f16x2_rn(p0, p1);
                 }
-                tmem_st32(lane_tm + 64 * (j & 1), w);
+                tmem_st32(lane_tm + 32 * hh, w);
+                const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                l_add += ratio > 0.0f ? psum / ratio : psum;
             }
-            // O holds PV(j - 1) once it completes: only then may it be rescaled
-            if (j > 0) {
-                ok = __all_sync(kFull, mbar_wait_bounded(&sm.o_done[t], (uint32_t)((j - 1) & 1)));
-                if (!ok) break;
-                tc_fence_after();
-            }
-            if (__any_sync(kFull, factor != 1.0f)) {  // O (columns 128..255) of the rows whose max moved
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            // O holds PV(i - 1) (complete before S(i) was issued): rescale the rows whose max moved
+            if (__any_sync(kFull, factor != 1.0f)) {
 #pragma unroll
                 for (int c = 0; c < 8; c++) {
                     float v[16];
                     tmem_ld16(lane_tm + 128 + 16 * c, v);
 #pragma unroll
-                    for (int i = 0; i < 16; i++) v[i] *= factor;
+                    for (int x = 0; x < 16; x++) v[x] *= factor;
                     tmem_st16(lane_tm + 128 + 16 * c, v);
                 }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             mbar_arrive(&sm.p_full[t]);
-            l_run = l_run * factor + (pv_ratio > 0.0f ? psum / pv_ratio : psum);
-            sk = nsk;
-            sv = nsv;
+            l_run = l_run * factor + l_add;
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                sk[hh] = nsk[hh];
+                sv[hh] = nsv[hh];
+            }
         }
-        if (ok && nt > 0) {  // out = s_ref * O / l after the last PV; loads warp-wide, stores per row
-            ok = __all_sync(kFull, mbar_wait_bounded(&sm.o_done[t], (uint32_t)((nt - 1) & 1)));
+        if (ok && nst > 0) {  // out = s_ref * O / l after the last PV; loads warp-wide, stores per row
+            ok = __all_sync(kFull, mbar_wait_bounded(&sm.o_done[t], (uint32_t)((nst - 1) & 1)));
             if (ok) {
                 tc_fence_after();
                 const int tile_rows = rows - kTcRows * t;
@@ -488,87 +500,105 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
             }
         }
     } else if (warp < kTiles * kPfWarps + kWidenThreads / 32) {
-        // ---- widening: codes -> fp16 operands of stage j % kStages ----
+        // ---- widening: the step's two pages -> fp16 codes in stage i & 1 ----
+        // Each thread loads 16-byte pieces of a page's K and V codes straight into registers
+        // (a warp reads 512 contiguous bytes), one page ahead of the one it converts.
         const int w = tid - kTiles * kPfWarps * 32;
-        int j = 0;
-        for (; j < npages; j++) {
-            const int s = j % kStages, cb = j & 1;
-            bool got = true;
-            if (j >= kStages) got = mbar_wait_bounded(&sm.kv_free[s], (uint32_t)((j / kStages - 1) & 1));
-            got = got && mbar_wait_bounded(&sm.code_full[cb], (uint32_t)((j >> 1) & 1));
+        constexpr int kLd = kPageBytes / (16 * kWidenThreads);  // 16-byte pieces per thread, per K and V
+        constexpr int kChunkBytes = RB / 16;                    // bytes of 8 codes
+        uint4 kr[kLd], vr[kLd];
+        auto load_page = [&](int pg) {
+            const size_t off = ((size_t)page_of(pg) * H + h) * kPageBytes;
+#pragma unroll
+            for (int r = 0; r < kLd; r++) {
+                kr[r] = ld_stream_v4(p.k_codes + off + 16 * (w + kWidenThreads * r));
+                vr[r] = ld_stream_v4(p.v_codes + off + 16 * (w + kWidenThreads * r));
+            }
+        };
+        if (npages > 0) load_page(0);
+        for (int i = 0; i < nsteps; i++) {
+            const int s = i & 1;
+            const bool got = i < 2 || mbar_wait_bounded(&sm.kv_free[s], (uint32_t)(((i >> 1) - 1) & 1));
             if (!widen_group_all(got)) {
                 ok = false;
                 break;
             }
-            // keys: 8 16-byte chunks per thread
+#pragma unroll 1
+            for (int hh = 0; hh < 2; hh++) {
+                const int pg = 2 * i + hh;
+                const bool real = pg < npages;  // a page past the last is zero
+                uint4 ck[kLd], cv[kLd];
 #pragma unroll
-            for (int r = 0; r < (kPage * 16) / kWidenThreads; r++) {
-                const int e = w + kWidenThreads * r;
-                const int key = e >> 4, c = e & 15;
-                *reinterpret_cast<uint4 *>(sm.k[s] + sw128(key, 8 * c, kPage)) = codes8<FMT>(sm.kc[cb], key, c);
+                for (int r = 0; r < kLd; r++) {
+                    ck[r] = real ? kr[r] : make_uint4(0u, 0u, 0u, 0u);
+                    cv[r] = real ? vr[r] : make_uint4(0u, 0u, 0u, 0u);
+                }
+                if (pg + 1 < npages) load_page(pg + 1);
+#pragma unroll
+                for (int r = 0; r < kLd; r++) {
+                    const int o = 16 * (w + kWidenThreads * r);  // byte of the page
+                    const int key = kPage * hh + o / RB, c0 = (o % RB) / kChunkBytes;
+                    uint4 kx[16 / kChunkBytes], vx[16 / kChunkBytes];
+                    widen16<FMT>(ck[r], kx);
+                    widen16<FMT>(cv[r], vx);
+#pragma unroll
+                    for (int x = 0; x < 16 / kChunkBytes; x++) {
+                        *reinterpret_cast<uint4 *>(sm.k[s] + k_chunk(key, c0 + x)) = kx[x];
+                        *reinterpret_cast<uint4 *>(sm.v[s] + v_chunk(key, c0 + x)) = vx[x];
+                    }
+                }
             }
-            {  // values: one 8 x 8 block per thread (keys 8 kb .., elements 8 dc ..), transposed
-                const int kb = w & 7, dc = w >> 3;
-                uint4 v8[8], x[8];
-#pragma unroll
-                for (int i = 0; i < 8; i++) v8[i] = codes8<FMT>(sm.vc[cb], 8 * kb + i, dc);
-                transpose8(v8, x);
-#pragma unroll
-                for (int i = 0; i < 8; i++)
-                    *reinterpret_cast<uint4 *>(sm.vt[s] + sw128(8 * dc + i, 8 * kb, kHeadDim)) = x[i];
-            }
-            fence_proxy_async_smem();  // the MMAs read stage s, the next copy overwrites code buffer cb
-            widen_group_sync();
-            if (w == 0 && j + 2 < npages) issue(j + 2);
+            fence_proxy_async_smem();  // the MMAs read stage s through the async proxy
             mbar_arrive(&sm.kv_ready[s]);
-        }
-        if (!ok && w == 0) {  // copies already started land before the CTA's shared memory goes away
-            for (int q = j; q < min(npages, j + 2); q++) mbar_wait_bounded(&sm.code_full[q & 1], (uint32_t)((q >> 1) & 1));
         }
     } else if ((tid & 31) == 0) {
         // ---- the MMA thread ----
-        const int n0 = pages_of(0), n1 = pages_of(1);
-        auto issue_s = [&](int t, int j) {  // S(j) = Q K(j)^T of tile t into its S buffer j & 1
-            const uint32_t aq = smem_addr(sm.q[t]), ak = smem_addr(sm.k[j % kStages]);
+        auto issue_s = [&](int t, int i) {  // S(i) = Q K(i)^T of tile t: 128 x 128 keys, 8 MMAs of K = 16
+            const uint32_t aq = smem_addr(sm.q[t]), ak = smem_addr(sm.k[i & 1]);
 #pragma unroll
             for (int ks = 0; ks < 8; ks++)
-                umma_f16(tmem + 256 * t + 64 * (j & 1), umma_desc(aq + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32),
-                         umma_desc(ak + (ks >> 2) * (kPage * 128) + (ks & 3) * 32), kIdescS, ks > 0);
+                umma_f16(tmem + 256 * t, umma_desc(aq + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32),
+                         umma_desc(ak + (ks >> 2) * (kStepKeys * 128) + (ks & 3) * 32), kIdescS, ks > 0);
             umma_commit(&sm.s_full[t]);
         };
-        auto issue_pv = [&](int t, int j) {  // O += P(j) V(j), P from tensor memory (8 columns per 16 keys)
-            const uint32_t tt = tmem + 256 * t, av = smem_addr(sm.vt[j % kStages]);
+        auto issue_pv = [&](int t, int i) {  // O += P(i) V(i): P from tensor memory, 8 columns per 16 keys
+            const uint32_t tt = tmem + 256 * t, av = smem_addr(sm.v[i & 1]);
 #pragma unroll
-            for (int ks = 0; ks < 4; ks++)
-                umma_f16_ts(tt + 128, tt + 64 * (j & 1) + 8 * ks, umma_desc(av + ks * 32), kIdescO, (j > 0 || ks > 0));
+            for (int ks = 0; ks < 8; ks++)
+                umma_f16_ts(tt + 128, tt + 8 * ks, umma_desc_mn(av + ks * 16 * 128, kStepKeys * 128, 1024), kIdescO,
+                            (i > 0 || ks > 0));
             umma_commit(&sm.o_done[t]);
         };
-        ok = mbar_wait_bounded(&sm.kv_ready[0], 0u);
-        if (ok) {
+        auto wait_ready = [&](int i) {
+            const bool r = mbar_wait_bounded(&sm.kv_ready[i & 1], (uint32_t)((i >> 1) & 1));
             tc_fence_after();
-            issue_s(0, 0);
-            if (n1 > 0) issue_s(1, 0);
-        }
-        for (int j = 0; j < npages && ok; j++) {
+            return r;
+        };
+        ok = wait_ready(0);
+        if (ok)
+            for (int t = 0; t < active; t++) issue_s(t, 0);
+        for (int i = 0; i < nsteps && ok; i++) {
             bool next_ready = false;
-            for (int t = 0; t < kTiles && ok; t++) {
-                const int nt = t == 0 ? n0 : n1;
-                if (j >= nt) continue;
-                ok = mbar_wait_bounded(&sm.p_full[t], (uint32_t)(j & 1));
+            for (int t = 0; t < active && ok; t++) {
+                const int nst = steps_of(t);
+                if (i >= nst) continue;
+                ok = mbar_wait_bounded(&sm.p_full[t], (uint32_t)(i & 1));
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(t, j);
-                if (j + 1 < nt) {
-                    if (!next_ready) {
-                        ok = mbar_wait_bounded(&sm.kv_ready[(j + 1) % kStages], (uint32_t)(((j + 1) / kStages) & 1));
-                        if (!ok) break;
-                        tc_fence_after();
+                issue_pv(t, i);
+                if (t == active - 1) umma_commit(&sm.kv_free[i & 1]);  // the stage's last reader
+                if (i + 1 < nst) {
+                    // S(i + 1) goes where P(i) is: only after PV(i) has read it
+                    ok = mbar_wait_bounded(&sm.o_done[t], (uint32_t)(i & 1));
+                    if (ok && !next_ready) {
+                        ok = wait_ready(i + 1);
                         next_ready = true;
                     }
-                    issue_s(t, j + 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(t, i + 1);
                 }
             }
-            if (ok) umma_commit(&sm.kv_free[j % kStages]);
         }
         umma_commit(&sm.mma_done);  // whatever was issued completes before tensor memory is freed
         if (!mbar_wait_bounded(&sm.mma_done, 0u)) ok = false;
