@@ -501,18 +501,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
         }
     } else if (warp < kTiles * kPfWarps + kWidenThreads / 32) {
         // ---- widening: the step's two pages -> fp16 codes in stage i & 1 ----
-        // Each thread loads 16-byte pieces of a page's K and V codes straight into registers
-        // (a warp reads 512 contiguous bytes), one page ahead of the one it converts.
+        // Each thread loads 16-byte pieces of a page's K and V codes straight into registers,
+        // one page ahead of the one it converts.  Piece r of thread w: key and 16-byte piece of
+        // the key's row chosen so that the 8 threads of a quarter-warp store to 8 different
+        // 16-byte bank groups (int4: 4 keys x 2 pieces; int8, FP8: 2 keys x 4 pieces).
         const int w = tid - kTiles * kPfWarps * 32;
         constexpr int kLd = kPageBytes / (16 * kWidenThreads);  // 16-byte pieces per thread, per K and V
         constexpr int kChunkBytes = RB / 16;                    // bytes of 8 codes
+        auto piece_key = [&](int r) {
+            return RB == 64 ? 4 * (w >> 3) + ((w & 7) >> 1) : 2 * (w >> 3) + ((w & 7) >> 2) + 32 * (r & 1);
+        };
+        auto piece_col = [&](int r) { return RB == 64 ? (w & 1) + 2 * r : (w & 3) + 4 * (r >> 1); };
         uint4 kr[kLd], vr[kLd];
         auto load_page = [&](int pg) {
             const size_t off = ((size_t)page_of(pg) * H + h) * kPageBytes;
 #pragma unroll
             for (int r = 0; r < kLd; r++) {
-                kr[r] = ld_stream_v4(p.k_codes + off + 16 * (w + kWidenThreads * r));
-                vr[r] = ld_stream_v4(p.v_codes + off + 16 * (w + kWidenThreads * r));
+                const int o = piece_key(r) * RB + 16 * piece_col(r);
+                kr[r] = ld_stream_v4(p.k_codes + off + o);
+                vr[r] = ld_stream_v4(p.v_codes + off + o);
             }
         };
         if (npages > 0) load_page(0);
@@ -536,8 +543,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                 if (pg + 1 < npages) load_page(pg + 1);
 #pragma unroll
                 for (int r = 0; r < kLd; r++) {
-                    const int o = 16 * (w + kWidenThreads * r);  // byte of the page
-                    const int key = kPage * hh + o / RB, c0 = (o % RB) / kChunkBytes;
+                    const int key = kPage * hh + piece_key(r), c0 = piece_col(r) * (16 / kChunkBytes);
                     uint4 kx[16 / kChunkBytes], vx[16 / kChunkBytes];
                     widen16<FMT>(ck[r], kx);
                     widen16<FMT>(cv[r], vx);
