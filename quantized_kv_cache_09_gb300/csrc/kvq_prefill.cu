@@ -404,14 +404,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                         if (k0 + x > qpos) sc[x] = -INFINITY;
                 }
             };
-            // pass 1: the row maximum of x = raw * sk over the step
-            float cur_sk[2];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int hh = 0; hh < 2; hh++) {
-                cur_sk[hh] = fmaxf(sk[hh] * sabs, kMinScale);
-                float sc[64];
-                load_half(hh, sc);
+            auto half_max = [&](const float (&sc)[64], float sk_h) {  // max of raw * sk_h, -inf if all masked
                 float m8[8];  // independent maxima, then a tree
 #pragma unroll
                 for (int x = 0; x < 8; x++) m8[x] = sc[x];
@@ -419,8 +412,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                 for (int x = 8; x < 64; x++) m8[x & 7] = fmaxf(m8[x & 7], sc[x]);
                 const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                          fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                if (mraw != -INFINITY) mx = fmaxf(mx, mraw * cur_sk[hh]);
+                return mraw == -INFINITY ? -INFINITY : mraw * sk_h;
+            };
+            const float cur_sk[2] = {fmaxf(sk[0] * sabs, kMinScale), fmaxf(sk[1] * sabs, kMinScale)};
+            // the row maximum over the step: the second half first, then the first half, which is
+            // kept for its P (three loads of 64 columns instead of four)
+            float sc0[64];
+            float mx;
+            {
+                float sc1[64];
+                load_half(1, sc1);
+                mx = half_max(sc1, cur_sk[1]);
             }
+            load_half(0, sc0);
+            mx = fmaxf(mx, half_max(sc0, cur_sk[0]));
             float factor = 1.0f;
             if (i == 0) {
                 m_used = mx;  // key 0 is never masked
@@ -428,14 +433,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                 factor = ex2_approx(m_used - mx);
                 m_used = mx;
             }
-            // pass 2: P * sv / s_ref = 2^(raw * sk - m + log2(sv / s_ref)), one FMA per element
-            // before ex2, as fp16 pairs over columns 32 hh .. 32 hh + 31 (S of those keys is read);
-            // the row sum of P is that sum times s_ref / sv (all-zero values add to l only)
+            // P * sv / s_ref = 2^(raw * sk - m + log2(sv / s_ref)), one FMA per element before
+            // ex2, as fp16 pairs over columns 32 hh .. 32 hh + 31 (S of keys already read: the
+            // first half's P goes over its own first 32 columns, the second half is loaded again
+            // before its P covers the first half's last 32); the row sum of P is that sum times
+            // s_ref / sv (all-zero values add to l only)
             float l_add = 0.0f;
-#pragma unroll
-            for (int hh = 0; hh < 2; hh++) {
-                float sc[64];
-                load_half(hh, sc);
+            auto half_p = [&](int hh, const float (&sc)[64]) {
                 const float ratio = sv[hh] / s_ref;
                 const float off = ratio > 0.0f ? m_used - __log2f(ratio) : m_used;
                 float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -450,6 +454,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                 tmem_st32(lane_tm + 32 * hh, w);
                 const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
                 l_add += ratio > 0.0f ? psum / ratio : psum;
+            };
+            half_p(0, sc0);
+            {
+                float sc1[64];
+                load_half(1, sc1);
+                half_p(1, sc1);
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             // O holds PV(i - 1) (complete before S(i) was issued): rescale the rows whose max moved
