@@ -489,8 +489,10 @@ def measure_chunked_prefill(K, Wm, seed, dev):
         wl.chunk_q_device(q[b * n:(b + 1) * n], b)
     out = torch.empty_like(q)
     cu = torch.arange(0, wl.B * n + 1, n, dtype=torch.int32, device=dev)
+    # the grid's last wave of 256-row units runs as key halves merged in this workspace
+    ws = kvq.prefill_workspace(wl.Hq, wl.B, n, device=dev)
     for _ in range(Wm):
-        kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out)
+        kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out, workspace=ws)
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
     clocks = ClockSampler(dev.index or 0)
@@ -500,7 +502,7 @@ def measure_chunked_prefill(K, Wm, seed, dev):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         ev[i][0].record(stream)
-        kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out)
+        kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out, workspace=ws)
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     clocks.window = (t_wall0, time.time())
@@ -513,7 +515,7 @@ def measure_chunked_prefill(K, Wm, seed, dev):
     e_s.record(stream)
     for _ in range(Ke):
         q.copy_(pin_q, non_blocking=True)
-        kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out)
+        kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out, workspace=ws)
         pin_o.copy_(out, non_blocking=True)
     e_e.record(stream)
     torch.cuda.synchronize(dev)

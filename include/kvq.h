@@ -84,7 +84,7 @@ typedef enum kvq_format {
 #define KVQ_FLAG_TIMEOUT 0x4     /* a bounded wait for a shared-memory copy ran out */
 #define KVQ_FLAG_NO_TAIL 0x8     /* an append into a partial block found no fp16 tail buffer */
 #define KVQ_FLAG_BAD_APPEND 0x10 /* cu_seqlens not increasing, or more new tokens than max_new_tokens */
-#define KVQ_FLAG_BAD_WORKSPACE 0x20 /* a decode workspace was not zero-filled before its first use */
+#define KVQ_FLAG_BAD_WORKSPACE 0x20 /* a decode or prefill workspace was not zero-filled before its first use */
 
 /*
  * The paged cache.  All pointers are caller-owned device memory.
@@ -253,14 +253,36 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const uint16_t *
  *   cu_seqlens_q     device int32 [num_seqs + 1], non-decreasing, cu[0] >= 0
  *   max_q_per_seq    host bound on every n_b (sizes the grid); 0 is a no-op
  *   seq_lens         device int32 [num_seqs], n_b <= seq_lens[b] <= max_blocks_per_seq * 64
+ *   workspace        NULL, or >= kvq_prefill_workspace_bytes(num_q_heads,
+ *                    num_seqs, max_q_per_seq) bytes, 16-byte aligned,
+ *                    zero-filled before its first use (the kernel puts its
+ *                    counters back to zero): the work is cut into units of 256 query rows of
+ *                    one (sequence, query head); with a workspace the units
+ *                    of the grid's last wave (all units when there are fewer
+ *                    than SMs) each run as two CTAs over the two halves of
+ *                    their keys, merged there.  Same results up to rounding
+ *                    order.  Do not share one workspace between calls that
+ *                    may run concurrently.
  * A sequence that breaks a bound is skipped and KVQ_FLAG_BAD_LENGTH set; a
  * block-table entry out of range sets KVQ_FLAG_BAD_PAGE (page 0 is read
- * instead).  Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA.
+ * instead); a workspace that was not zero-filled sets KVQ_FLAG_BAD_WORKSPACE.
+ * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE (too
+ * small or misaligned), KVQ_ERR_CUDA.
  */
 kvq_status kvq_prefill_attention(const kvq_cache *cache, const uint16_t *q, int32_t num_q_heads,
                                  const int32_t *cu_seqlens_q, int64_t total_q, int32_t max_q_per_seq,
                                  const int32_t *block_table, int32_t max_blocks_per_seq, const int32_t *seq_lens,
-                                 int32_t num_seqs, float softmax_scale, uint16_t *out, kvq_stream_t stream);
+                                 int32_t num_seqs, float softmax_scale, uint16_t *out, void *workspace,
+                                 size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * kvq_prefill_workspace_bytes -- bytes of the optional kvq_prefill_attention
+ * workspace for these sizes on the current device (0 when no unit is split
+ * or an argument is not positive).  A workspace sized for the largest call
+ * serves smaller ones only if their count is not larger: size it per call
+ * shape.
+ */
+size_t kvq_prefill_workspace_bytes(int32_t num_q_heads, int32_t num_seqs, int32_t max_q_per_seq);
 
 /*
  * Decode step as a CUDA graph (CUDA Graph instance reuse: "hardware-aware

@@ -3,6 +3,7 @@
 // memory is allocated here; every buffer belongs to the caller.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdint.h>
 
 #include "kvq.h"
 #include "kvq_internal.h"
@@ -171,10 +172,26 @@ kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, i
     return KVQ_OK;
 }
 
+static int device_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+size_t kvq_prefill_workspace_bytes(int32_t num_q_heads, int32_t num_seqs, int32_t max_q_per_seq)
+{
+    if (num_q_heads <= 0 || num_seqs <= 0 || max_q_per_seq <= 0) return 0;
+    const int64_t units = kvq::prefill_units(num_q_heads, num_seqs, max_q_per_seq);
+    return kvq::prefill_workspace_bytes(kvq::prefill_split_units(units, device_sms()));
+}
+
 kvq_status kvq_prefill_attention(const kvq_cache *cache, const uint16_t *q, int32_t num_q_heads,
                                  const int32_t *cu_seqlens_q, int64_t total_q, int32_t max_q_per_seq,
                                  const int32_t *block_table, int32_t max_blocks_per_seq, const int32_t *seq_lens,
-                                 int32_t num_seqs, float softmax_scale, uint16_t *out, kvq_stream_t stream)
+                                 int32_t num_seqs, float softmax_scale, uint16_t *out, void *workspace,
+                                 size_t workspace_bytes, kvq_stream_t stream)
 {
     kvq_status st = check_cache(cache);
     if (st != KVQ_OK) return st;
@@ -205,6 +222,20 @@ kvq_status kvq_prefill_attention(const kvq_cache *cache, const uint16_t *q, int3
     p.max_q = max_q_per_seq;
     p.total_q = total_q;
     p.score_scale = softmax_scale * 1.4426950408889634f;
+    const int64_t units = kvq::prefill_units(num_q_heads, num_seqs, max_q_per_seq);
+    if (units > INT32_MAX / 2) return KVQ_ERR_UNSUPPORTED;
+    p.units_x = (int)(units / ((int64_t)num_q_heads * num_seqs));
+    p.num_full = (int)units;
+    p.partials = nullptr;
+    p.counters = nullptr;
+    if (workspace) {  // split the last wave's units
+        const int64_t split = kvq::prefill_split_units(units, device_sms());
+        if (workspace_bytes < kvq::prefill_workspace_bytes(split) || !aligned16(workspace)) return KVQ_ERR_WORKSPACE;
+        const size_t counters = (size_t)split * sizeof(uint32_t);
+        p.num_full = (int)(units - split);
+        p.counters = static_cast<uint32_t *>(workspace);
+        p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + (counters + 255) / 256 * 256);
+    }
     return from_cuda(kvq::launch_prefill(cache->fmt, p, reinterpret_cast<cudaStream_t>(stream)));
 }
 

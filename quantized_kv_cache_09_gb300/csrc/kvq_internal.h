@@ -73,7 +73,20 @@ struct PrefillParams {
     int num_seqs, num_heads, num_q_heads, group, num_pages, max_blocks, max_q;
     int64_t total_q;
     float score_scale;            // softmax_scale * log2(e)
+    // work units: 256 query rows of one (sequence, query head), units_x of them per pair,
+    // ordered (sequence, query head, x); units from num_full on run as two CTAs over the two
+    // halves of their keys, merged through partials [unit - num_full][half][256][132] floats
+    // and counters [unit - num_full] (zero-filled before the first launch)
+    int units_x, num_full;
+    float *partials;
+    uint32_t *counters;
 };
+
+// prefill work units of a call and the units run as split halves (the grid's last
+// wave, or every unit of a grid smaller than one wave); workspace bytes for them
+int64_t prefill_units(int num_q_heads, int num_seqs, int max_q);
+int64_t prefill_split_units(int64_t units, int num_sms);
+size_t prefill_workspace_bytes(int64_t split_units);
 
 // launch `kernel` with programmatic stream serialization (see pdl_wait)
 template <typename... KArgs, typename... Args>

@@ -80,6 +80,8 @@ constexpr int kWidenThreads = 128;
 constexpr int kTcThreads = kTiles * kPfWarps * 32 + kWidenThreads + 32;
 // tile t: S (and P over its first 64 columns) at columns 256 t + 0..127, O at 256 t + 128..255
 constexpr uint32_t kTmemCols = 256 * kTiles;
+// a split half's partial of one query row: m, l, 2 pad, then s_ref * O (16-byte aligned)
+constexpr int kPartialFloats = 4 + kHeadDim;
 // f32 += f16 x f16, M = 128, N = 128; S: both operands K-major; PV: B (V) MN-major
 constexpr uint32_t kIdescS = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescO = kIdescS | (1u << 16);
@@ -225,6 +227,7 @@ struct alignas(1024) TcSmem {
     uint64_t mma_done;        // every MMA issued complete (commit, at the end)
     float s_ref;
     uint32_t tmem;
+    uint32_t ticket;  // split halves: the count of finished halves this CTA's add saw
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
@@ -277,16 +280,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
     // the swizzle pattern follows address bits: place the tiles on a 1024-byte boundary
     S &sm = *reinterpret_cast<S *>(smem_tc + ((1024u - (smem_addr(smem_tc) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int b = blockIdx.z, hq = blockIdx.y;
+    // CTA -> unit (256 query rows of one (sequence, query head)) and half: units before
+    // num_full run whole; each later unit runs as two CTAs over the two halves of its key
+    // steps, whose partials the second to finish merges
+    const int cta = blockIdx.x;
+    const int unit = cta < p.num_full ? cta : p.num_full + (cta - p.num_full) / 2;
+    const int half = cta < p.num_full ? -1 : (cta - p.num_full) & 1;
     const int H = p.num_heads, Hq = p.num_q_heads;
+    const int ux = unit % p.units_x;
+    const int hq = (unit / p.units_x) % Hq;
+    const int b = unit / (p.units_x * Hq);
     const int h = hq / p.group;
-    const int i0 = blockIdx.x * (kTiles * kTcRows);
+    const int i0 = ux * (kTiles * kTcRows);
 
     const int c0 = p.cu_q[b];
     const int n = p.cu_q[b + 1] - c0;
     const int L = p.seq_lens[b];
     if (n < 0 || n > p.max_q || n > L || L > p.max_blocks * kPage || c0 < 0 || (int64_t)c0 + n > p.total_q) {
-        if (blockIdx.x == 0 && hq == 0 && tid == 0) set_flag(p.status, KVQ_FLAG_BAD_LENGTH);
+        if (ux == 0 && hq == 0 && half <= 0 && tid == 0) set_flag(p.status, KVQ_FLAG_BAD_LENGTH);
         return;
     }
     if (i0 >= n) return;
@@ -300,6 +311,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
     auto steps_of = [&](int t) { return (pages_of(t) + 1) / 2; };
     const int npages = pages_of(active - 1);
     const int nsteps = (npages + 1) / 2;
+    // this CTA's steps [lo, hi): all of them, or one half
+    const int hsplit = (nsteps + 1) / 2;
+    const int lo = half == 1 ? hsplit : 0;
+    const int hi = half == 0 ? hsplit : nsteps;
+    const int nloc = hi - lo;                 // steps widened here
+    const int page_end = min(npages, 2 * hi);  // pages of the range: [2 lo, page_end)
+    auto local_steps = [&](int t) { return max(0, min(steps_of(t), hi) - lo); };
     const int32_t *bt = p.block_table + (int64_t)b * p.max_blocks;
 
     auto page_of = [&](int j) {
@@ -330,7 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
         // the largest value scale over the CTA's pages: P carries sv / s_ref <= 1
         float mx = 0.0f;
-        for (int j = tid; j < npages; j += 32) mx = fmaxf(mx, p.v_scales[(int64_t)page_of(j) * H + h]);
+        for (int j = 2 * lo + tid; j < page_end; j += 32) mx = fmaxf(mx, p.v_scales[(int64_t)page_of(j) * H + h]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
         if (tid == 0) sm.s_ref = mx > 0.0f ? mx : 1.0f;
@@ -352,7 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
     if (warp < kTiles * kPfWarps) {
         // ---- softmax: tile t, one query row per thread (its TMEM lane) ----
         const int t = warp / kPfWarps, row = tid % kTcRows;
-        const int nst = steps_of(t);
+        const int nst = local_steps(t);
         const uint32_t lane_tm = tmem + 256u * t + ((uint32_t)((warp % kPfWarps) * 32) << 16);
         const int tile_qpos0 = qpos0 + kTcRows * t;
         const int qpos = tile_qpos0 + row;  // this row's position in the sequence
@@ -374,11 +392,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
             }
         };
         float sk[2] = {0.0f, 0.0f}, sv[2] = {0.0f, 0.0f};
-        if (nst > 0) load_scales(0, sk, sv);
-        for (int i = 0; i < nst; i++) {
+        if (nst > 0) load_scales(lo, sk, sv);
+        for (int j = 0; j < nst; j++) {
+            const int i = lo + j;  // the step (keys 128 i .. 128 i + 127)
             float nsk[2] = {0.0f, 0.0f}, nsv[2] = {0.0f, 0.0f};
-            if (i + 1 < nst) load_scales(i + 1, nsk, nsv);
-            ok = __all_sync(kFull, mbar_wait_bounded(&sm.s_full[t], (uint32_t)(i & 1)));
+            if (j + 1 < nst) load_scales(i + 1, nsk, nsv);
+            ok = __all_sync(kFull, mbar_wait_bounded(&sm.s_full[t], (uint32_t)(j & 1)));
             if (!ok) break;
             tc_fence_after();
             const bool diag = i * kStepKeys + kStepKeys - 1 > tile_qpos0;  // keys past some row's position
@@ -427,8 +446,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
             load_half(0, sc0);
             mx = fmaxf(mx, half_max(sc0, cur_sk[0]));
             float factor = 1.0f;
-            if (i == 0) {
-                m_used = mx;  // key 0 is never masked
+            if (j == 0) {
+                m_used = mx;  // finite from key 0 on; -inf in a half before some rows' first key
             } else if (mx > m_used + kLazy) {
                 factor = ex2_approx(m_used - mx);
                 m_used = mx;
@@ -441,7 +460,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
             float l_add = 0.0f;
             auto half_p = [&](int hh, const float (&sc)[64]) {
                 const float ratio = sv[hh] / s_ref;
-                const float off = ratio > 0.0f ? m_used - __log2f(ratio) : m_used;
+                // a row with no key yet (m = -inf): every score here is -inf and P is 0
+                const float off = m_used == -INFINITY ? 0.0f : ratio > 0.0f ? m_used - __log2f(ratio) : m_used;
                 float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 uint32_t w[32];
 #pragma unroll
@@ -483,11 +503,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                 sv[hh] = nsv[hh];
             }
         }
-        if (ok && nst > 0) {  // out = s_ref * O / l after the last PV; loads warp-wide, stores per row
+        if (ok && nst > 0)  // O is final after the tile's last PV
             ok = __all_sync(kFull, mbar_wait_bounded(&sm.o_done[t], (uint32_t)((nst - 1) & 1)));
-            if (ok) {
-                tc_fence_after();
-                const int tile_rows = rows - kTcRows * t;
+        if (ok) {
+            tc_fence_after();
+            const int tile_rows = rows - kTcRows * t;
+            if (half < 0 && nst > 0) {  // out = s_ref * O / l; loads warp-wide, stores per row
                 const float inv = s_ref / l_run;
                 uint16_t *dst = p.out + ((int64_t)(c0 + i0 + kTcRows * t + row) * Hq + hq) * kHeadDim;
 #pragma unroll
@@ -507,6 +528,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                     reinterpret_cast<uint4 *>(dst + 16 * c)[0] = o0;
                     reinterpret_cast<uint4 *>(dst + 16 * c)[1] = o1;
                 }
+            } else if (half >= 0) {  // this half's partial of the row: m, l and s_ref * O (zero if no step)
+                float *pr = p.partials + (((int64_t)(unit - p.num_full) * 2 + half) * (kTiles * kTcRows) +
+                                          kTcRows * t + row) * kPartialFloats;
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    float v[16];
+                    if (nst > 0) {
+                        tmem_ld16(lane_tm + 128 + 16 * c, v);
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 16; x++) v[x] = 0.0f;
+                    }
+                    if (row >= tile_rows) continue;
+#pragma unroll
+                    for (int x = 0; x < 16; x += 4)
+                        *reinterpret_cast<float4 *>(pr + 4 + 16 * c + x) =
+                            make_float4(v[x] * s_ref, v[x + 1] * s_ref, v[x + 2] * s_ref, v[x + 3] * s_ref);
+                }
+                if (row < tile_rows) *reinterpret_cast<float4 *>(pr) = make_float4(m_used, l_run, 0.0f, 0.0f);
             }
         }
     } else if (warp < kTiles * kPfWarps + kWidenThreads / 32) {
@@ -532,10 +572,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                 vr[r] = ld_stream_v4(p.v_codes + off + o);
             }
         };
-        if (npages > 0) load_page(0);
-        for (int i = 0; i < nsteps; i++) {
-            const int s = i & 1;
-            const bool got = i < 2 || mbar_wait_bounded(&sm.kv_free[s], (uint32_t)(((i >> 1) - 1) & 1));
+        if (nloc > 0) load_page(2 * lo);
+        for (int j = 0; j < nloc; j++) {
+            const int i = lo + j, s = j & 1;
+            const bool got = j < 2 || mbar_wait_bounded(&sm.kv_free[s], (uint32_t)(((j >> 1) - 1) & 1));
             if (!widen_group_all(got)) {
                 ok = false;
                 break;
@@ -550,7 +590,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                     ck[r] = real ? kr[r] : make_uint4(0u, 0u, 0u, 0u);
                     cv[r] = real ? vr[r] : make_uint4(0u, 0u, 0u, 0u);
                 }
-                if (pg + 1 < npages) load_page(pg + 1);
+                if (pg + 1 < page_end) load_page(pg + 1);
 #pragma unroll
                 for (int r = 0; r < kLd; r++) {
                     const int key = kPage * hh + piece_key(r), c0 = piece_col(r) * (16 / kChunkBytes);
@@ -590,13 +630,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
             tc_fence_after();
             return r;
         };
-        ok = wait_ready(0);
-        if (ok)
-            for (int t = 0; t < active; t++) issue_s(t, 0);
-        for (int i = 0; i < nsteps && ok; i++) {
+        // steps are counted from the CTA's first (stage, barrier phase, accumulate flag)
+        if (nloc > 0) {
+            ok = wait_ready(0);
+            if (ok)
+                for (int t = 0; t < active; t++)
+                    if (local_steps(t) > 0) issue_s(t, 0);
+        }
+        for (int i = 0; i < nloc && ok; i++) {
             bool next_ready = false;
             for (int t = 0; t < active && ok; t++) {
-                const int nst = steps_of(t);
+                const int nst = local_steps(t);
                 if (i >= nst) continue;
                 ok = mbar_wait_bounded(&sm.p_full[t], (uint32_t)(i & 1));
                 if (!ok) break;
@@ -622,8 +666,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
     __syncwarp();
     if (!ok) set_flag(p.status, KVQ_FLAG_TIMEOUT);
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // every partial row of a split half is written
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    if (half < 0) return;
+    // Split halves: count this half on the unit's counter (release of its partials, acquire of
+    // the other's); the second to arrive merges the two partials of each row and puts the
+    // counter back to zero, so it starts every launch at zero once the workspace was zero-filled.
+    uint32_t *counter = p.counters + (unit - p.num_full);
+    if (tid == 0) {
+        __threadfence();
+        uint32_t old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+        if (old > 1) set_flag(p.status, KVQ_FLAG_BAD_WORKSPACE);  // not zero-filled, or an aborted launch
+        if (old == 1) *counter = 0u;
+        sm.ticket = old;
+    }
+    __syncthreads();
+    if (sm.ticket != 1u || warp >= kTiles * kPfWarps || tid >= rows) return;
+    // out = (sum_h 2^(m_h - M) s_ref_h O_h) / (sum_h 2^(m_h - M) l_h), M = max_h m_h; a half
+    // with no key for the row has m = -inf and weight 0 (half 0 always holds key 0)
+    const float *pa = p.partials + ((int64_t)(unit - p.num_full) * 2 * (kTiles * kTcRows) + tid) * kPartialFloats;
+    const float *pb = pa + (int64_t)(kTiles * kTcRows) * kPartialFloats;
+    const float4 ha = __ldcg(reinterpret_cast<const float4 *>(pa));
+    const float4 hb = __ldcg(reinterpret_cast<const float4 *>(pb));
+    const float mm = fmaxf(ha.x, hb.x);
+    const float wa = ha.x == -INFINITY ? 0.0f : ex2_approx(ha.x - mm);
+    const float wb = hb.x == -INFINITY ? 0.0f : ex2_approx(hb.x - mm);
+    const float inv = 1.0f / (ha.y * wa + hb.y * wb);
+    uint16_t *dst = p.out + ((int64_t)(c0 + i0 + tid) * Hq + hq) * kHeadDim;
+#pragma unroll 4
+    for (int c = 0; c < kHeadDim; c += 8) {
+        const float4 a0 = __ldcg(reinterpret_cast<const float4 *>(pa + 4 + c));
+        const float4 a1 = __ldcg(reinterpret_cast<const float4 *>(pa + 8 + c));
+        const float4 b0 = __ldcg(reinterpret_cast<const float4 *>(pb + 4 + c));
+        const float4 b1 = __ldcg(reinterpret_cast<const float4 *>(pb + 8 + c));
+        uint4 o;
+        o.x = f16x2_rn((a0.x * wa + b0.x * wb) * inv, (a0.y * wa + b0.y * wb) * inv);
+        o.y = f16x2_rn((a0.z * wa + b0.z * wb) * inv, (a0.w * wa + b0.w * wb) * inv);
+        o.z = f16x2_rn((a1.x * wa + b1.x * wb) * inv, (a1.y * wa + b1.y * wb) * inv);
+        o.w = f16x2_rn((a1.z * wa + b1.z * wb) * inv, (a1.w * wa + b1.w * wb) * inv);
+        *reinterpret_cast<uint4 *>(dst + c) = o;
+    }
 }
 
 template <int FMT>
@@ -633,15 +716,33 @@ static cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    constexpr int kCtaRows = kTiles * kTcRows;
-    const dim3 grid((unsigned)((p.max_q + kCtaRows - 1) / kCtaRows), (unsigned)p.num_q_heads, (unsigned)p.num_seqs);
+    const int64_t units = (int64_t)p.units_x * p.num_q_heads * p.num_seqs;
+    const dim3 grid((unsigned)(p.num_full + 2 * (units - p.num_full)));
     return launch_plain(prefill_attn_tc_kernel<FMT>, grid, dim3(kTcThreads), smem, s, p);
+}
+
+int64_t prefill_units(int num_q_heads, int num_seqs, int max_q)
+{
+    return (int64_t)((max_q + kTiles * kTcRows - 1) / (kTiles * kTcRows)) * num_q_heads * num_seqs;
+}
+
+// A unit takes about as long as its chain of key steps, so a last wave of r < num_sms units
+// would leave num_sms - r SMs idle for a whole unit; split in halves it takes half as long.
+int64_t prefill_split_units(int64_t units, int num_sms)
+{
+    if (num_sms <= 0) return 0;
+    return units >= num_sms ? units % num_sms : units;
+}
+
+size_t prefill_workspace_bytes(int64_t split_units)
+{
+    const size_t counters = ((size_t)split_units * sizeof(uint32_t) + 255) / 256 * 256;
+    return counters + (size_t)split_units * 2 * (kTiles * kTcRows) * kPartialFloats * sizeof(float);
 }
 
 cudaError_t launch_prefill(int fmt, const PrefillParams &p, cudaStream_t s)
 {
     if (p.num_seqs == 0 || p.max_q == 0) return cudaSuccess;
-    if (p.num_seqs > 65535 || p.num_q_heads > 65535) return cudaErrorInvalidValue;
     if (fmt == KVQ_INT4_B64) return launch_prefill_tc<KVQ_INT4_B64>(p, s);
     if (fmt == KVQ_FP8_E4M3) return launch_prefill_tc<KVQ_FP8_E4M3>(p, s);
     return launch_prefill_tc<KVQ_INT8_PAGE>(p, s);

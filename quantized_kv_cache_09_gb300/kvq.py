@@ -31,7 +31,8 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attention",
            "kvq_decode_workspace_bytes_gqa", "kvq_decode_attention_gqa",
-           "kvq_decode_attention_noalloc", "kvq_prefill_attention", "kvq_step_graph_create", "kvq_step_graph_update",
+           "kvq_decode_attention_noalloc", "kvq_prefill_workspace_bytes", "kvq_prefill_attention",
+           "kvq_step_graph_create", "kvq_step_graph_update",
            "kvq_step_graph_launch", "kvq_step_graph_destroy", "kvq_get_device_status", "kvq_status_string",
            "kvq_version")
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -91,7 +92,10 @@ def lib():
         L.kvq_decode_attention_gqa.restype = ctypes.c_int
         L.kvq_decode_attention_noalloc.argtypes = [cp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp]
         L.kvq_decode_attention_noalloc.restype = ctypes.c_int
-        L.kvq_prefill_attention.argtypes = [cp, vp, i32, vp, i64, i32, vp, i32, vp, i32, ctypes.c_float, vp, vp]
+        L.kvq_prefill_workspace_bytes.argtypes = [i32, i32, i32]
+        L.kvq_prefill_workspace_bytes.restype = sz
+        L.kvq_prefill_attention.argtypes = [cp, vp, i32, vp, i64, i32, vp, i32, vp, i32, ctypes.c_float, vp, vp, sz,
+                                            vp]
         L.kvq_prefill_attention.restype = ctypes.c_int
         ap = ctypes.POINTER(kvq_step_args)
         L.kvq_step_graph_create.argtypes = [cp, ap, i32, ctypes.POINTER(vp)]
@@ -231,12 +235,26 @@ def kvq_decode_attention_noalloc(cache, q, block_table, seq_lens, softmax_scale,
                                               _ptr(out), _stream(stream, q.device)), "kvq_decode_attention_noalloc")
 
 
+def kvq_prefill_workspace_bytes(num_q_heads, num_seqs, max_q_per_seq):
+    """Bytes of the optional kvq_prefill_attention workspace for these sizes
+    on the current device (0: nothing to split)."""
+    return int(lib().kvq_prefill_workspace_bytes(int(num_q_heads), int(num_seqs), int(max_q_per_seq)))
+
+
+def prefill_workspace(num_q_heads, num_seqs, max_q_per_seq, device="cuda"):
+    """A zero-filled workspace for kvq_prefill_attention (reusable by calls of
+    at most these sizes, one call at a time)."""
+    n = kvq_prefill_workspace_bytes(num_q_heads, num_seqs, max_q_per_seq)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+
+
 def kvq_prefill_attention(cache, q, cu_seqlens_q, max_q_per_seq, block_table, seq_lens, softmax_scale, out,
-                          stream=None):
+                          workspace=None, stream=None):
     """out fp16 [total][Hq][128] = causal attention of the chunk queries q fp16
     [total][Hq][128] over the cache: sequence b's chunk is its last
     cu[b+1] - cu[b] tokens (already appended); query i sits at position
-    seq_lens[b] - n_b + i.  Hq = g * cache heads."""
+    seq_lens[b] - n_b + i.  Hq = g * cache heads.  workspace (optional,
+    prefill_workspace): the grid's last wave runs as key halves merged there."""
     _cuda(q, torch.float16, "q")
     _cuda(out, torch.float16, "out")
     for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (block_table, "block_table"), (seq_lens, "seq_lens")):
@@ -248,6 +266,8 @@ def kvq_prefill_attention(cache, q, cu_seqlens_q, max_q_per_seq, block_table, se
     _check(lib().kvq_prefill_attention(ctypes.byref(cache.struct), _ptr(q), q.shape[1], _ptr(cu_seqlens_q),
                                        q.shape[0], int(max_q_per_seq), _ptr(block_table), block_table.shape[1],
                                        _ptr(seq_lens), B, float(softmax_scale), _ptr(out),
+                                       None if workspace is None else _ptr(workspace),
+                                       0 if workspace is None else workspace.numel() * workspace.element_size(),
                                        _stream(stream, q.device)), "kvq_prefill_attention")
 
 

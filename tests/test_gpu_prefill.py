@@ -35,13 +35,30 @@ def _oracle_cache(wl):
     return kc, vc, ks, vs
 
 
-def _run(dw, chunks, q_bits, max_q=None):
+def _counters_zero(ws):
+    """The workspace opens with one uint32 count per split unit (padded to 256
+    bytes), then 2 x 256 x 132 floats of partials per unit; the counts must be
+    back at zero after a call."""
+    per_unit = 2 * 256 * 132 * 4
+    n = ws.numel()
+    units = next(u for u in range(1, n // per_unit + 1) if -(-4 * u // 256) * 256 + u * per_unit == n)
+    return not ws[:-(-4 * units // 256) * 256].any()
+
+
+def _run(dw, chunks, q_bits, max_q=None, split=False):
+    """split: with a workspace, so the units of the grid's last wave (here every
+    unit: these grids are smaller than one wave) run as two key halves merged
+    through it."""
     cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
     q = torch.from_numpy(q_bits.view(np.float16)).cuda()
     out = torch.full_like(q, float("nan"))
-    kvq.kvq_prefill_attention(dw.cache, q, torch.from_numpy(cu).cuda(), max(chunks) if max_q is None else max_q,
-                              dw.block_table, dw.lens, dw.softmax_scale, out)
+    mq = max(chunks) if max_q is None else max_q
+    ws = kvq.prefill_workspace(q.shape[1], len(chunks), mq) if split else None
+    kvq.kvq_prefill_attention(dw.cache, q, torch.from_numpy(cu).cuda(), mq, dw.block_table, dw.lens,
+                              dw.softmax_scale, out, workspace=ws)
     torch.cuda.synchronize()
+    if split:
+        assert _counters_zero(ws)
     return cu, out.float().cpu().numpy().astype(np.float64)
 
 
@@ -60,8 +77,9 @@ def _check(wl, oc, cu, q_bits, got):
     return worst
 
 
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE, kvq.KVQ_FP8_E4M3])
-def test_prefill_ragged_chunks(cuda_ok, fmt):
+def test_prefill_ragged_chunks(cuda_ok, fmt, split):
     """Chunks of 1, 64, 65, 37, 130, 64, 200 and 300 tokens after histories of
     0 to 2000 tokens (query tiles and pages cut anywhere), and an empty chunk
     whose output rows do not exist."""
@@ -73,13 +91,14 @@ def test_prefill_ragged_chunks(cuda_ok, fmt):
     dw.prefill()
     oc = _oracle_cache(wl)
     q = (np.random.default_rng(62).standard_normal((sum(chunks), 4, D))).astype(np.float16).view(np.uint16)
-    cu, got = _run(dw, chunks, q)
+    cu, got = _run(dw, chunks, q, split=split)
     assert np.isfinite(got).all()
     _check(wl, oc, cu, q, got)
     assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
 
 
-def test_prefill_grouped_heads(cuda_ok):
+@pytest.mark.parametrize("split", [False, True])
+def test_prefill_grouped_heads(cuda_ok, split):
     """8 query heads over 2 cache heads (g = 4): query head i reads cache head i // 4."""
     hist, chunks = [300, 0, 64], [100, 129, 64]
     lens = [h + n for h, n in zip(hist, chunks)]
@@ -87,7 +106,7 @@ def test_prefill_grouped_heads(cuda_ok):
     dw = DeviceWorkload(wl)
     dw.prefill()
     q = (np.random.default_rng(64).standard_normal((sum(chunks), 8, D)) * 2).astype(np.float16).view(np.uint16)
-    cu, got = _run(dw, chunks, q)
+    cu, got = _run(dw, chunks, q, split=split)
     _check(wl, _oracle_cache(wl), cu, q, got)
 
 
@@ -109,12 +128,20 @@ def test_prefill_bad_lengths_are_flagged(cuda_ok):
                                   torch.tensor([0, 4, 4], dtype=torch.int32, device="cuda"), 4, dw.block_table,
                                   dw.lens, SM, torch.zeros((4, 3, D), dtype=torch.float16, device="cuda"))
     assert e.value.status == 1   # 3 query heads over 2 cache heads
+    small = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    q2 = torch.zeros((130, 2, D), dtype=torch.float16, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_prefill_attention(dw.cache, q2, torch.tensor([0, 60, 130], dtype=torch.int32, device="cuda"), 70,
+                                  dw.block_table, dw.lens, SM, torch.zeros_like(q2), workspace=small)
+    assert e.value.status == 6   # workspace too small
 
 
-def test_prefill_full_size_sampled(cuda_ok):
+@pytest.mark.parametrize("split", [False, True])
+def test_prefill_full_size_sampled(cuda_ok, split):
     """The chunked-prefill workload (B=8, H=32, the last 512 of 8192 tokens):
     sampled (sequence, query, head) outputs against the oracle, one query at a
-    time over its causal prefix."""
+    time over its causal prefix; with a workspace (as benchmarked) the grid's
+    last wave runs as key halves."""
     wl = W.make_workload(8)
     dw = DeviceWorkload(wl)
     dw.prefill(max_tokens_per_call=1 << 16)
@@ -124,9 +151,12 @@ def test_prefill_full_size_sampled(cuda_ok):
         wl.chunk_q_device(q[b * n:(b + 1) * n], b)
     out = torch.empty_like(q)
     cu = torch.arange(0, wl.B * n + 1, n, dtype=torch.int32, device="cuda")
-    kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out)
+    ws = kvq.prefill_workspace(wl.Hq, wl.B, n) if split else None
+    kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out, workspace=ws)
     torch.cuda.synchronize()
     assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
+    if split:
+        assert _counters_zero(ws)
     got = out.float().cpu().numpy()
     rng = np.random.default_rng(67)
     for b, h in synth_sample_heads(wl.B, wl.H, 4, seed=5):
@@ -144,8 +174,9 @@ def test_prefill_full_size_sampled(cuda_ok):
             assert err <= TOL, (b, h, i, err)
 
 
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_FP8_E4M3])
-def test_prefill_zero_pages_and_negative_scale(cuda_ok, fmt):
+def test_prefill_zero_pages_and_negative_scale(cuda_ok, fmt, split):
     """A page whose keys and values are all zero (scales 0) inside the causal
     range, and a negative softmax scale: both as the oracle defines them."""
     H, L, n = 2, 200, 100
@@ -175,8 +206,9 @@ def test_prefill_zero_pages_and_negative_scale(cuda_ok, fmt):
     vmax = orc.value_absmax(fmt, vc, vs, bt_np, np.array([L]), H, D)
     for sm_scale in (SM, -0.05):
         out = torch.full((n, H, D), float("nan"), dtype=torch.float16, device="cuda")
+        ws = kvq.prefill_workspace(H, 1, n) if split else None
         kvq.kvq_prefill_attention(cache, torch.from_numpy(q).cuda(), torch.from_numpy(cu).cuda(), n, bt, lens,
-                                  sm_scale, out)
+                                  sm_scale, out, workspace=ws)
         torch.cuda.synchronize()
         assert kvq.kvq_get_device_status(cache) == (0, 0)
         ref = orc.prefill_attention(fmt, kc, vc, ks, vs, bt_np, np.array([L]), cu, q.view(np.uint16),
