@@ -230,6 +230,14 @@ struct alignas(1024) TcSmem {
     uint32_t ticket;  // split halves: the count of finished halves this CTA's add saw
 };
 
+// a * b + c on binary32 pairs, each rounded once
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -462,17 +470,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                 const float ratio = sv[hh] / s_ref;
                 // a row with no key yet (m = -inf): every score here is -inf and P is 0
                 const float off = m_used == -INFINITY ? 0.0f : ratio > 0.0f ? m_used - __log2f(ratio) : m_used;
-                float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                // the exponent arguments and the partial sums two keys at a time (f32x2)
+                const uint64_t sk2 = pk2(cur_sk[hh], cur_sk[hh]), noff2 = pk2(-off, -off);
+                uint64_t ps2[2] = {pk2(0.0f, 0.0f), pk2(0.0f, 0.0f)};
                 uint32_t w[32];
 #pragma unroll
                 for (int c = 0; c < 32; c++) {
-                    const float p0 = ex2_approx(fmaf(sc[2 * c], cur_sk[hh], -off));
-                    const float p1 = ex2_approx(fmaf(sc[2 * c + 1], cur_sk[hh], -off));
-                    ps[c & 3] += p0 + p1;
+                    float x0, x1;
+                    upk2(fma2(pk2(sc[2 * c], sc[2 * c + 1]), sk2, noff2), x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    ps2[c & 1] = add2(ps2[c & 1], pk2(p0, p1));
                     w[c] = f16x2_rn(p0, p1);
                 }
                 tmem_st32(lane_tm + 32 * hh, w);
-                const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                float pa, pb, pc, pd;
+                upk2(ps2[0], pa, pb);
+                upk2(ps2[1], pc, pd);
+                const float psum = (pa + pb) + (pc + pd);
                 l_add += ratio > 0.0f ? psum / ratio : psum;
             };
             half_p(0, sc0);
