@@ -230,6 +230,14 @@ struct alignas(1024) TcSmem {
     uint32_t ticket;  // split halves: the count of finished halves this CTA's add saw
 };
 
+// the largest of three binary32 values (one instruction)
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // a * b + c on binary32 pairs, each rounded once
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
 {
@@ -432,13 +440,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                 }
             };
             auto half_max = [&](const float (&sc)[64], float sk_h) {  // max of raw * sk_h, -inf if all masked
-                float m8[8];  // independent maxima, then a tree
+                float m8[8];  // independent maxima of 8 scores each (three-input max), then a tree
 #pragma unroll
-                for (int x = 0; x < 8; x++) m8[x] = sc[x];
-#pragma unroll
-                for (int x = 8; x < 64; x++) m8[x & 7] = fmaxf(m8[x & 7], sc[x]);
-                const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                for (int x = 0; x < 8; x++) {
+                    const float *v = sc + 8 * x;
+                    m8[x] = max3(max3(v[0], v[1], v[2]), max3(v[3], v[4], v[5]), fmaxf(v[6], v[7]));
+                }
+                const float mraw = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 return mraw == -INFINITY ? -INFINITY : mraw * sk_h;
             };
             const float cur_sk[2] = {fmaxf(sk[0] * sabs, kMinScale), fmaxf(sk[1] * sabs, kMinScale)};
