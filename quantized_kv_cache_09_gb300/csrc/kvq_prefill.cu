@@ -10,11 +10,13 @@
 // hq / g.  Keys go in steps of 128 (two pages).  The CTA's warps split into
 // roles that hand work over through mbarriers:
 //   * 4 widening warps load the K and V codes of the cache head straight from
-//     global memory into registers (16-byte pieces, one page ahead) and widen
+//     global memory into registers (16-byte pieces; V while K is converted,
+//     the next step's K while V is converted) and widen
 //     them once, for both tiles, to fp16 codes (exact: integers or E4M3
 //     values) in shared memory, 128-byte swizzled, keys x elements; the same
 //     bytes are the K-major B operand of S and the MN-major B operand of PV.
-//     Two stages; the scales stay out of the fp16 operands;
+//     Two stages, K and V of each handed over and released separately; the
+//     scales stay out of the fp16 operands;
 //   * 1 MMA thread: per tile, S = Q K^T (M = 128, N = 128 keys, 8 MMAs of
 //     K = 16) into tensor memory and O += P V (M = 128, N = 128, 8 MMAs) with
 //     P read from tensor memory where S was;
@@ -219,8 +221,10 @@ struct alignas(1024) TcSmem {
     uint8_t q[kTiles][kTcRows * kHeadDim * 2];  // 32 KB per tile: query rows x elements (K-major)
     uint8_t k[2][kStepKeys * kHeadDim * 2];     // 32 KB per stage: keys x elements (K-major)
     uint8_t v[2][kStepKeys * kHeadDim * 2];     // 32 KB per stage: keys x elements (MN-major B of PV)
-    uint64_t kv_ready[2];   // a step's widened K and V written (every widening thread)
-    uint64_t kv_free[2];    // the MMAs reading a stage complete (commit)
+    uint64_t k_ready[2];    // a step's widened K written (every widening thread)
+    uint64_t v_ready[2];    // a step's widened V written (every widening thread)
+    uint64_t k_free[2];     // the S MMAs reading a stage's K complete (commit)
+    uint64_t v_free[2];     // the PV MMAs reading a stage's V complete (commit)
     uint64_t s_full[kTiles];  // S of a tile's step complete (commit); PV of the step before too
     uint64_t p_full[kTiles];  // P of a tile's step in tensor memory, O rescaled (every row of the tile)
     uint64_t o_done[kTiles];  // O += P V of a tile's step complete (commit)
@@ -264,20 +268,18 @@ __device__ __forceinline__ bool widen_group_all(bool v)
     return r != 0;
 }
 
-// byte offset of the 8 elements 8c .. 8c + 7 of key `key` in a stage's K tile (keys x
-// elements, K-major) and V tile (the same values MN-major: 64-element atoms of 128 keys)
+// byte offset of the 8 elements 8c .. 8c + 7 of key `key` in a stage's K or V tile: keys x
+// elements in 64-element atoms of 128 keys, 128-byte swizzled -- the K-major layout of K for
+// S and, read with the MN-major descriptor, of V for PV
 __device__ __forceinline__ uint32_t k_chunk(int key, int c) { return sw128(key, 8 * c, kStepKeys); }
-__device__ __forceinline__ uint32_t v_chunk(int key, int c)
-{
-    return (uint32_t)((c >> 3) * (kStepKeys * 128) + key * 128 + (((c & 7) ^ (key & 7)) << 4));
-}
 
 }  // namespace
 
 // Roles, per step i of 128 keys (pages 2i and 2i + 1); all hand-offs are mbarriers:
-//   widening warps  wait for stage i & 1 to be free, widen the codes of both pages
-//                   (already in registers) into it -- a page past the last is zero --
-//                   loading each next page's codes while converting the current one;
+//   widening warps  widen the K codes of both pages (already in registers) into stage
+//                   i & 1 once its K is free, then the V codes once its V is free -- a
+//                   page past the last is zero -- loading V while K is converted and the
+//                   next step's K while V is converted;
 //   MMA thread      per tile: once P(i) is in tensor memory, O += P(i) V(i); once
 //                   that is complete (P(i) lives where S goes), S(i + 1) = Q K(i + 1)^T;
 //                   the last reader of a stage releases it;
@@ -347,8 +349,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
 
     if (tid == 0) {
         for (int s = 0; s < 2; s++) {
-            mbar_init(&sm.kv_ready[s], kWidenThreads);
-            mbar_init(&sm.kv_free[s], 1);
+            mbar_init(&sm.k_ready[s], kWidenThreads);
+            mbar_init(&sm.v_ready[s], kWidenThreads);
+            mbar_init(&sm.k_free[s], 1);
+            mbar_init(&sm.v_free[s], 1);
         }
         for (int t = 0; t < kTiles; t++) {
             mbar_init(&sm.s_full[t], 1);
@@ -573,10 +577,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
         }
     } else if (warp < kTiles * kPfWarps + kWidenThreads / 32) {
         // ---- widening: the step's two pages -> fp16 codes in stage i & 1 ----
-        // Each thread loads 16-byte pieces of a page's K and V codes straight into registers,
-        // one page ahead of the one it converts.  Piece r of thread w: key and 16-byte piece of
-        // the key's row chosen so that the 8 threads of a quarter-warp store to 8 different
-        // 16-byte bank groups (int4: 4 keys x 2 pieces; int8, FP8: 2 keys x 4 pieces).
+        // K and V of a stage are widened and released separately: S needs a step's K (its
+        // buffer free once the S two steps back completed), PV its V (free once that step's
+        // PV completed).  Each thread loads 16-byte pieces of the step's two pages straight
+        // into registers -- V while K is converted, the next step's K while V is converted.
+        // Piece r of thread w: key and 16-byte piece of the key's row chosen so that the 8
+        // threads of a quarter-warp store to 8 different 16-byte bank groups (int4: 4 keys x
+        // 2 pieces; int8, FP8: 2 keys x 4 pieces).
         const int w = tid - kTiles * kPfWarps * 32;
         constexpr int kLd = kPageBytes / (16 * kWidenThreads);  // 16-byte pieces per thread, per K and V
         constexpr int kChunkBytes = RB / 16;                    // bytes of 8 codes
@@ -584,50 +591,59 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
             return RB == 64 ? 4 * (w >> 3) + ((w & 7) >> 1) : 2 * (w >> 3) + ((w & 7) >> 2) + 32 * (r & 1);
         };
         auto piece_col = [&](int r) { return RB == 64 ? (w & 1) + 2 * r : (w & 3) + 4 * (r >> 1); };
-        uint4 kr[kLd], vr[kLd];
-        auto load_page = [&](int pg) {
+        uint4 kr[2][kLd], vr[2][kLd];  // the step's two pages (zero past the last page)
+        auto load = [&](const uint8_t *codes, int pg, uint4 (&d)[kLd]) {
+            if (pg >= npages) {
+#pragma unroll
+                for (int r = 0; r < kLd; r++) d[r] = make_uint4(0u, 0u, 0u, 0u);
+                return;
+            }
             const size_t off = ((size_t)page_of(pg) * H + h) * kPageBytes;
 #pragma unroll
-            for (int r = 0; r < kLd; r++) {
-                const int o = piece_key(r) * RB + 16 * piece_col(r);
-                kr[r] = ld_stream_v4(p.k_codes + off + o);
-                vr[r] = ld_stream_v4(p.v_codes + off + o);
-            }
+            for (int r = 0; r < kLd; r++) d[r] = ld_stream_v4(codes + off + piece_key(r) * RB + 16 * piece_col(r));
         };
-        if (nloc > 0) load_page(2 * lo);
+        // the step's two pages -> dst (keys x elements; the same bytes for K and V)
+        auto widen_step = [&](uint8_t *dst, const uint4 (&src)[2][kLd]) {
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++)
+#pragma unroll
+                for (int r = 0; r < kLd; r++) {
+                    const int key = kPage * hh + piece_key(r), c0 = piece_col(r) * (16 / kChunkBytes);
+                    uint4 x[16 / kChunkBytes];
+                    widen16<FMT>(src[hh][r], x);
+#pragma unroll
+                    for (int xx = 0; xx < 16 / kChunkBytes; xx++)
+                        *reinterpret_cast<uint4 *>(dst + k_chunk(key, c0 + xx)) = x[xx];
+                }
+        };
+        if (nloc > 0) {
+            load(p.k_codes, 2 * lo, kr[0]);
+            load(p.k_codes, 2 * lo + 1, kr[1]);
+        }
         for (int j = 0; j < nloc; j++) {
             const int i = lo + j, s = j & 1;
-            const bool got = j < 2 || mbar_wait_bounded(&sm.kv_free[s], (uint32_t)(((j >> 1) - 1) & 1));
+            load(p.v_codes, 2 * i, vr[0]);
+            load(p.v_codes, 2 * i + 1, vr[1]);
+            bool got = j < 2 || mbar_wait_bounded(&sm.k_free[s], (uint32_t)(((j >> 1) - 1) & 1));
             if (!widen_group_all(got)) {
                 ok = false;
                 break;
             }
-#pragma unroll 1
-            for (int hh = 0; hh < 2; hh++) {
-                const int pg = 2 * i + hh;
-                const bool real = pg < npages;  // a page past the last is zero
-                uint4 ck[kLd], cv[kLd];
-#pragma unroll
-                for (int r = 0; r < kLd; r++) {
-                    ck[r] = real ? kr[r] : make_uint4(0u, 0u, 0u, 0u);
-                    cv[r] = real ? vr[r] : make_uint4(0u, 0u, 0u, 0u);
-                }
-                if (pg + 1 < page_end) load_page(pg + 1);
-#pragma unroll
-                for (int r = 0; r < kLd; r++) {
-                    const int key = kPage * hh + piece_key(r), c0 = piece_col(r) * (16 / kChunkBytes);
-                    uint4 kx[16 / kChunkBytes], vx[16 / kChunkBytes];
-                    widen16<FMT>(ck[r], kx);
-                    widen16<FMT>(cv[r], vx);
-#pragma unroll
-                    for (int x = 0; x < 16 / kChunkBytes; x++) {
-                        *reinterpret_cast<uint4 *>(sm.k[s] + k_chunk(key, c0 + x)) = kx[x];
-                        *reinterpret_cast<uint4 *>(sm.v[s] + v_chunk(key, c0 + x)) = vx[x];
-                    }
-                }
-            }
+            widen_step(sm.k[s], kr);
             fence_proxy_async_smem();  // the MMAs read stage s through the async proxy
-            mbar_arrive(&sm.kv_ready[s]);
+            mbar_arrive(&sm.k_ready[s]);
+            if (j + 1 < nloc) {
+                load(p.k_codes, 2 * i + 2, kr[0]);
+                load(p.k_codes, 2 * i + 3, kr[1]);
+            }
+            got = j < 2 || mbar_wait_bounded(&sm.v_free[s], (uint32_t)(((j >> 1) - 1) & 1));
+            if (!widen_group_all(got)) {
+                ok = false;
+                break;
+            }
+            widen_step(sm.v[s], vr);
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.v_ready[s]);
         }
     } else if ((tid & 31) == 0) {
         // ---- the MMA thread ----
@@ -647,38 +663,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                             (i > 0 || ks > 0));
             umma_commit(&sm.o_done[t]);
         };
-        auto wait_ready = [&](int i) {
-            const bool r = mbar_wait_bounded(&sm.kv_ready[i & 1], (uint32_t)((i >> 1) & 1));
-            tc_fence_after();
-            return r;
-        };
-        // steps are counted from the CTA's first (stage, barrier phase, accumulate flag)
+        // steps are counted from the CTA's first (stage, barrier phase, accumulate flag); the
+        // last tile (which has every step) issues a step's last S and last PV, after which
+        // the stage's K, V are released
         if (nloc > 0) {
-            ok = wait_ready(0);
-            if (ok)
+            ok = mbar_wait_bounded(&sm.k_ready[0], 0u);
+            tc_fence_after();
+            if (ok) {
                 for (int t = 0; t < active; t++)
                     if (local_steps(t) > 0) issue_s(t, 0);
+                umma_commit(&sm.k_free[0]);
+            }
         }
         for (int i = 0; i < nloc && ok; i++) {
-            bool next_ready = false;
+            bool v_seen = false, k_seen = false;
             for (int t = 0; t < active && ok; t++) {
                 const int nst = local_steps(t);
                 if (i >= nst) continue;
                 ok = mbar_wait_bounded(&sm.p_full[t], (uint32_t)(i & 1));
+                if (ok && !v_seen) {
+                    ok = mbar_wait_bounded(&sm.v_ready[i & 1], (uint32_t)((i >> 1) & 1));
+                    v_seen = true;
+                }
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(t, i);
-                if (t == active - 1) umma_commit(&sm.kv_free[i & 1]);  // the stage's last reader
+                if (t == active - 1) umma_commit(&sm.v_free[i & 1]);
                 if (i + 1 < nst) {
                     // S(i + 1) goes where P(i) is: only after PV(i) has read it
                     ok = mbar_wait_bounded(&sm.o_done[t], (uint32_t)(i & 1));
-                    if (ok && !next_ready) {
-                        ok = wait_ready(i + 1);
-                        next_ready = true;
+                    if (ok && !k_seen) {
+                        ok = mbar_wait_bounded(&sm.k_ready[(i + 1) & 1], (uint32_t)(((i + 1) >> 1) & 1));
+                        k_seen = true;
                     }
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(t, i + 1);
+                    if (t == active - 1) umma_commit(&sm.k_free[(i + 1) & 1]);
                 }
             }
         }
