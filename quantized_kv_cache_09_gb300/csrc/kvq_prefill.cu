@@ -282,12 +282,14 @@ __device__ __forceinline__ uint32_t k_chunk(int key, int c) { return sw128(key, 
 //                   next step's K while V is converted;
 //   MMA thread      per tile: once P(i) is in tensor memory, O += P(i) V(i); once
 //                   that is complete (P(i) lives where S goes), S(i + 1) = Q K(i + 1)^T;
-//                   the last reader of a stage releases it;
+//                   a step's last S releases the stage's K, its last PV the V;
 //   softmax warps   per tile (one thread per query row): wait S(i) (which also means
 //                   PV(i - 1) is complete), row max over the 128 keys, lazy online
 //                   softmax, P(i) into tensor memory over S(i), rescale O if a row's
 //                   max moved, hand P(i) to the MMA thread.
 // While one tile's rows are in the softmax, the tensor cores work on the other tile.
+// A CTA runs all key steps of its unit, or one half of them when the unit is split
+// (the grid's last wave); then its rows' partials are merged by the second half to end.
 template <int FMT>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillParams p)
 {
