@@ -176,7 +176,13 @@ size_t kvq_decode_workspace_bytes(kvq_format fmt, int32_t num_heads, int32_t hea
  *                    cudaMemsetAsync); every call that completes leaves it
  *                    ready for the next one.  After a call that set a
  *                    KVQ_FLAG_* bit, zero it again.  Do not share one
- *                    workspace between calls that may run concurrently
+ *                    workspace between calls that may run concurrently.
+ *                    The split counters in it carry a tag of the call, so a
+ *                    workspace that was not zero-filled, or that a call cut
+ *                    short left non-zero, is reported (KVQ_FLAG_BAD_WORKSPACE)
+ *                    by the next call that uses it -- except a replay of the
+ *                    same captured graph, which reuses its tag.  The outputs
+ *                    of a call that set any KVQ_FLAG_* bit are undefined
  * Launch: with programmatic dependent launch, the kernel starts while the
  * previous kernel of the stream finishes and reads seq_lens and block_table
  * before waiting for it (the codes, scales, q and out only after).  No kvq_*
@@ -221,19 +227,22 @@ kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, i
  * that cannot afford the device-wide synchronisation cudaMalloc / cudaFree
  * may cause.  It allocates nothing.
  *
- * The scratch is one fixed array of KVQ_NOALLOC_SCRATCH_BYTES (4 MiB) of
+ * The scratch is one fixed array of KVQ_NOALLOC_SCRATCH_BYTES (16 MiB) of
  * device memory inside the library; every GPU that loads the library holds it
  * until the process exits.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress, with that device current) and keeps
  * it, so make that first call before any stream capture.  A device whose split
- * grid needs more scratch than the array (more than about 330 SMs' worth of
- * partials) gets KVQ_ERR_WORKSPACE.  Every call uses the same array and it
- * keeps the last call's contents: calls that may overlap on the GPU (other
- * streams, other threads) race on it, so the caller must serialise them.
- * Nothing in it has to start at zero.  Arguments, results and other errors are
- * those of kvq_decode_attention.
+ * grid needs more scratch than the array (about 250 SMs' worth of split
+ * partials; a 152-SM GB300 needs 9.7 MB) gets KVQ_ERR_WORKSPACE.  Every call
+ * uses the same array and it keeps the last call's contents: calls that may
+ * overlap on the GPU (other streams, other threads) race on it, so the caller
+ * must serialise them.  The split's counters in the array must be zero when a
+ * launch starts: each call clears them first on `stream` (a memset of about
+ * 100 KB, no allocation), so a call that was cut short (a bounded wait that
+ * ran out) does not spoil later ones.  Arguments, results and other errors
+ * are those of kvq_decode_attention.
  */
-#define KVQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const uint16_t *q, const int32_t *block_table,
                                         int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
                                         float softmax_scale, uint16_t *out, kvq_stream_t stream);

@@ -5,8 +5,11 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kvq.h"
 #include "kvq_internal.h"
+#include "kvq_testing.h"
 
 namespace {
 
@@ -29,7 +32,20 @@ kvq_status check_cache(const kvq_cache *c)
     return KVQ_OK;
 }
 
+// test hook state (kvq_testing.h): read when a decode launch is set up
+std::atomic<uint32_t> g_test_wait_limit_us{0};
+std::atomic<int32_t> g_test_skip_chunk{-1};
+
 }  // namespace
+
+namespace kvq {
+void decode_test_settings(unsigned long long *wait_limit_ns, int32_t *skip_chunk)
+{
+    const uint32_t us = g_test_wait_limit_us.load(std::memory_order_relaxed);
+    *wait_limit_ns = us ? (unsigned long long)us * 1000ull : kvq::kDecodeWaitLimitNs;
+    *skip_chunk = g_test_skip_chunk.load(std::memory_order_relaxed);
+}
+}  // namespace kvq
 
 extern "C" {
 
@@ -134,6 +150,8 @@ kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, i
     if (st != KVQ_OK) return st;
     if (num_seqs < 0 || max_blocks_per_seq <= 0 || !isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
     if (num_q_heads <= 0 || num_q_heads % cache->num_heads) return KVQ_ERR_INVALID_ARG;
+    // the split counts units of a (sequence, head) in 24 bits: at most 2^22 pages of 64 tokens
+    if (max_blocks_per_seq > (1 << 22)) return KVQ_ERR_UNSUPPORTED;
     const int g = group_of(cache->fmt, cache->num_heads, num_q_heads);
     if (g == 0) return KVQ_ERR_UNSUPPORTED;
     if (num_seqs == 0) return KVQ_OK;
@@ -141,7 +159,6 @@ kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, i
     const size_t need = kvq::decode_workspace_bytes(cache->fmt, g);
     if (need == 0) return KVQ_ERR_CUDA;
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
-    const int grid_warps = kvq::decode_grid_warps(cache->fmt);
     kvq::DecodeParams p;
     p.k_codes = cache->k_codes;
     p.v_codes = cache->v_codes;
@@ -153,10 +170,9 @@ kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, i
     p.max_blocks = max_blocks_per_seq;
     p.score_scale = softmax_scale * 1.4426950408889634f;
     p.group = g;
-    p.partials = reinterpret_cast<float *>(workspace);
-    p.pieces = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(workspace) +
-                                                      (size_t)grid_warps * 2 * g * kvq::kPartialStride *
-                                                          sizeof(float));
+    p.counters = reinterpret_cast<unsigned long long *>(workspace);
+    p.partials = reinterpret_cast<float *>(reinterpret_cast<char *>(workspace) + kvq::decode_counter_bytes());
+    kvq::decode_test_settings(&p.wait_limit_ns, &p.test_skip_chunk);
     const int64_t HD = (int64_t)num_q_heads * kvq::kHeadDim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (int32_t b0 = 0; b0 < num_seqs; b0 += kvq::kMaxSeqsPerLaunch) {
@@ -166,6 +182,7 @@ kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, i
         d.out = out + b0 * HD;
         d.seq_lens = seq_lens + b0;
         d.block_table = block_table + (int64_t)b0 * max_blocks_per_seq;
+        d.epoch = kvq::decode_next_epoch();
         cudaError_t e = kvq::launch_decode(cache->fmt, d, s);
         if (e != cudaSuccess) return KVQ_ERR_CUDA;
     }
@@ -259,6 +276,14 @@ kvq_status kvq_get_device_status(const kvq_cache *cache, kvq_stream_t stream, in
     if (flags & KVQ_FLAG_TIMEOUT) return KVQ_ERR_TIMEOUT;
     if (flags & KVQ_FLAG_BAD_WORKSPACE) return KVQ_ERR_WORKSPACE;
     if (flags & (KVQ_FLAG_NO_TAIL | KVQ_FLAG_BAD_APPEND)) return KVQ_ERR_BAD_LENGTH;
+    return KVQ_OK;
+}
+
+kvq_status kvq_testing_set_decode_fault(uint32_t wait_limit_us, int32_t skip_chunk)
+{
+    if (skip_chunk < -1) return KVQ_ERR_INVALID_ARG;
+    g_test_wait_limit_us.store(wait_limit_us, std::memory_order_relaxed);
+    g_test_skip_chunk.store(skip_chunk, std::memory_order_relaxed);
     return KVQ_OK;
 }
 

@@ -31,6 +31,8 @@
 //            "Last" is decided by an atomic count per (sequence, head) that the
 //            last piece puts back to zero, so nothing waits and the workspace
 //            stays ready for the next launch.
+#include <atomic>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -74,11 +76,14 @@ template <>
 struct DecFmt<KVQ_FP8_E4M3> : DecFmt<KVQ_INT8_PAGE> {
 };
 
-// what a stage holds: units c .. c + nunits - 1 of (b, h), ntok tokens in all
+// what a stage holds: units c .. c + nunits - 1 of (b, h), ntok tokens in all,
+// of split piece `piece`; new_seg: the first chunk of a segment (a new
+// (sequence, head) or a new piece)
 struct alignas(16) StageMeta {
     int32_t b, h, c, ntok;
     float sk, sv;
     int32_t new_seg, nunits;
+    int32_t piece, pad[3];
 };
 
 template <int kStages, int kStageBytes, int kQRows>
@@ -90,7 +95,7 @@ struct alignas(128) WarpSmem {
     uint64_t full[kStages];
 };
 
-constexpr size_t kSeqSmemBytes = ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 127) / 128 * 128;
+constexpr size_t kSeqSmemBytes = ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 64 + 127) / 128 * 128;
 template <int FMT, int G>
 constexpr size_t dec_smem_bytes()
 {
@@ -791,20 +796,87 @@ struct Consumer<KVQ_FP8_E4M3> : ConsumerBytes<KVQ_FP8_E4M3> {
 };
 
 // ---------------------------------------------------------------------------
-// Combining the pieces of a (sequence, head) cut by warp-range boundaries.
+// The split: static pieces with dynamically executed tails.
+//
+// The units 0 .. U-1 of a launch are cut into GW contiguous warp ranges
+// [U w / GW, U (w+1) / GW).  Each range is one head piece followed by KT tail
+// pieces that together hold about kTailNum / kTailDen of it (at least KT
+// units, never the whole range).  Pieces are numbered w * (1 + KT) + j (j = 0
+// the head, 1 .. KT the tails), so in unit order.  Warp w runs its own head
+// piece; every tail piece is handed out through one ticket counter to
+// whichever warp asks next (warps ask when their queue runs dry), so the
+// last few microseconds of the launch are spread over the warps that finish
+// first instead of waiting for the slowest ones.  Where a piece begins and
+// ends depends only on (U, GW, KT), so the partials of a (sequence, head)
+// split over several pieces are found without knowing who ran them.
 // ---------------------------------------------------------------------------
+constexpr int kTailNum = 1;
+constexpr int kTailDen = 4;
 
-// Called by every lane of a warp right after it wrote one piece's partial:
-// counts the piece in the (sequence, head)'s slot and returns true in the warp
-// that wrote the last one, which also puts the slot back to zero -- so the
-// slots start every launch at zero provided the workspace was zero-filled
-// once and every earlier launch completed.  One atomic round trip, no retries:
-// all pieces of a (sequence, head) finish at about the same time, and a
-// compare-and-swap there retried under contention for several microseconds.
+struct Split {
+    int64_t U, GW;  // units, active warps
+    int KT, PW;     // tail pieces per warp, pieces per warp (1 + KT)
+
+    __device__ __forceinline__ void init(int64_t units, int64_t warps)
+    {
+        U = units;
+        GW = warps;
+        const int64_t rmin = GW > 0 ? U / GW : 0;
+        int64_t kt = rmin * kTailNum / kTailDen;
+        kt = kt < 1 ? 1 : (kt > kMaxTailPieces ? kMaxTailPieces : kt);
+        KT = rmin >= 2 ? (int)kt : 0;  // a range of one unit keeps it whole
+        PW = 1 + KT;
+    }
+    __device__ __forceinline__ int64_t lo(int64_t w) const { return U * w / GW; }
+    // units of a range of r units that go to its tail pieces
+    __device__ __forceinline__ int64_t tail(int64_t r) const
+    {
+        if (KT == 0) return 0;
+        const int64_t t = r * kTailNum / kTailDen;
+        return t > KT ? t : KT;
+    }
+    __device__ __forceinline__ int64_t start(int64_t pi) const
+    {
+        const int64_t w = pi / PW;
+        const int j = (int)(pi - w * PW);
+        const int64_t a = lo(w);
+        if (j == 0) return a;
+        const int64_t b = lo(w + 1);
+        const int64_t tl = tail(b - a);
+        return b - tl + tl * (j - 1) / KT;
+    }
+    __device__ __forceinline__ int64_t end(int64_t pi) const { return pi + 1 < GW * PW ? start(pi + 1) : U; }
+    // the piece that holds unit u
+    __device__ __forceinline__ int64_t piece_of(int64_t u) const
+    {
+        const int64_t w = ((u + 1) * GW - 1) / U;
+        if (KT == 0) return w;
+        const int64_t a = lo(w), b = lo(w + 1);
+        const int64_t tl = tail(b - a), xm = b - tl;
+        if (u < xm) return w * PW;
+        return w * PW + 1 + ((u - xm + 1) * KT - 1) / tl;
+    }
+    // the tail piece of ticket t (t < GW * KT)
+    __device__ __forceinline__ int64_t ticket_piece(int64_t t) const { return (t / KT) * PW + 1 + t % KT; }
+};
+
+// ---------------------------------------------------------------------------
+// Counters of the split.  A counter word holds a count in its low kCountBits
+// bits and, above them, count * epoch mod 2^40, where the epoch is an odd tag
+// chosen per call: an add of n is one atomic add of n * (1 + 2^24 epoch).
+// Within one call every word stays consistent (high part == low part *
+// epoch); a word left non-zero by another call (an aborted launch, a
+// workspace that was never zero-filled) is inconsistent under this call's
+// epoch, so KVQ_FLAG_BAD_WORKSPACE is raised instead of merging early.  The
+// warp whose add completes a count puts the word back to zero.  One atomic
+// round trip, no retries: the pieces of a (sequence, head) finish at about
+// the same time, and a compare-and-swap there retried under contention for
+// several microseconds.
 // Ordering: the warp barrier orders every lane's partial stores before lane
-// 0's acq_rel add (release), whose acquire side in the last warp, followed by
-// that warp's barrier, orders its reads of the other pieces' partials after
-// their writers' stores.
+// 0's acq_rel add (release), whose acquire side in the completing warp,
+// followed by that warp's barrier, orders its reads of the other pieces'
+// partials after their writers' stores.
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ unsigned long long add_acq_rel_gpu(unsigned long long *p, unsigned long long v)
 {
     unsigned long long old;
@@ -812,24 +884,64 @@ __device__ __forceinline__ unsigned long long add_acq_rel_gpu(unsigned long long
     return old;
 }
 
-__device__ __noinline__ bool last_piece(unsigned long long *slot, uint32_t pieces, int lane, int32_t *status)
+constexpr unsigned long long kCountMask = (1ull << kCountBits) - 1;
+constexpr unsigned long long kTagMask = (1ull << 40) - 1;
+
+__device__ __forceinline__ unsigned long long counter_step(unsigned long long epoch)
+{
+    return 1ull + (epoch << kCountBits);
+}
+
+// true when a counter word read under `epoch` carries only this call's adds
+__device__ __forceinline__ bool counter_consistent(unsigned long long w, unsigned long long epoch)
+{
+    return ((w >> kCountBits) & kTagMask) == (((w & kCountMask) * epoch) & kTagMask);
+}
+
+// Called by every lane of a warp right after it wrote a partial covering
+// `units` of a split (sequence, head) of `total` units: counts them and
+// returns true in the warp whose add completes the count.
+__device__ __noinline__ bool count_units(unsigned long long *slot, uint32_t units, uint32_t total,
+                                         unsigned long long epoch, int lane, int32_t *status)
 {
     __syncwarp();
-    unsigned long long count = 0;
+    int last = 0;
     if (lane == 0) {
-        count = add_acq_rel_gpu(slot, 1ull) + 1;
-        if (count > pieces || count == 0)  // the slot was not zero: workspace not zero-filled, or an aborted launch
-            set_flag(status, KVQ_FLAG_BAD_WORKSPACE);
-        if (count == pieces) *slot = 0ull;
+        const unsigned long long old = add_acq_rel_gpu(slot, (unsigned long long)units * counter_step(epoch));
+        const unsigned long long c = (old & kCountMask) + units;
+        if (!counter_consistent(old, epoch) || c > total) {
+            set_flag(status, KVQ_FLAG_BAD_WORKSPACE);  // not zero-filled, or left over by an aborted call
+        } else if (c == total) {
+            *slot = 0ull;
+            last = 1;
+        }
     }
-    count = __shfl_sync(kFull, count, 0);
-    if (count != pieces) return false;
+    last = __shfl_sync(kFull, last, 0);
+    if (!last) return false;
     __syncwarp();
     return true;
 }
 
-// One warp: combine the partials of warps gf .. gf + cnt - 1 (slot 1 of warp
-// gf when the (sequence, head) is that warp's last segment, slot 0 of the
+// One ticket of the tail pieces (lane 0 calls it): returns t, the tail piece
+// t of the launch when t < GW * KT; every active warp takes tickets until it
+// gets one past the end, so the launch takes GW * (KT + 1) of them and the
+// warp that takes the last one puts the counter back to zero.  A counter left
+// over by another call ends the warp's tail work (the flag is raised).
+__device__ __forceinline__ int64_t take_ticket(unsigned long long *ctr, int64_t takes, unsigned long long epoch,
+                                               int32_t *status)
+{
+    const unsigned long long old = atomicAdd(ctr, counter_step(epoch));
+    if (!counter_consistent(old, epoch)) {
+        set_flag(status, KVQ_FLAG_BAD_WORKSPACE);
+        return INT64_MAX;
+    }
+    const int64_t t = (int64_t)(old & kCountMask);
+    if (t == takes - 1) *ctr = 0ull;
+    return t;
+}
+
+// One warp: combine the partials of pieces gf .. gf + cnt - 1 (slot 1 of piece
+// gf when the (sequence, head) is that piece's last segment, slot 0 of the
 // others) into one fp16 output row.  Partials are read from L2 (ld.cg): other
 // SMs wrote them during this launch.  The loads of a batch of kBatch pieces
 // are independent of one another, so a merge of up to kBatch pieces costs one
@@ -1050,28 +1162,44 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     }
     __syncthreads();
 
-    const int64_t U = s_cu[B];
-    const int64_t GW = imin64((int64_t)grid_warps, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);  // active warps
+    // the split geometry, the same for every warp (kept in shared memory: it
+    // is read only when a piece starts or a segment ends)
+    Split *s_split = reinterpret_cast<Split *>(smem_raw + kDecWarps * sizeof(WS) +
+                                               ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 15) / 16 * 16);
+    if (tid == 0) {
+        const int64_t U = s_cu[B];
+        // active warps: at least kMinUnitsPerWarp units each
+        s_split->init(U, imin64((int64_t)grid_warps, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp));
+    }
+    __syncthreads();
+    const Split &sp = *s_split;
     // logical warp index, round-robin over the CTAs: when fewer than all warps
-    // have work (G < grid warps) the active ones spread over every SM
+    // have work (GW < grid warps) the active ones spread over every SM
     const int gw = warp * (int)gridDim.x + blockIdx.x;
-    const int64_t x0 = gw < GW ? U * gw / GW : 0;
-    const int64_t x1 = gw < GW ? U * (gw + 1) / GW : 0;
-    const bool active = x0 < x1;
+    const bool active = gw < sp.GW;
+    unsigned long long *const tickets = p.counters;        // word 0: tail-piece tickets
+    unsigned long long *const piece_ctr = p.counters + 1;  // then one word per piece
 
-    // ---- issue cursor: unit x0 + ni = (ib, ih, ic) ----
+    // ---- issue cursor: unit x_cur of piece pi_cur = (ib, ih, ic); rem units left in the piece ----
+    int pi_cur = gw * sp.PW;
+    int rem = 0;
     int ib = 0, ih = 0, ic = 0;
-    if (active) {
+    auto seek = [&](int64_t x) {
         int lo = 0, hi = B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (s_cu[mid] <= x0) lo = mid; else hi = mid - 1;
+            if (s_cu[mid] <= x) lo = mid; else hi = mid - 1;
         }
         ib = lo;
         const int n = units_of(s_len[ib], UT);
-        const int off = (int)(x0 - s_cu[ib]);
+        const int off = (int)(x - s_cu[ib]);
         ih = off / n;
         ic = off % n;
+    };
+    if (active) {
+        const int64_t x = sp.start(pi_cur);
+        rem = (int)(sp.end(pi_cur) - x);
+        seek(x);
     }
     int inb = units_of(s_len[ib], UT);  // units of the issue cursor's sequence
     // page ring: lane l holds page slot ring_j0 + l of (ring_b, ring_h) and,
@@ -1123,21 +1251,37 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     }
     __syncwarp();
 
-    const int N = (int)(x1 - x0);  // units of this warp
     constexpr uint32_t kPageBytes = kPage * RB;
 
-    int ci = 0;   // stages filled so far (chunk count)
-    int nis = 0;  // units issued so far
-    // fill stage ci % kStages with the next chunk: the cursor's unit and the
+    int ci = 0;                 // stages filled so far (chunk count)
+    bool issue_done = false;    // no piece is left for this warp
+    bool piece_new = true;      // the next stage starts a piece
+    // Fill stage ci % kStages with the next chunk: the cursor's unit and the
     // following ones of the same stage-sized group of its page, within the
-    // (sequence, head) and the warp's range
-    auto issue = [&]() {
+    // (sequence, head) and the piece.  When the piece is used up, a ticket
+    // brings the next tail piece.  Returns false when no work is left.
+    auto issue = [&]() -> bool {
+        if (rem == 0) {
+            int64_t t = INT64_MAX;
+            if (sp.KT > 0 && lane == 0) t = take_ticket(tickets, sp.GW * (sp.KT + 1), p.epoch, p.status);
+            t = __shfl_sync(kFull, t, 0);
+            if (t >= sp.GW * sp.KT) {
+                issue_done = true;
+                return false;
+            }
+            pi_cur = (int)sp.ticket_piece(t);
+            const int64_t x = sp.start(pi_cur);
+            rem = (int)(sp.end(pi_cur) - x);
+            seek(x);
+            inb = units_of(s_len[ib], UT);
+            piece_new = true;
+        }
         const int s = ci % kStages;
         const int j = ic / UPP;
-        const int nh = UPS > 1 ? min(min(UPS - ic % UPS, inb - ic), N - nis) : 1;
-        if (ib != ring_b || ih != ring_h || j >= ring_j0 + 32) ring_pages(ib, ih, j);
+        const int nh = UPS > 1 ? min(min(UPS - ic % UPS, inb - ic), rem) : 1;
+        if (ib != ring_b || ih != ring_h || j < ring_j0 || j >= ring_j0 + 32) ring_pages(ib, ih, j);
         const int pg = __shfl_sync(kFull, r_page, j - ring_j0);
-        const bool new_seg = (ci == 0) || (ic == 0);
+        const bool new_seg = piece_new || (ic == 0);
         if (ring_scales_due) {  // the ring's scales (after the wait: appends write them)
             r_sk = p.k_scales[(int64_t)r_page * H + ring_h];
             r_sv = p.v_scales[(int64_t)r_page * H + ring_h];
@@ -1150,11 +1294,16 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             const uint32_t cb = (uint32_t)nh * kUnitBytes;
             const uint32_t bytes = 2 * cb + (new_seg ? G * kHeadDim * 2 : 0);
             mbar_arrive_expect_tx(&ws.full[s], bytes);
-            const size_t off = ((size_t)pg * H + ih) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
-            bulk_copy_g2s(ws.k[s], p.k_codes + off, cb, &ws.full[s]);
-            bulk_copy_g2s(ws.v[s], p.v_codes + off, cb, &ws.full[s]);
-            if (new_seg)
-                bulk_copy_g2s(ws.q[s], p.q + ((size_t)ib * H + ih) * G * kHeadDim, G * kHeadDim * 2, &ws.full[s]);
+            // the timeout test leaves one chunk of warp 0 without its copies:
+            // the stage's wait then runs out with nothing in flight
+            if (!(p.test_skip_chunk == ci && gw == 0)) {
+                const size_t off = ((size_t)pg * H + ih) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
+                bulk_copy_g2s(ws.k[s], p.k_codes + off, cb, &ws.full[s]);
+                bulk_copy_g2s(ws.v[s], p.v_codes + off, cb, &ws.full[s]);
+                if (new_seg)
+                    bulk_copy_g2s(ws.q[s], p.q + ((size_t)ib * H + ih) * G * kHeadDim, G * kHeadDim * 2,
+                                  &ws.full[s]);
+            }
         }
         const float sk = __shfl_sync(kFull, r_sk, j - ring_j0);
         const float sv = __shfl_sync(kFull, r_sv, j - ring_j0);
@@ -1163,9 +1312,12 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             *reinterpret_cast<int4 *>(&ws.meta[s].b) = make_int4(ib, ih, ic, ntok);
             *reinterpret_cast<float4 *>(&ws.meta[s].sk) =
                 make_float4(sk, sv, __int_as_float(new_seg ? 1 : 0), __int_as_float(nh));
+            ws.meta[s].piece = pi_cur;
         }
         // advance the cursor by the chunk
         ic += nh;
+        rem -= nh;
+        piece_new = false;
         if (ic == inb) {
             ic = 0;
             if (++ih == H) {
@@ -1176,55 +1328,64 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             }
         }
         ++ci;
-        nis += nh;
+        return true;
     };
 
-    for (int i = 0; i < kStages && nis < N; i++) issue();
+    for (int i = 0; i < kStages; i++)
+        if (!issue()) break;
     __syncwarp();
 
     // ---- consumer: qk of unit n+1 overlaps pv of unit n ----
     typename ConsumerFor<FMT, G>::type cs;
     cs.reset();
     int cur_b = -1, cur_h = -1;
-    int seg_n = 0;
+    int seg_c = 0;        // first unit of the current segment within its (sequence, head)
+    int seg_units = 0;    // units of it consumed so far
+    int seg_pi = 0;       // its piece
 
-    auto flush = [&](int b, int h, int na, int nb) {
+    // units c .. c + units - 1 of (b, h), consumed in piece pi, are done
+    auto flush = [&](int b, int h, int c, int units, int pi) {
         const int n = units_of(s_len[b], UT);
         const int64_t u0 = s_cu[b] + (int64_t)h * n;
-        const int64_t sa = x0 + na, sb = x0 + nb;
-        if (sa == u0 && sb == u0 + n) {
+        const int64_t sa = u0 + c;
+        if (sa == u0 && units == n) {
             cs.finish(lane, p.out + ((int64_t)b * H + h) * G * kHeadDim, nullptr);
-        } else {  // cut by a range boundary: the first segment of the warp goes to slot 0, the last to slot 1
-            cs.finish(lane, nullptr, p.partials + ((int64_t)gw * 2 + (na == 0 ? 0 : 1)) * kSlotFloats);
-            const int64_t u1 = u0 + n;
-            const int64_t gf = ((u0 + 1) * GW - 1) / U;  // warp owning unit u0
-            const int64_t gl = (u1 * GW - 1) / U;        // warp owning unit u1 - 1
-            if (last_piece(p.pieces + gl, (uint32_t)(gl - gf + 1), lane, p.status)) {
-                const int first_slot = ((U * gf) / GW != u0) ? 1 : 0;
+        } else {  // split: the piece's first segment goes to its slot 0, its last to slot 1
+            cs.finish(lane, nullptr, p.partials + ((int64_t)pi * 2 + (sa == sp.start(pi) ? 0 : 1)) * kSlotFloats);
+            const int64_t pf = sp.piece_of(u0);
+            const int64_t pl = sp.piece_of(u0 + n - 1);
+            if (count_units(piece_ctr + pl, (uint32_t)units, (uint32_t)n, p.epoch, lane, p.status)) {
+                const int first_slot = (sp.start(pf) != u0) ? 1 : 0;
                 uint16_t *orow = p.out + ((int64_t)b * H + h) * G * kHeadDim;
                 if constexpr (G == 1)
-                    merge_pieces<F::kMergeBatch>(p.partials, kSlotFloats, 0, gf, (int)(gl - gf + 1), first_slot,
+                    merge_pieces<F::kMergeBatch>(p.partials, kSlotFloats, 0, pf, (int)(pl - pf + 1), first_slot,
                                                  orow, lane);
                 else
-                    merge_group<8 / G, G>(p.partials, gf, (int)(gl - gf + 1), first_slot, orow, lane);
+                    merge_group<8 / G, G>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane);
             }
         }
     };
     auto drain = [&](int from) {  // after a timeout: let the copies still in flight land
         for (int y = from; y < ci; y++)
-            mbar_wait_bounded(&ws.full[y % kStages], (uint32_t)((y / kStages) & 1));
+            mbar_wait_bounded(&ws.full[y % kStages], (uint32_t)((y / kStages) & 1), p.wait_limit_ns);
+    };
+    auto seg_start = [&](const int4 &m, int32_t piece) {
+        cur_b = m.x;
+        cur_h = m.y;
+        seg_c = m.z;
+        seg_units = 0;
+        seg_pi = piece;
     };
 
     // chunk 0, unit 0
-    if (!mbar_wait_bounded(&ws.full[0], 0u)) {
+    if (!mbar_wait_bounded(&ws.full[0], 0u, p.wait_limit_ns)) {
         if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
         drain(1);
         return;
     }
     int4 mi = *reinterpret_cast<const int4 *>(&ws.meta[0].b);
     float4 mf = *reinterpret_cast<const float4 *>(&ws.meta[0].sk);
-    cur_b = mi.x;
-    cur_h = mi.y;
+    seg_start(mi, ws.meta[0].piece);
     cs.load_q(ws.q[0], lane);
     constexpr int kScores = G == 1 ? 4 : 8;  // scores a lane holds per unit
     float sc[kScores];
@@ -1235,7 +1396,6 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     // One iteration per chunk cc (stage cc % kStages), entered with the
     // chunk's first unit scored (pf) and its units' qk / pv still to run:
     // qk of the next unit is always issued before pv of the current one.
-    int n = 0;  // units of the warp's range before chunk cc
     for (int cc = 0;; cc++) {
         const int s = cc % kStages;
         const float fac = mf.x * p.score_scale;
@@ -1249,36 +1409,36 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         const bool more = cc + 1 < ci;  // chunk cc + 1 was issued before chunk cc was consumed
         int4 mi1 = mi;
         float4 mf1 = mf;
+        int32_t piece1 = 0;
         float sc1[kScores];
         if (more) {
             const int s1 = (cc + 1) % kStages;
-            if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((cc + 1) / kStages) & 1))) {
+            if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((cc + 1) / kStages) & 1), p.wait_limit_ns)) {
                 if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
                 drain(cc + 2);
                 return;
             }
             mi1 = *reinterpret_cast<const int4 *>(&ws.meta[s1].b);
             mf1 = *reinterpret_cast<const float4 *>(&ws.meta[s1].sk);
+            piece1 = ws.meta[s1].piece;
             if (__float_as_int(mf1.z)) cs.load_q(ws.q[s1], lane);
             cs.qk(ws.k[s1], lane, sc1);  // the next chunk's first unit: independent of the pv below
         }
         cs.pv(ws.v[s] + (nh - 1) * kUnitBytes, pf, lane);  // the chunk's last unit
-        n += nh;
+        seg_units += nh;
         __syncwarp();  // every lane is done with stage s: refill it
-        if (nis < N) issue();
+        if (!issue_done) issue();
         if (!more) break;
-        if (__float_as_int(mf1.z)) {  // the next chunk starts a new (sequence, head)
-            flush(cur_b, cur_h, seg_n, n);
+        if (__float_as_int(mf1.z)) {  // the next chunk starts a new segment
+            flush(cur_b, cur_h, seg_c, seg_units, seg_pi);
             cs.reset();
-            cur_b = mi1.x;
-            cur_h = mi1.y;
-            seg_n = n;
+            seg_start(mi1, piece1);
         }
         cs.softmax(sc1, min(UT, mi1.w), mf1.x * p.score_scale, mf1.y, lane, pf);
         mi = mi1;
         mf = mf1;
     }
-    flush(cur_b, cur_h, seg_n, N);
+    flush(cur_b, cur_h, seg_c, seg_units, seg_pi);
 }
 
 template <int FMT, int G>
@@ -1329,12 +1489,38 @@ int decode_prepare(int fmt, int group)
     return ctas_per_sm<KVQ_INT8_PAGE, 1>();
 }
 
+size_t decode_counter_bytes()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    const size_t words = 1 + (size_t)sms * kMaxDecodeWarpsPerSm * kPiecesPerWarp;
+    return (words * sizeof(unsigned long long) + 255) / 256 * 256;
+}
+
 size_t decode_workspace_bytes(int fmt, int group)
 {
     const int gw = decode_grid_warps(fmt);
     if (gw <= 0 || !decode_group_supported(fmt, group)) return 0;
-    const size_t partial = (size_t)gw * 2 * group * kPartialStride * sizeof(float);
-    return partial + (size_t)gw * sizeof(unsigned long long);
+    static_assert(DecFmt<KVQ_INT4_B64>::kWarps * DecFmt<KVQ_INT4_B64>::kCtasPerSm <= kMaxDecodeWarpsPerSm &&
+                      DecFmt<KVQ_INT8_PAGE>::kWarps * DecFmt<KVQ_INT8_PAGE>::kCtasPerSm <= kMaxDecodeWarpsPerSm,
+                  "the counter region holds kMaxDecodeWarpsPerSm warps per SM");
+    const size_t counters = decode_counter_bytes();
+    if (counters == 0) return 0;
+    const size_t partial = (size_t)gw * kPiecesPerWarp * 2 * group * kPartialStride * sizeof(float);
+    return counters + partial;
+}
+
+unsigned long long decode_next_epoch()
+{
+    // splitmix64's output function over a call counter, forced odd, 40 bits:
+    // epochs of different calls differ in their low bits only by chance
+    static std::atomic<unsigned long long> calls{0};
+    unsigned long long z = (calls.fetch_add(1, std::memory_order_relaxed) + 1) * 0x9e3779b97f4a7c15ull;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    z ^= z >> 31;
+    return (z | 1ull) & ((1ull << 40) - 1);
 }
 
 cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s)

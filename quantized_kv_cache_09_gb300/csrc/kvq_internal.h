@@ -43,8 +43,8 @@ struct DecodeParams {
     const int32_t *block_table;
     const int32_t *seq_lens;
     uint16_t *out;
-    float *partials;              // [grid warps][2][kPartialStride]
-    unsigned long long *pieces;   // [grid warps]: pieces written so far of the (sequence, head) ending in warp g (0 between launches)
+    float *partials;               // [pieces][2][group * kPartialStride]: split partials, two slots per piece
+    unsigned long long *counters;  // [pieces] unit counts of split (sequence, head)s + [1] tail-piece tickets
     int32_t *status;
     int32_t num_seqs;
     int32_t num_heads;
@@ -52,7 +52,25 @@ struct DecodeParams {
     int32_t max_blocks;
     float score_scale;  // softmax_scale * log2(e): scores are kept in the base-2 domain
     int32_t group;      // query heads per cache head: q and out hold num_heads * group heads
+    // Tag of this call in the counters (odd, < 2^40).  A counter holds
+    // count + 2^24 * (count * epoch mod 2^40), so a count left over by another
+    // call (or memory that was never zero-filled) shows up as an inconsistent word.
+    unsigned long long epoch;
+    unsigned long long wait_limit_ns;  // bounded waits give up after this long
+    int32_t test_skip_chunk;           // >= 0: warp 0 leaves the copies of this chunk unissued (timeout test)
 };
+
+// default limit of a decode kernel's bounded waits (kernels finish in milliseconds)
+constexpr unsigned long long kDecodeWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+// counter words: the low kCountBits bits count, the rest carry count * epoch
+constexpr int kCountBits = 24;
+// tail-piece bound of the decode split: every warp's range ends in at most
+// kMaxTailPieces pieces handed out dynamically, so pieces <= warps * (1 + kMaxTailPieces)
+constexpr int kMaxTailPieces = 4;
+constexpr int kPiecesPerWarp = 1 + kMaxTailPieces;
+// warps per SM the decode workspace's counter region is sized for (every decode kernel uses at most this many)
+constexpr int kMaxDecodeWarpsPerSm = 16;
 
 // floats per split partial: m, l, 2 pad, acc[128]
 constexpr int kPartialStride = 132;
@@ -129,7 +147,14 @@ cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s);
 // number of warps of the persistent split grid on the current device (0 on error)
 int decode_grid_warps(int fmt);
 bool decode_group_supported(int fmt, int group);
+// the decode workspace: a counter region first (its size depends on the
+// device's SM count only), then the split partials
+size_t decode_counter_bytes();
 size_t decode_workspace_bytes(int fmt, int group);
+// a fresh odd 40-bit tag for one decode launch
+unsigned long long decode_next_epoch();
+// test hook of kvq_testing.h: wait limit (0: default) and chunk to leave unissued (-1: none)
+void decode_test_settings(unsigned long long *wait_limit_ns, int32_t *skip_chunk);
 // resolves (and caches) the occupancy query and shared-memory attribute of the
 // decode kernel for (fmt, group); returns CTAs per SM, 0 when unsupported
 int decode_prepare(int fmt, int group);

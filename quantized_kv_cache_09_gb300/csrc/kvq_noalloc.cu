@@ -14,11 +14,12 @@
 // host it names a host-side stand-in), so the first call on each device looks
 // the address up with cudaGetSymbolAddress while that device is current and
 // keeps it.  All calls share the one array: calls that may overlap on the GPU
-// race on it.  Its piece counters must start at zero: a __device__ array is
-// zero when the module loads, and every decode call that completes leaves the
-// counters at zero again (after a call that set a KVQ_FLAG_* bit they may not
-// be, and the device status word of later calls may show
-// KVQ_FLAG_BAD_WORKSPACE).
+// race on it.  The split's counters at the front of the array must be zero
+// when a launch starts; a launch that completes leaves them zero, but one that
+// was cut short (a bounded wait that ran out) may not, and the caller of this
+// entry point has no way to clear library memory.  So every call first clears
+// the counter region on the caller's stream (cudaMemsetAsync, which allocates
+// nothing); the partials behind it need no clearing.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -64,7 +65,13 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const
     if (st != KVQ_OK) return st;
     const size_t need = kvq_decode_workspace_bytes(static_cast<kvq_format>(cache->fmt), cache->num_heads,
                                                    cache->head_dim);
+    if (need == 0) return KVQ_ERR_UNSUPPORTED;
     if (need > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;  // this device needs more than the fixed array
+    const size_t counters = kvq::decode_counter_bytes();
+    if (counters == 0 || counters > need) return KVQ_ERR_CUDA;
+    if (num_seqs > 0 &&
+        cudaMemsetAsync(scratch, 0, counters, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KVQ_ERR_CUDA;
     return kvq_decode_attention(cache, q, block_table, max_blocks_per_seq, seq_lens, num_seqs, softmax_scale, out,
                                 scratch, KVQ_NOALLOC_SCRATCH_BYTES, stream);
 }

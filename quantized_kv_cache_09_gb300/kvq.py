@@ -35,7 +35,9 @@ EXPORTS = ("kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes", "kvq_deco
            "kvq_step_graph_create", "kvq_step_graph_update",
            "kvq_step_graph_launch", "kvq_step_graph_destroy", "kvq_get_device_status", "kvq_status_string",
            "kvq_version")
-NOALLOC_SCRATCH_BYTES = 4 << 20
+# every symbol include/kvq_testing.h declares (test hooks)
+TESTING_EXPORTS = ("kvq_testing_set_decode_fault",)
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class KvqError(RuntimeError):
@@ -112,6 +114,8 @@ def lib():
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_version.argtypes = []
         L.kvq_version.restype = i32
+        L.kvq_testing_set_decode_fault.argtypes = [ctypes.c_uint32, i32]
+        L.kvq_testing_set_decode_fault.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -144,6 +148,14 @@ def kvq_status_string(status):
 
 def kvq_version():
     return lib().kvq_version()
+
+
+def kvq_testing_set_decode_fault(wait_limit_us=0, skip_chunk=-1):
+    """Test hook (include/kvq_testing.h): every later decode launch of the
+    process waits at most wait_limit_us per copy (0: the default 0.5 s) and,
+    when skip_chunk >= 0, leaves the copies of that chunk of the grid's first
+    warp unissued, so its bounded wait runs out; (0, -1) restores the defaults."""
+    _check(lib().kvq_testing_set_decode_fault(int(wait_limit_us), int(skip_chunk)), "kvq_testing_set_decode_fault")
 
 
 def kvq_quantize(fmt, x, codes, scales, stream=None):
@@ -221,8 +233,9 @@ def kvq_decode_attention_noalloc(cache, q, block_table, seq_lens, softmax_scale,
     allocate device memory when they run decode attention (a plugin whose
     execute step must not allocate, memory reserved up front by another
     allocator, a loop that cannot afford cudaMalloc's synchronisation): the
-    scratch is a fixed 4 MiB array inside the library, shared by every call, so
-    calls that may overlap on the GPU must be serialised by the caller."""
+    scratch is a fixed 16 MiB array inside the library, shared by every call, so
+    calls that may overlap on the GPU must be serialised by the caller; each
+    call clears the array's split counters first on the same stream."""
     _cuda(q, torch.float16, "q")
     _cuda(out, torch.float16, "out")
     _cuda(block_table, torch.int32, "block_table")

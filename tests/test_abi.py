@@ -12,8 +12,8 @@ from quantized_kv_cache_09_gb300 import build, kvq
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _declared_functions():
-    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+def _declared_functions(header="kvq.h"):
+    src = open(os.path.join(ROOT, "include", header)).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(kvq_[a-z_0-9]+)\s*\(", src)))
 
@@ -23,9 +23,19 @@ def test_library_builds_and_exports_every_declared_symbol():
     lib = kvq.lib()
     names = _declared_functions()
     assert set(names) == set(kvq.EXPORTS), names
-    for n in names:
+    testing = _declared_functions("kvq_testing.h")
+    assert set(testing) == set(kvq.TESTING_EXPORTS), testing
+    headers = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    assert headers == ["kvq.h", "kvq_testing.h"], headers
+    for n in names + testing:
         assert hasattr(lib, n), n
     assert kvq.kvq_version() == 100
+
+
+def test_testing_hook_validates_on_the_host():
+    lib = kvq.lib()
+    assert lib.kvq_testing_set_decode_fault(0, -2) == 1
+    assert lib.kvq_testing_set_decode_fault(0, -1) == 0   # the defaults
 
 
 def test_status_strings():

@@ -1,14 +1,18 @@
 """GPU tests of the decode step captured as a CUDA graph (kvq_step_graph_*;
 CUDA Graph instance reuse, jsqmd.com/news/887038 section 4.1): replaying the
 graph must give bit-identical outputs and caches to the eager calls it
-records, with per-step inputs written into the bound tensors; rebinding with
-kvq_step_graph_update must move the step to the new tensors; rejected
-arguments must be reported as the eager calls report them.  Parity of the
-eager path against the oracle is covered by the decode tests."""
+records, with per-step inputs written into the bound tensors, and its outputs
+must match the binary64 oracle's attention over the oracle's own cache of the
+grown histories (2e-3 of max|v^|); rebinding with kvq_step_graph_update must
+move the step to the new tensors; rejected arguments must be reported as the
+eager calls report them."""
+import math
+
 import numpy as np
 import pytest
 import torch
 
+from oracle import oracle as orc
 from quantized_kv_cache_09_gb300 import kvq
 from quantized_kv_cache_09_gb300.runner import DecodeStep, DeviceWorkload
 from quantized_kv_cache_09_gb300.synth import workloads as W
@@ -24,6 +28,30 @@ def _pair(fmt, lens, H=4, Hq=None, seed=41):
     a.prefill()
     b.prefill()
     return wl, a, b
+
+
+TOL = 2e-3
+
+
+def _oracle_check(wl, lens_after, q_bits, out):
+    """The graph's output of one step against the oracle: quantize every
+    sequence's history up to lens_after with the oracle's codec, attend with
+    the step's query in binary64."""
+    rb = orc.row_bytes(wl.fmt, D)
+    kc = np.zeros((wl.num_pages, wl.H, 64, rb), np.uint8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((wl.num_pages, wl.H), np.float32)
+    vs = np.zeros_like(ks)
+    for b in range(wl.B):
+        L = int(lens_after[b])
+        orc.quantize_into_pages(wl.fmt, wl.kv_host("k", b, 0, L), wl.block_table[b], kc, ks)
+        orc.quantize_into_pages(wl.fmt, wl.kv_host("v", b, 0, L), wl.block_table[b], vc, vs)
+    ref = orc.decode_attention(wl.fmt, kc, vc, ks, vs, wl.block_table, lens_after, q_bits,
+                               np.float32(1 / math.sqrt(D)))
+    vmax = np.repeat(orc.value_absmax(wl.fmt, vc, vs, wl.block_table, lens_after, wl.H, D), wl.Hq // wl.H, axis=1)
+    err = orc.normalized_error(out.float().cpu().numpy().astype(np.float64), ref, vmax)
+    assert err <= TOL, err
+    return err
 
 
 def _same_cache(a, b):
@@ -56,6 +84,8 @@ def test_graph_replay_equals_eager(cuda_ok, fmt, H, Hq):
         g.launch()
         torch.cuda.synchronize()
         assert torch.equal(out_e, st_g.out), s
+        if s % 23 == 0 or s == 69:  # the replay against the oracle, not only against eager calls
+            _oracle_check(wl, wl.lens + s + 1, wl.q_host(s), st_g.out)
     g.close()
     _same_cache(ea, gr)
     assert kvq.kvq_get_device_status(ea.cache) == (0, 0)
@@ -95,6 +125,10 @@ def test_graph_of_layers_and_steps_equals_eager(cuda_ok):
         torch.cuda.synchronize()
         for i, (a, b) in enumerate(zip(outs_e, g_outs)):
             assert torch.equal(a, b), (rep_, i)
+    for s in (0, 4):  # the replayed outputs of the first and last step of every layer against the oracle
+        for li in range(3):
+            wl = layers[li][0]
+            _oracle_check(wl, wl.lens + s + 1, wl.q_host(s), g_outs[3 * s + li])
     g.close()
     for _, e, gdw in layers:
         _same_cache(e, gdw)
