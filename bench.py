@@ -1,25 +1,34 @@
 #!/usr/bin/env python3
-"""Benchmark of the quantized-KV decode step on one GB300 (or N, as replicas).
+"""Benchmark of the quantized-KV decode path on one GB300 (or N, as replicas).
 
-Workload (llama2-7b-layer): B=8 sequences, H=32 heads, D=128, context 8192,
-int4 64-token blocks, K/V ~ N(0,1) with 4 outlier channels per head x10,
-inputs generated in HBM by the seeded generator.  One step = the whole hot
-path once: append one token per sequence (re-quantizing each open block from
-its fp16 originals: absmax, scale, quantize, pack) and decode attention of the
-step's query over every sequence (one split-K launch that also merges).  The decode
-position cycles through one 64-token block, so the context stays 8193..8256
-tokens and the working set (~270 MB of codes) stays larger than L2 (129 MB).
+Headline workload (long-context): B=16 sequences, H=32 heads, D=128, context
+32768, int4 64-token blocks, K/V ~ N(0,1) with each (head, channel) an outlier
+x10 with probability 0.01, inputs generated in HBM by the seeded generator
+(2.15 GB of packed codes, far larger than L2).  One step = the whole hot path
+once: append one token per sequence (re-quantizing each open block from its
+fp16 originals: absmax, scale, quantize, pack) and decode attention of the
+step's query over every sequence (one split-K launch that also merges).  The
+decode position cycles through one 64-token block, so the context stays
+32769..32832 tokens.
+
+Every other workload of the path runs after it, each with its own roofline,
+under "workloads" in the same JSON line: tiny, llama2-7b-layer, paged-int8,
+prefill-append (quantize GB/s), llama3-8b-layer-gqa, llama2-7b-layer-fp8,
+chunked-prefill (tensor-core attention, TFLOP/s) and mqa-32k (one cache head
+serving 32 query heads).
 
 value    decode tokens/s = sequences advanced one token through one layer's
          attention per second, summed over ranks (weak scaling: every rank runs
          its own batch; no collective on the data path)
-e2e      the same steps through the C ABI with host buffers: each step copies its
-         new K/V rows and query from pinned host memory and its output back
+e2e      the same steps through the C ABI with host buffers: each step's new
+         K/V rows and query are copied from pinned host memory and its output
+         back, on a copy stream one step ahead of the compute stream
 roofline the split decode kernel's algorithmic bytes / its CUDA-event time
 cpu_baseline / --impl reference: the CPU oracle timed on host cores on a
          bounded sample of the same step
 """
 import argparse
+import concurrent.futures as cf
 import hashlib
 import json
 import math
@@ -33,26 +42,41 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-CONFIG = 2
 METRIC = "quantized-KV decode attention tokens/s and KV GB/s vs HBM roofline; quantize GB/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TFLOPS = 1900.0
+L2_BYTES = 129e6
+DEFAULT_WORKLOAD = "long-context"
+
+# name -> (kind, workload number in synth/workloads.py)
+WORKLOADS = {
+    "tiny": ("decode", 1),
+    "llama2-7b-layer": ("decode", 2),
+    "long-context": ("decode", 3),
+    "paged-int8": ("decode", 4),
+    "prefill-append": ("append", 5),
+    "llama3-8b-layer-gqa": ("decode", 6),
+    "llama2-7b-layer-fp8": ("decode", 7),
+    "chunked-prefill": ("prefill", 8),
+    "mqa-32k": ("decode", 9),
+}
+FORMAT_NAMES = {0: ("int4", "int4-b64"), 1: ("int8", "int8-page"), 2: ("fp8-e4m3", "fp8-e4m3-page")}
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--workload", default="llama2-7b-layer",
-                    choices=["tiny", "llama2-7b-layer", "long-context", "paged-int8", "prefill-append",
-                             "llama3-8b-layer-gqa", "llama2-7b-layer-fp8", "chunked-prefill"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--prefill-seqs", type=int, default=64)
-    ap.add_argument("--no-extras", dest="extras", action="store_false")
-    return ap.parse_args()
+    ap.add_argument("--sub-steps", type=int, default=100, help="timed steps of each further workload")
+    ap.add_argument("--no-extras", dest="extras", action="store_false", help="the headline workload only")
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -82,24 +106,29 @@ def whole_job_rate(world, units_per_rank, seconds):
     return world * units_per_rank / seconds
 
 
-def measured_peak():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _peaks():
     try:
-        with open(path) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return None
+
+
+def measured_peak():
+    """HBM GB/s: the measured copy bandwidth, else the fallback."""
+    p = _peaks()
+    if p and "hbm_gbs" in p:
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
 
 
 def measured_tensor_peak():
     """Dense fp16/bf16 tensor peak in TFLOP/s: the measured cuBLAS bf16 burst
     figure (fp16 and bf16 have the same nominal rate), else the fallback."""
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(path) as f:
-            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; fp16 same nominal rate)"
-    except Exception:
-        return 1900.0, "fallback"
+    p = _peaks()
+    if p and "bf16_tflops" in p:
+        return float(p["bf16_tflops"]), "measured (bf16 burst; fp16 same nominal rate)"
+    return FALLBACK_TFLOPS, "fallback"
 
 
 KERNEL_SOURCES = {
@@ -138,14 +167,15 @@ def ncu_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples of SM clock and throttle reasons."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, period_ms=20):
         self.index = index
+        self.period_ms = period_ms
         self.samples = []
         self.proc = None
         self.thread = None
@@ -154,7 +184,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                          "-lms", str(self.period_ms), "-i", str(self.index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -188,7 +218,7 @@ class ClockSampler:
             try:
                 sm.append(float(s[0]))
                 mx = float(s[1])
-            except ValueError:
+            except (ValueError, IndexError):
                 continue
             for n, v in zip(names, s[3:7]):
                 if v.strip().lower() == "active":
@@ -198,97 +228,217 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
-# the CPU oracle on a bounded sample of the same step
+# workload descriptions shared by both arms (the same `config` dict)
 # --------------------------------------------------------------------------
-def oracle_step_rate(seconds, seed, threads=None, cfg=None):
-    """Oracle decode steps of a uniform-length decode workload (default: the 7B
-    layer): for each sampled sequence, re-quantize its open block (oracle
-    quantize of the 64-token block holding the new token) and attend over its
-    L + 1 tokens, every query head, binary64.
-    Threads run independent sequences (the oracle releases the GIL).
-    Returns (steps per second, threads, description)."""
+def _make(name, seed, prefill_seqs=64):
+    from quantized_kv_cache_09_gb300.synth import workloads as W
+    kind, cfg = WORKLOADS[name]
+    if kind == "decode":
+        return W.make_workload(cfg, seed=seed, extra_tokens=64)
+    if kind == "append":
+        c = W.CONFIGS[5]
+        return W.Workload(prefill_seqs, c["H"], c["D"], [c["L"]] * prefill_seqs, c["fmt"], c["sigma"], None,
+                          "permuted", seed, 0, c["name"])
+    return W.make_workload(cfg, seed=seed)
+
+
+def decode_context(wl):
+    """The context range the decode steps run over (steps cycle through one block)."""
+    lens = wl.lens
+    if bool((lens % 64 == 0).all()) and lens.min() == lens.max():
+        return f"{int(lens[0]) + 1}..{int(lens[0]) + 64}"
+    return f"{int(lens.min()) + 1}..{int(lens.max()) + 1} (sum {int(lens.sum()) + len(lens)})"
+
+
+def decode_ctx_lens(wl, step):
+    """Lengths after the append of decode step `step` (the cycle of measure_decode)."""
+    aligned = bool((wl.lens % 64 == 0).all())
+    return wl.lens + ((step % 64) if aligned else 0) + 1
+
+
+def workload_config(name, world=1, seed=0, prefill_seqs=64):
+    kind, _ = WORKLOADS[name]
+    wl = _make(name, seed, prefill_seqs)
+    par = f"replicas x{world} (sequence-sharded, no collective)"
+    if kind == "decode":
+        dec_bytes = wl.decode_bytes(wl.lens + 1)
+        return {"workload": name, "B": wl.B, "H": wl.H, "Hq": wl.Hq, "D": wl.D, "context": decode_context(wl),
+                "format": FORMAT_NAMES[wl.fmt][1], "table": wl.table, "step": "append 1 token + decode attention",
+                "parallelism": par,
+                "l2": "inputs larger than L2" if dec_bytes > L2_BYTES else "fits in L2 (no flush; latency only)"}
+    if kind == "append":
+        return {"workload": name, "new_tokens": int(wl.lens.sum()), "H": wl.H, "D": wl.D, "format": "int4-b64",
+                "table": wl.table, "step": "one kvq_append of all new tokens", "parallelism": par,
+                "l2": "inputs larger than L2"}
+    return {"workload": name, "B": wl.B, "H": wl.H, "Hq": wl.Hq, "D": wl.D, "context": int(wl.lens[0]),
+            "chunk": wl.chunk, "format": FORMAT_NAMES[wl.fmt][1], "step": "one kvq_prefill_attention of every chunk query",
+            "parallelism": par, "l2": "codes (268 MB) larger than L2"}
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle on bounded samples of a workload
+# --------------------------------------------------------------------------
+def _threads():
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def oracle_decode_rate(name, seconds, seed, threads=None):
+    """Oracle decode steps on (sequence, cache head) samples of a decode
+    workload: each sample re-quantizes its open block with the appended token
+    (oracle codec) and attends over L + 1 tokens with the g query heads of that
+    cache head in binary64.  One thread per sample (the oracle releases the
+    GIL).  A token of a sequence needs every cache head, so tokens/s =
+    sample-steps/s / H.  Returns (tokens/s, threads, description)."""
     import numpy as np
 
     from oracle import oracle as orc
-    from quantized_kv_cache_09_gb300.synth import workloads as W
 
-    wl = W.make_workload(cfg or CONFIG, seed=seed, extra_tokens=64)
-    threads = threads or max(1, min(16, os.cpu_count() or 1))
-    L = int(wl.lens[0])
+    wl = _make(name, seed)
+    n = threads or _threads()
+    g = wl.Hq // wl.H
     sm = np.float32(1.0 / math.sqrt(wl.D))
+    units = [(i % wl.B, (i * 5 + i // wl.B) % wl.H) for i in range(n)]
 
-    # untimed setup: the oracle's cache of each sampled sequence's history
-    nseq = min(wl.B, threads)
-    caches = []
-    for b in range(nseq):
-        kc, ks = orc.quantize(wl.fmt, wl.kv_host("k", b, 0, L))
-        vc, vs = orc.quantize(wl.fmt, wl.kv_host("v", b, 0, L))
-        nb = kc.shape[0]
-        kc = np.concatenate([kc, np.zeros_like(kc[:1])])
-        vc = np.concatenate([vc, np.zeros_like(vc[:1])])
-        ks = np.concatenate([ks, np.zeros_like(ks[:1])])
-        vs = np.concatenate([vs, np.zeros_like(vs[:1])])
-        k_new = wl.kv_host("k", b, L, L + 1)
-        v_new = wl.kv_host("v", b, L, L + 1)
-        q = wl.q_host(0)[b:b + 1]
-        caches.append((kc, vc, ks, vs, nb, k_new, v_new, q))
+    def setup(u):  # untimed: the oracle's cache of one (sequence, head) history and the step's inputs
+        b, h = u
+        L = int(wl.lens[b])
+        o = (L // 64) * 64  # first row of the block the new token goes to
+        kc, ks = orc.quantize(wl.fmt, wl.kv_host_head("k", b, h, 0, L)) if L else (None, None)
+        vc, vs = orc.quantize(wl.fmt, wl.kv_host_head("v", b, h, 0, L)) if L else (None, None)
+        nb_full = o // 64
+        rb = orc.row_bytes(wl.fmt, wl.D)
+        kcp = np.zeros((nb_full + 1, 1, 64, rb), np.uint8)
+        vcp = np.zeros_like(kcp)
+        ksp = np.zeros((nb_full + 1, 1), np.float32)
+        vsp = np.zeros_like(ksp)
+        if nb_full:
+            kcp[:nb_full], vcp[:nb_full], ksp[:nb_full], vsp[:nb_full] = kc[:nb_full], vc[:nb_full], ks[:nb_full], vs[:nb_full]
+        k_open = wl.kv_host_head("k", b, h, o, L + 1)
+        v_open = wl.kv_host_head("v", b, h, o, L + 1)
+        q = np.ascontiguousarray(wl.q_host(0)[b:b + 1, h * g:(h + 1) * g])
+        return (kcp, vcp, ksp, vsp, nb_full, k_open, v_open, q, L)
 
-    done = [0] * nseq
+    # (sequentially: the per-token generator calls hold the interpreter lock between calls)
+    caches = [setup(u) for u in units]
+
+    done = [0] * n
     stop = time.time() + seconds
 
     def work(i):
-        kc, vc, ks, vs, nb, k_new, v_new, q = caches[i]
-        bt = np.arange(nb + 1, dtype=np.int32)[None, :]
+        kc, vc, ks, vs, nbf, k_open, v_open, q, L = caches[i]
+        bt = np.arange(nbf + 1, dtype=np.int32)[None, :]
         while time.time() < stop:
-            # append: the new token opens block nb; re-quantize it
-            c, s = orc.quantize(wl.fmt, k_new)
-            kc[nb], ks[nb] = c[0], s[0]
-            c, s = orc.quantize(wl.fmt, v_new)
-            vc[nb], vs[nb] = c[0], s[0]
+            c, s = orc.quantize(wl.fmt, k_open)   # the open block with the new token, re-quantized
+            kc[nbf], ks[nbf] = c[0], s[0]
+            c, s = orc.quantize(wl.fmt, v_open)
+            vc[nbf], vs[nbf] = c[0], s[0]
             orc.decode_attention(wl.fmt, kc, vc, ks, vs, bt, np.array([L + 1]), q, sm)
             done[i] += 1
 
     t0 = time.time()
-    ths = [threading.Thread(target=work, args=(i,)) for i in range(nseq)]
+    ths = [threading.Thread(target=work, args=(i,)) for i in range(n)]
     for t in ths:
         t.start()
     for t in ths:
         t.join()
     el = time.time() - t0
     steps = sum(done)
-    heads = f"{wl.H} heads" if wl.Hq == wl.H else f"{wl.Hq} query heads over {wl.H} cache heads"
-    desc = (f"{steps} oracle sequence-steps (append 1 token + binary64 attention over {L + 1} tokens x "
-            f"{heads}), {nseq} sequences on {nseq} threads for {el:.1f} s")
-    return steps / el, nseq, desc
+    heads = f"{g} query head{'s' if g > 1 else ''}"
+    desc = (f"{steps} oracle (sequence, cache head) steps of {name} (re-quantize the open block with the new "
+            f"token + binary64 attention of {heads} over its L+1 tokens), {n} samples on {n} threads for "
+            f"{el:.1f} s; tokens/s = steps/s / {wl.H} cache heads")
+    return steps / el / wl.H, n, desc
 
 
-# --------------------------------------------------------------------------
+def oracle_append_rate(seconds, seed, threads=None):
+    """The oracle codec on samples of prefill-append: each thread quantizes
+    4096-token x 32-head K and V chunks of its own sequence; GB/s of fp16 read
+    + codes + scales written, as for the GPU.  Returns (GB/s, threads, desc)."""
+    from oracle import oracle as orc
+
+    wl = _make("prefill-append", seed)
+    n = threads or _threads()
+    xs = []
+    for i in range(n):
+        b = i % wl.B
+        xs.append((wl.kv_host("k", b, 0, 1024), wl.kv_host("v", b, 0, 1024)))
+    done = [0] * n
+    stop = time.time() + seconds
+
+    def work(i):
+        k, v = xs[i]
+        while time.time() < stop:
+            orc.quantize(wl.fmt, k)
+            orc.quantize(wl.fmt, v)
+            done[i] += 1
+
+    t0 = time.time()
+    ths = [threading.Thread(target=work, args=(i,)) for i in range(n)]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
+    el = time.time() - t0
+    nbytes = sum(done) * wl.quantize_bytes(1024)
+    return nbytes / el / 1e9, n, f"{sum(done)} oracle quantizations of 1024-token x {wl.H}-head K+V chunks on {n} threads, {el:.1f} s"
+
+
+def oracle_prefill_rate(seconds, seed):
+    """The oracle's chunked-prefill rate on a sample of the workload: queries of
+    sequence 0, every head, each over its causal prefix (binary64), one thread."""
+    import numpy as np
+
+    from oracle import oracle as orc
+
+    wl = _make("chunked-prefill", seed)
+    L, n = int(wl.lens[0]), wl.chunk
+    kc, ks = orc.quantize(wl.fmt, wl.kv_host("k", 0, 0, L))
+    vc, vs = orc.quantize(wl.fmt, wl.kv_host("v", 0, 0, L))
+    bt = np.arange(kc.shape[0], dtype=np.int32)[None, :]
+    t0 = time.time()
+    done = 0
+    while time.time() - t0 < seconds and done < n:
+        i = n - 1 - done
+        orc.decode_attention(wl.fmt, kc, vc, ks, vs, bt, np.array([L - n + i + 1]),
+                             wl.chunk_q_host(0, i, i + 1), np.float32(1.0 / np.sqrt(wl.D)))
+        done += 1
+    el = time.time() - t0
+    return done / el, 1, (f"{done} chunk queries of sequence 0 (all {wl.Hq} heads, causal prefixes of ~{L} tokens, "
+                          f"binary64) in {el:.1f} s")
+
+
+def oracle_rate(name, seconds, seed):
+    kind, _ = WORKLOADS[name]
+    if kind == "decode":
+        return oracle_decode_rate(name, seconds, seed) + ("tokens/s",)
+    if kind == "append":
+        return oracle_append_rate(seconds, seed) + ("GB/s",)
+    return oracle_prefill_rate(seconds, seed) + ("tokens/s",)
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if world > 1 and rank != 0:
         return
-    from quantized_kv_cache_09_gb300.synth import workloads as W
-    name = args.workload if args.workload in ORACLE_WORKLOADS else "llama2-7b-layer"
-    cfg = W.CONFIGS[ORACLE_WORKLOADS[name]]
-    rate, cores, desc = oracle_step_rate(args.cpu_seconds, args.seed, cfg=ORACLE_WORKLOADS[name])
-    line = {"metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1000.0 / rate if rate else None, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": name, "B": cfg["B"], "H": cfg["H"], "Hq": cfg.get("Hq", cfg["H"]), "D": 128,
-                       "context": cfg["L"], "format": "int4-b64", "step": "append 1 token + decode attention"},
+    name = args.workload
+    rate, cores, desc, unit = oracle_rate(name, args.cpu_seconds, args.seed)
+    line = {"metric": METRIC if WORKLOADS[name][0] != "prefill" else PREFILL_METRIC, "value": rate, "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, f32 codec", "data": "synthetic",
+            "config": workload_config(name, world, args.seed, args.prefill_seqs),
             "impl": "reference",
-            "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
-            "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": rate, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-DECODE_WORKLOADS = {"tiny": 1, "llama2-7b-layer": 2, "long-context": 3, "paged-int8": 4,
-                    "llama3-8b-layer-gqa": 6, "llama2-7b-layer-fp8": 7}
-FORMAT_NAMES = {0: ("int4", "int4-b64"), 1: ("int8", "int8-page"), 2: ("fp8-e4m3", "fp8-e4m3-page")}
-# workloads whose cpu_baseline / reference arm samples their own shape (uniform lengths)
-ORACLE_WORKLOADS = {"llama2-7b-layer": 2, "llama3-8b-layer-gqa": 6}
+PREFILL_METRIC = "chunked-prefill attention tokens/s over the quantized cache (tensor roofline)"
 
 
+# --------------------------------------------------------------------------
+# GPU measurements
+# --------------------------------------------------------------------------
 def _sync_all(pg, dev):
     import torch
     torch.cuda.synchronize(dev)
@@ -296,7 +446,7 @@ def _sync_all(pg, dev):
         pg.barrier()
 
 
-def measure_decode(name, K, Wm, seed, dev, pg):
+def measure_decode(name, K, Wm, seed, dev, pg, clocks=None, graph=True):
     """Decode steps (append one token per sequence + decode attention) on a
     decode workload.  64-aligned histories cycle the appended position through
     one block (a real decode progression); ragged histories re-append the token
@@ -306,9 +456,8 @@ def measure_decode(name, K, Wm, seed, dev, pg):
 
     from quantized_kv_cache_09_gb300 import kvq
     from quantized_kv_cache_09_gb300.runner import DecodeStep, DeviceWorkload
-    from quantized_kv_cache_09_gb300.synth import workloads as W
 
-    wl = W.make_workload(DECODE_WORKLOADS[name], seed=seed, extra_tokens=64)
+    wl = _make(name, seed)
     dw = DeviceWorkload(wl, device=dev)
     dw.prefill(max_tokens_per_call=1 << 18)
     B, H, D, Hq = wl.B, wl.H, wl.D, wl.Hq
@@ -334,13 +483,10 @@ def measure_decode(name, K, Wm, seed, dev, pg):
     torch.cuda.synchronize(dev)
     rc, flags = kvq.kvq_get_device_status(dw.cache)
     if rc != 0:
-        raise RuntimeError(f"device status {rc} flags {flags:#x} after warm-up")
+        raise RuntimeError(f"{name}: device status {rc} flags {flags:#x} after warm-up")
 
     stream = torch.cuda.current_stream(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    clocks = ClockSampler(dev.index or 0)
-    clocks.start()
-    time.sleep(0.3)
     _sync_all(pg, dev)
     t_wall0 = time.time()
     # (1) the headline: K whole steps back to back, events only around them, so
@@ -352,9 +498,10 @@ def measure_decode(name, K, Wm, seed, dev, pg):
         s = (Wm + i) % NS
         kvq.kvq_append(dw.cache, k_steps[s], v_steps[s], step.cu, dw.block_table, lens_b[s], 1)
         kvq.kvq_decode_attention_gqa(dw.cache, q_steps[s], dw.block_table, lens_a[s], dw.softmax_scale, step.out,
-                                 dw.workspace)
+                                     dw.workspace)
     end.record(stream)
     _sync_all(pg, dev)
+    t_wall1 = time.time()
     total_ms = start.elapsed_time(end)
     # (2) the same K steps again with an event before, between and after the two
     # calls: each call's own duration (the events serialise the launches)
@@ -365,85 +512,120 @@ def measure_decode(name, K, Wm, seed, dev, pg):
         kvq.kvq_append(dw.cache, k_steps[s], v_steps[s], step.cu, dw.block_table, lens_b[s], 1)
         e1.record(stream)
         kvq.kvq_decode_attention_gqa(dw.cache, q_steps[s], dw.block_table, lens_a[s], dw.softmax_scale, step.out,
-                                 dw.workspace)
+                                     dw.workspace)
         e2.record(stream)
     _sync_all(pg, dev)
-    clocks.window = (t_wall0, time.time())
+    if clocks is not None:
+        clocks.window = (t_wall0, max(time.time(), t_wall1))
     app_ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
     dec_ms = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(K)) / K
     split_ms = ev[0][0].elapsed_time(ev[K - 1][2])
     rc, flags = kvq.kvq_get_device_status(dw.cache)
     if rc != 0:
-        raise RuntimeError(f"device status {rc} flags {flags:#x} after timed steps")
-    # (3) the steps replayed from one CUDA graph holding the 64-step input cycle
-    # (kvq_step_graph, captured before the timed loop): ceil(K / 64) replays
-    graph = kvq.StepGraph([step.graph_step(lens_b[s], lens_a[s], k_steps[s], v_steps[s], q_steps[s])
-                           for s in range(NS)])
-    graph.launch()
-    _sync_all(pg, dev)
-    reps = -(-K // NS)
-    g_s = torch.cuda.Event(enable_timing=True)
-    g_e = torch.cuda.Event(enable_timing=True)
-    g_s.record(stream)
-    for i in range(reps):
-        graph.launch()
-    g_e.record(stream)
-    _sync_all(pg, dev)
-    graph_ms = g_s.elapsed_time(g_e) * K / (reps * NS)  # per K steps
-    graph.close()
-    rc, flags = kvq.kvq_get_device_status(dw.cache)
-    if rc != 0:
-        raise RuntimeError(f"device status {rc} flags {flags:#x} after graph steps")
+        raise RuntimeError(f"{name}: device status {rc} flags {flags:#x} after timed steps")
+    dec_bytes = sum(wl.decode_bytes(decode_ctx_lens(wl, Wm + K + i)) for i in range(K)) / K
 
-    # end to end through the C ABI with host buffers
+    graph_ms = None
+    if graph:
+        # (3) the steps replayed from one CUDA graph holding the 64-step input
+        # cycle (kvq_step_graph, captured before the timing): ceil(K / 64) replays
+        g = kvq.StepGraph([step.graph_step(lens_b[s], lens_a[s], k_steps[s], v_steps[s], q_steps[s])
+                           for s in range(NS)])
+        g.launch()
+        _sync_all(pg, dev)
+        reps = -(-K // NS)
+        g_s = torch.cuda.Event(enable_timing=True)
+        g_e = torch.cuda.Event(enable_timing=True)
+        g_s.record(stream)
+        for _ in range(reps):
+            g.launch()
+        g_e.record(stream)
+        _sync_all(pg, dev)
+        graph_ms = g_s.elapsed_time(g_e) * K / (reps * NS)  # per K steps
+        g.close()
+        rc, flags = kvq.kvq_get_device_status(dw.cache)
+        if rc != 0:
+            raise RuntimeError(f"{name}: device status {rc} flags {flags:#x} after graph steps")
+
+    # (4) end to end through the C ABI with host buffers.  A copy stream runs one
+    # step ahead: it brings step i+1's new rows and query from pinned memory
+    # while step i computes, and copies step i's output back once it is done; the
+    # compute stream waits only for events, so consecutive kernels keep their
+    # programmatic-launch overlap.  Inputs and outputs are double-buffered.
     pin_k = [k.cpu().pin_memory() for k in k_steps]
     pin_v = [v.cpu().pin_memory() for v in v_steps]
     pin_q = [q.cpu().pin_memory() for q in q_steps]
-    pin_o = torch.empty((B, Hq, D), dtype=torch.float16).pin_memory()
-    dk, dv, dq = (torch.empty_like(k_steps[0]), torch.empty_like(v_steps[0]), torch.empty_like(q_steps[0]))
-    Ke = max(1, K // 2)
+    pin_o = [torch.empty((B, Hq, D), dtype=torch.float16).pin_memory() for _ in range(2)]
+    dk = [torch.empty_like(k_steps[0]) for _ in range(2)]
+    dv = [torch.empty_like(v_steps[0]) for _ in range(2)]
+    dq = [torch.empty_like(q_steps[0]) for _ in range(2)]
+    outs = [torch.empty((B, Hq, D), dtype=torch.float16, device=dev) for _ in range(2)]
+    copy = torch.cuda.Stream(dev)
+    h2d = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    d2h = [torch.cuda.Event() for _ in range(2)]
+    Ke = K
+    base = Wm + 2 * K
+
+    def stage(i, slot):
+        s = (base + i) % NS
+        with torch.cuda.stream(copy):
+            dk[slot].copy_(pin_k[s], non_blocking=True)
+            dv[slot].copy_(pin_v[s], non_blocking=True)
+            dq[slot].copy_(pin_q[s], non_blocking=True)
+            h2d[slot].record(copy)
+
     _sync_all(pg, dev)
     e2e_s = torch.cuda.Event(enable_timing=True)
     e2e_e = torch.cuda.Event(enable_timing=True)
     e2e_s.record(stream)
+    copy.wait_event(e2e_s)
+    stage(0, 0)
     for i in range(Ke):
-        s = (Wm + 2 * K + i) % NS
-        dk.copy_(pin_k[s], non_blocking=True)
-        dv.copy_(pin_v[s], non_blocking=True)
-        dq.copy_(pin_q[s], non_blocking=True)
-        kvq.kvq_append(dw.cache, dk, dv, step.cu, dw.block_table, lens_b[s], 1)
-        kvq.kvq_decode_attention_gqa(dw.cache, dq, dw.block_table, lens_a[s], dw.softmax_scale, step.out,
+        slot = i & 1
+        s = (base + i) % NS
+        if i + 1 < Ke:
+            if i >= 1:
+                copy.wait_event(done[1 - slot])  # step i-1 is done with that slot's inputs
+            stage(i + 1, 1 - slot)
+        stream.wait_event(h2d[slot])
+        if i >= 2:
+            stream.wait_event(d2h[slot])  # step i-2's output has been read back
+        kvq.kvq_append(dw.cache, dk[slot], dv[slot], step.cu, dw.block_table, lens_b[s], 1)
+        kvq.kvq_decode_attention_gqa(dw.cache, dq[slot], dw.block_table, lens_a[s], dw.softmax_scale, outs[slot],
                                      dw.workspace)
-        pin_o.copy_(step.out, non_blocking=True)
+        done[slot].record(stream)
+        copy.wait_event(done[slot])
+        with torch.cuda.stream(copy):
+            pin_o[slot].copy_(outs[slot], non_blocking=True)
+            d2h[slot].record(copy)
+    stream.wait_stream(copy)
     e2e_e.record(stream)
     _sync_all(pg, dev)
     e2e_ms = e2e_s.elapsed_time(e2e_e)
-    clocks.stop()
+    rc, flags = kvq.kvq_get_device_status(dw.cache)
+    if rc != 0:
+        raise RuntimeError(f"{name}: device status {rc} flags {flags:#x} after end-to-end steps")
 
-    ctx = [(wl.lens + ((Wm + K + i) % NS if aligned else 0) + 1) for i in range(K)]
-    dec_bytes = sum(wl.decode_bytes(c) for c in ctx) / K
-    res = dict(wl=wl, B=B, H=H, D=D, aligned=aligned, total_ms=total_ms, app_ms=app_ms, dec_ms=dec_ms, graph_ms=graph_ms,
-               e2e_ms=e2e_ms, Ke=Ke, dec_bytes=dec_bytes, clocks=clocks.summary(), split_ms=split_ms,
-               h2d=(2 * H + Hq) * B * D * 2, d2h=B * Hq * D * 2, launches=(1 + -(-B // 512)) * K, Hq=Hq)
+    res = dict(wl=wl, B=B, H=H, D=D, Hq=Hq, aligned=aligned, total_ms=total_ms, app_ms=app_ms, dec_ms=dec_ms,
+               graph_ms=graph_ms, e2e_ms=e2e_ms, Ke=Ke, dec_bytes=dec_bytes, split_ms=split_ms,
+               h2d=(2 * H + Hq) * B * D * 2, d2h=B * Hq * D * 2, launches=(1 + -(-B // 512)) * K)
     del dw
     torch.cuda.empty_cache()
     return res
 
 
-def measure_prefill(K, Wm, seed, dev, nseqs=64):
+def measure_append(K, Wm, seed, dev, nseqs=64):
     """prefill-append: one kvq_append of nseqs x 4096 new tokens (H=32) into
     randomly permuted empty pages; repeated calls write the same bytes."""
     import torch
 
     from quantized_kv_cache_09_gb300 import kvq
     from quantized_kv_cache_09_gb300.runner import DeviceWorkload
-    from quantized_kv_cache_09_gb300.synth import workloads as W
 
-    c = W.CONFIGS[5]
-    wl = W.Workload(nseqs, c["H"], c["D"], [c["L"]] * nseqs, c["fmt"], c["sigma"], None, "permuted", seed,
-                    0, c["name"])
+    wl = _make("prefill-append", seed, nseqs)
     dw = DeviceWorkload(wl, device=dev)
-    L = c["L"]
+    L = int(wl.lens[0])
     k_new = torch.empty((nseqs * L, wl.H, wl.D), dtype=torch.float16, device=dev)
     v_new = torch.empty_like(k_new)
     for b in range(nseqs):
@@ -464,7 +646,7 @@ def measure_prefill(K, Wm, seed, dev, nseqs=64):
     ms = sum(a.elapsed_time(b) for a, b in ev) / K
     rc, flags = kvq.kvq_get_device_status(dw.cache)
     if rc != 0:
-        raise RuntimeError(f"device status {rc} flags {flags:#x} in prefill-append")
+        raise RuntimeError(f"prefill-append: device status {rc} flags {flags:#x}")
     nbytes = wl.quantize_bytes(L) * nseqs
     del k_new, v_new, dw
     torch.cuda.empty_cache()
@@ -478,9 +660,8 @@ def measure_chunked_prefill(K, Wm, seed, dev):
 
     from quantized_kv_cache_09_gb300 import kvq
     from quantized_kv_cache_09_gb300.runner import DeviceWorkload
-    from quantized_kv_cache_09_gb300.synth import workloads as W
 
-    wl = W.make_workload(8, seed=seed)
+    wl = _make("chunked-prefill", seed)
     dw = DeviceWorkload(wl, device=dev)
     dw.prefill(max_tokens_per_call=1 << 16)
     n = wl.chunk
@@ -495,64 +676,119 @@ def measure_chunked_prefill(K, Wm, seed, dev):
         kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out, workspace=ws)
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
-    clocks = ClockSampler(dev.index or 0)
-    clocks.start()
-    time.sleep(0.3)
-    t_wall0 = time.time()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         ev[i][0].record(stream)
         kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out, workspace=ws)
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    clocks.window = (t_wall0, time.time())
     ms = sum(a.elapsed_time(b) for a, b in ev) / K
     # end to end: the chunk's queries from pinned host memory, the output back
     pin_q = q.cpu().pin_memory()
     pin_o = torch.empty_like(pin_q).pin_memory()
     e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    Ke = max(1, K // 2)
     e_s.record(stream)
-    for _ in range(Ke):
+    for _ in range(K):
         q.copy_(pin_q, non_blocking=True)
         kvq.kvq_prefill_attention(dw.cache, q, cu, n, dw.block_table, dw.lens, dw.softmax_scale, out, workspace=ws)
         pin_o.copy_(out, non_blocking=True)
     e_e.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e_s.elapsed_time(e_e) / Ke
-    clocks.stop()
+    e2e_ms = e_s.elapsed_time(e_e) / K
     rc, flags = kvq.kvq_get_device_status(dw.cache)
     if rc != 0:
-        raise RuntimeError(f"device status {rc} flags {flags:#x} in chunked-prefill")
-    res = dict(ms=ms, e2e_ms=e2e_ms, flops=wl.prefill_flops(), tokens=wl.B * n, B=wl.B, H=wl.H, Hq=wl.Hq, n=n,
-               L=int(wl.lens[0]), qbytes=q.numel() * 2, clocks=clocks.summary())
+        raise RuntimeError(f"chunked-prefill: device status {rc} flags {flags:#x}")
+    res = dict(ms=ms, e2e_ms=e2e_ms, flops=wl.prefill_flops(), tokens=wl.B * n, qbytes=q.numel() * 2)
     del dw, q, out
     torch.cuda.empty_cache()
     return res
 
 
-def oracle_prefill_rate(seconds, seed):
-    """The oracle's chunked-prefill rate on a sample of the workload: queries of
-    sequence 0, every head, each over its causal prefix (binary64), one thread."""
-    import numpy as np
+# --------------------------------------------------------------------------
+# result lines
+# --------------------------------------------------------------------------
+def decode_result(name, r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed=0):
+    total_ms = max_over_ranks(pg, r["total_ms"], dev)
+    e2e_ms = max_over_ranks(pg, r["e2e_ms"], dev)
+    dec_ms = max_over_ranks(pg, r["dec_ms"], dev)
+    app_ms = max_over_ranks(pg, r["app_ms"], dev)
+    B = r["B"]
+    achieved = r["dec_bytes"] / (dec_ms * 1e-3) / 1e9
+    out = {"metric": METRIC, "value": whole_job_rate(world, B * K, total_ms * 1e-3), "unit": "tokens/s",
+           "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": FORMAT_NAMES[r["wl"].fmt][0] + " codes, fp32 math",
+           "data": "synthetic (seeded generator in HBM)",
+           "config": workload_config(name, world, cfg_seed),
+           "kv_gb_per_s": achieved, "decode_us": dec_ms * 1e3, "append_us": app_ms * 1e3,
+           "step_us_events_between_calls": r["split_ms"] / K * 1e3,
+           "roofline": {"kernel": "kvq_decode_attention (decode_split_kernel, merge fused)", "bound": "hbm",
+                        "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                        "frac": achieved / peak, "traffic": ncu_traffic("decode_split_kernel", name),
+                        "algorithmic_bytes_per_launch": r["dec_bytes"],
+                        "timing": "mean CUDA-event time of one kvq_decode_attention call (events on the launching "
+                                  "stream between calls)"},
+           "e2e": {"value": whole_job_rate(world, B * r["Ke"], e2e_ms * 1e-3), "unit": "tokens/s",
+                   "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                   "how": "pinned host -> device copies of each step's new K/V rows and query and the output back, "
+                          "on a copy stream one step ahead"},
+           "gpu_launches": r["launches"]}
+    if r["graph_ms"] is not None:
+        graph_ms = max_over_ranks(pg, r["graph_ms"], dev)
+        out["graph"] = {"ms_per_step": graph_ms / K, "value": whole_job_rate(world, B * K, graph_ms * 1e-3),
+                        "unit": "tokens/s", "how": "one kvq_step_graph of 64 steps (append + decode each), replayed"}
+    return out
 
-    from oracle import oracle as orc
-    from quantized_kv_cache_09_gb300.synth import workloads as W
 
-    wl = W.make_workload(8, seed=seed)
-    L, n = int(wl.lens[0]), wl.chunk
-    kc, ks = orc.quantize(wl.fmt, wl.kv_host("k", 0, 0, L))
-    vc, vs = orc.quantize(wl.fmt, wl.kv_host("v", 0, 0, L))
-    bt = np.arange(kc.shape[0], dtype=np.int32)[None, :]
-    t0 = time.time()
-    done = 0
-    while time.time() - t0 < seconds and done < n:
-        i = n - 1 - done
-        orc.decode_attention(wl.fmt, kc, vc, ks, vs, bt, np.array([L - n + i + 1]),
-                             wl.chunk_q_host(0, i, i + 1), np.float32(1.0 / np.sqrt(wl.D)))
-        done += 1
-    el = time.time() - t0
-    return done / el, 1, f"{done} chunk queries of sequence 0 (all {wl.Hq} heads, causal prefixes of ~{L} tokens, binary64) in {el:.1f} s"
+def append_result(r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed=0, prefill_seqs=64):
+    ms = max_over_ranks(pg, r["ms"], dev)
+    gbs = r["bytes"] / (ms * 1e-3) / 1e9
+    return {"metric": METRIC, "value": whole_job_rate(world, r["bytes"] / 1e9, ms * 1e-3), "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp16 in, int4 codes out, fp32 math",
+            "data": "synthetic (seeded generator in HBM)", "config": workload_config("prefill-append", world, cfg_seed, prefill_seqs),
+            "roofline": {"kernel": "append_kernel", "bound": "hbm", "achieved": gbs, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": ncu_traffic("append_kernel", "prefill-append"),
+                         "algorithmic_bytes_per_launch": r["bytes"]},
+            "gpu_launches": K}
+
+
+def prefill_result(r, world, pg, dev, K, Wm, cfg_seed=0):
+    ms = max_over_ranks(pg, r["ms"], dev)
+    e2e_ms = max_over_ranks(pg, r["e2e_ms"], dev)
+    tflops = r["flops"] / (ms * 1e-3) / 1e12
+    tpeak, tkind = measured_tensor_peak()
+    return {"metric": PREFILL_METRIC, "value": whole_job_rate(world, r["tokens"], ms * 1e-3), "unit": "tokens/s",
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4 codes, fp16 MMA operands, fp32 accumulation",
+            "data": "synthetic (seeded generator in HBM)", "config": workload_config("chunked-prefill", world, cfg_seed),
+            "tflops": tflops,
+            "roofline": {"kernel": "prefill_attn_tc_kernel", "bound": "tensor", "achieved": tflops, "peak": tpeak,
+                         "peak_kind": tkind, "unit": "TFLOP/s", "frac": tflops / tpeak,
+                         "traffic": ncu_traffic("prefill_attn_tc_kernel", "chunked-prefill"),
+                         "algorithmic_flops_per_launch": r["flops"]},
+            "e2e": {"value": whole_job_rate(world, r["tokens"], e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": r["qbytes"], "d2h_bytes_per_step": r["qbytes"]},
+            "gpu_launches": K}
+
+
+def measure(name, K, Wm, seed, dev, pg, world, clocks=None, prefill_seqs=64, cfg_seed=0):
+    """One workload's result dict.  seed: this rank's inputs; cfg_seed: the
+    base seed the `config` is described with (the same in both arms)."""
+    peak, peak_kind = measured_peak()
+    kind, _ = WORKLOADS[name]
+    if kind == "decode":
+        r = measure_decode(name, K, Wm, seed, dev, pg, clocks=clocks)
+        return decode_result(name, r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed)
+    if kind == "append":
+        r = measure_append(K, max(Wm, 1), seed, dev, prefill_seqs)
+        return append_result(r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed, prefill_seqs)
+    r = measure_chunked_prefill(K, max(Wm, 1), seed, dev)
+    return prefill_result(r, world, pg, dev, K, Wm, cfg_seed)
+
+
+SUB_KEYS = ("value", "unit", "ms_per_step", "steps", "decode_us", "append_us", "kv_gb_per_s", "tflops", "roofline",
+            "e2e", "graph", "config")
 
 
 def run_ours(args):
@@ -569,103 +805,32 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     seed = rank_seed(args.seed, rank)
-    peak, peak_kind = measured_peak()
-
     K, Wm = args.steps, args.warmup
-    if args.workload == "prefill-append":
-        r = measure_prefill(K, max(Wm, 1), seed, dev, args.prefill_seqs)
-        ms = max_over_ranks(pg, r["ms"], dev)
-        gbs = r["bytes"] / (ms * 1e-3) / 1e9
-        line = {"metric": METRIC, "value": whole_job_rate(world, r["bytes"] / 1e9, ms * 1e-3), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm,
-                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "fp16 in, int4 codes out, fp32 math", "data": "synthetic (seeded generator in HBM)",
-                "config": {"workload": "prefill-append", "new_tokens": r["tokens"], "H": 32, "D": 128,
-                           "format": "int4-b64", "step": "one kvq_append of all new tokens"},
-                "roofline": {"kernel": "append_kernel", "bound": "hbm", "achieved": gbs, "peak": peak,
-                             "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
-                             "traffic": ncu_traffic("append_kernel", "prefill-append"), "algorithmic_bytes_per_launch": r["bytes"]},
-                "gpu_launches": K}
-        if rank == 0:
-            print(json.dumps(line), flush=True)
-        if pg:
-            pg.destroy_process_group()
-        return
 
-    if args.workload == "chunked-prefill":
-        r = measure_chunked_prefill(K, max(Wm, 1), seed, dev)
-        ms = max_over_ranks(pg, r["ms"], dev)
-        e2e_ms = max_over_ranks(pg, r["e2e_ms"], dev)
-        tflops = r["flops"] / (ms * 1e-3) / 1e12
-        tpeak, tkind = measured_tensor_peak()
-        line = {"metric": "chunked-prefill attention tokens/s over the quantized cache (tensor roofline)",
-                "value": whole_job_rate(world, r["tokens"], ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
-                "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "int4 codes, fp16 MMA operands, fp32 accumulation",
-                "data": "synthetic (seeded generator in HBM)",
-                "config": {"workload": "chunked-prefill", "B": r["B"], "H": r["H"], "Hq": r["Hq"], "D": 128,
-                           "context": r["L"], "chunk": r["n"], "format": "int4-b64",
-                           "step": "one kvq_prefill_attention of every chunk query",
-                           "l2": "codes (268 MB) larger than L2"},
-                "tflops": tflops,
-                "roofline": {"kernel": "prefill_attn_tc_kernel", "bound": "tensor", "achieved": tflops, "peak": tpeak,
-                             "peak_kind": tkind, "unit": "TFLOP/s", "frac": tflops / tpeak,
-                             "traffic": ncu_traffic("prefill_attn_tc_kernel", "chunked-prefill"),
-                             "algorithmic_flops_per_launch": r["flops"]},
-                "e2e": {"value": whole_job_rate(world, r["tokens"], e2e_ms * 1e-3), "unit": "tokens/s",
-                        "h2d_bytes_per_step": r["qbytes"], "d2h_bytes_per_step": r["qbytes"]},
-                "gpu_launches": K, "clocks": r["clocks"]}
-        if rank == 0 and not args.no_cpu_baseline:
-            rate, cores, desc = oracle_prefill_rate(args.cpu_seconds, args.seed)
-            line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                    "sample": desc}
-        if rank == 0:
-            print(json.dumps(line), flush=True)
-        if pg:
-            pg.destroy_process_group()
-        return
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    line = measure(args.workload, K, Wm, seed, dev, pg, world, clocks=clocks, prefill_seqs=args.prefill_seqs,
+                   cfg_seed=args.seed)
+    if clocks.window == (0.0, 0.0):
+        clocks.window = (t0, time.time())
+    clocks.stop()
+    line["clocks"] = clocks.summary()
 
-    r = measure_decode(args.workload, K, Wm, seed, dev, pg)
-    total_ms = max_over_ranks(pg, r["total_ms"], dev)
-    e2e_ms = max_over_ranks(pg, r["e2e_ms"], dev)
-    dec_ms = max_over_ranks(pg, r["dec_ms"], dev)
-    app_ms = max_over_ranks(pg, r["app_ms"], dev)
-    graph_ms = max_over_ranks(pg, r["graph_ms"], dev)
-    B = r["B"]
-    wl = r["wl"]
-    achieved = r["dec_bytes"] / (dec_ms * 1e-3) / 1e9
-    value = whole_job_rate(world, B * K, total_ms * 1e-3)
-    lens = wl.lens
-    ctx = (f"{int(lens[0]) + 1}..{int(lens[0]) + 64}" if r["aligned"] and lens.min() == lens.max()
-           else f"{int(lens.min()) + 1}..{int(lens.max()) + 1} (sum {int(lens.sum()) + len(lens)})")
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
-            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": FORMAT_NAMES[wl.fmt][0] + " codes, fp32 math",
-            "data": "synthetic (seeded generator in HBM)",
-            "config": {"workload": args.workload, "B": B, "H": r["H"], "Hq": r["Hq"], "D": r["D"], "context": ctx,
-                       "format": FORMAT_NAMES[wl.fmt][1],
-                       "step": "append 1 token + decode attention",
-                       "parallelism": f"replicas x{world} (sequence-sharded, no collective)",
-                       "l2": "inputs larger than L2" if r["dec_bytes"] > 129e6 else "fits in L2 (no flush)"},
-            "kv_gb_per_s": achieved, "decode_us": dec_ms * 1e3, "append_us": app_ms * 1e3,
-            "step_us_events_between_calls": r["split_ms"] / K * 1e3,
-            "graph": {"ms_per_step": graph_ms / K, "value": whole_job_rate(world, B * K, graph_ms * 1e-3),
-                      "unit": "tokens/s", "how": "one kvq_step_graph of 64 steps (append + decode each), replayed"},
-            "roofline": {"kernel": "kvq_decode_attention (decode_split_kernel, merge fused)", "bound": "hbm",
-                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": ncu_traffic("decode_split_kernel", args.workload),
-                         "algorithmic_bytes_per_launch": r["dec_bytes"]},
-            "e2e": {"value": whole_job_rate(world, B * r["Ke"], e2e_ms * 1e-3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            "gpu_launches": r["launches"], "clocks": r["clocks"]}
-    if args.extras and args.workload == "llama2-7b-layer":
-        q = measure_prefill(5, 2, seed, dev, args.prefill_seqs)
-        qms = max_over_ranks(pg, q["ms"], dev)
-        qg = q["bytes"] / (qms * 1e-3) / 1e9
-        line["quantize"] = {"workload": "prefill-append", "new_tokens": q["tokens"], "gb_per_s": qg,
-                            "frac": qg / peak, "ms": qms}
+    if args.extras:
+        subs = {}
+        Ks = max(args.sub_steps, 3)
+        for name in WORKLOADS:
+            if name == args.workload:
+                continue
+            r = measure(name, Ks, max(Wm, 3), seed, dev, pg, world, prefill_seqs=args.prefill_seqs,
+                        cfg_seed=args.seed)
+            subs[name] = {k: r[k] for k in SUB_KEYS if k in r}
+        line["workloads"] = subs
     if rank == 0 and not args.no_cpu_baseline:
-        rate, cores, desc = oracle_step_rate(args.cpu_seconds, args.seed, cfg=ORACLE_WORKLOADS.get(args.workload))
-        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+        rate, cores, desc, unit = oracle_rate(args.workload, args.cpu_seconds, args.seed)
+        line["cpu_baseline"] = {"value": rate, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:

@@ -206,10 +206,17 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
  *   q, out           fp16 [num_seqs][num_q_heads][head_dim], 16-byte aligned
  *   workspace        >= kvq_decode_workspace_bytes_gqa(...) bytes, zero-filled
  *                    once before first use (as for kvq_decode_attention)
- * g = 1 is kvq_decode_attention.  Supported: g = 1 for every format, g = 2 and
- * 4 for KVQ_INT4_B64; other g return KVQ_ERR_UNSUPPORTED, and num_q_heads not
- * a multiple of cache->num_heads returns KVQ_ERR_INVALID_ARG.  Other errors as
- * for kvq_decode_attention.
+ * g = 1 is kvq_decode_attention.  Every format takes any g from 1 to 1024.
+ * Two kernels serve it: for int4 with g = 2 or 4 the multi-head kernel carries
+ * the group's heads in the spare columns of its MMAs (one launch); every other
+ * g > 1 runs tiles of up to 16 query heads of one cache head as the rows of
+ * the MMAs (a group of more than 16 heads is several tiles, each streaming
+ * its cache head's codes), and a second, small launch merges the split
+ * pieces.  In that path the probabilities enter the PV product as fp16.
+ * num_q_heads not a multiple of cache->num_heads returns KVQ_ERR_INVALID_ARG;
+ * g > 1024, or a problem whose work units overflow 32 bits (at most 512
+ * sequences x unit heads x 4 units per page), KVQ_ERR_UNSUPPORTED.  Other
+ * errors as for kvq_decode_attention.
  */
 size_t kvq_decode_workspace_bytes_gqa(kvq_format fmt, int32_t num_kv_heads, int32_t num_q_heads,
                                       int32_t head_dim);
@@ -227,22 +234,22 @@ kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, i
  * that cannot afford the device-wide synchronisation cudaMalloc / cudaFree
  * may cause.  It allocates nothing.
  *
- * The scratch is one fixed array of KVQ_NOALLOC_SCRATCH_BYTES (16 MiB) of
+ * The scratch is one fixed array of KVQ_NOALLOC_SCRATCH_BYTES (4 MiB) of
  * device memory inside the library; every GPU that loads the library holds it
  * until the process exits.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress, with that device current) and keeps
  * it, so make that first call before any stream capture.  A device whose split
- * grid needs more scratch than the array (about 250 SMs' worth of split
- * partials; a 152-SM GB300 needs 9.7 MB) gets KVQ_ERR_WORKSPACE.  Every call
+ * grid needs more scratch than the array (about 320 SMs' worth of split
+ * partials; a 152-SM GB300 needs 1.95 MB) gets KVQ_ERR_WORKSPACE.  Every call
  * uses the same array and it keeps the last call's contents: calls that may
  * overlap on the GPU (other streams, other threads) race on it, so the caller
  * must serialise them.  The split's counters in the array must be zero when a
  * launch starts: each call clears them first on `stream` (a memset of about
- * 100 KB, no allocation), so a call that was cut short (a bounded wait that
+ * 20 KB, no allocation), so a call that was cut short (a bounded wait that
  * ran out) does not spoil later ones.  Arguments, results and other errors
  * are those of kvq_decode_attention.
  */
-#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define KVQ_NOALLOC_SCRATCH_BYTES (4u << 20)
 kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const uint16_t *q, const int32_t *block_table,
                                         int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
                                         float softmax_scale, uint16_t *out, kvq_stream_t stream);

@@ -154,6 +154,11 @@ kvq_status kvq_decode_attention_gqa(const kvq_cache *cache, const uint16_t *q, i
     if (max_blocks_per_seq > (1 << 22)) return KVQ_ERR_UNSUPPORTED;
     const int g = group_of(cache->fmt, cache->num_heads, num_q_heads);
     if (g == 0) return KVQ_ERR_UNSUPPORTED;
+    {  // the units of one launch (at most 4 per page, per unit head) are counted in 32 bits
+        const int64_t unit_heads = (int64_t)cache->num_heads * (g == 1 || g == 2 || g == 4 ? 1 : (g + 15) / 16);
+        const int64_t seqs = num_seqs < kvq::kMaxSeqsPerLaunch ? num_seqs : kvq::kMaxSeqsPerLaunch;
+        if ((int64_t)max_blocks_per_seq * 4 * unit_heads * seqs > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+    }
     if (num_seqs == 0) return KVQ_OK;
     if (!q || !block_table || !seq_lens || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
     const size_t need = kvq::decode_workspace_bytes(cache->fmt, g);

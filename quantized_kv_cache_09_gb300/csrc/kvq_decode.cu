@@ -76,14 +76,12 @@ template <>
 struct DecFmt<KVQ_FP8_E4M3> : DecFmt<KVQ_INT8_PAGE> {
 };
 
-// what a stage holds: units c .. c + nunits - 1 of (b, h), ntok tokens in all,
-// of split piece `piece`; new_seg: the first chunk of a segment (a new
-// (sequence, head) or a new piece)
+// what a stage holds: units c .. c + nunits - 1 of (b, h), ntok tokens in all;
+// new_seg: the first chunk of a segment (the warp's first, or a new (sequence, head))
 struct alignas(16) StageMeta {
     int32_t b, h, c, ntok;
     float sk, sv;
     int32_t new_seg, nunits;
-    int32_t piece, pad[3];
 };
 
 template <int kStages, int kStageBytes, int kQRows>
@@ -96,11 +94,22 @@ struct alignas(128) WarpSmem {
 };
 
 constexpr size_t kSeqSmemBytes = ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 64 + 127) / 128 * 128;
+// the group value of the tile consumer (16 query heads per tile, any group size)
+constexpr int kMqG = 16;
+constexpr int kMqRows = 16;
+// warps of a decode CTA: the tile consumer's stages carry 16 query rows, so
+// fewer warps fit in shared memory (and each has more registers)
+template <int FMT, int G>
+struct DecShape {
+    static constexpr int kWarps = G == kMqG ? 8 : DecFmt<FMT>::kWarps;
+    static constexpr int kQRows = G == kMqG ? kMqRows : G;
+};
 template <int FMT, int G>
 constexpr size_t dec_smem_bytes()
 {
     using F = DecFmt<FMT>;
-    return F::kWarps * sizeof(WarpSmem<F::kStages, F::kUnitsPerStage * kUnitBytes, G>) + kSeqSmemBytes;
+    using S = DecShape<FMT, G>;
+    return S::kWarps * sizeof(WarpSmem<F::kStages, F::kUnitsPerStage * kUnitBytes, S::kQRows>) + kSeqSmemBytes;
 }
 
 // ---------------------------------------------------------------------------
@@ -254,6 +263,9 @@ __device__ __forceinline__ void hi_lo_pairs(uint64_t x, uint32_t &hi, uint32_t &
 // qk of the next unit with pv of this one.
 template <>
 struct Consumer<KVQ_INT4_B64> {
+    static constexpr int kScores = 4;
+    static constexpr int kPf = 4;
+    int rows;  // (unused: one query row)
     uint32_t qb[8][2];
     float acc[8][4];
     float m_run;
@@ -448,6 +460,9 @@ struct Consumer<KVQ_INT4_B64> {
 template <int G>
 struct ConsumerGqa {
     static_assert(G == 2 || G == 4, "query heads per cache head");
+    static constexpr int kScores = 8;
+    static constexpr int kPf = 4;
+    int rows;  // (unused: G query rows)
     uint32_t qb[8][2];
     float acc[8][4];
     float m_run[2];
@@ -666,6 +681,9 @@ struct ConsumerGqa {
 // shuffled from the lanes that scored them.
 template <int FMT>
 struct ConsumerBytes {
+    static constexpr int kScores = 4;
+    static constexpr int kPf = 4;
+    int rows;  // (unused: one query row)
     float qf[16];
     float acc[16];
     float m_run;
@@ -796,74 +814,355 @@ struct Consumer<KVQ_FP8_E4M3> : ConsumerBytes<KVQ_FP8_E4M3> {
 };
 
 // ---------------------------------------------------------------------------
-// The split: static pieces with dynamically executed tails.
-//
-// The units 0 .. U-1 of a launch are cut into GW contiguous warp ranges
-// [U w / GW, U (w+1) / GW).  Each range is one head piece followed by KT tail
-// pieces that together hold about kTailNum / kTailDen of it (at least KT
-// units, never the whole range).  Pieces are numbered w * (1 + KT) + j (j = 0
-// the head, 1 .. KT the tails), so in unit order.  Warp w runs its own head
-// piece; every tail piece is handed out through one ticket counter to
-// whichever warp asks next (warps ask when their queue runs dry), so the
-// last few microseconds of the launch are spread over the warps that finish
-// first instead of waiting for the slowest ones.  Where a piece begins and
-// ends depends only on (U, GW, KT), so the partials of a (sequence, head)
-// split over several pieces are found without knowing who ran them.
+// Grouped query heads as the rows of the MMA: a tile of up to kMqRows query
+// heads that share one cache head (GQA with a large group, or MQA -- the
+// pages' MLA decode absorbed into MQA).  Here one pass over the codes serves
+// 16 query heads, so the work per byte is a real small GEMM and the orientation
+// flips: QK has A = the tile's q rows (16 heads x 16 elements), B = K^T (16
+// elements x 8 tokens), and the S accumulators of two token tiles are, as
+// they stand, the A operand of PV (16 heads x 16 tokens) with B = V (16 tokens
+// x 8 elements of the head dimension).  No shuffles between QK and PV.
+//   k index of QK: a fixed permutation of the head dimension that q's
+//   fragment repeats -- int4: k-step (m, s), rows 2t, 2t+1 = elements
+//   32t + 8m + 2s + {0, 4}, rows 2t+8, 2t+9 = + {1, 5} (the pairs the nibble
+//   widening produces); int8 / FP8: k-step k, rows = elements 32t + 4k + {0,1}
+//   and + {2,3}.
+//   n index of PV: int4 tile (R, e) holds elements 64R + 8n + e; int8 / FP8
+//   tile (R, e) holds 32R + 4n + e, so each lane's output elements of a row
+//   are contiguous (int4: 64R + 16t .. +15; bytes: 32R + 8t .. +7).
+// Probabilities go to the PV MMA as fp16 x = e * sv / sv_ref, where
+// e = 2^(s - m) (the lazy row maximum m keeps e < 2^8) and sv_ref is the
+// largest value scale of the segment so far (x <= 2^8, normal fp16 unless
+// negligible against the largest value); the output is sv_ref * O / l.
 // ---------------------------------------------------------------------------
-constexpr int kTailNum = 1;
-constexpr int kTailDen = 4;
 
+// the int8 pair {a.byte e, b.byte e} widened exactly to fp16 (a, b already XOR 0x80808080)
+__device__ __forceinline__ uint32_t pair_int8(uint32_t a, uint32_t b, int e)
+{
+    const uint32_t x = __byte_perm(a, b, (uint32_t)e | ((uint32_t)(4 + e) << 8));
+    uint32_t y;
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(y) : "r"(x), "r"(0x00ff00ffu), "r"(0x64006400u));  // (x & m) | c
+    return h2_bits(__hsub2(*reinterpret_cast<const __half2 *>(&y), __float2half2_rn(1152.0f)));
+}
+
+// the FP8 E4M3 pair {a.byte e, b.byte e} widened exactly to fp16
+__device__ __forceinline__ uint32_t pair_e4m3(uint32_t a, uint32_t b, int e)
+{
+    const uint32_t x = __byte_perm(a, b, (uint32_t)e | ((uint32_t)(4 + e) << 4));
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(x & 0xffffu)));
+    return d;
+}
+
+template <int FMT>
+struct ConsumerMq {
+    static constexpr bool kInt4 = FMT == KVQ_INT4_B64;
+    static constexpr int kNT = kInt4 ? 4 : 2;  // token tiles of 8 per unit
+    static constexpr int kScores = 4 * kNT;   // S accumulators per lane per unit
+    static constexpr int kPf = 2 * kNT;       // P A-fragment registers per unit
+    static constexpr float kLazy = 8.0f;      // the row maximum moves only when exceeded by more than this (log2)
+
+    uint32_t qa[8][4];  // Q A-fragments of the 8 k-steps
+    float o[16][4];     // O accumulators: 16 tiles of the head dimension
+    float m_run[2];     // rows grp, grp + 8 (base-2 scores)
+    float l_run[2];     // this lane's part of the row sums of 2^(s - m)
+    float r_ref;        // log2 of the reference value scale
+    int rows;           // valid rows of the tile
+    Magic mk;
+
+    __device__ __forceinline__ void reset()
+    {
+        mk.init();
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.0f;
+        r_ref = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) o[i][j] = 0.0f;
+    }
+
+    // qs: the tile's kMqRows query rows (fp16 [16][128]; rows past `rows` hold finite values)
+    __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
+    {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const uint4 va = *reinterpret_cast<const uint4 *>(qs + g * kHeadDim + 32 * t + 8 * m);
+            const uint4 vb = *reinterpret_cast<const uint4 *>(qs + (g + 8) * kHeadDim + 32 * t + 8 * m);
+            if constexpr (kInt4) {
+                qa[2 * m][0] = __byte_perm(va.x, va.z, 0x5410);
+                qa[2 * m][1] = __byte_perm(vb.x, vb.z, 0x5410);
+                qa[2 * m][2] = __byte_perm(va.x, va.z, 0x7632);
+                qa[2 * m][3] = __byte_perm(vb.x, vb.z, 0x7632);
+                qa[2 * m + 1][0] = __byte_perm(va.y, va.w, 0x5410);
+                qa[2 * m + 1][1] = __byte_perm(vb.y, vb.w, 0x5410);
+                qa[2 * m + 1][2] = __byte_perm(va.y, va.w, 0x7632);
+                qa[2 * m + 1][3] = __byte_perm(vb.y, vb.w, 0x7632);
+            } else {
+                qa[2 * m][0] = va.x;
+                qa[2 * m][1] = vb.x;
+                qa[2 * m][2] = va.y;
+                qa[2 * m][3] = vb.y;
+                qa[2 * m + 1][0] = va.z;
+                qa[2 * m + 1][1] = vb.z;
+                qa[2 * m + 1][2] = va.w;
+                qa[2 * m + 1][3] = vb.w;
+            }
+        }
+    }
+
+    // raw q . c of rows (grp, grp+8) x tokens 8j + 2t, 8j + 2t + 1: sc[4j + {0,1}] row grp, sc[4j + {2,3}] row grp+8
+    __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[kScores]) const
+    {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int j = 0; j < kNT; j++) {
+            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if constexpr (kInt4) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(ks + (8 * j + g) * 64 + 16 * t);
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int m = 0; m < 4; m++) {
+                    uint32_t b[4];
+                    widen_int4_u32(u[m], b, mk);
+                    mma16816(c, qa[2 * m][0], qa[2 * m][1], qa[2 * m][2], qa[2 * m][3], b[0], b[1]);
+                    mma16816(c, qa[2 * m + 1][0], qa[2 * m + 1][1], qa[2 * m + 1][2], qa[2 * m + 1][3], b[2], b[3]);
+                }
+            } else {
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(ks + (8 * j + g) * 128 + 32 * t);
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(ks + (8 * j + g) * 128 + 32 * t + 16);
+                const uint32_t u[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    __half2 b[2];
+                    widen_bytes<FMT>(u[k], b);
+                    mma16816(c, qa[k][0], qa[k][1], qa[k][2], qa[k][3], h2_bits(b[0]), h2_bits(b[1]));
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; e++) sc[4 * j + e] = c[e];
+        }
+    }
+
+    // online softmax of the unit; pf = P as the A fragments of the unit's
+    // token tiles of 16 (int4: two, bytes: one), fp16 x = 2^(s - m) sv / sv_ref
+    __device__ __forceinline__ void softmax(const float sc[kScores], int ntok, float fac, float sv, int lane,
+                                            uint32_t pf[kPf])
+    {
+        const int t = lane & 3;
+        // the reference value scale: the segment's largest so far (uniform over the warp)
+        const float lsv = __log2f(fmaxf(sv, 1.17549435e-38f));
+        if (lsv > r_ref) {
+            const float beta = ex2_approx(r_ref - lsv);
+#pragma unroll
+            for (int i = 0; i < 16; i++)
+#pragma unroll
+                for (int j = 0; j < 4; j++) o[i][j] *= beta;
+            r_ref = lsv;
+        }
+        const float ratio = ex2_approx(lsv - r_ref);
+        float s[kScores];
+#pragma unroll
+        for (int j = 0; j < kNT; j++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int tok = 8 * j + 2 * t + (e & 1);
+                s[4 * j + e] = tok < ntok ? sc[4 * j + e] * fac : -INFINITY;
+            }
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < kScores; i++) mx[(i >> 1) & 1] = fmaxf(mx[(i >> 1) & 1], s[i]);
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 1));
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 2));
+        }
+        const bool up0 = mx[0] > m_run[0] + kLazy, up1 = mx[1] > m_run[1] + kLazy;
+        if (__any_sync(kFull, up0 || up1)) {
+            const float a0 = up0 ? ex2_approx(m_run[0] - mx[0]) : 1.0f;
+            const float a1 = up1 ? ex2_approx(m_run[1] - mx[1]) : 1.0f;
+            if (up0) m_run[0] = mx[0];
+            if (up1) m_run[1] = mx[1];
+            l_run[0] *= a0;
+            l_run[1] *= a1;
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                o[i][0] *= a0;
+                o[i][1] *= a0;
+                o[i][2] *= a1;
+                o[i][3] *= a1;
+            }
+        }
+        float e[kScores];
+#pragma unroll
+        for (int i = 0; i < kScores; i++) e[i] = ex2_approx(s[i] - m_run[(i >> 1) & 1]);
+#pragma unroll
+        for (int j = 0; j < kNT; j++) {
+            l_run[0] += e[4 * j] + e[4 * j + 1];
+            l_run[1] += e[4 * j + 2] + e[4 * j + 3];
+        }
+        // A fragment of token tile k (tokens 16k .. 16k+15) = S tiles 2k, 2k+1
+#pragma unroll
+        for (int k = 0; k < kNT / 2; k++) {
+            pf[4 * k + 0] = f16x2_rn(e[8 * k + 0] * ratio, e[8 * k + 1] * ratio);
+            pf[4 * k + 1] = f16x2_rn(e[8 * k + 2] * ratio, e[8 * k + 3] * ratio);
+            pf[4 * k + 2] = f16x2_rn(e[8 * k + 4] * ratio, e[8 * k + 5] * ratio);
+            pf[4 * k + 3] = f16x2_rn(e[8 * k + 6] * ratio, e[8 * k + 7] * ratio);
+        }
+    }
+
+    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t pf[kPf], int lane)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        if constexpr (kInt4) {
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+#pragma unroll
+                for (int R = 0; R < 2; R++) {
+                    // word g + 8R (elements 64R + 8g .. +7) of tokens 16k + 2t, +1, +8, +9
+                    const uint8_t *vb = vs + (16 * k + 2 * t) * 64 + 4 * (g + 8 * R);
+                    const uint32_t wa = *reinterpret_cast<const uint32_t *>(vb);
+                    const uint32_t wb = *reinterpret_cast<const uint32_t *>(vb + 64);
+                    const uint32_t wc = *reinterpret_cast<const uint32_t *>(vb + 8 * 64);
+                    const uint32_t wd = *reinterpret_cast<const uint32_t *>(vb + 9 * 64);
+                    uint32_t xab[4], xcd[4];
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const uint32_t bsel = (uint32_t)q | ((uint32_t)q << 4) | ((uint32_t)(4 + q) << 8) |
+                                              ((uint32_t)(4 + q) << 12);
+                        xab[q] = __byte_perm(wa, wb, bsel);
+                        xcd[q] = __byte_perm(wc, wd, bsel);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; e++)
+                        mma16816(o[8 * R + e], pf[4 * k], pf[4 * k + 1], pf[4 * k + 2], pf[4 * k + 3],
+                                 nib_pair(xab[e >> 1], e & 1, mk), nib_pair(xcd[e >> 1], e & 1, mk));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int R = 0; R < 4; R++) {
+                // word g + 8R (elements 32R + 4g .. +3) of tokens 2t, 2t+1, 2t+8, 2t+9
+                const uint8_t *vb = vs + (2 * t) * 128 + 4 * (g + 8 * R);
+                uint32_t wa = *reinterpret_cast<const uint32_t *>(vb);
+                uint32_t wb = *reinterpret_cast<const uint32_t *>(vb + 128);
+                uint32_t wc = *reinterpret_cast<const uint32_t *>(vb + 8 * 128);
+                uint32_t wd = *reinterpret_cast<const uint32_t *>(vb + 9 * 128);
+                if constexpr (FMT == KVQ_INT8_PAGE) {
+                    wa ^= 0x80808080u;
+                    wb ^= 0x80808080u;
+                    wc ^= 0x80808080u;
+                    wd ^= 0x80808080u;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    uint32_t b0, b1;
+                    if constexpr (FMT == KVQ_INT8_PAGE) {
+                        b0 = pair_int8(wa, wb, e);
+                        b1 = pair_int8(wc, wd, e);
+                    } else {
+                        b0 = pair_e4m3(wa, wb, e);
+                        b1 = pair_e4m3(wc, wd, e);
+                    }
+                    mma16816(o[4 * R + e], pf[0], pf[1], pf[2], pf[3], b0, b1);
+                }
+            }
+        }
+    }
+
+    // rows: the tile's output rows (orow, fp16, 128 apart) or partial slots
+    // (part, kPartialStride floats apart: m, l, pad, pad, sv_ref * O)
+    __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        float l[2];
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            l[r] = l_run[r] + __shfl_xor_sync(kFull, l_run[r], 1);
+            l[r] += __shfl_xor_sync(kFull, l[r], 2);
+        }
+        const float ref = ex2_approx(r_ref);
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            const int row = g + 8 * r;
+            if (row >= rows) continue;
+            const float mul = orow ? ref / l[r] : ref;
+            if constexpr (kInt4) {
+#pragma unroll
+                for (int R = 0; R < 2; R++) {
+                    float v[16];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        v[e] = o[8 * R + e][2 * r] * mul;          // element 64R + 16t + e
+                        v[8 + e] = o[8 * R + e][2 * r + 1] * mul;  // element 64R + 16t + 8 + e
+                    }
+                    if (orow) {
+                        uint4 *d = reinterpret_cast<uint4 *>(orow + row * kHeadDim + 64 * R + 16 * t);
+                        d[0] = make_uint4(f16x2_rn(v[0], v[1]), f16x2_rn(v[2], v[3]), f16x2_rn(v[4], v[5]),
+                                          f16x2_rn(v[6], v[7]));
+                        d[1] = make_uint4(f16x2_rn(v[8], v[9]), f16x2_rn(v[10], v[11]), f16x2_rn(v[12], v[13]),
+                                          f16x2_rn(v[14], v[15]));
+                    } else {
+                        float4 *d = reinterpret_cast<float4 *>(part + row * kPartialStride + 4 + 64 * R + 16 * t);
+#pragma unroll
+                        for (int i = 0; i < 4; i++) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int R = 0; R < 4; R++) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        v[e] = o[4 * R + e][2 * r] * mul;          // element 32R + 8t + e
+                        v[4 + e] = o[4 * R + e][2 * r + 1] * mul;  // element 32R + 8t + 4 + e
+                    }
+                    if (orow) {
+                        *reinterpret_cast<uint4 *>(orow + row * kHeadDim + 32 * R + 8 * t) =
+                            make_uint4(f16x2_rn(v[0], v[1]), f16x2_rn(v[2], v[3]), f16x2_rn(v[4], v[5]),
+                                       f16x2_rn(v[6], v[7]));
+                    } else {
+                        float4 *d = reinterpret_cast<float4 *>(part + row * kPartialStride + 4 + 32 * R + 8 * t);
+                        d[0] = make_float4(v[0], v[1], v[2], v[3]);
+                        d[1] = make_float4(v[4], v[5], v[6], v[7]);
+                    }
+                }
+            }
+            if (part && t == 0) {
+                part[row * kPartialStride] = m_run[r];
+                part[row * kPartialStride + 1] = l[r];
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// The split: the units 0 .. U-1 of a launch are cut into GW contiguous warp
+// ranges [U w / GW, U (w+1) / GW), one per active warp (the pieces of the
+// split).  Where a piece begins and ends depends only on (U, GW), so the
+// partials of a (sequence, head) split over several pieces are found without
+// any bookkeeping.
+// ---------------------------------------------------------------------------
 struct Split {
     int64_t U, GW;  // units, active warps
-    int KT, PW;     // tail pieces per warp, pieces per warp (1 + KT)
 
     __device__ __forceinline__ void init(int64_t units, int64_t warps)
     {
         U = units;
         GW = warps;
-        const int64_t rmin = GW > 0 ? U / GW : 0;
-        int64_t kt = rmin * kTailNum / kTailDen;
-        kt = kt < 1 ? 1 : (kt > kMaxTailPieces ? kMaxTailPieces : kt);
-        KT = rmin >= 2 ? (int)kt : 0;  // a range of one unit keeps it whole
-        PW = 1 + KT;
     }
-    __device__ __forceinline__ int64_t lo(int64_t w) const { return U * w / GW; }
-    // units of a range of r units that go to its tail pieces
-    __device__ __forceinline__ int64_t tail(int64_t r) const
-    {
-        if (KT == 0) return 0;
-        const int64_t t = r * kTailNum / kTailDen;
-        return t > KT ? t : KT;
-    }
-    __device__ __forceinline__ int64_t start(int64_t pi) const
-    {
-        const int64_t w = pi / PW;
-        const int j = (int)(pi - w * PW);
-        const int64_t a = lo(w);
-        if (j == 0) return a;
-        const int64_t b = lo(w + 1);
-        const int64_t tl = tail(b - a);
-        return b - tl + tl * (j - 1) / KT;
-    }
-    __device__ __forceinline__ int64_t end(int64_t pi) const { return pi + 1 < GW * PW ? start(pi + 1) : U; }
-    // the piece that holds unit u
-    __device__ __forceinline__ int64_t piece_of(int64_t u) const
-    {
-        const int64_t w = ((u + 1) * GW - 1) / U;
-        if (KT == 0) return w;
-        const int64_t a = lo(w), b = lo(w + 1);
-        const int64_t tl = tail(b - a), xm = b - tl;
-        if (u < xm) return w * PW;
-        return w * PW + 1 + ((u - xm + 1) * KT - 1) / tl;
-    }
-    // the tail piece of ticket t (t < GW * KT)
-    __device__ __forceinline__ int64_t ticket_piece(int64_t t) const { return (t / KT) * PW + 1 + t % KT; }
+    __device__ __forceinline__ int64_t start(int64_t w) const { return U * w / GW; }
+    // the piece (warp range) that holds unit u
+    __device__ __forceinline__ int64_t piece_of(int64_t u) const { return ((u + 1) * GW - 1) / U; }
 };
 
 // ---------------------------------------------------------------------------
-// Counters of the split.  A counter word holds a count in its low kCountBits
-// bits and, above them, count * epoch mod 2^40, where the epoch is an odd tag
-// chosen per call: an add of n is one atomic add of n * (1 + 2^24 epoch).
+// Counters of the split, one word per piece: the word of the piece that holds
+// a split (sequence, head)'s last unit counts the units of it whose partials
+// are written.  A counter word holds a count in its low kCountBits bits and,
+// above them, count * epoch mod 2^40, where the epoch is an odd tag chosen per
+// call: an add of n is one atomic add of n * (1 + 2^24 epoch).
 // Within one call every word stays consistent (high part == low part *
 // epoch); a word left non-zero by another call (an aborted launch, a
 // workspace that was never zero-filled) is inconsistent under this call's
@@ -920,24 +1219,6 @@ __device__ __noinline__ bool count_units(unsigned long long *slot, uint32_t unit
     if (!last) return false;
     __syncwarp();
     return true;
-}
-
-// One ticket of the tail pieces (lane 0 calls it): returns t, the tail piece
-// t of the launch when t < GW * KT; every active warp takes tickets until it
-// gets one past the end, so the launch takes GW * (KT + 1) of them and the
-// warp that takes the last one puts the counter back to zero.  A counter left
-// over by another call ends the warp's tail work (the flag is raised).
-__device__ __forceinline__ int64_t take_ticket(unsigned long long *ctr, int64_t takes, unsigned long long epoch,
-                                               int32_t *status)
-{
-    const unsigned long long old = atomicAdd(ctr, counter_step(epoch));
-    if (!counter_consistent(old, epoch)) {
-        set_flag(status, KVQ_FLAG_BAD_WORKSPACE);
-        return INT64_MAX;
-    }
-    const int64_t t = (int64_t)(old & kCountMask);
-    if (t == takes - 1) *ctr = 0ull;
-    return t;
 }
 
 // One warp: combine the partials of pieces gf .. gf + cnt - 1 (slot 1 of piece
@@ -1094,40 +1375,21 @@ template <int FMT>
 struct ConsumerFor<FMT, 1> {
     using type = Consumer<FMT>;
 };
+template <int FMT>
+struct ConsumerFor<FMT, kMqG> {
+    using type = ConsumerMq<FMT>;
+};
 
-// G: query heads per cache head (1: multi-head attention)
-template <int FMT, int G>
-__global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPerSm)
-    decode_split_kernel(DecodeParams p, int grid_warps)
+// Shared prologue of the split and merge kernels: the sequence lengths (clamped
+// to the table, flagged), the prefix of units over (sequence, unit head) with
+// HU unit heads per sequence, and the split geometry -- the same in every CTA.
+template <int UT>
+__device__ __forceinline__ void decode_prologue(const DecodeParams &p, int HU, int grid_warps, int32_t *s_cu,
+                                                int32_t *s_len, Split *s_split)
 {
-    using F = DecFmt<FMT>;
-    constexpr int kStages = F::kStages;
-    constexpr int UPS = F::kUnitsPerStage;
-    using WS = WarpSmem<kStages, UPS * kUnitBytes, G>;
-    constexpr int64_t kSlotFloats = (int64_t)G * kPartialStride;  // one piece's partials
-    constexpr int UT = F::kUnitTok;
-    constexpr int UPP = F::kUnitsPerPage;
-    constexpr int RB = F::kRowBytes;
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    WS *wsm_all = reinterpret_cast<WS *>(smem_raw);
-    constexpr int kDecWarps = F::kWarps;
-    int32_t *s_cu = reinterpret_cast<int32_t *>(smem_raw + kDecWarps * sizeof(WS));
-    int32_t *s_len = s_cu + kMaxSeqsPerLaunch + 1;
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = p.num_seqs;
-    const int H = p.num_heads;
     const int max_len = p.max_blocks * kPage;
-    pdl_launch_dependents();
-    // Until pdl_wait below, the previous kernel of the stream may still be
-    // running.  Only the sequence lengths and the block table are read before
-    // it: no kernel of this library writes them (the codes, scales, query and
-    // output are touched only after the wait), so the prologue and the first
-    // block-table fetch overlap the previous kernel's tail.
-
-    // ---- per-sequence lengths and the (H x units) prefix, in shared memory ----
     for (int b = tid; b < B; b += blockDim.x) {
         int L = p.seq_lens[b];
         if (L < 0 || L > max_len) {
@@ -1142,7 +1404,7 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         int sum = 0;
         for (int k = 0; k < per; k++) {
             const int i = lane * per + k;
-            if (i < B) sum += units_of(s_len[i], UT) * H;
+            if (i < B) sum += units_of(s_len[i], UT) * HU;
         }
         int incl = sum;
 #pragma unroll
@@ -1155,33 +1417,74 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             const int i = lane * per + k;
             if (i < B) {
                 s_cu[i] = run;
-                run += units_of(s_len[i], UT) * H;
+                run += units_of(s_len[i], UT) * HU;
             }
         }
         if (lane == 31) s_cu[B] = incl;
     }
     __syncthreads();
-
-    // the split geometry, the same for every warp (kept in shared memory: it
-    // is read only when a piece starts or a segment ends)
-    Split *s_split = reinterpret_cast<Split *>(smem_raw + kDecWarps * sizeof(WS) +
-                                               ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 15) / 16 * 16);
     if (tid == 0) {
         const int64_t U = s_cu[B];
         // active warps: at least kMinUnitsPerWarp units each
         s_split->init(U, imin64((int64_t)grid_warps, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp));
     }
     __syncthreads();
+}
+
+// G: query heads per cache head (1: multi-head attention; 2, 4: int4 grouped
+// heads in spare MMA columns; kMqG: tiles of up to 16 query heads of any group
+// size p.group, p.tiles tiles per cache head, each tile a unit head of its own)
+template <int FMT, int G>
+__global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kCtasPerSm)
+    decode_split_kernel(DecodeParams p, int grid_warps)
+{
+    using F = DecFmt<FMT>;
+    using CS = typename ConsumerFor<FMT, G>::type;
+    constexpr bool kTiles = G == kMqG;
+    constexpr int kStages = F::kStages;
+    constexpr int UPS = F::kUnitsPerStage;
+    constexpr int kQRows = DecShape<FMT, G>::kQRows;
+    using WS = WarpSmem<kStages, UPS * kUnitBytes, kQRows>;
+    constexpr int64_t kSlotFloats = (int64_t)kQRows * kPartialStride;  // one piece's partials
+    constexpr int UT = F::kUnitTok;
+    constexpr int UPP = F::kUnitsPerPage;
+    constexpr int RB = F::kRowBytes;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    WS *wsm_all = reinterpret_cast<WS *>(smem_raw);
+    constexpr int kDecWarps = DecShape<FMT, G>::kWarps;
+    int32_t *s_cu = reinterpret_cast<int32_t *>(smem_raw + kDecWarps * sizeof(WS));
+    int32_t *s_len = s_cu + kMaxSeqsPerLaunch + 1;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int B = p.num_seqs;
+    const int H = p.num_heads;                  // cache heads
+    const int T = kTiles ? p.tiles : 1;         // unit heads per cache head
+    const int HU = H * T;                       // unit heads per sequence
+    const int g_rows = kTiles ? p.group : G;    // query heads per cache head
+    pdl_launch_dependents();
+    // Until pdl_wait below, the previous kernel of the stream may still be
+    // running.  Only the sequence lengths and the block table are read before
+    // it: no kernel of this library writes them (the codes, scales, query and
+    // output are touched only after the wait), so the prologue and the first
+    // block-table fetch overlap the previous kernel's tail.
+
+    // ---- per-sequence lengths, the (unit heads x units) prefix and the split
+    // geometry, in shared memory (the split is read only when a piece starts
+    // or a segment ends) ----
+    Split *s_split = reinterpret_cast<Split *>(smem_raw + kDecWarps * sizeof(WS) +
+                                               ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 15) / 16 * 16);
+    decode_prologue<UT>(p, HU, grid_warps, s_cu, s_len, s_split);
     const Split &sp = *s_split;
     // logical warp index, round-robin over the CTAs: when fewer than all warps
     // have work (GW < grid warps) the active ones spread over every SM
     const int gw = warp * (int)gridDim.x + blockIdx.x;
     const bool active = gw < sp.GW;
-    unsigned long long *const tickets = p.counters;        // word 0: tail-piece tickets
-    unsigned long long *const piece_ctr = p.counters + 1;  // then one word per piece
+    unsigned long long *const piece_ctr = p.counters;  // one word per piece
 
-    // ---- issue cursor: unit x_cur of piece pi_cur = (ib, ih, ic); rem units left in the piece ----
-    int pi_cur = gw * sp.PW;
+    // ---- issue cursor: the next unit of this warp's piece = (ib, ih, ic); rem units left ----
+    const int pi_cur = gw;
     int rem = 0;
     int ib = 0, ih = 0, ic = 0;
     auto seek = [&](int64_t x) {
@@ -1198,7 +1501,7 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     };
     if (active) {
         const int64_t x = sp.start(pi_cur);
-        rem = (int)(sp.end(pi_cur) - x);
+        rem = (int)(sp.start(pi_cur + 1) - x);
         seek(x);
     }
     int inb = units_of(s_len[ib], UT);  // units of the issue cursor's sequence
@@ -1225,7 +1528,7 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         r_page = pg;
         ring_scales_due = true;
     };
-    if (active) ring_pages(ib, ih, ic / UPP);
+    if (active) ring_pages(ib, ih / T, ic / UPP);
 
     pdl_wait();  // from here on, the previous kernel's writes are visible
 
@@ -1236,8 +1539,8 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
                 const int b = base + __ffs(m) - 1;
                 m &= m - 1;
                 if (b % (int)gridDim.x != (int)blockIdx.x) continue;
-                uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)b * H * G * kHeadDim);
-                for (int e = lane; e < H * G * (kHeadDim / 8); e += 32) row[e] = make_uint4(0u, 0u, 0u, 0u);
+                uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)b * H * g_rows * kHeadDim);
+                for (int e = lane; e < H * g_rows * (kHeadDim / 8); e += 32) row[e] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
     }
@@ -1254,32 +1557,25 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     constexpr uint32_t kPageBytes = kPage * RB;
 
     int ci = 0;                 // stages filled so far (chunk count)
-    bool issue_done = false;    // no piece is left for this warp
-    bool piece_new = true;      // the next stage starts a piece
+    // the timeout test's chunk (kvq_testing.h): the grid's first warp leaves
+    // its copies unissued, so the stage's wait runs out with nothing in flight
+    const int skip_ci = gw == 0 ? p.test_skip_chunk : -1;
+    bool issue_done = false;    // the warp's range is fully issued
+    bool piece_new = true;      // the next stage is the warp's first
     // Fill stage ci % kStages with the next chunk: the cursor's unit and the
     // following ones of the same stage-sized group of its page, within the
-    // (sequence, head) and the piece.  When the piece is used up, a ticket
-    // brings the next tail piece.  Returns false when no work is left.
+    // (sequence, head) and the warp's range.  Returns false when no work is left.
     auto issue = [&]() -> bool {
         if (rem == 0) {
-            int64_t t = INT64_MAX;
-            if (sp.KT > 0 && lane == 0) t = take_ticket(tickets, sp.GW * (sp.KT + 1), p.epoch, p.status);
-            t = __shfl_sync(kFull, t, 0);
-            if (t >= sp.GW * sp.KT) {
-                issue_done = true;
-                return false;
-            }
-            pi_cur = (int)sp.ticket_piece(t);
-            const int64_t x = sp.start(pi_cur);
-            rem = (int)(sp.end(pi_cur) - x);
-            seek(x);
-            inb = units_of(s_len[ib], UT);
-            piece_new = true;
+            issue_done = true;
+            return false;
         }
         const int s = ci % kStages;
         const int j = ic / UPP;
         const int nh = UPS > 1 ? min(min(UPS - ic % UPS, inb - ic), rem) : 1;
-        if (ib != ring_b || ih != ring_h || j < ring_j0 || j >= ring_j0 + 32) ring_pages(ib, ih, j);
+        const int hc = kTiles ? ih / T : ih;  // the cache head of the unit head
+        // (tiles of one cache head share its ring: a tile after the first starts again at page 0)
+        if (ib != ring_b || hc != ring_h || j < ring_j0 || j >= ring_j0 + 32) ring_pages(ib, hc, j);
         const int pg = __shfl_sync(kFull, r_page, j - ring_j0);
         const bool new_seg = piece_new || (ic == 0);
         if (ring_scales_due) {  // the ring's scales (after the wait: appends write them)
@@ -1292,16 +1588,18 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             // consumed those values (mma operands) before the __syncwarp that
             // precedes this issue, so the copy cannot overtake them.
             const uint32_t cb = (uint32_t)nh * kUnitBytes;
-            const uint32_t bytes = 2 * cb + (new_seg ? G * kHeadDim * 2 : 0);
+            // the unit head's query rows: G rows of the cache head, or one tile of the group
+            const int tile = kTiles ? ih - hc * T : 0;
+            const int qrows = kTiles ? min(kMqRows, g_rows - kMqRows * tile) : G;
+            const uint32_t qbytes = (uint32_t)qrows * kHeadDim * 2;
+            const uint32_t bytes = 2 * cb + (new_seg ? qbytes : 0);
             mbar_arrive_expect_tx(&ws.full[s], bytes);
-            // the timeout test leaves one chunk of warp 0 without its copies:
-            // the stage's wait then runs out with nothing in flight
-            if (!(p.test_skip_chunk == ci && gw == 0)) {
-                const size_t off = ((size_t)pg * H + ih) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
+            if (ci != skip_ci) {
+                const size_t off = ((size_t)pg * H + hc) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
                 bulk_copy_g2s(ws.k[s], p.k_codes + off, cb, &ws.full[s]);
                 bulk_copy_g2s(ws.v[s], p.v_codes + off, cb, &ws.full[s]);
                 if (new_seg)
-                    bulk_copy_g2s(ws.q[s], p.q + ((size_t)ib * H + ih) * G * kHeadDim, G * kHeadDim * 2,
+                    bulk_copy_g2s(ws.q[s], p.q + (((size_t)ib * H + hc) * g_rows + kMqRows * tile) * kHeadDim, qbytes,
                                   &ws.full[s]);
             }
         }
@@ -1312,7 +1610,6 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             *reinterpret_cast<int4 *>(&ws.meta[s].b) = make_int4(ib, ih, ic, ntok);
             *reinterpret_cast<float4 *>(&ws.meta[s].sk) =
                 make_float4(sk, sv, __int_as_float(new_seg ? 1 : 0), __int_as_float(nh));
-            ws.meta[s].piece = pi_cur;
         }
         // advance the cursor by the chunk
         ic += nh;
@@ -1320,7 +1617,7 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         piece_new = false;
         if (ic == inb) {
             ic = 0;
-            if (++ih == H) {
+            if (++ih == HU) {
                 ih = 0;
                 ++ib;
                 while (ib < B && s_len[ib] == 0) ++ib;
@@ -1336,31 +1633,41 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     __syncwarp();
 
     // ---- consumer: qk of unit n+1 overlaps pv of unit n ----
-    typename ConsumerFor<FMT, G>::type cs;
+    CS cs;
     cs.reset();
     int cur_b = -1, cur_h = -1;
     int seg_c = 0;        // first unit of the current segment within its (sequence, head)
     int seg_units = 0;    // units of it consumed so far
-    int seg_pi = 0;       // its piece
 
-    // units c .. c + units - 1 of (b, h), consumed in piece pi, are done
-    auto flush = [&](int b, int h, int c, int units, int pi) {
+    // the first output row of unit head h of sequence b
+    auto out_rows = [&](int b, int h) -> uint16_t * {
+        if constexpr (kTiles) {
+            const int hc = h / T;
+            return p.out + (((int64_t)b * H + hc) * g_rows + kMqRows * (h - hc * T)) * kHeadDim;
+        } else {
+            return p.out + ((int64_t)b * H + h) * G * kHeadDim;
+        }
+    };
+    // units c .. c + units - 1 of (b, h), consumed by this warp (piece pi), are done
+    auto flush = [&](int b, int h, int c, int units) {
+        const int pi = pi_cur;
         const int n = units_of(s_len[b], UT);
         const int64_t u0 = s_cu[b] + (int64_t)h * n;
         const int64_t sa = u0 + c;
         if (sa == u0 && units == n) {
-            cs.finish(lane, p.out + ((int64_t)b * H + h) * G * kHeadDim, nullptr);
+            cs.finish(lane, out_rows(b, h), nullptr);
         } else {  // split: the piece's first segment goes to its slot 0, its last to slot 1
             cs.finish(lane, nullptr, p.partials + ((int64_t)pi * 2 + (sa == sp.start(pi) ? 0 : 1)) * kSlotFloats);
+            if constexpr (kTiles) return;  // merged by the second launch
             const int64_t pf = sp.piece_of(u0);
             const int64_t pl = sp.piece_of(u0 + n - 1);
             if (count_units(piece_ctr + pl, (uint32_t)units, (uint32_t)n, p.epoch, lane, p.status)) {
                 const int first_slot = (sp.start(pf) != u0) ? 1 : 0;
-                uint16_t *orow = p.out + ((int64_t)b * H + h) * G * kHeadDim;
+                uint16_t *orow = out_rows(b, h);
                 if constexpr (G == 1)
                     merge_pieces<F::kMergeBatch>(p.partials, kSlotFloats, 0, pf, (int)(pl - pf + 1), first_slot,
                                                  orow, lane);
-                else
+                else if constexpr (!kTiles)
                     merge_group<8 / G, G>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane);
             }
         }
@@ -1369,12 +1676,12 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         for (int y = from; y < ci; y++)
             mbar_wait_bounded(&ws.full[y % kStages], (uint32_t)((y / kStages) & 1), p.wait_limit_ns);
     };
-    auto seg_start = [&](const int4 &m, int32_t piece) {
+    auto seg_start = [&](const int4 &m) {
         cur_b = m.x;
         cur_h = m.y;
         seg_c = m.z;
         seg_units = 0;
-        seg_pi = piece;
+        if constexpr (kTiles) cs.rows = min(kMqRows, g_rows - kMqRows * (m.y % T));
     };
 
     // chunk 0, unit 0
@@ -1385,11 +1692,11 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
     }
     int4 mi = *reinterpret_cast<const int4 *>(&ws.meta[0].b);
     float4 mf = *reinterpret_cast<const float4 *>(&ws.meta[0].sk);
-    seg_start(mi, ws.meta[0].piece);
+    seg_start(mi);
     cs.load_q(ws.q[0], lane);
-    constexpr int kScores = G == 1 ? 4 : 8;  // scores a lane holds per unit
+    constexpr int kScores = CS::kScores;  // scores a lane holds per unit
     float sc[kScores];
-    uint32_t pf[4];
+    uint32_t pf[CS::kPf];
     cs.qk(ws.k[0], lane, sc);
     cs.softmax(sc, min(UT, mi.w), mf.x * p.score_scale, mf.y, lane, pf);
 
@@ -1409,7 +1716,6 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         const bool more = cc + 1 < ci;  // chunk cc + 1 was issued before chunk cc was consumed
         int4 mi1 = mi;
         float4 mf1 = mf;
-        int32_t piece1 = 0;
         float sc1[kScores];
         if (more) {
             const int s1 = (cc + 1) % kStages;
@@ -1420,7 +1726,6 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
             }
             mi1 = *reinterpret_cast<const int4 *>(&ws.meta[s1].b);
             mf1 = *reinterpret_cast<const float4 *>(&ws.meta[s1].sk);
-            piece1 = ws.meta[s1].piece;
             if (__float_as_int(mf1.z)) cs.load_q(ws.q[s1], lane);
             cs.qk(ws.k[s1], lane, sc1);  // the next chunk's first unit: independent of the pv below
         }
@@ -1430,15 +1735,48 @@ __global__ void __launch_bounds__(DecFmt<FMT>::kWarps * 32, DecFmt<FMT>::kCtasPe
         if (!issue_done) issue();
         if (!more) break;
         if (__float_as_int(mf1.z)) {  // the next chunk starts a new segment
-            flush(cur_b, cur_h, seg_c, seg_units, seg_pi);
+            flush(cur_b, cur_h, seg_c, seg_units);
             cs.reset();
-            seg_start(mi1, piece1);
+            seg_start(mi1);
         }
         cs.softmax(sc1, min(UT, mi1.w), mf1.x * p.score_scale, mf1.y, lane, pf);
         mi = mi1;
         mf = mf1;
     }
-    flush(cur_b, cur_h, seg_c, seg_units, seg_pi);
+    flush(cur_b, cur_h, seg_c, seg_units);
+}
+
+// Second launch of the tile path: merges the split partials of every
+// (sequence, unit head) that the split cut into pieces, one warp per query row
+// of the tile (the split kernel wrote every other output itself).  Launched
+// right after the split kernel with programmatic dependent launch: the
+// prologue (lengths, unit prefix, split geometry -- the same values the split
+// computed) overlaps the split's tail; partials are read after the wait.
+template <int UT>
+__global__ void __launch_bounds__(kMqRows * 32) decode_tile_merge_kernel(DecodeParams p, int grid_warps)
+{
+    __shared__ int32_t s_cu[kMaxSeqsPerLaunch + 1];
+    __shared__ int32_t s_len[kMaxSeqsPerLaunch];
+    __shared__ Split s_split;
+    const int T = p.tiles, H = p.num_heads, HU = H * T;
+    pdl_launch_dependents();
+    decode_prologue<UT>(p, HU, grid_warps, s_cu, s_len, &s_split);
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = (int)(blockIdx.x / HU), h = (int)(blockIdx.x - (unsigned)b * HU);
+    const Split &sp = s_split;
+    const int n = units_of(s_len[b], UT);
+    if (n == 0) return;
+    const int64_t u0 = s_cu[b] + (int64_t)h * n;
+    const int64_t pf = sp.piece_of(u0), pl = sp.piece_of(u0 + n - 1);
+    if (pf == pl) return;  // inside one piece: the split kernel wrote the rows
+    const int hc = h / T, tile = h - hc * T;
+    const int rows = min(kMqRows, p.group - kMqRows * tile);
+    if (warp >= rows) return;
+    const int first_slot = sp.start(pf) != u0 ? 1 : 0;
+    uint16_t *orow = p.out + (((int64_t)b * H + hc) * p.group + kMqRows * tile + warp) * kHeadDim;
+    merge_pieces<16>(p.partials, (int64_t)kMqRows * kPartialStride, warp, pf, (int)(pl - pf + 1), first_slot, orow,
+                     lane);
 }
 
 template <int FMT, int G>
@@ -1452,7 +1790,8 @@ static int ctas_per_sm()
                                  (int)dec_smem_bytes<FMT, G>()) != cudaSuccess)
             return 0;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<FMT, G>, DecFmt<FMT>::kWarps * 32,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<FMT, G>,
+                                                          DecShape<FMT, G>::kWarps * 32,
                                                           dec_smem_bytes<FMT, G>()) != cudaSuccess)
             return 0;
         constexpr int cap = DecFmt<FMT>::kCtasPerSm;
@@ -1461,32 +1800,67 @@ static int ctas_per_sm()
     return cached[dev];
 }
 
-int decode_grid_warps(int fmt)
+// the kernel variant (template group value) that serves group size g
+static int kernel_group(int fmt, int g)
+{
+    if (g == 1) return 1;
+    if (fmt == KVQ_INT4_B64 && (g == 2 || g == 4)) return g;
+    return kMqG;
+}
+
+// CTAs per SM of the variant (resolving its occupancy query and attributes), 0 on error
+template <int FMT>
+static int variant_ctas(int kg)
+{
+    switch (kg) {
+    case 1: return ctas_per_sm<FMT, 1>();
+    case kMqG: return ctas_per_sm<FMT, kMqG>();
+    default: break;
+    }
+    if constexpr (FMT == KVQ_INT4_B64) {
+        if (kg == 2) return ctas_per_sm<FMT, 2>();
+        if (kg == 4) return ctas_per_sm<FMT, 4>();
+    }
+    return 0;
+}
+
+static int variant_warps(int fmt, int kg)
+{
+    if (kg == kMqG) return DecShape<KVQ_INT4_B64, kMqG>::kWarps;
+    return fmt == KVQ_INT4_B64 ? DecFmt<KVQ_INT4_B64>::kWarps : DecFmt<KVQ_INT8_PAGE>::kWarps;
+}
+
+static int sm_count()
 {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (fmt == KVQ_INT4_B64) return sms * ctas_per_sm<KVQ_INT4_B64, 1>() * DecFmt<KVQ_INT4_B64>::kWarps;
-    if (fmt == KVQ_FP8_E4M3) return sms * ctas_per_sm<KVQ_FP8_E4M3, 1>() * DecFmt<KVQ_FP8_E4M3>::kWarps;
-    return sms * ctas_per_sm<KVQ_INT8_PAGE, 1>() * DecFmt<KVQ_INT8_PAGE>::kWarps;
+    return sms;
+}
+
+int decode_grid_warps(int fmt, int group)
+{
+    const int kg = kernel_group(fmt, group);
+    int ctas = 0;
+    if (fmt == KVQ_INT4_B64) ctas = variant_ctas<KVQ_INT4_B64>(kg);
+    else if (fmt == KVQ_FP8_E4M3) ctas = variant_ctas<KVQ_FP8_E4M3>(kg);
+    else ctas = variant_ctas<KVQ_INT8_PAGE>(kg);
+    return sm_count() * ctas * variant_warps(fmt, kg);
 }
 
 bool decode_group_supported(int fmt, int group)
 {
-    return group == 1 || (fmt == KVQ_INT4_B64 && (group == 2 || group == 4));
+    (void)fmt;
+    return group >= 1 && group <= kMaxDecodeGroup;
 }
 
 int decode_prepare(int fmt, int group)
 {
-    if (fmt == KVQ_INT4_B64) {
-        if (group == 1) return ctas_per_sm<KVQ_INT4_B64, 1>();
-        if (group == 2) return ctas_per_sm<KVQ_INT4_B64, 2>();
-        if (group == 4) return ctas_per_sm<KVQ_INT4_B64, 4>();
-        return 0;
-    }
-    if (group != 1) return 0;
-    if (fmt == KVQ_FP8_E4M3) return ctas_per_sm<KVQ_FP8_E4M3, 1>();
-    return ctas_per_sm<KVQ_INT8_PAGE, 1>();
+    if (!decode_group_supported(fmt, group)) return 0;
+    const int kg = kernel_group(fmt, group);
+    if (fmt == KVQ_INT4_B64) return variant_ctas<KVQ_INT4_B64>(kg);
+    if (fmt == KVQ_FP8_E4M3) return variant_ctas<KVQ_FP8_E4M3>(kg);
+    return variant_ctas<KVQ_INT8_PAGE>(kg);
 }
 
 size_t decode_counter_bytes()
@@ -1494,20 +1868,23 @@ size_t decode_counter_bytes()
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    const size_t words = 1 + (size_t)sms * kMaxDecodeWarpsPerSm * kPiecesPerWarp;
+    const size_t words = (size_t)sms * kMaxDecodeWarpsPerSm;
     return (words * sizeof(unsigned long long) + 255) / 256 * 256;
 }
 
 size_t decode_workspace_bytes(int fmt, int group)
 {
-    const int gw = decode_grid_warps(fmt);
-    if (gw <= 0 || !decode_group_supported(fmt, group)) return 0;
+    if (!decode_group_supported(fmt, group)) return 0;
+    const int gw = decode_grid_warps(fmt, group);
+    if (gw <= 0) return 0;
     static_assert(DecFmt<KVQ_INT4_B64>::kWarps * DecFmt<KVQ_INT4_B64>::kCtasPerSm <= kMaxDecodeWarpsPerSm &&
-                      DecFmt<KVQ_INT8_PAGE>::kWarps * DecFmt<KVQ_INT8_PAGE>::kCtasPerSm <= kMaxDecodeWarpsPerSm,
+                      DecFmt<KVQ_INT8_PAGE>::kWarps * DecFmt<KVQ_INT8_PAGE>::kCtasPerSm <= kMaxDecodeWarpsPerSm &&
+                      DecShape<KVQ_INT4_B64, kMqG>::kWarps * DecFmt<KVQ_INT4_B64>::kCtasPerSm <= kMaxDecodeWarpsPerSm,
                   "the counter region holds kMaxDecodeWarpsPerSm warps per SM");
     const size_t counters = decode_counter_bytes();
     if (counters == 0) return 0;
-    const size_t partial = (size_t)gw * kPiecesPerWarp * 2 * group * kPartialStride * sizeof(float);
+    const int rows = kernel_group(fmt, group) == kMqG ? kMqRows : group;  // query rows of one partial
+    const size_t partial = (size_t)gw * 2 * rows * kPartialStride * sizeof(float);
     return counters + partial;
 }
 
@@ -1523,39 +1900,50 @@ unsigned long long decode_next_epoch()
     return (z | 1ull) & ((1ull << 40) - 1);
 }
 
+template <int FMT>
+static cudaError_t launch_variant(const DecodeParams &p0, int kg, int gw, cudaStream_t s)
+{
+    DecodeParams p = p0;
+    const dim3 grid(gw / variant_warps(FMT, kg));
+    if (kg == kMqG) {
+        p.tiles = (p.group + kMqRows - 1) / kMqRows;
+        if (ctas_per_sm<FMT, kMqG>() < 1) return cudaErrorInvalidDevice;  // also sets the smem attribute
+        cudaError_t e = launch_pdl(decode_split_kernel<FMT, kMqG>, grid, dim3(variant_warps(FMT, kg) * 32),
+                                   dec_smem_bytes<FMT, kMqG>(), s, p, gw);
+        if (e != cudaSuccess) return e;
+        const unsigned pairs = (unsigned)p.num_seqs * (unsigned)(p.num_heads * p.tiles);
+        if (pairs == 0) return cudaSuccess;
+        return launch_pdl(decode_tile_merge_kernel<DecFmt<FMT>::kUnitTok>, dim3(pairs), dim3(kMqRows * 32), 0, s, p,
+                          gw);
+    }
+    p.tiles = 1;
+    const dim3 block(variant_warps(FMT, kg) * 32);
+    if (kg == 1)
+        return launch_pdl(decode_split_kernel<FMT, 1>, grid, block, dec_smem_bytes<FMT, 1>(), s, p, gw);
+    if constexpr (FMT == KVQ_INT4_B64) {
+        if (kg == 2) {
+            if (ctas_per_sm<FMT, 2>() < 1) return cudaErrorInvalidDevice;
+            return launch_pdl(decode_split_kernel<FMT, 2>, grid, block, dec_smem_bytes<FMT, 2>(), s, p, gw);
+        }
+        if (kg == 4) {
+            if (ctas_per_sm<FMT, 4>() < 1) return cudaErrorInvalidDevice;
+            return launch_pdl(decode_split_kernel<FMT, 4>, grid, block, dec_smem_bytes<FMT, 4>(), s, p, gw);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s)
 {
-    const int gw = decode_grid_warps(fmt);
+    if (!decode_group_supported(fmt, p.group)) return cudaErrorInvalidValue;
+    const int gw = decode_grid_warps(fmt, p.group);
     if (gw <= 0) return cudaErrorInvalidDevice;
     static_assert(DecFmt<KVQ_INT4_B64>::kWarps == DecFmt<KVQ_INT8_PAGE>::kWarps &&
                   DecFmt<KVQ_FP8_E4M3>::kWarps == DecFmt<KVQ_INT8_PAGE>::kWarps, "one CTA size");
-    const dim3 grid(gw / DecFmt<KVQ_INT8_PAGE>::kWarps);
-    if (fmt == KVQ_INT8_PAGE) {
-        if (p.group != 1) return cudaErrorInvalidValue;
-        return launch_pdl(decode_split_kernel<KVQ_INT8_PAGE, 1>, grid, dim3(DecFmt<KVQ_INT8_PAGE>::kWarps * 32),
-                          dec_smem_bytes<KVQ_INT8_PAGE, 1>(), s, p, gw);
-    }
-    if (fmt == KVQ_FP8_E4M3) {
-        if (p.group != 1) return cudaErrorInvalidValue;
-        return launch_pdl(decode_split_kernel<KVQ_FP8_E4M3, 1>, grid, dim3(DecFmt<KVQ_FP8_E4M3>::kWarps * 32),
-                          dec_smem_bytes<KVQ_FP8_E4M3, 1>(), s, p, gw);
-    }
-    const dim3 block(DecFmt<KVQ_INT4_B64>::kWarps * 32);
-    switch (p.group) {
-    case 1:
-        return launch_pdl(decode_split_kernel<KVQ_INT4_B64, 1>, grid, block, dec_smem_bytes<KVQ_INT4_B64, 1>(), s, p,
-                          gw);
-    case 2:
-        if (ctas_per_sm<KVQ_INT4_B64, 2>() < 1) return cudaErrorInvalidDevice;  // also sets the smem attribute
-        return launch_pdl(decode_split_kernel<KVQ_INT4_B64, 2>, grid, block, dec_smem_bytes<KVQ_INT4_B64, 2>(), s, p,
-                          gw);
-    case 4:
-        if (ctas_per_sm<KVQ_INT4_B64, 4>() < 1) return cudaErrorInvalidDevice;
-        return launch_pdl(decode_split_kernel<KVQ_INT4_B64, 4>, grid, block, dec_smem_bytes<KVQ_INT4_B64, 4>(), s, p,
-                          gw);
-    default:
-        return cudaErrorInvalidValue;
-    }
+    const int kg = kernel_group(fmt, p.group);
+    if (fmt == KVQ_INT4_B64) return launch_variant<KVQ_INT4_B64>(p, kg, gw, s);
+    if (fmt == KVQ_FP8_E4M3) return launch_variant<KVQ_FP8_E4M3>(p, kg, gw, s);
+    return launch_variant<KVQ_INT8_PAGE>(p, kg, gw, s);
 }
 
 }  // namespace kvq

@@ -43,8 +43,8 @@ struct DecodeParams {
     const int32_t *block_table;
     const int32_t *seq_lens;
     uint16_t *out;
-    float *partials;               // [pieces][2][group * kPartialStride]: split partials, two slots per piece
-    unsigned long long *counters;  // [pieces] unit counts of split (sequence, head)s + [1] tail-piece tickets
+    float *partials;               // [grid warps][2][rows * kPartialStride]: split partials, two slots per warp
+    unsigned long long *counters;  // [grid warps] unit counts of split (sequence, head)s
     int32_t *status;
     int32_t num_seqs;
     int32_t num_heads;
@@ -58,17 +58,17 @@ struct DecodeParams {
     unsigned long long epoch;
     unsigned long long wait_limit_ns;  // bounded waits give up after this long
     int32_t test_skip_chunk;           // >= 0: warp 0 leaves the copies of this chunk unissued (timeout test)
+    int32_t tiles;                     // tiles of 16 query heads per cache head (set by the launcher)
 };
+
+// the largest group (query heads per cache head) the decode kernels take
+constexpr int kMaxDecodeGroup = 1024;
 
 // default limit of a decode kernel's bounded waits (kernels finish in milliseconds)
 constexpr unsigned long long kDecodeWaitLimitNs = 500ull * 1000ull * 1000ull;
 
 // counter words: the low kCountBits bits count, the rest carry count * epoch
 constexpr int kCountBits = 24;
-// tail-piece bound of the decode split: every warp's range ends in at most
-// kMaxTailPieces pieces handed out dynamically, so pieces <= warps * (1 + kMaxTailPieces)
-constexpr int kMaxTailPieces = 4;
-constexpr int kPiecesPerWarp = 1 + kMaxTailPieces;
 // warps per SM the decode workspace's counter region is sized for (every decode kernel uses at most this many)
 constexpr int kMaxDecodeWarpsPerSm = 16;
 
@@ -144,8 +144,8 @@ cudaError_t launch_quantize(int fmt, const uint16_t *x, int64_t T, int H, uint8_
                             cudaStream_t s);
 cudaError_t launch_append(int fmt, const AppendParams &p, cudaStream_t s);
 
-// number of warps of the persistent split grid on the current device (0 on error)
-int decode_grid_warps(int fmt);
+// number of warps of the persistent split grid of (format, group) on the current device (0 on error)
+int decode_grid_warps(int fmt, int group);
 bool decode_group_supported(int fmt, int group);
 // the decode workspace: a counter region first (its size depends on the
 // device's SM count only), then the split partials

@@ -37,7 +37,7 @@ EXPORTS = ("kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes", "kvq_deco
            "kvq_version")
 # every symbol include/kvq_testing.h declares (test hooks)
 TESTING_EXPORTS = ("kvq_testing_set_decode_fault",)
-NOALLOC_SCRATCH_BYTES = 16 << 20
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class KvqError(RuntimeError):
@@ -233,7 +233,7 @@ def kvq_decode_attention_noalloc(cache, q, block_table, seq_lens, softmax_scale,
     allocate device memory when they run decode attention (a plugin whose
     execute step must not allocate, memory reserved up front by another
     allocator, a loop that cannot afford cudaMalloc's synchronisation): the
-    scratch is a fixed 16 MiB array inside the library, shared by every call, so
+    scratch is a fixed 4 MiB array inside the library, shared by every call, so
     calls that may overlap on the GPU must be serialised by the caller; each
     call clears the array's split counters first on the same stream."""
     _cuda(q, torch.float16, "q")

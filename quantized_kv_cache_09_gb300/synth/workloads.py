@@ -22,6 +22,9 @@
   chunked-prefill  B=8, H=32, L=8192 of which the last 512 tokens are a new
                    chunk (already appended), int4, K/V as llama2-7b-layer,
                    chunk queries ~ N(0,1); causal attention of the chunk
+  mqa-32k          B=64, 1 cache head, 32 query heads (multi-query decode, the
+                   pages' MLA decode absorbed into MQA), L=32768, int4, K/V as
+                   llama2-7b-layer, randomly permuted pages; 268 MB of codes
 
 D = 128 and 64-token blocks throughout.  q ~ N(0, 1).  All values are fp16.
 """
@@ -56,6 +59,10 @@ CONFIGS = {
     # chunked prefill: the last 512 of 8192 tokens attend causally over the cache
     8: dict(name="chunked-prefill", B=8, H=32, D=128, L=8192, chunk=512, fmt=INT4, sigma=1.0,
             outliers=("per_head", 4, 10.0), table="contiguous"),
+    # multi-query decode (MLA absorbed into MQA): one cache head serves 32 query
+    # heads; 64 sequences of 32K tokens put 268 MB of codes behind one step
+    9: dict(name="mqa-32k", B=64, H=1, Hq=32, D=128, L=32768, fmt=INT4, sigma=1.0,
+            outliers=("per_head", 4, 10.0), table="permuted"),
 }
 
 
@@ -113,6 +120,18 @@ class Workload:
         x = fill_f16_host(n, self.seed, stream_id(kind, b), t0 * self.H * self.D, self.sigma, mask,
                           self.outlier_mult)
         return x.reshape(t1 - t0, self.H, self.D)
+
+    def kv_host_head(self, which, b, h, t0, t1):
+        """fp16 bits [t1-t0][1][D] of head h alone of the key ('k') or value ('v')
+        history of sequence b: the same bits as kv_host(...)[:, h:h+1, :],
+        generated one D-element row per token."""
+        kind, mask = (K_HIST, self.k_mask) if which == "k" else (V_HIST, self.v_mask)
+        out = np.empty((t1 - t0, 1, self.D), dtype=np.uint16)
+        sid = stream_id(kind, b)
+        for t in range(t0, t1):
+            out[t - t0, 0] = fill_f16_host(self.D, self.seed, sid, (t * self.H + h) * self.D, self.sigma, mask,
+                                           self.outlier_mult)
+        return out
 
     def q_host(self, step=0):
         """fp16 bits [B][Hq][D] of the query of decode step `step`."""

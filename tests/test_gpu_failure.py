@@ -2,7 +2,7 @@
 the GPU.
 
 * A bounded wait that runs out.  The test hook (include/kvq_testing.h) makes
-  the grid's first warp arm the barrier of one of its chunks without issuing
+  the grid's first warp arm the barrier of its second chunk without issuing
   that chunk's copies; with the wait limit at 1 ms the warp's wait for the
   chunk runs out with nothing in flight, it sets KVQ_FLAG_TIMEOUT and returns.
   The call completes, kvq_get_device_status reports KVQ_ERR_TIMEOUT, and the
@@ -29,10 +29,14 @@ TOL = 2e-3
 D = 128
 
 
+LENS = [16384, 12000, 16385, 10000]
+H = 4
+
+
 def _problem(fmt, seed):
-    # long enough that every warp of the grid has several units and tail pieces,
-    # and every (sequence, head) is cut into pieces
-    wl = W.Workload(4, 8, D, [4096, 3000, 4097, 2500], fmt, 1.0, ("per_head", 4, 10.0), "permuted", seed=seed)
+    # long enough that every warp of the grid has several units (so the first
+    # warp fills at least two stages) and every (sequence, head) is cut into pieces
+    wl = W.Workload(len(LENS), H, D, LENS, fmt, 1.0, ("per_head", 4, 10.0), "permuted", seed=seed)
     dw = DeviceWorkload(wl)
     dw.prefill()
     q = torch.empty((wl.B, wl.H, D), dtype=torch.float16, device="cuda")
@@ -109,20 +113,34 @@ def test_skip_beyond_the_warps_chunks_changes_nothing(cuda_ok, fault_hook):
     assert _err(out, ref, vmax) <= TOL
 
 
-@pytest.mark.parametrize("pattern", ["ticket_word", "piece_words", "garbage"])
+def _counter_word_of_first_head():
+    """The counter word that counts (sequence 0, head 0) of the int4 problem:
+    the split gives warp w the units [U w / GW, U (w+1) / GW) with U = the
+    units of all (sequence, head)s (32 tokens each, sequence-major), GW =
+    min(SMs x 12, ceil(U / 2)); a split (sequence, head) is counted in the
+    word of the warp that holds its last unit."""
+    units = [(L + 31) // 32 for L in LENS]
+    U = H * sum(units)
+    GW = min(torch.cuda.get_device_properties(0).multi_processor_count * 12, (U + 1) // 2)
+    last = units[0] - 1
+    return ((last + 1) * GW - 1) // U
+
+
+@pytest.mark.parametrize("pattern", ["one_word", "every_word", "garbage"])
 def test_dirty_workspace_is_reported(cuda_ok, pattern):
-    """Word 0 of the counter region hands out the tail pieces, words 1.. count
-    the units of split (sequence, head)s.  A stale count of 1 in either, or
-    arbitrary bytes everywhere, must raise KVQ_FLAG_BAD_WORKSPACE."""
+    """The workspace starts with one counter word per warp of the grid, which
+    counts the units of split (sequence, head)s.  A stale count of 1 in the
+    word that (sequence 0, head 0) uses, in every word, or arbitrary bytes
+    everywhere, must raise KVQ_FLAG_BAD_WORKSPACE."""
     wl, dw, q = _problem(kvq.KVQ_INT4_B64, 13)
     ref, vmax = _oracle_out(wl)
     ws = dw.workspace
     words = ws.view(torch.int64)
-    if pattern == "ticket_word":
-        words[0] = 1
-    elif pattern == "piece_words":
+    if pattern == "one_word":
+        words[_counter_word_of_first_head()] = 1
+    elif pattern == "every_word":
         sms = torch.cuda.get_device_properties(0).multi_processor_count
-        words[1:1 + sms * 16 * 5] = 1  # every piece counter the grid can use
+        words[:sms * 16] = 1  # every counter the grid can use
     else:
         g = torch.Generator(device="cuda").manual_seed(5)
         ws.copy_(torch.randint(0, 256, ws.shape, dtype=torch.uint8, device="cuda", generator=g))

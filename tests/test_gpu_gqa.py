@@ -56,12 +56,21 @@ def _check(wl, lens, q_bits, got, g, oc=None):
     return err
 
 
-@pytest.mark.parametrize("g", [2, 4])
-def test_grouped_heads_ragged_lengths(cuda_ok, g):
+FMTS = {"int4": kvq.KVQ_INT4_B64, "int8": kvq.KVQ_INT8_PAGE, "fp8": kvq.KVQ_FP8_E4M3}
+# (format, g): g = 2, 4 on int4 use the spare-column kernel; every other pair
+# the 16-query-head tile kernel (g = 3: one partial tile, 24: a full and a half
+# tile, 32: two tiles)
+GROUPS = [("int4", 2), ("int4", 4), ("int4", 3), ("int4", 8), ("int4", 16), ("int4", 32),
+          ("int8", 2), ("int8", 8), ("int8", 24), ("int8", 32),
+          ("fp8", 4), ("fp8", 8), ("fp8", 16), ("fp8", 32)]
+
+
+@pytest.mark.parametrize("fmt,g", GROUPS)
+def test_grouped_heads_ragged_lengths(cuda_ok, fmt, g):
     """Lengths at every unit/page edge, an empty sequence, a permuted table,
     outlier channels; 3 cache heads x g query heads."""
     lens = [1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 0, 257, 700, 1000]
-    wl = W.Workload(len(lens), 3, D, lens, kvq.KVQ_INT4_B64, 1.0, ("per_head", 3, 10.0), "permuted", seed=31)
+    wl = W.Workload(len(lens), 3, D, lens, FMTS[fmt], 1.0, ("per_head", 3, 10.0), "permuted", seed=31)
     dw = DeviceWorkload(wl)
     dw.prefill()
     q = _queries(wl.B, 3 * g, 32 + g)
@@ -71,12 +80,29 @@ def test_grouped_heads_ragged_lengths(cuda_ok, g):
     assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
 
 
-@pytest.mark.parametrize("g", [2, 4])
-def test_grouped_heads_one_long_sequence_many_pieces(cuda_ok, g):
+@pytest.mark.parametrize("fmt", ["int4", "int8", "fp8"])
+@pytest.mark.parametrize("g", [32, 64])
+def test_multi_query_one_cache_head(cuda_ok, fmt, g):
+    """Multi-query decode (the pages' MLA decode absorbed into MQA): one cache
+    head serves all g query heads; ragged lengths in a permuted table, long
+    enough that every sequence is split over many warps."""
+    lens = [9000, 1, 4100, 0, 333, 12000]
+    wl = W.Workload(len(lens), 1, D, lens, FMTS[fmt], 1.0, ("per_head", 4, 10.0), "permuted", seed=40 + g)
+    dw = DeviceWorkload(wl)
+    dw.prefill()
+    q = _queries(wl.B, g, 41 + g, scale=1.5)
+    got = _run(dw, q, g)
+    _check(wl, wl.lens, q, got, g)
+    assert np.all(got[lens.index(0)] == 0)
+    assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
+
+
+@pytest.mark.parametrize("fmt,g", [("int4", 2), ("int4", 4), ("int4", 8), ("int8", 32), ("fp8", 16)])
+def test_grouped_heads_one_long_sequence_many_pieces(cuda_ok, fmt, g):
     """One cache head long enough to be cut into about a thousand split pieces:
-    the last piece's warp merges all g query heads (several rounds of 32 lanes);
-    the workspace is reused without clearing."""
-    wl = W.Workload(1, 1, D, [65536 + 40], kvq.KVQ_INT4_B64, 1.0, None, "permuted", seed=33)
+    the merge combines them all (several rounds of 32 lanes); the workspace is
+    reused without clearing and gives the same bits."""
+    wl = W.Workload(1, 1, D, [65536 + 40], FMTS[fmt], 1.0, None, "permuted", seed=33)
     dw = DeviceWorkload(wl)
     dw.prefill()
     q = _queries(1, g, 34, scale=2.0)
@@ -129,24 +155,22 @@ def test_grouped_heads_share_the_cache_pass(cuda_ok):
 
 
 def test_grouped_heads_argument_checks(cuda_ok):
-    cache8 = kvq.PagedKVCache(kvq.KVQ_INT8_PAGE, 4, 2)
-    q = torch.zeros((1, 4, D), dtype=torch.float16, device="cuda")
+    cache4 = kvq.PagedKVCache(kvq.KVQ_INT4_B64, 4, 2)
     bt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
     sl = torch.ones(1, dtype=torch.int32, device="cuda")
     ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
-    with pytest.raises(kvq.KvqError) as e:   # int8 runs g = 1 only
-        kvq.kvq_decode_attention_gqa(cache8, q, bt, sl, 0.1, q.clone(), ws)
-    assert e.value.status == 2
-    cache4 = kvq.PagedKVCache(kvq.KVQ_INT4_B64, 4, 2)
     q3 = torch.zeros((1, 3, D), dtype=torch.float16, device="cuda")
     with pytest.raises(kvq.KvqError) as e:   # not a multiple of the cache heads
         kvq.kvq_decode_attention_gqa(cache4, q3, bt, sl, 0.1, q3.clone(), ws)
     assert e.value.status == 1
-    q16 = torch.zeros((1, 16, D), dtype=torch.float16, device="cuda")
-    with pytest.raises(kvq.KvqError) as e:   # g = 8 is not built
-        kvq.kvq_decode_attention_gqa(cache4, q16, bt, sl, 0.1, q16.clone(), ws)
+    q_big = torch.zeros((1, 2 * 2048, D), dtype=torch.float16, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:   # g = 2048 is beyond the largest group
+        kvq.kvq_decode_attention_gqa(cache4, q_big, bt, sl, 0.1, q_big.clone(), ws)
     assert e.value.status == 2
     w1 = kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT4_B64, 8, 8)
     w4 = kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT4_B64, 8, 32)
     assert w1 == kvq.kvq_decode_workspace_bytes(kvq.KVQ_INT4_B64, 8) and 3 * w1 < w4 < 4 * w1
-    assert kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT4_B64, 8, 64) == 0
+    # tiles of 16 query heads: the partials hold 16 rows whatever the group
+    w8 = kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT8_PAGE, 8, 64)
+    assert w8 > 0 and w8 == kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT8_PAGE, 1, 32)
+    assert kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT4_B64, 1, 2048) == 0

@@ -60,7 +60,8 @@ def _same_cache(a, b):
 
 
 @pytest.mark.parametrize("fmt,H,Hq", [(kvq.KVQ_INT4_B64, 4, None), (kvq.KVQ_INT8_PAGE, 4, None),
-                                      (kvq.KVQ_FP8_E4M3, 4, None), (kvq.KVQ_INT4_B64, 2, 8)])
+                                      (kvq.KVQ_FP8_E4M3, 4, None), (kvq.KVQ_INT4_B64, 2, 8),
+                                      (kvq.KVQ_INT8_PAGE, 2, 16), (kvq.KVQ_INT4_B64, 1, 32)])
 def test_graph_replay_equals_eager(cuda_ok, fmt, H, Hq):
     """70 steps (every sequence crosses a page boundary): the graph, fed
     through its bound slots, and the eager calls give identical bits."""

@@ -85,7 +85,7 @@ def test_noalloc_recovers_after_a_call_cut_short(cuda_ok):
     """The test hook makes one call's bounded wait run out (1 ms, with no copy
     in flight); that call reports KVQ_ERR_TIMEOUT and leaves the shared
     array's counters non-zero.  The next two calls still match the oracle."""
-    dw, q, ref, oref, vmax = _problem(kvq.KVQ_INT4_B64, [4096, 3000, 4097, 2500], 4)
+    dw, q, ref, oref, vmax = _problem(kvq.KVQ_INT4_B64, [16384, 12000, 16385, 10000], 4)
     try:
         kvq.kvq_testing_set_decode_fault(1000, 1)
         _noalloc(dw, q)
