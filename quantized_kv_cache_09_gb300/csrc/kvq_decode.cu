@@ -1752,15 +1752,17 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
 // right after the split kernel with programmatic dependent launch: the
 // prologue (lengths, unit prefix, split geometry -- the same values the split
 // computed) overlaps the split's tail; partials are read after the wait.
-template <int UT>
-__global__ void __launch_bounds__(kMqRows * 32) decode_tile_merge_kernel(DecodeParams p, int grid_warps)
+constexpr int kMergeWarps = 16;  // warps of a merge CTA; each merges query rows warp, warp + 16, ...
+
+template <int UT, int kRowsPerHead>
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_tile_merge_kernel(DecodeParams p, int grid_workers)
 {
     __shared__ int32_t s_cu[kMaxSeqsPerLaunch + 1];
     __shared__ int32_t s_len[kMaxSeqsPerLaunch];
     __shared__ Split s_split;
     const int T = p.tiles, H = p.num_heads, HU = H * T;
     pdl_launch_dependents();
-    decode_prologue<UT>(p, HU, grid_warps, s_cu, s_len, &s_split);
+    decode_prologue<UT>(p, HU, grid_workers, s_cu, s_len, &s_split);
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = (int)(blockIdx.x / HU), h = (int)(blockIdx.x - (unsigned)b * HU);
@@ -1771,12 +1773,13 @@ __global__ void __launch_bounds__(kMqRows * 32) decode_tile_merge_kernel(DecodeP
     const int64_t pf = sp.piece_of(u0), pl = sp.piece_of(u0 + n - 1);
     if (pf == pl) return;  // inside one piece: the split kernel wrote the rows
     const int hc = h / T, tile = h - hc * T;
-    const int rows = min(kMqRows, p.group - kMqRows * tile);
-    if (warp >= rows) return;
+    const int rows = min(kRowsPerHead, p.group - kRowsPerHead * tile);
     const int first_slot = sp.start(pf) != u0 ? 1 : 0;
-    uint16_t *orow = p.out + (((int64_t)b * H + hc) * p.group + kMqRows * tile + warp) * kHeadDim;
-    merge_pieces<16>(p.partials, (int64_t)kMqRows * kPartialStride, warp, pf, (int)(pl - pf + 1), first_slot, orow,
-                     lane);
+    for (int r = warp; r < rows; r += kMergeWarps) {
+        uint16_t *orow = p.out + (((int64_t)b * H + hc) * p.group + kRowsPerHead * tile + r) * kHeadDim;
+        merge_pieces<16>(p.partials, (int64_t)kRowsPerHead * kPartialStride, r, pf, (int)(pl - pf + 1), first_slot,
+                         orow, lane);
+    }
 }
 
 template <int FMT, int G>
@@ -1913,8 +1916,8 @@ static cudaError_t launch_variant(const DecodeParams &p0, int kg, int gw, cudaSt
         if (e != cudaSuccess) return e;
         const unsigned pairs = (unsigned)p.num_seqs * (unsigned)(p.num_heads * p.tiles);
         if (pairs == 0) return cudaSuccess;
-        return launch_pdl(decode_tile_merge_kernel<DecFmt<FMT>::kUnitTok>, dim3(pairs), dim3(kMqRows * 32), 0, s, p,
-                          gw);
+        return launch_pdl(decode_tile_merge_kernel<DecFmt<FMT>::kUnitTok, kMqRows>, dim3(pairs),
+                          dim3(kMergeWarps * 32), 0, s, p, gw);
     }
     p.tiles = 1;
     const dim3 block(variant_warps(FMT, kg) * 32);

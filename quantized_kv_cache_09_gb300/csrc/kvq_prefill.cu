@@ -250,11 +250,6 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
     return d;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // barrier 1 over the widening warpgroup, returning whether every thread passed `v`
 __device__ __forceinline__ bool widen_group_all(bool v)
 {
