@@ -707,6 +707,14 @@ def measure_chunked_prefill(K, Wm, seed, dev):
 # --------------------------------------------------------------------------
 # result lines
 # --------------------------------------------------------------------------
+def _decode_kernels(wl):
+    """The kernels one decode call launches (the roofline's event time covers them all)."""
+    g = wl.Hq // wl.H
+    if g == 1 or (wl.fmt == 0 and g in (2, 4)):
+        return "kvq_decode_attention (decode_split_kernel, split merge in the same launch)"
+    return "kvq_decode_attention_gqa (decode_split_kernel on 16-query-head tiles + decode_tile_merge_kernel)"
+
+
 def decode_result(name, r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed=0):
     total_ms = max_over_ranks(pg, r["total_ms"], dev)
     e2e_ms = max_over_ranks(pg, r["e2e_ms"], dev)
@@ -721,7 +729,7 @@ def decode_result(name, r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed=0):
            "config": workload_config(name, world, cfg_seed),
            "kv_gb_per_s": achieved, "decode_us": dec_ms * 1e3, "append_us": app_ms * 1e3,
            "step_us_events_between_calls": r["split_ms"] / K * 1e3,
-           "roofline": {"kernel": "kvq_decode_attention (decode_split_kernel, merge fused)", "bound": "hbm",
+           "roofline": {"kernel": _decode_kernels(r["wl"]), "bound": "hbm",
                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                         "frac": achieved / peak, "traffic": ncu_traffic("decode_split_kernel", name),
                         "algorithmic_bytes_per_launch": r["dec_bytes"],

@@ -21,9 +21,11 @@ extern "C" {
 #endif
 
 /*
- * kvq_testing_set_decode_fault -- settings of every later decode launch of
- * this process (kvq_decode_attention, _gqa, _noalloc and decode steps captured
- * into a graph after the call), on every device, until changed again:
+ * kvq_testing_set_decode_fault -- settings of every later multi-head decode
+ * launch of this process (kvq_decode_attention, _noalloc, _gqa with one query
+ * head per cache head, and such steps captured into a graph after the call),
+ * on every device, until changed again; while they differ from the defaults
+ * those launches run an instantiation of the kernel that reads them:
  *   wait_limit_us  limit of each bounded wait in microseconds; 0 restores the
  *                  default of 0.5 s
  *   skip_chunk     >= 0: the first warp of the grid arms the barrier of its

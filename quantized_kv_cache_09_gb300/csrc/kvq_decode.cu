@@ -1433,8 +1433,12 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams &p, int HU, i
 
 // G: query heads per cache head (1: multi-head attention; 2, 4: int4 grouped
 // heads in spare MMA columns; kMqG: tiles of up to 16 query heads of any group
-// size p.group, p.tiles tiles per cache head, each tile a unit head of its own)
-template <int FMT, int G>
+// size p.group, p.tiles tiles per cache head, each tile a unit head of its own).
+// kHook: the instantiation launched while the test hook of kvq_testing.h is
+// set -- its waits take their limit from p.wait_limit_ns and the grid's first
+// warp can leave a chunk unissued; the other instantiations wait the fixed
+// kWaitLimitNs and carry no such check.
+template <int FMT, int G, bool kHook = false>
 __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kCtasPerSm)
     decode_split_kernel(DecodeParams p, int grid_warps)
 {
@@ -1559,7 +1563,8 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
     int ci = 0;                 // stages filled so far (chunk count)
     // the timeout test's chunk (kvq_testing.h): the grid's first warp leaves
     // its copies unissued, so the stage's wait runs out with nothing in flight
-    const int skip_ci = gw == 0 ? p.test_skip_chunk : -1;
+    const int skip_ci = kHook && gw == 0 ? p.test_skip_chunk : -1;
+    const uint64_t wait_ns = kHook ? p.wait_limit_ns : kWaitLimitNs;
     bool issue_done = false;    // the warp's range is fully issued
     bool piece_new = true;      // the next stage is the warp's first
     // Fill stage ci % kStages with the next chunk: the cursor's unit and the
@@ -1594,7 +1599,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
             const uint32_t qbytes = (uint32_t)qrows * kHeadDim * 2;
             const uint32_t bytes = 2 * cb + (new_seg ? qbytes : 0);
             mbar_arrive_expect_tx(&ws.full[s], bytes);
-            if (ci != skip_ci) {
+            if (!kHook || ci != skip_ci) {
                 const size_t off = ((size_t)pg * H + hc) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
                 bulk_copy_g2s(ws.k[s], p.k_codes + off, cb, &ws.full[s]);
                 bulk_copy_g2s(ws.v[s], p.v_codes + off, cb, &ws.full[s]);
@@ -1674,7 +1679,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
     };
     auto drain = [&](int from) {  // after a timeout: let the copies still in flight land
         for (int y = from; y < ci; y++)
-            mbar_wait_bounded(&ws.full[y % kStages], (uint32_t)((y / kStages) & 1), p.wait_limit_ns);
+            mbar_wait_bounded(&ws.full[y % kStages], (uint32_t)((y / kStages) & 1), wait_ns);
     };
     auto seg_start = [&](const int4 &m) {
         cur_b = m.x;
@@ -1685,7 +1690,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
     };
 
     // chunk 0, unit 0
-    if (!mbar_wait_bounded(&ws.full[0], 0u, p.wait_limit_ns)) {
+    if (!mbar_wait_bounded(&ws.full[0], 0u, wait_ns)) {
         if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
         drain(1);
         return;
@@ -1719,7 +1724,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
         float sc1[kScores];
         if (more) {
             const int s1 = (cc + 1) % kStages;
-            if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((cc + 1) / kStages) & 1), p.wait_limit_ns)) {
+            if (!mbar_wait_bounded(&ws.full[s1], (uint32_t)(((cc + 1) / kStages) & 1), wait_ns)) {
                 if (lane == 0) set_flag(p.status, KVQ_FLAG_TIMEOUT);
                 drain(cc + 2);
                 return;
@@ -1792,6 +1797,10 @@ static int ctas_per_sm()
         if (cudaFuncSetAttribute(decode_split_kernel<FMT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)dec_smem_bytes<FMT, G>()) != cudaSuccess)
             return 0;
+        if constexpr (G == 1)
+            if (cudaFuncSetAttribute(decode_split_kernel<FMT, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)dec_smem_bytes<FMT, 1>()) != cudaSuccess)
+                return 0;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<FMT, G>,
                                                           DecShape<FMT, G>::kWarps * 32,
@@ -1921,8 +1930,11 @@ static cudaError_t launch_variant(const DecodeParams &p0, int kg, int gw, cudaSt
     }
     p.tiles = 1;
     const dim3 block(variant_warps(FMT, kg) * 32);
-    if (kg == 1)
-        return launch_pdl(decode_split_kernel<FMT, 1>, grid, block, dec_smem_bytes<FMT, 1>(), s, p, gw);
+    if (kg == 1) {
+        const bool hook = p.test_skip_chunk >= 0 || p.wait_limit_ns != kWaitLimitNs;
+        return launch_pdl(hook ? decode_split_kernel<FMT, 1, true> : decode_split_kernel<FMT, 1, false>, grid, block,
+                          dec_smem_bytes<FMT, 1>(), s, p, gw);
+    }
     if constexpr (FMT == KVQ_INT4_B64) {
         if (kg == 2) {
             if (ctas_per_sm<FMT, 2>() < 1) return cudaErrorInvalidDevice;

@@ -15,7 +15,7 @@ namespace kvq {
 constexpr unsigned kFull = 0xffffffffu;
 
 // a bounded wait gives up after this long; kernels finish in milliseconds
-constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+constexpr uint64_t kWaitLimitNs = kDecodeWaitLimitNs;
 
 __device__ __forceinline__ void set_flag(int32_t *status, int32_t bit)
 {
