@@ -28,7 +28,6 @@ cpu_baseline / --impl reference: the CPU oracle timed on host cores on a
          bounded sample of the same step
 """
 import argparse
-import concurrent.futures as cf
 import hashlib
 import json
 import math
