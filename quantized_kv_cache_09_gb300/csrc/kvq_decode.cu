@@ -235,6 +235,34 @@ __device__ __forceinline__ uint32_t nib_pair(uint32_t x, bool odd, const Magic &
     return odd ? nib_hi(x, k) : nib_lo(x, k);
 }
 
+// Offset-binary widening to fp16 subnormals, one lop3 per pair: with the
+// nibble's sign bit flipped, the low nibble of each 16-bit half read as an
+// fp16 is the subnormal (c + 8) * 2^-24, bits 4..7 the subnormal
+// (c + 8) * 2^-20 -- exact, and the tensor cores take subnormal operands at
+// full precision.  The offset 8 and the two powers of two are taken out after
+// the contraction: QK with the odd (bits 4..7) elements of q scaled by 1/16
+// and 8 * sum(q) subtracted from each score; PV with 8 * sum(p * scale_v)
+// subtracted from each output and the odd elements scaled by 1/16.
+struct SubMagic {
+    uint32_t m_lo, m_hi, x_lo, x_hi;  // 0x000f000f, 0x00f000f0, 0x00080008, 0x00800080
+    __device__ __forceinline__ void init()
+    {
+        m_lo = 0x000f000fu;
+        m_hi = 0x00f000f0u;
+        x_lo = 0x00080008u;
+        x_hi = 0x00800080u;
+        asm volatile("" : "+r"(m_lo), "+r"(m_hi), "+r"(x_lo), "+r"(x_hi));
+    }
+};
+__device__ __forceinline__ uint32_t sub_lo(uint32_t x, const SubMagic &k) { return lop_and_xor(x, k.m_lo, k.x_lo); }
+__device__ __forceinline__ uint32_t sub_hi(uint32_t x, const SubMagic &k) { return lop_and_xor(x, k.m_hi, k.x_hi); }
+__device__ __forceinline__ uint32_t sub_pair(uint32_t x, bool odd, const SubMagic &k)
+{
+    return odd ? sub_hi(x, k) : sub_lo(x, k);
+}
+constexpr float kSubLo = 16777216.0f;  // 2^24: the even elements' unit
+constexpr float kSubHi = 1048576.0f;   // 2^20: the odd elements' unit
+
 // two softmax weights split into fp16 pairs hi = {RN16(x0), RN16(x1)} and
 // lo = {RN16(x0 - hi0), RN16(x1 - hi1)}: hi + lo keeps ~22 significant bits
 __device__ __forceinline__ void hi_lo_pairs(uint64_t x, uint32_t &hi, uint32_t &lo)
@@ -266,17 +294,20 @@ struct Consumer<KVQ_INT4_B64> {
     static constexpr int kScores = 4;
     static constexpr int kPf = 4;
     int rows;  // (unused: one query row)
-    uint32_t qb[8][2];
-    float acc[8][4];
+    uint32_t qb[8][2];  // q as the B operand, the odd elements scaled by 1/16
+    float acc[8][4];    // sum of x * (c + 8) in units of 2^-24 (even elements) or 2^-20 (odd)
     float m_run;
+    float qbias;  // -8 * sum(q): the offset's share of every score
     uint64_t l2;  // running sum of the weights in this lane's slots, as a pair
-    Magic mk;
+    uint64_t x2;  // running sum of x = p * scale_v in this lane's slots, as a pair
+    SubMagic mk;
 
     __device__ __forceinline__ void reset()
     {
         mk.init();
         m_run = -INFINITY;
         l2 = pk2(0.0f, 0.0f);
+        x2 = pk2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 8; i++)
 #pragma unroll
@@ -287,18 +318,34 @@ struct Consumer<KVQ_INT4_B64> {
     {
         const int t = lane & 3;
         const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + 32 * t);
+        const __half2 sixteenth = __float2half2_rn(0.0625f);
+        float qsum = 0.0f;
 #pragma unroll
         for (int m = 0; m < 4; m++) {
             const uint4 v = q4[m];  // elements 32t + 8m .. +7 as pairs (0,1) (2,3) (4,5) (6,7)
-            qb[2 * m][0] = __byte_perm(v.x, v.z, 0x5410);      // {e0, e4}
-            qb[2 * m][1] = __byte_perm(v.x, v.z, 0x7632);      // {e1, e5}
-            qb[2 * m + 1][0] = __byte_perm(v.y, v.w, 0x5410);  // {e2, e6}
-            qb[2 * m + 1][1] = __byte_perm(v.y, v.w, 0x7632);  // {e3, e7}
+            const uint32_t e04 = __byte_perm(v.x, v.z, 0x5410), e15 = __byte_perm(v.x, v.z, 0x7632);
+            const uint32_t e26 = __byte_perm(v.y, v.w, 0x5410), e37 = __byte_perm(v.y, v.w, 0x7632);
+            const __half2 o15 = __hmul2(*reinterpret_cast<const __half2 *>(&e15), sixteenth);
+            const __half2 o37 = __hmul2(*reinterpret_cast<const __half2 *>(&e37), sixteenth);
+            qb[2 * m][0] = e04;               // {e0, e4}
+            qb[2 * m][1] = h2_bits(o15);      // {e1, e5} / 16
+            qb[2 * m + 1][0] = e26;           // {e2, e6}
+            qb[2 * m + 1][1] = h2_bits(o37);  // {e3, e7} / 16
+            // the sum of q as the mma sees it: odd elements are 16 x their scaled copies
+            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&e04));
+            const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&e26));
+            const float2 o = __half22float2(__hadd2(o15, o37));
+            qsum += (a.x + a.y) + (c.x + c.y);
+            qsum = fmaf(16.0f, o.x + o.y, qsum);
         }
+        qsum += __shfl_xor_sync(kFull, qsum, 1);  // the four lanes t of a row hold the four slices
+        qsum += __shfl_xor_sync(kFull, qsum, 2);
+        qbias = -8.0f * qsum;
     }
 
-    // raw dot products q . c of tokens g, g+8, 16+g, 24+g (every lane); four
-    // accumulator chains per tile keep the mma dependency chains short
+    // raw dot products 2^-24 (q . c + 8 sum(q)) of tokens g, g+8, 16+g, 24+g
+    // (every lane); four accumulator chains per tile keep the mma dependency
+    // chains short
     __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[4]) const
     {
         const int g = lane >> 2, t = lane & 3;
@@ -316,10 +363,12 @@ struct Consumer<KVQ_INT4_B64> {
 #pragma unroll
             for (int m = 0; m < 4; m++) {
                 uint32_t ca[4], cb[4];
-                widen_int4_u32(ua[m], ca, mk);
-                widen_int4_u32(ub[m], cb, mk);
-                mma16816(c[m], ca[0], cb[0], ca[1], cb[1], qb[2 * m][0], qb[2 * m][1]);
-                mma16816(c[m], ca[2], cb[2], ca[3], cb[3], qb[2 * m + 1][0], qb[2 * m + 1][1]);
+                // {c0,c4}, {c1,c5}, {c2,c6}, {c3,c7} of each token row
+                const uint32_t ah = ua[m] >> 8, bh = ub[m] >> 8;
+                mma16816(c[m], sub_lo(ua[m], mk), sub_lo(ub[m], mk), sub_hi(ua[m], mk), sub_hi(ub[m], mk),
+                         qb[2 * m][0], qb[2 * m][1]);
+                mma16816(c[m], sub_lo(ah, mk), sub_lo(bh, mk), sub_hi(ah, mk), sub_hi(bh, mk), qb[2 * m + 1][0],
+                         qb[2 * m + 1][1]);
             }
             sc[2 * tau] = (c[0][0] + c[1][0]) + (c[2][0] + c[3][0]);
             sc[2 * tau + 1] = (c[0][2] + c[1][2]) + (c[2][2] + c[3][2]);
@@ -334,10 +383,10 @@ struct Consumer<KVQ_INT4_B64> {
                                             uint32_t px[2])
     {
         const int g = lane >> 2, t = lane & 3;
-        const uint64_t ff = pk2(fac, fac);
+        const uint64_t ff = pk2(fac * kSubLo, fac * kSubLo), fb = pk2(qbias * fac, qbias * fac);
         float s2[4];
-        upk2(mul2(pk2(sc[0], sc[1]), ff), s2[0], s2[1]);
-        upk2(mul2(pk2(sc[2], sc[3]), ff), s2[2], s2[3]);
+        upk2(fma2(pk2(sc[0], sc[1]), ff, fb), s2[0], s2[1]);
+        upk2(fma2(pk2(sc[2], sc[3]), ff, fb), s2[2], s2[3]);
         if (ntok < 32) {  // the last unit of a sequence: tokens past its end get no weight
 #pragma unroll
             for (int i = 0; i < 4; i++)
@@ -348,6 +397,7 @@ struct Consumer<KVQ_INT4_B64> {
             const float mu = warp_max(lm);
             const float alpha = ex2_approx(m_run - mu);
             l2 = mul2(l2, pk2(alpha, alpha));
+            x2 = mul2(x2, pk2(alpha, alpha));
 #pragma unroll
             for (int i = 0; i < 8; i++)
 #pragma unroll
@@ -358,8 +408,10 @@ struct Consumer<KVQ_INT4_B64> {
 #pragma unroll
         for (int i = 0; i < 4; i++) pe[i] = ex2_approx(s2[i] - m_run);
         const uint64_t p01 = pk2(pe[0], pe[1]), p23 = pk2(pe[2], pe[3]);
-        l2 = add2(l2, add2(p01, p23));
+        const uint64_t psum = add2(p01, p23);
         const uint64_t vv = pk2(sv, sv);
+        l2 = add2(l2, psum);
+        x2 = fma2(psum, vv, x2);
         uint32_t hi, lo;
         hi_lo_pairs(mul2(p01, vv), hi, lo);
         px[0] = t == 0 ? hi : lo;
@@ -399,20 +451,23 @@ struct Consumer<KVQ_INT4_B64> {
 #pragma unroll
                 for (int jj = 0; jj < 4; jj++) {
                     const bool odd = jj & 1;
-                    mma16816(acc[4 * R + jj], nib_pair(xab[jj >> 1], odd, mk), nib_pair(xab[2 + (jj >> 1)], odd, mk),
-                             nib_pair(xcd[jj >> 1], odd, mk), nib_pair(xcd[2 + (jj >> 1)], odd, mk), b0, b1);
+                    mma16816(acc[4 * R + jj], sub_pair(xab[jj >> 1], odd, mk), sub_pair(xab[2 + (jj >> 1)], odd, mk),
+                             sub_pair(xcd[jj >> 1], odd, mk), sub_pair(xcd[2 + (jj >> 1)], odd, mk), b0, b1);
                 }
             }
         }
     }
 
     // out row (final) or partial slot: lanes with t == 0 hold elements
-    // 64R + 8g + e (e < 4: tile 4R+e rows g; e >= 4: tile 4R+e-4 rows g+8)
+    // 64R + 8g + e (e < 4: tile 4R+e rows g; e >= 4: tile 4R+e-4 rows g+8);
+    // odd elements come from bits 4..7 (unit 2^-20), even ones from bits 0..3
     __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
     {
-        float la, lb;
+        float la, lb, xa, xb;
         upk2(l2, la, lb);
+        upk2(x2, xa, xb);
         const float l = warp_sum(la + lb) * 0.25f;  // the four lanes of a row group hold the same weights
+        const float xbias = -8.0f * 0.25f * warp_sum(xa + xb);
         const int g = lane >> 2, t = lane & 3;
         if (t != 0) return;
 #pragma unroll
@@ -420,8 +475,9 @@ struct Consumer<KVQ_INT4_B64> {
             float v[8];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                v[e] = acc[4 * R + e][0] + acc[4 * R + e][1];
-                v[4 + e] = acc[4 * R + e][2] + acc[4 * R + e][3];
+                const float f = (e & 1) ? kSubHi : kSubLo;
+                v[e] = fmaf(acc[4 * R + e][0] + acc[4 * R + e][1], f, xbias);
+                v[4 + e] = fmaf(acc[4 * R + e][2] + acc[4 * R + e][3], f, xbias);
             }
             if (orow) {
                 const float inv = 1.0f / l;

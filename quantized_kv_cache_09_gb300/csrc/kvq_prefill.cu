@@ -242,14 +242,6 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return d;
 }
 
-// a * b + c on binary32 pairs, each rounded once
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
 // barrier 1 over the widening warpgroup, returning whether every thread passed `v`
 __device__ __forceinline__ bool widen_group_all(bool v)
 {
