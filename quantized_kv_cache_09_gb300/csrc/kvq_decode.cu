@@ -4,7 +4,8 @@
 //
 // Decode is a GEMV per (sequence, head): every cached byte is read once and
 // used for a handful of flops, so the kernel is built around HBM streaming.
-// The int4 path widens codes exactly to fp16 in registers and feeds the
+// The int4 path widens codes exactly to fp16 subnormals in registers (one
+// lop3 per pair, the offset taken out after the contraction) and feeds the
 // legacy tensor-core mma (m16n8k16) because the widening, not the multiply,
 // is the cost; the int8 path stays on CUDA-core FMAs.
 //
@@ -180,23 +181,6 @@ template <int FMT>
 struct Consumer;
 
 
-// The masks and magic words of the widening, held in registers: a SASS lop3
-// takes at most one immediate, so (x & mask) ^ magic with both as literals
-// costs two lop3 on the half-rate integer pipe; with both in registers it is
-// one.  The empty asm makes the values opaque so they are not folded back
-// into immediates.
-struct Magic {
-    uint32_t m_lo, m_hi, x_lo, x_hi;  // 0x000f000f, 0x00f000f0, 0x64086408, 0x64806480
-    __device__ __forceinline__ void init()
-    {
-        m_lo = 0x000f000fu;
-        m_hi = 0x00f000f0u;
-        x_lo = 0x64086408u;
-        x_hi = 0x64806480u;
-        asm volatile("" : "+r"(m_lo), "+r"(m_hi), "+r"(x_lo), "+r"(x_hi));
-    }
-};
-
 __device__ __forceinline__ uint32_t lop_and_xor(uint32_t x, uint32_t m, uint32_t c)
 {
     uint32_t d;
@@ -204,53 +188,36 @@ __device__ __forceinline__ uint32_t lop_and_xor(uint32_t x, uint32_t m, uint32_t
     return d;
 }
 
-// low nibble of each 16-bit half -> exact fp16 of its signed value: 1024 + (n ^ 8) - 1032
-__device__ __forceinline__ uint32_t nib_lo(uint32_t x, const Magic &k)
-{
-    const uint32_t a = lop_and_xor(x, k.m_lo, k.x_lo);
-    return h2_bits(__hsub2(*reinterpret_cast<const __half2 *>(&a), __float2half2_rn(1032.0f)));
-}
-
-// bits 4..7 of each 16-bit half -> exact fp16 of its signed value: (1024 + 16 (n ^ 8)) / 16 - 72
-__device__ __forceinline__ uint32_t nib_hi(uint32_t x, const Magic &k)
-{
-    const uint32_t b = lop_and_xor(x, k.m_hi, k.x_hi);
-    return h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&b), __float2half2_rn(0.0625f),
-                           __float2half2_rn(-72.0f)));
-}
-
-// int4 word -> exact fp16 pairs {c0,c4},{c1,c5},{c2,c6},{c3,c7}
-__device__ __forceinline__ void widen_int4_u32(uint32_t w, uint32_t c[4], const Magic &k)
-{
-    const uint32_t hi = w >> 8;
-    c[0] = nib_lo(w, k);
-    c[1] = nib_hi(w, k);
-    c[2] = nib_lo(hi, k);
-    c[3] = nib_hi(hi, k);
-}
-
-// the fp16 pair held by nibble `odd` of each 16-bit half of x (two tokens, one element)
-__device__ __forceinline__ uint32_t nib_pair(uint32_t x, bool odd, const Magic &k)
-{
-    return odd ? nib_hi(x, k) : nib_lo(x, k);
-}
-
-// Offset-binary widening to fp16 subnormals, one lop3 per pair: with the
-// nibble's sign bit flipped, the low nibble of each 16-bit half read as an
-// fp16 is the subnormal (c + 8) * 2^-24, bits 4..7 the subnormal
-// (c + 8) * 2^-20 -- exact, and the tensor cores take subnormal operands at
-// full precision.  The offset 8 and the two powers of two are taken out after
-// the contraction: QK with the odd (bits 4..7) elements of q scaled by 1/16
-// and 8 * sum(q) subtracted from each score; PV with 8 * sum(p * scale_v)
-// subtracted from each output and the odd elements scaled by 1/16.
+// int4 codes widened exactly to fp16, one lop3 per pair.  With c the signed
+// code of a nibble, flipping its bit 3 gives n = c + 8 and flipping bits
+// 0..2 gives n = 7 - c; the nibble n in the low four bits of a 16-bit half,
+// read as an fp16, is the subnormal n * 2^-24, and in bits 4..7 the subnormal
+// n * 2^-20.  So each element reaches the mma as
+//   even element (low nibble of its byte):  (c + 8) * 2^-24
+//   odd element (bits 4..7):                (7 - c) * 2^-20
+// exactly (the tensor cores take subnormal operands at full precision, and
+// every product stays far above binary32's range limit).  The offsets and the
+// powers of two come out after the contraction instead of per pair:
+//   QK: q's odd elements are scaled by -1/16, so every product is
+//       q_d c_d 2^-24 plus an offset share (+8 q_d even, -7 q_d odd); the
+//       score is 2^24 raw - (8 sum_even q - 7 sum_odd q).  The two signs
+//       make the shares of a smooth q cancel inside each mma, which keeps the
+//       tensor core's running sums -- and their rounding -- small;
+//   PV: output element d is 2^24 raw_d - 8 sum(x) (even d) or
+//       7 sum(x) - 2^20 raw_d (odd d), x the weights that went into the
+//       contraction.
+// The masks and offsets are held in registers: a SASS lop3 takes at most one
+// immediate, so (x & mask) ^ offset with both as literals costs two lop3 on the
+// half-rate integer pipe; with both in registers it is one.  The empty asm
+// makes the values opaque so they are not folded back into immediates.
 struct SubMagic {
-    uint32_t m_lo, m_hi, x_lo, x_hi;  // 0x000f000f, 0x00f000f0, 0x00080008, 0x00800080
+    uint32_t m_lo, m_hi, x_lo, x_hi;  // 0x000f000f, 0x00f000f0, 0x00080008, 0x00700070
     __device__ __forceinline__ void init()
     {
         m_lo = 0x000f000fu;
         m_hi = 0x00f000f0u;
         x_lo = 0x00080008u;
-        x_hi = 0x00800080u;
+        x_hi = 0x00700070u;
         asm volatile("" : "+r"(m_lo), "+r"(m_hi), "+r"(x_lo), "+r"(x_hi));
     }
 };
@@ -260,8 +227,19 @@ __device__ __forceinline__ uint32_t sub_pair(uint32_t x, bool odd, const SubMagi
 {
     return odd ? sub_hi(x, k) : sub_lo(x, k);
 }
-constexpr float kSubLo = 16777216.0f;  // 2^24: the even elements' unit
-constexpr float kSubHi = 1048576.0f;   // 2^20: the odd elements' unit
+// element d of a contraction over widened codes = kUnit[d & 1] * raw - kOff[d & 1] * (sum of the other operand)
+constexpr float kUnitEven = 16777216.0f;  // 2^24
+constexpr float kUnitOdd = -1048576.0f;   // -2^20
+constexpr float kOffEven = 8.0f;
+constexpr float kOffOdd = -7.0f;
+// q's odd elements as the mma takes them
+constexpr float kQOdd = -0.0625f;
+// the offset share of a score: 8 sum_even q - 7 sum_odd q, from the sums of
+// q's even elements and of its scaled odd elements (q_d = -16 * scaled)
+__device__ __forceinline__ float q_offset(float sum_even, float sum_odd_scaled)
+{
+    return fmaf(kOffOdd * -16.0f, sum_odd_scaled, kOffEven * sum_even);
+}
 
 // two softmax weights split into fp16 pairs hi = {RN16(x0), RN16(x1)} and
 // lo = {RN16(x0 - hi0), RN16(x1 - hi1)}: hi + lo keeps ~22 significant bits
@@ -277,7 +255,8 @@ __device__ __forceinline__ void hi_lo_pairs(uint64_t x, uint32_t &hi, uint32_t &
 }
 
 // int4: both contractions of a unit on the tensor cores (mma.sync m16n8k16),
-// codes widened exactly to fp16 in registers, fp32 accumulation.
+// codes widened exactly to fp16 subnormals in registers (SubMagic), fp32
+// accumulation.
 //   QK: A = 16 tokens x 16 head elements of K, every column of B = q, so every
 //       lane receives the scores of its rows (tokens g, g+8 of each tile);
 //       lane (g, t) feeds rows g, g+8 from its 16-byte slice (elements
@@ -294,10 +273,10 @@ struct Consumer<KVQ_INT4_B64> {
     static constexpr int kScores = 4;
     static constexpr int kPf = 4;
     int rows;  // (unused: one query row)
-    uint32_t qb[8][2];  // q as the B operand, the odd elements scaled by 1/16
-    float acc[8][4];    // sum of x * (c + 8) in units of 2^-24 (even elements) or 2^-20 (odd)
+    uint32_t qb[8][2];  // q as the B operand, the odd elements scaled by kQOdd
+    float acc[8][4];    // PV over the widened codes (SubMagic): raw sums
     float m_run;
-    float qbias;  // -8 * sum(q): the offset's share of every score
+    float qbias;  // minus the offset share of every score (q_offset)
     uint64_t l2;  // running sum of the weights in this lane's slots, as a pair
     uint64_t x2;  // running sum of x = p * scale_v in this lane's slots, as a pair
     SubMagic mk;
@@ -318,32 +297,34 @@ struct Consumer<KVQ_INT4_B64> {
     {
         const int t = lane & 3;
         const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + 32 * t);
-        const __half2 sixteenth = __float2half2_rn(0.0625f);
-        float qsum = 0.0f;
+        const __half2 odd_scale = __float2half2_rn(kQOdd);
+        float se = 0.0f, so = 0.0f;  // sums of the even elements and of the scaled odd ones
 #pragma unroll
         for (int m = 0; m < 4; m++) {
             const uint4 v = q4[m];  // elements 32t + 8m .. +7 as pairs (0,1) (2,3) (4,5) (6,7)
             const uint32_t e04 = __byte_perm(v.x, v.z, 0x5410), e15 = __byte_perm(v.x, v.z, 0x7632);
             const uint32_t e26 = __byte_perm(v.y, v.w, 0x5410), e37 = __byte_perm(v.y, v.w, 0x7632);
-            const __half2 o15 = __hmul2(*reinterpret_cast<const __half2 *>(&e15), sixteenth);
-            const __half2 o37 = __hmul2(*reinterpret_cast<const __half2 *>(&e37), sixteenth);
+            const __half2 o15 = __hmul2(*reinterpret_cast<const __half2 *>(&e15), odd_scale);
+            const __half2 o37 = __hmul2(*reinterpret_cast<const __half2 *>(&e37), odd_scale);
             qb[2 * m][0] = e04;               // {e0, e4}
-            qb[2 * m][1] = h2_bits(o15);      // {e1, e5} / 16
+            qb[2 * m][1] = h2_bits(o15);      // {e1, e5} * kQOdd
             qb[2 * m + 1][0] = e26;           // {e2, e6}
-            qb[2 * m + 1][1] = h2_bits(o37);  // {e3, e7} / 16
-            // the sum of q as the mma sees it: odd elements are 16 x their scaled copies
+            qb[2 * m + 1][1] = h2_bits(o37);  // {e3, e7} * kQOdd
+            // the sums in binary32 (the offset share is scaled by each page's K scale, so an
+            // error in it does not cancel in the softmax)
             const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&e04));
             const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&e26));
-            const float2 o = __half22float2(__hadd2(o15, o37));
-            qsum += (a.x + a.y) + (c.x + c.y);
-            qsum = fmaf(16.0f, o.x + o.y, qsum);
+            const float2 o = __half22float2(o15), u = __half22float2(o37);
+            se += (a.x + a.y) + (c.x + c.y);
+            so += (o.x + o.y) + (u.x + u.y);
         }
-        qsum += __shfl_xor_sync(kFull, qsum, 1);  // the four lanes t of a row hold the four slices
-        qsum += __shfl_xor_sync(kFull, qsum, 2);
-        qbias = -8.0f * qsum;
+        float qo = q_offset(se, so);
+        qo += __shfl_xor_sync(kFull, qo, 1);  // the four lanes t of a row hold the four slices
+        qo += __shfl_xor_sync(kFull, qo, 2);
+        qbias = -qo;
     }
 
-    // raw dot products 2^-24 (q . c + 8 sum(q)) of tokens g, g+8, 16+g, 24+g
+    // raw dot products (2^-24 (q . c + q_offset)) of tokens g, g+8, 16+g, 24+g
     // (every lane); four accumulator chains per tile keep the mma dependency
     // chains short
     __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[4]) const
@@ -383,7 +364,7 @@ struct Consumer<KVQ_INT4_B64> {
                                             uint32_t px[2])
     {
         const int g = lane >> 2, t = lane & 3;
-        const uint64_t ff = pk2(fac * kSubLo, fac * kSubLo), fb = pk2(qbias * fac, qbias * fac);
+        const uint64_t ff = pk2(fac * kUnitEven, fac * kUnitEven), fb = pk2(qbias * fac, qbias * fac);
         float s2[4];
         upk2(fma2(pk2(sc[0], sc[1]), ff, fb), s2[0], s2[1]);
         upk2(fma2(pk2(sc[2], sc[3]), ff, fb), s2[2], s2[3]);
@@ -460,14 +441,15 @@ struct Consumer<KVQ_INT4_B64> {
 
     // out row (final) or partial slot: lanes with t == 0 hold elements
     // 64R + 8g + e (e < 4: tile 4R+e rows g; e >= 4: tile 4R+e-4 rows g+8);
-    // odd elements come from bits 4..7 (unit 2^-20), even ones from bits 0..3
+    // (odd elements from bits 4..7, even ones from bits 0..3: SubMagic)
     __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
     {
         float la, lb, xa, xb;
         upk2(l2, la, lb);
         upk2(x2, xa, xb);
         const float l = warp_sum(la + lb) * 0.25f;  // the four lanes of a row group hold the same weights
-        const float xbias = -8.0f * 0.25f * warp_sum(xa + xb);
+        const float xs = warp_sum(xa + xb) * 0.25f;
+        const float xb_even = -kOffEven * xs, xb_odd = -kOffOdd * xs;
         const int g = lane >> 2, t = lane & 3;
         if (t != 0) return;
 #pragma unroll
@@ -475,9 +457,9 @@ struct Consumer<KVQ_INT4_B64> {
             float v[8];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                const float f = (e & 1) ? kSubHi : kSubLo;
-                v[e] = fmaf(acc[4 * R + e][0] + acc[4 * R + e][1], f, xbias);
-                v[4 + e] = fmaf(acc[4 * R + e][2] + acc[4 * R + e][3], f, xbias);
+                const float f = (e & 1) ? kUnitOdd : kUnitEven, xb = (e & 1) ? xb_odd : xb_even;
+                v[e] = fmaf(acc[4 * R + e][0] + acc[4 * R + e][1], f, xb);
+                v[4 + e] = fmaf(acc[4 * R + e][2] + acc[4 * R + e][3], f, xb);
             }
             if (orow) {
                 const float inv = 1.0f / l;
@@ -519,17 +501,20 @@ struct ConsumerGqa {
     static constexpr int kScores = 8;
     static constexpr int kPf = 4;
     int rows;  // (unused: G query rows)
-    uint32_t qb[8][2];
-    float acc[8][4];
+    uint32_t qb[8][2];  // q of head hq(grp) as the B operand, the odd elements scaled by kQOdd
+    float acc[8][4];    // PV over the widened codes (SubMagic): raw sums
     float m_run[2];
     float l_lane[2];
-    Magic mk;
+    float x_lane[2];    // this lane's part of sum(x), x = p * scale_v, per head slot
+    float qbias[2];     // minus the offset share of the scores of the lane's two slot heads
+    SubMagic mk;
 
     __device__ __forceinline__ void reset()
     {
         mk.init();
         m_run[0] = m_run[1] = -INFINITY;
         l_lane[0] = l_lane[1] = 0.0f;
+        x_lane[0] = x_lane[1] = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; i++)
 #pragma unroll
@@ -542,17 +527,37 @@ struct ConsumerGqa {
         const int g = lane >> 2, t = lane & 3;
         const int head = (((g >> 2) << 1) | (g & 1)) % G;  // column g of B
         const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + head * kHeadDim + 32 * t);
+        const __half2 odd_scale = __float2half2_rn(kQOdd);
+        float se = 0.0f, so = 0.0f;
 #pragma unroll
         for (int m = 0; m < 4; m++) {
             const uint4 v = q4[m];
-            qb[2 * m][0] = __byte_perm(v.x, v.z, 0x5410);
-            qb[2 * m][1] = __byte_perm(v.x, v.z, 0x7632);
-            qb[2 * m + 1][0] = __byte_perm(v.y, v.w, 0x5410);
-            qb[2 * m + 1][1] = __byte_perm(v.y, v.w, 0x7632);
+            const uint32_t e04 = __byte_perm(v.x, v.z, 0x5410), e15 = __byte_perm(v.x, v.z, 0x7632);
+            const uint32_t e26 = __byte_perm(v.y, v.w, 0x5410), e37 = __byte_perm(v.y, v.w, 0x7632);
+            const __half2 o15 = __hmul2(*reinterpret_cast<const __half2 *>(&e15), odd_scale);
+            const __half2 o37 = __hmul2(*reinterpret_cast<const __half2 *>(&e37), odd_scale);
+            qb[2 * m][0] = e04;
+            qb[2 * m][1] = h2_bits(o15);
+            qb[2 * m + 1][0] = e26;
+            qb[2 * m + 1][1] = h2_bits(o37);
+            // the sums in binary32 (the offset share is scaled by each page's K scale, so an
+            // error in it does not cancel in the softmax)
+            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&e04));
+            const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&e26));
+            const float2 o = __half22float2(o15), u = __half22float2(o37);
+            se += (a.x + a.y) + (c.x + c.y);
+            so += (o.x + o.y) + (u.x + u.y);
         }
+        float qo = q_offset(se, so);
+        qo += __shfl_xor_sync(kFull, qo, 1);  // the offset share of head hq(grp) in every lane of grp
+        qo += __shfl_xor_sync(kFull, qo, 2);
+        // the lane's score slots c are columns 2t + c of B, held by the lanes grp = 2t + c
+#pragma unroll
+        for (int c = 0; c < 2; c++) qbias[c] = -__shfl_sync(kFull, qo, 4 * (2 * t + c));
     }
 
-    // raw dot products: sc[4 tau + 2 r + c] = token 16 tau + grp + 8 r, head slot c
+    // raw dot products (2^-24 (q . c + q_offset)): sc[4 tau + 2 r + c] = token
+    // 16 tau + grp + 8 r, head slot c
     __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[8]) const
     {
         const int g = lane >> 2, t = lane & 3;
@@ -569,11 +574,11 @@ struct ConsumerGqa {
             const uint32_t ub[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
             for (int m = 0; m < 4; m++) {
-                uint32_t ca[4], cb[4];
-                widen_int4_u32(ua[m], ca, mk);
-                widen_int4_u32(ub[m], cb, mk);
-                mma16816(c[m], ca[0], cb[0], ca[1], cb[1], qb[2 * m][0], qb[2 * m][1]);
-                mma16816(c[m], ca[2], cb[2], ca[3], cb[3], qb[2 * m + 1][0], qb[2 * m + 1][1]);
+                const uint32_t ah = ua[m] >> 8, bh = ub[m] >> 8;
+                mma16816(c[m], sub_lo(ua[m], mk), sub_lo(ub[m], mk), sub_hi(ua[m], mk), sub_hi(ub[m], mk),
+                         qb[2 * m][0], qb[2 * m][1]);
+                mma16816(c[m], sub_lo(ah, mk), sub_lo(bh, mk), sub_hi(ah, mk), sub_hi(bh, mk), qb[2 * m + 1][0],
+                         qb[2 * m + 1][1]);
             }
 #pragma unroll
             for (int e = 0; e < 4; e++) sc[4 * tau + e] = (c[0][e] + c[1][e]) + (c[2][e] + c[3][e]);
@@ -587,10 +592,10 @@ struct ConsumerGqa {
                                             uint32_t px[4])
     {
         const int g = lane >> 2, t = lane & 3;
-        const uint64_t ff = pk2(fac, fac);
+        const uint64_t ff = pk2(fac * kUnitEven, fac * kUnitEven), fb = pk2(qbias[0] * fac, qbias[1] * fac);
         float s2[8];
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) upk2(mul2(pk2(sc[i], sc[i + 1]), ff), s2[i], s2[i + 1]);
+        for (int i = 0; i < 8; i += 2) upk2(fma2(pk2(sc[i], sc[i + 1]), ff, fb), s2[i], s2[i + 1]);
         if (ntok < 32) {  // the last unit of a sequence: tokens past its end get no weight
 #pragma unroll
             for (int i = 0; i < 8; i++)
@@ -609,6 +614,7 @@ struct ConsumerGqa {
                 mu = fmaxf(mu, m_run[c]);
                 const float alpha = ex2_approx(m_run[c] - mu);
                 l_lane[c] *= alpha;
+                x_lane[c] *= alpha;
 #pragma unroll
                 for (int i = 0; i < 8; i++) {
                     acc[i][c] *= alpha;
@@ -620,8 +626,11 @@ struct ConsumerGqa {
         float pe[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) pe[i] = ex2_approx(s2[i] - m_run[i & 1]);
-        l_lane[0] += (pe[0] + pe[2]) + (pe[4] + pe[6]);
-        l_lane[1] += (pe[1] + pe[3]) + (pe[5] + pe[7]);
+        const float ps0 = (pe[0] + pe[2]) + (pe[4] + pe[6]), ps1 = (pe[1] + pe[3]) + (pe[5] + pe[7]);
+        l_lane[0] += ps0;
+        l_lane[1] += ps1;
+        x_lane[0] = fmaf(ps0, sv, x_lane[0]);
+        x_lane[1] = fmaf(ps1, sv, x_lane[1]);
         const uint64_t vv = pk2(sv, sv);
         const bool lo_part = t & 1;
 #pragma unroll
@@ -670,8 +679,8 @@ struct ConsumerGqa {
 #pragma unroll
                 for (int jj = 0; jj < 4; jj++) {
                     const bool odd = jj & 1;
-                    mma16816(acc[4 * R + jj], nib_pair(xab[jj >> 1], odd, mk), nib_pair(xab[2 + (jj >> 1)], odd, mk),
-                             nib_pair(xcd[jj >> 1], odd, mk), nib_pair(xcd[2 + (jj >> 1)], odd, mk), b0, b1);
+                    mma16816(acc[4 * R + jj], sub_pair(xab[jj >> 1], odd, mk), sub_pair(xab[2 + (jj >> 1)], odd, mk),
+                             sub_pair(xcd[jj >> 1], odd, mk), sub_pair(xcd[2 + (jj >> 1)], odd, mk), b0, b1);
                 }
             }
         }
@@ -684,14 +693,18 @@ struct ConsumerGqa {
     __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
     {
         const int g = lane >> 2, t = lane & 3;
-        float l[2];
+        float l[2], xs[2];
 #pragma unroll
         for (int c = 0; c < 2; c++) {
-            float v = l_lane[c];
+            float v = l_lane[c], x = x_lane[c];
             v += __shfl_xor_sync(kFull, v, 4);
             v += __shfl_xor_sync(kFull, v, 8);
             v += __shfl_xor_sync(kFull, v, 16);
+            x += __shfl_xor_sync(kFull, x, 4);
+            x += __shfl_xor_sync(kFull, x, 8);
+            x += __shfl_xor_sync(kFull, x, 16);
             l[c] = v;
+            xs[c] = x;
         }
 #pragma unroll
         for (int i = 0; i < 8; i++)
@@ -705,9 +718,11 @@ struct ConsumerGqa {
             for (int R = 0; R < 2; R++) {
                 float v[8];
 #pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    v[e] = acc[4 * R + e][c];
-                    v[4 + e] = acc[4 * R + e][2 + c];
+                for (int e = 0; e < 4; e++) {  // elements 64R + 8g + e, + 4: odd ones from bits 4..7
+                    const float f = (e & 1) ? kUnitOdd : kUnitEven;
+                    const float xb = -((e & 1) ? kOffOdd : kOffEven) * xs[c];
+                    v[e] = fmaf(acc[4 * R + e][c], f, xb);
+                    v[4 + e] = fmaf(acc[4 * R + e][2 + c], f, xb);
                 }
                 if (orow) {
                     const float inv = 1.0f / l[c];
@@ -924,7 +939,12 @@ struct ConsumerMq {
     float l_run[2];     // this lane's part of the row sums of 2^(s - m)
     float r_ref;        // log2 of the reference value scale
     int rows;           // valid rows of the tile
-    Magic mk;
+    // int4 only: codes are widened to fp16 subnormals (SubMagic); ob = P x
+    // 2^-21 = 2^-24 * 8 sum(x) of rows grp, grp + 8 (the offset's share of
+    // every output column), qbias = minus the offset share of their scores
+    float ob[4];
+    float qbias[2];
+    SubMagic mk;
 
     __device__ __forceinline__ void reset()
     {
@@ -932,6 +952,7 @@ struct ConsumerMq {
         m_run[0] = m_run[1] = -INFINITY;
         l_run[0] = l_run[1] = 0.0f;
         r_ref = -INFINITY;
+        ob[0] = ob[1] = ob[2] = ob[3] = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; i++)
 #pragma unroll
@@ -942,19 +963,32 @@ struct ConsumerMq {
     __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
     {
         const int g = lane >> 2, t = lane & 3;
+        const __half2 odd_scale = __float2half2_rn(kQOdd);
+        float se[2] = {0.0f, 0.0f}, so[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int m = 0; m < 4; m++) {
             const uint4 va = *reinterpret_cast<const uint4 *>(qs + g * kHeadDim + 32 * t + 8 * m);
             const uint4 vb = *reinterpret_cast<const uint4 *>(qs + (g + 8) * kHeadDim + 32 * t + 8 * m);
             if constexpr (kInt4) {
-                qa[2 * m][0] = __byte_perm(va.x, va.z, 0x5410);
-                qa[2 * m][1] = __byte_perm(vb.x, vb.z, 0x5410);
-                qa[2 * m][2] = __byte_perm(va.x, va.z, 0x7632);
-                qa[2 * m][3] = __byte_perm(vb.x, vb.z, 0x7632);
-                qa[2 * m + 1][0] = __byte_perm(va.y, va.w, 0x5410);
-                qa[2 * m + 1][1] = __byte_perm(vb.y, vb.w, 0x5410);
-                qa[2 * m + 1][2] = __byte_perm(va.y, va.w, 0x7632);
-                qa[2 * m + 1][3] = __byte_perm(vb.y, vb.w, 0x7632);
+                // k rows 2t + 8, 2t + 9 of each step meet the odd (bits 4..7) elements: q * kQOdd there
+                const uint32_t w[2][4] = {{__byte_perm(va.x, va.z, 0x5410), __byte_perm(va.x, va.z, 0x7632),
+                                           __byte_perm(va.y, va.w, 0x5410), __byte_perm(va.y, va.w, 0x7632)},
+                                          {__byte_perm(vb.x, vb.z, 0x5410), __byte_perm(vb.x, vb.z, 0x7632),
+                                           __byte_perm(vb.y, vb.w, 0x5410), __byte_perm(vb.y, vb.w, 0x7632)}};
+#pragma unroll
+                for (int r = 0; r < 2; r++) {
+                    const __half2 o1 = __hmul2(*reinterpret_cast<const __half2 *>(&w[r][1]), odd_scale);
+                    const __half2 o3 = __hmul2(*reinterpret_cast<const __half2 *>(&w[r][3]), odd_scale);
+                    qa[2 * m][r] = w[r][0];
+                    qa[2 * m][2 + r] = h2_bits(o1);
+                    qa[2 * m + 1][r] = w[r][2];
+                    qa[2 * m + 1][2 + r] = h2_bits(o3);
+                    const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(&w[r][0]));
+                    const float2 x2 = __half22float2(*reinterpret_cast<const __half2 *>(&w[r][2]));
+                    const float2 x1 = __half22float2(o1), x3 = __half22float2(o3);  // binary32 sums
+                    se[r] += (x0.x + x0.y) + (x2.x + x2.y);
+                    so[r] += (x1.x + x1.y) + (x3.x + x3.y);
+                }
             } else {
                 qa[2 * m][0] = va.x;
                 qa[2 * m][1] = vb.x;
@@ -966,9 +1000,19 @@ struct ConsumerMq {
                 qa[2 * m + 1][3] = vb.w;
             }
         }
+        if constexpr (kInt4) {
+#pragma unroll
+            for (int r = 0; r < 2; r++) {  // the four lanes t of a row hold its four slices
+                float qo = q_offset(se[r], so[r]);
+                qo += __shfl_xor_sync(kFull, qo, 1);
+                qo += __shfl_xor_sync(kFull, qo, 2);
+                qbias[r] = -qo;
+            }
+        }
     }
 
     // raw q . c of rows (grp, grp+8) x tokens 8j + 2t, 8j + 2t + 1: sc[4j + {0,1}] row grp, sc[4j + {2,3}] row grp+8
+    // (int4: 2^-24 (q . c + q_offset))
     __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[kScores]) const
     {
         const int g = lane >> 2, t = lane & 3;
@@ -980,10 +1024,11 @@ struct ConsumerMq {
                 const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int m = 0; m < 4; m++) {
-                    uint32_t b[4];
-                    widen_int4_u32(u[m], b, mk);
-                    mma16816(c, qa[2 * m][0], qa[2 * m][1], qa[2 * m][2], qa[2 * m][3], b[0], b[1]);
-                    mma16816(c, qa[2 * m + 1][0], qa[2 * m + 1][1], qa[2 * m + 1][2], qa[2 * m + 1][3], b[2], b[3]);
+                    const uint32_t h = u[m] >> 8;
+                    mma16816(c, qa[2 * m][0], qa[2 * m][1], qa[2 * m][2], qa[2 * m][3], sub_lo(u[m], mk),
+                             sub_hi(u[m], mk));
+                    mma16816(c, qa[2 * m + 1][0], qa[2 * m + 1][1], qa[2 * m + 1][2], qa[2 * m + 1][3], sub_lo(h, mk),
+                             sub_hi(h, mk));
                 }
             } else {
                 const uint4 w0 = *reinterpret_cast<const uint4 *>(ks + (8 * j + g) * 128 + 32 * t);
@@ -1015,16 +1060,21 @@ struct ConsumerMq {
             for (int i = 0; i < 16; i++)
 #pragma unroll
                 for (int j = 0; j < 4; j++) o[i][j] *= beta;
+            if constexpr (kInt4)
+#pragma unroll
+                for (int j = 0; j < 4; j++) ob[j] *= beta;
             r_ref = lsv;
         }
         const float ratio = ex2_approx(lsv - r_ref);
         float s[kScores];
+        const float f1 = kInt4 ? fac * kUnitEven : fac;
+        const float fb0 = kInt4 ? qbias[0] * fac : 0.0f, fb1 = kInt4 ? qbias[1] * fac : 0.0f;
 #pragma unroll
         for (int j = 0; j < kNT; j++)
 #pragma unroll
             for (int e = 0; e < 4; e++) {
                 const int tok = 8 * j + 2 * t + (e & 1);
-                s[4 * j + e] = tok < ntok ? sc[4 * j + e] * fac : -INFINITY;
+                s[4 * j + e] = tok < ntok ? fmaf(sc[4 * j + e], f1, (e & 2) ? fb1 : fb0) : -INFINITY;
             }
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -1048,6 +1098,12 @@ struct ConsumerMq {
                 o[i][1] *= a0;
                 o[i][2] *= a1;
                 o[i][3] *= a1;
+            }
+            if constexpr (kInt4) {
+                ob[0] *= a0;
+                ob[1] *= a0;
+                ob[2] *= a1;
+                ob[3] *= a1;
             }
         }
         float e[kScores];
@@ -1074,6 +1130,8 @@ struct ConsumerMq {
         if constexpr (kInt4) {
 #pragma unroll
             for (int k = 0; k < 2; k++) {
+                // the offset: every column of B = 8 * 2^-24 (the fp16 subnormal 0x0008)
+                mma16816(ob, pf[4 * k], pf[4 * k + 1], pf[4 * k + 2], pf[4 * k + 3], 0x00080008u, 0x00080008u);
 #pragma unroll
                 for (int R = 0; R < 2; R++) {
                     // word g + 8R (elements 64R + 8g .. +7) of tokens 16k + 2t, +1, +8, +9
@@ -1093,7 +1151,7 @@ struct ConsumerMq {
 #pragma unroll
                     for (int e = 0; e < 8; e++)
                         mma16816(o[8 * R + e], pf[4 * k], pf[4 * k + 1], pf[4 * k + 2], pf[4 * k + 3],
-                                 nib_pair(xab[e >> 1], e & 1, mk), nib_pair(xcd[e >> 1], e & 1, mk));
+                                 sub_pair(xab[e >> 1], e & 1, mk), sub_pair(xcd[e >> 1], e & 1, mk));
                 }
             }
         } else {
@@ -1145,13 +1203,17 @@ struct ConsumerMq {
             if (row >= rows) continue;
             const float mul = orow ? ref / l[r] : ref;
             if constexpr (kInt4) {
+                // raw sums over the widened codes, less the offset share (2^24 ob = 8 sum(x))
+                const float xs = kUnitEven / kOffEven * ob[2 * r];
+                const float xb_even = -kOffEven * xs, xb_odd = -kOffOdd * xs;
 #pragma unroll
                 for (int R = 0; R < 2; R++) {
                     float v[16];
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
-                        v[e] = o[8 * R + e][2 * r] * mul;          // element 64R + 16t + e
-                        v[8 + e] = o[8 * R + e][2 * r + 1] * mul;  // element 64R + 16t + 8 + e
+                        const float f = (e & 1) ? kUnitOdd : kUnitEven, xb = (e & 1) ? xb_odd : xb_even;
+                        v[e] = fmaf(o[8 * R + e][2 * r], f, xb) * mul;          // element 64R + 16t + e
+                        v[8 + e] = fmaf(o[8 * R + e][2 * r + 1], f, xb) * mul;  // element 64R + 16t + 8 + e
                     }
                     if (orow) {
                         uint4 *d = reinterpret_cast<uint4 *>(orow + row * kHeadDim + 64 * R + 16 * t);

@@ -174,3 +174,25 @@ def test_grouped_heads_argument_checks(cuda_ok):
     w8 = kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT8_PAGE, 8, 64)
     assert w8 > 0 and w8 == kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT8_PAGE, 1, 32)
     assert kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT4_B64, 1, 2048) == 0
+
+
+OFFSET_CASES = [("int4", 1), ("int4", 2), ("int4", 4), ("int4", 8), ("int4", 32), ("int8", 1), ("fp8", 1), ("fp8", 8)]
+
+
+@pytest.mark.parametrize("fmt,g", OFFSET_CASES)
+@pytest.mark.parametrize("qmean", [4.0, 12.0])
+def test_query_with_a_large_common_offset(cuda_ok, fmt, g, qmean):
+    """q ~ N(qmean, 1) on every element, over heads with outlier channels, so
+    that the K scales of a head's pages differ and its softmax is peaked.  The
+    int4 kernels take a share of every score that depends on q alone out after
+    the contraction, scaled by each page's K scale: an error in that share does
+    not cancel across pages, and this case makes it show."""
+    lens = [1, 33, 64, 700, 3000, 8192, 20000, 5]
+    wl = W.Workload(len(lens), 4, D, lens, FMTS[fmt], 1.0, ("per_head", 4, 10.0), "permuted", seed=8)
+    dw = DeviceWorkload(wl)
+    dw.prefill()
+    rng = np.random.default_rng(80 + g)
+    q = (rng.standard_normal((wl.B, 4 * g, D)) + qmean).astype(np.float16).view(np.uint16)
+    got = _run(dw, q, g)
+    _check(wl, wl.lens, q, got, g)
+    assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
