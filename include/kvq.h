@@ -143,7 +143,13 @@ kvq_status kvq_quantize(kvq_format fmt, const uint16_t *x, int64_t num_tokens, i
  *                    beyond them is skipped and flagged)
  *   max_new_tokens   host bound on cu_seqlens[b+1] - cu_seqlens[b] (sizes the grid)
  * Device-detected problems set KVQ_FLAG_* bits in cache->status and skip the
- * affected blocks.  Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA.
+ * affected blocks.
+ * Launch: an append of at most 64 tokens per sequence uses programmatic
+ * dependent launch and reads cu_seqlens, seq_lens_before and block_table
+ * before waiting for the previous kernel of the stream (the scales, codes,
+ * tail and new rows only after); the same condition as for
+ * kvq_decode_attention's seq_lens and block_table holds for these three.
+ * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA.
  */
 kvq_status kvq_append(const kvq_cache *cache, const uint16_t *k_new, const uint16_t *v_new,
                       const int32_t *cu_seqlens, const int32_t *block_table, int32_t max_blocks_per_seq,

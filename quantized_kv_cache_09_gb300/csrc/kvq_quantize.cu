@@ -402,7 +402,10 @@ __global__ void __launch_bounds__(kShortWarps * 32)
     using C = Codec<FMT>;
     __shared__ uint32_t s_max[kShortWarps];
     pdl_launch_dependents();
-    pdl_wait();
+    // Until pdl_wait below, the previous kernel of the stream may still be
+    // running: only cu_seqlens, seq_lens_before and the block table are read
+    // before it (no kernel of this library writes them); the scales, codes,
+    // tail and new rows are touched after it.
     const int b = blockIdx.y;
     const bool is_v = blockIdx.z != 0;
     const int H = p.num_heads;
@@ -429,6 +432,8 @@ __global__ void __launch_bounds__(kShortWarps * 32)
     const int h = blockIdx.x % H;
     if (jrel > j1 - j0) return;
     const int j = j0 + jrel;
+    const int page = p.block_table[(int64_t)b * p.max_blocks + j];
+    pdl_wait();  // from here on, the previous kernel's writes are visible
     const int64_t HD = (int64_t)H * kHeadDim;
     const uint16_t *fresh = (is_v ? p.v_new : p.k_new) + (int64_t)h * kHeadDim;
     uint16_t *tail = is_v ? p.v_tail : p.k_tail;
@@ -438,7 +443,6 @@ __global__ void __launch_bounds__(kShortWarps * 32)
         if (tid == 0) set_flag(p.status, KVQ_FLAG_NO_TAIL);
         return;
     }
-    const int page = p.block_table[(int64_t)b * p.max_blocks + j];
     const bool page_ok = page >= 0 && page < p.num_pages;
     if (!page_ok && tid == 0) set_flag(p.status, KVQ_FLAG_BAD_PAGE);
     const int64_t pg = page_ok ? page : 0;
