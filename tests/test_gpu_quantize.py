@@ -165,20 +165,22 @@ def test_append_chunkings_equal_full_history(cuda_ok, fmt):
             assert np.array_equal(got, want)
 
 
-def test_append_reports_device_problems(cuda_ok):
+@pytest.mark.parametrize("n", [10, 100])
+def test_append_reports_device_problems(cuda_ok, n):
     """A block-table entry out of range, a length beyond the table, an open
-    block without a tail buffer: flagged in the status word, nothing faults."""
+    block without a tail buffer: flagged in the status word, nothing faults.
+    n = 10 takes the short-append kernel, n = 100 the persistent one."""
     fmt = kvq.KVQ_INT4_B64
     cache = kvq.PagedKVCache(fmt, 4, 2, max_seqs=0, with_tail=False)
-    k = torch.zeros((10, 2, D), dtype=torch.float16, device="cuda")
-    cu = torch.tensor([0, 10], dtype=torch.int32, device="cuda")
+    k = torch.zeros((n, 2, D), dtype=torch.float16, device="cuda")
+    cu = torch.tensor([0, n], dtype=torch.int32, device="cuda")
     bt = torch.tensor([[7, 1]], dtype=torch.int32, device="cuda")
-    kvq.kvq_append(cache, k, k, cu, bt, torch.tensor([0], dtype=torch.int32, device="cuda"), 10)
+    kvq.kvq_append(cache, k, k, cu, bt, torch.tensor([0], dtype=torch.int32, device="cuda"), n)
     assert kvq.kvq_get_device_status(cache)[0] == 4
-    kvq.kvq_append(cache, k, k, cu, bt, torch.tensor([120], dtype=torch.int32, device="cuda"), 10)
+    kvq.kvq_append(cache, k, k, cu, bt, torch.tensor([120], dtype=torch.int32, device="cuda"), n)
     assert kvq.kvq_get_device_status(cache)[0] == 7
     bt2 = torch.tensor([[0, 1]], dtype=torch.int32, device="cuda")
-    kvq.kvq_append(cache, k, k, cu, bt2, torch.tensor([5], dtype=torch.int32, device="cuda"), 10)
+    kvq.kvq_append(cache, k, k, cu, bt2, torch.tensor([5], dtype=torch.int32, device="cuda"), n)
     rc, flags = kvq.kvq_get_device_status(cache)
     assert flags & kvq.KVQ_FLAG_NO_TAIL
     assert kvq.kvq_get_device_status(cache) == (0, 0)   # the word was cleared
