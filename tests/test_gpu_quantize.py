@@ -57,6 +57,35 @@ def test_exact_rounding_ties_bit_exact(cuda_ok, fmt):
     _assert_same(fmt, x.astype(np.float16).view(np.uint16))
 
 
+@pytest.mark.parametrize("fmt", FMTS[:2])
+def test_values_nearest_the_ties_of_random_scales_bit_exact(cuda_ok, fmt):
+    """Whole blocks take the quantizer's unchecked fast path when no binary16
+    value can lie within its error window of a half-integer quotient t.  Each
+    block here holds +-a and, for every half-integer t below the largest code,
+    the binary16 value nearest t * scale and its two neighbours, both signs,
+    for 4096 random scales: the values the block test must find, wherever the
+    scale puts them."""
+    rng = np.random.default_rng(23 + fmt)
+    n = 4096
+    div = np.float32(7.5 if fmt == kvq.KVQ_INT4_B64 else 127.0)
+    ts = np.arange(7 if fmt == kvq.KVQ_INT4_B64 else 127, dtype=np.float32) + np.float32(0.5)
+    a = np.exp(rng.uniform(np.log(1e-3), np.log(6e4), n)).astype(np.float16)
+    a = a[np.isfinite(a) & (a > 0)]
+    x = np.zeros((64 * a.size, 1, D), dtype=np.float16)
+    for i, ai in enumerate(a):
+        s = np.float32(ai) / div
+        v = (ts * s).astype(np.float16)
+        cand = np.concatenate([v, np.nextafter(v, np.float16(np.inf)), np.nextafter(v, np.float16(0))])
+        cand = cand[np.abs(cand.astype(np.float32)) <= np.float32(ai)]
+        vals = np.concatenate([[ai, -ai], cand, -cand])
+        blk = x[64 * i:64 * i + 64, 0, :].reshape(-1)
+        blk[:vals.size] = vals
+        fill = np.clip(rng.standard_normal(blk.size - vals.size) * 0.3, -0.9, 0.9) * np.float32(ai)
+        blk[vals.size:] = fill.astype(np.float16)
+        x[64 * i:64 * i + 64, 0, :] = blk.reshape(64, D)
+    _assert_same(fmt, x.view(np.uint16))
+
+
 def test_fp8_grid_midpoints_and_signed_zeros_bit_exact(cuda_ok):
     """Blocks with max|x| = 448 (scale 1) whose elements are E4M3 values, the
     midpoints between neighbours (ties to even), one binary16 step either side
