@@ -113,12 +113,7 @@ constexpr size_t dec_smem_bytes()
     return S::kWarps * sizeof(WarpSmem<F::kStages, F::kUnitsPerStage * kUnitBytes, S::kQRows>) + kSeqSmemBytes;
 }
 
-// ---------------------------------------------------------------------------
-// exact widening of packed codes to fp16 pairs (magic-number bias)
-//   int4, low nibble n of a 16-bit half: (1024 + (n ^ 8)) - 1032 = c;
-//   int4, bits 4..7 of a half: (1024 + 16 (n ^ 8)) / 16 - 72 = c.
-// ---------------------------------------------------------------------------
-// the byte formats' widening, by format
+// the byte formats' exact widening to fp16 pairs, by format (int4: SubMagic below)
 template <int FMT>
 __device__ __forceinline__ void widen_bytes(uint32_t w, __half2 c[2])
 {
