@@ -4,10 +4,10 @@
 //
 // Decode is a GEMV per (sequence, head): every cached byte is read once and
 // used for a handful of flops, so the kernel is built around HBM streaming.
-// The int4 path widens codes exactly to fp16 subnormals in registers (one
-// lop3 per pair, the offset taken out after the contraction) and feeds the
-// legacy tensor-core mma (m16n8k16) because the widening, not the multiply,
-// is the cost; the int8 path stays on CUDA-core FMAs.
+// Codes are widened exactly to fp16 in registers -- int4 to fp16 subnormals
+// (one lop3 per pair, the offset taken out after the contraction), int8 and
+// FP8 E4M3 to fp16 pairs -- and both contractions run on the legacy
+// tensor-core mma (m16n8k16): the widening, not the multiply, is the cost.
 //
 // Work decomposition (persistent, split-K over the sequence):
 //   unit   = 32 tokens (int4) or 16 tokens (int8) of one (sequence, head):
@@ -121,33 +121,6 @@ __device__ __forceinline__ void widen_bytes(uint32_t w, __half2 c[2])
         widen_e4m3(w, c);
     else
         widen_int8(w, c);
-}
-
-template <int FMT>
-__device__ __forceinline__ float dot4_bytes(uint32_t w, const float *q, float acc)
-{
-    __half2 c[2];
-    widen_bytes<FMT>(w, c);
-    const float2 f0 = __half22float2(c[0]);
-    const float2 f1 = __half22float2(c[1]);
-    acc = fmaf(q[0], f0.x, acc);
-    acc = fmaf(q[1], f0.y, acc);
-    acc = fmaf(q[2], f1.x, acc);
-    acc = fmaf(q[3], f1.y, acc);
-    return acc;
-}
-
-template <int FMT>
-__device__ __forceinline__ void axpy4_bytes(uint32_t w, float p, float *acc)
-{
-    __half2 c[2];
-    widen_bytes<FMT>(w, c);
-    const float2 f0 = __half22float2(c[0]);
-    const float2 f1 = __half22float2(c[1]);
-    acc[0] = fmaf(p, f0.x, acc[0]);
-    acc[1] = fmaf(p, f0.y, acc[1]);
-    acc[2] = fmaf(p, f1.x, acc[2]);
-    acc[3] = fmaf(p, f1.y, acc[3]);
 }
 
 __device__ __forceinline__ float warp_max(float v)
@@ -740,143 +713,192 @@ struct ConsumerGqa {
         }
     }
 };
-// int8 and FP8 E4M3 (one byte per element): CUDA-core path on codes widened
-// exactly to fp16, then fp32 FMAs.  K: lane = (token group g = lane >> 3,
-// 16-element chunk r = lane & 7), 4 passes of 4 tokens, reduce-scatter over the
-// 8 lanes of a token; V: lane = (16-element chunk, token subset), weights
-// shuffled from the lanes that scored them.
+// int8 and FP8 E4M3 (one byte per element), one query head per cache head:
+// both contractions of a 16-token unit on the tensor cores (mma.sync m16n8k16),
+// the codes widened exactly to fp16 pairs (FP8: one cvt.rn.f16x2.e4m3x2 per
+// pair; int8: the 1024 + (byte ^ 0x80) - 1152 bias, a prmt and an hsub2 per
+// pair), fp32 accumulation.
+//   QK: A = 16 tokens x 16 elements; lane (g, t) feeds rows g, g + 8 from its
+//       32-byte slice (elements 32t .. 32t+31) of each token row: k-step m
+//       takes elements 32t + 4m + {0,1} as k rows 2t, 2t+1 and + {2,3} as
+//       2t+8, 2t+9, a fixed permutation of the head dimension that q's
+//       fragment repeats; q fills every column of B, so every lane receives
+//       the scores of its tokens g, g + 8.
+//   PV: A = V^T with the rows of m-tile R taken as elements 16 (row mod 8) +
+//       2R + row / 8, so lane (g, t) reads elements 16g .. 16g+15 of its
+//       tokens 2t, 2t+1, 2t+8, 2t+9 as one 16-byte load each; one prmt pairs
+//       two tokens' bytes of elements 2R and 2R+1 at once.  B column 0 =
+//       RN16(p), column 1 = the remainder (~22 bits), as for int4.
 template <int FMT>
-struct ConsumerBytes {
-    static constexpr int kScores = 4;
-    static constexpr int kPf = 4;
+struct ConsumerMma8 {
+    static constexpr int kScores = 2;
+    static constexpr int kPf = 1;
     int rows;  // (unused: one query row)
-    float qf[16];
-    float acc[16];
+    uint32_t qb[8][2];
+    float acc[8][4];
     float m_run;
-    float l_lane;
+    uint64_t l2;  // running sum of the weights of this lane's two tokens, as a pair
 
     __device__ __forceinline__ void reset()
     {
         m_run = -INFINITY;
-        l_lane = 0.0f;
+        l2 = pk2(0.0f, 0.0f);
 #pragma unroll
-        for (int i = 0; i < 16; i++) acc[i] = 0.0f;
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) acc[i][j] = 0.0f;
     }
 
     __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
     {
-        const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + (lane & 7) * 16);
+        const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + 32 * (lane & 3));
 #pragma unroll
-        for (int i = 0; i < 2; i++) {
-            const uint4 v = q4[i];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
-                qf[8 * i + 2 * k] = f.x;
-                qf[8 * i + 2 * k + 1] = f.y;
-            }
+        for (int u = 0; u < 4; u++) {
+            const uint4 v = q4[u];  // elements 32t + 8u .. +7 as pairs
+            qb[2 * u][0] = v.x;
+            qb[2 * u][1] = v.y;
+            qb[2 * u + 1][0] = v.z;
+            qb[2 * u + 1][1] = v.w;
         }
     }
 
-    // sc[0]: the raw dot product of this lane's token (lanes l and l ^ 4 share one)
-    __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[4]) const
+    // two exact fp16 pairs of the bytes of w: {b0, b1}, {b2, b3}
+    __device__ __forceinline__ static void widen2(uint32_t w, uint32_t &lo, uint32_t &hi)
     {
-        constexpr int RB = 128;
-        const int g = lane >> 3, r = lane & 7;
-        float P[4];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(ks + (4 * k + g) * RB + r * 16);
-            float a = 0.0f;
-            a = dot4_bytes<FMT>(w.x, qf + 0, a);
-            a = dot4_bytes<FMT>(w.y, qf + 4, a);
-            a = dot4_bytes<FMT>(w.z, qf + 8, a);
-            a = dot4_bytes<FMT>(w.w, qf + 12, a);
-            P[k] = a;
+        if constexpr (FMT == KVQ_FP8_E4M3) {
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(static_cast<unsigned short>(w & 0xffffu)));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(static_cast<unsigned short>(w >> 16)));
+        } else {
+            const uint32_t x = w ^ 0x80808080u;
+            const __half2 k1152 = __float2half2_rn(1152.0f);
+            const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140), b = __byte_perm(x, 0x64646464u, 0x4342);
+            lo = h2_bits(__hsub2(*reinterpret_cast<const __half2 *>(&a), k1152));
+            hi = h2_bits(__hsub2(*reinterpret_cast<const __half2 *>(&b), k1152));
         }
-        const bool o1 = r & 1;
-        float k0 = o1 ? P[2] : P[0], k1 = o1 ? P[3] : P[1];
-        const float s0 = o1 ? P[0] : P[2], s1 = o1 ? P[1] : P[3];
-        k0 += __shfl_xor_sync(kFull, s0, 1);
-        k1 += __shfl_xor_sync(kFull, s1, 1);
-        const bool o2 = r & 2;
-        const float x = (o2 ? k1 : k0) + __shfl_xor_sync(kFull, o2 ? k0 : k1, 2);
-        sc[0] = x + __shfl_xor_sync(kFull, x, 4);
     }
 
-    __device__ __forceinline__ void softmax(const float sc[4], int ntok, float fac, float sv, int lane,
-                                            uint32_t pf[4])
+    // raw dot products q . c of tokens g, g + 8
+    __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[2]) const
     {
-        const int g = lane >> 3, r = lane & 7;
-        const int tok = 4 * (2 * (r & 1) + ((r >> 1) & 1)) + g;
-        const float s2 = (tok < ntok) ? sc[0] * fac : -INFINITY;
-        if (__any_sync(kFull, s2 > m_run)) {
-            const float mu = warp_max(s2);
+        const int g = lane >> 2, t = lane & 3;
+        float c[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; m++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) c[m][e] = 0.0f;
+        const uint4 *ra = reinterpret_cast<const uint4 *>(ks + g * 128 + 32 * t);
+        const uint4 *rb = reinterpret_cast<const uint4 *>(ks + (g + 8) * 128 + 32 * t);
+        const uint4 a0 = ra[0], a1 = ra[1], b0 = rb[0], b1 = rb[1];
+        const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int m = 0; m < 8; m++) {
+            uint32_t al, ah, bl, bh;
+            widen2(wa[m], al, ah);
+            widen2(wb[m], bl, bh);
+            mma16816(c[m & 3], al, bl, ah, bh, qb[m][0], qb[m][1]);
+        }
+        sc[0] = (c[0][0] + c[1][0]) + (c[2][0] + c[3][0]);
+        sc[1] = (c[0][2] + c[1][2]) + (c[2][2] + c[3][2]);
+    }
+
+    // online softmax of the unit's scores; px = the fp16 pair {x(g), x(g + 8)} of
+    // x = p * sv: the rounded values in lanes t == 0, the remainders elsewhere
+    __device__ __forceinline__ void softmax(const float sc[2], int ntok, float fac, float sv, int lane,
+                                            uint32_t px[1])
+    {
+        const int g = lane >> 2, t = lane & 3;
+        float s0, s1;
+        upk2(mul2(pk2(sc[0], sc[1]), pk2(fac, fac)), s0, s1);
+        if (g >= ntok) s0 = -INFINITY;
+        if (g + 8 >= ntok) s1 = -INFINITY;
+        const float lm = fmaxf(s0, s1);
+        if (__any_sync(kFull, lm > m_run)) {
+            const float mu = warp_max(lm);
             const float alpha = ex2_approx(m_run - mu);
-            l_lane *= alpha;
+            l2 = mul2(l2, pk2(alpha, alpha));
 #pragma unroll
-            for (int i = 0; i < 16; i++) acc[i] *= alpha;
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+                for (int j = 0; j < 4; j++) acc[i][j] *= alpha;
             m_run = mu;
         }
-        const float pe = ex2_approx(s2 - m_run);
-        l_lane += (lane & 4) ? 0.0f : pe;  // each token is held by two lanes
-        pf[0] = __float_as_uint(pe * sv);
+        const uint64_t p01 = pk2(ex2_approx(s0 - m_run), ex2_approx(s1 - m_run));
+        l2 = add2(l2, p01);
+        uint32_t hi, lo;
+        hi_lo_pairs(mul2(p01, pk2(sv, sv)), hi, lo);
+        px[0] = t == 0 ? hi : lo;
     }
 
-    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t pf[4], int lane)
+    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t px[1], int lane)
     {
-        constexpr int RB = 128;
-        const float pv = __uint_as_float(pf[0]);
-        const int vc = lane & 7, ts = lane >> 3;
+        const int g = lane >> 2, t = lane & 3;
+        // column g of B: lanes g == 0 read the rounded weights (from a t == 0 lane), g == 1 the
+        // remainders; tokens 2t, 2t + 8 come from lane (2t, .), 2t + 1, 2t + 9 from lane (2t + 1, .)
+        const int src = 8 * t + (g & 3);
+        const uint32_t ua = __shfl_sync(kFull, px[0], src);
+        const uint32_t ub = __shfl_sync(kFull, px[0], src + 4);
+        const uint32_t b0 = __byte_perm(ua, ub, 0x5410);  // tokens 2t, 2t + 1
+        const uint32_t b1 = __byte_perm(ua, ub, 0x7632);  // tokens 2t + 8, 2t + 9
+        const uint4 v0 = *reinterpret_cast<const uint4 *>(vs + (2 * t) * 128 + 16 * g);
+        const uint4 v1 = *reinterpret_cast<const uint4 *>(vs + (2 * t + 1) * 128 + 16 * g);
+        const uint4 v8 = *reinterpret_cast<const uint4 *>(vs + (2 * t + 8) * 128 + 16 * g);
+        const uint4 v9 = *reinterpret_cast<const uint4 *>(vs + (2 * t + 9) * 128 + 16 * g);
+        const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+        const uint32_t w8[4] = {v8.x, v8.y, v8.z, v8.w}, w9[4] = {v9.x, v9.y, v9.z, v9.w};
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int tv = 4 * j + ts;
-            const int src = ts * 8 + ((j & 1) << 1) + (j >> 1);
-            const float pt = __shfl_sync(kFull, pv, src);
-            const uint4 w = *reinterpret_cast<const uint4 *>(vs + tv * RB + vc * 16);
-            axpy4_bytes<FMT>(w.x, pt, acc);
-            axpy4_bytes<FMT>(w.y, pt, acc + 4);
-            axpy4_bytes<FMT>(w.z, pt, acc + 8);
-            axpy4_bytes<FMT>(w.w, pt, acc + 12);
+        for (int R = 0; R < 8; R++) {
+            // bytes 2R, 2R + 1 (elements 16g + 2R, + 1) of two tokens: [x.2R, y.2R, x.2R+1, y.2R+1]
+            const uint32_t sel = (R & 1) ? 0x7362u : 0x5140u;
+            const uint32_t p01 = __byte_perm(w0[R >> 1], w1[R >> 1], sel);
+            const uint32_t p89 = __byte_perm(w8[R >> 1], w9[R >> 1], sel);
+            uint32_t a0, a1, a2, a3;  // (element 2R: tokens 2t, 2t+1), (2R+1: same), (2R: 2t+8, 2t+9), (2R+1)
+            widen2(p01, a0, a1);
+            widen2(p89, a2, a3);
+            mma16816(acc[R], a0, a1, a2, a3, b0, b1);
         }
     }
 
+    // out row (final) or partial slot: lanes with t == 0 hold elements 16g .. 16g + 15
+    // (tile R: row g = element 16g + 2R, row g + 8 = 16g + 2R + 1)
     __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
     {
+        float la, lb;
+        upk2(l2, la, lb);
+        const float l = warp_sum(la + lb) * 0.25f;  // the four lanes of a row group hold the same weights
+        const int g = lane >> 2, t = lane & 3;
+        if (t != 0) return;
+        float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            acc[i] += __shfl_xor_sync(kFull, acc[i], 8);
-            acc[i] += __shfl_xor_sync(kFull, acc[i], 16);
+        for (int R = 0; R < 8; R++) {
+            v[2 * R] = acc[R][0] + acc[R][1];
+            v[2 * R + 1] = acc[R][2] + acc[R][3];
         }
-        const float l = warp_sum(l_lane);
-        const int vc = lane & 7;
-        if (lane >= 8) return;
         if (orow) {
             const float inv = 1.0f / l;
             uint32_t hw[8];
 #pragma unroll
-            for (int i = 0; i < 8; i++) hw[i] = h2_bits(__floats2half2_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv));
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + vc * 16);
+            for (int i = 0; i < 8; i++) hw[i] = h2_bits(__floats2half2_rn(v[2 * i] * inv, v[2 * i + 1] * inv));
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + 16 * g);
             dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
         } else {
+            float4 *d4 = reinterpret_cast<float4 *>(part + 4 + 16 * g);
+#pragma unroll
+            for (int i = 0; i < 4; i++) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
             if (lane == 0) {
                 part[0] = m_run;
                 part[1] = l;
             }
-            float4 *d4 = reinterpret_cast<float4 *>(part + 4 + vc * 16);
-#pragma unroll
-            for (int i = 0; i < 4; i++) d4[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
         }
     }
 };
 
 template <>
-struct Consumer<KVQ_INT8_PAGE> : ConsumerBytes<KVQ_INT8_PAGE> {
+struct Consumer<KVQ_INT8_PAGE> : ConsumerMma8<KVQ_INT8_PAGE> {
 };
 template <>
-struct Consumer<KVQ_FP8_E4M3> : ConsumerBytes<KVQ_FP8_E4M3> {
+struct Consumer<KVQ_FP8_E4M3> : ConsumerMma8<KVQ_FP8_E4M3> {
 };
 
 // ---------------------------------------------------------------------------
