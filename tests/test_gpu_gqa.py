@@ -58,10 +58,10 @@ def _check(wl, lens, q_bits, got, g, oc=None):
 
 FMTS = {"int4": kvq.KVQ_INT4_B64, "int8": kvq.KVQ_INT8_PAGE, "fp8": kvq.KVQ_FP8_E4M3}
 # (format, g): g = 2, 4 on int4 use the spare-column kernel; every other pair
-# the 16-query-head tile kernel (g = 3: one partial tile, 24: a full and a half
-# tile, 32: two tiles)
-GROUPS = [("int4", 2), ("int4", 4), ("int4", 3), ("int4", 8), ("int4", 16), ("int4", 32),
-          ("int8", 2), ("int8", 8), ("int8", 24), ("int8", 32),
+# the 16-query-head tile kernel (g = 3: one partial tile, 20 and 24: a full and
+# a partial tile, 32: two tiles, 48: three)
+GROUPS = [("int4", 2), ("int4", 4), ("int4", 3), ("int4", 8), ("int4", 16), ("int4", 20), ("int4", 32),
+          ("int4", 48), ("int8", 2), ("int8", 8), ("int8", 24), ("int8", 32),
           ("fp8", 4), ("fp8", 8), ("fp8", 16), ("fp8", 32)]
 
 
@@ -97,7 +97,7 @@ def test_multi_query_one_cache_head(cuda_ok, fmt, g):
     assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
 
 
-@pytest.mark.parametrize("fmt,g", [("int4", 2), ("int4", 4), ("int4", 8), ("int8", 32), ("fp8", 16)])
+@pytest.mark.parametrize("fmt,g", [("int4", 2), ("int4", 4), ("int4", 8), ("int4", 32), ("int8", 32), ("fp8", 16)])
 def test_grouped_heads_one_long_sequence_many_pieces(cuda_ok, fmt, g):
     """One cache head long enough to be cut into about a thousand split pieces:
     the merge combines them all (several rounds of 32 lanes); the workspace is
