@@ -127,6 +127,41 @@ def test_batch_context_does_not_change_results(cuda_ok, fmt):
     _check_decode(wl, wl.lens, q_np, out_all)
 
 
+@pytest.mark.parametrize("fmt", [kvq.KVQ_INT4_B64, kvq.KVQ_INT8_PAGE, kvq.KVQ_FP8_E4M3])
+def test_more_sequences_than_one_launch(cuda_ok, fmt):
+    """700 sequences: the entry point runs them as launches of at most 512
+    (each with its own slice of q, out, lengths and block table).  Ragged
+    lengths with empty sequences on both sides of the launch boundary; every
+    (sequence, query head) against the oracle for multi-head attention and for
+    groups of 4 (int4: the spare-column kernel) and 32 (the 16-head tiles and
+    their merge launch)."""
+    rng = np.random.default_rng(77)
+    lens = rng.integers(1, 260, size=700).astype(np.int64)
+    lens[[0, 300, 511, 512, 699]] = 0
+    wl = W.Workload(len(lens), 2, D, lens.tolist(), fmt, 1.0, None, "permuted", seed=78)
+    dw = DeviceWorkload(wl)
+    dw.prefill()
+    oc = _oracle_cache(wl, wl.lens)
+    q_np, out = _run_decode(dw)
+    _check_decode(wl, wl.lens, q_np, out, oc)
+    got = out.float().cpu().numpy()
+    assert np.all(got[[0, 300, 511, 512, 699]] == 0)
+    kc, vc, ks, vs = oc
+    sm = np.float32(1.0 / math.sqrt(D))
+    for g in (4, 32):
+        qg = (rng.standard_normal((wl.B, wl.H * g, D))).astype(np.float16).view(np.uint16)
+        q = torch.from_numpy(qg.view(np.float16)).cuda()
+        og = torch.full_like(q, float("nan"))
+        kvq.kvq_decode_attention_gqa(dw.cache, q, dw.block_table, dw.lens, dw.softmax_scale, og,
+                                     dw.cache.workspace(wl.H * g))
+        torch.cuda.synchronize()
+        ref = orc.decode_attention(wl.fmt, kc, vc, ks, vs, wl.block_table, wl.lens, qg, sm)
+        vmax = np.repeat(orc.value_absmax(wl.fmt, vc, vs, wl.block_table, wl.lens, wl.H, D), g, axis=1)
+        err = orc.normalized_error(og.float().cpu().numpy().astype(np.float64), ref, vmax)
+        assert err <= TOL, f"g={g}: normalised error {err:.3e} > {TOL}"
+    assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
+
+
 def test_special_queries(cuda_ok):
     """q = 0 gives the mean of the values; one sequence of one token returns
     that token's value row."""
