@@ -3,8 +3,14 @@
 Argument marshalling only -- torch tensors in, raw device pointers, sizes and
 the current CUDA stream out; every step of the work runs in the CUDA kernels.
 There is no fallback: if the library is missing the first call raises.
+
+With KVQ_NVTX set (to anything but 0) when this module is imported, every
+entry point that launches work is wrapped in an NVTX range named after its C
+function, for profilers that filter by range (ncu --nvtx --nvtx-include ...);
+unset, the wrappers are the plain functions.
 """
 import ctypes
+import functools
 import os
 
 import torch
@@ -38,6 +44,28 @@ EXPORTS = ("kvq_quantize", "kvq_append", "kvq_decode_workspace_bytes", "kvq_deco
 # every symbol include/kvq_testing.h declares (test hooks)
 TESTING_EXPORTS = ("kvq_testing_set_decode_fault",)
 NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+NVTX = os.environ.get("KVQ_NVTX", "") not in ("", "0")
+
+
+def _nvtx(fn=None, *, name=None):
+    """The entry point inside an NVTX range named after its C function (only with KVQ_NVTX set)."""
+    if fn is None:
+        return lambda f: _nvtx(f, name=name)
+    if not NVTX:
+        return fn
+    label = name or fn.__name__
+
+    @functools.wraps(fn)
+    def ranged(*args, **kwargs):
+        torch.cuda.nvtx.range_push(label)
+        try:
+            return fn(*args, **kwargs)
+        finally:
+            torch.cuda.nvtx.range_pop()
+
+    return ranged
 
 
 class KvqError(RuntimeError):
@@ -158,6 +186,7 @@ def kvq_testing_set_decode_fault(wait_limit_us=0, skip_chunk=-1):
     _check(lib().kvq_testing_set_decode_fault(int(wait_limit_us), int(skip_chunk)), "kvq_testing_set_decode_fault")
 
 
+@_nvtx
 def kvq_quantize(fmt, x, codes, scales, stream=None):
     """x fp16 [T][H][128] -> codes uint8 [ceil(T/64)][H][64][64 or 128], scales fp32 [ceil(T/64)][H]."""
     _cuda(x, torch.float16, "x")
@@ -172,6 +201,7 @@ def kvq_quantize(fmt, x, codes, scales, stream=None):
            "kvq_quantize")
 
 
+@_nvtx
 def kvq_append(cache, k_new, v_new, cu_seqlens, block_table, seq_lens_before, max_new_tokens, stream=None):
     """Append the rows of k_new/v_new fp16 [total][H][128] to every sequence (see kvq.h)."""
     _cuda(k_new, torch.float16, "k_new")
@@ -192,6 +222,7 @@ def kvq_decode_workspace_bytes(fmt, num_heads, head_dim=HEAD_DIM):
     return int(lib().kvq_decode_workspace_bytes(int(fmt), int(num_heads), int(head_dim)))
 
 
+@_nvtx
 def kvq_decode_attention(cache, q, block_table, seq_lens, softmax_scale, out, workspace, stream=None):
     """out fp16 [B][H][128] = decode attention of q fp16 [B][H][128] over the cache."""
     _cuda(q, torch.float16, "q")
@@ -211,6 +242,7 @@ def kvq_decode_workspace_bytes_gqa(fmt, num_kv_heads, num_q_heads, head_dim=HEAD
     return int(lib().kvq_decode_workspace_bytes_gqa(int(fmt), int(num_kv_heads), int(num_q_heads), int(head_dim)))
 
 
+@_nvtx
 def kvq_decode_attention_gqa(cache, q, block_table, seq_lens, softmax_scale, out, workspace, stream=None):
     """out fp16 [B][Hq][128] = decode attention of q fp16 [B][Hq][128] over the
     cache, Hq = g * cache heads, query head i reading cache head i // g."""
@@ -228,6 +260,7 @@ def kvq_decode_attention_gqa(cache, q, block_table, seq_lens, softmax_scale, out
            "kvq_decode_attention_gqa")
 
 
+@_nvtx
 def kvq_decode_attention_noalloc(cache, q, block_table, seq_lens, softmax_scale, out, stream=None):
     """kvq_decode_attention without a workspace, for callers that cannot
     allocate device memory when they run decode attention (a plugin whose
@@ -261,6 +294,7 @@ def prefill_workspace(num_q_heads, num_seqs, max_q_per_seq, device="cuda"):
     return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 
 
+@_nvtx
 def kvq_prefill_attention(cache, q, cu_seqlens_q, max_q_per_seq, block_table, seq_lens, softmax_scale, out,
                           workspace=None, stream=None):
     """out fp16 [total][Hq][128] = causal attention of the chunk queries q fp16
@@ -340,6 +374,7 @@ class StepGraph:
         _check(lib().kvq_step_graph_update(self._h, caches, args, len(steps)), "kvq_step_graph_update")
         self._caches, self._args, self._keep = caches, args, keep
 
+    @_nvtx(name="kvq_step_graph_launch")
     def launch(self, stream=None):
         _check(lib().kvq_step_graph_launch(self._h, _stream(stream, self._device)), "kvq_step_graph_launch")
 
