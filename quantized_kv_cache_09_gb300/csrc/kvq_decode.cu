@@ -311,7 +311,6 @@ struct Consumer<KVQ_INT4_B64> {
             const uint32_t ub[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
             for (int m = 0; m < 4; m++) {
-                uint32_t ca[4], cb[4];
                 // {c0,c4}, {c1,c5}, {c2,c6}, {c3,c7} of each token row
                 const uint32_t ah = ua[m] >> 8, bh = ub[m] >> 8;
                 mma16816(c[m], sub_lo(ua[m], mk), sub_lo(ub[m], mk), sub_hi(ua[m], mk), sub_hi(ub[m], mk),
@@ -1614,16 +1613,22 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
     // or a segment ends) ----
     Split *s_split = reinterpret_cast<Split *>(smem_raw + kDecWarps * sizeof(WS) +
                                                ((2 * kMaxSeqsPerLaunch + 1) * sizeof(int32_t) + 15) / 16 * 16);
-    decode_prologue<UT>(p, HU, grid_warps, s_cu, s_len, s_split);
+    // Tiles: the split runs over the units of one tile, (sequence, cache head,
+    // unit), cut into split_warps pieces; the warps come in T groups and group
+    // t runs tile t of every piece, so the T tiles of a cache head stream the
+    // same pages at the same time and all but the first read them from L2.
+    const int split_warps = kTiles ? grid_warps / T : grid_warps;
+    decode_prologue<UT>(p, kTiles ? H : HU, split_warps, s_cu, s_len, s_split);
     const Split &sp = *s_split;
     // logical warp index, round-robin over the CTAs: when fewer than all warps
     // have work (GW < grid warps) the active ones spread over every SM
     const int gw = warp * (int)gridDim.x + blockIdx.x;
-    const bool active = gw < sp.GW;
+    const int my_tile = kTiles ? gw / split_warps : 0;  // tile t of the warp's piece (tiles: the same warp slot of each CTA)
+    const int pi_cur = gw - my_tile * split_warps;      // the warp's piece
+    const bool active = my_tile < T && pi_cur < sp.GW;
     unsigned long long *const piece_ctr = p.counters;  // one word per piece
 
     // ---- issue cursor: the next unit of this warp's piece = (ib, ih, ic); rem units left ----
-    const int pi_cur = gw;
     int rem = 0;
     int ib = 0, ih = 0, ic = 0;
     auto seek = [&](int64_t x) {
@@ -1635,7 +1640,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
         ib = lo;
         const int n = units_of(s_len[ib], UT);
         const int off = (int)(x - s_cu[ib]);
-        ih = off / n;
+        ih = (off / n) * T + my_tile;  // the unit head: cache head off / n, the warp's tile
         ic = off % n;
     };
     if (active) {
@@ -1757,8 +1762,9 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
         piece_new = false;
         if (ic == inb) {
             ic = 0;
-            if (++ih == HU) {
-                ih = 0;
+            ih += T;  // the next cache head, same tile
+            if (ih >= HU) {
+                ih = my_tile;
                 ++ib;
                 while (ib < B && s_len[ib] == 0) ++ib;
                 if (ib < B) inb = units_of(s_len[ib], UT);
@@ -1792,12 +1798,15 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
     auto flush = [&](int b, int h, int c, int units) {
         const int pi = pi_cur;
         const int n = units_of(s_len[b], UT);
-        const int64_t u0 = s_cu[b] + (int64_t)h * n;
+        const int64_t u0 = s_cu[b] + (int64_t)(kTiles ? h / T : h) * n;  // in the split's unit space
         const int64_t sa = u0 + c;
         if (sa == u0 && units == n) {
             cs.finish(lane, out_rows(b, h), nullptr);
         } else {  // split: the piece's first segment goes to its slot 0, its last to slot 1
-            cs.finish(lane, nullptr, p.partials + ((int64_t)pi * 2 + (sa == sp.start(pi) ? 0 : 1)) * kSlotFloats);
+            // (tiles: the partials of tile t's pieces follow those of tile t - 1)
+            const int64_t slot_piece = (int64_t)my_tile * split_warps + pi;
+            cs.finish(lane, nullptr,
+                      p.partials + (slot_piece * 2 + (sa == sp.start(pi) ? 0 : 1)) * kSlotFloats);
             if constexpr (kTiles) return;  // merged by the second launch
             const int64_t pf = sp.piece_of(u0);
             const int64_t pl = sp.piece_of(u0 + n - 1);
@@ -1901,24 +1910,26 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_tile_merge_kernel(Dec
     __shared__ int32_t s_len[kMaxSeqsPerLaunch];
     __shared__ Split s_split;
     const int T = p.tiles, H = p.num_heads, HU = H * T;
+    const int split_warps = grid_workers / T;  // the split kernel's pieces per tile
     pdl_launch_dependents();
-    decode_prologue<UT>(p, HU, grid_workers, s_cu, s_len, &s_split);
+    decode_prologue<UT>(p, H, split_warps, s_cu, s_len, &s_split);
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = (int)(blockIdx.x / HU), h = (int)(blockIdx.x - (unsigned)b * HU);
     const Split &sp = s_split;
     const int n = units_of(s_len[b], UT);
     if (n == 0) return;
-    const int64_t u0 = s_cu[b] + (int64_t)h * n;
+    const int hc = h / T, tile = h - hc * T;
+    const int64_t u0 = s_cu[b] + (int64_t)hc * n;  // the units of one tile
     const int64_t pf = sp.piece_of(u0), pl = sp.piece_of(u0 + n - 1);
     if (pf == pl) return;  // inside one piece: the split kernel wrote the rows
-    const int hc = h / T, tile = h - hc * T;
     const int rows = min(kRowsPerHead, p.group - kRowsPerHead * tile);
     const int first_slot = sp.start(pf) != u0 ? 1 : 0;
+    const int64_t slot_floats = (int64_t)kRowsPerHead * kPartialStride;
+    const float *tile_partials = p.partials + (int64_t)tile * split_warps * 2 * slot_floats;
     for (int r = warp; r < rows; r += kMergeWarps) {
         uint16_t *orow = p.out + (((int64_t)b * H + hc) * p.group + kRowsPerHead * tile + r) * kHeadDim;
-        merge_pieces<16>(p.partials, (int64_t)kRowsPerHead * kPartialStride, r, pf, (int)(pl - pf + 1), first_slot,
-                         orow, lane);
+        merge_pieces<16>(tile_partials, slot_floats, r, pf, (int)(pl - pf + 1), first_slot, orow, lane);
     }
 }
 
@@ -2054,6 +2065,7 @@ static cudaError_t launch_variant(const DecodeParams &p0, int kg, int gw, cudaSt
     const dim3 grid(gw / variant_warps(FMT, kg));
     if (kg == kMqG) {
         p.tiles = (p.group + kMqRows - 1) / kMqRows;
+        if (gw / p.tiles < 1) return cudaErrorInvalidDevice;  // every tile needs a warp per piece
         if (ctas_per_sm<FMT, kMqG>() < 1) return cudaErrorInvalidDevice;  // also sets the smem attribute
         cudaError_t e = launch_pdl(decode_split_kernel<FMT, kMqG>, grid, dim3(variant_warps(FMT, kg) * 32),
                                    dec_smem_bytes<FMT, kMqG>(), s, p, gw);
