@@ -115,14 +115,6 @@ __device__ __forceinline__ uint64_t umma_desc_mn(uint32_t saddr, uint32_t lbo, u
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
@@ -168,26 +160,30 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
         : "memory");
 }
 
-// 32 consecutive 32-bit columns of this thread's TMEM lane (completes at tcgen05.wait::st)
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&w)[32])
+// D (tensor memory) = A x B (+ D if acc = 1), f32 += f16 x f16, one CTA.  Each shared-memory
+// descriptor comes as its two 32-bit halves: the start address sits in bits 0..13 (address
+// / 16 < 2^14 for any shared-memory address), so stepping through a tile adds (byte offset
+// / 16) to the low half without a carry and an MMA issues after a few integer adds.
+// umma_f16_ss: A and B in shared memory; umma_f16_ts: A in tensor memory.
+__device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc, uint32_t acc)
 {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]),
-        "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]), "r"(w[16]), "r"(w[17]), "r"(w[18]),
-        "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]), "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]),
-        "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
-        : "memory");
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc));
 }
-
-// D (tensor memory) += A (tensor memory) x B (shared-memory descriptor)
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                             uint32_t idesc, uint32_t acc)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc));
 }
 
 // 16 code bytes (consecutive elements of one row) -> their fp16 values, 8 per uint4
@@ -474,16 +470,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
                 // the exponent arguments and the partial sums two keys at a time (f32x2)
                 const uint64_t sk2 = pk2(cur_sk[hh], cur_sk[hh]), noff2 = pk2(-off, -off);
                 uint64_t ps2[2] = {pk2(0.0f, 0.0f), pk2(0.0f, 0.0f)};
-                uint32_t w[32];
 #pragma unroll
-                for (int c = 0; c < 32; c++) {
-                    float x0, x1;
-                    upk2(fma2(pk2(sc[2 * c], sc[2 * c + 1]), sk2, noff2), x0, x1);
-                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                    ps2[c & 1] = add2(ps2[c & 1], pk2(p0, p1));
-                    w[c] = f16x2_rn(p0, p1);
+                for (int q = 0; q < 2; q++) {  // two stores of 16 columns
+                    float w[16];
+#pragma unroll
+                    for (int cc = 0; cc < 16; cc++) {
+                        const int c = 16 * q + cc;
+                        float x0, x1;
+                        upk2(fma2(pk2(sc[2 * c], sc[2 * c + 1]), sk2, noff2), x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        ps2[c & 1] = add2(ps2[c & 1], pk2(p0, p1));
+                        w[cc] = __uint_as_float(f16x2_rn(p0, p1));
+                    }
+                    tmem_st16(lane_tm + 32 * hh + 16 * q, w);
                 }
-                tmem_st32(lane_tm + 32 * hh, w);
                 float pa, pb, pc, pd;
                 upk2(ps2[0], pa, pb);
                 upk2(ps2[1], pc, pd);
@@ -636,20 +636,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(PrefillP
         }
     } else if ((tid & 31) == 0) {
         // ---- the MMA thread ----
+        // descriptor halves of the operands' first k-step (per tile, per stage), computed once
+        static_assert(kTiles == 2, "one descriptor register per tile");
+        const uint32_t dq_lo0 = (uint32_t)umma_desc(smem_addr(sm.q[0])), dq_lo1 = (uint32_t)umma_desc(smem_addr(sm.q[1]));
+        const uint32_t dk_lo0 = (uint32_t)umma_desc(smem_addr(sm.k[0])), dk_lo1 = (uint32_t)umma_desc(smem_addr(sm.k[1]));
+        const uint32_t dv_lo0 = (uint32_t)umma_desc_mn(smem_addr(sm.v[0]), kStepKeys * 128, 1024);
+        const uint32_t dv_lo1 = (uint32_t)umma_desc_mn(smem_addr(sm.v[1]), kStepKeys * 128, 1024);
+        const uint32_t dsw_hi = (uint32_t)(umma_desc(smem_addr(sm.q[0])) >> 32);  // SBO, version, swizzle
+        const uint32_t dv_hi = (uint32_t)(umma_desc_mn(smem_addr(sm.v[0]), kStepKeys * 128, 1024) >> 32);
         auto issue_s = [&](int t, int i) {  // S(i) = Q K(i)^T of tile t: 128 x 128 keys, 8 MMAs of K = 16
-            const uint32_t aq = smem_addr(sm.q[t]), ak = smem_addr(sm.k[i & 1]);
+            const uint32_t aq = t == 0 ? dq_lo0 : dq_lo1, ak = (i & 1) ? dk_lo1 : dk_lo0;
 #pragma unroll
-            for (int ks = 0; ks < 8; ks++)
-                umma_f16(tmem + 256 * t, umma_desc(aq + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32),
-                         umma_desc(ak + (ks >> 2) * (kStepKeys * 128) + (ks & 3) * 32), kIdescS, ks > 0);
+            for (int ks = 0; ks < 8; ks++) {
+                // k-step ks: elements 16 ks .. 16 ks + 15 = 32-byte column (ks & 3) of 64-element block ks >> 2
+                umma_f16_ss(tmem + 256 * t, aq + (uint32_t)(((ks >> 2) * (kTcRows * 128) + (ks & 3) * 32) >> 4), dsw_hi,
+                            ak + (uint32_t)(((ks >> 2) * (kStepKeys * 128) + (ks & 3) * 32) >> 4), dsw_hi, kIdescS,
+                            ks > 0 ? 1u : 0u);
+            }
             umma_commit(&sm.s_full[t]);
         };
         auto issue_pv = [&](int t, int i) {  // O += P(i) V(i): P from tensor memory, 8 columns per 16 keys
-            const uint32_t tt = tmem + 256 * t, av = smem_addr(sm.v[i & 1]);
+            const uint32_t tt = tmem + 256 * t, av = (i & 1) ? dv_lo1 : dv_lo0;
 #pragma unroll
             for (int ks = 0; ks < 8; ks++)
-                umma_f16_ts(tt + 128, tt + 8 * ks, umma_desc_mn(av + ks * 16 * 128, kStepKeys * 128, 1024), kIdescO,
-                            (i > 0 || ks > 0));
+                umma_f16_ts(tt + 128, tt + 8 * ks, av + (uint32_t)((ks * 16 * 128) >> 4), dv_hi, kIdescO,
+                             (i > 0 || ks > 0) ? 1u : 0u);
             umma_commit(&sm.o_done[t]);
         };
         // steps are counted from the CTA's first (stage, barrier phase, accumulate flag); the
