@@ -14,8 +14,10 @@ decode position cycles through one 64-token block, so the context stays
 Every other workload of the path runs after it, each with its own roofline,
 under "workloads" in the same JSON line: tiny, llama2-7b-layer, paged-int8,
 prefill-append (quantize GB/s), llama3-8b-layer-gqa, llama2-7b-layer-fp8,
-chunked-prefill (tensor-core attention, TFLOP/s) and mqa-32k (one cache head
-serving 32 query heads).
+chunked-prefill (tensor-core attention, TFLOP/s), mqa-32k (one cache head
+serving 32 query heads) and the stateless codec (kvq_quantize, GB/s) over the
+whole K and V history of the 7B layer (int4, int8, FP8) and of long-context
+(int4).
 
 value    decode tokens/s = sequences advanced one token through one layer's
          attention per second, summed over ranks (weak scaling: every rank runs
@@ -58,7 +60,13 @@ WORKLOADS = {
     "llama2-7b-layer-fp8": ("decode", 7),
     "chunked-prefill": ("prefill", 8),
     "mqa-32k": ("decode", 9),
+    "quantize-7b-layer": ("quantize", 2),
+    "quantize-long-context": ("quantize", 3),
+    "quantize-7b-layer-int8": ("quantize", 2),
+    "quantize-7b-layer-fp8": ("quantize", 7),
 }
+# stateless-codec workloads whose format is not their history's
+QUANT_FORMAT = {"quantize-7b-layer-int8": 1}
 FORMAT_NAMES = {0: ("int4", "int4-b64"), 1: ("int8", "int8-page"), 2: ("fp8-e4m3", "fp8-e4m3-page")}
 
 
@@ -133,6 +141,7 @@ def measured_tensor_peak():
 KERNEL_SOURCES = {
     "decode_split_kernel": ("kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h"),
     "append_kernel": ("kvq_quantize.cu", "kvq_device.cuh", "kvq_internal.h"),
+    "quantize_contig_kernel": ("kvq_quantize.cu", "kvq_device.cuh", "kvq_internal.h"),
     "prefill_attn_tc_kernel": ("kvq_prefill.cu", "kvq_device.cuh", "kvq_internal.h"),
 }
 
@@ -239,7 +248,10 @@ def _make(name, seed, prefill_seqs=64):
         c = W.CONFIGS[5]
         return W.Workload(prefill_seqs, c["H"], c["D"], [c["L"]] * prefill_seqs, c["fmt"], c["sigma"], None,
                           "permuted", seed, 0, c["name"])
-    return W.make_workload(cfg, seed=seed)
+    wl = W.make_workload(cfg, seed=seed)
+    if kind == "quantize" and name in QUANT_FORMAT:
+        wl.fmt = QUANT_FORMAT[name]
+    return wl
 
 
 def decode_context(wl):
@@ -270,6 +282,11 @@ def workload_config(name, world=1, seed=0, prefill_seqs=64):
         return {"workload": name, "new_tokens": int(wl.lens.sum()), "H": wl.H, "D": wl.D, "format": "int4-b64",
                 "table": wl.table, "step": "one kvq_append of all new tokens", "parallelism": par,
                 "l2": "inputs larger than L2"}
+    if kind == "quantize":
+        return {"workload": name, "tokens": int(wl.lens.sum()), "B": wl.B, "H": wl.H, "D": wl.D,
+                "format": FORMAT_NAMES[wl.fmt][1],
+                "step": "kvq_quantize of the K history, then of V ([tokens][H][D] each, sequences back to back)",
+                "parallelism": par, "l2": "inputs larger than L2"}
     return {"workload": name, "B": wl.B, "H": wl.H, "Hq": wl.Hq, "D": wl.D, "context": int(wl.lens[0]),
             "chunk": wl.chunk, "format": FORMAT_NAMES[wl.fmt][1], "step": "one kvq_prefill_attention of every chunk query",
             "parallelism": par, "l2": "codes (268 MB) larger than L2"}
@@ -350,13 +367,14 @@ def oracle_decode_rate(name, seconds, seed, threads=None):
     return steps / el / wl.H, n, desc
 
 
-def oracle_append_rate(seconds, seed, threads=None):
-    """The oracle codec on samples of prefill-append: each thread quantizes
-    4096-token x 32-head K and V chunks of its own sequence; GB/s of fp16 read
-    + codes + scales written, as for the GPU.  Returns (GB/s, threads, desc)."""
+def oracle_append_rate(seconds, seed, threads=None, name="prefill-append"):
+    """The oracle codec on samples of a quantize workload (prefill-append or a
+    stateless quantize): each thread quantizes 1024-token x H-head K and V
+    chunks of its own sequence; GB/s of fp16 read + codes + scales written, as
+    for the GPU.  Returns (GB/s, threads, desc)."""
     from oracle import oracle as orc
 
-    wl = _make("prefill-append", seed)
+    wl = _make(name, seed)
     n = threads or _threads()
     xs = []
     for i in range(n):
@@ -380,7 +398,8 @@ def oracle_append_rate(seconds, seed, threads=None):
         t.join()
     el = time.time() - t0
     nbytes = sum(done) * wl.quantize_bytes(1024)
-    return nbytes / el / 1e9, n, f"{sum(done)} oracle quantizations of 1024-token x {wl.H}-head K+V chunks on {n} threads, {el:.1f} s"
+    return nbytes / el / 1e9, n, (f"{sum(done)} oracle {FORMAT_NAMES[wl.fmt][0]} quantizations of 1024-token x "
+                                  f"{wl.H}-head K+V chunks of {name} on {n} threads, {el:.1f} s")
 
 
 def oracle_prefill_rate(seconds, seed):
@@ -413,6 +432,8 @@ def oracle_rate(name, seconds, seed):
         return oracle_decode_rate(name, seconds, seed) + ("tokens/s",)
     if kind == "append":
         return oracle_append_rate(seconds, seed) + ("GB/s",)
+    if kind == "quantize":
+        return oracle_append_rate(seconds, seed, name=name) + ("GB/s",)
     return oracle_prefill_rate(seconds, seed) + ("tokens/s",)
 
 
@@ -652,6 +673,49 @@ def measure_append(K, Wm, seed, dev, nseqs=64):
     return dict(ms=ms, bytes=nbytes, tokens=nseqs * L)
 
 
+def measure_quantize(name, K, Wm, seed, dev):
+    """A stateless-codec workload: kvq_quantize of the whole K history of the
+    workload's sequences ([B*L][H][D], sequences back to back, so every 64-row
+    block is one (sequence, head, block) of quantize_block), then of V."""
+    import torch
+
+    from quantized_kv_cache_09_gb300 import kvq
+
+    wl = _make(name, seed)
+    L = int(wl.lens[0])
+    if not bool((wl.lens == L).all()) or L % 64:
+        raise ValueError(f"{name}: the stateless quantize workloads need equal, block-aligned lengths")
+    T = wl.B * L
+    xs, codes, scales = [], [], []
+    for which in ("k", "v"):
+        x = torch.empty((T, wl.H, wl.D), dtype=torch.float16, device=dev)
+        for b in range(wl.B):
+            wl.kv_device(which, b, 0, L, x[b * L:(b + 1) * L])
+        xs.append(x)
+        codes.append(torch.empty((T // 64, wl.H, 64, wl.row_bytes), dtype=torch.uint8, device=dev))
+        scales.append(torch.empty((T // 64, wl.H), dtype=torch.float32, device=dev))
+
+    def step():
+        for i in range(2):
+            kvq.kvq_quantize(wl.fmt, xs[i], codes[i], scales[i])
+
+    for _ in range(Wm):
+        step()
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    nbytes = wl.quantize_bytes(L) * wl.B
+    del xs, codes, scales
+    torch.cuda.empty_cache()
+    return dict(ms=ms, bytes=nbytes, tokens=T, fmt=wl.fmt)
+
+
 def measure_chunked_prefill(K, Wm, seed, dev):
     """chunked-prefill: kvq_prefill_attention of the last 512 of 8192 tokens of
     8 sequences (H=32, int4) over the cache that holds them."""
@@ -760,6 +824,22 @@ def append_result(r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed=0, prefill
             "gpu_launches": K}
 
 
+def quantize_result(name, r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed=0):
+    ms = max_over_ranks(pg, r["ms"], dev)
+    gbs = r["bytes"] / (ms * 1e-3) / 1e9
+    return {"metric": METRIC, "value": whole_job_rate(world, r["bytes"] / 1e9, ms * 1e-3), "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": f"fp16 in, {FORMAT_NAMES[r['fmt']][0]} codes out, fp32 math",
+            "data": "synthetic (seeded generator in HBM)", "config": workload_config(name, world, cfg_seed),
+            "roofline": {"kernel": "quantize_contig_kernel", "bound": "hbm", "achieved": gbs, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": ncu_traffic("quantize_contig_kernel", name),
+                         "algorithmic_bytes_per_launch": r["bytes"] / 2,
+                         "timing": "mean CUDA-event time of one step = two kvq_quantize calls (K, V)"},
+            "gpu_launches": 2 * K}
+
+
 def prefill_result(r, world, pg, dev, K, Wm, cfg_seed=0):
     ms = max_over_ranks(pg, r["ms"], dev)
     e2e_ms = max_over_ranks(pg, r["e2e_ms"], dev)
@@ -790,6 +870,9 @@ def measure(name, K, Wm, seed, dev, pg, world, clocks=None, prefill_seqs=64, cfg
     if kind == "append":
         r = measure_append(K, max(Wm, 1), seed, dev, prefill_seqs)
         return append_result(r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed, prefill_seqs)
+    if kind == "quantize":
+        r = measure_quantize(name, K, max(Wm, 1), seed, dev)
+        return quantize_result(name, r, world, pg, dev, K, Wm, peak, peak_kind, cfg_seed)
     r = measure_chunked_prefill(K, max(Wm, 1), seed, dev)
     return prefill_result(r, world, pg, dev, K, Wm, cfg_seed)
 

@@ -1,0 +1,43 @@
+"""Host logic of the benchmark's workload table (no GPU): every workload has a
+config, the stateless-codec workloads carry the codec they name, and their
+algorithmic bytes are the per-element figures of the codec -- fp16 read (2 B)
+plus the code written (0.5 B int4, 1 B int8 / FP8) per element, and one fp32
+scale per (64-token block, head) -- for K and V."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_every_workload_has_a_config():
+    for name, (kind, _) in bench.WORKLOADS.items():
+        cfg = bench.workload_config(name)
+        assert cfg["workload"] == name
+        assert kind in ("decode", "append", "prefill", "quantize")
+
+
+def test_quantize_workloads_bytes_per_element():
+    per_elem = {"int4-b64": 2.5, "int8-page": 3.0, "fp8-e4m3-page": 3.0}
+    seen = set()
+    for name, (kind, _) in bench.WORKLOADS.items():
+        if kind != "quantize":
+            continue
+        cfg = bench.workload_config(name)
+        wl = bench._make(name, 0)
+        L = int(wl.lens[0])
+        assert (wl.lens == L).all() and L % 64 == 0  # whole blocks, sequences back to back
+        elems = 2 * wl.B * L * wl.H * wl.D  # K and V
+        scales = 2 * wl.B * (L // 64) * wl.H * 4
+        assert wl.quantize_bytes(L) * wl.B == per_elem[cfg["format"]] * elems + scales
+        seen.add((cfg["format"], cfg["tokens"]))
+    # the 7B layer's history in all three codecs and the long-context history in int4
+    assert seen == {("int4-b64", 65536), ("int8-page", 65536), ("fp8-e4m3-page", 65536), ("int4-b64", 524288)}
+
+
+def test_reference_arm_of_a_quantize_workload():
+    rate, cores, desc, unit = bench.oracle_rate("quantize-7b-layer-int8", 0.3, 0)
+    assert unit == "GB/s" and rate > 0 and cores >= 1
+    assert "int8" in desc and "quantize-7b-layer-int8" in desc

@@ -157,3 +157,38 @@ def test_prefill_append_every_sequence(cuda_ok):
     dw.prefill(max_tokens_per_call=1 << 20)
     assert kvq.kvq_get_device_status(dw.cache) == (0, 0)
     _verify_all(dw, wl.lens)
+
+
+@pytest.mark.parametrize("cfg,fmt,seqs", [(2, W.INT4, None), (2, W.INT8, None), (7, W.FP8, None), (3, W.INT4, (0, 5, 10, 15))])
+def test_stateless_quantize_full_size(cuda_ok, cfg, fmt, seqs):
+    """kvq_quantize as the quantize workloads time it: the whole K history of
+    the workload's sequences as one [B*L][H][D] tensor (sequences back to
+    back), then V; every code block and both scale arrays of the checked
+    sequences bit-exact against the oracle (long-context: four of its 16
+    sequences, the first and the last among them)."""
+    wl = W.make_workload(cfg)
+    wl.fmt = fmt
+    L = int(wl.lens[0])
+    T = wl.B * L
+    nb = L // 64
+    res = []
+    for which in ("k", "v"):
+        x = torch.empty((T, wl.H, D), dtype=torch.float16, device="cuda")
+        for b in range(wl.B):
+            wl.kv_device(which, b, 0, L, x[b * L:(b + 1) * L])
+        codes = torch.empty((T // 64, wl.H, 64, wl.row_bytes), dtype=torch.uint8, device="cuda")
+        scales = torch.empty((T // 64, wl.H), dtype=torch.float32, device="cuda")
+        kvq.kvq_quantize(fmt, x, codes, scales)
+        del x
+        res.append((codes, scales))
+    torch.cuda.synchronize()
+    (kc, ks), (vc, vs) = res
+    check = range(wl.B) if seqs is None else seqs
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        futs = [ex.submit(_check_sequence, wl, b, L,
+                          (kc[b * nb:(b + 1) * nb].cpu().numpy(), ks[b * nb:(b + 1) * nb].cpu().numpy(),
+                           vc[b * nb:(b + 1) * nb].cpu().numpy(), vs[b * nb:(b + 1) * nb].cpu().numpy()),
+                          None, None) for b in check]
+        for f in futs:
+            f.result()
