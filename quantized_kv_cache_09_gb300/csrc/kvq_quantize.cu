@@ -27,8 +27,9 @@
 // fraction, saturating, by the hardware conversion.  The fast path converts
 // y' (1 - 2^-21) and y' (1 + 2^-21) for y' = RN(x * r): RN(x / scale) lies
 // between them (|y' - RN(x / scale)| < 1.5 * 2^-23 |y|), the conversion is
-// monotone, so equal codes are the code; a pair whose two ends differ (y near
-// a midpoint of the E4M3 grid) takes the correctly rounded division.
+// monotone, so equal codes are the code; a group of 8 in which some pair's two
+// ends differ (y near a midpoint of the E4M3 grid) takes the correctly rounded
+// division for all 8 (one branch per group instead of one per pair).
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -76,7 +77,7 @@ __device__ __forceinline__ uint2 quant8_fp8(const uint4 &v, uint64_t rr, float s
     if (scale == 0.0f) return make_uint2(0u, 0u);  // all-zero block: codes 0x00 (also for -0.0)
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     const uint64_t dn = pk2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f), up = pk2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f);
-    uint32_t c[4];
+    uint32_t c[4], diff = 0u;
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
@@ -85,7 +86,14 @@ __device__ __forceinline__ uint2 quant8_fp8(const uint4 &v, uint64_t rr, float s
         upk2(mul2(y, dn), a0, a1);
         upk2(mul2(y, up), b0, b1);
         c[i] = e4m3x2_rn(a0, a1);
-        if (c[i] != e4m3x2_rn(b0, b1)) c[i] = e4m3x2_rn(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+        diff |= c[i] ^ e4m3x2_rn(b0, b1);
+    }
+    if (diff != 0u) {  // some pair of the 8 brackets a grid midpoint: the whole group divides exactly
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+            c[i] = e4m3x2_rn(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+        }
     }
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }

@@ -105,6 +105,33 @@ def test_fp8_grid_midpoints_and_signed_zeros_bit_exact(cuda_ok):
     _assert_same(kvq.KVQ_FP8_E4M3, x.astype(np.float16).view(np.uint16))
 
 
+def test_fp8_values_nearest_the_midpoints_of_random_scales_bit_exact(cuda_ok):
+    """The FP8 fast path brackets RN(x / scale) between y' (1 -+ 2^-21) and
+    keeps the code when both ends convert alike.  Each block here holds +-a
+    and, for every midpoint m of the E4M3 grid below 448, the binary16 value
+    nearest m * scale and its two neighbours, both signs, for 2048 random
+    absmax values a (scale = a / 448 inexact): the elements whose groups the
+    check must send to the exact division."""
+    rng = np.random.default_rng(31)
+    vals = np.array([orc.e4m3_to_float(c) for c in range(127)])
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    a = np.exp(rng.uniform(np.log(1e-3), np.log(6e4), 2048)).astype(np.float16)
+    a = a[np.isfinite(a) & (a > 0)]
+    x = np.zeros((64 * a.size, 1, D), dtype=np.float16)
+    for i, ai in enumerate(a):
+        s = np.float32(ai) / np.float32(448.0)
+        v = (mids * s).astype(np.float16)
+        cand = np.concatenate([v, np.nextafter(v, np.float16(np.inf)), np.nextafter(v, np.float16(0))])
+        cand = cand[np.isfinite(cand) & (np.abs(cand.astype(np.float32)) <= np.float32(ai))]
+        vals_blk = np.concatenate([[ai, -ai], cand, -cand])[:64 * D]
+        blk = x[64 * i:64 * i + 64, 0, :].reshape(-1)
+        blk[:vals_blk.size] = vals_blk
+        fill = np.clip(rng.standard_normal(blk.size - vals_blk.size) * 0.3, -0.9, 0.9) * np.float32(ai)
+        blk[vals_blk.size:] = fill.astype(np.float16)
+        x[64 * i:64 * i + 64, 0, :] = blk.reshape(64, D)
+    _assert_same(kvq.KVQ_FP8_E4M3, x.view(np.uint16))
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_every_fp16_absmax_bit_exact(cuda_ok, fmt):
     """One block per positive finite fp16 magnitude a, row 0 = (a, -a, a/3, ...):
