@@ -102,7 +102,8 @@ constexpr int kMqRows = 16;
 // fewer warps fit in shared memory (and each has more registers)
 template <int FMT, int G>
 struct DecShape {
-    static constexpr int kWarps = G == kMqG ? 8 : DecFmt<FMT>::kWarps;
+    // G = 8: the 8 query rows a stage carries leave room for 11 warps (12 need 247 KB)
+    static constexpr int kWarps = G == kMqG ? 8 : G == 8 ? 11 : DecFmt<FMT>::kWarps;
     static constexpr int kQRows = G == kMqG ? kMqRows : G;
 };
 template <int FMT, int G>
@@ -112,6 +113,7 @@ constexpr size_t dec_smem_bytes()
     using S = DecShape<FMT, G>;
     return S::kWarps * sizeof(WarpSmem<F::kStages, F::kUnitsPerStage * kUnitBytes, S::kQRows>) + kSeqSmemBytes;
 }
+static_assert(dec_smem_bytes<KVQ_INT4_B64, 8>() <= 227 * 1024, "the G = 8 warps fit one CTA's shared memory");
 
 // the byte formats' exact widening to fp16 pairs, by format (int4: SubMagic below)
 template <int FMT>
@@ -449,22 +451,31 @@ struct Consumer<KVQ_INT4_B64> {
     }
 };
 
-// int4 with grouped query heads: G = 2 or 4 query heads share each cache
+// int4 with grouped query heads: G = 2, 4 or 8 query heads share each cache
 // head, and one pass over the codes serves all G (the mma columns that the
 // multi-head consumer fills with copies of q carry the group's other heads).
 // Lane (grp = lane >> 2, t = lane & 3):
-//   QK: column c of B holds q of head hq(c) = (((c >> 2) << 1) | (c & 1)) % G,
-//       so the lane receives, for tokens grp and grp + 8 of each tile, the
-//       scores of its head slots c = 0, 1: heads (2 (t >> 1) + c) % G.
-//   PV: column c of B holds part (c >> 1) & 1 (0: RN16(x), 1: the remainder)
-//       of head hq(c); the lane's accumulators are then exactly its slot
-//       heads, part t & 1, so a rescale of a head's running max is local.
+//   QK: column c of B holds q of head hq(c) = (((c >> 2) << 1) | (c & 1)) % G
+//       for G = 2, 4 and hq(c) = c for G = 8, so the lane receives, for tokens
+//       grp and grp + 8 of each tile, the scores of its head slots c = 0, 1:
+//       the heads of columns 2t + c.
+//   PV, G = 2, 4: column c of B holds part (c >> 1) & 1 (0: RN16(x), 1: the
+//       remainder) of head hq(c); the lane's accumulators are then exactly its
+//       slot heads, part t & 1, so a rescale of a head's running max is local.
+//   PV, G = 8: the eight columns are the eight heads and carry RN16(x) alone
+//       (no remainder column is left; the tile kernel's weights are single
+//       fp16 values too), so a weight keeps 11 bits: the error of the output
+//       is at most 2^-11 of max|v^| from the weights (one dominant key) plus
+//       the fp16 rounding of the output.  The offset share of PV is taken out
+//       with the sum of the rounded weights the MMA multiplied, not of x.
+//       The lane's accumulators are its slot heads.
 //   The weights of column grp_d come from lane 4 * token + (grp_d >> 1),
 //   slot grp_d & 1 (that lane holds head hq(grp_d) and produces part
-//   (grp_d >> 1) & 1).
+//   (grp_d >> 1) & 1; for G = 8, RN16(x)).
 template <int G>
 struct ConsumerGqa {
-    static_assert(G == 2 || G == 4, "query heads per cache head");
+    static_assert(G == 2 || G == 4 || G == 8, "query heads per cache head");
+    static constexpr bool kAllHeads = G == 8;  // every B column a head of its own
     static constexpr int kScores = 8;
     static constexpr int kPf = 4;
     int rows;  // (unused: G query rows)
@@ -492,7 +503,7 @@ struct ConsumerGqa {
     __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
     {
         const int g = lane >> 2, t = lane & 3;
-        const int head = (((g >> 2) << 1) | (g & 1)) % G;  // column g of B
+        const int head = kAllHeads ? g : (((g >> 2) << 1) | (g & 1)) % G;  // column g of B
         const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + head * kHeadDim + 32 * t);
         const __half2 odd_scale = __float2half2_rn(kQOdd);
         float se = 0.0f, so = 0.0f;
@@ -554,7 +565,7 @@ struct ConsumerGqa {
 
     // online softmax over the unit, per head slot.  px[2 tau + c] = this
     // lane's part (t & 1) of x = p * sv for tokens (grp, grp + 8) of tile tau,
-    // head slot c, as an fp16 pair
+    // head slot c, as an fp16 pair (G = 8: RN16(x))
     __device__ __forceinline__ void softmax(const float sc[8], int ntok, float fac, float sv, int lane,
                                             uint32_t px[4])
     {
@@ -596,24 +607,42 @@ struct ConsumerGqa {
         const float ps0 = (pe[0] + pe[2]) + (pe[4] + pe[6]), ps1 = (pe[1] + pe[3]) + (pe[5] + pe[7]);
         l_lane[0] += ps0;
         l_lane[1] += ps1;
-        x_lane[0] = fmaf(ps0, sv, x_lane[0]);
-        x_lane[1] = fmaf(ps1, sv, x_lane[1]);
         const uint64_t vv = pk2(sv, sv);
-        const bool lo_part = t & 1;
-#pragma unroll
-        for (int tau = 0; tau < 2; tau++)
+        if constexpr (kAllHeads) {
+            // RN16(x) alone, and the sum of exactly those weights for the offset share
 #pragma unroll
             for (int c = 0; c < 2; c++) {
-                uint32_t hi, lo;
-                hi_lo_pairs(mul2(pk2(pe[4 * tau + c], pe[4 * tau + 2 + c]), vv), hi, lo);
-                px[2 * tau + c] = lo_part ? lo : hi;
+                float xr = 0.0f;
+#pragma unroll
+                for (int tau = 0; tau < 2; tau++) {
+                    float x0, x1;
+                    upk2(mul2(pk2(pe[4 * tau + c], pe[4 * tau + 2 + c]), vv), x0, x1);
+                    const uint32_t h = f16x2_rn(x0, x1);
+                    const float2 r = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+                    xr += r.x + r.y;
+                    px[2 * tau + c] = h;
+                }
+                x_lane[c] += xr;
             }
+        } else {
+            x_lane[0] = fmaf(ps0, sv, x_lane[0]);
+            x_lane[1] = fmaf(ps1, sv, x_lane[1]);
+            const bool lo_part = t & 1;
+#pragma unroll
+            for (int tau = 0; tau < 2; tau++)
+#pragma unroll
+                for (int c = 0; c < 2; c++) {
+                    uint32_t hi, lo;
+                    hi_lo_pairs(mul2(pk2(pe[4 * tau + c], pe[4 * tau + 2 + c]), vv), hi, lo);
+                    px[2 * tau + c] = lo_part ? lo : hi;
+                }
+        }
     }
 
-    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t px[4], int lane)
+    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t px[kPf], int lane)
     {
         const int g = lane >> 2, t = lane & 3;
-        // column g of B: head slot g & 1, part (g >> 1) & 1, from lanes 4 token + (g >> 1)
+        // column g of B: head slot g & 1, part (g >> 1) & 1 (G = 8: RN16(x)), from lanes 4 token + (g >> 1)
         const int src = 8 * t + (g >> 1);
         const bool slot1 = g & 1;
 #pragma unroll
@@ -655,8 +684,9 @@ struct ConsumerGqa {
 
 
     // the group's output rows (orow: G rows) or partial slots (part: G
-    // partials of kPartialStride floats).  The two parts of a head are in lanes
-    // t and t ^ 1; lanes with even t, t >> 1 < G / 2, write heads 2 (t >> 1) + c.
+    // partials of kPartialStride floats).  G = 2, 4: the two parts of a head are
+    // in lanes t and t ^ 1; lanes with even t, t >> 1 < G / 2, write heads
+    // 2 (t >> 1) + c.  G = 8: every lane writes its heads 2t + c.
     __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
     {
         const int g = lane >> 2, t = lane & 3;
@@ -673,14 +703,16 @@ struct ConsumerGqa {
             l[c] = v;
             xs[c] = x;
         }
+        if constexpr (!kAllHeads) {
 #pragma unroll
-        for (int i = 0; i < 8; i++)
+            for (int i = 0; i < 8; i++)
 #pragma unroll
-            for (int j = 0; j < 4; j++) acc[i][j] += __shfl_xor_sync(kFull, acc[i][j], 1);
-        if ((t & 1) || 2 * (t >> 1) >= G) return;
+                for (int j = 0; j < 4; j++) acc[i][j] += __shfl_xor_sync(kFull, acc[i][j], 1);
+            if ((t & 1) || 2 * (t >> 1) >= G) return;
+        }
 #pragma unroll
         for (int c = 0; c < 2; c++) {
-            const int head = 2 * (t >> 1) + c;
+            const int head = kAllHeads ? 2 * t + c : 2 * (t >> 1) + c;
 #pragma unroll
             for (int R = 0; R < 2; R++) {
                 float v[8];
@@ -1421,13 +1453,17 @@ __device__ __noinline__ void merge_pieces(const float *partials, int64_t slot_fl
 // piece holds the G heads' partials side by side; the loads of kBatch pieces x
 // G heads are issued together, so a merge of cnt pieces takes about cnt /
 // kBatch round trips to L2 instead of G times as many (kBatch = 8 / G keeps
-// the call within the kernel's register budget).
-template <int kBatch, int G>
+// the call within the kernel's register budget).  A slot holds kSlotHeads
+// heads; this call merges G of them from head0 on (a group of 8 is merged as
+// two calls of 4: one call of 8 heads would not fit beside the streaming
+// loop's live registers).
+template <int kBatch, int G, int kSlotHeads = G>
 __device__ __noinline__ void merge_group(const float *partials, int64_t gf, int cnt, int first_slot,
-                                         uint16_t *out_rows, int lane)
+                                         uint16_t *out_rows, int lane, int head0 = 0)
 {
-    constexpr int64_t kSlot = (int64_t)G * kPartialStride;
-    const float *pbase = partials + gf * 2 * kSlot;
+    constexpr int64_t kSlot = (int64_t)kSlotHeads * kPartialStride;
+    const float *pbase = partials + gf * 2 * kSlot + (int64_t)head0 * kPartialStride;
+    out_rows += (int64_t)head0 * kHeadDim;
     auto part = [&](int i) { return pbase + ((int64_t)i * 2 + (i == 0 ? first_slot : 0)) * kSlot; };
     float2 ml[G];
     float4 a[kBatch][G];
@@ -1816,7 +1852,10 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
                 if constexpr (G == 1)
                     merge_pieces<F::kMergeBatch>(p.partials, kSlotFloats, 0, pf, (int)(pl - pf + 1), first_slot,
                                                  orow, lane);
-                else if constexpr (!kTiles)
+                else if constexpr (G == 8) {
+                    merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 0);
+                    merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 4);
+                } else if constexpr (!kTiles)
                     merge_group<8 / G, G>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane);
             }
         }
@@ -1962,7 +2001,7 @@ static int ctas_per_sm()
 static int kernel_group(int fmt, int g)
 {
     if (g == 1) return 1;
-    if (fmt == KVQ_INT4_B64 && (g == 2 || g == 4)) return g;
+    if (fmt == KVQ_INT4_B64 && (g == 2 || g == 4 || g == 8)) return g;
     return kMqG;
 }
 
@@ -1978,6 +2017,7 @@ static int variant_ctas(int kg)
     if constexpr (FMT == KVQ_INT4_B64) {
         if (kg == 2) return ctas_per_sm<FMT, 2>();
         if (kg == 4) return ctas_per_sm<FMT, 4>();
+        if (kg == 8) return ctas_per_sm<FMT, 8>();
     }
     return 0;
 }
@@ -1985,6 +2025,7 @@ static int variant_ctas(int kg)
 static int variant_warps(int fmt, int kg)
 {
     if (kg == kMqG) return DecShape<KVQ_INT4_B64, kMqG>::kWarps;
+    if (kg == 8) return DecShape<KVQ_INT4_B64, 8>::kWarps;
     return fmt == KVQ_INT4_B64 ? DecFmt<KVQ_INT4_B64>::kWarps : DecFmt<KVQ_INT8_PAGE>::kWarps;
 }
 
@@ -2037,7 +2078,8 @@ size_t decode_workspace_bytes(int fmt, int group)
     if (gw <= 0) return 0;
     static_assert(DecFmt<KVQ_INT4_B64>::kWarps * DecFmt<KVQ_INT4_B64>::kCtasPerSm <= kMaxDecodeWarpsPerSm &&
                       DecFmt<KVQ_INT8_PAGE>::kWarps * DecFmt<KVQ_INT8_PAGE>::kCtasPerSm <= kMaxDecodeWarpsPerSm &&
-                      DecShape<KVQ_INT4_B64, kMqG>::kWarps * DecFmt<KVQ_INT4_B64>::kCtasPerSm <= kMaxDecodeWarpsPerSm,
+                      DecShape<KVQ_INT4_B64, kMqG>::kWarps * DecFmt<KVQ_INT4_B64>::kCtasPerSm <= kMaxDecodeWarpsPerSm &&
+                      DecShape<KVQ_INT4_B64, 8>::kWarps * DecFmt<KVQ_INT4_B64>::kCtasPerSm <= kMaxDecodeWarpsPerSm,
                   "the counter region holds kMaxDecodeWarpsPerSm warps per SM");
     const size_t counters = decode_counter_bytes();
     if (counters == 0) return 0;
@@ -2090,6 +2132,10 @@ static cudaError_t launch_variant(const DecodeParams &p0, int kg, int gw, cudaSt
         if (kg == 4) {
             if (ctas_per_sm<FMT, 4>() < 1) return cudaErrorInvalidDevice;
             return launch_pdl(decode_split_kernel<FMT, 4>, grid, block, dec_smem_bytes<FMT, 4>(), s, p, gw);
+        }
+        if (kg == 8) {
+            if (ctas_per_sm<FMT, 8>() < 1) return cudaErrorInvalidDevice;
+            return launch_pdl(decode_split_kernel<FMT, 8>, grid, block, dec_smem_bytes<FMT, 8>(), s, p, gw);
         }
     }
     return cudaErrorInvalidValue;

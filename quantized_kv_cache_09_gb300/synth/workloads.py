@@ -63,6 +63,10 @@ CONFIGS = {
     # heads; 64 sequences of 32K tokens put 268 MB of codes behind one step
     9: dict(name="mqa-32k", B=64, H=1, Hq=32, D=128, L=32768, fmt=INT4, sigma=1.0,
             outliers=("per_head", 4, 10.0), table="permuted"),
+    # 64 query heads over 8 cache heads (g = 8), the Llama-3-70B attention shape,
+    # with the 8B layer's batch and context: the same 268 MB of codes per step
+    10: dict(name="llama3-70b-layer-gqa", B=32, H=8, Hq=64, D=128, L=8192, fmt=INT4, sigma=1.0,
+             outliers=("per_head", 4, 10.0), table="contiguous"),
 }
 
 

@@ -21,6 +21,8 @@ sequences' histories are on the host at a time.
   llama2-7b-layer-fp8  B=8, H=32, L=8192, FP8 E4M3: decode steps, as timed
   mqa-32k              B=64, 1 cache head x 32 query heads, L=32768 int4,
                        permuted pages: decode steps, as timed
+  llama3-70b-layer-gqa B=32, 8 cache heads x 8 query heads, L=8192 int4:
+                       decode steps, as timed
 """
 import concurrent.futures as cf
 import math
@@ -103,10 +105,10 @@ def _verify_all(dw, lens, q_bits=None, out=None):
     return worst
 
 
-@pytest.mark.parametrize("cfg", [2, 6, 7, 9])
+@pytest.mark.parametrize("cfg", [2, 6, 7, 9, 10])
 def test_layer_decode_steps(cuda_ok, cfg):
     """llama2-7b-layer (int4), llama3-8b-layer-gqa, llama2-7b-layer-fp8,
-    mqa-32k: three timed-style steps, then every sequence's pages and every
+    mqa-32k, llama3-70b-layer-gqa: three timed-style steps, then every sequence's pages and every
     (sequence, query head) output against the oracle."""
     wl = W.make_workload(cfg, extra_tokens=64)
     dw = DeviceWorkload(wl)

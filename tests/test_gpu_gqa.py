@@ -57,7 +57,7 @@ def _check(wl, lens, q_bits, got, g, oc=None):
 
 
 FMTS = {"int4": kvq.KVQ_INT4_B64, "int8": kvq.KVQ_INT8_PAGE, "fp8": kvq.KVQ_FP8_E4M3}
-# (format, g): g = 2, 4 on int4 use the spare-column kernel; every other pair
+# (format, g): g = 2, 4, 8 on int4 use the column kernel; every other pair
 # the 16-query-head tile kernel (g = 3: one partial tile, 20 and 24: a full and
 # a partial tile, 32: two tiles, 48: three)
 GROUPS = [("int4", 2), ("int4", 4), ("int4", 3), ("int4", 8), ("int4", 16), ("int4", 20), ("int4", 32),
