@@ -478,7 +478,7 @@ struct ConsumerGqa {
     static constexpr bool kAllHeads = G == 8;  // every B column a head of its own
     static constexpr int kScores = 8;
     static constexpr int kPf = 4;
-    int rows;  // (unused: G query rows)
+    int rows;  // the group's g <= G query heads: columns of heads past it carry zero queries
     uint32_t qb[8][2];  // q of head hq(grp) as the B operand, the odd elements scaled by kQOdd
     float acc[8][4];    // PV over the widened codes (SubMagic): raw sums
     float m_run[2];
@@ -504,12 +504,13 @@ struct ConsumerGqa {
     {
         const int g = lane >> 2, t = lane & 3;
         const int head = kAllHeads ? g : (((g >> 2) << 1) | (g & 1)) % G;  // column g of B
+        const bool live = head < rows;  // the stage holds rows 0 .. rows - 1 of the buffer's G
         const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + head * kHeadDim + 32 * t);
         const __half2 odd_scale = __float2half2_rn(kQOdd);
         float se = 0.0f, so = 0.0f;
 #pragma unroll
         for (int m = 0; m < 4; m++) {
-            const uint4 v = q4[m];
+            const uint4 v = live ? q4[m] : make_uint4(0u, 0u, 0u, 0u);
             const uint32_t e04 = __byte_perm(v.x, v.z, 0x5410), e15 = __byte_perm(v.x, v.z, 0x7632);
             const uint32_t e26 = __byte_perm(v.y, v.w, 0x5410), e37 = __byte_perm(v.y, v.w, 0x7632);
             const __half2 o15 = __hmul2(*reinterpret_cast<const __half2 *>(&e15), odd_scale);
@@ -683,8 +684,8 @@ struct ConsumerGqa {
     }
 
 
-    // the group's output rows (orow: G rows) or partial slots (part: G
-    // partials of kPartialStride floats).  G = 2, 4: the two parts of a head are
+    // the group's output rows (orow: its `rows` rows) or partial slots (part:
+    // G partials of kPartialStride floats).  G = 2, 4: the two parts of a head are
     // in lanes t and t ^ 1; lanes with even t, t >> 1 < G / 2, write heads
     // 2 (t >> 1) + c.  G = 8: every lane writes its heads 2t + c.
     __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
@@ -713,6 +714,7 @@ struct ConsumerGqa {
 #pragma unroll
         for (int c = 0; c < 2; c++) {
             const int head = kAllHeads ? 2 * t + c : 2 * (t >> 1) + c;
+            if (orow && head >= rows) continue;  // a column past the group (its partial slot is written)
 #pragma unroll
             for (int R = 0; R < 2; R++) {
                 float v[8];
@@ -1454,12 +1456,13 @@ __device__ __noinline__ void merge_pieces(const float *partials, int64_t slot_fl
 // G heads are issued together, so a merge of cnt pieces takes about cnt /
 // kBatch round trips to L2 instead of G times as many (kBatch = 8 / G keeps
 // the call within the kernel's register budget).  A slot holds kSlotHeads
-// heads; this call merges G of them from head0 on (a group of 8 is merged as
-// two calls of 4: one call of 8 heads would not fit beside the streaming
-// loop's live registers).
+// heads; this call merges G of them from head0 on and writes the first nheads
+// (a group of g < G heads leaves slots of heads that do not exist; a group of
+// 8 is merged as two calls of 4: one call of 8 heads would not fit beside the
+// streaming loop's live registers).
 template <int kBatch, int G, int kSlotHeads = G>
 __device__ __noinline__ void merge_group(const float *partials, int64_t gf, int cnt, int first_slot,
-                                         uint16_t *out_rows, int lane, int head0 = 0)
+                                         uint16_t *out_rows, int lane, int head0, int nheads)
 {
     constexpr int64_t kSlot = (int64_t)kSlotHeads * kPartialStride;
     const float *pbase = partials + gf * 2 * kSlot + (int64_t)head0 * kPartialStride;
@@ -1529,6 +1532,7 @@ __device__ __noinline__ void merge_group(const float *partials, int64_t gf, int 
     }
 #pragma unroll
     for (int g = 0; g < G; g++) {
+        if (g >= nheads) break;
         const float inv = 1.0f / L[g];
         const __half2 lo = __floats2half2_rn(o[g].x * inv, o[g].y * inv);
         const __half2 hi = __floats2half2_rn(o[g].z * inv, o[g].w * inv);
@@ -1636,7 +1640,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
     const int H = p.num_heads;                  // cache heads
     const int T = kTiles ? p.tiles : 1;         // unit heads per cache head
     const int HU = H * T;                       // unit heads per sequence
-    const int g_rows = kTiles ? p.group : G;    // query heads per cache head
+    const int g_rows = G > 1 ? p.group : 1;  // query heads per cache head (column kernels: g <= G)
     pdl_launch_dependents();
     // Until pdl_wait below, the previous kernel of the stream may still be
     // running.  Only the sequence lengths and the block table are read before
@@ -1769,9 +1773,9 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
             // consumed those values (mma operands) before the __syncwarp that
             // precedes this issue, so the copy cannot overtake them.
             const uint32_t cb = (uint32_t)nh * kUnitBytes;
-            // the unit head's query rows: G rows of the cache head, or one tile of the group
+            // the unit head's query rows: the g rows of the cache head, or one tile of the group
             const int tile = kTiles ? ih - hc * T : 0;
-            const int qrows = kTiles ? min(kMqRows, g_rows - kMqRows * tile) : G;
+            const int qrows = kTiles ? min(kMqRows, g_rows - kMqRows * tile) : g_rows;
             const uint32_t qbytes = (uint32_t)qrows * kHeadDim * 2;
             const uint32_t bytes = 2 * cb + (new_seg ? qbytes : 0);
             mbar_arrive_expect_tx(&ws.full[s], bytes);
@@ -1827,7 +1831,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
             const int hc = h / T;
             return p.out + (((int64_t)b * H + hc) * g_rows + kMqRows * (h - hc * T)) * kHeadDim;
         } else {
-            return p.out + ((int64_t)b * H + h) * G * kHeadDim;
+            return p.out + ((int64_t)b * H + h) * g_rows * kHeadDim;
         }
     };
     // units c .. c + units - 1 of (b, h), consumed by this warp (piece pi), are done
@@ -1852,11 +1856,11 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
                 if constexpr (G == 1)
                     merge_pieces<F::kMergeBatch>(p.partials, kSlotFloats, 0, pf, (int)(pl - pf + 1), first_slot,
                                                  orow, lane);
-                else if constexpr (G == 8) {
-                    merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 0);
-                    merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 4);
+                else if constexpr (G == 8) {  // g = 5 .. 8: heads 0 .. 3, then 4 .. g - 1
+                    merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 0, 4);
+                    merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 4, g_rows - 4);
                 } else if constexpr (!kTiles)
-                    merge_group<8 / G, G>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane);
+                    merge_group<8 / G, G>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 0, g_rows);
             }
         }
     };
@@ -1870,6 +1874,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
         seg_c = m.z;
         seg_units = 0;
         if constexpr (kTiles) cs.rows = min(kMqRows, g_rows - kMqRows * (m.y % T));
+        else cs.rows = g_rows;
     };
 
     // chunk 0, unit 0
@@ -2001,7 +2006,10 @@ static int ctas_per_sm()
 static int kernel_group(int fmt, int g)
 {
     if (g == 1) return 1;
-    if (fmt == KVQ_INT4_B64 && (g == 2 || g == 4 || g == 8)) return g;
+    // int4: the column kernels serve every g up to their width (columns past g carry zero queries)
+    if (fmt == KVQ_INT4_B64 && g == 2) return 2;
+    if (fmt == KVQ_INT4_B64 && g <= 4) return 4;
+    if (fmt == KVQ_INT4_B64 && g <= 8) return 8;
     return kMqG;
 }
 
@@ -2083,7 +2091,8 @@ size_t decode_workspace_bytes(int fmt, int group)
                   "the counter region holds kMaxDecodeWarpsPerSm warps per SM");
     const size_t counters = decode_counter_bytes();
     if (counters == 0) return 0;
-    const int rows = kernel_group(fmt, group) == kMqG ? kMqRows : group;  // query rows of one partial
+    const int kg = kernel_group(fmt, group);
+    const int rows = kg == kMqG ? kMqRows : kg;  // query rows of one partial: the kernel's, not g
     const size_t partial = (size_t)gw * 2 * rows * kPartialStride * sizeof(float);
     return counters + partial;
 }

@@ -57,11 +57,13 @@ def _check(wl, lens, q_bits, got, g, oc=None):
 
 
 FMTS = {"int4": kvq.KVQ_INT4_B64, "int8": kvq.KVQ_INT8_PAGE, "fp8": kvq.KVQ_FP8_E4M3}
-# (format, g): g = 2, 4, 8 on int4 use the column kernel; every other pair
-# the 16-query-head tile kernel (g = 3: one partial tile, 20 and 24: a full and
-# a partial tile, 32: two tiles, 48: three)
-GROUPS = [("int4", 2), ("int4", 4), ("int4", 3), ("int4", 8), ("int4", 16), ("int4", 20), ("int4", 32),
-          ("int4", 48), ("int8", 2), ("int8", 8), ("int8", 24), ("int8", 32),
+# (format, g): every g <= 8 on int4 uses a column kernel (g = 2; 3, 4 on the
+# 4-column one, whose columns past g carry zero queries; 5 .. 8 on the
+# 8-column one); every other pair the 16-query-head tile kernel (byte formats
+# g = 2, 8: one partial tile, 20 and 24: a full and a partial tile, 32: two
+# tiles, 48: three)
+GROUPS = [("int4", 2), ("int4", 4), ("int4", 3), ("int4", 5), ("int4", 6), ("int4", 7), ("int4", 8), ("int4", 16),
+          ("int4", 20), ("int4", 32), ("int4", 48), ("int8", 2), ("int8", 8), ("int8", 24), ("int8", 32),
           ("fp8", 4), ("fp8", 8), ("fp8", 16), ("fp8", 32)]
 
 
