@@ -213,10 +213,10 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
  *   workspace        >= kvq_decode_workspace_bytes_gqa(...) bytes, zero-filled
  *                    once before first use (as for kvq_decode_attention)
  * g = 1 is kvq_decode_attention.  Every format takes any g from 1 to 1024.
- * Two kernels serve it: for int4 with g <= 8 the multi-head kernel carries
- * the group's heads in the columns of its MMAs (one launch; 4 columns for
- * g = 2 .. 4, 8 for g = 5 .. 8, columns past g carrying zero queries; for
- * g >= 5 the probabilities enter the PV product as fp16); every other
+ * Two kernels serve it: for g <= 8 the multi-head kernel carries the group's
+ * heads in the columns of its MMAs (one launch; int4: 4 columns for g = 2 .. 4,
+ * 8 for g = 5 .. 8; int8 / FP8: 8 columns; columns past g carry zero queries;
+ * except int4 g <= 4 the probabilities enter the PV product as fp16); every other
  * g > 1 runs tiles of up to 16 query heads of one cache head as the rows of
  * the MMAs (a group of more than 16 heads is several tiles, each streaming
  * its cache head's codes), and a second, small launch merges the split

@@ -113,7 +113,9 @@ constexpr size_t dec_smem_bytes()
     using S = DecShape<FMT, G>;
     return S::kWarps * sizeof(WarpSmem<F::kStages, F::kUnitsPerStage * kUnitBytes, S::kQRows>) + kSeqSmemBytes;
 }
-static_assert(dec_smem_bytes<KVQ_INT4_B64, 8>() <= 227 * 1024, "the G = 8 warps fit one CTA's shared memory");
+static_assert(dec_smem_bytes<KVQ_INT4_B64, 8>() <= 227 * 1024 && dec_smem_bytes<KVQ_INT8_PAGE, 8>() <= 227 * 1024 &&
+                  dec_smem_bytes<KVQ_FP8_E4M3, 8>() <= 227 * 1024,
+              "the G = 8 warps fit one CTA's shared memory");
 
 // the byte formats' exact widening to fp16 pairs, by format (int4: SubMagic below)
 template <int FMT>
@@ -934,6 +936,194 @@ template <>
 struct Consumer<KVQ_FP8_E4M3> : ConsumerMma8<KVQ_FP8_E4M3> {
 };
 
+// int8 and FP8 with grouped query heads, any g <= 8: the 8 MMA columns carry
+// the group's heads (column c = head c; columns past g load zero queries), so
+// one pass over the codes serves the group.  QK and the V operand are those of
+// ConsumerMma8; lane (grp, t) receives the scores of tokens grp, grp + 8 for
+// the heads of columns 2t, 2t + 1 (its two slots), and PV column c holds
+// RN16(x) of head c (a single fp16 weight, as in the tile kernel: no column is
+// left for the remainder), so the lane's accumulators are its slot heads and a
+// running-max rescale stays local.  The weights of column grp_d come from lane
+// 4 * token + (grp_d >> 1), slot grp_d & 1.
+template <int FMT>
+struct ConsumerMma8Gqa {
+    static constexpr int kScores = 4;
+    static constexpr int kPf = 2;
+    int rows;  // the group's g <= 8 query heads
+    uint32_t qb[8][2];
+    float acc[8][4];
+    float m_run[2];
+    float l_lane[2];
+
+    __device__ __forceinline__ void reset()
+    {
+        m_run[0] = m_run[1] = -INFINITY;
+        l_lane[0] = l_lane[1] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) acc[i][j] = 0.0f;
+    }
+
+    // qs: the stage's query rows (rows 0 .. g - 1 of a buffer of 8); column g of B = head g
+    __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
+    {
+        const int g = lane >> 2;
+        const bool live = g < rows;
+        const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + g * kHeadDim + 32 * (lane & 3));
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const uint4 v = live ? q4[u] : make_uint4(0u, 0u, 0u, 0u);  // elements 32t + 8u .. +7 as pairs
+            qb[2 * u][0] = v.x;
+            qb[2 * u][1] = v.y;
+            qb[2 * u + 1][0] = v.z;
+            qb[2 * u + 1][1] = v.w;
+        }
+    }
+
+    // raw dot products: sc[2 r + c] = token grp + 8 r, head slot c (column 2t + c)
+    __device__ __forceinline__ void qk(const uint8_t *ks, int lane, float sc[4]) const
+    {
+        const int g = lane >> 2, t = lane & 3;
+        float c[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; m++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) c[m][e] = 0.0f;
+        const uint4 *ra = reinterpret_cast<const uint4 *>(ks + g * 128 + 32 * t);
+        const uint4 *rb = reinterpret_cast<const uint4 *>(ks + (g + 8) * 128 + 32 * t);
+        const uint4 a0 = ra[0], a1 = ra[1], b0 = rb[0], b1 = rb[1];
+        const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int m = 0; m < 8; m++) {
+            uint32_t al, ah, bl, bh;
+            ConsumerMma8<FMT>::widen2(wa[m], al, ah);
+            ConsumerMma8<FMT>::widen2(wb[m], bl, bh);
+            mma16816(c[m & 3], al, bl, ah, bh, qb[m][0], qb[m][1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; e++) sc[e] = (c[0][e] + c[1][e]) + (c[2][e] + c[3][e]);
+    }
+
+    // online softmax per head slot; px[c] = {RN16(x(grp)), RN16(x(grp + 8))} of slot c, x = p * sv
+    __device__ __forceinline__ void softmax(const float sc[4], int ntok, float fac, float sv, int lane,
+                                            uint32_t px[2])
+    {
+        const int g = lane >> 2;
+        float s[4];
+        upk2(mul2(pk2(sc[0], sc[1]), pk2(fac, fac)), s[0], s[1]);
+        upk2(mul2(pk2(sc[2], sc[3]), pk2(fac, fac)), s[2], s[3]);
+        if (g >= ntok) s[0] = s[1] = -INFINITY;
+        if (g + 8 >= ntok) s[2] = s[3] = -INFINITY;
+        const float lm0 = fmaxf(s[0], s[2]), lm1 = fmaxf(s[1], s[3]);
+        if (__any_sync(kFull, lm0 > m_run[0] || lm1 > m_run[1])) {  // a running maximum moves: rescale
+#pragma unroll
+            for (int c = 0; c < 2; c++) {
+                float mu = c ? lm1 : lm0;  // max over the 8 lanes of this t (the unit's 16 tokens)
+                mu = fmaxf(mu, __shfl_xor_sync(kFull, mu, 4));
+                mu = fmaxf(mu, __shfl_xor_sync(kFull, mu, 8));
+                mu = fmaxf(mu, __shfl_xor_sync(kFull, mu, 16));
+                mu = fmaxf(mu, m_run[c]);
+                const float alpha = ex2_approx(m_run[c] - mu);
+                l_lane[c] *= alpha;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    acc[i][c] *= alpha;
+                    acc[i][2 + c] *= alpha;
+                }
+                m_run[c] = mu;
+            }
+        }
+        const uint64_t vv = pk2(sv, sv);
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+            const float p0 = ex2_approx(s[c] - m_run[c]), p1 = ex2_approx(s[2 + c] - m_run[c]);
+            l_lane[c] += p0 + p1;
+            float x0, x1;
+            upk2(mul2(pk2(p0, p1), vv), x0, x1);
+            px[c] = f16x2_rn(x0, x1);
+        }
+    }
+
+    __device__ __forceinline__ void pv(const uint8_t *vs, const uint32_t px[2], int lane)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        // column g of B: head g = slot g & 1 of lanes 4 token + (g >> 1); tokens 2t, 2t + 8 from
+        // lane (2t, .), 2t + 1, 2t + 9 from lane (2t + 1, .)
+        const int src = 8 * t + (g >> 1);
+        const bool slot1 = g & 1;
+        const uint32_t a0 = __shfl_sync(kFull, px[0], src), a1 = __shfl_sync(kFull, px[1], src);
+        const uint32_t c0 = __shfl_sync(kFull, px[0], src + 4), c1 = __shfl_sync(kFull, px[1], src + 4);
+        const uint32_t ua = slot1 ? a1 : a0, ub = slot1 ? c1 : c0;
+        const uint32_t b0 = __byte_perm(ua, ub, 0x5410);  // tokens 2t, 2t + 1
+        const uint32_t b1 = __byte_perm(ua, ub, 0x7632);  // tokens 2t + 8, 2t + 9
+        const uint4 v0 = *reinterpret_cast<const uint4 *>(vs + (2 * t) * 128 + 16 * g);
+        const uint4 v1 = *reinterpret_cast<const uint4 *>(vs + (2 * t + 1) * 128 + 16 * g);
+        const uint4 v8 = *reinterpret_cast<const uint4 *>(vs + (2 * t + 8) * 128 + 16 * g);
+        const uint4 v9 = *reinterpret_cast<const uint4 *>(vs + (2 * t + 9) * 128 + 16 * g);
+        const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+        const uint32_t w8[4] = {v8.x, v8.y, v8.z, v8.w}, w9[4] = {v9.x, v9.y, v9.z, v9.w};
+#pragma unroll
+        for (int R = 0; R < 8; R++) {
+            // bytes 2R, 2R + 1 (elements 16g + 2R, + 1) of two tokens: [x.2R, y.2R, x.2R+1, y.2R+1]
+            const uint32_t sel = (R & 1) ? 0x7362u : 0x5140u;
+            const uint32_t p01 = __byte_perm(w0[R >> 1], w1[R >> 1], sel);
+            const uint32_t p89 = __byte_perm(w8[R >> 1], w9[R >> 1], sel);
+            uint32_t e0, e1, e2, e3;
+            ConsumerMma8<FMT>::widen2(p01, e0, e1);
+            ConsumerMma8<FMT>::widen2(p89, e2, e3);
+            mma16816(acc[R], e0, e1, e2, e3, b0, b1);
+        }
+    }
+
+    // the group's output rows (orow: its `rows` rows) or partial slots (part: 8
+    // partials of kPartialStride floats); lane (grp, t) holds elements 16 grp ..
+    // 16 grp + 15 of the heads of columns 2t, 2t + 1 (tile R: row grp = element
+    // 16 grp + 2R, row grp + 8 = 16 grp + 2R + 1)
+    __device__ __forceinline__ void finish(int lane, uint16_t *orow, float *part)
+    {
+        const int g = lane >> 2, t = lane & 3;
+        float l[2];
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+            float v = l_lane[c];
+            v += __shfl_xor_sync(kFull, v, 4);
+            v += __shfl_xor_sync(kFull, v, 8);
+            v += __shfl_xor_sync(kFull, v, 16);
+            l[c] = v;
+        }
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+            const int head = 2 * t + c;
+            if (orow && head >= rows) continue;  // a column past the group (its partial slot is written)
+            float v[16];
+#pragma unroll
+            for (int R = 0; R < 8; R++) {
+                v[2 * R] = acc[R][c];
+                v[2 * R + 1] = acc[R][2 + c];
+            }
+            if (orow) {
+                const float inv = 1.0f / l[c];
+                uint32_t hw[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) hw[i] = h2_bits(__floats2half2_rn(v[2 * i] * inv, v[2 * i + 1] * inv));
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + head * kHeadDim + 16 * g);
+                dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+            } else {
+                float4 *d4 = reinterpret_cast<float4 *>(part + head * kPartialStride + 4 + 16 * g);
+#pragma unroll
+                for (int i = 0; i < 4; i++) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                if (g == 0) {
+                    part[head * kPartialStride] = m_run[c];
+                    part[head * kPartialStride + 1] = l[c];
+                }
+            }
+        }
+    }
+};
+
 // ---------------------------------------------------------------------------
 // Grouped query heads as the rows of the MMA: a tile of up to kMqRows query
 // heads that share one cache head (GQA with a large group, or MQA -- the
@@ -1545,6 +1735,14 @@ template <int FMT, int G>
 struct ConsumerFor {
     using type = ConsumerGqa<G>;
 };
+template <>
+struct ConsumerFor<KVQ_INT8_PAGE, 8> {
+    using type = ConsumerMma8Gqa<KVQ_INT8_PAGE>;
+};
+template <>
+struct ConsumerFor<KVQ_FP8_E4M3, 8> {
+    using type = ConsumerMma8Gqa<KVQ_FP8_E4M3>;
+};
 template <int FMT>
 struct ConsumerFor<FMT, 1> {
     using type = Consumer<FMT>;
@@ -1605,8 +1803,8 @@ __device__ __forceinline__ void decode_prologue(const DecodeParams &p, int HU, i
     __syncthreads();
 }
 
-// G: query heads per cache head (1: multi-head attention; 2, 4: int4 grouped
-// heads in spare MMA columns; kMqG: tiles of up to 16 query heads of any group
+// G: query heads per cache head (1: multi-head attention; 2, 4, 8: grouped
+// heads in the MMA columns, any g <= G; kMqG: tiles of up to 16 query heads of any group
 // size p.group, p.tiles tiles per cache head, each tile a unit head of its own).
 // kHook: the instantiation launched while the test hook of kvq_testing.h is
 // set -- its waits take their limit from p.wait_limit_ns and the grid's first
@@ -1856,9 +2054,12 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
                 if constexpr (G == 1)
                     merge_pieces<F::kMergeBatch>(p.partials, kSlotFloats, 0, pf, (int)(pl - pf + 1), first_slot,
                                                  orow, lane);
-                else if constexpr (G == 8) {  // g = 5 .. 8: heads 0 .. 3, then 4 .. g - 1
-                    merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 0, 4);
-                    merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 4, g_rows - 4);
+                else if constexpr (G == 8) {  // g <= 8: heads 0 .. min(g, 4) - 1, then 4 .. g - 1
+                    merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 0,
+                                         min(g_rows, 4));
+                    if (g_rows > 4)
+                        merge_group<2, 4, 8>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 4,
+                                             g_rows - 4);
                 } else if constexpr (!kTiles)
                     merge_group<8 / G, G>(p.partials, pf, (int)(pl - pf + 1), first_slot, orow, lane, 0, g_rows);
             }
@@ -2009,7 +2210,7 @@ static int kernel_group(int fmt, int g)
     // int4: the column kernels serve every g up to their width (columns past g carry zero queries)
     if (fmt == KVQ_INT4_B64 && g == 2) return 2;
     if (fmt == KVQ_INT4_B64 && g <= 4) return 4;
-    if (fmt == KVQ_INT4_B64 && g <= 8) return 8;
+    if (g <= 8) return 8;  // int4: 5 .. 8; int8 / FP8: 2 .. 8
     return kMqG;
 }
 
@@ -2020,12 +2221,12 @@ static int variant_ctas(int kg)
     switch (kg) {
     case 1: return ctas_per_sm<FMT, 1>();
     case kMqG: return ctas_per_sm<FMT, kMqG>();
+    case 8: return ctas_per_sm<FMT, 8>();
     default: break;
     }
     if constexpr (FMT == KVQ_INT4_B64) {
         if (kg == 2) return ctas_per_sm<FMT, 2>();
         if (kg == 4) return ctas_per_sm<FMT, 4>();
-        if (kg == 8) return ctas_per_sm<FMT, 8>();
     }
     return 0;
 }
@@ -2142,10 +2343,10 @@ static cudaError_t launch_variant(const DecodeParams &p0, int kg, int gw, cudaSt
             if (ctas_per_sm<FMT, 4>() < 1) return cudaErrorInvalidDevice;
             return launch_pdl(decode_split_kernel<FMT, 4>, grid, block, dec_smem_bytes<FMT, 4>(), s, p, gw);
         }
-        if (kg == 8) {
-            if (ctas_per_sm<FMT, 8>() < 1) return cudaErrorInvalidDevice;
-            return launch_pdl(decode_split_kernel<FMT, 8>, grid, block, dec_smem_bytes<FMT, 8>(), s, p, gw);
-        }
+    }
+    if (kg == 8) {
+        if (ctas_per_sm<FMT, 8>() < 1) return cudaErrorInvalidDevice;
+        return launch_pdl(decode_split_kernel<FMT, 8>, grid, block, dec_smem_bytes<FMT, 8>(), s, p, gw);
     }
     return cudaErrorInvalidValue;
 }

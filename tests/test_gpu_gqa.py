@@ -57,13 +57,14 @@ def _check(wl, lens, q_bits, got, g, oc=None):
 
 
 FMTS = {"int4": kvq.KVQ_INT4_B64, "int8": kvq.KVQ_INT8_PAGE, "fp8": kvq.KVQ_FP8_E4M3}
-# (format, g): every g <= 8 on int4 uses a column kernel (g = 2; 3, 4 on the
+# (format, g): every g <= 8 uses a column kernel (int4: g = 2; 3, 4 on the
 # 4-column one, whose columns past g carry zero queries; 5 .. 8 on the
-# 8-column one); every other pair the 16-query-head tile kernel (byte formats
-# g = 2, 8: one partial tile, 20 and 24: a full and a partial tile, 32: two
+# 8-column one; int8 / FP8: 2 .. 8 on their 8-column one); every larger g the
+# 16-query-head tile kernel (20 and 24: a full and a partial tile, 32: two
 # tiles, 48: three)
 GROUPS = [("int4", 2), ("int4", 4), ("int4", 3), ("int4", 5), ("int4", 6), ("int4", 7), ("int4", 8), ("int4", 16),
-          ("int4", 20), ("int4", 32), ("int4", 48), ("int8", 2), ("int8", 8), ("int8", 24), ("int8", 32),
+          ("int4", 20), ("int4", 32), ("int4", 48), ("int8", 2), ("int8", 5), ("int8", 8), ("int8", 24), ("int8", 32),
+          ("fp8", 3), ("fp8", 7),
           ("fp8", 4), ("fp8", 8), ("fp8", 16), ("fp8", 32)]
 
 
@@ -173,8 +174,13 @@ def test_grouped_heads_argument_checks(cuda_ok):
     w4 = kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT4_B64, 8, 32)
     assert w1 == kvq.kvq_decode_workspace_bytes(kvq.KVQ_INT4_B64, 8) and 3 * w1 < w4 < 4 * w1
     # tiles of 16 query heads: the partials hold 16 rows whatever the group
+    w16 = kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT8_PAGE, 8, 128)
+    assert w16 > 0 and w16 == kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT8_PAGE, 1, 32)
+    # the 8-column kernels: 8 rows per partial for every g from 2 to 8 (int4: 5 to 8)
     w8 = kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT8_PAGE, 8, 64)
-    assert w8 > 0 and w8 == kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT8_PAGE, 1, 32)
+    assert w8 > 0 and w8 == kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT8_PAGE, 1, 2)
+    assert kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT4_B64, 1, 5) == kvq.kvq_decode_workspace_bytes_gqa(
+        kvq.KVQ_INT4_B64, 2, 16)
     assert kvq.kvq_decode_workspace_bytes_gqa(kvq.KVQ_INT4_B64, 1, 2048) == 0
 
 
