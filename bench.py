@@ -15,8 +15,8 @@ Every other workload of the path runs after it, each with its own roofline,
 under "workloads" in the same JSON line: tiny, llama2-7b-layer, paged-int8,
 prefill-append (quantize GB/s), llama3-8b-layer-gqa, llama2-7b-layer-fp8,
 chunked-prefill (tensor-core attention, TFLOP/s), mqa-32k (one cache head
-serving 32 query heads), llama3-70b-layer-gqa (8 query heads per cache head)
-and the stateless codec (kvq_quantize, GB/s) over the
+serving 32 query heads), llama3-70b-layer-gqa and llama3-70b-layer-gqa-fp8
+(8 query heads per cache head, int4 and FP8) and the stateless codec (kvq_quantize, GB/s) over the
 whole K and V history of the 7B layer (int4, int8, FP8) and of long-context
 (int4).
 
@@ -62,6 +62,7 @@ WORKLOADS = {
     "chunked-prefill": ("prefill", 8),
     "mqa-32k": ("decode", 9),
     "llama3-70b-layer-gqa": ("decode", 10),
+    "llama3-70b-layer-gqa-fp8": ("decode", 11),
     "quantize-7b-layer": ("quantize", 2),
     "quantize-long-context": ("quantize", 3),
     "quantize-7b-layer-int8": ("quantize", 2),

@@ -67,6 +67,9 @@ CONFIGS = {
     # with the 8B layer's batch and context: the same 268 MB of codes per step
     10: dict(name="llama3-70b-layer-gqa", B=32, H=8, Hq=64, D=128, L=8192, fmt=INT4, sigma=1.0,
              outliers=("per_head", 4, 10.0), table="contiguous"),
+    # the same shape over an FP8 E4M3 cache (537 MB of codes per step)
+    11: dict(name="llama3-70b-layer-gqa-fp8", B=32, H=8, Hq=64, D=128, L=8192, fmt=FP8, sigma=1.0,
+             outliers=("per_head", 4, 10.0), table="contiguous"),
 }
 
 

@@ -22,7 +22,8 @@ sequences' histories are on the host at a time.
   mqa-32k              B=64, 1 cache head x 32 query heads, L=32768 int4,
                        permuted pages: decode steps, as timed
   llama3-70b-layer-gqa B=32, 8 cache heads x 8 query heads, L=8192 int4:
-                       decode steps, as timed
+                       decode steps, as timed (and the same over FP8:
+                       llama3-70b-layer-gqa-fp8)
 """
 import concurrent.futures as cf
 import math
@@ -105,10 +106,10 @@ def _verify_all(dw, lens, q_bits=None, out=None):
     return worst
 
 
-@pytest.mark.parametrize("cfg", [2, 6, 7, 9, 10])
+@pytest.mark.parametrize("cfg", [2, 6, 7, 9, 10, 11])
 def test_layer_decode_steps(cuda_ok, cfg):
     """llama2-7b-layer (int4), llama3-8b-layer-gqa, llama2-7b-layer-fp8,
-    mqa-32k, llama3-70b-layer-gqa: three timed-style steps, then every sequence's pages and every
+    mqa-32k, llama3-70b-layer-gqa (int4, FP8): three timed-style steps, then every sequence's pages and every
     (sequence, query head) output against the oracle."""
     wl = W.make_workload(cfg, extra_tokens=64)
     dw = DeviceWorkload(wl)
