@@ -216,11 +216,12 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
  * Two kernels serve it: for g <= 8 the multi-head kernel carries the group's
  * heads in the columns of its MMAs (one launch; int4: 4 columns for g = 2 .. 4,
  * 8 for g = 5 .. 8; int8 / FP8: 8 columns; columns past g carry zero queries;
- * except int4 g <= 4 the probabilities enter the PV product as fp16); every other
- * g > 1 runs tiles of up to 16 query heads of one cache head as the rows of
- * the MMAs (a group of more than 16 heads is several tiles, each streaming
- * its cache head's codes), and a second, small launch merges the split
- * pieces.  In that path the probabilities enter the PV product as fp16.
+ * except int4 g <= 4 the probabilities enter the PV product as fp16); every
+ * g > 8 runs tiles of up to 16 query heads of one cache head as the rows of
+ * the MMAs (a group of more than 16 heads is several tiles, which run side by
+ * side so that the cache head's codes come from DRAM once), and a second,
+ * small launch merges the split pieces.  In that path the probabilities enter
+ * the PV product as fp16.
  * num_q_heads not a multiple of cache->num_heads returns KVQ_ERR_INVALID_ARG;
  * g > 1024, or a problem whose work units overflow 32 bits (at most 512
  * sequences x unit heads x 4 units per page), KVQ_ERR_UNSUPPORTED.  Other
