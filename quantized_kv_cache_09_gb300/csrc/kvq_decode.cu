@@ -2359,9 +2359,20 @@ cudaError_t launch_decode(int fmt, const DecodeParams &p, cudaStream_t s)
     static_assert(DecFmt<KVQ_INT4_B64>::kWarps == DecFmt<KVQ_INT8_PAGE>::kWarps &&
                   DecFmt<KVQ_FP8_E4M3>::kWarps == DecFmt<KVQ_INT8_PAGE>::kWarps, "one CTA size");
     const int kg = kernel_group(fmt, p.group);
-    if (fmt == KVQ_INT4_B64) return launch_variant<KVQ_INT4_B64>(p, kg, gw, s);
-    if (fmt == KVQ_FP8_E4M3) return launch_variant<KVQ_FP8_E4M3>(p, kg, gw, s);
-    return launch_variant<KVQ_INT8_PAGE>(p, kg, gw, s);
+    // A small problem launches only the CTAs its units can keep busy: every sequence at the
+    // block table's full width bounds the units of a unit head, and the kernel gives each
+    // active warp at least kMinUnitsPerWarp of them (the rest of a full grid would only run
+    // the prologue).  Large problems keep the whole persistent grid.
+    const int wpc = variant_warps(fmt, kg);
+    const int64_t tiles = kg == kMqG ? (p.group + kMqRows - 1) / kMqRows : 1;
+    const int64_t upp = fmt == KVQ_INT4_B64 ? DecFmt<KVQ_INT4_B64>::kUnitsPerPage : DecFmt<KVQ_INT8_PAGE>::kUnitsPerPage;
+    const int64_t units_max = (int64_t)p.num_seqs * p.num_heads * p.max_blocks * upp;
+    const int64_t need = tiles * ((units_max + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);
+    int gwl = gw;
+    if (need < gw) gwl = (int)(need < wpc ? wpc : (need + wpc - 1) / wpc * wpc);
+    if (fmt == KVQ_INT4_B64) return launch_variant<KVQ_INT4_B64>(p, kg, gwl, s);
+    if (fmt == KVQ_FP8_E4M3) return launch_variant<KVQ_FP8_E4M3>(p, kg, gwl, s);
+    return launch_variant<KVQ_INT8_PAGE>(p, kg, gwl, s);
 }
 
 }  // namespace kvq
