@@ -41,3 +41,21 @@ def test_reference_arm_of_a_quantize_workload():
     rate, cores, desc, unit = bench.oracle_rate("quantize-7b-layer-int8", 0.3, 0)
     assert unit == "GB/s" and rate > 0 and cores >= 1
     assert "int8" in desc and "quantize-7b-layer-int8" in desc
+
+
+def test_decode_workloads_bytes_per_unit():
+    """The decode rooflines' numerator: 128 B per token-head for int4 (64 B of K
+    codes and 64 of V) and 256 B for int8 / FP8, 8 B per (page, cache head) for
+    its two scales, and 256 B each for a query row read and an output row
+    written -- per decode call over the lengths the benchmark decodes at."""
+    per_tok = {"int4-b64": 128, "int8-page": 256, "fp8-e4m3-page": 256}
+    for name, (kind, _) in bench.WORKLOADS.items():
+        if kind != "decode":
+            continue
+        cfg = bench.workload_config(name)
+        wl = bench._make(name, 0)
+        lens = wl.lens + 1  # one appended token per sequence, as a decode step
+        pages = ((lens + 63) // 64).sum()
+        expect = (int(lens.sum()) * wl.H * per_tok[cfg["format"]] + int(pages) * wl.H * 8
+                  + 2 * wl.B * wl.Hq * wl.D * 2)
+        assert wl.decode_bytes(lens) == expect, name
