@@ -102,9 +102,11 @@ constexpr int kMqRows = 16;
 // fewer warps fit in shared memory (and each has more registers)
 template <int FMT, int G>
 struct DecShape {
-    // G = 8: the 8 query rows a stage carries leave room for 11 warps (12 need 247 KB)
-    static constexpr int kWarps = G == kMqG ? 8 : G == 8 ? 11 : DecFmt<FMT>::kWarps;
-    static constexpr int kQRows = G == kMqG ? kMqRows : G;
+    // G = 8: the stages carry no query rows (8 rows a stage would leave room for 11 warps
+    // only: 12 need 247 KB); the consumer reads a segment's rows from global memory
+    static constexpr bool kQGlobal = G == 8;
+    static constexpr int kWarps = G == kMqG ? 8 : DecFmt<FMT>::kWarps;
+    static constexpr int kQRows = G == kMqG ? kMqRows : kQGlobal ? 1 : G;  // (1: an unused placeholder)
 };
 template <int FMT, int G>
 constexpr size_t dec_smem_bytes()
@@ -114,8 +116,8 @@ constexpr size_t dec_smem_bytes()
     return S::kWarps * sizeof(WarpSmem<F::kStages, F::kUnitsPerStage * kUnitBytes, S::kQRows>) + kSeqSmemBytes;
 }
 static_assert(dec_smem_bytes<KVQ_INT4_B64, 8>() <= 227 * 1024 && dec_smem_bytes<KVQ_INT8_PAGE, 8>() <= 227 * 1024 &&
-                  dec_smem_bytes<KVQ_FP8_E4M3, 8>() <= 227 * 1024,
-              "the G = 8 warps fit one CTA's shared memory");
+                  dec_smem_bytes<KVQ_FP8_E4M3, 8>() <= 227 * 1024 && dec_smem_bytes<KVQ_INT4_B64, 4>() <= 227 * 1024,
+              "the warps fit one CTA's shared memory");
 
 // the byte formats' exact widening to fp16 pairs, by format (int4: SubMagic below)
 template <int FMT>
@@ -1820,8 +1822,10 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
     constexpr int kStages = F::kStages;
     constexpr int UPS = F::kUnitsPerStage;
     constexpr int kQRows = DecShape<FMT, G>::kQRows;
+    constexpr bool kQGlobal = DecShape<FMT, G>::kQGlobal;
     using WS = WarpSmem<kStages, UPS * kUnitBytes, kQRows>;
-    constexpr int64_t kSlotFloats = (int64_t)kQRows * kPartialStride;  // one piece's partials
+    // one piece's partials: a row per query head of the unit head (G, or a tile's 16)
+    constexpr int64_t kSlotFloats = (int64_t)(kTiles ? kMqRows : G) * kPartialStride;
     constexpr int UT = F::kUnitTok;
     constexpr int UPP = F::kUnitsPerPage;
     constexpr int RB = F::kRowBytes;
@@ -1973,7 +1977,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
             const uint32_t cb = (uint32_t)nh * kUnitBytes;
             // the unit head's query rows: the g rows of the cache head, or one tile of the group
             const int tile = kTiles ? ih - hc * T : 0;
-            const int qrows = kTiles ? min(kMqRows, g_rows - kMqRows * tile) : g_rows;
+            const int qrows = kTiles ? min(kMqRows, g_rows - kMqRows * tile) : kQGlobal ? 0 : g_rows;
             const uint32_t qbytes = (uint32_t)qrows * kHeadDim * 2;
             const uint32_t bytes = 2 * cb + (new_seg ? qbytes : 0);
             mbar_arrive_expect_tx(&ws.full[s], bytes);
@@ -1981,7 +1985,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
                 const size_t off = ((size_t)pg * H + hc) * kPageBytes + (size_t)(ic % UPP) * kUnitBytes;
                 bulk_copy_g2s(ws.k[s], p.k_codes + off, cb, &ws.full[s]);
                 bulk_copy_g2s(ws.v[s], p.v_codes + off, cb, &ws.full[s]);
-                if (new_seg)
+                if (new_seg && qbytes)
                     bulk_copy_g2s(ws.q[s], p.q + (((size_t)ib * H + hc) * g_rows + kMqRows * tile) * kHeadDim, qbytes,
                                   &ws.full[s]);
             }
@@ -2087,7 +2091,12 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
     int4 mi = *reinterpret_cast<const int4 *>(&ws.meta[0].b);
     float4 mf = *reinterpret_cast<const float4 *>(&ws.meta[0].sk);
     seg_start(mi);
-    cs.load_q(ws.q[0], lane);
+    // a segment's query rows: from its stage, or (kQGlobal) from global memory
+    auto q_rows = [&](const int4 &m, int stage) -> const uint16_t * {
+        if constexpr (kQGlobal) return p.q + ((int64_t)m.x * H + m.y) * g_rows * kHeadDim;
+        else return ws.q[stage];
+    };
+    cs.load_q(q_rows(mi, 0), lane);
     constexpr int kScores = CS::kScores;  // scores a lane holds per unit
     float sc[kScores];
     uint32_t pf[CS::kPf];
@@ -2120,7 +2129,7 @@ __global__ void __launch_bounds__(DecShape<FMT, G>::kWarps * 32, DecFmt<FMT>::kC
             }
             mi1 = *reinterpret_cast<const int4 *>(&ws.meta[s1].b);
             mf1 = *reinterpret_cast<const float4 *>(&ws.meta[s1].sk);
-            if (__float_as_int(mf1.z)) cs.load_q(ws.q[s1], lane);
+            if (__float_as_int(mf1.z)) cs.load_q(q_rows(mi1, s1), lane);
             cs.qk(ws.k[s1], lane, sc1);  // the next chunk's first unit: independent of the pv below
         }
         cs.pv(ws.v[s] + (nh - 1) * kUnitBytes, pf, lane);  // the chunk's last unit
