@@ -59,3 +59,26 @@ def test_decode_workloads_bytes_per_unit():
         expect = (int(lens.sum()) * wl.H * per_tok[cfg["format"]] + int(pages) * wl.H * 8
                   + 2 * wl.B * wl.Hq * wl.D * 2)
         assert wl.decode_bytes(lens) == expect, name
+
+
+def test_reference_arm_line_keeps_the_contract():
+    """`bench.py --impl reference` (the oracle on the host's cores) prints one
+    JSON line with the keys a bench line carries, `impl: reference`, a
+    cpu_baseline describing the run and an e2e with no host copies."""
+    import json
+    import subprocess
+
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "llama2-7b-layer", "--cpu-seconds", "0.5", "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [x for x in out.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline",
+              "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["value"] > 0
+    assert d["config"] == bench.workload_config("llama2-7b-layer")
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
