@@ -13,7 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _declared_functions(header="kvq.h"):
-    src = open(os.path.join(ROOT, "include", header)).read()
+    with open(os.path.join(ROOT, "include", header)) as fh:
+        src = fh.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(kvq_[a-z_0-9]+)\s*\(", src)))
 
@@ -70,9 +71,11 @@ def test_oracle_and_product_share_no_code():
     """The oracle directory and the CUDA library sources include nothing of each other."""
     csrc = os.path.join(ROOT, "quantized_kv_cache_09_gb300", "csrc")
     for f in os.listdir(csrc):
-        text = open(os.path.join(csrc, f)).read()
+        with open(os.path.join(csrc, f)) as fh:
+            text = fh.read()
         assert "oracle" not in text.lower(), f
     for f in os.listdir(os.path.join(ROOT, "oracle")):
         if f.endswith((".c", ".py")):
-            text = open(os.path.join(ROOT, "oracle", f)).read()
+            with open(os.path.join(ROOT, "oracle", f)) as fh:
+                text = fh.read()
             assert "quantized_kv_cache_09_gb300" not in text and "kvq_synth" not in text, f
