@@ -503,12 +503,12 @@ struct ConsumerGqa {
             for (int j = 0; j < 4; j++) acc[i][j] = 0.0f;
     }
 
-    // qs: the group's G query rows (fp16 [G][128])
+    // qs: the group's query rows (fp16 [g][128]: a stage's buffer, or global memory for G = 8)
     __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
     {
         const int g = lane >> 2, t = lane & 3;
         const int head = kAllHeads ? g : (((g >> 2) << 1) | (g & 1)) % G;  // column g of B
-        const bool live = head < rows;  // the stage holds rows 0 .. rows - 1 of the buffer's G
+        const bool live = head < rows;  // rows 0 .. rows - 1 exist; a head past them reads nothing
         const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + head * kHeadDim + 32 * t);
         const __half2 odd_scale = __float2half2_rn(kQOdd);
         float se = 0.0f, so = 0.0f;
@@ -967,7 +967,7 @@ struct ConsumerMma8Gqa {
             for (int j = 0; j < 4; j++) acc[i][j] = 0.0f;
     }
 
-    // qs: the stage's query rows (rows 0 .. g - 1 of a buffer of 8); column g of B = head g
+    // qs: the segment's g query rows in global memory; column g of B = head g (zeros past the group)
     __device__ __forceinline__ void load_q(const uint16_t *qs, int lane)
     {
         const int g = lane >> 2;
