@@ -166,3 +166,29 @@ def _decode(fmt, row, d):
         return orc.e4m3_to_float(int(row[d]))
     v = int(row[d])
     return v - 256 if v >= 128 else v
+
+
+def test_normalized_error_known_by_construction():
+    """The parity measure itself: for each (sequence, head) the largest
+    |test - ref| over the head elements, divided by that (sequence, head)'s own
+    max|v^|, then the maximum over all of them.  The numbers are chosen so that
+    each plausible mistake gives another answer: the largest absolute error
+    (0.006, head (0, 2)) is not the largest ratio (0.004, head (1, 2), where the
+    test value is below the reference); one global max|v^| instead of the
+    per-head one gives 0.0015; dropping the absolute value gives 0.0015; a
+    zero-valued head with a zero error counts as 0 and one with
+    any error as infinite."""
+    ref = np.zeros((2, 3, 4))
+    test = ref.copy()
+    vmax = np.array([[2.0, 0.0, 4.0], [1.0, 0.0, 0.5]])
+    test[0, 0, 3] = 0.002        # 0.001
+    test[0, 2, 1] = 0.006        # 0.0015
+    test[1, 0, 0] = 0.0015       # 0.0015
+    ref[1, 2, 2] = 0.75
+    test[1, 2, 2] = 0.748        # 0.004
+    assert orc.normalized_error(test, ref, vmax) == pytest.approx(0.004, rel=1e-12)
+    # a zero-valued head must match exactly
+    test[0, 1, 0] = 1e-300
+    assert orc.normalized_error(test, ref, vmax) == np.inf
+    # shapes with no elements have no error
+    assert orc.normalized_error(np.zeros((0, 3, 4)), np.zeros((0, 3, 4)), np.zeros((0, 3))) == 0.0
