@@ -235,7 +235,7 @@ def test_matches_independent_numpy_softmax():
 
 
 @pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8, orc.FP8])
-@pytest.mark.parametrize("g", [2, 4, 8, 32])
+@pytest.mark.parametrize("g", [2, 3, 4, 8, 32])
 def test_grouped_heads_equal_multi_head_over_repeated_heads(fmt, g):
     """Grouped query heads (Hq = g * Hkv, query head i reads cache head i // g)
     give exactly the multi-head result over a cache whose head i is a copy of
