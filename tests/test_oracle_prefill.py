@@ -57,10 +57,11 @@ def _dequant(fmt, codes, scales, bt_row, L, h):
 
 
 @pytest.mark.parametrize("fmt", [orc.INT4, orc.INT8, orc.FP8])
-def test_matches_numpy_causal_softmax(fmt):
-    B, H, g = 2, 2, 2
-    L = [70, 131]
-    n = [70, 5]   # a whole sequence as one chunk, and a short chunk after history
+@pytest.mark.parametrize("g", [1, 2, 3])
+def test_matches_numpy_causal_softmax(fmt, g):
+    B, H = 3, 2
+    L = [70, 131, 64]
+    n = [70, 5, 0]   # a whole sequence as one chunk, a short chunk after history, no new tokens
     kc, vc, ks, vs, bt = _cache(fmt, B, H, max(L), 3)
     cu = np.concatenate([[0], np.cumsum(n)])
     rng = np.random.default_rng(4)
@@ -106,3 +107,15 @@ def test_causal_mask_reaches_only_later_queries():
     pos = 180 - 80 + np.arange(80)
     changed = np.any(a[:, 0] != b[:, 0], axis=1)
     assert not changed[pos < 150].any() and changed[pos >= 150].all()
+
+
+def test_empty_and_oversized_chunks():
+    """No new tokens anywhere gives an empty result; a chunk longer than its
+    sequence (queries before position 0) is rejected."""
+    kc, vc, ks, vs, bt = _cache(orc.INT4, 2, 1, 64, 11)
+    q = np.zeros((0, 1, D), np.uint16)
+    out = orc.prefill_attention(orc.INT4, kc, vc, ks, vs, bt, [10, 20], [0, 0, 0], q, SM)
+    assert out.shape == (0, 1, D)
+    q = np.zeros((11, 1, D), np.uint16)
+    with pytest.raises(ValueError):
+        orc.prefill_attention(orc.INT4, kc, vc, ks, vs, bt, [10, 20], [0, 11, 11], q, SM)
