@@ -248,7 +248,7 @@ def _make(name, seed, prefill_seqs=64):
     if kind == "decode":
         return W.make_workload(cfg, seed=seed, extra_tokens=64)
     if kind == "append":
-        c = W.CONFIGS[5]
+        c = W.RECIPES[5]
         return W.Workload(prefill_seqs, c["H"], c["D"], [c["L"]] * prefill_seqs, c["fmt"], c["sigma"], None,
                           "permuted", seed, 0, c["name"])
     wl = W.make_workload(cfg, seed=seed)

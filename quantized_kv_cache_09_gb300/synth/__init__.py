@@ -135,7 +135,7 @@ def synth_sample_heads(B, H, n, seed):
     return [(int(b), int(h)) for b, h in zip(bs, hs)]
 
 
-from .workloads import Workload, make_workload, CONFIGS  # noqa: E402
+from .workloads import Workload, make_workload, RECIPES  # noqa: E402
 
 __all__ = ["fill_f16_host", "fill_f16_device", "outliers_per_head", "outliers_bernoulli", "permutation",
-           "uniform_int", "stream_id", "synth_sample_heads", "Workload", "make_workload", "CONFIGS", "f32_to_f16_bits"]
+           "uniform_int", "stream_id", "synth_sample_heads", "Workload", "make_workload", "RECIPES", "f32_to_f16_bits"]

@@ -39,7 +39,7 @@ INT8 = 1
 FP8 = 2
 PAGE = 64
 
-CONFIGS = {
+RECIPES = {
     1: dict(name="tiny", B=2, H=4, D=128, L=256, fmt=INT4, sigma=1.0, outliers=None, table="contiguous"),
     2: dict(name="llama2-7b-layer", B=8, H=32, D=128, L=8192, fmt=INT4, sigma=1.0,
             outliers=("per_head", 4, 10.0), table="contiguous"),
@@ -49,7 +49,7 @@ CONFIGS = {
             outliers=None, table="permuted"),
     5: dict(name="prefill-append", B=64, H=32, D=128, L=4096, fmt=INT4, sigma=1.5, outliers=None,
             table="permuted"),
-    # grouped query heads (beyond the five configurations above): 32 query heads
+    # grouped query heads: 32 query heads
     # over 8 cache heads, the Llama-3-8B attention shape
     6: dict(name="llama3-8b-layer-gqa", B=32, H=8, Hq=32, D=128, L=8192, fmt=INT4, sigma=1.0,
             outliers=("per_head", 4, 10.0), table="contiguous"),
@@ -211,7 +211,7 @@ class Workload:
 
 
 def make_workload(cfg, seed=0, extra_tokens=0):
-    c = CONFIGS[cfg]
+    c = RECIPES[cfg]
     B = c["B"]
     if isinstance(c["L"], tuple):
         _, lo, hi = c["L"]
