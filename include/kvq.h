@@ -223,9 +223,11 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const uint16_t *q, const
  * small launch merges the split pieces.  In that path the probabilities enter
  * the PV product as fp16.
  * num_q_heads not a multiple of cache->num_heads returns KVQ_ERR_INVALID_ARG;
- * g > 1024, or a problem whose work units overflow 32 bits (at most 512
- * sequences x unit heads x 4 units per page), KVQ_ERR_UNSUPPORTED.  Other
- * errors as for kvq_decode_attention.
+ * g > 1024, max_blocks_per_seq > 2^22 (the split counts the units of one
+ * (sequence, head) in 24 bits; this bound holds for kvq_decode_attention too),
+ * or a problem whose work units overflow 32 bits (at most 512 sequences x
+ * unit heads x 4 units per page), KVQ_ERR_UNSUPPORTED.  Other errors as for
+ * kvq_decode_attention.
  */
 size_t kvq_decode_workspace_bytes_gqa(kvq_format fmt, int32_t num_kv_heads, int32_t num_q_heads,
                                       int32_t head_dim);
@@ -291,7 +293,8 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const uint16_t *
  * A sequence that breaks a bound is skipped and KVQ_FLAG_BAD_LENGTH set; a
  * block-table entry out of range sets KVQ_FLAG_BAD_PAGE (page 0 is read
  * instead); a workspace that was not zero-filled sets KVQ_FLAG_BAD_WORKSPACE.
- * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE (too
+ * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED (also num_seqs or
+ * num_q_heads above 65535, or 2^30 or more units), KVQ_ERR_WORKSPACE (too
  * small or misaligned), KVQ_ERR_CUDA.
  */
 kvq_status kvq_prefill_attention(const kvq_cache *cache, const uint16_t *q, int32_t num_q_heads,
